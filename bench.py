@@ -1,0 +1,427 @@
+"""Benchmark of the paged attention hot path on one GB300 (or N replicas).
+
+A step is one decode round of the batched-decode workload (8 streams x 8,192
+positions, 32 query / 8 KV heads, head_dim 128, bf16 KV; streams 0-3 on slabs,
+4-7 on 256-position pages of a permuted 512-page pool): write each stream's
+new K/V row (tfpa_write_kv), then split-K partials and their merge
+(tfpa_decode).  value = algorithmic KV bytes (+ Q and O) per step / step time,
+in GB/s.  The prompt-chunk workload (28,672-position paged prefix plus a
+4,096-row causal chunk) is timed beside it and reported in TFLOP/s of its
+unmasked (row, key) pairs.
+
+Inputs are 268 MB of KV per step, above the 129 MB L2, so no flush is needed
+between decode steps; the prompt-chunk timing flushes L2 between launches.
+
+Launch: ``python bench.py [--gpus N --steps K --warmup W] [--impl reference]``;
+for N > 1 under torchrun every rank runs its own replica (no collective on the
+data path) and rank 0 prints one JSON line with the max time over ranks.
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode KV GB/s (% HBM peak); prompt-chunk attn TFLOP/s (% TC peak)"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._proc = None
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self._proc = None
+        return self
+
+    def _read(self):
+        for line in self._proc.stdout:
+            self.samples.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self._proc:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except Exception:
+                self._proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4)
+                          if len(s) > 3 + i and s[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.samples)}
+
+
+# --------------------------------------------------------------------- set-up
+def device_case(w, torch, B):
+    """A workload's cache on the GPU with device-generated N(0,1) values.
+
+    The bench measures speed; parity is established by the tests.  Every
+    stream's K/V goes through tfpa_write_kv, as in the tests."""
+    dev = "cuda"
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    fp8 = w.kv_dtype == "fp8"
+
+    def randn(*shape):
+        return torch.randn(*shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+    store = torch.uint8 if fp8 else torch.bfloat16
+    kp = torch.empty(w.num_pages, w.hkv, 256, 128, dtype=store, device=dev)
+    vp = torch.empty_like(kp)
+    if fp8:
+        kp.random_(0, 127, generator=g)
+        vp.random_(0, 127, generator=g)
+    else:
+        kp.copy_(randn(*kp.shape))
+        vp.copy_(randn(*vp.shape))
+    ks = vs = None
+    if fp8:   # amax/448 of N(0,1) draws at these sizes
+        ks = torch.full((w.hkv,), 5.6 / 448, dtype=torch.float32, device=dev)
+        vs = ks.clone()
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    cache = B.Cache(w.kv_dtype, w.hq, w.hkv, kp, vp, ks, vs, err, w.num_pages)
+    segs = []
+    for st in w.streams:
+        if st.paged:
+            segs.append(B.Seg(st.seq_len, page_table=torch.from_numpy(st.page_table).to(dev),
+                              page_table_host=st.page_table))
+        else:
+            cap = st.slab_cap
+            segs.append(B.Seg(st.seq_len, k_slab=torch.empty(w.hkv, cap, 128, dtype=store, device=dev),
+                              v_slab=torch.empty(w.hkv, cap, 128, dtype=store, device=dev),
+                              slab_cap=cap))
+    for s, st in enumerate(w.streams):
+        L = st.seq_len
+        for a in range(0, L, 65536):
+            n = min(65536, L - a)
+            B.tfpa_write_kv(cache, segs, randn(n, w.hkv, 128), randn(n, w.hkv, 128),
+                            np.full(n, s, np.int32), np.arange(a, a + n, dtype=np.int32))
+    torch.cuda.synchronize()
+    q = randn(w.rows, w.hq, 128)
+    return cache, segs, q
+
+
+def kv_bytes(w):
+    b = 1 if w.kv_dtype == "fp8" else 2
+    kv = sum(st.seq_len for st in w.streams) * w.hkv * 128 * 2 * b
+    return kv, w.rows * w.hq * 128 * 2 * 2   # KV, Q + O
+
+
+def prefill_flops(w):
+    return 4.0 * 128 * w.hq * float(np.sum(w.row_pos.astype(np.float64) + 1))
+
+
+def barrier(dist, torch):
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(dist, torch, x):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------- oracle
+def cpu_oracle_sample(seconds: float = 12.0):
+    """The oracle on this host's cores, on stream 0 of the batched-decode
+    workload (1 row x 32 heads over 8,192 keys), repeated for ~`seconds`."""
+    from oracle import attention, kvcache
+    from paged_kv_cache_235_gb300 import workloads as wl
+    w = wl.batched_decode()
+    k, v = w.stream_kv_bits(0)
+    L = w.streams[0].seq_len
+    cache = kvcache.Cache("bf16", w.hkv, w.d, None, None)
+    seg = kvcache.Segment(L, k_slab=k, v_slab=v)
+    q = w.q_bits()[:1]
+    n, t0 = 0, time.perf_counter()
+    while True:
+        attention.attend(cache, [seg], q, [0], [L - 1], w.softmax_scale)
+        n += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = (time.perf_counter() - t0) / n
+    bytes_ = L * w.hkv * 128 * 2 * 2
+    return {"value": bytes_ / dt / 1e9, "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle", "calls": n, "s_per_call": dt,
+            "sample": "stream 0 of the batched-decode workload: 1 row x 32 heads over 8,192 "
+                      "bf16 keys (1/8 of a step), float64 NumPy, repeated for ~%ds" % seconds}
+
+
+# --------------------------------------------------------------------- timing
+def time_decode(w, torch, B, steps, warmup, dist):
+    """Device-timed decode steps plus the partial kernel timed on its own."""
+    cache, segs, q = device_case(w, torch, B)
+    sc = B.make_scratch(min(128, w.rows), w.hq)
+    out = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(w.rows, w.hq, dtype=torch.float32, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    newk = torch.randn(len(w.streams), w.hkv, 128, generator=g, device="cuda").to(torch.bfloat16)
+    newv = torch.randn(len(w.streams), w.hkv, 128, generator=g, device="cuda").to(torch.bfloat16)
+    last = np.array([st.seq_len - 1 for st in w.streams], np.int32)
+    sidx = np.arange(len(w.streams), dtype=np.int32)
+
+    def step():
+        B.tfpa_write_kv(cache, segs, newk, newv, sidx, last)
+        B.tfpa_decode(cache, segs, q, w.row_seg, w.row_pos, w.softmax_scale, sc, out, lse)
+
+    for _ in range(warmup):
+        step()
+    barrier(dist, torch)
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        step()
+    e1.record(s)
+    barrier(dist, torch)
+    step_ms = e0.elapsed_time(e1) / steps
+
+    # the dominant kernel alone: decode partial launches, back to back
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    n = max(steps, 10)
+    ev[0].record(s)
+    for _ in range(n):
+        B.tfpa_decode_partial(cache, segs, q, w.row_seg, w.row_pos, w.softmax_scale, sc)
+    ev[1].record(s)
+    torch.cuda.synchronize()
+    partial_ms = ev[0].elapsed_time(ev[1]) / n
+    assert int(cache.err_flag.item()) == 0, "kernel error flag set"
+    return step_ms, partial_ms, (cache, segs, q, sc, out)
+
+
+def time_e2e(w, torch, B, ctx, steps, warmup):
+    """Through the public API with host buffers: per step, copy the step's
+    inputs (q and the new K/V rows) from pinned host memory, run the step and
+    read the output back to the host."""
+    cache, segs, _, sc, out = ctx
+    nst = len(w.streams)
+    hq = torch.randn(w.rows, w.hq, 128).to(torch.bfloat16).pin_memory()
+    hk = torch.randn(nst, w.hkv, 128).to(torch.bfloat16).pin_memory()
+    hv = torch.randn(nst, w.hkv, 128).to(torch.bfloat16).pin_memory()
+    hout = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16).pin_memory()
+    dq = torch.empty_like(hq, device="cuda")
+    dk = torch.empty_like(hk, device="cuda")
+    dv = torch.empty_like(hv, device="cuda")
+    last = np.array([st.seq_len - 1 for st in w.streams], np.int32)
+    sidx = np.arange(nst, dtype=np.int32)
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        B.tfpa_write_kv(cache, segs, dk, dv, sidx, last)
+        B.tfpa_decode(cache, segs, dq, w.row_seg, w.row_pos, w.softmax_scale, sc, out)
+        hout.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = (time.perf_counter() - t0) / steps
+    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
+    return dt, h2d, hout.numel() * 2
+
+
+def time_prefill(w, torch, B, reps):
+    """One launch per rep, L2 flushed between reps, CUDA events around each."""
+    cache, segs, _ = device_case(w, torch, B)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    q = torch.randn(w.rows, w.hq, 128, generator=g, device="cuda").to(torch.bfloat16)
+    out = torch.empty_like(q)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    times = []
+    for i in range(reps + 2):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        B.tfpa_prefill(cache, segs, q, w.row_seg, w.row_pos, w.softmax_scale, out)
+        e1.record(s)
+        torch.cuda.synchronize()
+        if i >= 2:
+            times.append(e0.elapsed_time(e1))
+    return statistics.median(times)
+
+
+# --------------------------------------------------------------------- main
+def reference_arm(args):
+    """The CPU oracle as the reference arm: same metric, config and unit."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        cpu_oracle_sample(seconds=0.0)
+    secs = []
+    base = None
+    for _ in range(args.steps):
+        base = cpu_oracle_sample(seconds=0.0)
+        secs.append(base["s_per_call"] * 8)          # 8 streams make one step
+    from paged_kv_cache_235_gb300 import workloads as wl
+    w = wl.batched_decode()
+    kv, qo = kv_bytes(w)
+    ms = statistics.mean(secs) * 1e3
+    value = (kv + qo) / (ms / 1e3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) rounded to bf16)",
+        "config": {"workload": "batched_decode: 8 streams x 8,192 positions, 32/8 heads, "
+                               "head_dim 128, bf16 KV, streams 0-3 slabs, 4-7 paged",
+                   "sample": "each step runs stream 0 once and counts it 8 times"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": base["sample"]},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-prefill", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+
+    import torch
+    from paged_kv_cache_235_gb300 import binding as B
+    from paged_kv_cache_235_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    B.lib()
+    pk = peaks()
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample()      # before any timed GPU work
+
+    w = wl.batched_decode()
+    kv, qo = kv_bytes(w)
+    with ClockSampler(local) as clk:
+        step_ms, partial_ms, ctx = time_decode(w, torch, B, args.steps, args.warmup, dist)
+    step_ms = max_over_ranks(dist, torch, step_ms)
+    e2e_s, h2d, d2h = time_e2e(w, torch, B, ctx, max(10, args.steps // 2), args.warmup)
+    e2e_s = max_over_ranks(dist, torch, e2e_s)
+    value = world * (kv + qo) / (step_ms / 1e3) / 1e9
+    achieved = (kv + qo) / (partial_ms / 1e3) / 1e9
+    del ctx
+
+    extra = {}
+    w3 = wl.fp8_verify()
+    s3, p3, ctx3 = time_decode(w3, torch, B, max(10, args.steps // 2), args.warmup, None)
+    kv3, qo3 = kv_bytes(w3)
+    extra["fp8_verify"] = {
+        "workload": "8 streams x 65,536 positions, 4 causal verify rows each, fp8 e4m3 KV",
+        "ms_per_call": s3, "kv_gbs": (kv3 + qo3) / (s3 / 1e3) / 1e9,
+        "partial_ms": p3, "partial_gbs": (kv3 + qo3) / (p3 / 1e3) / 1e9,
+        "frac_of_measured_hbm": (kv3 + qo3) / (p3 / 1e3) / 1e9 / pk["hbm_gbs"]}
+    del ctx3
+    if not args.skip_prefill:
+        w4 = wl.prompt_chunk()
+        try:
+            ms4 = time_prefill(w4, torch, B, 5)
+            fl = prefill_flops(w4)
+            extra["prefill"] = {
+                "workload": "28,672-position paged prefix + 4,096-row causal chunk, 32/8 heads",
+                "ms_per_call": ms4, "tflops": fl / (ms4 / 1e3) / 1e12,
+                "frac_of_measured_bf16": fl / (ms4 / 1e3) / 1e12 / pk["bf16_tflops"]}
+        except B.TfpaError as e:
+            extra["prefill"] = {"unavailable": str(e)}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) rounded to bf16; pages from a seeded permutation)",
+        "config": {"workload": "batched_decode: 8 streams x 8,192 positions, 1 row each, "
+                               "32/8 heads, head_dim 128, bf16 KV, streams 0-3 slabs, 4-7 "
+                               "paged in a 512-page pool; step = tfpa_write_kv + tfpa_decode",
+                   "l2": "no flush: 268 MB of KV per step exceeds the 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                     "kernel": "decode_partial_kernel<bf16>", "peak_source": pk["source"],
+                     "partial_ms": partial_ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * (kv + qo) / e2e_s / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        **extra,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

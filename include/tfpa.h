@@ -1,0 +1,170 @@
+/*
+ * tfpa: GQA attention over a paged KV cache, for GB300 (sm_103a).
+ *
+ * Keys and values live in 256-position pages drawn from one shared pool; a
+ * stream reaches its pages through its own page table (TensorFold PR #2011,
+ * "What this changes": every stream takes 256-position pages from the core
+ * pool).  A stream may instead hold a contiguous slab; both are read with one
+ * arithmetic, so a stream's output is the same bytes paged or not, batched or
+ * alone (PR #1373, "What changes"; Issue #1344, "Conclusion").
+ *
+ * Layouts (all row-major, element = bf16 or one e4m3 byte):
+ *   pool  K, V : [num_pages][hkv][256][128]   key j of kv head g of a paged
+ *                stream is pool[PT[j/256]][g][j%256]  (PR #2011, review
+ *                "Is paged output the same as windowed output?": base
+ *                PT[k0/256]*PS + (hk*256 + k0%256)*D)
+ *   slab  K, V : [hkv][slab_cap][128]          key j of kv head g is slab[g][j]
+ *   q, out     : bf16 [rows][hq][128]
+ *   k_rows, v_rows (KV write input): bf16 [rows][hkv][128]
+ *   lse        : float [rows][hq], natural log, nullable
+ * Query head h reads kv head h / (hq/hkv).
+ *
+ * Rows and segments.  A call covers `rows` query rows; row r belongs to
+ * segment row_seg[r] (an index into `segs`) and sits at cache position
+ * row_pos[r]; it attends to keys 0..row_pos[r] of its segment (causal).
+ * Rows of one segment should be contiguous with consecutive positions (a
+ * decode/verify group or a prompt chunk); other orders are accepted and run
+ * as more, smaller groups.
+ *
+ * Memory and ownership.  Every buffer is allocated by the caller.  Pointers
+ * marked DEVICE are device memory of the current device; HOST arrays are read
+ * during the call only and not retained.  The library allocates nothing, keeps
+ * no state between calls except a host-side cache of TMA tensor maps, and never
+ * synchronises the stream: all work is enqueued on `stream`.
+ *
+ * Errors.  Every call returns TFPA_OK (0) or a negative code below and
+ * enqueues nothing on error.  Kernels never trap: a page id outside
+ * [0, num_pages) found on the device is read as zeros and sets bit 1 of
+ * cache->err_flag (if non-NULL).
+ */
+#ifndef TFPA_H
+#define TFPA_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TFPA_PAGE 256          /* positions per page (compile-time constant) */
+#define TFPA_HEAD_DIM 128      /* the only head size built                  */
+#define TFPA_MAX_SPLITS 32     /* split-K partials per (row, head), at most */
+
+enum {
+  TFPA_OK = 0,
+  TFPA_EINVAL = -1,      /* bad dims, dtype, NULL pointer or misalignment    */
+  TFPA_ERANGE = -2,      /* a position, segment or (host-mirrored) page id out of range */
+  TFPA_ECAPACITY = -3,   /* scratch too small for the requested rows/splits */
+  TFPA_ECUDA = -4,       /* a CUDA runtime/driver call or a launch failed    */
+  TFPA_EDEVICE = -5      /* current device is not sm_100-family (tcgen05)    */
+};
+
+typedef enum { TFPA_BF16 = 0, TFPA_FP8_E4M3 = 1 } tfpa_kv_dtype;
+
+/* One stream (a segment of the call). */
+typedef struct {
+  int32_t seq_len;                /* valid keys, >= 1 (includes rows written by this round) */
+  const int32_t* page_table;      /* DEVICE int32[ceil(seq_len/256)]; NULL => slab stream   */
+  const int32_t* page_table_host; /* optional HOST mirror, checked against num_pages        */
+  void* k_slab;                   /* DEVICE [hkv][slab_cap][128], slab streams only          */
+  void* v_slab;
+  int32_t slab_cap;               /* slab capacity in positions, multiple of 256            */
+} tfpa_seg;
+
+/* One layer's KV cache. */
+typedef struct {
+  tfpa_kv_dtype dtype;
+  int32_t hq, hkv, head_dim;      /* hq % hkv == 0, head_dim == 128                        */
+  void* k_pool;                   /* DEVICE [num_pages][hkv][256][128], 1024-byte aligned;  */
+  void* v_pool;                   /*   may be NULL when no segment is paged                 */
+  int32_t num_pages;
+  const float* k_scale;           /* DEVICE float[hkv], fp8 only: value = e4m3 * scale      */
+  const float* v_scale;
+  int32_t* err_flag;              /* optional DEVICE int32, OR-ed with 1 on a bad page id   */
+} tfpa_cache;
+
+/* Split-K scratch for decode partials (float32).
+ *   part_o  : DEVICE [cap_rows][hq][max_splits][128]  unnormalised outputs o
+ *   part_ml : DEVICE [cap_rows][hq][max_splits][2]    (m, l): running max of the
+ *             scores in log2 units (score * log2(e)) and the sum of 2^(s2 - m)  */
+typedef struct {
+  float* part_o;
+  float* part_ml;
+  int32_t cap_rows;               /* rows one partial launch can hold                      */
+  int32_t max_splits;             /* >= tfpa_num_splits(seq_len) of every segment used     */
+} tfpa_scratch;
+
+/* Split policy, a function of a stream's own length only (so a stream's
+ * partials never depend on its batch): pages_per_split = max(1,
+ * ceil(npages / 32)), nsplit = ceil(npages / pages_per_split). */
+int32_t tfpa_pages_per_split(int32_t seq_len);
+int32_t tfpa_num_splits(int32_t seq_len);
+
+/* KV write (the KV store kernels that write a stream's page run, PR #1373,
+ * "What changes"): row r's K and V for every kv head go to position
+ * row_pos[r] of segment row_seg[r], through its page table or slab.  bf16
+ * caches copy the bits; fp8 caches store e4m3(RNE, saturating) of
+ * float32(x) / scale[g].  row_seg/row_pos are HOST int32[rows]. */
+int tfpa_write_kv(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                  const void* k_rows, const void* v_rows,
+                  const int32_t* row_seg, const int32_t* row_pos, int32_t rows,
+                  cudaStream_t stream);
+
+/* Decode/verify split-K partials (Issue #1344, "Mechanism": the partial
+ * kernels write pm/pl/po, then attn_merge).  For each row r < rows, head h
+ * and split s < tfpa_num_splits(seq_len): (m, l, o) at scratch row r.
+ * Requires rows <= scratch->cap_rows (TFPA_ECAPACITY otherwise). */
+int tfpa_decode_partial(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                        const void* q, const int32_t* row_seg, const int32_t* row_pos,
+                        int32_t rows, float softmax_scale, const tfpa_scratch* scratch,
+                        cudaStream_t stream);
+
+/* Log-sum-exp merge of scratch rows 0..rows-1 (PR #1355: one merge per slice
+ * of at most most_verify rows): out = sum_s o_s 2^(m_s-M) / sum_s l_s 2^(m_s-M),
+ * lse = ln2 * (M + log2 sum_s l_s 2^(m_s-M)).  nsplit is HOST int32[rows]. */
+int tfpa_merge(const tfpa_scratch* scratch, int32_t hq, int32_t rows,
+               const int32_t* nsplit, void* out, float* lse, cudaStream_t stream);
+
+/* Decode/verify attention: partial + merge, in slices of at most
+ * scratch->cap_rows rows on shifted q/row-table/out pointers (PR #1355,
+ * "Follow-up checks": slices never overrun the partial scratch). */
+int tfpa_decode(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                const void* q, const int32_t* row_seg, const int32_t* row_pos,
+                int32_t rows, float softmax_scale, const tfpa_scratch* scratch,
+                void* out, float* lse, cudaStream_t stream);
+
+/* Causal prompt-chunk attention over the paged prefix, one pass with online
+ * softmax on tcgen05/TMEM tiles (PR #2011, "hpattn_p256_kernel": page size a
+ * constant 256, one page lookup per key tile).  max_rows_per_launch > 0 runs
+ * the rows in slices of that many (a slice's result is the same bytes as one
+ * launch); 0 = one launch.  bf16 and fp8 caches. */
+int tfpa_prefill(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                 const void* q, const int32_t* row_seg, const int32_t* row_pos,
+                 int32_t rows, float softmax_scale, int32_t max_rows_per_launch,
+                 void* out, float* lse, cudaStream_t stream);
+
+/* Launch recording for host tests (PR #1355: "a launch-recording host test
+ * where a 257-row chunk issues 3 slices").  With a hook installed every
+ * launch is reported; with dry_run != 0 nothing is enqueued and no CUDA call
+ * is made, so the slicing logic runs on a machine without a GPU. */
+typedef struct {
+  int32_t kind;          /* 0 write_kv, 1 decode partial, 2 merge, 3 prefill */
+  int32_t row0;          /* first row of the call this launch covers */
+  int32_t rows;          /* rows it covers */
+  int32_t runs;          /* row groups (segment, consecutive positions) */
+  int32_t items;         /* work items (decode: tiles of (kv head, m-tile, split)) */
+  int32_t grid;          /* CTAs */
+  int64_t q_offset;      /* element offset of the q pointer it got, from the call's q */
+  int64_t out_offset;    /* element offset of the out pointer, from the call's out */
+} tfpa_launch_record;
+typedef void (*tfpa_launch_hook)(const tfpa_launch_record* rec, void* user);
+void tfpa_set_launch_hook(tfpa_launch_hook hook, void* user, int dry_run);
+
+const char* tfpa_strerror(int code);
+const char* tfpa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TFPA_H */

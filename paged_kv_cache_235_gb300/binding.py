@@ -1,0 +1,269 @@
+"""Thin ctypes binding of libtfpa.so: the same entry-point names as the C ABI.
+
+Only argument marshalling happens here: tensors become device pointers, row
+tables become host int32 arrays, the current torch stream becomes the
+``cudaStream_t``.  Every step of the attention runs in the library's kernels.
+Loading fails loudly if the library has not been built.
+"""
+
+import contextlib
+import ctypes
+import os
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtfpa.so")
+
+PAGE = 256
+HEAD_DIM = 128
+MAX_SPLITS = 32
+BF16, FP8_E4M3 = 0, 1
+
+TFPA_OK, TFPA_EINVAL, TFPA_ERANGE, TFPA_ECAPACITY, TFPA_ECUDA, TFPA_EDEVICE = 0, -1, -2, -3, -4, -5
+
+EXPORTS = ("tfpa_pages_per_split", "tfpa_num_splits", "tfpa_write_kv", "tfpa_decode_partial",
+           "tfpa_merge", "tfpa_decode", "tfpa_prefill", "tfpa_set_launch_hook",
+           "tfpa_strerror", "tfpa_version")
+
+
+class TfpaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {code} ({strerror(code)})")
+
+
+class tfpa_seg(ctypes.Structure):
+    _fields_ = [("seq_len", ctypes.c_int32), ("page_table", ctypes.c_void_p),
+                ("page_table_host", ctypes.c_void_p), ("k_slab", ctypes.c_void_p),
+                ("v_slab", ctypes.c_void_p), ("slab_cap", ctypes.c_int32)]
+
+
+class tfpa_cache(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int), ("hq", ctypes.c_int32), ("hkv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("k_pool", ctypes.c_void_p),
+                ("v_pool", ctypes.c_void_p), ("num_pages", ctypes.c_int32),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("err_flag", ctypes.c_void_p)]
+
+
+class tfpa_scratch(ctypes.Structure):
+    _fields_ = [("part_o", ctypes.c_void_p), ("part_ml", ctypes.c_void_p),
+                ("cap_rows", ctypes.c_int32), ("max_splits", ctypes.c_int32)]
+
+
+class tfpa_launch_record(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("row0", ctypes.c_int32), ("rows", ctypes.c_int32),
+                ("runs", ctypes.c_int32), ("items", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("q_offset", ctypes.c_int64), ("out_offset", ctypes.c_int64)]
+
+
+HOOK = ctypes.CFUNCTYPE(None, ctypes.POINTER(tfpa_launch_record), ctypes.c_void_p)
+KINDS = {0: "write_kv", 1: "partial", 2: "merge", 3: "prefill"}
+
+_lib = None
+
+
+def lib():
+    """The loaded library (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        i32, vp, P = ctypes.c_int32, ctypes.c_void_p, ctypes.POINTER
+        L.tfpa_pages_per_split.argtypes = [i32]
+        L.tfpa_pages_per_split.restype = i32
+        L.tfpa_num_splits.argtypes = [i32]
+        L.tfpa_num_splits.restype = i32
+        L.tfpa_write_kv.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, vp, i32, vp]
+        L.tfpa_write_kv.restype = ctypes.c_int
+        L.tfpa_decode_partial.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, i32,
+                                          ctypes.c_float, P(tfpa_scratch), vp]
+        L.tfpa_decode_partial.restype = ctypes.c_int
+        L.tfpa_merge.argtypes = [P(tfpa_scratch), i32, i32, vp, vp, vp, vp]
+        L.tfpa_merge.restype = ctypes.c_int
+        L.tfpa_decode.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, i32,
+                                  ctypes.c_float, P(tfpa_scratch), vp, vp, vp]
+        L.tfpa_decode.restype = ctypes.c_int
+        L.tfpa_prefill.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, i32,
+                                   ctypes.c_float, i32, vp, vp, vp]
+        L.tfpa_prefill.restype = ctypes.c_int
+        L.tfpa_set_launch_hook.argtypes = [HOOK, vp, ctypes.c_int]
+        L.tfpa_set_launch_hook.restype = None
+        L.tfpa_strerror.argtypes = [ctypes.c_int]
+        L.tfpa_strerror.restype = ctypes.c_char_p
+        L.tfpa_version.argtypes = []
+        L.tfpa_version.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().tfpa_strerror(code).decode()
+
+
+def _check(code: int, where: str):
+    if code != TFPA_OK:
+        raise TfpaError(code, where)
+
+
+def _ptr(x) -> Optional[int]:
+    """Device (or host) address of a tensor/array, or an int passed through."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    if torch.cuda.is_available():
+        return torch.cuda.current_stream().cuda_stream
+    return None
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+@dataclass
+class Cache:
+    """One layer's KV cache; holds the tensors so their memory stays alive."""
+    dtype: str                    # "bf16" or "fp8"
+    hq: int
+    hkv: int
+    k_pool: object = None         # [num_pages][hkv][256][128] bf16 (or int16) / uint8
+    v_pool: object = None
+    k_scale: object = None        # float32 [hkv] (fp8)
+    v_scale: object = None
+    err_flag: object = None       # int32 [1]
+    num_pages: int = 0
+
+    def c(self) -> tfpa_cache:
+        return tfpa_cache(BF16 if self.dtype == "bf16" else FP8_E4M3, self.hq, self.hkv,
+                          HEAD_DIM, _ptr(self.k_pool), _ptr(self.v_pool), self.num_pages,
+                          _ptr(self.k_scale), _ptr(self.v_scale), _ptr(self.err_flag))
+
+
+@dataclass
+class Seg:
+    """One stream: a device page table or a pair of slabs."""
+    seq_len: int
+    page_table: object = None         # device int32 [>= ceil(seq_len/256)]
+    page_table_host: object = None    # optional host int32 mirror (validated)
+    k_slab: object = None             # [hkv][slab_cap][128]
+    v_slab: object = None
+    slab_cap: int = 0
+
+    def c(self) -> tfpa_seg:
+        host = None
+        if self.page_table_host is not None:
+            self.page_table_host = _i32(self.page_table_host)
+            host = _ptr(self.page_table_host)
+        return tfpa_seg(int(self.seq_len), _ptr(self.page_table), host, _ptr(self.k_slab),
+                        _ptr(self.v_slab), int(self.slab_cap))
+
+
+@dataclass
+class Scratch:
+    part_o: object
+    part_ml: object
+    cap_rows: int
+    max_splits: int = MAX_SPLITS
+
+    def c(self) -> tfpa_scratch:
+        return tfpa_scratch(_ptr(self.part_o), _ptr(self.part_ml), self.cap_rows, self.max_splits)
+
+
+def make_scratch(cap_rows: int, hq: int, max_splits: int = MAX_SPLITS, device="cuda") -> Scratch:
+    import torch
+    o = torch.empty(cap_rows * hq * max_splits * HEAD_DIM, dtype=torch.float32, device=device)
+    ml = torch.empty(cap_rows * hq * max_splits * 2, dtype=torch.float32, device=device)
+    return Scratch(o, ml, cap_rows, max_splits)
+
+
+def _segs(segs: Sequence[Seg]):
+    arr = (tfpa_seg * max(1, len(segs)))(*[s.c() for s in segs])
+    return arr, len(segs)
+
+
+def tfpa_pages_per_split(seq_len: int) -> int:
+    return lib().tfpa_pages_per_split(int(seq_len))
+
+
+def tfpa_num_splits(seq_len: int) -> int:
+    return lib().tfpa_num_splits(int(seq_len))
+
+
+def tfpa_write_kv(cache: Cache, segs: Sequence[Seg], k_rows, v_rows, row_seg, row_pos,
+                  stream=None) -> None:
+    cs, n = _segs(segs)
+    rs, rp = _i32(row_seg), _i32(row_pos)
+    cc = cache.c()
+    _check(lib().tfpa_write_kv(ctypes.byref(cc), cs, n, _ptr(k_rows), _ptr(v_rows), _ptr(rs),
+                               _ptr(rp), len(rs), _stream(stream)), "tfpa_write_kv")
+
+
+def tfpa_decode_partial(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, softmax_scale,
+                        scratch: Scratch, stream=None) -> None:
+    cs, n = _segs(segs)
+    rs, rp = _i32(row_seg), _i32(row_pos)
+    cc, sc = cache.c(), scratch.c()
+    _check(lib().tfpa_decode_partial(ctypes.byref(cc), cs, n, _ptr(q), _ptr(rs), _ptr(rp),
+                                     len(rs), float(softmax_scale), ctypes.byref(sc),
+                                     _stream(stream)), "tfpa_decode_partial")
+
+
+def tfpa_merge(scratch: Scratch, hq: int, nsplit, out, lse=None, stream=None) -> None:
+    ns = _i32(nsplit)
+    sc = scratch.c()
+    _check(lib().tfpa_merge(ctypes.byref(sc), int(hq), len(ns), _ptr(ns), _ptr(out), _ptr(lse),
+                            _stream(stream)), "tfpa_merge")
+
+
+def tfpa_decode(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, softmax_scale,
+                scratch: Scratch, out, lse=None, stream=None) -> None:
+    cs, n = _segs(segs)
+    rs, rp = _i32(row_seg), _i32(row_pos)
+    cc, sc = cache.c(), scratch.c()
+    _check(lib().tfpa_decode(ctypes.byref(cc), cs, n, _ptr(q), _ptr(rs), _ptr(rp), len(rs),
+                             float(softmax_scale), ctypes.byref(sc), _ptr(out), _ptr(lse),
+                             _stream(stream)), "tfpa_decode")
+
+
+def tfpa_prefill(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, softmax_scale, out,
+                 lse=None, max_rows_per_launch: int = 0, stream=None) -> None:
+    cs, n = _segs(segs)
+    rs, rp = _i32(row_seg), _i32(row_pos)
+    cc = cache.c()
+    _check(lib().tfpa_prefill(ctypes.byref(cc), cs, n, _ptr(q), _ptr(rs), _ptr(rp), len(rs),
+                              float(softmax_scale), int(max_rows_per_launch), _ptr(out),
+                              _ptr(lse), _stream(stream)), "tfpa_prefill")
+
+
+@contextlib.contextmanager
+def record_launches(dry_run: bool = True):
+    """Collects the library's launches as dicts; with dry_run nothing runs."""
+    records: List[dict] = []
+
+    def _cb(rec, _user):
+        r = rec.contents
+        records.append(dict(kind=KINDS[r.kind], row0=r.row0, rows=r.rows, runs=r.runs,
+                            items=r.items, grid=r.grid, q_offset=r.q_offset,
+                            out_offset=r.out_offset))
+
+    cb = HOOK(_cb)
+    lib().tfpa_set_launch_hook(cb, None, 1 if dry_run else 0)
+    try:
+        yield records
+    finally:
+        lib().tfpa_set_launch_hook(HOOK(), None, 0)

@@ -1,0 +1,578 @@
+// Decode/verify attention as split-K partials plus a log-sum-exp merge
+// (TensorFold Issue #1344, "Mechanism": partial kernels write running max,
+// sum and unnormalised output per split, then attn_merge combines them).
+//
+// Partial kernel: persistent CTAs walk a list of work items
+// (run, kv head g, m-tile of 16 query vectors, split).  A split is a fixed
+// number of whole pages chosen from the stream's own length, so a row's
+// partials never depend on its batch or on how rows are sliced.  Per CTA:
+//   warp 4      producer: looks each page up once (PR #2011, "the decode
+//               tiles ... look a page up once"), stages K and V chunks into
+//               shared memory with TMA tiled loads (128B swizzle), 3 stages;
+//   warps 0..3  consumers: each takes a quarter of every chunk's keys, runs
+//               QK^T and PV on mma.sync m16n8k16 (bf16, or f16 for e4m3
+//               caches, whose bytes convert to f16 exactly) and an online
+//               softmax reduced with warp shuffles; at the end of an item the
+//               four warps' states are combined in a fixed order.
+// Paged and slab streams differ only in the TMA row coordinate, so they
+// produce the same bytes (PR #1373, "What changes").
+#include "common.cuh"
+#include "params.h"
+
+namespace tfpa {
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kStageBytes = 65536;    // K 32 KB + V 32 KB
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kCombRow = 132;         // padded float row of the combine buffer
+constexpr int kCombBytes = kConsumerWarps * 16 * kCombRow * 4;
+constexpr int kSmemBytes = kStages * kStageBytes + kCombBytes + kConsumerWarps * 16 * 2 * 4 +
+                           kStages * 16 + (2 * kStages + 2) * 8 + 1024;
+
+template <bool FP8>
+struct Cfg {
+  static constexpr int kChunk = FP8 ? 256 : 128;      // keys per stage
+  static constexpr int kKeysPerWarp = kChunk / kConsumerWarps;
+  static constexpr int kNT = kKeysPerWarp / 8;         // score n-tiles per warp
+  static constexpr int kKS = kKeysPerWarp / 16;        // PV k-steps per warp
+};
+
+struct Item {
+  int run, g, mt, sigma;
+};
+
+__device__ __forceinline__ Item item_of(const DecodeParams& p, int it) {
+  int r = 0;
+  while (r + 1 < p.nruns && p.runs[r + 1].item0 <= it) ++r;
+  const RunInfo& ru = p.runs[r];
+  int local = it - ru.item0;
+  const int mtiles = (ru.nrows * p.group + 15) >> 4;
+  Item x;
+  x.run = r;
+  x.sigma = local % ru.nsplit;
+  local /= ru.nsplit;
+  x.mt = local % mtiles;
+  x.g = local / mtiles;
+  return x;
+}
+
+// Key range [klo, khi) an item must read: its split's pages, cut at the
+// stream length and at the last position among the m-tile's rows.
+__device__ __forceinline__ void item_keys(const DecodeParams& p, const Item& x, int& klo,
+                                          int& khi) {
+  const RunInfo& ru = p.runs[x.run];
+  const int nq = ru.nrows * p.group;
+  const int last_qv = min(x.mt * 16 + 15, nq - 1);
+  const int maxpos = ru.pos0 + last_qv / p.group;
+  klo = x.sigma * ru.pps * kPage;
+  khi = min(min(klo + ru.pps * kPage, ru.seq_len), maxpos + 1);
+}
+
+template <bool FP8>
+__device__ void producer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* full,
+                         uint64_t* empty, int* stage_bad) {
+  using C = Cfg<FP8>;
+  const int lane = threadIdx.x & 31;
+  uint32_t stage = 0;
+  for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+    const Item x = item_of(p, it);
+    const RunInfo& ru = p.runs[x.run];
+    int klo, khi;
+    item_keys(p, x, klo, khi);
+    const CUtensorMap* mk = &p.maps[ru.src].k;
+    const CUtensorMap* mv = &p.maps[ru.src].v;
+    int cached_page = -1, cached_pid = 0;
+    for (int k0 = klo; k0 < khi; k0 += C::kChunk, ++stage) {
+      const int buf = stage % kStages;
+      const uint32_t ph = (stage / kStages) & 1;
+      if (lane == 0) {
+        if (!mbar_wait(&empty[buf], ph ^ 1, p.err_flag)) return;
+        const int page = k0 >> 8;
+        int y, bad = 0;
+        if (ru.page_table) {
+          if (page != cached_page) {  // one lookup per page
+            cached_pid = __ldg(ru.page_table + page);
+            cached_page = page;
+          }
+          int pid = cached_pid;
+          if ((unsigned)pid >= (unsigned)p.num_pages) {
+            flag_error(p.err_flag, kErrBadPage);
+            bad = 1;
+            pid = 0;
+          }
+          y = (pid * p.hkv + x.g) * kPage + (k0 & (kPage - 1));
+        } else {
+          y = x.g * ru.slab_cap + k0;
+        }
+        stage_bad[buf] = bad;
+        uint64_t* fb = &full[buf];
+        uint8_t* sb = stage_mem + (size_t)buf * kStageBytes;
+        mbar_arrive_expect_tx(fb, kStageBytes);
+        if (FP8) {
+          tma_load_2d(sb, mk, 0, y, fb);
+          tma_load_2d(sb + 32768, mv, 0, y, fb);
+        } else {
+          tma_load_2d(sb, mk, 0, y, fb);
+          tma_load_2d(sb + 16384, mk, 64, y, fb);
+          tma_load_2d(sb + 32768, mv, 0, y, fb);
+          tma_load_2d(sb + 49152, mv, 64, y, fb);
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// Real head-dim index of C-fragment column n of PV n-tile nt (the V fragments
+// are loaded so a thread's sixteen n-tiles cover contiguous 16-byte chunks).
+template <bool FP8>
+__device__ __forceinline__ int out_col(int nt, int n) {
+  if (FP8) return 16 * n + nt;
+  return nt < 8 ? 8 * n + nt : 64 + 8 * n + (nt - 8);
+}
+
+// Bounded barrier among the four consumer warps (an mbarrier of count 4).
+__device__ __forceinline__ bool consumers_sync(uint64_t* bar, uint32_t& phase, int32_t* err) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait(bar, phase & 1, err);
+  ++phase;
+  return ok;
+}
+
+template <bool FP8>
+__device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* full,
+                         uint64_t* empty, const int* stage_bad, float* comb, float* comb_ml,
+                         uint64_t* cbar) {
+  using C = Cfg<FP8>;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gq = lane >> 2, c = lane & 3;
+  const uint32_t sbase = smem_u32(stage_mem);
+  uint32_t stage = 0, cphase = 0;
+
+  for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+    const Item x = item_of(p, it);
+    const RunInfo& ru = p.runs[x.run];
+    int klo, khi;
+    item_keys(p, x, klo, khi);
+    const int nq = ru.nrows * p.group;
+
+    // ---- query fragments (rows gq and gq+8 of the m-tile)
+    int lim[2];
+    float sc[2];
+    uint32_t qr[2][16];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int qv = x.mt * 16 + gq + 8 * hr;
+      uint4 v[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                    make_uint4(0, 0, 0, 0)};
+      lim[hr] = -1;
+      if (qv < nq) {
+        const int r = qv / p.group;
+        const int h = x.g * p.group + (qv - r * p.group);
+        lim[hr] = ru.pos0 + r;
+        const uint4* qp = reinterpret_cast<const uint4*>(
+            p.q + ((size_t)(ru.row0 + r) * p.hq + h) * kHeadDim);
+        if (FP8) {
+#pragma unroll
+          for (int m = 0; m < 4; ++m) v[m] = __ldg(qp + 4 * c + m);
+        } else {
+          v[0] = __ldg(qp + 2 * c);
+          v[1] = __ldg(qp + 2 * c + 1);
+          v[2] = __ldg(qp + 8 + 2 * c);
+          v[3] = __ldg(qp + 8 + 2 * c + 1);
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        qr[hr][4 * m + 0] = v[m].x;
+        qr[hr][4 * m + 1] = v[m].y;
+        qr[hr][4 * m + 2] = v[m].z;
+        qr[hr][4 * m + 3] = v[m].w;
+      }
+      sc[hr] = p.scale_log2;
+      if (FP8) {
+        // f16 operands: scale the row by a power of two into f16 range (exact
+        // for every element within 2^28 of the row's largest).
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          amax = fmaxf(amax, fabsf(__uint_as_float(qr[hr][j] << 16)));
+          amax = fmaxf(amax, fabsf(__uint_as_float(qr[hr][j] & 0xFFFF0000u)));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        int ex;
+        frexpf(amax, &ex);
+        ex = max(min(ex, 120), -100);
+        const float up = __int_as_float((127 + 14 - ex) << 23);
+        const float down = __int_as_float((127 - 14 + ex) << 23);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float lo = __uint_as_float(qr[hr][j] << 16) * up;
+          const float hi = __uint_as_float(qr[hr][j] & 0xFFFF0000u) * up;
+          qr[hr][j] = pack_f16x2(lo, hi);
+        }
+        sc[hr] = p.scale_log2 * down * __ldg(p.k_scale + x.g);
+      }
+    }
+    const int maxlim = __reduce_max_sync(0xffffffffu, max(lim[0], lim[1]));
+
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+    float o[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+
+    bool aborted = false;
+    for (int k0 = klo; k0 < khi; k0 += C::kChunk, ++stage) {
+      const int buf = stage % kStages;
+      const uint32_t ph = (stage / kStages) & 1;
+      if (!mbar_wait(&full[buf], ph, p.err_flag)) {
+        aborted = true;
+        break;
+      }
+      const uint32_t sb = sbase + (uint32_t)buf * kStageBytes;
+      const int wk0 = warp * C::kKeysPerWarp;
+      const int key_base = k0 + wk0;
+      if (!stage_bad[buf] && key_base <= maxlim) {
+        // ---- S = Q K^T over this warp's keys
+        float s[C::kNT][4];
+#pragma unroll
+        for (int nt = 0; nt < C::kNT; ++nt) {
+          s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+          const int kr = wk0 + nt * 8 + gq;
+          uint32_t kb[16];
+          if (FP8) {
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+              const uint4 w = lds128(swz128(sb, kr, 2 * c + ch));
+              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                kb[8 * ch + 2 * i] = e4m3x2_to_f16x2((uint16_t)(ws[i] & 0xFFFF));
+                kb[8 * ch + 2 * i + 1] = e4m3x2_to_f16x2((uint16_t)(ws[i] >> 16));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              const uint32_t base = sb + (ch >> 1) * 16384u;
+              const uint4 w = lds128(swz128(base, kr, 2 * c + (ch & 1)));
+              kb[4 * ch + 0] = w.x;
+              kb[4 * ch + 1] = w.y;
+              kb[4 * ch + 2] = w.z;
+              kb[4 * ch + 3] = w.w;
+            }
+          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t a[4] = {qr[0][2 * ks], qr[1][2 * ks], qr[0][2 * ks + 1],
+                                   qr[1][2 * ks + 1]};
+            if (FP8)
+              mma_f16(s[nt], a, kb[2 * ks], kb[2 * ks + 1]);
+            else
+              mma_bf16(s[nt], a, kb[2 * ks], kb[2 * ks + 1]);
+          }
+        }
+        // ---- scale, causal mask, online softmax (rows gq, gq+8; a row's
+        // keys are spread over the 4 threads of a quad)
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int nt = 0; nt < C::kNT; ++nt) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int hr = j >> 1;
+            const int key = key_base + nt * 8 + 2 * c + (j & 1);
+            const float v = key <= lim[hr] ? s[nt][j] * sc[hr] : -INFINITY;
+            s[nt][j] = v;
+            mx[hr] = fmaxf(mx[hr], v);
+          }
+        }
+        float alpha[2], base[2];
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
+          mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
+          const float mnew = fmaxf(m_run[hr], mx[hr]);
+          base[hr] = mnew == -INFINITY ? 0.f : mnew;
+          alpha[hr] = fast_exp2(m_run[hr] - base[hr]);
+          m_run[hr] = mnew;
+        }
+        float rs[2] = {0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < C::kNT; ++nt) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float e = fast_exp2(s[nt][j] - base[j >> 1]);
+            s[nt][j] = e;
+            rs[j >> 1] += e;
+          }
+        }
+        l_run[0] = l_run[0] * alpha[0] + rs[0];
+        l_run[1] = l_run[1] * alpha[1] + rs[1];
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+          o[nt][0] *= alpha[0];
+          o[nt][1] *= alpha[0];
+          o[nt][2] *= alpha[1];
+          o[nt][3] *= alpha[1];
+        }
+        // ---- O += P V
+        const uint32_t vb = sb + 32768u;
+#pragma unroll
+        for (int kk = 0; kk < C::kKS; ++kk) {
+          uint32_t a[4];
+          if (FP8) {
+            a[0] = pack_f16x2(s[2 * kk][0], s[2 * kk][1]);
+            a[1] = pack_f16x2(s[2 * kk][2], s[2 * kk][3]);
+            a[2] = pack_f16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+            a[3] = pack_f16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+          } else {
+            a[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
+            a[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
+            a[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+            a[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+          }
+          const int kv0 = wk0 + 16 * kk + 2 * c;   // rows kv0, kv0+1, kv0+8, kv0+9
+          const int krow[4] = {kv0, kv0 + 1, kv0 + 8, kv0 + 9};
+          if (FP8) {
+            uint32_t w[4][4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 t = lds128(swz128(vb, krow[q4], gq));
+              if (k0 + krow[q4] >= ru.seq_len) t = make_uint4(0, 0, 0, 0);
+              w[q4][0] = t.x; w[q4][1] = t.y; w[q4][2] = t.z; w[q4][3] = t.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t x01 = prmt(w[0][i], w[1][i], 0x5140);
+              const uint32_t y01 = prmt(w[0][i], w[1][i], 0x7362);
+              const uint32_t x23 = prmt(w[2][i], w[3][i], 0x5140);
+              const uint32_t y23 = prmt(w[2][i], w[3][i], 0x7362);
+              mma_f16(o[4 * i + 0], a, e4m3x2_to_f16x2((uint16_t)(x01 & 0xFFFF)),
+                      e4m3x2_to_f16x2((uint16_t)(x23 & 0xFFFF)));
+              mma_f16(o[4 * i + 1], a, e4m3x2_to_f16x2((uint16_t)(x01 >> 16)),
+                      e4m3x2_to_f16x2((uint16_t)(x23 >> 16)));
+              mma_f16(o[4 * i + 2], a, e4m3x2_to_f16x2((uint16_t)(y01 & 0xFFFF)),
+                      e4m3x2_to_f16x2((uint16_t)(y23 & 0xFFFF)));
+              mma_f16(o[4 * i + 3], a, e4m3x2_to_f16x2((uint16_t)(y01 >> 16)),
+                      e4m3x2_to_f16x2((uint16_t)(y23 >> 16)));
+            }
+          } else {
+            uint32_t r[4][8];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 t0 = lds128(swz128(vb, krow[q4], gq));
+              uint4 t1 = lds128(swz128(vb + 16384u, krow[q4], gq));
+              if (k0 + krow[q4] >= ru.seq_len) {
+                t0 = make_uint4(0, 0, 0, 0);
+                t1 = t0;
+              }
+              r[q4][0] = t0.x; r[q4][1] = t0.y; r[q4][2] = t0.z; r[q4][3] = t0.w;
+              r[q4][4] = t1.x; r[q4][5] = t1.y; r[q4][6] = t1.z; r[q4][7] = t1.w;
+            }
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt) {
+              const uint32_t sel = (nt & 1) ? 0x7632u : 0x5410u;
+              const uint32_t b0 = prmt(r[0][nt >> 1], r[1][nt >> 1], sel);
+              const uint32_t b1 = prmt(r[2][nt >> 1], r[3][nt >> 1], sel);
+              mma_bf16(o[nt], a, b0, b1);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[buf]);
+    }
+    if (aborted) return;
+
+    // ---- combine the four warps' states in a fixed order
+    l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 1);
+    l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 2);
+    l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 1);
+    l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 2);
+    if (c == 0) {
+      comb_ml[(warp * 16 + gq) * 2 + 0] = m_run[0];
+      comb_ml[(warp * 16 + gq) * 2 + 1] = l_run[0];
+      comb_ml[(warp * 16 + gq + 8) * 2 + 0] = m_run[1];
+      comb_ml[(warp * 16 + gq + 8) * 2 + 1] = l_run[1];
+    }
+    float* cw = comb + warp * 16 * kCombRow;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      const int d0 = out_col<FP8>(nt, 2 * c), d1 = out_col<FP8>(nt, 2 * c + 1);
+      cw[gq * kCombRow + d0] = o[nt][0];
+      cw[gq * kCombRow + d1] = o[nt][1];
+      cw[(gq + 8) * kCombRow + d0] = o[nt][2];
+      cw[(gq + 8) * kCombRow + d1] = o[nt][3];
+    }
+    if (!consumers_sync(cbar, cphase, p.err_flag)) return;
+    {
+      const int t = threadIdx.x;          // 0..127
+      const int row = t >> 3;             // m-tile row
+      const int d0 = (t & 7) * 16;
+      const int qv = x.mt * 16 + row;
+      if (qv < nq) {
+        float mw[kConsumerWarps], lw[kConsumerWarps];
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          mw[w] = comb_ml[(w * 16 + row) * 2 + 0];
+          lw[w] = comb_ml[(w * 16 + row) * 2 + 1];
+          M = fmaxf(M, mw[w]);
+        }
+        float aw[kConsumerWarps], L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          aw[w] = mw[w] == -INFINITY ? 0.f : fast_exp2(mw[w] - M);
+          L += aw[w] * lw[w];
+        }
+        const float vs = FP8 ? __ldg(p.v_scale + x.g) : 1.f;
+        const int r = qv / p.group;
+        const int h = x.g * p.group + (qv - r * p.group);
+        const size_t slot = ((size_t)(ru.row0 + r) * p.hq + h) * p.max_splits + x.sigma;
+        float4* dst = reinterpret_cast<float4*>(p.part_o + slot * kHeadDim + d0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w)
+              acc += aw[w] * comb[(w * 16 + row) * kCombRow + d0 + 4 * j + e];
+            v[e] = acc * vs;
+          }
+          dst[j] = make_float4(v[0], v[1], v[2], v[3]);
+        }
+        if ((t & 7) == 0) {
+          p.part_ml[slot * 2 + 0] = M;
+          p.part_ml[slot * 2 + 1] = L;
+        }
+      }
+    }
+    if (!consumers_sync(cbar, cphase, p.err_flag)) return;
+  }
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
+    const __grid_constant__ DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* stage_mem = smem;
+  float* comb = reinterpret_cast<float*>(smem + kStages * kStageBytes);
+  float* comb_ml = comb + kConsumerWarps * 16 * kCombRow;
+  int* stage_bad = reinterpret_cast<int*>(comb_ml + kConsumerWarps * 16 * 2);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage_bad + 4 * kStages);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* cbar = bars + 2 * kStages;
+
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    mbar_init(cbar, kConsumerWarps);
+    fence_mbar_init();
+  }
+  if (warp == kConsumerWarps && (threadIdx.x & 31) == 0) {
+    for (int i = 0; i < p.nsrc; ++i) {
+      tma_prefetch_desc(&p.maps[i].k);
+      tma_prefetch_desc(&p.maps[i].v);
+    }
+  }
+  __syncthreads();
+  if (warp == kConsumerWarps)
+    producer<FP8>(p, stage_mem, full, empty, stage_bad);
+  else
+    consumer<FP8>(p, stage_mem, full, empty, stage_bad, comb, comb_ml, cbar);
+}
+
+// ---------------------------------------------------------------- merge
+// One warp per (row, head): lane s holds split s's (m, l); lanes own 4
+// consecutive head-dim elements of the output.  Fixed summation order.
+__global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ MergeParams p) {
+  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= p.rows * p.hq) return;
+  const int row = wid / p.hq;
+  const int h = wid - row * p.hq;
+  int ri = 0;
+  while (ri + 1 < p.nruns && p.runs[ri + 1].row0 <= row) ++ri;
+  const int nsplit = p.runs[ri].nsplit;
+  const size_t slot0 = ((size_t)row * p.hq + h) * p.max_splits;
+  float m = -INFINITY, l = 0.f;
+  if (lane < nsplit) {
+    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (slot0 + lane) * 2);
+    m = ml.x;
+    l = ml.y;
+  }
+  float M = m;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float a = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
+  float L = a * l;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < nsplit; ++s) {
+    const float as = __shfl_sync(0xffffffffu, a, s);
+    if (as != 0.f) {
+      const float4 v =
+          *reinterpret_cast<const float4*>(p.part_o + (slot0 + s) * kHeadDim + lane * 4);
+      acc.x += as * v.x;
+      acc.y += as * v.y;
+      acc.z += as * v.z;
+      acc.w += as * v.w;
+    }
+  }
+  const float inv = 1.f / L;
+  uint2 packed;
+  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(p.out + ((size_t)row * p.hq + h) * kHeadDim + lane * 4) = packed;
+  if (p.lse && lane == 0) p.lse[(size_t)row * p.hq + h] = (M + log2f(L)) * 0.6931471805599453f;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cudaStream_t s) {
+  if (grid <= 0 || p.n_items == 0) return cudaSuccess;
+  static bool configured[2] = {false, false};
+  cudaError_t e;
+  if (fp8) {
+    if (!configured[1]) {
+      e = cudaFuncSetAttribute(decode_partial_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e != cudaSuccess) return e;
+      configured[1] = true;
+    }
+    decode_partial_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
+  } else {
+    if (!configured[0]) {
+      e = cudaFuncSetAttribute(decode_partial_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e != cudaSuccess) return e;
+      configured[0] = true;
+    }
+    decode_partial_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
+  const int warps = p.rows * p.hq;
+  if (warps == 0) return cudaSuccess;
+  merge_kernel<<<(warps + 7) / 8, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace tfpa

@@ -1,0 +1,562 @@
+// C-ABI entry points: argument checks, row grouping, slicing, TMA
+// descriptors and launches.  No allocation, no stream synchronisation.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+#include "params.h"
+#include "tfpa.h"
+
+using namespace tfpa;
+
+namespace {
+
+// ------------------------------------------------------------ launch hook
+struct Hook {
+  tfpa_launch_hook fn = nullptr;
+  void* user = nullptr;
+  int dry = 0;
+};
+Hook g_hook;
+std::mutex g_mu;
+
+bool dry_run() { return g_hook.fn != nullptr && g_hook.dry != 0; }
+
+void record(int kind, int row0, int rows, int runs, int items, int grid, int64_t qoff,
+            int64_t ooff) {
+  if (!g_hook.fn) return;
+  tfpa_launch_record r;
+  r.kind = kind;
+  r.row0 = row0;
+  r.rows = rows;
+  r.runs = runs;
+  r.items = items;
+  r.grid = grid;
+  r.q_offset = qoff;
+  r.out_offset = ooff;
+  g_hook.fn(&r, g_hook.user);
+}
+
+// ------------------------------------------------------------ device info
+int sm_count() {
+  if (dry_run()) return 152;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+int check_device() {
+  if (dry_run()) return TFPA_OK;
+  int dev = 0, major = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TFPA_ECUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    return TFPA_ECUDA;
+  return major == 10 ? TFPA_OK : TFPA_EDEVICE;
+}
+
+// ------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+struct MapKey {
+  const void* ptr;
+  uint64_t rows;
+  int fp8, box_inner, box_rows;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && fp8 == o.fp8 && box_inner == o.box_inner &&
+           box_rows == o.box_rows;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    size_t h = std::hash<const void*>()(k.ptr);
+    h ^= std::hash<uint64_t>()(k.rows) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+    h ^= (size_t)(k.fp8 * 131 + k.box_inner * 7 + k.box_rows);
+    return h;
+  }
+};
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+// A 2D view [rows][128] of a K or V buffer, 128B swizzle, box
+// [box_inner elements][box_rows rows].
+int get_map(const void* ptr, uint64_t rows, bool fp8, int box_inner, int box_rows,
+            CUtensorMap* out) {
+  if (dry_run()) {
+    std::memset(out, 0, sizeof(*out));
+    return TFPA_OK;
+  }
+  MapKey key{ptr, rows, fp8 ? 1 : 0, box_inner, box_rows};
+  auto it = g_maps.find(key);
+  if (it != g_maps.end()) {
+    *out = it->second;
+    return TFPA_OK;
+  }
+  auto fn = encode_fn();
+  if (!fn) return TFPA_ECUDA;
+  const uint64_t esz = fp8 ? 1 : 2;
+  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(kHeadDim * esz)};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  CUresult r = fn(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return TFPA_ECUDA;
+  if (g_maps.size() > 4096) g_maps.clear();
+  g_maps.emplace(key, m);
+  *out = m;
+  return TFPA_OK;
+}
+
+// ------------------------------------------------------------ validation
+int32_t pages_of(int32_t L) { return (L + kPage - 1) / kPage; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_cache(const tfpa_cache* c) {
+  if (!c) return TFPA_EINVAL;
+  if (c->dtype != TFPA_BF16 && c->dtype != TFPA_FP8_E4M3) return TFPA_EINVAL;
+  if (c->head_dim != kHeadDim || c->hkv < 1 || c->hq < 1 || c->hq % c->hkv) return TFPA_EINVAL;
+  if (c->dtype == TFPA_FP8_E4M3 && (!c->k_scale || !c->v_scale)) return TFPA_EINVAL;
+  if ((c->k_pool && !aligned(c->k_pool, 16)) || (c->v_pool && !aligned(c->v_pool, 16)))
+    return TFPA_EINVAL;
+  return TFPA_OK;
+}
+
+int check_segs(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg) {
+  if (nseg < 0 || (nseg > 0 && !segs)) return TFPA_EINVAL;
+  for (int32_t s = 0; s < nseg; ++s) {
+    const tfpa_seg& g = segs[s];
+    if (g.seq_len < 1) return TFPA_EINVAL;
+    if (g.page_table) {
+      if (!c->k_pool || !c->v_pool || c->num_pages < 1) return TFPA_EINVAL;
+      if ((int64_t)c->num_pages * c->hkv * kPage > INT32_MAX) return TFPA_EINVAL;
+      if (g.page_table_host) {
+        const int32_t n = pages_of(g.seq_len);
+        for (int32_t i = 0; i < n; ++i)
+          if (g.page_table_host[i] < 0 || g.page_table_host[i] >= c->num_pages)
+            return TFPA_ERANGE;
+      }
+    } else {
+      if (!g.k_slab || !g.v_slab) return TFPA_EINVAL;
+      if (!aligned(g.k_slab, 16) || !aligned(g.v_slab, 16)) return TFPA_EINVAL;
+      if (g.slab_cap % kPage || g.slab_cap < pages_of(g.seq_len) * kPage) return TFPA_EINVAL;
+      if ((int64_t)c->hkv * g.slab_cap > INT32_MAX) return TFPA_EINVAL;
+    }
+  }
+  return TFPA_OK;
+}
+
+// A run: consecutive rows of one segment at consecutive positions.
+struct Run {
+  int32_t seg, row0, nrows, pos0;
+};
+
+int build_runs(const tfpa_seg* segs, int32_t nseg, const int32_t* row_seg,
+               const int32_t* row_pos, int32_t rows, std::vector<Run>& out) {
+  out.clear();
+  if (rows < 0 || (rows > 0 && (!row_seg || !row_pos))) return TFPA_EINVAL;
+  for (int32_t r = 0; r < rows; ++r) {
+    const int32_t s = row_seg[r], p = row_pos[r];
+    if (s < 0 || s >= nseg) return TFPA_ERANGE;
+    if (p < 0 || p >= segs[s].seq_len) return TFPA_ERANGE;
+    if (!out.empty()) {
+      Run& b = out.back();
+      if (b.seg == s && b.pos0 + b.nrows == p) {
+        ++b.nrows;
+        continue;
+      }
+    }
+    out.push_back(Run{s, r, 1, p});
+  }
+  return TFPA_OK;
+}
+
+int to_err(cudaError_t e) { return e == cudaSuccess ? TFPA_OK : TFPA_ECUDA; }
+
+}  // namespace
+
+extern "C" int32_t tfpa_pages_per_split(int32_t seq_len) {
+  const int32_t np = pages_of(std::max(seq_len, 1));
+  return std::max<int32_t>(1, (np + kMaxSplits - 1) / kMaxSplits);
+}
+
+extern "C" int32_t tfpa_num_splits(int32_t seq_len) {
+  const int32_t np = pages_of(std::max(seq_len, 1));
+  const int32_t pps = tfpa_pages_per_split(seq_len);
+  return (np + pps - 1) / pps;
+}
+
+namespace {
+
+// K/V sources of one launch: source 0 is the pool, 1.. are slab streams.
+struct SourceSet {
+  int slab_seg[kMaxSlabs];
+  int nslab = 0;
+  bool pool = false;
+  // Source index for segment `s`, or -1 if the set is full.
+  int add(const tfpa_seg* segs, int s) {
+    if (segs[s].page_table) {
+      pool = true;
+      return 0;
+    }
+    for (int i = 0; i < nslab; ++i)
+      if (slab_seg[i] == s) return i + 1;
+    if (nslab == kMaxSlabs) return -1;
+    slab_seg[nslab] = s;
+    return ++nslab;
+  }
+};
+
+int fill_maps(const tfpa_cache* c, const tfpa_seg* segs, const SourceSet& ss, bool fp8,
+              int box_inner, int box_rows, KVMaps* maps, int32_t& nsrc) {
+  int e;
+  if (ss.pool) {
+    const uint64_t rows = (uint64_t)c->num_pages * c->hkv * kPage;
+    if ((e = get_map(c->k_pool, rows, fp8, box_inner, box_rows, &maps[0].k))) return e;
+    if ((e = get_map(c->v_pool, rows, fp8, box_inner, box_rows, &maps[0].v))) return e;
+  }
+  for (int i = 0; i < ss.nslab; ++i) {
+    const tfpa_seg& g = segs[ss.slab_seg[i]];
+    const uint64_t rows = (uint64_t)c->hkv * g.slab_cap;
+    if ((e = get_map(g.k_slab, rows, fp8, box_inner, box_rows, &maps[i + 1].k))) return e;
+    if ((e = get_map(g.v_slab, rows, fp8, box_inner, box_rows, &maps[i + 1].v))) return e;
+  }
+  nsrc = 1 + ss.nslab;
+  return TFPA_OK;
+}
+
+void fill_run(RunInfo& ri, const tfpa_seg& g, int src, int row0, int nrows, int pos0) {
+  ri.page_table = g.page_table;
+  ri.src = src;
+  ri.seq_len = g.seq_len;
+  ri.row0 = row0;
+  ri.nrows = nrows;
+  ri.pos0 = pos0;
+  ri.nsplit = tfpa_num_splits(g.seq_len);
+  ri.pps = tfpa_pages_per_split(g.seq_len);
+  ri.item0 = 0;
+  ri.slab_cap = g.page_table ? 0 : g.slab_cap;
+  ri.pad_ = 0;
+}
+
+// Partial (and optionally merge) launches over the call's rows.  With
+// `sliced`, each launch's partials start at scratch row 0 and are merged
+// before the next launch; otherwise partials land at the call's own row and
+// no merge runs.
+int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const void* q,
+                const int32_t* row_seg, const int32_t* row_pos, int32_t rows, float scale,
+                const tfpa_scratch* sc, void* out, float* lse, cudaStream_t stream, bool sliced) {
+  int e;
+  if ((e = check_cache(c)) || (e = check_segs(c, segs, nseg))) return e;
+  if (!sc || !sc->part_o || !sc->part_ml || sc->cap_rows < 1 || sc->max_splits < 1)
+    return TFPA_EINVAL;
+  if (rows > 0 && (!q || !aligned(q, 16))) return TFPA_EINVAL;
+  if (sliced && rows > 0 && (!out || !aligned(out, 8))) return TFPA_EINVAL;
+  if (!std::isfinite(scale)) return TFPA_EINVAL;
+  if (!sliced && rows > sc->cap_rows) return TFPA_ECAPACITY;
+  std::vector<Run> runs;
+  if ((e = build_runs(segs, nseg, row_seg, row_pos, rows, runs))) return e;
+  for (const Run& r : runs)
+    if (tfpa_num_splits(segs[r.seg].seq_len) > sc->max_splits) return TFPA_ECAPACITY;
+  if (rows == 0) return TFPA_OK;
+  if ((e = check_device())) return e;
+  const bool fp8 = c->dtype == TFPA_FP8_E4M3;
+  const int G = c->hq / c->hkv;
+  const int nsm = sm_count();
+  if (nsm < 1) return TFPA_ECUDA;
+  const size_t hd = (size_t)c->hq * kHeadDim;
+
+  size_t ri = 0;
+  int32_t taken = 0;  // rows of runs[ri] already launched
+  static DecodeParams p;  // large; built under the lock below
+  static MergeParams mp;
+  std::lock_guard<std::mutex> lock(g_mu);
+  while (ri < runs.size()) {
+    std::memset(&p, 0, sizeof(p));
+    SourceSet ss;
+    const int32_t base = runs[ri].row0 + taken;  // first call row of this launch
+    int32_t nrows = 0, items = 0;
+    int nr = 0;
+    while (ri < runs.size() && nr < kMaxRuns && nrows < sc->cap_rows) {
+      const Run& r = runs[ri];
+      const int src = ss.add(segs, r.seg);
+      if (src < 0) break;
+      const int32_t take = std::min(r.nrows - taken, sc->cap_rows - nrows);
+      RunInfo& info = p.runs[nr];
+      fill_run(info, segs[r.seg], src, nrows, take, r.pos0 + taken);
+      info.item0 = items;
+      items += c->hkv * ((take * G + 15) / 16) * info.nsplit;
+      mp.runs[nr] = MergeRun{nrows, take, info.nsplit, 0};
+      ++nr;
+      nrows += take;
+      taken += take;
+      if (taken == r.nrows) {
+        ++ri;
+        taken = 0;
+      }
+    }
+    if ((e = fill_maps(c, segs, ss, fp8, fp8 ? 128 : 64, fp8 ? 256 : 128, p.maps, p.nsrc)))
+      return e;
+    const int32_t srow = sliced ? 0 : base;  // scratch row of this launch's first row
+    const size_t srow_elems = (size_t)srow * c->hq * sc->max_splits;
+    p.q = static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd;
+    p.part_o = sc->part_o + srow_elems * kHeadDim;
+    p.part_ml = sc->part_ml + srow_elems * 2;
+    p.k_scale = c->k_scale;
+    p.v_scale = c->v_scale;
+    p.err_flag = c->err_flag;
+    p.nruns = nr;
+    p.n_items = items;
+    p.hq = c->hq;
+    p.hkv = c->hkv;
+    p.group = G;
+    p.max_splits = sc->max_splits;
+    p.num_pages = c->num_pages;
+    p.rows = nrows;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const int grid = std::min(items, nsm);
+    record(1, base, nrows, nr, items, grid, (int64_t)base * hd, 0);
+    if (!dry_run()) {
+      if ((e = to_err(launch_decode_partial(p, fp8, grid, stream)))) return e;
+    }
+    if (sliced) {
+      mp.part_o = p.part_o;
+      mp.part_ml = p.part_ml;
+      mp.out = static_cast<__nv_bfloat16*>(out) + (size_t)base * hd;
+      mp.lse = lse ? lse + (size_t)base * c->hq : nullptr;
+      mp.nruns = nr;
+      mp.rows = nrows;
+      mp.hq = c->hq;
+      mp.max_splits = sc->max_splits;
+      record(2, base, nrows, nr, nrows * c->hq, (nrows * c->hq + 7) / 8, 0, (int64_t)base * hd);
+      if (!dry_run()) {
+        if ((e = to_err(launch_merge(mp, stream)))) return e;
+      }
+    }
+  }
+  return TFPA_OK;
+}
+
+}  // namespace
+
+extern "C" int tfpa_decode_partial(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                                   const void* q, const int32_t* row_seg, const int32_t* row_pos,
+                                   int32_t rows, float softmax_scale, const tfpa_scratch* scratch,
+                                   cudaStream_t stream) {
+  return decode_impl(cache, segs, nseg, q, row_seg, row_pos, rows, softmax_scale, scratch,
+                     nullptr, nullptr, stream, false);
+}
+
+extern "C" int tfpa_decode(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                           const void* q, const int32_t* row_seg, const int32_t* row_pos,
+                           int32_t rows, float softmax_scale, const tfpa_scratch* scratch,
+                           void* out, float* lse, cudaStream_t stream) {
+  return decode_impl(cache, segs, nseg, q, row_seg, row_pos, rows, softmax_scale, scratch, out,
+                     lse, stream, true);
+}
+
+extern "C" int tfpa_merge(const tfpa_scratch* sc, int32_t hq, int32_t rows,
+                          const int32_t* nsplit, void* out, float* lse, cudaStream_t stream) {
+  if (!sc || !sc->part_o || !sc->part_ml || hq < 1 || rows < 0) return TFPA_EINVAL;
+  if (rows > sc->cap_rows) return TFPA_ECAPACITY;
+  if (rows == 0) return TFPA_OK;
+  if (!nsplit || !out || !aligned(out, 8)) return TFPA_EINVAL;
+  for (int32_t r = 0; r < rows; ++r)
+    if (nsplit[r] < 1 || nsplit[r] > std::min(sc->max_splits, kMaxSplits)) return TFPA_ECAPACITY;
+  int e;
+  if ((e = check_device())) return e;
+  std::lock_guard<std::mutex> lock(g_mu);
+  static MergeParams mp;
+  int32_t r = 0;
+  while (r < rows) {
+    std::memset(&mp, 0, sizeof(mp));
+    const int32_t base = r;
+    int nr = 0;
+    while (r < rows && nr < (int)(sizeof(mp.runs) / sizeof(mp.runs[0]))) {
+      int32_t n = 1;
+      while (r + n < rows && nsplit[r + n] == nsplit[r]) ++n;
+      mp.runs[nr++] = MergeRun{r - base, n, nsplit[r], 0};
+      r += n;
+    }
+    const size_t srow = (size_t)base * hq * sc->max_splits;
+    mp.part_o = sc->part_o + srow * kHeadDim;
+    mp.part_ml = sc->part_ml + srow * 2;
+    mp.out = static_cast<__nv_bfloat16*>(out) + (size_t)base * hq * kHeadDim;
+    mp.lse = lse ? lse + (size_t)base * hq : nullptr;
+    mp.nruns = nr;
+    mp.rows = r - base;
+    mp.hq = hq;
+    mp.max_splits = sc->max_splits;
+    record(2, base, r - base, nr, (r - base) * hq, ((r - base) * hq + 7) / 8, 0,
+           (int64_t)base * hq * kHeadDim);
+    if (!dry_run())
+      if ((e = to_err(launch_merge(mp, stream)))) return e;
+  }
+  return TFPA_OK;
+}
+
+extern "C" int tfpa_write_kv(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg,
+                             const void* k_rows, const void* v_rows, const int32_t* row_seg,
+                             const int32_t* row_pos, int32_t rows, cudaStream_t stream) {
+  int e;
+  if ((e = check_cache(c)) || (e = check_segs(c, segs, nseg))) return e;
+  if (rows > 0 && (!k_rows || !v_rows || !aligned(k_rows, 16) || !aligned(v_rows, 16)))
+    return TFPA_EINVAL;
+  std::vector<Run> runs;
+  if ((e = build_runs(segs, nseg, row_seg, row_pos, rows, runs))) return e;
+  if (rows == 0) return TFPA_OK;
+  if ((e = check_device())) return e;
+  const size_t rd = (size_t)c->hkv * kHeadDim;
+  std::lock_guard<std::mutex> lock(g_mu);
+  static WriteParams p;
+  size_t ri = 0;
+  while (ri < runs.size()) {
+    std::memset(&p, 0, sizeof(p));
+    const int32_t base = runs[ri].row0;
+    int nr = 0;
+    int32_t nrows = 0;
+    while (ri < runs.size() && nr < kMaxRuns) {
+      const Run& r = runs[ri++];
+      const tfpa_seg& g = segs[r.seg];
+      WriteRun& w = p.runs[nr++];
+      w.page_table = g.page_table;
+      w.k_dst = g.page_table ? c->k_pool : g.k_slab;
+      w.v_dst = g.page_table ? c->v_pool : g.v_slab;
+      w.row0 = r.row0 - base;
+      w.nrows = r.nrows;
+      w.pos0 = r.pos0;
+      w.slab_cap = g.slab_cap;
+      w.seq_len = g.seq_len;
+      nrows = r.row0 + r.nrows - base;
+    }
+    p.k_rows = static_cast<const __nv_bfloat16*>(k_rows) + (size_t)base * rd;
+    p.v_rows = static_cast<const __nv_bfloat16*>(v_rows) + (size_t)base * rd;
+    p.k_scale = c->k_scale;
+    p.v_scale = c->v_scale;
+    p.err_flag = c->err_flag;
+    p.nruns = nr;
+    p.rows = nrows;
+    p.hkv = c->hkv;
+    p.num_pages = c->num_pages;
+    p.fp8 = c->dtype == TFPA_FP8_E4M3;
+    record(0, base, nrows, nr, nrows * c->hkv, (nrows * c->hkv + 15) / 16, 0, 0);
+    if (!dry_run())
+      if ((e = to_err(launch_write_kv(p, stream)))) return e;
+  }
+  return TFPA_OK;
+}
+
+extern "C" void tfpa_set_launch_hook(tfpa_launch_hook hook, void* user, int dry_run_flag) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_hook.fn = hook;
+  g_hook.user = user;
+  g_hook.dry = hook ? dry_run_flag : 0;
+}
+
+extern "C" const char* tfpa_strerror(int code) {
+  switch (code) {
+    case TFPA_OK: return "ok";
+    case TFPA_EINVAL: return "invalid argument (dims, dtype, null pointer or alignment)";
+    case TFPA_ERANGE: return "segment, position or page id out of range";
+    case TFPA_ECAPACITY: return "scratch capacity exceeded (rows or splits)";
+    case TFPA_ECUDA: return "CUDA call or launch failed";
+    case TFPA_EDEVICE: return "current device is not sm_100-family";
+    default: return "unknown error";
+  }
+}
+
+extern "C" const char* tfpa_version(void) { return "tfpa 0.1 (sm_103a)"; }
+
+// ------------------------------------------------------------ prefill
+namespace {
+constexpr int kPrefillTileRows = 128;
+}
+
+extern "C" int tfpa_prefill(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg,
+                            const void* q, const int32_t* row_seg, const int32_t* row_pos,
+                            int32_t rows, float scale, int32_t max_rows_per_launch, void* out,
+                            float* lse, cudaStream_t stream) {
+  int e;
+  if ((e = check_cache(c)) || (e = check_segs(c, segs, nseg))) return e;
+  if (rows > 0 && (!q || !aligned(q, 16) || !out || !aligned(out, 16))) return TFPA_EINVAL;
+  if (max_rows_per_launch < 0 || !std::isfinite(scale)) return TFPA_EINVAL;
+  std::vector<Run> runs;
+  if ((e = build_runs(segs, nseg, row_seg, row_pos, rows, runs))) return e;
+  if (rows == 0) return TFPA_OK;
+  if ((e = check_device())) return e;
+  const bool fp8 = c->dtype == TFPA_FP8_E4M3;
+  const int G = c->hq / c->hkv;
+  const int npairs = (G + 1) / 2;
+  const int32_t cap = max_rows_per_launch > 0 ? max_rows_per_launch : INT32_MAX;
+  const int nsm = sm_count();
+  if (nsm < 1) return TFPA_ECUDA;
+  const size_t hd = (size_t)c->hq * kHeadDim;
+  std::lock_guard<std::mutex> lock(g_mu);
+  static PrefillParams p;
+  size_t ri = 0;
+  int32_t taken = 0;
+  while (ri < runs.size()) {
+    std::memset(&p, 0, sizeof(p));
+    SourceSet ss;
+    const int32_t base = runs[ri].row0 + taken;
+    int32_t nrows = 0, tiles = 0;
+    int nr = 0;
+    while (ri < runs.size() && nr < kMaxRuns && nrows < cap) {
+      const Run& r = runs[ri];
+      const int src = ss.add(segs, r.seg);
+      if (src < 0) break;
+      const int32_t take = std::min(r.nrows - taken, cap - nrows);
+      RunInfo& info = p.runs[nr++];
+      fill_run(info, segs[r.seg], src, nrows, take, r.pos0 + taken);
+      info.item0 = tiles;
+      tiles += c->hkv * npairs * ((take + kPrefillTileRows - 1) / kPrefillTileRows);
+      nrows += take;
+      taken += take;
+      if (taken == r.nrows) {
+        ++ri;
+        taken = 0;
+      }
+    }
+    if ((e = fill_maps(c, segs, ss, fp8, fp8 ? 128 : 64, 128, p.maps, p.nsrc))) return e;
+    p.q = static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd;
+    p.out = static_cast<__nv_bfloat16*>(out) + (size_t)base * hd;
+    p.lse = lse ? lse + (size_t)base * c->hq : nullptr;
+    p.k_scale = c->k_scale;
+    p.v_scale = c->v_scale;
+    p.err_flag = c->err_flag;
+    p.nruns = nr;
+    p.n_tiles = tiles;
+    p.hq = c->hq;
+    p.hkv = c->hkv;
+    p.group = G;
+    p.num_pages = c->num_pages;
+    p.rows = nrows;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const int grid = std::min(tiles, nsm);
+    record(3, base, nrows, nr, tiles, grid, (int64_t)base * hd, (int64_t)base * hd);
+    if (!dry_run())
+      if ((e = to_err(launch_prefill(p, fp8, grid, stream)))) return e;
+  }
+  return TFPA_OK;
+}

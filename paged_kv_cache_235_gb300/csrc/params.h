@@ -1,0 +1,132 @@
+// Kernel launch parameters shared by the host planner and the kernels.
+//
+// A call's rows are grouped into runs: consecutive rows of one segment at
+// consecutive positions.  Everything a kernel needs about a run travels in
+// the launch parameters (passed by value, so a launch captured in a graph
+// keeps them); only the bulk data (pages, tables, q, out, scratch) is in
+// device memory.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace tfpa {
+
+constexpr int kPage = 256;          // positions per page
+constexpr int kHeadDim = 128;       // head size
+constexpr int kMaxSplits = 32;      // split-K partials per (row, head), at most
+constexpr int kMaxRuns = 64;        // runs per launch
+constexpr int kMaxSlabs = 15;       // slab streams per launch (+1 source for the pool)
+constexpr int kMaxSources = kMaxSlabs + 1;
+
+// TMA descriptors of one K/V source: the page pool (source 0) or a slab.
+struct KVMaps {
+  CUtensorMap k;
+  CUtensorMap v;
+};
+
+struct RunInfo {
+  const int32_t* page_table;  // device; nullptr => slab source
+  int32_t src;                // index into maps[]
+  int32_t seq_len;
+  int32_t row0;               // first row, relative to this launch
+  int32_t nrows;
+  int32_t pos0;               // position of the first row
+  int32_t nsplit;             // decode: splits of this stream
+  int32_t pps;                // decode: pages per split
+  int32_t item0;              // first work item of this run
+  int32_t slab_cap;           // slab capacity in positions (slab runs)
+  int32_t pad_;
+};
+
+struct DecodeParams {
+  KVMaps maps[kMaxSources];
+  RunInfo runs[kMaxRuns];
+  const __nv_bfloat16* q;     // rows of this launch: [rows][hq][128]
+  float* part_o;              // [cap_rows][hq][max_splits][128]
+  float* part_ml;             // [cap_rows][hq][max_splits][2]
+  const float* k_scale;       // fp8: [hkv]
+  const float* v_scale;
+  int32_t* err_flag;
+  int32_t nruns;
+  int32_t nsrc;
+  int32_t n_items;
+  int32_t hq, hkv, group;     // group = hq / hkv
+  int32_t max_splits;
+  int32_t num_pages;
+  int32_t rows;
+  float scale_log2;           // softmax_scale * log2(e)
+};
+
+struct MergeRun {
+  int32_t row0;
+  int32_t nrows;
+  int32_t nsplit;
+  int32_t pad_;
+};
+
+struct MergeParams {
+  MergeRun runs[kMaxRuns * 2];
+  const float* part_o;
+  const float* part_ml;
+  __nv_bfloat16* out;         // rows of this launch: [rows][hq][128]
+  float* lse;                 // [rows][hq] or nullptr
+  int32_t nruns;
+  int32_t rows;
+  int32_t hq;
+  int32_t max_splits;
+};
+
+struct WriteRun {
+  const int32_t* page_table;  // nullptr => slab
+  void* k_dst;                // pool base or slab base
+  void* v_dst;
+  int32_t row0;               // first row of the run, relative to this launch
+  int32_t nrows;
+  int32_t pos0;
+  int32_t slab_cap;
+  int32_t seq_len;
+  int32_t pad_;
+};
+
+struct WriteParams {
+  WriteRun runs[kMaxRuns];
+  const __nv_bfloat16* k_rows;  // [rows][hkv][128], rows of this launch
+  const __nv_bfloat16* v_rows;
+  const float* k_scale;
+  const float* v_scale;
+  int32_t* err_flag;
+  int32_t nruns;
+  int32_t rows;
+  int32_t hkv;
+  int32_t num_pages;
+  int32_t fp8;
+};
+
+// Prefill: one work tile = (run, kv head g, query-head pair, 128 rows).
+struct PrefillParams {
+  KVMaps maps[kMaxSources];
+  RunInfo runs[kMaxRuns];     // item0 = first tile of the run
+  const __nv_bfloat16* q;     // [rows][hq][128]
+  __nv_bfloat16* out;
+  float* lse;
+  const float* k_scale;
+  const float* v_scale;
+  int32_t* err_flag;
+  int32_t nruns;
+  int32_t nsrc;
+  int32_t n_tiles;
+  int32_t hq, hkv, group;
+  int32_t num_pages;
+  int32_t rows;
+  float scale_log2;
+};
+
+// Launchers (defined next to their kernels).
+cudaError_t launch_write_kv(const WriteParams& p, cudaStream_t s);
+cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cudaStream_t s);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillParams& p, bool fp8, int grid, cudaStream_t s);
+
+}  // namespace tfpa

@@ -36,9 +36,9 @@ def randn_bf16_bits(shape, seed: int) -> np.ndarray:
 
 def random_fp8_codes(shape, seed: int) -> np.ndarray:
     """Random e4m3 codes with the two NaN codes (0x7F, 0xFF) avoided."""
-    c = torch.randint(0, 254, tuple(shape), generator=_gen(seed), dtype=torch.int32)
-    c = c + (c >= 0x7F).to(torch.int32)   # skip 0x7F; 254 values -> 0..0xFE
-    return c.numpy().astype(np.uint8)
+    c = torch.randint(0, 254, tuple(shape), generator=_gen(seed), dtype=torch.uint8)
+    c += (c >= 0x7F).to(torch.uint8)      # skip 0x7F; 254 values -> 0..0xFE
+    return c.numpy()
 
 
 @dataclass

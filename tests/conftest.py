@@ -16,3 +16,12 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def tfpa_library():
+    """Builds libtfpa.so if it is missing (nvcc cross-compiles without a GPU)."""
+    from paged_kv_cache_235_gb300 import binding, build
+    if not os.path.exists(binding.LIB_PATH):
+        build.build()
+    return binding.lib()

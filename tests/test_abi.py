@@ -1,0 +1,147 @@
+"""Host-side tests of the C ABI (no GPU): exports, the split policy, the slice
+loop (recorded in dry-run mode, as the pages' launch-recording host test did)
+and argument checking."""
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+from paged_kv_cache_235_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+FAKE = 1 << 20   # a 1 MiB-aligned fake device address; dry runs never touch it
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "tfpa.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"\b(tfpa_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared()
+    assert "tfpa_decode" in names and "tfpa_prefill" in names
+    L = B.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(B.EXPORTS)
+
+
+def test_split_policy_depends_on_length_only():
+    for L, pps, ns in [(1, 1, 1), (256, 1, 1), (257, 1, 2), (1000, 1, 4), (8192, 1, 32),
+                       (8193, 2, 17), (65536, 8, 32), (262144, 32, 32), (109000, 14, 31)]:
+        assert B.tfpa_pages_per_split(L) == pps, L
+        assert B.tfpa_num_splits(L) == ns, L
+    for L in range(1, 300000, 997):
+        n = B.tfpa_num_splits(L)
+        assert 1 <= n <= B.MAX_SPLITS
+        assert (n - 1) * B.tfpa_pages_per_split(L) * 256 < L <= n * B.tfpa_pages_per_split(L) * 256
+
+
+def _cache(hq=32, hkv=8, dtype="bf16"):
+    return B.Cache(dtype, hq, hkv, FAKE, 2 * FAKE, FAKE if dtype == "fp8" else None,
+                   FAKE if dtype == "fp8" else None, None, 4096)
+
+
+@pytest.mark.parametrize("rows", [1, 127, 128, 129, 255, 256, 257, 4096])
+def test_decode_slices_of_at_most_cap_rows(rows):
+    c = _cache()
+    segs = [B.Seg(rows + 40000, page_table=3 * FAKE)]
+    with B.record_launches() as rec:
+        B.tfpa_decode(c, segs, 4 * FAKE, np.zeros(rows), np.arange(40000, 40000 + rows), 0.088,
+                      B.Scratch(5 * FAKE, 6 * FAKE, 128), 7 * FAKE)
+    parts = [r for r in rec if r["kind"] == "partial"]
+    merges = [r for r in rec if r["kind"] == "merge"]
+    n = (rows + 127) // 128
+    assert len(parts) == len(merges) == n
+    assert [r["kind"] for r in rec] == ["partial", "merge"] * n      # pairs, in order
+    assert [r["row0"] for r in parts] == [128 * i for i in range(n)]
+    assert sum(r["rows"] for r in merges) == rows                    # every row merged once
+    hd = 32 * 128
+    assert [r["q_offset"] for r in parts] == [128 * i * hd for i in range(n)]
+    assert [r["out_offset"] for r in merges] == [128 * i * hd for i in range(n)]
+
+
+def test_257_row_chunk_issues_three_pairs():
+    c = _cache()
+    segs = [B.Seg(32768, page_table=3 * FAKE)]
+    with B.record_launches() as rec:
+        B.tfpa_decode(c, segs, 4 * FAKE, np.zeros(257), np.arange(28672, 28929), 0.088,
+                      B.Scratch(5 * FAKE, 6 * FAKE, 128), 7 * FAKE)
+    assert [(r["kind"], r["row0"], r["rows"]) for r in rec] == [
+        ("partial", 0, 128), ("merge", 0, 128), ("partial", 128, 128), ("merge", 128, 128),
+        ("partial", 256, 1), ("merge", 256, 1)]
+
+
+def test_mixed_paged_and_slab_streams_cross_slices():
+    c = _cache()
+    segs = [B.Seg(700, k_slab=8 * FAKE, v_slab=9 * FAKE, slab_cap=768),
+            B.Seg(300, page_table=3 * FAKE)]
+    rs = np.array([0] * 100 + [1] * 100)
+    rp = np.concatenate([np.arange(600, 700), np.arange(200, 300)])
+    with B.record_launches() as rec:
+        B.tfpa_decode(c, segs, 4 * FAKE, rs, rp, 0.088, B.Scratch(5 * FAKE, 6 * FAKE, 128),
+                      7 * FAKE)
+    parts = [r for r in rec if r["kind"] == "partial"]
+    assert [(r["row0"], r["rows"], r["runs"]) for r in parts] == [(0, 128, 2), (128, 72, 1)]
+
+
+def test_prefill_slices():
+    c = _cache()
+    segs = [B.Seg(28672 + 257, page_table=3 * FAKE)]
+    with B.record_launches() as rec:
+        B.tfpa_prefill(c, segs, 4 * FAKE, np.zeros(257), np.arange(28672, 28929), 0.088,
+                       7 * FAKE, max_rows_per_launch=128)
+    assert [(r["kind"], r["row0"], r["rows"]) for r in rec] == [
+        ("prefill", 0, 128), ("prefill", 128, 128), ("prefill", 256, 1)]
+    # tiles: kv heads x head pairs x 128-row tiles
+    assert [r["items"] for r in rec] == [8 * 2 * 1] * 3
+    with B.record_launches() as rec:
+        B.tfpa_prefill(c, segs, 4 * FAKE, np.zeros(257), np.arange(28672, 28929), 0.088,
+                       7 * FAKE)
+    assert [(r["kind"], r["rows"], r["items"]) for r in rec] == [("prefill", 257, 8 * 2 * 3)]
+
+
+def test_write_kv_one_launch_per_64_runs():
+    c = _cache()
+    segs = [B.Seg(1000, page_table=3 * FAKE) for _ in range(100)]
+    with B.record_launches() as rec:
+        B.tfpa_write_kv(c, segs, 4 * FAKE, 5 * FAKE, np.arange(100), np.full(100, 999))
+    assert [(r["kind"], r["rows"]) for r in rec] == [("write_kv", 64), ("write_kv", 36)]
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(hq=30, hkv=8), B.TFPA_EINVAL),
+    (dict(pos=1000), B.TFPA_ERANGE),
+    (dict(pos=-1), B.TFPA_ERANGE),
+    (dict(seg=1), B.TFPA_ERANGE),
+    (dict(max_splits=3), B.TFPA_ECAPACITY),
+    (dict(page=5000), B.TFPA_ERANGE),
+    (dict(q=FAKE + 2), B.TFPA_EINVAL),
+    (dict(slab_cap=1000), B.TFPA_EINVAL),
+])
+def test_argument_errors(bad, code):
+    c = _cache(hq=bad.get("hq", 32), hkv=bad.get("hkv", 8))
+    table = np.arange(4, dtype=np.int32)
+    if "page" in bad:
+        table[2] = bad["page"]
+    segs = [B.Seg(1000, page_table=3 * FAKE, page_table_host=table)]
+    if "slab_cap" in bad:
+        segs = [B.Seg(1000, k_slab=FAKE, v_slab=FAKE, slab_cap=bad["slab_cap"])]
+    with B.record_launches() as rec:
+        with pytest.raises(B.TfpaError) as e:
+            B.tfpa_decode(c, segs, bad.get("q", 4 * FAKE), [bad.get("seg", 0)],
+                          [bad.get("pos", 999)], 0.088,
+                          B.Scratch(5 * FAKE, 6 * FAKE, 128, bad.get("max_splits", 32)), 7 * FAKE)
+    assert e.value.code == code
+    assert rec == []                 # nothing enqueued on error
+
+
+def test_merge_rejects_rows_beyond_capacity():
+    with B.record_launches():
+        with pytest.raises(B.TfpaError) as e:
+            B.tfpa_merge(B.Scratch(5 * FAKE, 6 * FAKE, 128), 32, np.ones(129), 7 * FAKE)
+    assert e.value.code == B.TFPA_ECAPACITY
