@@ -10,7 +10,7 @@
 namespace tfpa {
 
 // Error bits a kernel may OR into the caller's err_flag.
-constexpr int kErrBadPage = 1;     // page id outside [0, num_pages): read as zeros
+constexpr int kErrBadPage = 1;     // page id outside [0, num_pages): its keys are masked
 constexpr int kErrTimeout = 2;     // a wait gave up (a bug; the kernel returned early)
 
 // Longest a wait may spin before the kernel gives up (ns of %globaltimer).
@@ -71,6 +71,37 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
     }
   }
   return true;
+}
+
+// As mbar_wait, but also gives up at once when *abort is set, and sets it on
+// a timeout, so that every role of a CTA leaves its loop promptly.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, int32_t* err,
+                                                   volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t n = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++n & 63u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        flag_error(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// 3D tiled load (x innermost).
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
+        "r"(smem_u32(bar))
+      : "memory");
 }
 
 // ---------------------------------------------------------------- TMA

@@ -107,6 +107,7 @@ struct WriteParams {
 // Prefill: one work tile = (run, kv head g, query-head pair, 128 rows).
 struct PrefillParams {
   KVMaps maps[kMaxSources];
+  CUtensorMap qmap;           // q as 3D [rows][hq][128], box 64 x 1 x 128, 128B swizzle
   RunInfo runs[kMaxRuns];     // item0 = first tile of the run
   const __nv_bfloat16* q;     // [rows][hq][128]
   __nv_bfloat16* out;
