@@ -34,8 +34,9 @@
  *
  * Errors.  Every call returns TFPA_OK (0) or a negative code below and
  * enqueues nothing on error.  Kernels never trap: a page id outside
- * [0, num_pages) found on the device is read as zeros and sets bit 1 of
- * cache->err_flag (if non-NULL).
+ * [0, num_pages) found on the device is skipped (its keys take no part in
+ * attention; the KV write skips its rows) and sets bit 1 of cache->err_flag
+ * (if non-NULL); a wait inside a kernel that gives up sets bit 2.
  */
 #ifndef TFPA_H
 #define TFPA_H
@@ -133,6 +134,37 @@ int tfpa_decode(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
                 const void* q, const int32_t* row_seg, const int32_t* row_pos,
                 int32_t rows, float softmax_scale, const tfpa_scratch* scratch,
                 void* out, float* lse, cudaStream_t stream);
+
+/* Decode/verify attention for callers that cannot allocate device memory.
+ *
+ * Some callers cannot call cudaMalloc: code that runs inside another
+ * framework's memory manager, a plug-in that may not grow its host process's
+ * device footprint, or a runtime whose allocations are all made before it
+ * starts serving.  This entry point needs no caller scratch: the split-K
+ * partials live in one array compiled into the library (a file-scope
+ * __device__ array of TFPA_STATIC_SCRATCH_SLOTS slots of 130 floats, about
+ * 4.3 MB), which every device that loads the library holds until the process
+ * exits.  The paper has no counterpart to this entry point.
+ *
+ * Same arguments and result as tfpa_decode without `scratch`; rows are
+ * processed in slices of TFPA_STATIC_SCRATCH_SLOTS / (hq * TFPA_MAX_SPLITS)
+ * rows (8 at hq = 32), which gives the same bytes as tfpa_decode.  Head
+ * counts with hq * TFPA_MAX_SPLITS > TFPA_STATIC_SCRATCH_SLOTS (hq > 256) are
+ * refused with TFPA_ECAPACITY.  It allocates no device memory and calls no
+ * allocating CUDA or library routine.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.  Every call shares the one array and it
+ * keeps the last call's contents; nothing in it needs to start at zero, as
+ * every slot the merge reads is written by the partial kernel of the same
+ * call.  Calls that overlap on the GPU (other streams, other host threads)
+ * race on the array: serialise them. */
+#define TFPA_STATIC_SCRATCH_SLOTS 8192
+int tfpa_decode_static(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                       const void* q, const int32_t* row_seg, const int32_t* row_pos,
+                       int32_t rows, float softmax_scale, void* out, float* lse,
+                       cudaStream_t stream);
 
 /* Causal prompt-chunk attention over the paged prefix, one pass with online
  * softmax on tcgen05/TMEM tiles (PR #2011, "hpattn_p256_kernel": page size a

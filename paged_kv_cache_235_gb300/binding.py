@@ -26,7 +26,7 @@ TFPA_OK, TFPA_EINVAL, TFPA_ERANGE, TFPA_ECAPACITY, TFPA_ECUDA, TFPA_EDEVICE = 0,
 
 EXPORTS = ("tfpa_pages_per_split", "tfpa_num_splits", "tfpa_write_kv", "tfpa_decode_partial",
            "tfpa_merge", "tfpa_decode", "tfpa_prefill", "tfpa_set_launch_hook",
-           "tfpa_strerror", "tfpa_version")
+           "tfpa_strerror", "tfpa_version", "tfpa_decode_static")
 
 
 class TfpaError(RuntimeError):
@@ -89,6 +89,9 @@ def lib():
         L.tfpa_decode.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, i32,
                                   ctypes.c_float, P(tfpa_scratch), vp, vp, vp]
         L.tfpa_decode.restype = ctypes.c_int
+        L.tfpa_decode_static.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, i32,
+                                         ctypes.c_float, vp, vp, vp]
+        L.tfpa_decode_static.restype = ctypes.c_int
         L.tfpa_prefill.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, i32,
                                    ctypes.c_float, i32, vp, vp, vp]
         L.tfpa_prefill.restype = ctypes.c_int
@@ -238,6 +241,18 @@ def tfpa_decode(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, softmax_
     _check(lib().tfpa_decode(ctypes.byref(cc), cs, n, _ptr(q), _ptr(rs), _ptr(rp), len(rs),
                              float(softmax_scale), ctypes.byref(sc), _ptr(out), _ptr(lse),
                              _stream(stream)), "tfpa_decode")
+
+
+def tfpa_decode_static(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, softmax_scale,
+                       out, lse=None, stream=None) -> None:
+    """Decode without caller scratch: the partials live in an array compiled
+    into the library, for callers that cannot allocate device memory."""
+    cs, n = _segs(segs)
+    rs, rp = _i32(row_seg), _i32(row_pos)
+    cc = cache.c()
+    _check(lib().tfpa_decode_static(ctypes.byref(cc), cs, n, _ptr(q), _ptr(rs), _ptr(rp),
+                                    len(rs), float(softmax_scale), _ptr(out), _ptr(lse),
+                                    _stream(stream)), "tfpa_decode_static")
 
 
 def tfpa_prefill(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, softmax_scale, out,
