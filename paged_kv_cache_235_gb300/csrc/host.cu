@@ -128,6 +128,25 @@ int get_map(const void* ptr, uint64_t rows, bool fp8, int box_inner, int box_row
   return TFPA_OK;
 }
 
+// q of one launch as a 3D tensor [rows][hq][128] bf16, box 64 x 1 x 128 rows
+// (one head's 128-row tile, half the head dim), 128B swizzle.
+int get_qmap(const void* q, int hq, int rows, CUtensorMap* out) {
+  if (dry_run()) {
+    std::memset(out, 0, sizeof(*out));
+    return TFPA_OK;
+  }
+  auto fn = encode_fn();
+  if (!fn) return TFPA_ECUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hq, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)hq * kHeadDim * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TFPA_OK : TFPA_ECUDA;
+}
+
 // ------------------------------------------------------------ validation
 int32_t pages_of(int32_t L) { return (L + kPage - 1) / kPage; }
 
@@ -501,6 +520,7 @@ extern "C" int tfpa_prefill(const tfpa_cache* c, const tfpa_seg* segs, int32_t n
   if ((e = check_cache(c)) || (e = check_segs(c, segs, nseg))) return e;
   if (rows > 0 && (!q || !aligned(q, 16) || !out || !aligned(out, 16))) return TFPA_EINVAL;
   if (max_rows_per_launch < 0 || !std::isfinite(scale)) return TFPA_EINVAL;
+  if (c->dtype != TFPA_BF16) return TFPA_EINVAL;   // e4m3 prompt tiles: not built yet
   std::vector<Run> runs;
   if ((e = build_runs(segs, nseg, row_seg, row_pos, rows, runs))) return e;
   if (rows == 0) return TFPA_OK;
@@ -539,6 +559,9 @@ extern "C" int tfpa_prefill(const tfpa_cache* c, const tfpa_seg* segs, int32_t n
       }
     }
     if ((e = fill_maps(c, segs, ss, fp8, fp8 ? 128 : 64, 128, p.maps, p.nsrc))) return e;
+    if ((e = get_qmap(static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd, c->hq, nrows,
+                      &p.qmap)))
+      return e;
     p.q = static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd;
     p.out = static_cast<__nv_bfloat16*>(out) + (size_t)base * hd;
     p.lse = lse ? lse + (size_t)base * c->hq : nullptr;
@@ -553,7 +576,7 @@ extern "C" int tfpa_prefill(const tfpa_cache* c, const tfpa_seg* segs, int32_t n
     p.num_pages = c->num_pages;
     p.rows = nrows;
     p.scale_log2 = scale * 1.4426950408889634f;
-    const int grid = std::min(tiles, nsm);
+    const int grid = tiles;   // one CTA per tile, heaviest tiles first
     record(3, base, nrows, nr, tiles, grid, (int64_t)base * hd, (int64_t)base * hd);
     if (!dry_run())
       if ((e = to_err(launch_prefill(p, fp8, grid, stream)))) return e;
