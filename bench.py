@@ -296,6 +296,24 @@ def time_prefill(w, torch, B, reps):
     return statistics.median(times)
 
 
+def profile_case(args, torch, B, wl):
+    """One workload's kernels only, for profiler captures (a small launch list)."""
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    if args.case == "prefill":
+        w = wl.prompt_chunk()
+        ms = time_prefill(w, torch, B, args.steps)
+        print(f"prefill: {ms:.4f} ms, {prefill_flops(w) / ms / 1e9:.1f} TFLOP/s")
+        return
+    w = wl.batched_decode() if args.case == "decode" else wl.fp8_verify()
+    cache, segs, q = device_case(w, torch, B)
+    sc = B.make_scratch(min(128, w.rows), w.hq)
+    out = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16, device="cuda")
+    for _ in range(args.warmup + args.steps):
+        B.tfpa_decode(cache, segs, q, w.row_seg, w.row_pos, w.softmax_scale, sc, out)
+    torch.cuda.synchronize()
+    print(f"{args.case}: {args.warmup + args.steps} decode calls done")
+
+
 # --------------------------------------------------------------------- main
 def reference_arm(args):
     """The CPU oracle as the reference arm: same metric, config and unit."""
@@ -338,6 +356,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--case", default=None, choices=["decode", "fp8_verify", "prefill"],
+                    help="profiling mode: run only this workload's kernels --steps times "
+                         "after --warmup, print its timing, no JSON line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -347,6 +368,10 @@ def main():
     import torch
     from paged_kv_cache_235_gb300 import binding as B
     from paged_kv_cache_235_gb300 import workloads as wl
+
+    if args.case:
+        profile_case(args, torch, B, wl)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
