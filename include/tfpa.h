@@ -97,7 +97,7 @@ typedef struct {
 } tfpa_scratch;
 
 /* Split policy, a function of a stream's own length only (so a stream's
- * partials never depend on its batch): pages_per_split = max(1,
+ * partials never depend on its batch): pages_per_split = max(2,
  * ceil(npages / 32)), nsplit = ceil(npages / pages_per_split). */
 int32_t tfpa_pages_per_split(int32_t seq_len);
 int32_t tfpa_num_splits(int32_t seq_len);

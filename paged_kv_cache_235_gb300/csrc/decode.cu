@@ -2,18 +2,20 @@
 // (TensorFold Issue #1344, "Mechanism": partial kernels write running max,
 // sum and unnormalised output per split, then attn_merge combines them).
 //
-// Partial kernel: persistent CTAs walk a list of work items
-// (run, kv head g, m-tile of 16 query vectors, split).  A split is a fixed
-// number of whole pages chosen from the stream's own length, so a row's
-// partials never depend on its batch or on how rows are sliced.  Per CTA:
-//   warp 4      producer: looks each page up once (PR #2011, "the decode
+// Partial kernel: persistent CTAs, each taking a contiguous range of work
+// items (run, kv head g, m-tile of 16 query vectors, split).  A split is a
+// fixed number of whole pages chosen from the stream's own length, so a
+// row's partials never depend on its batch or on how rows are sliced.
+// Per CTA:
+//   warp 8      producer: looks each page up once (PR #2011, "the decode
 //               tiles ... look a page up once"), stages K and V chunks into
-//               shared memory with TMA tiled loads (128B swizzle), 3 stages;
-//   warps 0..3  consumers: each takes a quarter of every chunk's keys, runs
+//               shared memory with TMA tiled loads (128B swizzle), 3 stages
+//               of 64 KB;
+//   warps 0..7  consumers: each takes an eighth of every chunk's keys, runs
 //               QK^T and PV on mma.sync m16n8k16 (bf16, or f16 for e4m3
 //               caches, whose bytes convert to f16 exactly) and an online
 //               softmax reduced with warp shuffles; at the end of an item the
-//               four warps' states are combined in a fixed order.
+//               eight warps' states are combined in a fixed order.
 // Paged and slab streams differ only in the TMA row coordinate, so they
 // produce the same bytes (PR #1373, "What changes").
 #include "common.cuh"
@@ -24,12 +26,17 @@ namespace {
 
 constexpr int kStages = 3;
 constexpr int kStageBytes = 65536;    // K 32 KB + V 32 KB
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 8;
+constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kCombRow = 132;         // padded float row of the combine buffer
-constexpr int kCombBytes = kConsumerWarps * 16 * kCombRow * 4;
-constexpr int kSmemBytes = kStages * kStageBytes + kCombBytes + kConsumerWarps * 16 * 2 * 4 +
-                           kStages * 16 + (2 * kStages + 2) * 8 + 1024;
+constexpr int kCombRow = 130;         // padded float row of the combine buffer
+constexpr int kCombWarps = 4;         // the combine buffer holds four warps' O
+constexpr int kCombBytes = kCombWarps * 16 * kCombRow * 4;
+constexpr int kMlBytes = kConsumerWarps * 16 * 2 * 4;
+constexpr int kSmemBytes =
+    kStages * kStageBytes + kCombBytes + kMlBytes + kStages * 4 + (2 * kStages + 2) * 8 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory");
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 template <bool FP8>
 struct Cfg {
@@ -58,6 +65,13 @@ __device__ __forceinline__ Item item_of(const DecodeParams& p, int it) {
   return x;
 }
 
+// Items [begin, end) of this CTA: a contiguous share, so consecutive items
+// are mostly consecutive splits of one (stream, kv head, m-tile).
+__device__ __forceinline__ void cta_items(int n, int& begin, int& end) {
+  begin = (int)(((long long)blockIdx.x * n) / gridDim.x);
+  end = (int)(((long long)(blockIdx.x + 1) * n) / gridDim.x);
+}
+
 // Key range [klo, khi) an item must read: its split's pages, cut at the
 // stream length and at the last position among the m-tile's rows.
 __device__ __forceinline__ void item_keys(const DecodeParams& p, const Item& x, int& klo,
@@ -74,9 +88,11 @@ template <bool FP8>
 __device__ void producer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* full,
                          uint64_t* empty, int* stage_bad) {
   using C = Cfg<FP8>;
-  const int lane = threadIdx.x & 31;
+  if ((threadIdx.x & 31) != 0) return;
+  int ib, ie;
+  cta_items(p.n_items, ib, ie);
   uint32_t stage = 0;
-  for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+  for (int it = ib; it < ie; ++it) {
     const Item x = item_of(p, it);
     const RunInfo& ru = p.runs[x.run];
     int klo, khi;
@@ -87,40 +103,37 @@ __device__ void producer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
     for (int k0 = klo; k0 < khi; k0 += C::kChunk, ++stage) {
       const int buf = stage % kStages;
       const uint32_t ph = (stage / kStages) & 1;
-      if (lane == 0) {
-        if (!mbar_wait(&empty[buf], ph ^ 1, p.err_flag)) return;
-        const int page = k0 >> 8;
-        int y, bad = 0;
-        if (ru.page_table) {
-          if (page != cached_page) {  // one lookup per page
-            cached_pid = __ldg(ru.page_table + page);
-            cached_page = page;
-          }
-          int pid = cached_pid;
-          if ((unsigned)pid >= (unsigned)p.num_pages) {
-            flag_error(p.err_flag, kErrBadPage);
-            bad = 1;
-            pid = 0;
-          }
-          y = (pid * p.hkv + x.g) * kPage + (k0 & (kPage - 1));
-        } else {
-          y = x.g * ru.slab_cap + k0;
+      const int page = k0 >> 8;
+      int y, bad = 0;
+      if (ru.page_table) {
+        if (page != cached_page) {  // one lookup per page
+          cached_pid = __ldg(ru.page_table + page);
+          cached_page = page;
         }
-        stage_bad[buf] = bad;
-        uint64_t* fb = &full[buf];
-        uint8_t* sb = stage_mem + (size_t)buf * kStageBytes;
-        mbar_arrive_expect_tx(fb, kStageBytes);
-        if (FP8) {
-          tma_load_2d(sb, mk, 0, y, fb);
-          tma_load_2d(sb + 32768, mv, 0, y, fb);
-        } else {
-          tma_load_2d(sb, mk, 0, y, fb);
-          tma_load_2d(sb + 16384, mk, 64, y, fb);
-          tma_load_2d(sb + 32768, mv, 0, y, fb);
-          tma_load_2d(sb + 49152, mv, 64, y, fb);
+        int pid = cached_pid;
+        if ((unsigned)pid >= (unsigned)p.num_pages) {
+          flag_error(p.err_flag, kErrBadPage);
+          bad = 1;
+          pid = 0;
         }
+        y = (pid * p.hkv + x.g) * kPage + (k0 & (kPage - 1));
+      } else {
+        y = x.g * ru.slab_cap + k0;
       }
-      __syncwarp();
+      if (!mbar_wait(&empty[buf], ph ^ 1, p.err_flag)) return;
+      stage_bad[buf] = bad;
+      uint64_t* fb = &full[buf];
+      uint8_t* sb = stage_mem + (size_t)buf * kStageBytes;
+      mbar_arrive_expect_tx(fb, kStageBytes);
+      if (FP8) {
+        tma_load_2d(sb, mk, 0, y, fb);
+        tma_load_2d(sb + 32768, mv, 0, y, fb);
+      } else {
+        tma_load_2d(sb, mk, 0, y, fb);
+        tma_load_2d(sb + 16384, mk, 64, y, fb);
+        tma_load_2d(sb + 32768, mv, 0, y, fb);
+        tma_load_2d(sb + 49152, mv, 64, y, fb);
+      }
     }
   }
 }
@@ -133,13 +146,77 @@ __device__ __forceinline__ int out_col(int nt, int n) {
   return nt < 8 ? 8 * n + nt : 64 + 8 * n + (nt - 8);
 }
 
-// Bounded barrier among the four consumer warps (an mbarrier of count 4).
+// Bounded barrier among the consumer warps (an mbarrier of count 8).
 __device__ __forceinline__ bool consumers_sync(uint64_t* bar, uint32_t& phase, int32_t* err) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
   const bool ok = mbar_wait(bar, phase & 1, err);
   ++phase;
   return ok;
+}
+
+// Query fragments of rows gq and gq+8 of an m-tile, the rows' causal limits
+// and their score multipliers (f16 operands for e4m3 caches: each row is
+// scaled by a power of two into f16 range, exact for every element within
+// 2^28 of the row's largest).
+template <bool FP8>
+__device__ __forceinline__ void load_q(const DecodeParams& p, const RunInfo& ru, const Item& x,
+                                       int gq, int c, uint32_t (&qr)[2][16], int (&lim)[2],
+                                       float (&sc)[2]) {
+  const int nq = ru.nrows * p.group;
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int qv = x.mt * 16 + gq + 8 * hr;
+    uint4 v[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                  make_uint4(0, 0, 0, 0)};
+    lim[hr] = -1;
+    if (qv < nq) {
+      const int r = qv / p.group;
+      const int h = x.g * p.group + (qv - r * p.group);
+      lim[hr] = ru.pos0 + r;
+      const uint4* qp =
+          reinterpret_cast<const uint4*>(p.q + ((size_t)(ru.row0 + r) * p.hq + h) * kHeadDim);
+      if (FP8) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) v[m] = __ldg(qp + 4 * c + m);
+      } else {
+        v[0] = __ldg(qp + 2 * c);
+        v[1] = __ldg(qp + 2 * c + 1);
+        v[2] = __ldg(qp + 8 + 2 * c);
+        v[3] = __ldg(qp + 8 + 2 * c + 1);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      qr[hr][4 * m + 0] = v[m].x;
+      qr[hr][4 * m + 1] = v[m].y;
+      qr[hr][4 * m + 2] = v[m].z;
+      qr[hr][4 * m + 3] = v[m].w;
+    }
+    sc[hr] = p.scale_log2;
+    if (FP8) {
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(qr[hr][j] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(qr[hr][j] & 0xFFFF0000u)));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      int ex;
+      frexpf(amax, &ex);
+      ex = max(min(ex, 120), -100);
+      const float up = __int_as_float((127 + 14 - ex) << 23);
+      const float down = __int_as_float((127 - 14 + ex) << 23);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float lo = __uint_as_float(qr[hr][j] << 16) * up;
+        const float hi = __uint_as_float(qr[hr][j] & 0xFFFF0000u) * up;
+        qr[hr][j] = pack_f16x2(lo, hi);
+      }
+      sc[hr] = p.scale_log2 * down * __ldg(p.k_scale + x.g);
+    }
+  }
 }
 
 template <bool FP8>
@@ -152,74 +229,27 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
   const int gq = lane >> 2, c = lane & 3;
   const uint32_t sbase = smem_u32(stage_mem);
   uint32_t stage = 0, cphase = 0;
+  int ib, ie;
+  cta_items(p.n_items, ib, ie);
+  int q_run = -1, q_g = -1, q_mt = -1;     // the m-tile whose query is loaded
+  int lim[2] = {-1, -1};
+  float sc[2] = {0.f, 0.f};
+  uint32_t qr[2][16];
+  int maxlim = -1;
 
-  for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+  for (int it = ib; it < ie; ++it) {
     const Item x = item_of(p, it);
     const RunInfo& ru = p.runs[x.run];
     int klo, khi;
     item_keys(p, x, klo, khi);
     const int nq = ru.nrows * p.group;
-
-    // ---- query fragments (rows gq and gq+8 of the m-tile)
-    int lim[2];
-    float sc[2];
-    uint32_t qr[2][16];
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int qv = x.mt * 16 + gq + 8 * hr;
-      uint4 v[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                    make_uint4(0, 0, 0, 0)};
-      lim[hr] = -1;
-      if (qv < nq) {
-        const int r = qv / p.group;
-        const int h = x.g * p.group + (qv - r * p.group);
-        lim[hr] = ru.pos0 + r;
-        const uint4* qp = reinterpret_cast<const uint4*>(
-            p.q + ((size_t)(ru.row0 + r) * p.hq + h) * kHeadDim);
-        if (FP8) {
-#pragma unroll
-          for (int m = 0; m < 4; ++m) v[m] = __ldg(qp + 4 * c + m);
-        } else {
-          v[0] = __ldg(qp + 2 * c);
-          v[1] = __ldg(qp + 2 * c + 1);
-          v[2] = __ldg(qp + 8 + 2 * c);
-          v[3] = __ldg(qp + 8 + 2 * c + 1);
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        qr[hr][4 * m + 0] = v[m].x;
-        qr[hr][4 * m + 1] = v[m].y;
-        qr[hr][4 * m + 2] = v[m].z;
-        qr[hr][4 * m + 3] = v[m].w;
-      }
-      sc[hr] = p.scale_log2;
-      if (FP8) {
-        // f16 operands: scale the row by a power of two into f16 range (exact
-        // for every element within 2^28 of the row's largest).
-        float amax = 0.f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          amax = fmaxf(amax, fabsf(__uint_as_float(qr[hr][j] << 16)));
-          amax = fmaxf(amax, fabsf(__uint_as_float(qr[hr][j] & 0xFFFF0000u)));
-        }
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        int ex;
-        frexpf(amax, &ex);
-        ex = max(min(ex, 120), -100);
-        const float up = __int_as_float((127 + 14 - ex) << 23);
-        const float down = __int_as_float((127 - 14 + ex) << 23);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float lo = __uint_as_float(qr[hr][j] << 16) * up;
-          const float hi = __uint_as_float(qr[hr][j] & 0xFFFF0000u) * up;
-          qr[hr][j] = pack_f16x2(lo, hi);
-        }
-        sc[hr] = p.scale_log2 * down * __ldg(p.k_scale + x.g);
-      }
+    if (x.run != q_run || x.g != q_g || x.mt != q_mt) {
+      load_q<FP8>(p, ru, x, gq, c, qr, lim, sc);
+      maxlim = __reduce_max_sync(0xffffffffu, max(lim[0], lim[1]));
+      q_run = x.run;
+      q_g = x.g;
+      q_mt = x.mt;
     }
-    const int maxlim = __reduce_max_sync(0xffffffffu, max(lim[0], lim[1]));
 
     float m_run[2] = {-INFINITY, -INFINITY};
     float l_run[2] = {0.f, 0.f};
@@ -227,14 +257,10 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
-    bool aborted = false;
     for (int k0 = klo; k0 < khi; k0 += C::kChunk, ++stage) {
       const int buf = stage % kStages;
       const uint32_t ph = (stage / kStages) & 1;
-      if (!mbar_wait(&full[buf], ph, p.err_flag)) {
-        aborted = true;
-        break;
-      }
+      if (!mbar_wait(&full[buf], ph, p.err_flag)) return;
       const uint32_t sb = sbase + (uint32_t)buf * kStageBytes;
       const int wk0 = warp * C::kKeysPerWarp;
       const int key_base = k0 + wk0;
@@ -279,7 +305,8 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
           }
         }
         // ---- scale, causal mask, online softmax (rows gq, gq+8; a row's
-        // keys are spread over the 4 threads of a quad)
+        // keys are spread over the 4 threads of a quad).  The running max is
+        // only moved when it grows by more than 2^8, so O is rarely rescaled.
         float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int nt = 0; nt < C::kNT; ++nt) {
@@ -292,34 +319,39 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
             mx[hr] = fmaxf(mx[hr], v);
           }
         }
-        float alpha[2], base[2];
+        float alpha[2];
+        bool resc = false;
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
           mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
-          const float mnew = fmaxf(m_run[hr], mx[hr]);
-          base[hr] = mnew == -INFINITY ? 0.f : mnew;
-          alpha[hr] = fast_exp2(m_run[hr] - base[hr]);
-          m_run[hr] = mnew;
+          alpha[hr] = 1.f;
+          if (mx[hr] > m_run[hr] + kRescaleThreshold) {
+            alpha[hr] = fast_exp2(m_run[hr] - mx[hr]);
+            l_run[hr] *= alpha[hr];
+            m_run[hr] = mx[hr];
+            resc = true;
+          }
         }
-        float rs[2] = {0.f, 0.f};
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int nt = 0; nt < 16; ++nt) {
+            o[nt][0] *= alpha[0];
+            o[nt][1] *= alpha[0];
+            o[nt][2] *= alpha[1];
+            o[nt][3] *= alpha[1];
+          }
+        }
+        const float base0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
+        const float base1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
 #pragma unroll
         for (int nt = 0; nt < C::kNT; ++nt) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const float e = fast_exp2(s[nt][j] - base[j >> 1]);
+            const float e = fast_exp2(s[nt][j] - ((j >> 1) ? base1 : base0));
             s[nt][j] = e;
-            rs[j >> 1] += e;
+            l_run[j >> 1] += e;
           }
-        }
-        l_run[0] = l_run[0] * alpha[0] + rs[0];
-        l_run[1] = l_run[1] * alpha[1] + rs[1];
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-          o[nt][0] *= alpha[0];
-          o[nt][1] *= alpha[0];
-          o[nt][2] *= alpha[1];
-          o[nt][3] *= alpha[1];
         }
         // ---- O += P V
         const uint32_t vb = sb + 32768u;
@@ -388,54 +420,83 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[buf]);
     }
-    if (aborted) return;
 
-    // ---- combine the four warps' states in a fixed order
-    l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 1);
-    l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 2);
-    l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 1);
-    l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 2);
+    // ---- combine the eight warps' states in a fixed order:
+    // (1) every warp posts (m, l); warps 4..7 post O;
+    // (2) warp w < 4 folds warp w+4's O into its own, rescaled to the
+    //     eight-warp max, and posts the sum;
+    // (3) 128 threads add the four posted O's in order and write the partial.
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
+      l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
+    }
     if (c == 0) {
       comb_ml[(warp * 16 + gq) * 2 + 0] = m_run[0];
       comb_ml[(warp * 16 + gq) * 2 + 1] = l_run[0];
       comb_ml[(warp * 16 + gq + 8) * 2 + 0] = m_run[1];
       comb_ml[(warp * 16 + gq + 8) * 2 + 1] = l_run[1];
     }
-    float* cw = comb + warp * 16 * kCombRow;
+    const int slot = warp & (kCombWarps - 1);
+    float* cw = comb + slot * 16 * kCombRow;
+    if (warp >= kCombWarps) {
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int d0 = out_col<FP8>(nt, 2 * c), d1 = out_col<FP8>(nt, 2 * c + 1);
-      cw[gq * kCombRow + d0] = o[nt][0];
-      cw[gq * kCombRow + d1] = o[nt][1];
-      cw[(gq + 8) * kCombRow + d0] = o[nt][2];
-      cw[(gq + 8) * kCombRow + d1] = o[nt][3];
+      for (int nt = 0; nt < 16; ++nt) {
+        const int d0 = out_col<FP8>(nt, 2 * c), d1 = out_col<FP8>(nt, 2 * c + 1);
+        cw[gq * kCombRow + d0] = o[nt][0];
+        cw[gq * kCombRow + d1] = o[nt][1];
+        cw[(gq + 8) * kCombRow + d0] = o[nt][2];
+        cw[(gq + 8) * kCombRow + d1] = o[nt][3];
+      }
     }
     if (!consumers_sync(cbar, cphase, p.err_flag)) return;
-    {
+    if (warp < kCombWarps) {
+      float a_me[2], a_pair[2];
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int row = gq + 8 * hr;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_ml[(w * 16 + row) * 2]);
+        const float mp = comb_ml[((warp + kCombWarps) * 16 + row) * 2];
+        a_me[hr] = m_run[hr] == -INFINITY ? 0.f : fast_exp2(m_run[hr] - M);
+        a_pair[hr] = mp == -INFINITY ? 0.f : fast_exp2(mp - M);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int d0 = out_col<FP8>(nt, 2 * c), d1 = out_col<FP8>(nt, 2 * c + 1);
+        float* p0 = &cw[gq * kCombRow + d0];
+        float* p1 = &cw[gq * kCombRow + d1];
+        float* p2 = &cw[(gq + 8) * kCombRow + d0];
+        float* p3 = &cw[(gq + 8) * kCombRow + d1];
+        *p0 = a_me[0] * o[nt][0] + a_pair[0] * *p0;
+        *p1 = a_me[0] * o[nt][1] + a_pair[0] * *p1;
+        *p2 = a_me[1] * o[nt][2] + a_pair[1] * *p2;
+        *p3 = a_me[1] * o[nt][3] + a_pair[1] * *p3;
+      }
+    }
+    if (!consumers_sync(cbar, cphase, p.err_flag)) return;
+    if (warp < kCombWarps) {
       const int t = threadIdx.x;          // 0..127
       const int row = t >> 3;             // m-tile row
       const int d0 = (t & 7) * 16;
       const int qv = x.mt * 16 + row;
       if (qv < nq) {
-        float mw[kConsumerWarps], lw[kConsumerWarps];
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          mw[w] = comb_ml[(w * 16 + row) * 2 + 0];
-          lw[w] = comb_ml[(w * 16 + row) * 2 + 1];
-          M = fmaxf(M, mw[w]);
-        }
-        float aw[kConsumerWarps], L = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_ml[(w * 16 + row) * 2]);
+        float L = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
-          aw[w] = mw[w] == -INFINITY ? 0.f : fast_exp2(mw[w] - M);
-          L += aw[w] * lw[w];
+          const float mw = comb_ml[(w * 16 + row) * 2];
+          const float lw = comb_ml[(w * 16 + row) * 2 + 1];
+          L += (mw == -INFINITY ? 0.f : fast_exp2(mw - M)) * lw;
         }
         const float vs = FP8 ? __ldg(p.v_scale + x.g) : 1.f;
         const int r = qv / p.group;
         const int h = x.g * p.group + (qv - r * p.group);
-        const size_t slot = ((size_t)(ru.row0 + r) * p.hq + h) * p.max_splits + x.sigma;
-        float4* dst = reinterpret_cast<float4*>(p.part_o + slot * kHeadDim + d0);
+        const size_t pslot = ((size_t)(ru.row0 + r) * p.hq + h) * p.max_splits + x.sigma;
+        float4* dst = reinterpret_cast<float4*>(p.part_o + pslot * kHeadDim + d0);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           float v[4];
@@ -443,15 +504,15 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
           for (int e = 0; e < 4; ++e) {
             float acc = 0.f;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w)
-              acc += aw[w] * comb[(w * 16 + row) * kCombRow + d0 + 4 * j + e];
+            for (int w = 0; w < kCombWarps; ++w)
+              acc += comb[(w * 16 + row) * kCombRow + d0 + 4 * j + e];
             v[e] = acc * vs;
           }
           dst[j] = make_float4(v[0], v[1], v[2], v[3]);
         }
         if ((t & 7) == 0) {
-          p.part_ml[slot * 2 + 0] = M;
-          p.part_ml[slot * 2 + 1] = L;
+          p.part_ml[pslot * 2 + 0] = M;
+          p.part_ml[pslot * 2 + 1] = L;
         }
       }
     }
@@ -467,9 +528,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
                                              ~uintptr_t(1023));
   uint8_t* stage_mem = smem;
   float* comb = reinterpret_cast<float*>(smem + kStages * kStageBytes);
-  float* comb_ml = comb + kConsumerWarps * 16 * kCombRow;
+  float* comb_ml = comb + kCombWarps * 16 * kCombRow;
   int* stage_bad = reinterpret_cast<int*>(comb_ml + kConsumerWarps * 16 * 2);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stage_bad + 4 * kStages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(stage_bad + kStages) + 7) & ~uintptr_t(7));
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* cbar = bars + 2 * kStages;
@@ -483,14 +545,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
     mbar_init(cbar, kConsumerWarps);
     fence_mbar_init();
   }
-  if (warp == kConsumerWarps && (threadIdx.x & 31) == 0) {
+  if (warp == kProducerWarp && (threadIdx.x & 31) == 0) {
     for (int i = 0; i < p.nsrc; ++i) {
       tma_prefetch_desc(&p.maps[i].k);
       tma_prefetch_desc(&p.maps[i].v);
     }
   }
   __syncthreads();
-  if (warp == kConsumerWarps)
+  if (warp == kProducerWarp)
     producer<FP8>(p, stage_mem, full, empty, stage_bad);
   else
     consumer<FP8>(p, stage_mem, full, empty, stage_bad, comb, comb_ml, cbar);
@@ -522,17 +584,31 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
   float L = a * l;
 #pragma unroll
   for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  // Every slot below nsplit was written by the partial kernel (an empty split
+  // holds o = 0 with weight 0), so the loads need no guard and can be batched.
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < nsplit; ++s) {
-    const float as = __shfl_sync(0xffffffffu, a, s);
-    if (as != 0.f) {
-      const float4 v =
-          *reinterpret_cast<const float4*>(p.part_o + (slot0 + s) * kHeadDim + lane * 4);
-      acc.x += as * v.x;
-      acc.y += as * v.y;
-      acc.z += as * v.z;
-      acc.w += as * v.w;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + slot0 * kHeadDim) + lane;
+  int s = 0;
+  for (; s + 8 <= nsplit; s += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = po[(s + u) * (kHeadDim / 4)];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float as = __shfl_sync(0xffffffffu, a, s + u);
+      acc.x += as * v[u].x;
+      acc.y += as * v[u].y;
+      acc.z += as * v[u].z;
+      acc.w += as * v[u].w;
     }
+  }
+  for (; s < nsplit; ++s) {
+    const float4 v = po[s * (kHeadDim / 4)];
+    const float as = __shfl_sync(0xffffffffu, a, s);
+    acc.x += as * v.x;
+    acc.y += as * v.y;
+    acc.z += as * v.z;
+    acc.w += as * v.w;
   }
   const float inv = 1.f / L;
   uint2 packed;

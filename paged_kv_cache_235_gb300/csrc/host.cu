@@ -217,7 +217,7 @@ int to_err(cudaError_t e) { return e == cudaSuccess ? TFPA_OK : TFPA_ECUDA; }
 
 extern "C" int32_t tfpa_pages_per_split(int32_t seq_len) {
   const int32_t np = pages_of(std::max(seq_len, 1));
-  return std::max<int32_t>(1, (np + kMaxSplits - 1) / kMaxSplits);
+  return std::max<int32_t>(2, (np + kMaxSplits - 1) / kMaxSplits);
 }
 
 extern "C" int32_t tfpa_num_splits(int32_t seq_len) {

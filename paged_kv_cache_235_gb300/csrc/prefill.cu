@@ -265,32 +265,27 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
   for (int j = 0; j < gm.nkt; ++j) {
     if (!mbar_wait_or_abort(&s_full[hh], j & 1, p.err_flag, abort)) return;
     umma::fence_after_sync();
-    uint32_t sv[4][32];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) umma::tmem_ld32(tS + 32 * c, sv[c]);
-    umma::tmem_ld_wait();
     const int kt = j * kTileKeys;
     if (ru.page_table && (kt >> 8) != cached_page) {
       cached_page = kt >> 8;
       page_bad = tile_page(p, ru, j) < 0;
     }
     const int lim = page_bad ? -1 : pos - kt;            // key kt+i visible iff i <= lim
+    const bool full_tile = lim >= kTileKeys - 1;
+    // Pass 1: the row's max over this key tile, 32 columns at a time.
     float mx = -INFINITY;
-    if (lim >= kTileKeys - 1) {
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        const float v = __uint_as_float(sv[i >> 5][i & 31]) * sl2;
-        sv[i >> 5][i & 31] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
-      }
-    } else {
+    for (int c = 0; c < 4; ++c) {
+      uint32_t sv[32];
+      umma::tmem_ld32(tS + 32 * c, sv);
+      umma::tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        const float v = i <= lim ? __uint_as_float(sv[i >> 5][i & 31]) * sl2 : -INFINITY;
-        sv[i >> 5][i & 31] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+      for (int i = 0; i < 32; ++i) {
+        const float v = __uint_as_float(sv[i]);
+        mx = (full_tile || 32 * c + i <= lim) ? fmaxf(mx, v) : mx;
       }
     }
+    mx = mx * sl2;
     const float m_new = fmaxf(m_run, mx);
     const bool resc = m_new > m_run + kRescaleThreshold;
     float alpha = 1.f;
@@ -311,18 +306,29 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
       }
     }
     const float base = m_run == -INFINITY ? 0.f : m_run;
+    // Pass 2: p = 2^(s*scale - m), packed to bf16 pairs over the first 64
+    // columns of S; chunk c's 16 packed columns lie in S columns already read.
     float rs = 0.f;
-    // P as bf16 pairs, written over the first 64 columns of S.
 #pragma unroll
-    for (int k = 0; k < 64; ++k) {
-      const float p0 = fast_exp2(__uint_as_float(sv[(2 * k) >> 5][(2 * k) & 31]) - base);
-      const float p1 = fast_exp2(__uint_as_float(sv[(2 * k + 1) >> 5][(2 * k + 1) & 31]) - base);
-      rs += p0 + p1;
-      sv[k >> 5][k & 31] = pack_bf16x2(p0, p1);
+    for (int c = 0; c < 4; ++c) {
+      uint32_t sv[32];
+      umma::tmem_ld32(tS + 32 * c, sv);
+      umma::tmem_ld_wait();
+      uint32_t pk[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int i0 = 32 * c + 2 * k;
+        const float s0 = (full_tile || i0 <= lim) ? __uint_as_float(sv[2 * k]) * sl2 : -INFINITY;
+        const float s1 =
+            (full_tile || i0 + 1 <= lim) ? __uint_as_float(sv[2 * k + 1]) * sl2 : -INFINITY;
+        const float p0 = fast_exp2(s0 - base);
+        const float p1 = fast_exp2(s1 - base);
+        rs += p0 + p1;
+        pk[k] = pack_bf16x2(p0, p1);
+      }
+      umma::tmem_st16(tS + 16 * c, pk);
     }
     l += rs;
-    umma::tmem_st32(tS, sv[0]);
-    umma::tmem_st32(tS + 32, sv[1]);
     umma::tmem_st_wait();
     umma::fence_before_sync();
     __syncwarp();

@@ -31,8 +31,9 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_split_policy_depends_on_length_only():
-    for L, pps, ns in [(1, 1, 1), (256, 1, 1), (257, 1, 2), (1000, 1, 4), (8192, 1, 32),
-                       (8193, 2, 17), (65536, 8, 32), (262144, 32, 32), (109000, 14, 31)]:
+    for L, pps, ns in [(1, 2, 1), (256, 2, 1), (257, 2, 1), (513, 2, 2), (1000, 2, 2),
+                       (8192, 2, 16), (8193, 2, 17), (16384, 2, 32), (16385, 3, 22),
+                       (65536, 8, 32), (262144, 32, 32), (109000, 14, 31)]:
         assert B.tfpa_pages_per_split(L) == pps, L
         assert B.tfpa_num_splits(L) == ns, L
     for L in range(1, 300000, 997):
@@ -118,7 +119,7 @@ def test_write_kv_one_launch_per_64_runs():
     (dict(pos=1000), B.TFPA_ERANGE),
     (dict(pos=-1), B.TFPA_ERANGE),
     (dict(seg=1), B.TFPA_ERANGE),
-    (dict(max_splits=3), B.TFPA_ECAPACITY),
+    (dict(max_splits=1), B.TFPA_ECAPACITY),
     (dict(page=5000), B.TFPA_ERANGE),
     (dict(q=FAKE + 2), B.TFPA_EINVAL),
     (dict(slab_cap=1000), B.TFPA_EINVAL),

@@ -114,13 +114,15 @@ def test_partials_match_oracle_partials():
         n = nsplit[r]
         assert n == B.tfpa_num_splits(w.streams[w.row_seg[r]].seq_len)
         fin = np.isfinite(m[r, :, :n])
-        assert np.array_equal(fin, np.isfinite(gm[r, :, :n]))
-        # the partials are defined up to the common factor exp(m); compare
-        # l and o relative to each split's own max
-        np.testing.assert_allclose(gm[r, :, :n][fin], m[r, :, :n][fin], rtol=0, atol=2e-3)
-        scale = np.exp(gm[r, :, :n] - np.where(fin, m[r, :, :n], 0))[..., None]
-        assert_close(gl[r, :, :n][fin], (l[r, :, :n] * scale[..., 0])[fin], 3e-2, "l")
-        assert_close(go[r, :, :n][fin], (o[r, :, :n] * scale)[fin], 3e-2, "o")
+        assert np.array_equal(fin, gl[r, :, :n] > 0)
+        # (m, l, o) is defined up to the reference max m (the kernel may keep
+        # a stale one): compare each split's lse and normalised output
+        lse_o = m[r, :, :n] + np.log(np.where(fin, l[r, :, :n], 1.0))
+        lse_g = gm[r, :, :n] + np.log(np.where(fin, gl[r, :, :n], 1.0))
+        np.testing.assert_allclose(lse_g[fin], lse_o[fin], rtol=0, atol=2e-3)
+        on = o[r, :, :n] / np.where(fin, l[r, :, :n], 1.0)[..., None]
+        gn = go[r, :, :n] / np.where(fin, gl[r, :, :n], 1.0)[..., None]
+        assert_close(gn[fin], on[fin], 3e-2, "normalised o")
 
 
 def test_swapped_table_control_is_red():
