@@ -272,18 +272,15 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
     }
     const int lim = page_bad ? -1 : pos - kt;            // key kt+i visible iff i <= lim
     const bool full_tile = lim >= kTileKeys - 1;
-    // Pass 1: the row's max over this key tile, 32 columns at a time.
+    uint32_t sv[4][32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) umma::tmem_ld32(tS + 32 * c, sv[c]);
+    umma::tmem_ld_wait();
     float mx = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t sv[32];
-      umma::tmem_ld32(tS + 32 * c, sv);
-      umma::tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float v = __uint_as_float(sv[i]);
-        mx = (full_tile || 32 * c + i <= lim) ? fmaxf(mx, v) : mx;
-      }
+    for (int i = 0; i < 128; ++i) {
+      const float v = __uint_as_float(sv[i >> 5][i & 31]);
+      mx = (full_tile || i <= lim) ? fmaxf(mx, v) : mx;
     }
     mx = mx * sl2;
     const float m_new = fmaxf(m_run, mx);
@@ -294,6 +291,26 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
       l *= alpha;
       m_run = m_new;
     }
+    const float base = m_run == -INFINITY ? 0.f : m_run;
+    // p = 2^(s*scale - m), packed to bf16 pairs in place (pair k lands in
+    // slot k <= 2k, after both of its inputs are read), then written over
+    // the first 64 columns of S.
+    float rs = 0.f;
+#pragma unroll
+    for (int k = 0; k < 64; ++k) {
+      const int i0 = 2 * k;
+      const float s0 =
+          (full_tile || i0 <= lim) ? __uint_as_float(sv[i0 >> 5][i0 & 31]) * sl2 : -INFINITY;
+      const float s1 = (full_tile || i0 + 1 <= lim)
+                           ? __uint_as_float(sv[(i0 + 1) >> 5][(i0 + 1) & 31]) * sl2
+                           : -INFINITY;
+      const float p0 = fast_exp2(s0 - base);
+      const float p1 = fast_exp2(s1 - base);
+      rs += p0 + p1;
+      sv[k >> 5][k & 31] = pack_bf16x2(p0, p1);
+    }
+    umma::tmem_st32(tS, sv[0]);
+    umma::tmem_st32(tS + 32, sv[1]);
     if (j > 0 && __any_sync(0xffffffffu, resc)) {      // O *= alpha in TMEM
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -304,29 +321,6 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
         umma::tmem_st32(tO + 32 * c, o);
       }
-    }
-    const float base = m_run == -INFINITY ? 0.f : m_run;
-    // Pass 2: p = 2^(s*scale - m), packed to bf16 pairs over the first 64
-    // columns of S; chunk c's 16 packed columns lie in S columns already read.
-    float rs = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t sv[32];
-      umma::tmem_ld32(tS + 32 * c, sv);
-      umma::tmem_ld_wait();
-      uint32_t pk[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int i0 = 32 * c + 2 * k;
-        const float s0 = (full_tile || i0 <= lim) ? __uint_as_float(sv[2 * k]) * sl2 : -INFINITY;
-        const float s1 =
-            (full_tile || i0 + 1 <= lim) ? __uint_as_float(sv[2 * k + 1]) * sl2 : -INFINITY;
-        const float p0 = fast_exp2(s0 - base);
-        const float p1 = fast_exp2(s1 - base);
-        rs += p0 + p1;
-        pk[k] = pack_bf16x2(p0, p1);
-      }
-      umma::tmem_st16(tS + 16 * c, pk);
     }
     l += rs;
     umma::tmem_st_wait();
