@@ -215,12 +215,24 @@ def time_decode(w, torch, B, steps, warmup, dist):
 
     for _ in range(warmup):
         step()
+    torch.cuda.synchronize()
+    # One step captured as a CUDA graph (the library enqueues only kernels,
+    # with parameters by value, so a step replays without host work).
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            step()
+    torch.cuda.current_stream().wait_stream(cap)
+    for _ in range(warmup):
+        graph.replay()
     barrier(dist, torch)
     s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)
     for _ in range(steps):
-        step()
+        graph.replay()
     e1.record(s)
     barrier(dist, torch)
     step_ms = e0.elapsed_time(e1) / steps
@@ -299,10 +311,10 @@ def time_prefill(w, torch, B, reps):
 def profile_case(args, torch, B, wl):
     """One workload's kernels only, for profiler captures (a small launch list)."""
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-    if args.case == "prefill":
-        w = wl.prompt_chunk()
+    if args.case in ("prefill", "prefill_fp8"):
+        w = wl.prompt_chunk(kv_dtype="fp8" if args.case == "prefill_fp8" else "bf16")
         ms = time_prefill(w, torch, B, args.steps)
-        print(f"prefill: {ms:.4f} ms, {prefill_flops(w) / ms / 1e9:.1f} TFLOP/s")
+        print(f"{args.case}: {ms:.4f} ms, {prefill_flops(w) / ms / 1e9:.1f} TFLOP/s")
         return
     w = wl.batched_decode() if args.case == "decode" else wl.fp8_verify()
     cache, segs, q = device_case(w, torch, B)
@@ -356,7 +368,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true")
-    ap.add_argument("--case", default=None, choices=["decode", "fp8_verify", "prefill"],
+    ap.add_argument("--case", default=None,
+                    choices=["decode", "fp8_verify", "prefill", "prefill_fp8"],
                     help="profiling mode: run only this workload's kernels --steps times "
                          "after --warmup, print its timing, no JSON line")
     args = ap.parse_args()
@@ -389,36 +402,44 @@ def main():
 
     w = wl.batched_decode()
     kv, qo = kv_bytes(w)
-    with ClockSampler(local) as clk:
-        step_ms, partial_ms, ctx = time_decode(w, torch, B, args.steps, args.warmup, dist)
-    step_ms = max_over_ranks(dist, torch, step_ms)
-    e2e_s, h2d, d2h = time_e2e(w, torch, B, ctx, max(10, args.steps // 2), args.warmup)
-    e2e_s = max_over_ranks(dist, torch, e2e_s)
-    value = world * (kv + qo) / (step_ms / 1e3) / 1e9
-    achieved = (kv + qo) / (partial_ms / 1e3) / 1e9
-    del ctx
-
     extra = {}
     w3 = wl.fp8_verify()
-    s3, p3, ctx3 = time_decode(w3, torch, B, max(10, args.steps // 2), args.warmup, None)
     kv3, qo3 = kv_bytes(w3)
+    with ClockSampler(local) as clk:
+        step_ms, partial_ms, ctx = time_decode(w, torch, B, args.steps, args.warmup, dist)
+        step_ms = max_over_ranks(dist, torch, step_ms)
+        e2e_s, h2d, d2h = time_e2e(w, torch, B, ctx, max(10, args.steps // 2), args.warmup)
+        e2e_s = max_over_ranks(dist, torch, e2e_s)
+        del ctx
+        s3, p3, ctx3 = time_decode(w3, torch, B, max(10, args.steps // 2), args.warmup, None)
+        del ctx3
+        if not args.skip_prefill:
+            w4 = wl.prompt_chunk()
+            try:
+                ms4 = time_prefill(w4, torch, B, 5)
+                fl = prefill_flops(w4)
+                extra["prefill"] = {
+                    "workload": "28,672-position paged prefix + 4,096-row causal chunk, "
+                                "32/8 heads, bf16, one launch, L2 flushed before each",
+                    "ms_per_call": ms4, "tflops": fl / (ms4 / 1e3) / 1e12,
+                    "frac_of_measured_bf16": fl / (ms4 / 1e3) / 1e12 / pk["bf16_tflops"],
+                    "kernel": "prefill_kernel (tcgen05)"}
+            except B.TfpaError as e:
+                extra["prefill"] = {"unavailable": str(e)}
+            w5 = wl.prompt_chunk(kv_dtype="fp8")
+            ms5 = time_prefill(w5, torch, B, 5)
+            fl5 = prefill_flops(w5)
+            extra["prefill_fp8"] = {
+                "workload": "the same prompt chunk over an e4m3 cache (f16 MMAs)",
+                "ms_per_call": ms5, "tflops": fl5 / (ms5 / 1e3) / 1e12,
+                "frac_of_measured_bf16": fl5 / (ms5 / 1e3) / 1e12 / pk["bf16_tflops"]}
+    value = world * (kv + qo) / (step_ms / 1e3) / 1e9
+    achieved = (kv + qo) / (partial_ms / 1e3) / 1e9
     extra["fp8_verify"] = {
         "workload": "8 streams x 65,536 positions, 4 causal verify rows each, fp8 e4m3 KV",
         "ms_per_call": s3, "kv_gbs": (kv3 + qo3) / (s3 / 1e3) / 1e9,
         "partial_ms": p3, "partial_gbs": (kv3 + qo3) / (p3 / 1e3) / 1e9,
         "frac_of_measured_hbm": (kv3 + qo3) / (p3 / 1e3) / 1e9 / pk["hbm_gbs"]}
-    del ctx3
-    if not args.skip_prefill:
-        w4 = wl.prompt_chunk()
-        try:
-            ms4 = time_prefill(w4, torch, B, 5)
-            fl = prefill_flops(w4)
-            extra["prefill"] = {
-                "workload": "28,672-position paged prefix + 4,096-row causal chunk, 32/8 heads",
-                "ms_per_call": ms4, "tflops": fl / (ms4 / 1e3) / 1e12,
-                "frac_of_measured_bf16": fl / (ms4 / 1e3) / 1e12 / pk["bf16_tflops"]}
-        except B.TfpaError as e:
-            extra["prefill"] = {"unavailable": str(e)}
 
     if rank != 0:
         return
@@ -440,6 +461,8 @@ def main():
         "e2e": {"value": world * (kv + qo) / e2e_s / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
+        "timing": "decode step = one CUDA-graph replay of tfpa_write_kv + tfpa_decode "
+                  "(3 kernels), CUDA events over --steps replays",
         "clocks": clk.summary(),
         **extra,
     }

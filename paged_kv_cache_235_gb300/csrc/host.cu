@@ -520,7 +520,6 @@ extern "C" int tfpa_prefill(const tfpa_cache* c, const tfpa_seg* segs, int32_t n
   if ((e = check_cache(c)) || (e = check_segs(c, segs, nseg))) return e;
   if (rows > 0 && (!q || !aligned(q, 16) || !out || !aligned(out, 16))) return TFPA_EINVAL;
   if (max_rows_per_launch < 0 || !std::isfinite(scale)) return TFPA_EINVAL;
-  if (c->dtype != TFPA_BF16) return TFPA_EINVAL;   // e4m3 prompt tiles: not built yet
   std::vector<Run> runs;
   if ((e = build_runs(segs, nseg, row_seg, row_pos, rows, runs))) return e;
   if (rows == 0) return TFPA_OK;

@@ -15,10 +15,18 @@
 //               V MN-major from shared memory).  The two heads ping-pong:
 //               S_A(j+1) is issued right after PV_A(j), so head A's softmax
 //               overlaps head B's MMAs and the other way round.
+//   warps 2-3   (e4m3 caches only) converters: TMA lands e4m3 K/V tiles in
+//               a staging buffer; these warps write the exact f16 operand
+//               tiles (and zero V rows past the stream's end).
 //   warps 4-7   softmax of head A, warps 8-11 of head B: one thread per row
 //               (TMEM lane), causal mask on the diagonal tiles, online
-//               max/sum, P written back over S as bf16, O rescaled in TMEM
-//               only when the running max grows by more than 2^8.
+//               max/sum, P written back over S as bf16 (f16 for e4m3
+//               caches), O rescaled in TMEM only when the running max grows
+//               by more than 2^8.
+// With an e4m3 cache the MMAs run in f16: each softmax thread first turns its
+// Q row into f16 scaled by a power of two (exact for every element within
+// 2^28 of the row's largest), and the K and V scales are applied to the
+// scores and to the output.
 // TMEM (512 columns): S_A [0,128) O_A [128,256) S_B [256,384) O_B [384,512).
 #include "common.cuh"
 #include "params.h"
@@ -30,16 +38,41 @@ namespace {
 constexpr int kTileRows = 128;
 constexpr int kTileKeys = 128;
 constexpr int kThreads = 384;
-constexpr int kOffQ = 0;                 // 2 heads x [128 rows][128] bf16 = 64 KB
-constexpr int kOffK = 65536;             // 2 stages x 32 KB
+constexpr int kOffQ = 0;                 // 2 heads x [128 rows][128] 16-bit = 64 KB
+constexpr int kOffK = 65536;             // 2 stages x 32 KB (16-bit operand tiles)
 constexpr int kOffV = 131072;            // 2 stages x 32 KB
-constexpr int kOffBar = 196608;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;
+constexpr int kOffK8 = 196608;           // e4m3 staging: one K tile, 16 KB
+constexpr int kOffV8 = 212992;           // e4m3 staging: one V tile, 16 KB
+template <bool FP8>
+struct Layout {
+  static constexpr int kOffBar = FP8 ? 229376 : 196608;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+};
+static_assert(Layout<true>::kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 __device__ __forceinline__ uint32_t col_s(int hh) { return hh ? 256u : 0u; }
 __device__ __forceinline__ uint32_t col_o(int hh) { return hh ? 384u : 128u; }
+
+struct Bars {
+  uint64_t* q_full;      // Q tiles landed (TMA)
+  uint64_t* q_ready;     // Q operand ready for the MMA (e4m3 caches: after conversion)
+  uint64_t* k_full;      // [2] K operand stage ready
+  uint64_t* k_empty;     // [2]
+  uint64_t* v_full;      // [2]
+  uint64_t* v_empty;     // [2]
+  uint64_t* k8_full;     // e4m3 staging landed / free
+  uint64_t* k8_empty;
+  uint64_t* v8_full;
+  uint64_t* v8_empty;
+  uint64_t* s_full;      // [2] per head: S in TMEM
+  uint64_t* p_ready;     // [2] per head: P in TMEM, O corrected
+  uint64_t* o_final;
+  uint64_t* drain;
+  uint32_t* tmem_slot;
+  volatile int* abort;
+};
 
 struct Tile {
   int run, g, hp, t;
@@ -88,18 +121,27 @@ __device__ __forceinline__ int tile_page(const PrefillParams& p, const RunInfo& 
   return (unsigned)pid < (unsigned)p.num_pages ? pid : -1;
 }
 
+// First V row of key tile j that must read as zero: keys past the stream's
+// end, or every row of a tile whose page id is bad.
+__device__ __forceinline__ int v_zero_from(const PrefillParams& p, const RunInfo& ru, int j) {
+  const int kt = j * kTileKeys;
+  int z0 = kTileKeys;
+  if (kt + kTileKeys > ru.seq_len) z0 = ru.seq_len - kt;
+  if (ru.page_table && tile_page(p, ru, j) < 0) z0 = 0;
+  return z0;
+}
+
+template <bool FP8>
 __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& x,
-                         const TileGeom& gm, uint8_t* smem, uint64_t* q_full, uint64_t* k_full,
-                         uint64_t* k_empty, uint64_t* v_full, uint64_t* v_empty,
-                         volatile int* abort) {
+                         const TileGeom& gm, uint8_t* smem, const Bars& b) {
   const CUtensorMap* mk = &p.maps[ru.src].k;
   const CUtensorMap* mv = &p.maps[ru.src].v;
   const int h0 = x.g * p.group + 2 * x.hp;
-  mbar_arrive_expect_tx(q_full, 65536);
+  mbar_arrive_expect_tx(b.q_full, 65536);
   for (int hh = 0; hh < 2; ++hh)
     for (int rg = 0; rg < 2; ++rg)
       tma_load_3d(smem + kOffQ + hh * 32768 + rg * 16384, &p.qmap, rg * 64, h0 + hh,
-                  ru.row0 + gm.row_lo, q_full);
+                  ru.row0 + gm.row_lo, b.q_full);
   int cached_page = -1, cached_pid = 0;
   int issued_k = 0, issued_v = 0;
   for (int j = 0; j < gm.nkt; ++j) {
@@ -121,27 +163,45 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
     } else {
       y = x.g * ru.slab_cap + kt;
     }
-    if (!mbar_wait_or_abort(&k_empty[s], ph ^ 1, p.err_flag, abort)) break;
-    mbar_arrive_expect_tx(&k_full[s], 32768);
-    tma_load_2d(smem + kOffK + s * 32768, mk, 0, y, &k_full[s]);
-    tma_load_2d(smem + kOffK + s * 32768 + 16384, mk, 64, y, &k_full[s]);
-    issued_k = j + 1;
-    if (!mbar_wait_or_abort(&v_empty[s], ph ^ 1, p.err_flag, abort)) break;
-    mbar_arrive_expect_tx(&v_full[s], 32768);
-    tma_load_2d(smem + kOffV + s * 32768, mv, 0, y, &v_full[s]);
-    tma_load_2d(smem + kOffV + s * 32768 + 16384, mv, 64, y, &v_full[s]);
-    issued_v = j + 1;
+    if (FP8) {
+      // One staging tile each for K and V; the converters free them.
+      if (!mbar_wait_or_abort(b.k8_empty, (j & 1) ^ 1, p.err_flag, b.abort)) break;
+      mbar_arrive_expect_tx(b.k8_full, 16384);
+      tma_load_2d(smem + kOffK8, mk, 0, y, b.k8_full);
+      issued_k = j + 1;
+      if (!mbar_wait_or_abort(b.v8_empty, (j & 1) ^ 1, p.err_flag, b.abort)) break;
+      mbar_arrive_expect_tx(b.v8_full, 16384);
+      tma_load_2d(smem + kOffV8, mv, 0, y, b.v8_full);
+      issued_v = j + 1;
+    } else {
+      if (!mbar_wait_or_abort(&b.k_empty[s], ph ^ 1, p.err_flag, b.abort)) break;
+      mbar_arrive_expect_tx(&b.k_full[s], 32768);
+      tma_load_2d(smem + kOffK + s * 32768, mk, 0, y, &b.k_full[s]);
+      tma_load_2d(smem + kOffK + s * 32768 + 16384, mk, 64, y, &b.k_full[s]);
+      issued_k = j + 1;
+      if (!mbar_wait_or_abort(&b.v_empty[s], ph ^ 1, p.err_flag, b.abort)) break;
+      mbar_arrive_expect_tx(&b.v_full[s], 32768);
+      tma_load_2d(smem + kOffV + s * 32768, mv, 0, y, &b.v_full[s]);
+      tma_load_2d(smem + kOffV + s * 32768 + 16384, mv, 64, y, &b.v_full[s]);
+      issued_v = j + 1;
+    }
   }
-  if (*abort) {
+  if (*b.abort) {
     // Let this CTA's loads in flight land before it exits.
-    for (int j = max(0, issued_k - 2); j < issued_k; ++j)
-      mbar_wait(&k_full[j & 1], (j >> 1) & 1, p.err_flag);
-    for (int j = max(0, issued_v - 2); j < issued_v; ++j)
-      mbar_wait(&v_full[j & 1], (j >> 1) & 1, p.err_flag);
+    mbar_wait(b.q_full, 0, p.err_flag);
+    if (FP8) {
+      if (issued_k) mbar_wait(b.k8_full, (issued_k - 1) & 1, p.err_flag);
+      if (issued_v) mbar_wait(b.v8_full, (issued_v - 1) & 1, p.err_flag);
+    } else {
+      for (int j = max(0, issued_k - 2); j < issued_k; ++j)
+        mbar_wait(&b.k_full[j & 1], (j >> 1) & 1, p.err_flag);
+      for (int j = max(0, issued_v - 2); j < issued_v; ++j)
+        mbar_wait(&b.v_full[j & 1], (j >> 1) & 1, p.err_flag);
+    }
   }
 }
 
-// Zero rows [z0, 128) of a V tile (both 64-column halves) in shared memory:
+// Zero rows [z0, 128) of a 16-bit V operand tile (both 64-column halves):
 // keys past the stream's end, or a tile whose page id was bad, must add
 // exactly nothing to O even if the bytes there are not finite.
 __device__ __forceinline__ void zero_v_rows(uint8_t* vtile, int z0, int lane) {
@@ -154,15 +214,69 @@ __device__ __forceinline__ void zero_v_rows(uint8_t* vtile, int z0, int lane) {
   __syncwarp();
 }
 
+// e4m3 staging tile [128 rows][128 B] (128B swizzle) -> f16 operand tile
+// [128 rows][2 halves of 64] (128B swizzle), 64 threads; rows >= z0 become 0.
+__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int z0, int t) {
+  const uint32_t sb = smem_u32(src), db = smem_u32(dst);
+#pragma unroll 4
+  for (int k = 0; k < 16; ++k) {
+    const int i = t + 64 * k;              // (row, 16-byte source chunk)
+    const int row = i >> 3, c8 = i & 7;    // source chunk c8 = head dims 16*c8 .. +15
+    uint4 w = lds128(swz128(sb, row, c8));
+    if (row >= z0) w = make_uint4(0, 0, 0, 0);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      h[2 * q] = e4m3x2_to_f16x2((uint16_t)(ws[q] & 0xFFFF));
+      h[2 * q + 1] = e4m3x2_to_f16x2((uint16_t)(ws[q] >> 16));
+    }
+    const uint32_t half = db + (uint32_t)(c8 >> 2) * 16384u;
+    const int c16 = 2 * (c8 & 3);
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(swz128(half, row, c16)),
+                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(swz128(half, row, c16 + 1)),
+                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]) : "memory");
+  }
+}
+
+// Warps 2-3 for e4m3 caches: staging -> f16 operand stages.
+__device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileGeom& gm,
+                          uint8_t* smem, const Bars& b) {
+  const int t = threadIdx.x - 64;   // 0..63
+  const int lane = threadIdx.x & 31;
+  for (int j = 0; j < gm.nkt; ++j) {
+    const int s = j & 1;
+    const uint32_t ph = (j >> 1) & 1;
+    if (!mbar_wait_or_abort(b.k8_full, j & 1, p.err_flag, b.abort)) return;
+    if (!mbar_wait_or_abort(&b.k_empty[s], ph ^ 1, p.err_flag, b.abort)) return;
+    convert_tile(smem + kOffK8, smem + kOffK + s * 32768, kTileKeys, t);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(b.k8_empty);
+      mbar_arrive(&b.k_full[s]);
+    }
+    const int z0 = v_zero_from(p, ru, j);
+    if (!mbar_wait_or_abort(b.v8_full, j & 1, p.err_flag, b.abort)) return;
+    if (!mbar_wait_or_abort(&b.v_empty[s], ph ^ 1, p.err_flag, b.abort)) return;
+    convert_tile(smem + kOffV8, smem + kOffV + s * 32768, z0, t);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(b.v8_empty);
+      mbar_arrive(&b.v_full[s]);
+    }
+  }
+}
+
+template <bool FP8>
 __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const TileGeom& gm,
-                           uint8_t* smem, uint32_t tmem, uint64_t* q_full, uint64_t* k_full,
-                           uint64_t* k_empty, uint64_t* v_full, uint64_t* v_empty,
-                           uint64_t* s_full, uint64_t* p_ready, uint64_t* o_final,
-                           uint64_t* drain, volatile int* abort) {
+                           uint8_t* smem, uint32_t tmem, const Bars& b) {
   const int lane = threadIdx.x & 31;
   const bool leader = lane == 0;
-  constexpr uint32_t kIdescQK = umma::idesc_f16(128, 128, true, false);
-  constexpr uint32_t kIdescPV = umma::idesc_f16(128, 128, true, true);
+  constexpr uint32_t kIdescQK = umma::idesc_f16(128, 128, !FP8, false);
+  constexpr uint32_t kIdescPV = umma::idesc_f16(128, 128, !FP8, true);
   const uint32_t qb = smem_u32(smem + kOffQ);
   const uint32_t kb = smem_u32(smem + kOffK);
   const uint32_t vb = smem_u32(smem + kOffV);
@@ -172,29 +286,29 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
     for (int ks = 0; ks < 8; ++ks) {
       const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
       const uint64_t a = umma::smem_desc_sw128(qb + hh * 32768 + off, 16, 1024);
-      const uint64_t b = umma::smem_desc_sw128(kb + s * 32768 + off, 16, 1024);
-      umma::mma_ss(tmem + col_s(hh), a, b, kIdescQK, ks > 0 ? 1u : 0u);
+      const uint64_t bd = umma::smem_desc_sw128(kb + s * 32768 + off, 16, 1024);
+      umma::mma_ss(tmem + col_s(hh), a, bd, kIdescQK, ks > 0 ? 1u : 0u);
     }
   };
   auto issue_pv = [&](int hh, int s, bool acc) {   // O_hh (+)= P_hh V_s
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-      const uint64_t b = umma::smem_desc_sw128(vb + s * 32768 + kk * 2048, 16384, 1024);
-      umma::mma_ts(tmem + col_o(hh), tmem + col_s(hh) + kk * 8, b, kIdescPV,
+      const uint64_t bd = umma::smem_desc_sw128(vb + s * 32768 + kk * 2048, 16384, 1024);
+      umma::mma_ts(tmem + col_o(hh), tmem + col_s(hh) + kk * 8, bd, kIdescPV,
                    (acc || kk > 0) ? 1u : 0u);
     }
   };
 
-  bool ok = mbar_wait_or_abort(q_full, 0, p.err_flag, abort) &&
-            mbar_wait_or_abort(&k_full[0], 0, p.err_flag, abort);
+  bool ok = mbar_wait_or_abort(b.q_ready, 0, p.err_flag, b.abort) &&
+            mbar_wait_or_abort(&b.k_full[0], 0, p.err_flag, b.abort);
   if (ok) {
     umma::fence_after_sync();
     if (leader) {
       issue_s(0, 0);
-      umma::commit(&s_full[0]);
+      umma::commit(&b.s_full[0]);
       issue_s(1, 0);
-      umma::commit(&s_full[1]);
-      umma::commit(&k_empty[0]);
+      umma::commit(&b.s_full[1]);
+      umma::commit(&b.k_empty[0]);
     }
     __syncwarp();
   }
@@ -204,52 +318,88 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
     const int s1 = (j + 1) & 1;
     const uint32_t ph1 = ((j + 1) >> 1) & 1;
     const bool more = j + 1 < gm.nkt;
-    if (!(ok = mbar_wait_or_abort(&v_full[s], ph, p.err_flag, abort))) break;
-    const int kt = j * kTileKeys;
-    int z0 = kTileKeys;
-    if (kt + kTileKeys > ru.seq_len) z0 = ru.seq_len - kt;
-    if (ru.page_table && tile_page(p, ru, j) < 0) z0 = 0;
-    if (z0 < kTileKeys) zero_v_rows(smem + kOffV + s * 32768, z0, lane);
+    if (!(ok = mbar_wait_or_abort(&b.v_full[s], ph, p.err_flag, b.abort))) break;
+    if (!FP8) {   // the e4m3 converters zero these rows themselves
+      const int z0 = v_zero_from(p, ru, j);
+      if (z0 < kTileKeys) zero_v_rows(smem + kOffV + s * 32768, z0, lane);
+    }
     // head A
-    if (!(ok = mbar_wait_or_abort(&p_ready[0], j & 1, p.err_flag, abort))) break;
+    if (!(ok = mbar_wait_or_abort(&b.p_ready[0], j & 1, p.err_flag, b.abort))) break;
     umma::fence_after_sync();
     if (leader) issue_pv(0, s, j > 0);
     if (more) {
-      if (!(ok = mbar_wait_or_abort(&k_full[s1], ph1, p.err_flag, abort))) break;
+      if (!(ok = mbar_wait_or_abort(&b.k_full[s1], ph1, p.err_flag, b.abort))) break;
       umma::fence_after_sync();
       if (leader) {
         issue_s(0, s1);
-        umma::commit(&s_full[0]);
+        umma::commit(&b.s_full[0]);
       }
     }
     // head B
-    if (!(ok = mbar_wait_or_abort(&p_ready[1], j & 1, p.err_flag, abort))) break;
+    if (!(ok = mbar_wait_or_abort(&b.p_ready[1], j & 1, p.err_flag, b.abort))) break;
     umma::fence_after_sync();
     if (leader) {
       issue_pv(1, s, j > 0);
       if (more) {
         issue_s(1, s1);
-        umma::commit(&s_full[1]);
-        umma::commit(&k_empty[s1]);
+        umma::commit(&b.s_full[1]);
+        umma::commit(&b.k_empty[s1]);
       }
-      umma::commit(&v_empty[s]);
+      umma::commit(&b.v_empty[s]);
     }
     __syncwarp();
   }
   if (leader) {
     if (ok) {
-      umma::commit(o_final);
+      umma::commit(b.o_final);
     } else {
-      umma::commit(drain);          // let issued MMAs finish before TMEM is freed
-      mbar_wait(drain, 0, p.err_flag);
+      umma::commit(b.drain);          // let issued MMAs finish before TMEM is freed
+      mbar_wait(b.drain, 0, p.err_flag);
     }
   }
   __syncwarp();
 }
 
+// e4m3 caches: turn this thread's Q row (bf16, in the operand tile) into f16
+// in place, scaled by 2^e so its largest element lies in [2^13, 2^14).
+// Returns 2^-e, the factor that undoes the scaling.
+__device__ __forceinline__ float q_row_to_f16(uint8_t* qtile, int r) {
+  const uint32_t base = smem_u32(qtile);
+  uint32_t v[64];
+#pragma unroll
+  for (int ch = 0; ch < 16; ++ch) {
+    const uint4 w = lds128(swz128(base + (ch >> 3) * 16384u, r, ch & 7));
+    v[4 * ch + 0] = w.x;
+    v[4 * ch + 1] = w.y;
+    v[4 * ch + 2] = w.z;
+    v[4 * ch + 3] = w.w;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    amax = fmaxf(amax, fabsf(__uint_as_float(v[i] << 16)));
+    amax = fmaxf(amax, fabsf(__uint_as_float(v[i] & 0xFFFF0000u)));
+  }
+  int ex;
+  frexpf(amax, &ex);
+  ex = max(min(ex, 120), -100);
+  const float up = __int_as_float((127 + 14 - ex) << 23);
+#pragma unroll
+  for (int i = 0; i < 64; ++i)
+    v[i] = pack_f16x2(__uint_as_float(v[i] << 16) * up, __uint_as_float(v[i] & 0xFFFF0000u) * up);
+#pragma unroll
+  for (int ch = 0; ch < 16; ++ch)
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};"
+                 ::"r"(swz128(base + (ch >> 3) * 16384u, r, ch & 7)), "r"(v[4 * ch]),
+                   "r"(v[4 * ch + 1]), "r"(v[4 * ch + 2]), "r"(v[4 * ch + 3])
+                 : "memory");
+  return __int_as_float((127 - 14 + ex) << 23);
+}
+
+template <bool FP8>
 __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Tile& x,
-                             const TileGeom& gm, int hh, uint32_t tmem, uint64_t* s_full,
-                             uint64_t* p_ready, uint64_t* o_final, volatile int* abort) {
+                             const TileGeom& gm, int hh, uint8_t* smem, uint32_t tmem,
+                             const Bars& b) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = 32 * (warp & 3) + lane;                 // row of the tile = TMEM lane
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
@@ -257,13 +407,21 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
   const uint32_t tO = tmem + lane_off + col_o(hh);
   const bool valid = r < gm.nrows;
   const int pos = ru.pos0 + gm.row_lo + (valid ? r : 0);
-  const float sl2 = p.scale_log2;
+  float sl2 = p.scale_log2;
+  if (FP8) {
+    if (!mbar_wait_or_abort(b.q_full, 0, p.err_flag, b.abort)) return;
+    const float down = q_row_to_f16(smem + kOffQ + hh * 32768, r);
+    sl2 = p.scale_log2 * down * __ldg(p.k_scale + x.g);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b.q_ready);
+  }
   float m_run = -INFINITY, l = 0.f;
   int cached_page = -1;
   bool page_bad = false;
 
   for (int j = 0; j < gm.nkt; ++j) {
-    if (!mbar_wait_or_abort(&s_full[hh], j & 1, p.err_flag, abort)) return;
+    if (!mbar_wait_or_abort(&b.s_full[hh], j & 1, p.err_flag, b.abort)) return;
     umma::fence_after_sync();
     const int kt = j * kTileKeys;
     if (ru.page_table && (kt >> 8) != cached_page) {
@@ -292,9 +450,9 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
       m_run = m_new;
     }
     const float base = m_run == -INFINITY ? 0.f : m_run;
-    // p = 2^(s*scale - m), packed to bf16 pairs in place (pair k lands in
-    // slot k <= 2k, after both of its inputs are read), then written over
-    // the first 64 columns of S.
+    // p = 2^(s*scale - m), packed in place (pair k lands in slot k <= 2k,
+    // after both of its inputs are read), then written over the first 64
+    // columns of S.
     float rs = 0.f;
 #pragma unroll
     for (int k = 0; k < 64; ++k) {
@@ -307,7 +465,7 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
       const float p0 = fast_exp2(s0 - base);
       const float p1 = fast_exp2(s1 - base);
       rs += p0 + p1;
-      sv[k >> 5][k & 31] = pack_bf16x2(p0, p1);
+      sv[k >> 5][k & 31] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
     }
     umma::tmem_st32(tS, sv[0]);
     umma::tmem_st32(tS + 32, sv[1]);
@@ -326,13 +484,13 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
     umma::tmem_st_wait();
     umma::fence_before_sync();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&p_ready[hh]);
+    if (lane == 0) mbar_arrive(&b.p_ready[hh]);
   }
-  if (!mbar_wait_or_abort(o_final, 0, p.err_flag, abort)) return;
+  if (!mbar_wait_or_abort(b.o_final, 0, p.err_flag, b.abort)) return;
   umma::fence_after_sync();
   const int h = x.g * p.group + 2 * x.hp + hh;
   const bool write = valid && (2 * x.hp + hh) < p.group;
-  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const float inv = (l > 0.f ? 1.f / l : 0.f) * (FP8 ? __ldg(p.v_scale + x.g) : 1.f);
   uint4* dst = reinterpret_cast<uint4*>(
       p.out + ((size_t)(ru.row0 + gm.row_lo + r) * p.hq + h) * kHeadDim);
 #pragma unroll
@@ -357,37 +515,50 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
         l > 0.f ? (m_run + log2f(l)) * 0.6931471805599453f : -INFINITY;
 }
 
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = bars + 3;
-  uint64_t* v_full = bars + 5;
-  uint64_t* v_empty = bars + 7;
-  uint64_t* s_full = bars + 9;
-  uint64_t* p_ready = bars + 11;
-  uint64_t* o_final = bars + 13;
-  uint64_t* drain = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-  volatile int* abort = reinterpret_cast<volatile int*>(bars + 17);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Layout<FP8>::kOffBar);
+  Bars b;
+  b.q_full = bars + 0;
+  b.q_ready = FP8 ? bars + 1 : bars + 0;
+  b.k_full = bars + 2;
+  b.k_empty = bars + 4;
+  b.v_full = bars + 6;
+  b.v_empty = bars + 8;
+  b.k8_full = bars + 10;
+  b.k8_empty = bars + 11;
+  b.v8_full = bars + 12;
+  b.v8_empty = bars + 13;
+  b.s_full = bars + 14;
+  b.p_ready = bars + 16;
+  b.o_final = bars + 18;
+  b.drain = bars + 19;
+  b.tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  b.abort = reinterpret_cast<volatile int*>(bars + 21);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    const uint32_t stage_arrivals = FP8 ? 2 : 1;   // the converters, or the producer
+    mbar_init(b.q_full, 1);
+    mbar_init(bars + 1, 8);                        // q_ready: the softmax warps
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_ready[i], 4);
+      mbar_init(&b.k_full[i], stage_arrivals);
+      mbar_init(&b.k_empty[i], 1);
+      mbar_init(&b.v_full[i], stage_arrivals);
+      mbar_init(&b.v_empty[i], 1);
+      mbar_init(&b.s_full[i], 1);
+      mbar_init(&b.p_ready[i], 4);
     }
-    mbar_init(o_final, 1);
-    mbar_init(drain, 1);
-    *abort = 0;
+    mbar_init(b.k8_full, 1);
+    mbar_init(b.k8_empty, 2);
+    mbar_init(b.v8_full, 1);
+    mbar_init(b.v8_empty, 2);
+    mbar_init(b.o_final, 1);
+    mbar_init(b.drain, 1);
+    *b.abort = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -397,23 +568,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       tma_prefetch_desc(&p.maps[i].v);
     }
   }
-  if (warp == 1) umma::tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) umma::tmem_alloc(b.tmem_slot, kTmemCols);
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = *b.tmem_slot;
 
   const Tile x = tile_of(p, blockIdx.x);
   const RunInfo& ru = p.runs[x.run];
   const TileGeom gm = geom_of(ru, x);
 
   if (warp == 0) {
-    if (lane == 0) producer(p, ru, x, gm, smem, q_full, k_full, k_empty, v_full, v_empty, abort);
+    if (lane == 0) producer<FP8>(p, ru, x, gm, smem, b);
   } else if (warp == 1) {
-    mma_issuer(p, ru, gm, smem, tmem, q_full, k_full, k_empty, v_full, v_empty, s_full, p_ready,
-               o_final, drain, abort);
-  } else if (warp >= 4) {
-    softmax_role(p, ru, x, gm, (warp - 4) >> 2, tmem, s_full, p_ready, o_final, abort);
+    mma_issuer<FP8>(p, ru, gm, smem, tmem, b);
+  } else if (warp < 4) {
+    if (FP8) converter(p, ru, gm, smem, b);
+  } else {
+    softmax_role<FP8>(p, ru, x, gm, (warp - 4) >> 2, smem, tmem, b);
   }
   umma::fence_before_sync();
   __syncthreads();
@@ -423,20 +595,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   }
 }
 
-}  // namespace
-
-cudaError_t launch_prefill(const PrefillParams& p, bool fp8, int grid, cudaStream_t s) {
-  if (fp8) return cudaErrorNotSupported;
-  if (grid <= 0) return cudaSuccess;
+template <bool FP8>
+cudaError_t launch(const PrefillParams& p, int grid, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<FP8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Layout<FP8>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  prefill_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+  prefill_kernel<FP8><<<grid, kThreads, Layout<FP8>::kSmemBytes, s>>>(p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillParams& p, bool fp8, int grid, cudaStream_t s) {
+  if (grid <= 0) return cudaSuccess;
+  return fp8 ? launch<true>(p, grid, s) : launch<false>(p, grid, s);
 }
 
 }  // namespace tfpa

@@ -212,15 +212,15 @@ def fp8_verify(seed: int = 238, seq_len: int = 65536, n_streams: int = 8,
 
 
 def prompt_chunk(seed: int = 239, prefix: int = 28672, chunk: int = 4096,
-                 slack_pages: int = 32, paged: bool = True) -> Workload:
-    """One stream: a paged prefix plus a causal chunk of rows; 32/8 heads; bf16."""
+                 slack_pages: int = 32, paged: bool = True, kv_dtype: str = "bf16") -> Workload:
+    """One stream: a paged prefix plus a causal chunk of rows; 32/8 heads."""
     L = prefix + chunk
     num_pages = _pages(L) + slack_pages
     tables = permuted_tables([L], [paged], num_pages, seed)
     st = Stream(L, paged, tables[0], 0 if paged else _pages(L) * PAGE)
     rs = np.zeros(chunk, dtype=np.int32)
     rp = np.arange(prefix, L, dtype=np.int32)
-    return Workload("prompt_chunk", 32, 8, "bf16", num_pages, [st], rs, rp, seed)
+    return Workload("prompt_chunk", 32, 8, kv_dtype, num_pages, [st], rs, rp, seed)
 
 
 def overcommitted_pool(seed: int = 240, n_short: int = 16, lo: int = 1000,

@@ -7,14 +7,21 @@ import torch
 
 from oracle import attention
 from paged_kv_cache_235_gb300 import workloads as wl
-from tests.gpu_cases import GpuCase, assert_close, bits, to_f64
+from tests.gpu_cases import GpuCase, assert_close, bits, fp8_scales, to_f64
 from tests.oracle_cases import build_oracle_cache
 
 pytestmark = pytest.mark.gpu
 
+TOL = {"bf16": 1e-2, "fp8": 3e-2}
 
-def _oracle(w, rows=None):
-    cache, segs = build_oracle_cache(w)
+
+def _case(w, **kw):
+    scales = fp8_scales(w) if w.kv_dtype == "fp8" else None
+    return GpuCase(w, scales, **kw), scales
+
+
+def _oracle(w, rows=None, scales=None):
+    cache, segs = build_oracle_cache(w, *(scales or (None, None)))
     q = w.q_bits()
     rs, rp = w.row_seg, w.row_pos
     if rows is not None:
@@ -22,26 +29,29 @@ def _oracle(w, rows=None):
     return attention.attend(cache, segs, q, rs, rp, w.softmax_scale)
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
 @pytest.mark.parametrize("prefix,chunk", [(300, 257), (0, 300), (256, 128), (1000, 1), (77, 130)])
-def test_prompt_chunk_matches_oracle(prefix, chunk):
-    w = wl.prompt_chunk(seed=300 + prefix + chunk, prefix=prefix, chunk=chunk, slack_pages=3)
-    g = GpuCase(w)
+def test_prompt_chunk_matches_oracle(prefix, chunk, kv):
+    w = wl.prompt_chunk(seed=300 + prefix + chunk, prefix=prefix, chunk=chunk, slack_pages=3,
+                        kv_dtype=kv)
+    g, scales = _case(w)
     out, lse = g.prefill(g.q(), w.row_seg, w.row_pos)
-    ref, ref_lse = _oracle(w)
-    assert_close(to_f64(out), ref, 1e-2, f"prefill {prefix}+{chunk}")
+    ref, ref_lse = _oracle(w, scales=scales)
+    assert_close(to_f64(out), ref, TOL[kv], f"prefill {kv} {prefix}+{chunk}")
     assert_close(to_f64(lse), ref_lse, 1e-3, "lse")
     assert int(g.err.item()) == 0
 
 
-def test_prompt_chunk_slices_equal_one_launch_and_contiguous():
-    w = wl.small("prompt_chunk")              # 300-position prefix + 257 rows
-    g = GpuCase(w)
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_prompt_chunk_slices_equal_one_launch_and_contiguous(kv):
+    w = wl.prompt_chunk(seed=1235, prefix=300, chunk=257, slack_pages=3, kv_dtype=kv)
+    g, scales = _case(w)
     q = g.q()
     one, l1 = g.prefill(q, w.row_seg, w.row_pos)
     sl, l2 = g.prefill(q, w.row_seg, w.row_pos, max_rows=128)
     assert np.array_equal(bits(one), bits(sl))
     assert torch.equal(l1, l2)
-    gc = GpuCase(w, all_paged=False)
+    gc = GpuCase(w, scales, all_paged=False)
     cont, l3 = gc.prefill(gc.q(), w.row_seg, w.row_pos)
     assert np.array_equal(bits(one), bits(cont))
     assert torch.equal(l1, l3)
@@ -66,14 +76,15 @@ def test_two_prompt_chunks_in_one_call():
         assert np.array_equal(bits(alone), bits(out[sel]))
 
 
-def test_prefill_equals_decode_within_tolerance():
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_prefill_equals_decode_within_tolerance(kv):
     """The prompt tiles and the decode partials compute the same attention."""
-    w = wl.small("prompt_chunk")
-    g = GpuCase(w)
+    w = wl.prompt_chunk(seed=1235, prefix=300, chunk=257, slack_pages=3, kv_dtype=kv)
+    g, _ = _case(w)
     q = g.q()
     a, _ = g.prefill(q, w.row_seg, w.row_pos)
     b, _ = g.decode(q, w.row_seg, w.row_pos, cap_rows=64)
-    assert_close(to_f64(a), to_f64(b), 1e-2, "prefill vs decode")
+    assert_close(to_f64(a), to_f64(b), TOL[kv], "prefill vs decode")
 
 
 def test_swapped_table_control_is_red_for_prompt_rows():
@@ -90,16 +101,17 @@ def test_swapped_table_control_is_red_for_prompt_rows():
 
 
 @pytest.mark.slow
-def test_prompt_chunk_full_size_sampled():
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_prompt_chunk_full_size_sampled(kv):
     """28,672-position paged prefix + 4,096 causal rows, as the bench runs it;
     a sample of rows (first, last, and across tiles) against the oracle."""
     from tests.test_gpu_full import oracle_stream
-    w = wl.prompt_chunk()
-    g = GpuCase(w)
+    w = wl.prompt_chunk(kv_dtype=kv)
+    g, scales = _case(w)
     q = g.q()
     out, lse = g.prefill(q, w.row_seg, w.row_pos)
     rows = np.array([0, 1, 127, 128, 1000, 2047, 2048, 4000, 4094, 4095])
-    ref, ref_lse = oracle_stream(w, 0, rows, None)
-    assert_close(to_f64(out[rows]), ref, 1e-2, "full prefill")
+    ref, ref_lse = oracle_stream(w, 0, rows, scales)
+    assert_close(to_f64(out[rows]), ref, TOL[kv], "full prefill")
     assert_close(to_f64(lse[rows]), ref_lse, 1e-3, "full prefill lse")
     assert int(g.err.item()) == 0
