@@ -63,7 +63,7 @@ class ClockSampler:
         try:
             self._proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()
         except Exception:
@@ -363,7 +363,7 @@ def reference_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -408,10 +408,10 @@ def main():
     with ClockSampler(local) as clk:
         step_ms, partial_ms, ctx = time_decode(w, torch, B, args.steps, args.warmup, dist)
         step_ms = max_over_ranks(dist, torch, step_ms)
-        e2e_s, h2d, d2h = time_e2e(w, torch, B, ctx, max(10, args.steps // 2), args.warmup)
+        e2e_s, h2d, d2h = time_e2e(w, torch, B, ctx, max(10, min(args.steps, 500)), args.warmup)
         e2e_s = max_over_ranks(dist, torch, e2e_s)
         del ctx
-        s3, p3, ctx3 = time_decode(w3, torch, B, max(10, args.steps // 2), args.warmup, None)
+        s3, p3, ctx3 = time_decode(w3, torch, B, max(10, args.steps // 4), args.warmup, None)
         del ctx3
         if not args.skip_prefill:
             w4 = wl.prompt_chunk()

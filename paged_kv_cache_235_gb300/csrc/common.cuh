@@ -136,6 +136,25 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// 2^x on the FMA pipe, for x in [-125, 8]: Cody-Waite split x = n + f with
+// n = rint(x) (the 1.5 * 2^23 shifter) and f in [-0.5, 0.5]; 2^f by a degree-3
+// polynomial whose coefficients were fitted here for least maximum relative
+// error on that interval (Lawson-reweighted least squares; 7.5e-5, below the
+// bf16 or f16 rounding the result gets next); 2^n added to the exponent field.
+constexpr float kExp2C0 = 0.9999281167984009f;
+constexpr float kExp2C1 = 0.6932617425918579f;
+constexpr float kExp2C2 = 0.24261078238487244f;
+constexpr float kExp2C3 = 0.055167440325021744f;
+__device__ __forceinline__ float poly_exp2(float x) {
+  x = fmaxf(x, -125.f);
+  const float t = x + 12582912.f;
+  const float n = t - 12582912.f;
+  const float f = x - n;
+  const float p = fmaf(fmaf(fmaf(kExp2C3, f, kExp2C2), f, kExp2C1), f, kExp2C0);
+  const int ni = __float_as_int(t) - 0x4B400000;
+  return __int_as_float(__float_as_int(p) + (ni << 23));
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));

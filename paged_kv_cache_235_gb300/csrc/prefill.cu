@@ -50,6 +50,9 @@ struct Layout {
 };
 static_assert(Layout<true>::kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
+constexpr int kRegsLow = 64;       // warps 0-3 after the register split
+constexpr int kRegsHigh = 216;     // warps 4-11
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * 168, "register split");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 __device__ __forceinline__ uint32_t col_s(int hh) { return hh ? 256u : 0u; }
@@ -115,20 +118,35 @@ __device__ __forceinline__ TileGeom geom_of(const RunInfo& ru, const Tile& x) {
   return gm;
 }
 
-// Page id of key tile j (paged runs), or -1 if it is outside the pool.
-__device__ __forceinline__ int tile_page(const PrefillParams& p, const RunInfo& ru, int j) {
-  const int pid = __ldg(ru.page_table + ((j * kTileKeys) >> 8));
-  return (unsigned)pid < (unsigned)p.num_pages ? pid : -1;
-}
+// Validity of the page under key tile j, read one page ahead so the table
+// load is off the critical path (two key tiles share a page).
+struct PageCheck {
+  const int32_t* pt;
+  int npages, num_pages, next_pid;
+  bool cur_bad;
+  __device__ __forceinline__ PageCheck(const PrefillParams& p, const RunInfo& ru, int kend)
+      : pt(ru.page_table), npages((kend + kPage - 1) / kPage), num_pages(p.num_pages),
+        next_pid(0), cur_bad(false) {
+    if (pt) next_pid = __ldg(pt);
+  }
+  // Call for j = 0, 1, 2, ... in order; true if tile j's page is bad.
+  __device__ __forceinline__ bool bad(int j) {
+    if (!pt) return false;
+    if ((j & 1) == 0) {
+      const int page = j >> 1;
+      cur_bad = (unsigned)next_pid >= (unsigned)num_pages;
+      if (page + 1 < npages) next_pid = __ldg(pt + page + 1);
+    }
+    return cur_bad;
+  }
+};
 
 // First V row of key tile j that must read as zero: keys past the stream's
 // end, or every row of a tile whose page id is bad.
-__device__ __forceinline__ int v_zero_from(const PrefillParams& p, const RunInfo& ru, int j) {
+__device__ __forceinline__ int v_zero_from(const RunInfo& ru, int j, bool page_bad) {
+  if (page_bad) return 0;
   const int kt = j * kTileKeys;
-  int z0 = kTileKeys;
-  if (kt + kTileKeys > ru.seq_len) z0 = ru.seq_len - kt;
-  if (ru.page_table && tile_page(p, ru, j) < 0) z0 = 0;
-  return z0;
+  return kt + kTileKeys > ru.seq_len ? ru.seq_len - kt : kTileKeys;
 }
 
 template <bool FP8>
@@ -245,7 +263,9 @@ __device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileG
                           uint8_t* smem, const Bars& b) {
   const int t = threadIdx.x - 64;   // 0..63
   const int lane = threadIdx.x & 31;
+  PageCheck pc(p, ru, gm.kend);
   for (int j = 0; j < gm.nkt; ++j) {
+    const int z0 = v_zero_from(ru, j, pc.bad(j));
     const int s = j & 1;
     const uint32_t ph = (j >> 1) & 1;
     if (!mbar_wait_or_abort(b.k8_full, j & 1, p.err_flag, b.abort)) return;
@@ -257,7 +277,6 @@ __device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileG
       mbar_arrive(b.k8_empty);
       mbar_arrive(&b.k_full[s]);
     }
-    const int z0 = v_zero_from(p, ru, j);
     if (!mbar_wait_or_abort(b.v8_full, j & 1, p.err_flag, b.abort)) return;
     if (!mbar_wait_or_abort(&b.v_empty[s], ph ^ 1, p.err_flag, b.abort)) return;
     convert_tile(smem + kOffV8, smem + kOffV + s * 32768, z0, t);
@@ -312,7 +331,9 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
     }
     __syncwarp();
   }
+  PageCheck pc(p, ru, gm.kend);
   for (int j = 0; ok && j < gm.nkt; ++j) {
+    const bool page_bad = pc.bad(j);
     const int s = j & 1;
     const uint32_t ph = (j >> 1) & 1;
     const int s1 = (j + 1) & 1;
@@ -320,7 +341,7 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
     const bool more = j + 1 < gm.nkt;
     if (!(ok = mbar_wait_or_abort(&b.v_full[s], ph, p.err_flag, b.abort))) break;
     if (!FP8) {   // the e4m3 converters zero these rows themselves
-      const int z0 = v_zero_from(p, ru, j);
+      const int z0 = v_zero_from(ru, j, page_bad);
       if (z0 < kTileKeys) zero_v_rows(smem + kOffV + s * 32768, z0, lane);
     }
     // head A
@@ -417,17 +438,13 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
     if (lane == 0) mbar_arrive(b.q_ready);
   }
   float m_run = -INFINITY, l = 0.f;
-  int cached_page = -1;
-  bool page_bad = false;
+  PageCheck pc(p, ru, gm.kend);
 
   for (int j = 0; j < gm.nkt; ++j) {
+    const bool page_bad = pc.bad(j);
     if (!mbar_wait_or_abort(&b.s_full[hh], j & 1, p.err_flag, b.abort)) return;
     umma::fence_after_sync();
     const int kt = j * kTileKeys;
-    if (ru.page_table && (kt >> 8) != cached_page) {
-      cached_page = kt >> 8;
-      page_bad = tile_page(p, ru, j) < 0;
-    }
     const int lim = page_bad ? -1 : pos - kt;            // key kt+i visible iff i <= lim
     const bool full_tile = lim >= kTileKeys - 1;
     uint32_t sv[4][32];
@@ -449,23 +466,39 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
       l *= alpha;
       m_run = m_new;
     }
-    const float base = m_run == -INFINITY ? 0.f : m_run;
+    const float nbase = m_run == -INFINITY ? 0.f : -m_run;
     // p = 2^(s*scale - m), packed in place (pair k lands in slot k <= 2k,
     // after both of its inputs are read), then written over the first 64
     // columns of S.
     float rs = 0.f;
+    // One pair in four goes through the FMA-pipe exp2 so the MUFU does not
+    // bound the two softmax warpgroups; which pairs is fixed by key position.
+    if (full_tile) {
 #pragma unroll
-    for (int k = 0; k < 64; ++k) {
-      const int i0 = 2 * k;
-      const float s0 =
-          (full_tile || i0 <= lim) ? __uint_as_float(sv[i0 >> 5][i0 & 31]) * sl2 : -INFINITY;
-      const float s1 = (full_tile || i0 + 1 <= lim)
-                           ? __uint_as_float(sv[(i0 + 1) >> 5][(i0 + 1) & 31]) * sl2
-                           : -INFINITY;
-      const float p0 = fast_exp2(s0 - base);
-      const float p1 = fast_exp2(s1 - base);
-      rs += p0 + p1;
-      sv[k >> 5][k & 31] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+      for (int k = 0; k < 64; ++k) {
+        const float t0 = fmaf(__uint_as_float(sv[(2 * k) >> 5][(2 * k) & 31]), sl2, nbase);
+        const float t1 = fmaf(__uint_as_float(sv[(2 * k + 1) >> 5][(2 * k + 1) & 31]), sl2, nbase);
+        const float p0 = (k & 3) == 0 ? poly_exp2(t0) : fast_exp2(t0);
+        const float p1 = (k & 3) == 0 ? poly_exp2(t1) : fast_exp2(t1);
+        rs += p0 + p1;
+        sv[k >> 5][k & 31] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        const int i0 = 2 * k;
+        const float t0 =
+            i0 <= lim ? fmaf(__uint_as_float(sv[i0 >> 5][i0 & 31]), sl2, nbase) : -INFINITY;
+        const float t1 = i0 + 1 <= lim
+                             ? fmaf(__uint_as_float(sv[(i0 + 1) >> 5][(i0 + 1) & 31]), sl2, nbase)
+                             : -INFINITY;
+        const float p0 =
+            i0 <= lim ? ((k & 3) == 0 ? poly_exp2(t0) : fast_exp2(t0)) : 0.f;
+        const float p1 =
+            i0 + 1 <= lim ? ((k & 3) == 0 ? poly_exp2(t1) : fast_exp2(t1)) : 0.f;
+        rs += p0 + p1;
+        sv[k >> 5][k & 31] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+      }
     }
     umma::tmem_st32(tS, sv[0]);
     umma::tmem_st32(tS + 32, sv[1]);
@@ -578,13 +611,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const RunInfo& ru = p.runs[x.run];
   const TileGeom gm = geom_of(ru, x);
 
-  if (warp == 0) {
-    if (lane == 0) producer<FP8>(p, ru, x, gm, smem, b);
-  } else if (warp == 1) {
-    mma_issuer<FP8>(p, ru, gm, smem, tmem, b);
-  } else if (warp < 4) {
-    if (FP8) converter(p, ru, gm, smem, b);
+  // Registers: the block launches with 384 x 168 = 64,512.  The TMA, MMA
+  // and converter warpgroup needs few; the two softmax warpgroups hold a
+  // 128-column S row per thread: 128 x kRegsLow + 256 x kRegsHigh <= 64,512.
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    if (warp == 0) {
+      if (lane == 0) producer<FP8>(p, ru, x, gm, smem, b);
+    } else if (warp == 1) {
+      mma_issuer<FP8>(p, ru, gm, smem, tmem, b);
+    } else if (FP8) {
+      converter(p, ru, gm, smem, b);
+    }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     softmax_role<FP8>(p, ru, x, gm, (warp - 4) >> 2, smem, tmem, b);
   }
   umma::fence_before_sync();
@@ -599,9 +639,14 @@ template <bool FP8>
 cudaError_t launch(const PrefillParams& p, int grid, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<FP8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Layout<FP8>::kSmemBytes);
+    // The register split only works if the block launches with at least the
+    // registers it hands out; otherwise setmaxnreg.inc would wait forever.
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, prefill_kernel<FP8>);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs * kThreads < 128 * kRegsLow + 256 * kRegsHigh) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(prefill_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Layout<FP8>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
