@@ -136,23 +136,34 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// 2^x on the FMA pipe, for x in [-125, 8]: Cody-Waite split x = n + f with
-// n = rint(x) (the 1.5 * 2^23 shifter) and f in [-0.5, 0.5]; 2^f by a degree-3
-// polynomial whose coefficients were fitted here for least maximum relative
-// error on that interval (Lawson-reweighted least squares; 7.5e-5, below the
-// bf16 or f16 rounding the result gets next); 2^n added to the exponent field.
-constexpr float kExp2C0 = 0.9999281167984009f;
-constexpr float kExp2C1 = 0.6932617425918579f;
-constexpr float kExp2C2 = 0.24261078238487244f;
-constexpr float kExp2C3 = 0.055167440325021744f;
-__device__ __forceinline__ float poly_exp2(float x) {
-  x = fmaxf(x, -125.f);
-  const float t = x + 12582912.f;
-  const float n = t - 12582912.f;
-  const float f = x - n;
-  const float p = fmaf(fmaf(fmaf(kExp2C3, f, kExp2C2), f, kExp2C1), f, kExp2C0);
-  const int ni = __float_as_int(t) - 0x4B400000;
-  return __int_as_float(__float_as_int(p) + (ni << 23));
+// Packed float32 pairs (Blackwell f32x2 FMA/ADD: one instruction for two
+// independent, individually rounded operations).
+struct f2 {
+  float x, y;
+};
+__device__ __forceinline__ f2 ffma2(f2 a, f2 b, f2 c) {
+  uint64_t ra, rb, rc, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  f2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+__device__ __forceinline__ f2 fadd2(f2 a, f2 b) {
+  uint64_t ra, rb, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  f2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {

@@ -452,10 +452,15 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
     for (int c = 0; c < 4; ++c) umma::tmem_ld32(tS + 32 * c, sv[c]);
     umma::tmem_ld_wait();
     float mx = -INFINITY;
+    if (full_tile) {
 #pragma unroll
-    for (int i = 0; i < 128; ++i) {
-      const float v = __uint_as_float(sv[i >> 5][i & 31]);
-      mx = (full_tile || i <= lim) ? fmaxf(mx, v) : mx;
+      for (int k = 0; k < 64; ++k)
+        mx = fmax3(mx, __uint_as_float(sv[(2 * k) >> 5][(2 * k) & 31]),
+                   __uint_as_float(sv[(2 * k + 1) >> 5][(2 * k + 1) & 31]));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 128; ++i)
+        mx = i <= lim ? fmaxf(mx, __uint_as_float(sv[i >> 5][i & 31])) : mx;
     }
     mx = mx * sl2;
     const float m_new = fmaxf(m_run, mx);
@@ -467,39 +472,26 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
       m_run = m_new;
     }
     const float nbase = m_run == -INFINITY ? 0.f : -m_run;
-    // p = 2^(s*scale - m), packed in place (pair k lands in slot k <= 2k,
-    // after both of its inputs are read), then written over the first 64
-    // columns of S.
-    float rs = 0.f;
-    // One pair in four goes through the FMA-pipe exp2 so the MUFU does not
-    // bound the two softmax warpgroups; which pairs is fixed by key position.
-    if (full_tile) {
+    // p = 2^(s*scale - m) on pairs of columns (packed f32x2 FMA and add),
+    // packed to 16-bit pairs in place (pair k lands in slot k <= 2k, after
+    // both of its inputs are read), then written over the first 64 columns
+    // of S.  The row sum is kept as two interleaved partial sums.
+    f2 acc = {0.f, 0.f};
+    const f2 sc2 = {sl2, sl2}, nb2 = {nbase, nbase};
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        const float t0 = fmaf(__uint_as_float(sv[(2 * k) >> 5][(2 * k) & 31]), sl2, nbase);
-        const float t1 = fmaf(__uint_as_float(sv[(2 * k + 1) >> 5][(2 * k + 1) & 31]), sl2, nbase);
-        const float p0 = (k & 3) == 0 ? poly_exp2(t0) : fast_exp2(t0);
-        const float p1 = (k & 3) == 0 ? poly_exp2(t1) : fast_exp2(t1);
-        rs += p0 + p1;
-        sv[k >> 5][k & 31] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+    for (int k = 0; k < 64; ++k) {
+      const int i0 = 2 * k;
+      f2 t = ffma2({__uint_as_float(sv[i0 >> 5][i0 & 31]),
+                    __uint_as_float(sv[(i0 + 1) >> 5][(i0 + 1) & 31])}, sc2, nb2);
+      f2 e = {fast_exp2(t.x), fast_exp2(t.y)};
+      if (!full_tile) {
+        e.x = i0 <= lim ? e.x : 0.f;
+        e.y = i0 + 1 <= lim ? e.y : 0.f;
       }
-    } else {
-#pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        const int i0 = 2 * k;
-        const float t0 =
-            i0 <= lim ? fmaf(__uint_as_float(sv[i0 >> 5][i0 & 31]), sl2, nbase) : -INFINITY;
-        const float t1 = i0 + 1 <= lim
-                             ? fmaf(__uint_as_float(sv[(i0 + 1) >> 5][(i0 + 1) & 31]), sl2, nbase)
-                             : -INFINITY;
-        const float p0 =
-            i0 <= lim ? ((k & 3) == 0 ? poly_exp2(t0) : fast_exp2(t0)) : 0.f;
-        const float p1 =
-            i0 + 1 <= lim ? ((k & 3) == 0 ? poly_exp2(t1) : fast_exp2(t1)) : 0.f;
-        rs += p0 + p1;
-        sv[k >> 5][k & 31] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
-      }
+      acc = fadd2(acc, e);
+      sv[k >> 5][k & 31] = FP8 ? pack_f16x2(e.x, e.y) : pack_bf16x2(e.x, e.y);
     }
+    const float rs = acc.x + acc.y;
     umma::tmem_st32(tS, sv[0]);
     umma::tmem_st32(tS + 32, sv[1]);
     if (j > 0 && __any_sync(0xffffffffu, resc)) {      // O *= alpha in TMEM
@@ -611,11 +603,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const RunInfo& ru = p.runs[x.run];
   const TileGeom gm = geom_of(ru, x);
 
-  // Registers: the block launches with 384 x 168 = 64,512.  The TMA, MMA
-  // and converter warpgroup needs few; the two softmax warpgroups hold a
-  // 128-column S row per thread: 128 x kRegsLow + 256 x kRegsHigh <= 64,512.
+  // Registers (e4m3 caches, where the softmax also holds the Q conversion):
+  // the block launches with 384 x 168 = 64,512; the TMA/MMA/converter
+  // warpgroup needs few, the two softmax warpgroups more:
+  // 128 x kRegsLow + 256 x kRegsHigh <= 64,512.
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    if (FP8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 0) {
       if (lane == 0) producer<FP8>(p, ru, x, gm, smem, b);
     } else if (warp == 1) {
@@ -624,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       converter(p, ru, gm, smem, b);
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+    if (FP8) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     softmax_role<FP8>(p, ru, x, gm, (warp - 4) >> 2, smem, tmem, b);
   }
   umma::fence_before_sync();
@@ -644,7 +637,8 @@ cudaError_t launch(const PrefillParams& p, int grid, cudaStream_t s) {
     cudaFuncAttributes attr;
     cudaError_t e = cudaFuncGetAttributes(&attr, prefill_kernel<FP8>);
     if (e != cudaSuccess) return e;
-    if (attr.numRegs * kThreads < 128 * kRegsLow + 256 * kRegsHigh) return cudaErrorInvalidValue;
+    if (FP8 && attr.numRegs * kThreads < 128 * kRegsLow + 256 * kRegsHigh)
+      return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(prefill_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Layout<FP8>::kSmemBytes);
     if (e != cudaSuccess) return e;
