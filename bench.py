@@ -35,6 +35,26 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode KV GB/s (% HBM peak); prompt-chunk attn TFLOP/s (% TC peak)"
 
 
+# DRAM traffic of one decode partial launch on the batched-decode workload,
+# from ncu (dram__bytes_read.sum + dram__bytes_write.sum, see
+# profiles/decode_partial_batched_decode.md), valid only while the kernel's
+# sources hash to the value it was taken on.
+DECODE_TRAFFIC = {"bytes": 268_600_064 + 5_035_008, "sources_sha256_16": "bba9e1cc957bcaa5"}
+DECODE_SOURCES = ["paged_kv_cache_235_gb300/csrc/decode.cu",
+                  "paged_kv_cache_235_gb300/csrc/common.cuh",
+                  "paged_kv_cache_235_gb300/csrc/params.h"]
+
+
+def decode_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return DECODE_TRAFFIC["bytes"] if h.hexdigest()[:16] == DECODE_TRAFFIC["sources_sha256_16"] \
+        else None
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -454,7 +474,7 @@ def main():
                    "l2": "no flush: 268 MB of KV per step exceeds the 129 MB L2",
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                     "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": decode_traffic(),
                      "kernel": "decode_partial_kernel<bf16>", "peak_source": pk["source"],
                      "partial_ms": partial_ms},
         "cpu_baseline": cpu,
