@@ -552,6 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
     }
   }
   __syncthreads();
+  allow_next_grid();
+  wait_prior_grid();
   if (warp == kProducerWarp)
     producer<FP8>(p, stage_mem, full, empty, stage_bad);
   else
@@ -562,6 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
 // One warp per (row, head): lane s holds split s's (m, l); lanes own 4
 // consecutive head-dim elements of the output.  Fixed summation order.
 __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ MergeParams p) {
+  allow_next_grid();
+  wait_prior_grid();
   const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (wid >= p.rows * p.hq) return;
@@ -631,7 +635,8 @@ cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cud
       if (e != cudaSuccess) return e;
       configured[1] = true;
     }
-    decode_partial_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
+    e = launch_pdl(decode_partial_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
+    if (e != cudaSuccess) return e;
   } else {
     if (!configured[0]) {
       e = cudaFuncSetAttribute(decode_partial_kernel<false>,
@@ -639,7 +644,8 @@ cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cud
       if (e != cudaSuccess) return e;
       configured[0] = true;
     }
-    decode_partial_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
+    e = launch_pdl(decode_partial_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
@@ -647,8 +653,7 @@ cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cud
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
   const int warps = p.rows * p.hq;
   if (warps == 0) return cudaSuccess;
-  merge_kernel<<<(warps + 7) / 8, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel, dim3((warps + 7) / 8), dim3(256), 0, s, p);
 }
 
 }  // namespace tfpa

@@ -598,6 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   __syncthreads();
   umma::fence_after_sync();
   const uint32_t tmem = *b.tmem_slot;
+  allow_next_grid();
+  wait_prior_grid();
 
   const Tile x = tile_of(p, blockIdx.x);
   const RunInfo& ru = p.runs[x.run];
@@ -644,8 +646,8 @@ cudaError_t launch(const PrefillParams& p, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  prefill_kernel<FP8><<<grid, kThreads, Layout<FP8>::kSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(prefill_kernel<FP8>, dim3(grid), dim3(kThreads), Layout<FP8>::kSmemBytes,
+                    s, p);
 }
 
 }  // namespace

@@ -13,6 +13,8 @@
 namespace tfpa {
 
 __global__ void __launch_bounds__(256) write_kv_kernel(const __grid_constant__ WriteParams p) {
+  allow_next_grid();
+  wait_prior_grid();
   const int gid = blockIdx.x * 16 + (threadIdx.x >> 4);  // (row, head) pair
   const int t = threadIdx.x & 15;                          // 8-element slice
   if (gid >= p.rows * p.hkv) return;
@@ -73,8 +75,7 @@ cudaError_t launch_write_kv(const WriteParams& p, cudaStream_t s) {
   const int pairs = p.rows * p.hkv;
   const int grid = (pairs + 15) / 16;
   if (grid == 0) return cudaSuccess;
-  write_kv_kernel<<<grid, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(write_kv_kernel, dim3(grid), dim3(256), 0, s, p);
 }
 
 }  // namespace tfpa
