@@ -34,7 +34,7 @@ constexpr int kCombWarps = 4;         // the combine buffer holds four warps' O
 constexpr int kCombBytes = kCombWarps * 16 * kCombRow * 4;
 constexpr int kMlBytes = kConsumerWarps * 16 * 2 * 4;
 constexpr int kSmemBytes =
-    kStages * kStageBytes + kCombBytes + kMlBytes + kStages * 4 + (2 * kStages + 2) * 8 + 1024;
+    kStages * kStageBytes + kCombBytes + kMlBytes + kStages * 4 + (2 * kStages + 4) * 8 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
@@ -146,15 +146,6 @@ __device__ __forceinline__ int out_col(int nt, int n) {
   return nt < 8 ? 8 * n + nt : 64 + 8 * n + (nt - 8);
 }
 
-// Bounded barrier among the consumer warps (an mbarrier of count 8).
-__device__ __forceinline__ bool consumers_sync(uint64_t* bar, uint32_t& phase, int32_t* err) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-  const bool ok = mbar_wait(bar, phase & 1, err);
-  ++phase;
-  return ok;
-}
-
 // Query fragments of rows gq and gq+8 of an m-tile, the rows' causal limits
 // and their score multipliers (f16 operands for e4m3 caches: each row is
 // scaled by a power of two into f16 range, exact for every element within
@@ -219,16 +210,22 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, const RunInfo& ru,
   }
 }
 
+struct CombBars {
+  uint64_t* comb_post;   // all 8 warps posted (m, l) and warps 4..7 their O
+  uint64_t* comb_fold;   // warps 0..3 folded their pair's O
+  uint64_t* comb_free;   // warps 0..3 finished reading the buffer
+};
+
 template <bool FP8>
 __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* full,
                          uint64_t* empty, const int* stage_bad, float* comb, float* comb_ml,
-                         uint64_t* cbar) {
+                         CombBars bars) {
   using C = Cfg<FP8>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int gq = lane >> 2, c = lane & 3;
   const uint32_t sbase = smem_u32(stage_mem);
-  uint32_t stage = 0, cphase = 0;
+  uint32_t stage = 0;
   int ib, ie;
   cta_items(p.n_items, ib, ie);
   int q_run = -1, q_g = -1, q_mt = -1;     // the m-tile whose query is loaded
@@ -422,14 +419,23 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
     }
 
     // ---- combine the eight warps' states in a fixed order:
-    // (1) every warp posts (m, l); warps 4..7 post O;
+    // (1) every warp posts (m, l); warps 4..7 post O and go on to the next
+    //     item at once (they only wait, before posting again, until the
+    //     previous item's combine has read the buffer);
     // (2) warp w < 4 folds warp w+4's O into its own, rescaled to the
     //     eight-warp max, and posts the sum;
-    // (3) 128 threads add the four posted O's in order and write the partial.
+    // (3) warps 0..3 add the four posted O's in order and write the partial.
+    // Each barrier completes once per item, so parity = item index & 1.
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
       l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
+    }
+    const uint32_t par = (uint32_t)(it - ib) & 1u;
+    const int slot = warp & (kCombWarps - 1);
+    float* cw = comb + slot * 16 * kCombRow;
+    if (warp >= kCombWarps && it > ib) {
+      if (!mbar_wait(bars.comb_free, par ^ 1u, p.err_flag)) return;
     }
     if (c == 0) {
       comb_ml[(warp * 16 + gq) * 2 + 0] = m_run[0];
@@ -437,8 +443,6 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
       comb_ml[(warp * 16 + gq + 8) * 2 + 0] = m_run[1];
       comb_ml[(warp * 16 + gq + 8) * 2 + 1] = l_run[1];
     }
-    const int slot = warp & (kCombWarps - 1);
-    float* cw = comb + slot * 16 * kCombRow;
     if (warp >= kCombWarps) {
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
@@ -448,9 +452,14 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
         cw[(gq + 8) * kCombRow + d0] = o[nt][2];
         cw[(gq + 8) * kCombRow + d1] = o[nt][3];
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.comb_post);
+      continue;
     }
-    if (!consumers_sync(cbar, cphase, p.err_flag)) return;
-    if (warp < kCombWarps) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.comb_post);
+    if (!mbar_wait(bars.comb_post, par, p.err_flag)) return;
+    {
       float a_me[2], a_pair[2];
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
@@ -475,9 +484,11 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
         *p3 = a_me[1] * o[nt][3] + a_pair[1] * *p3;
       }
     }
-    if (!consumers_sync(cbar, cphase, p.err_flag)) return;
-    if (warp < kCombWarps) {
-      const int t = threadIdx.x;          // 0..127
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.comb_fold);
+    if (!mbar_wait(bars.comb_fold, par, p.err_flag)) return;
+    {
+      const int t = threadIdx.x;          // 0..127 (warps 0..3)
       const int row = t >> 3;             // m-tile row
       const int d0 = (t & 7) * 16;
       const int qv = x.mt * 16 + row;
@@ -516,7 +527,8 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
         }
       }
     }
-    if (!consumers_sync(cbar, cphase, p.err_flag)) return;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.comb_free);
   }
 }
 
@@ -534,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
       (reinterpret_cast<uintptr_t>(stage_bad + kStages) + 7) & ~uintptr_t(7));
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
-  uint64_t* cbar = bars + 2 * kStages;
+  CombBars cb{bars + 2 * kStages, bars + 2 * kStages + 1, bars + 2 * kStages + 2};
 
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
@@ -542,7 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
-    mbar_init(cbar, kConsumerWarps);
+    mbar_init(cb.comb_post, kConsumerWarps);
+    mbar_init(cb.comb_fold, kCombWarps);
+    mbar_init(cb.comb_free, kCombWarps);
     fence_mbar_init();
   }
   if (warp == kProducerWarp && (threadIdx.x & 31) == 0) {
@@ -557,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
   if (warp == kProducerWarp)
     producer<FP8>(p, stage_mem, full, empty, stage_bad);
   else
-    consumer<FP8>(p, stage_mem, full, empty, stage_bad, comb, comb_ml, cbar);
+    consumer<FP8>(p, stage_mem, full, empty, stage_bad, comb, comb_ml, cb);
 }
 
 // ---------------------------------------------------------------- merge
