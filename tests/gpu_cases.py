@@ -26,11 +26,16 @@ class WKey:
     def __init__(self, w):
         self.w = w
 
+    def _key(self):
+        w = self.w
+        return (w.name, w.seed, w.hq, w.hkv, w.d, w.kv_dtype,
+                tuple(st.seq_len for st in w.streams))
+
     def __hash__(self):
-        return hash((self.w.name, self.w.seed, tuple(st.seq_len for st in self.w.streams)))
+        return hash(self._key())
 
     def __eq__(self, o):
-        return hash(self) == hash(o)
+        return self._key() == o._key()
 
 
 def fp8_scales(w):

@@ -56,7 +56,7 @@ def test_gqa_group_sizes(hq, hkv, kv):
 def test_stream_lengths_around_page_edges(L):
     w = _make([L, L], [True, False], [0, 1], [L - 1, L - 1])
     _check(w, f"decode L={L}")
-    _check(_make([L], [True], list(range(L)), list(range(L))), f"prefill L={L}", prefill=True)
+    _check(_make([L], [True], [0] * L, list(range(L))), f"prefill L={L}", prefill=True)
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
