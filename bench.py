@@ -273,7 +273,7 @@ def time_decode(w, torch, B, steps, warmup, dist):
 def time_e2e(w, torch, B, ctx, steps, warmup):
     """Through the public API with host buffers: per step, copy the step's
     inputs (q and the new K/V rows) from pinned host memory, run the step and
-    read the output back to the host."""
+    read the output back to the host (host clock, one sync per step)."""
     cache, segs, _, sc, out = ctx
     nst = len(w.streams)
     hq = torch.randn(w.rows, w.hq, 128).to(torch.bfloat16).pin_memory()
@@ -286,21 +286,35 @@ def time_e2e(w, torch, B, ctx, steps, warmup):
     last = np.array([st.seq_len - 1 for st in w.streams], np.int32)
     sidx = np.arange(nst, dtype=np.int32)
 
-    def step():
+    def enqueue():
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
         B.tfpa_write_kv(cache, segs, dk, dv, sidx, last)
         B.tfpa_decode(cache, segs, dq, w.row_seg, w.row_pos, w.softmax_scale, sc, out)
         hout.copy_(out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
 
     for _ in range(warmup):
-        step()
+        enqueue()
     torch.cuda.synchronize()
+    # The whole step (copies in, kernels, copy out) as one CUDA graph; the
+    # host waits for each step's output before starting the next.
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            enqueue()
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        graph.replay()
+        s.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
-        step()
+        graph.replay()
+        s.synchronize()
     dt = (time.perf_counter() - t0) / steps
     h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
     return dt, h2d, hout.numel() * 2
