@@ -6,20 +6,28 @@
 // items (run, kv head g, m-tile of 16 query vectors, split).  A split is a
 // fixed number of whole pages chosen from the stream's own length, so a
 // row's partials never depend on its batch or on how rows are sliced.
-// Per CTA:
-//   warp 8      producer: looks each page up once (PR #2011, "the decode
+// Per CTA (four warpgroups):
+//   warp 12     producer: looks each page up once (PR #2011, "the decode
 //               tiles ... look a page up once"), stages K and V chunks into
 //               shared memory with TMA tiled loads (128B swizzle), 3 stages
 //               of 64 KB;
 //   warps 0..7  consumers: each takes an eighth of every chunk's keys, runs
 //               QK^T and PV on mma.sync m16n8k16 (bf16, or f16 for e4m3
 //               caches, whose bytes convert to f16 exactly) and an online
-//               softmax reduced with warp shuffles; at the end of an item the
-//               eight warps' states are combined in a fixed order.
+//               softmax reduced with warp shuffles; at the end of an item
+//               each warp stores its state (O, m, l) into tensor memory and
+//               goes straight on to the next item;
+//   warps 8..11 combiners: warp 8+q reads the states of consumer warps q and
+//               q+4 (the two warps that share its TMEM lane quarter and its
+//               fragment layout), folds them, and the four combiners add
+//               their folds in a fixed order and write the partial.
+// TMEM holds two items' states, so the combine of one item overlaps the
+// next item's loads and math.
 // Paged and slab streams differ only in the TMA row coordinate, so they
 // produce the same bytes (PR #1373, "What changes").
 #include "common.cuh"
 #include "params.h"
+#include "tcgen05.cuh"
 
 namespace tfpa {
 namespace {
@@ -27,14 +35,27 @@ namespace {
 constexpr int kStages = 3;
 constexpr int kStageBytes = 65536;    // K 32 KB + V 32 KB
 constexpr int kConsumerWarps = 8;
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kCombRow = 130;         // padded float row of the combine buffer
-constexpr int kCombWarps = 4;         // the combine buffer holds four warps' O
-constexpr int kCombBytes = kCombWarps * 16 * kCombRow * 4;
+constexpr int kCombineWarp0 = 8;      // warps 8..11
+constexpr int kCombineWarps = 4;
+constexpr int kProducerWarp = 12;     // warps 13..15 only take part in the register split
+constexpr int kThreads = 16 * 32;
+// Registers after the split: the block launches with 512 x 128 = 65,536 and
+// 128 x (2 x kRegsConsumer + kRegsCombine + kRegsProducer) must not exceed it.
+constexpr int kRegsConsumer = 184;
+constexpr int kRegsCombine = 104;
+constexpr int kRegsProducer = 40;
+static_assert(128 * (2 * kRegsConsumer + kRegsCombine + kRegsProducer) <= 65536, "register split");
+// TMEM: two buffers (item parity) x two halves (consumer warps q, q+4) of
+// 64 O columns + (m0, l0, m1, l1); lane quarter q belongs to warps q, q+4, 8+q.
+constexpr int kTmemCols = 512;
+constexpr int kBufCols = 256;
+constexpr int kHalfCols = 128;
+constexpr int kCombRow = 130;         // padded float row of the fold buffer
+constexpr int kCombBytes = kCombineWarps * 16 * kCombRow * 4;
 constexpr int kMlBytes = kConsumerWarps * 16 * 2 * 4;
+constexpr int kNumBars = 2 * kStages + 7;
 constexpr int kSmemBytes =
-    kStages * kStageBytes + kCombBytes + kMlBytes + kStages * 4 + (2 * kStages + 4) * 8 + 1024;
+    kStages * kStageBytes + kCombBytes + kMlBytes + kStages * 4 + 4 + kNumBars * 8 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
@@ -211,15 +232,16 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, const RunInfo& ru,
 }
 
 struct CombBars {
-  uint64_t* comb_post;   // all 8 warps posted (m, l) and warps 4..7 their O
-  uint64_t* comb_fold;   // warps 0..3 folded their pair's O
-  uint64_t* comb_free;   // warps 0..3 finished reading the buffer
+  uint64_t* posted;      // [2] by item parity: the 8 consumer warps stored their state
+  uint64_t* tmem_free;   // [2] by item parity: the combiners read that TMEM buffer
+  uint64_t* pub;         // the combiners published their pairs' (m, l)
+  uint64_t* folded;      // the combiners wrote their folds
+  uint64_t* done;        // the combiners finished the item (fold buffer free)
 };
 
 template <bool FP8>
 __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* full,
-                         uint64_t* empty, const int* stage_bad, float* comb, float* comb_ml,
-                         CombBars bars) {
+                         uint64_t* empty, const int* stage_bad, uint32_t tmem, CombBars bars) {
   using C = Cfg<FP8>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -239,7 +261,6 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
     const RunInfo& ru = p.runs[x.run];
     int klo, khi;
     item_keys(p, x, klo, khi);
-    const int nq = ru.nrows * p.group;
     if (x.run != q_run || x.g != q_g || x.mt != q_mt) {
       load_q<FP8>(p, ru, x, gq, c, qr, lim, sc);
       maxlim = __reduce_max_sync(0xffffffffu, max(lim[0], lim[1]));
@@ -418,89 +439,138 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
       if (lane == 0) mbar_arrive(&empty[buf]);
     }
 
-    // ---- combine the eight warps' states in a fixed order:
-    // (1) every warp posts (m, l); warps 4..7 post O and go on to the next
-    //     item at once (they only wait, before posting again, until the
-    //     previous item's combine has read the buffer);
-    // (2) warp w < 4 folds warp w+4's O into its own, rescaled to the
-    //     eight-warp max, and posts the sum;
-    // (3) warps 0..3 add the four posted O's in order and write the partial.
-    // Each barrier completes once per item, so parity = item index & 1.
+    // ---- hand the state to the combiners: O and (m, l) into this warp's
+    // lanes of TMEM buffer (item & 1), once the combine of item - 2 has
+    // read that buffer.
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
       l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
     }
-    const uint32_t par = (uint32_t)(it - ib) & 1u;
-    const int slot = warp & (kCombWarps - 1);
-    float* cw = comb + slot * 16 * kCombRow;
-    if (warp >= kCombWarps && it > ib) {
-      if (!mbar_wait(bars.comb_free, par ^ 1u, p.err_flag)) return;
-    }
-    if (c == 0) {
-      comb_ml[(warp * 16 + gq) * 2 + 0] = m_run[0];
-      comb_ml[(warp * 16 + gq) * 2 + 1] = l_run[0];
-      comb_ml[(warp * 16 + gq + 8) * 2 + 0] = m_run[1];
-      comb_ml[(warp * 16 + gq + 8) * 2 + 1] = l_run[1];
-    }
-    if (warp >= kCombWarps) {
+    const int rel = it - ib;
+    const int b = rel & 1;
+    if (rel >= 2 &&
+        !mbar_wait(&bars.tmem_free[b], (uint32_t)((rel >> 1) - 1) & 1u, p.err_flag))
+      return;
+    umma::fence_after_sync();
+    const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) +
+                        (uint32_t)(b * kBufCols + (warp >> 2) * kHalfCols);
+    {
+      uint32_t ov[64];
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
-        const int d0 = out_col<FP8>(nt, 2 * c), d1 = out_col<FP8>(nt, 2 * c + 1);
-        cw[gq * kCombRow + d0] = o[nt][0];
-        cw[gq * kCombRow + d1] = o[nt][1];
-        cw[(gq + 8) * kCombRow + d0] = o[nt][2];
-        cw[(gq + 8) * kCombRow + d1] = o[nt][3];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ov[4 * nt + j] = __float_as_uint(o[nt][j]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars.comb_post);
-      continue;
+      umma::tmem_st64(ta, ov);
+      const uint32_t ml[4] = {__float_as_uint(m_run[0]), __float_as_uint(l_run[0]),
+                              __float_as_uint(m_run[1]), __float_as_uint(l_run[1])};
+      umma::tmem_st4(ta + 64, ml);
     }
+    umma::tmem_st_wait();
+    umma::fence_before_sync();
     __syncwarp();
-    if (lane == 0) mbar_arrive(bars.comb_post);
-    if (!mbar_wait(bars.comb_post, par, p.err_flag)) return;
-    {
-      float a_me[2], a_pair[2];
+    if (lane == 0) mbar_arrive(&bars.posted[b]);
+  }
+}
+
+// Combiner warp 8+q: for every item of the CTA, reads the states of consumer
+// warps q and q+4 from TMEM, and
+// (1) publishes their (m, l) so that each combiner knows the eight-warp max;
+// (2) folds the two O's, each rescaled to that max, into fold slot q;
+// (3) with the other combiners, adds the four slots in order and writes the
+//     partial (o, m, l).  The sums are taken in a fixed order, so a partial's
+//     bits depend only on its keys.
+// Each of pub, folded and done completes once per item (parity = item & 1);
+// a combiner waits for done of the previous item before publishing, so the
+// fold and (m, l) buffers are never overwritten while still being read.
+template <bool FP8>
+__device__ void combiner(const DecodeParams& p, uint32_t tmem, float* comb, float* ml_buf,
+                         CombBars bars) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int q = warp - kCombineWarp0;
+  const int gq = lane >> 2, c = lane & 3;
+  int ib, ie;
+  cta_items(p.n_items, ib, ie);
+  float* cw = comb + q * 16 * kCombRow;
+  const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+  for (int it = ib; it < ie; ++it) {
+    const Item x = item_of(p, it);
+    const RunInfo& ru = p.runs[x.run];
+    const int nq = ru.nrows * p.group;
+    const int rel = it - ib;
+    const int b = rel & 1;
+    const uint32_t par = (uint32_t)rel & 1u;
+    if (!mbar_wait(&bars.posted[b], (uint32_t)(rel >> 1) & 1u, p.err_flag)) return;
+    umma::fence_after_sync();
+    const uint32_t tA = tl + (uint32_t)(b * kBufCols);          // consumer warp q
+    const uint32_t tB = tA + kHalfCols;                          // consumer warp q + 4
+    uint32_t mlA[4], mlB[4];
+    umma::tmem_ld4(tA + 64, mlA);
+    umma::tmem_ld4(tB + 64, mlB);
+    umma::tmem_ld_wait();
+    if (rel > 0 && !mbar_wait(bars.done, par ^ 1u, p.err_flag)) return;
+    if (c == 0) {
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int row = gq + 8 * hr;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_ml[(w * 16 + row) * 2]);
-        const float mp = comb_ml[((warp + kCombWarps) * 16 + row) * 2];
-        a_me[hr] = m_run[hr] == -INFINITY ? 0.f : fast_exp2(m_run[hr] - M);
-        a_pair[hr] = mp == -INFINITY ? 0.f : fast_exp2(mp - M);
-      }
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int d0 = out_col<FP8>(nt, 2 * c), d1 = out_col<FP8>(nt, 2 * c + 1);
-        float* p0 = &cw[gq * kCombRow + d0];
-        float* p1 = &cw[gq * kCombRow + d1];
-        float* p2 = &cw[(gq + 8) * kCombRow + d0];
-        float* p3 = &cw[(gq + 8) * kCombRow + d1];
-        *p0 = a_me[0] * o[nt][0] + a_pair[0] * *p0;
-        *p1 = a_me[0] * o[nt][1] + a_pair[0] * *p1;
-        *p2 = a_me[1] * o[nt][2] + a_pair[1] * *p2;
-        *p3 = a_me[1] * o[nt][3] + a_pair[1] * *p3;
+        ml_buf[(q * 16 + row) * 2 + 0] = __uint_as_float(mlA[2 * hr]);
+        ml_buf[(q * 16 + row) * 2 + 1] = __uint_as_float(mlA[2 * hr + 1]);
+        ml_buf[((q + 4) * 16 + row) * 2 + 0] = __uint_as_float(mlB[2 * hr]);
+        ml_buf[((q + 4) * 16 + row) * 2 + 1] = __uint_as_float(mlB[2 * hr + 1]);
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(bars.comb_fold);
-    if (!mbar_wait(bars.comb_fold, par, p.err_flag)) return;
+    if (lane == 0) mbar_arrive(bars.pub);
+    if (!mbar_wait(bars.pub, par, p.err_flag)) return;
+    float aA[2], aB[2];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int row = gq + 8 * hr;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ml_buf[(w * 16 + row) * 2]);
+      const float mA = __uint_as_float(mlA[2 * hr]), mB = __uint_as_float(mlB[2 * hr]);
+      aA[hr] = mA == -INFINITY ? 0.f : fast_exp2(mA - M);
+      aB[hr] = mB == -INFINITY ? 0.f : fast_exp2(mB - M);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t xa[16], xb[16];
+      umma::tmem_ld16(tA + 16 * k, xa);
+      umma::tmem_ld16(tB + 16 * k, xb);
+      umma::tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int f = 16 * k + i;               // o[nt][j] of the consumer, f = 4 nt + j
+        const int nt = f >> 2, j = f & 3, hr = j >> 1;
+        const int col = out_col<FP8>(nt, 2 * c + (j & 1));
+        cw[(gq + 8 * hr) * kCombRow + col] =
+            __fmaf_rn(aB[hr], __uint_as_float(xb[i]), __fmul_rn(aA[hr], __uint_as_float(xa[i])));
+      }
+    }
+    umma::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&bars.tmem_free[b]);
+      mbar_arrive(bars.folded);
+    }
+    if (!mbar_wait(bars.folded, par, p.err_flag)) return;
     {
-      const int t = threadIdx.x;          // 0..127 (warps 0..3)
+      const int t = threadIdx.x - kCombineWarp0 * 32;   // 0..127
       const int row = t >> 3;             // m-tile row
       const int d0 = (t & 7) * 16;
       const int qv = x.mt * 16 + row;
       if (qv < nq) {
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_ml[(w * 16 + row) * 2]);
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ml_buf[(w * 16 + row) * 2]);
         float L = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
-          const float mw = comb_ml[(w * 16 + row) * 2];
-          const float lw = comb_ml[(w * 16 + row) * 2 + 1];
+          const float mw = ml_buf[(w * 16 + row) * 2];
+          const float lw = ml_buf[(w * 16 + row) * 2 + 1];
           L += (mw == -INFINITY ? 0.f : fast_exp2(mw - M)) * lw;
         }
         const float vs = FP8 ? __ldg(p.v_scale + x.g) : 1.f;
@@ -515,7 +585,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
           for (int e = 0; e < 4; ++e) {
             float acc = 0.f;
 #pragma unroll
-            for (int w = 0; w < kCombWarps; ++w)
+            for (int w = 0; w < kCombineWarps; ++w)
               acc += comb[(w * 16 + row) * kCombRow + d0 + 4 * j + e];
             v[e] = acc * vs;
           }
@@ -528,7 +598,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(bars.comb_free);
+    if (lane == 0) mbar_arrive(bars.done);
   }
 }
 
@@ -540,13 +610,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
                                              ~uintptr_t(1023));
   uint8_t* stage_mem = smem;
   float* comb = reinterpret_cast<float*>(smem + kStages * kStageBytes);
-  float* comb_ml = comb + kCombWarps * 16 * kCombRow;
-  int* stage_bad = reinterpret_cast<int*>(comb_ml + kConsumerWarps * 16 * 2);
+  float* ml_buf = comb + kCombineWarps * 16 * kCombRow;
+  int* stage_bad = reinterpret_cast<int*>(ml_buf + kConsumerWarps * 16 * 2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stage_bad + kStages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(stage_bad + kStages) + 7) & ~uintptr_t(7));
+      (reinterpret_cast<uintptr_t>(tmem_slot + 1) + 7) & ~uintptr_t(7));
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
-  CombBars cb{bars + 2 * kStages, bars + 2 * kStages + 1, bars + 2 * kStages + 2};
+  uint64_t* cbar = bars + 2 * kStages;
+  CombBars cb{cbar, cbar + 2, cbar + 4, cbar + 5, cbar + 6};
 
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
@@ -554,9 +626,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
-    mbar_init(cb.comb_post, kConsumerWarps);
-    mbar_init(cb.comb_fold, kCombWarps);
-    mbar_init(cb.comb_free, kCombWarps);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&cb.posted[i], kConsumerWarps);
+      mbar_init(&cb.tmem_free[i], kCombineWarps);
+    }
+    mbar_init(cb.pub, kCombineWarps);
+    mbar_init(cb.folded, kCombineWarps);
+    mbar_init(cb.done, kCombineWarps);
     fence_mbar_init();
   }
   if (warp == kProducerWarp && (threadIdx.x & 31) == 0) {
@@ -565,13 +641,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
       tma_prefetch_desc(&p.maps[i].v);
     }
   }
+  if (warp == kCombineWarp0) umma::tmem_alloc(tmem_slot, kTmemCols);
+  umma::fence_before_sync();
   __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
   allow_next_grid();
   wait_prior_grid();
-  if (warp == kProducerWarp)
-    producer<FP8>(p, stage_mem, full, empty, stage_bad);
-  else
-    consumer<FP8>(p, stage_mem, full, empty, stage_bad, comb, comb_ml, cb);
+  if (warp < kCombineWarp0) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsConsumer));
+    consumer<FP8>(p, stage_mem, full, empty, stage_bad, tmem, cb);
+  } else if (warp < kProducerWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCombine));
+    combiner<FP8>(p, tmem, comb, ml_buf, cb);
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
+    if (warp == kProducerWarp) producer<FP8>(p, stage_mem, full, empty, stage_bad);
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  if (warp == kCombineWarp0) {
+    umma::fence_after_sync();
+    umma::tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 // ---------------------------------------------------------------- merge
@@ -636,32 +728,33 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
   if (p.lse && lane == 0) p.lse[(size_t)row * p.hq + h] = (M + log2f(L)) * 0.6931471805599453f;
 }
 
+template <bool FP8>
+cudaError_t launch_partial(const DecodeParams& p, int grid, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    // The register split only works if the block launches with at least the
+    // registers it hands out; otherwise setmaxnreg.inc would wait forever.
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, decode_partial_kernel<FP8>);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs * kThreads < 128 * (2 * kRegsConsumer + kRegsCombine + kRegsProducer))
+      return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(decode_partial_kernel<FP8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaError_t e =
+      launch_pdl(decode_partial_kernel<FP8>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cudaStream_t s) {
   if (grid <= 0 || p.n_items == 0) return cudaSuccess;
-  static bool configured[2] = {false, false};
-  cudaError_t e;
-  if (fp8) {
-    if (!configured[1]) {
-      e = cudaFuncSetAttribute(decode_partial_kernel<true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (e != cudaSuccess) return e;
-      configured[1] = true;
-    }
-    e = launch_pdl(decode_partial_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
-    if (e != cudaSuccess) return e;
-  } else {
-    if (!configured[0]) {
-      e = cudaFuncSetAttribute(decode_partial_kernel<false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (e != cudaSuccess) return e;
-      configured[0] = true;
-    }
-    e = launch_pdl(decode_partial_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaGetLastError();
+  return fp8 ? launch_partial<true>(p, grid, s) : launch_partial<false>(p, grid, s);
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
