@@ -42,16 +42,17 @@ constexpr int kThreads = 16 * 32;
 // Registers after the split: the block launches with 512 x 128 = 65,536 and
 // 128 x (2 x kRegsConsumer + kRegsCombine + kRegsProducer) must not exceed it.
 constexpr int kRegsConsumer = 184;
-constexpr int kRegsCombine = 104;
-constexpr int kRegsProducer = 40;
+constexpr int kRegsCombine = 112;
+constexpr int kRegsProducer = 32;
 static_assert(128 * (2 * kRegsConsumer + kRegsCombine + kRegsProducer) <= 65536, "register split");
 // TMEM: two buffers (item parity) x two halves (consumer warps q, q+4) of
 // 64 O columns + (m0, l0, m1, l1); lane quarter q belongs to warps q, q+4, 8+q.
 constexpr int kTmemCols = 512;
 constexpr int kBufCols = 256;
 constexpr int kHalfCols = 128;
-constexpr int kCombRow = 130;         // padded float row of the fold buffer
-constexpr int kCombBytes = kCombineWarps * 16 * kCombRow * 4;
+// Fold buffer: [slot q][PV n-tile][lane] float4, the C-fragment order of the
+// consumer warps (conflict-free float4 stores and loads).
+constexpr int kCombBytes = kCombineWarps * 16 * 32 * 16;
 constexpr int kMlBytes = kConsumerWarps * 16 * 2 * 4;
 constexpr int kNumBars = 2 * kStages + 7;
 constexpr int kSmemBytes =
@@ -478,14 +479,14 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
 // warps q and q+4 from TMEM, and
 // (1) publishes their (m, l) so that each combiner knows the eight-warp max;
 // (2) folds the two O's, each rescaled to that max, into fold slot q;
-// (3) with the other combiners, adds the four slots in order and writes the
-//     partial (o, m, l).  The sums are taken in a fixed order, so a partial's
-//     bits depend only on its keys.
+// (3) adds the four slots in order for PV n-tiles 4q..4q+3 and writes that
+//     part of the partial o (warp 8 also writes m and l).  The sums are
+//     taken in a fixed order, so a partial's bits depend only on its keys.
 // Each of pub, folded and done completes once per item (parity = item & 1);
 // a combiner waits for done of the previous item before publishing, so the
 // fold and (m, l) buffers are never overwritten while still being read.
 template <bool FP8>
-__device__ void combiner(const DecodeParams& p, uint32_t tmem, float* comb, float* ml_buf,
+__device__ void combiner(const DecodeParams& p, uint32_t tmem, float4* fold, float* ml_buf,
                          CombBars bars) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -493,7 +494,6 @@ __device__ void combiner(const DecodeParams& p, uint32_t tmem, float* comb, floa
   const int gq = lane >> 2, c = lane & 3;
   int ib, ie;
   cta_items(p.n_items, ib, ie);
-  float* cw = comb + q * 16 * kCombRow;
   const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
   for (int it = ib; it < ie; ++it) {
     const Item x = item_of(p, it);
@@ -524,17 +524,18 @@ __device__ void combiner(const DecodeParams& p, uint32_t tmem, float* comb, floa
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.pub);
     if (!mbar_wait(bars.pub, par, p.err_flag)) return;
-    float aA[2], aB[2];
+    float M[2], aA[2], aB[2];
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int row = gq + 8 * hr;
-      float M = -INFINITY;
+      M[hr] = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ml_buf[(w * 16 + row) * 2]);
+      for (int w = 0; w < kConsumerWarps; ++w) M[hr] = fmaxf(M[hr], ml_buf[(w * 16 + row) * 2]);
       const float mA = __uint_as_float(mlA[2 * hr]), mB = __uint_as_float(mlB[2 * hr]);
-      aA[hr] = mA == -INFINITY ? 0.f : fast_exp2(mA - M);
-      aB[hr] = mB == -INFINITY ? 0.f : fast_exp2(mB - M);
+      aA[hr] = mA == -INFINITY ? 0.f : fast_exp2(mA - M[hr]);
+      aB[hr] = mB == -INFINITY ? 0.f : fast_exp2(mB - M[hr]);
     }
+    // fold: TMEM column f of a consumer lane holds o[f / 4][f % 4]
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       uint32_t xa[16], xb[16];
@@ -542,12 +543,14 @@ __device__ void combiner(const DecodeParams& p, uint32_t tmem, float* comb, floa
       umma::tmem_ld16(tB + 16 * k, xb);
       umma::tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int f = 16 * k + i;               // o[nt][j] of the consumer, f = 4 nt + j
-        const int nt = f >> 2, j = f & 3, hr = j >> 1;
-        const int col = out_col<FP8>(nt, 2 * c + (j & 1));
-        cw[(gq + 8 * hr) * kCombRow + col] =
-            __fmaf_rn(aB[hr], __uint_as_float(xb[i]), __fmul_rn(aA[hr], __uint_as_float(xa[i])));
+      for (int u = 0; u < 4; ++u) {
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = 4 * u + j, hr = j >> 1;
+          v[j] = __fmaf_rn(aB[hr], __uint_as_float(xb[i]), __fmul_rn(aA[hr], __uint_as_float(xa[i])));
+        }
+        fold[(q * 16 + 4 * k + u) * 32 + lane] = make_float4(v[0], v[1], v[2], v[3]);
       }
     }
     umma::fence_before_sync();
@@ -557,42 +560,52 @@ __device__ void combiner(const DecodeParams& p, uint32_t tmem, float* comb, floa
       mbar_arrive(bars.folded);
     }
     if (!mbar_wait(bars.folded, par, p.err_flag)) return;
+    // final: n-tiles 4q..4q+3 of this lane's fragment, summed over the slots
     {
-      const int t = threadIdx.x - kCombineWarp0 * 32;   // 0..127
-      const int row = t >> 3;             // m-tile row
-      const int d0 = (t & 7) * 16;
-      const int qv = x.mt * 16 + row;
-      if (qv < nq) {
-        float M = -INFINITY;
+      float4 acc[4];
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ml_buf[(w * 16 + row) * 2]);
-        float L = 0.f;
+      for (int u = 0; u < 4; ++u) {
+        const int nt = 4 * q + u;
+        float4 a = fold[nt * 32 + lane];
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float mw = ml_buf[(w * 16 + row) * 2];
-          const float lw = ml_buf[(w * 16 + row) * 2 + 1];
-          L += (mw == -INFINITY ? 0.f : fast_exp2(mw - M)) * lw;
+        for (int sl = 1; sl < kCombineWarps; ++sl) {
+          const float4 t = fold[(sl * 16 + nt) * 32 + lane];
+          a.x += t.x;
+          a.y += t.y;
+          a.z += t.z;
+          a.w += t.w;
         }
-        const float vs = FP8 ? __ldg(p.v_scale + x.g) : 1.f;
+        acc[u] = a;
+      }
+      const float vs = FP8 ? __ldg(p.v_scale + x.g) : 1.f;
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int qv = x.mt * 16 + gq + 8 * hr;
+        if (qv >= nq) continue;
         const int r = qv / p.group;
         const int h = x.g * p.group + (qv - r * p.group);
         const size_t pslot = ((size_t)(ru.row0 + r) * p.hq + h) * p.max_splits + x.sigma;
-        float4* dst = reinterpret_cast<float4*>(p.part_o + pslot * kHeadDim + d0);
+        float* orow = p.part_o + pslot * kHeadDim;
+        // fragment element j = 2 hr + e sits at column out_col(nt, 2c + e);
+        // over nt = 4q..4q+3 those are four consecutive columns
+        const float4 o0 = hr ? make_float4(acc[0].z, acc[1].z, acc[2].z, acc[3].z)
+                             : make_float4(acc[0].x, acc[1].x, acc[2].x, acc[3].x);
+        const float4 o1 = hr ? make_float4(acc[0].w, acc[1].w, acc[2].w, acc[3].w)
+                             : make_float4(acc[0].y, acc[1].y, acc[2].y, acc[3].y);
+        *reinterpret_cast<float4*>(orow + out_col<FP8>(4 * q, 2 * c)) =
+            make_float4(o0.x * vs, o0.y * vs, o0.z * vs, o0.w * vs);
+        *reinterpret_cast<float4*>(orow + out_col<FP8>(4 * q, 2 * c + 1)) =
+            make_float4(o1.x * vs, o1.y * vs, o1.z * vs, o1.w * vs);
+        if (q == 0 && c == 0) {
+          const int row = gq + 8 * hr;
+          float L = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float v[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float acc = 0.f;
-#pragma unroll
-            for (int w = 0; w < kCombineWarps; ++w)
-              acc += comb[(w * 16 + row) * kCombRow + d0 + 4 * j + e];
-            v[e] = acc * vs;
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float mw = ml_buf[(w * 16 + row) * 2];
+            const float lw = ml_buf[(w * 16 + row) * 2 + 1];
+            L += (mw == -INFINITY ? 0.f : fast_exp2(mw - M[hr])) * lw;
           }
-          dst[j] = make_float4(v[0], v[1], v[2], v[3]);
-        }
-        if ((t & 7) == 0) {
-          p.part_ml[pslot * 2 + 0] = M;
+          p.part_ml[pslot * 2 + 0] = M[hr];
           p.part_ml[pslot * 2 + 1] = L;
         }
       }
@@ -609,8 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* stage_mem = smem;
-  float* comb = reinterpret_cast<float*>(smem + kStages * kStageBytes);
-  float* ml_buf = comb + kCombineWarps * 16 * kCombRow;
+  float4* fold = reinterpret_cast<float4*>(smem + kStages * kStageBytes);
+  float* ml_buf = reinterpret_cast<float*>(smem + kStages * kStageBytes + kCombBytes);
   int* stage_bad = reinterpret_cast<int*>(ml_buf + kConsumerWarps * 16 * 2);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stage_bad + kStages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(
@@ -653,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
     consumer<FP8>(p, stage_mem, full, empty, stage_bad, tmem, cb);
   } else if (warp < kProducerWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCombine));
-    combiner<FP8>(p, tmem, comb, ml_buf, cb);
+    combiner<FP8>(p, tmem, fold, ml_buf, cb);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
     if (warp == kProducerWarp) producer<FP8>(p, stage_mem, full, empty, stage_bad);
