@@ -39,10 +39,11 @@ METRIC = "paged decode KV GB/s (% HBM peak); prompt-chunk attn TFLOP/s (% TC pea
 # from ncu (dram__bytes_read.sum + dram__bytes_write.sum, see
 # profiles/decode_partial_batched_decode.md), valid only while the kernel's
 # sources hash to the value it was taken on.
-DECODE_TRAFFIC = {"bytes": 268_600_064 + 5_035_008, "sources_sha256_16": "bba9e1cc957bcaa5"}
+DECODE_TRAFFIC = {"bytes": 268_598_784 + 4_458_240, "sources_sha256_16": "383004a4e26b3207"}
 DECODE_SOURCES = ["paged_kv_cache_235_gb300/csrc/decode.cu",
                   "paged_kv_cache_235_gb300/csrc/common.cuh",
-                  "paged_kv_cache_235_gb300/csrc/params.h"]
+                  "paged_kv_cache_235_gb300/csrc/params.h",
+                  "paged_kv_cache_235_gb300/csrc/tcgen05.cuh"]
 
 
 def decode_traffic():

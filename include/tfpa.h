@@ -144,7 +144,8 @@ int tfpa_decode(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
  * partials live in one array compiled into the library (a file-scope
  * __device__ array of TFPA_STATIC_SCRATCH_SLOTS slots of 130 floats, about
  * 4.3 MB), which every device that loads the library holds until the process
- * exits.  The paper has no counterpart to this entry point.
+ * exits.  None of the TensorFold sources has a counterpart to this entry
+ * point.
  *
  * Same arguments and result as tfpa_decode without `scratch`; rows are
  * processed in slices of TFPA_STATIC_SCRATCH_SLOTS / (hq * TFPA_MAX_SPLITS)
