@@ -37,7 +37,12 @@ namespace {
 
 constexpr int kTileRows = 128;
 constexpr int kTileKeys = 128;
-constexpr int kThreads = 384;
+// bf16: warps 0-11.  e4m3: warps 0-15, warps 12-15 converting the staged
+// e4m3 tiles (one warp per SM sub-partition, beside the softmax warps).
+template <bool FP8>
+constexpr int threads_of() { return FP8 ? 512 : 384; }
+constexpr int kConvWarp0 = 12;
+constexpr int kConvWarps = 4;
 constexpr int kOffQ = 0;                 // 2 heads x [128 rows][128] 16-bit = 64 KB
 constexpr int kOffK = 65536;             // 2 stages x 32 KB (16-bit operand tiles)
 constexpr int kOffV = 131072;            // 2 stages x 32 KB
@@ -50,9 +55,11 @@ struct Layout {
 };
 static_assert(Layout<true>::kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
-constexpr int kRegsLow = 64;       // warps 0-3 after the register split
-constexpr int kRegsHigh = 216;     // warps 4-11
-static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * 168, "register split");
+// e4m3 register split (the block launches with 512 x 128 = 65,536):
+constexpr int kRegsLow = 56;       // warps 0-3: TMA producer, MMA issuer
+constexpr int kRegsHigh = 200;     // warps 4-11: softmax
+constexpr int kRegsConv = 56;      // warps 12-15: converters
+static_assert(128 * (kRegsLow + 2 * kRegsHigh + kRegsConv) <= 512 * 128, "register split");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 __device__ __forceinline__ uint32_t col_s(int hh) { return hh ? 256u : 0u; }
@@ -237,8 +244,8 @@ __device__ __forceinline__ void zero_v_rows(uint8_t* vtile, int z0, int lane) {
 __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int z0, int t) {
   const uint32_t sb = smem_u32(src), db = smem_u32(dst);
 #pragma unroll 4
-  for (int k = 0; k < 16; ++k) {
-    const int i = t + 64 * k;              // (row, 16-byte source chunk)
+  for (int k = 0; k < 8; ++k) {
+    const int i = t + 128 * k;             // (row, 16-byte source chunk)
     const int row = i >> 3, c8 = i & 7;    // source chunk c8 = head dims 16*c8 .. +15
     uint4 w = lds128(swz128(sb, row, c8));
     if (row >= z0) w = make_uint4(0, 0, 0, 0);
@@ -258,10 +265,10 @@ __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, i
   }
 }
 
-// Warps 2-3 for e4m3 caches: staging -> f16 operand stages.
+// Warps 12-15 for e4m3 caches: staging -> f16 operand stages.
 __device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileGeom& gm,
                           uint8_t* smem, const Bars& b) {
-  const int t = threadIdx.x - 64;   // 0..63
+  const int t = threadIdx.x - kConvWarp0 * 32;   // 0..127
   const int lane = threadIdx.x & 31;
   PageCheck pc(p, ru, gm.kend);
   for (int j = 0; j < gm.nkt; ++j) {
@@ -541,7 +548,8 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
 }
 
 template <bool FP8>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(threads_of<FP8>(), 1)
+    prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -566,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    const uint32_t stage_arrivals = FP8 ? 2 : 1;   // the converters, or the producer
+    const uint32_t stage_arrivals = FP8 ? kConvWarps : 1;   // the converters, or the producer
     mbar_init(b.q_full, 1);
     mbar_init(bars + 1, 8);                        // q_ready: the softmax warps
     for (int i = 0; i < 2; ++i) {
@@ -578,9 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       mbar_init(&b.p_ready[i], 4);
     }
     mbar_init(b.k8_full, 1);
-    mbar_init(b.k8_empty, 2);
+    mbar_init(b.k8_empty, kConvWarps);
     mbar_init(b.v8_full, 1);
-    mbar_init(b.v8_empty, 2);
+    mbar_init(b.v8_empty, kConvWarps);
     mbar_init(b.o_final, 1);
     mbar_init(b.drain, 1);
     *b.abort = 0;
@@ -606,21 +614,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const TileGeom gm = geom_of(ru, x);
 
   // Registers (e4m3 caches, where the softmax also holds the Q conversion):
-  // the block launches with 384 x 168 = 64,512; the TMA/MMA/converter
-  // warpgroup needs few, the two softmax warpgroups more:
-  // 128 x kRegsLow + 256 x kRegsHigh <= 64,512.
+  // the block launches with 512 x 128 = 65,536; the TMA/MMA warpgroup and
+  // the converters need few, the two softmax warpgroups more.
   if (warp < 4) {
     if (FP8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 0) {
       if (lane == 0) producer<FP8>(p, ru, x, gm, smem, b);
     } else if (warp == 1) {
       mma_issuer<FP8>(p, ru, gm, smem, tmem, b);
-    } else if (FP8) {
-      converter(p, ru, gm, smem, b);
     }
-  } else {
+  } else if (warp < kConvWarp0) {
     if (FP8) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     softmax_role<FP8>(p, ru, x, gm, (warp - 4) >> 2, smem, tmem, b);
+  } else if (FP8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsConv));
+    converter(p, ru, gm, smem, b);
   }
   umma::fence_before_sync();
   __syncthreads();
@@ -639,15 +647,15 @@ cudaError_t launch(const PrefillParams& p, int grid, cudaStream_t s) {
     cudaFuncAttributes attr;
     cudaError_t e = cudaFuncGetAttributes(&attr, prefill_kernel<FP8>);
     if (e != cudaSuccess) return e;
-    if (FP8 && attr.numRegs * kThreads < 128 * kRegsLow + 256 * kRegsHigh)
+    if (FP8 && attr.numRegs * threads_of<FP8>() < 128 * (kRegsLow + 2 * kRegsHigh + kRegsConv))
       return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(prefill_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Layout<FP8>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_pdl(prefill_kernel<FP8>, dim3(grid), dim3(kThreads), Layout<FP8>::kSmemBytes,
-                    s, p);
+  return launch_pdl(prefill_kernel<FP8>, dim3(grid), dim3(threads_of<FP8>()),
+                    Layout<FP8>::kSmemBytes, s, p);
 }
 
 }  // namespace
