@@ -343,6 +343,29 @@ def time_prefill(w, torch, B, reps):
     return statistics.median(times)
 
 
+def time_decode_calls(w, torch, B, reps, flush):
+    """tfpa_decode (partial + merge) one call at a time, CUDA events around
+    each, optionally with L2 flushed before each call; median in ms."""
+    cache, segs, q = device_case(w, torch, B)
+    sc = B.make_scratch(min(128, w.rows), w.hq)
+    out = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16, device="cuda")
+    buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush else None
+    s = torch.cuda.current_stream()
+    times = []
+    for i in range(reps + 3):
+        if buf is not None:
+            buf.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        B.tfpa_decode(cache, segs, q, w.row_seg, w.row_pos, w.softmax_scale, sc, out)
+        e1.record(s)
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1))
+    assert int(cache.err_flag.item()) == 0, "kernel error flag set"
+    return statistics.median(times)
+
+
 def profile_case(args, torch, B, wl):
     """One workload's kernels only, for profiler captures (a small launch list)."""
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
@@ -468,6 +491,25 @@ def main():
                 "workload": "the same prompt chunk over an e4m3 cache (f16 MMAs)",
                 "ms_per_call": ms5, "tflops": fl5 / (ms5 / 1e3) / 1e12,
                 "frac_of_measured_bf16": fl5 / (ms5 / 1e3) / 1e12 / pk["bf16_tflops"]}
+        w1 = wl.tiny_paged_decode()
+        ms1 = time_decode_calls(w1, torch, B, 50, flush=True)
+        kv1, qo1 = kv_bytes(w1)
+        extra["tiny_decode"] = {
+            "workload": "1 stream, 1 row at position 999, 8/2 heads, bf16, 4 of 16 pool pages; "
+                        "tfpa_decode per call, L2 flushed before each",
+            "us_per_call": ms1 * 1e3, "kv_gbs": (kv1 + qo1) / (ms1 / 1e3) / 1e9,
+            "frac_of_measured_hbm": (kv1 + qo1) / (ms1 / 1e3) / 1e9 / pk["hbm_gbs"],
+            "note": "1 MB of KV: launch and latency bound, the HBM roofline is out of reach"}
+        w6 = wl.overcommitted_pool()
+        ms6 = time_decode_calls(w6, torch, B, 20, flush=False)
+        kv6, qo6 = kv_bytes(w6)
+        extra["overcommitted_pool"] = {
+            "workload": "16 streams of U[1k,109k] positions + one of 262,144, fp8, 32/8 heads, "
+                        "first-fit pool of 5,078 pages after seeded churn, 1 row each; "
+                        "tfpa_decode per call",
+            "seated_streams": len(w6.streams), "waiting_streams": len(w6.waiting),
+            "us_per_call": ms6 * 1e3, "kv_gbs": (kv6 + qo6) / (ms6 / 1e3) / 1e9,
+            "frac_of_measured_hbm": (kv6 + qo6) / (ms6 / 1e3) / 1e9 / pk["hbm_gbs"]}
     value = world * (kv + qo) / (step_ms / 1e3) / 1e9
     achieved = (kv + qo) / (partial_ms / 1e3) / 1e9
     extra["fp8_verify"] = {

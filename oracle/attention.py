@@ -18,6 +18,19 @@ The causal rule: a row at position ``p`` sees keys ``0..p`` inclusive; its own
 K/V are written before it attends.  Masked keys contribute nothing (PR #2011,
 review: masked keys "read offset 0 and land zeros").
 
+Draft-tree verify rows (TensorFold PR #1355, "Follow-up checks": the partial
+kernels index the queries, ``rowseg``, ``rowanc``, the partials and the output
+by row, and a sliced launch shifts the ancestor table with the other row
+tables).  The pages name the per-row ancestor table but do not spell out its
+format; the reading taken here: ``row_anc[r]`` is a 64-bit mask relative to
+the row's own position ``p``.  Bit ``d`` set means the key at position
+``p - d`` is visible to the row; keys more than 63 positions back are always
+visible and keys after ``p`` never are.  A causal chain is every bit set.  A
+draft tree of at most 64 nodes laid out at consecutive positions sets, for
+each node, the bits of its ancestors and itself plus every bit that reaches
+below the tree's first position (the committed prefix).  Bit 0 (the row's own
+key) must be set.
+
 Split partials (TensorFold Issue #1344, "Mechanism": the partial kernels then
 ``attn_merge``): a split covers a page-aligned range of positions; for the
 visible keys in it ``m = max s`` (``-inf`` if none), ``l = sum exp(s - m)``,
@@ -43,13 +56,28 @@ def _check_rows(segs, row_seg, row_pos):
             raise ValueError(f"row {r}: position {p} outside 0..{segs[s].seq_len - 1}")
 
 
+ALL_VISIBLE = (1 << 64) - 1      # the ancestor mask of a causal row
+
+
+def visible_keys(p: int, anc: int = ALL_VISIBLE) -> np.ndarray:
+    """Positions a row at position ``p`` with ancestor mask ``anc`` sees, ascending."""
+    anc = int(anc) & ALL_VISIBLE
+    if not anc & 1:
+        raise ValueError("an ancestor mask must let a row see its own key (bit 0)")
+    keys = [j for j in range(max(0, p - 63), p + 1) if (anc >> (p - j)) & 1]
+    return np.concatenate([np.arange(0, max(0, p - 63), dtype=np.int64),
+                           np.asarray(keys, dtype=np.int64)])
+
+
 def attend(cache: Cache, segs: List[Segment], q_bits: np.ndarray,
-           row_seg: Sequence[int], row_pos: Sequence[int], scale: float):
-    """One-pass causal GQA attention.  Returns (out [rows][hq][d], lse [rows][hq]).
+           row_seg: Sequence[int], row_pos: Sequence[int], scale: float,
+           row_anc: Sequence[int] = None):
+    """One-pass GQA attention.  Returns (out [rows][hq][d], lse [rows][hq]).
 
     ``q_bits`` holds bf16 bit patterns ``[rows][hq][d]``; all arithmetic is
-    float64.  Rows are grouped by segment only so each (segment, kv head) is
-    gathered once; every row is computed on its own.
+    float64.  Rows are causal, or see the keys their ancestor mask
+    ``row_anc[r]`` allows.  Rows are grouped by segment only so each (segment,
+    kv head) is gathered once; every row is computed on its own.
     """
     rows, hq, d = q_bits.shape
     hkv = cache.hkv
@@ -69,7 +97,11 @@ def attend(cache: Cache, segs: List[Segment], q_bits: np.ndarray,
             K, V = gather(cache, segs[s], g, n)
             for r in rs:
                 p = int(row_pos[r])
-                Kp, Vp = K[: p + 1], V[: p + 1]
+                if row_anc is None:
+                    Kp, Vp = K[: p + 1], V[: p + 1]
+                else:
+                    idx = visible_keys(p, row_anc[r])
+                    Kp, Vp = K[idx], V[idx]
                 Q = q[r, g * G:(g + 1) * G]             # [G][d]
                 S = scale * (Q @ Kp.T)                  # [G][p+1]
                 mx = S.max(axis=1, keepdims=True)
@@ -87,7 +119,7 @@ def split_ranges(seq_len: int, pages_per_split: int):
 
 
 def attend_partials(cache: Cache, segs: List[Segment], q_bits: np.ndarray,
-                    row_seg, row_pos, scale: float, pages_per_split):
+                    row_seg, row_pos, scale: float, pages_per_split, row_anc=None):
     """Split partials per (row, head, split).
 
     ``pages_per_split`` is an int or a callable ``seq_len -> int``.  Returns
@@ -113,16 +145,17 @@ def attend_partials(cache: Cache, segs: List[Segment], q_bits: np.ndarray,
         for g in range(hkv):
             K, V = gather(cache, segs[s], g, segs[s].seq_len)
             for h in range(g * G, (g + 1) * G):
+                vis = visible_keys(p, ALL_VISIBLE if row_anc is None else row_anc[r])
                 for si, (lo, hi) in enumerate(ranges[r]):
-                    top = min(hi, p + 1)
-                    if top <= lo:
+                    idx = vis[(vis >= lo) & (vis < hi)]
+                    if idx.size == 0:
                         continue  # no visible key in this split
-                    sc = scale * (K[lo:top] @ q[r, h])
+                    sc = scale * (K[idx] @ q[r, h])
                     mm = sc.max()
                     e = np.exp(sc - mm)
                     m[r, h, si] = mm
                     l[r, h, si] = e.sum()
-                    o[r, h, si] = e @ V[lo:top]
+                    o[r, h, si] = e @ V[idx]
     nsplit = np.array([len(x) for x in ranges], dtype=np.int64)
     return m, l, o, nsplit
 

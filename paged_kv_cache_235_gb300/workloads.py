@@ -63,6 +63,7 @@ class Workload:
     seed: int
     d: int = HEAD_DIM
     waiting: List[int] = field(default_factory=list)  # streams not seated
+    row_anc: Optional[np.ndarray] = None   # uint64 [rows] ancestor masks; None = causal
 
     @property
     def rows(self) -> int:
@@ -113,6 +114,38 @@ def decode_rows(lengths, rows_per_stream):
             seg.append(s)
             pos.append(L - R + i)
     return np.array(seg, dtype=np.int32), np.array(pos, dtype=np.int32)
+
+
+ALL_VISIBLE = (1 << 64) - 1
+
+
+def tree_masks(parents) -> List[int]:
+    """Ancestor masks of a draft tree laid out at consecutive positions.
+
+    Node ``i`` sits at position ``base + i`` and ``parents[i] < i`` is its
+    parent (``parents[0] = -1``: the root).  The mask of node ``i`` is relative
+    to its own position: bit ``d`` set means the key ``d`` positions back is
+    visible.  It holds node ``i``, its ancestors, and every position before
+    the root (the committed prefix).  At most 64 nodes.
+    """
+    n = len(parents)
+    if n > 64:
+        raise ValueError("at most 64 tree nodes")
+    masks = []
+    for i in range(n):
+        m = ALL_VISIBLE & ~((1 << (i + 1)) - 1)      # bits i+1..63: before the root
+        a = i
+        while a >= 0:
+            m |= 1 << (i - a)
+            a = parents[a]
+        masks.append(m)
+    return masks
+
+
+def random_tree(n: int, seed: int) -> List[int]:
+    """Parents of a seeded random recursive tree of ``n`` nodes (node 0 the root)."""
+    rng = np.random.default_rng(seed)
+    return [-1] + [int(rng.integers(0, i)) for i in range(1, n)]
 
 
 def permuted_tables(lengths, paged_flags, num_pages: int, seed: int):
@@ -211,6 +244,23 @@ def fp8_verify(seed: int = 238, seq_len: int = 65536, n_streams: int = 8,
     return Workload("fp8_verify", 32, 8, "fp8", num_pages, streams, rs, rp, seed)
 
 
+def tree_verify(seed: int = 241, seq_len: int = 65536, n_streams: int = 8, nodes: int = 16,
+                kv_dtype: str = "fp8", slack_pages: int = 64) -> Workload:
+    """Draft-tree verify: each stream's last ``nodes`` positions hold a seeded
+    random draft tree, one row per node, attending through ancestor masks."""
+    lengths = [seq_len] * n_streams
+    num_pages = sum(_pages(L) for L in lengths) + slack_pages
+    tables = permuted_tables(lengths, [True] * n_streams, num_pages, seed)
+    streams = [Stream(L, True, t) for L, t in zip(lengths, tables)]
+    rs, rp = decode_rows(lengths, nodes)
+    anc = []
+    for s in range(n_streams):
+        anc += tree_masks(random_tree(nodes, seed * 1_000_003 + 77 + s))
+    w = Workload("tree_verify", 32, 8, kv_dtype, num_pages, streams, rs, rp, seed)
+    w.row_anc = np.array(anc, dtype=np.uint64)
+    return w
+
+
 def prompt_chunk(seed: int = 239, prefix: int = 28672, chunk: int = 4096,
                  slack_pages: int = 32, paged: bool = True, kv_dtype: str = "bf16") -> Workload:
     """One stream: a paged prefix plus a causal chunk of rows; 32/8 heads."""
@@ -260,6 +310,9 @@ def small(w_name: str, seed: int = 1235) -> Workload:
         return fp8_verify(seed, seq_len=1300, n_streams=3, slack_pages=5)
     if w_name == "prompt_chunk":
         return prompt_chunk(seed, prefix=300, chunk=257, slack_pages=3)
+    if w_name == "tree_verify":
+        return tree_verify(seed, seq_len=1300, n_streams=3, nodes=20, kv_dtype="fp8",
+                           slack_pages=5)
     if w_name == "overcommitted_pool":
         return overcommitted_pool(seed, n_short=5, lo=100, hi=2000, long_len=3000,
                                   pool_rows=60 * PAGE)
