@@ -135,6 +135,27 @@ int tfpa_decode(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
                 int32_t rows, float softmax_scale, const tfpa_scratch* scratch,
                 void* out, float* lse, cudaStream_t stream);
 
+/* Draft-tree verify: tfpa_decode whose rows see the keys their ancestor
+ * masks allow instead of every earlier key.  The pages' partial and merge
+ * kernels index the queries, the row tables, the ancestor table (rowanc),
+ * the partials and the output by row, and a sliced launch shifts the
+ * ancestor table with the other row tables (PR #1355, "Follow-up checks");
+ * the pages do not spell out the table's format, and this reading is used:
+ *   row_anc : DEVICE uint64[rows], 8-byte aligned, read from the launch's
+ *             stream.  Bit d of row_anc[r] set: the key at position
+ *             row_pos[r] - d is visible to row r.  Keys more than 63
+ *             positions back are always visible, keys after row_pos[r] never.
+ *             Bit 0 (the row's own key) must be set.  All bits set is the
+ *             causal row, and then the result equals tfpa_decode's bytes.
+ * A draft tree of at most 64 nodes laid out at consecutive positions sets,
+ * for node i, the bits of its ancestors and itself and every bit that
+ * reaches before the root (the committed prefix).  Errors as tfpa_decode;
+ * TFPA_EINVAL also for a NULL or misaligned row_anc. */
+int tfpa_decode_tree(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                     const void* q, const int32_t* row_seg, const int32_t* row_pos,
+                     const uint64_t* row_anc, int32_t rows, float softmax_scale,
+                     const tfpa_scratch* scratch, void* out, float* lse, cudaStream_t stream);
+
 /* Decode/verify attention for callers that cannot allocate device memory.
  *
  * Some callers cannot call cudaMalloc: code that runs inside another

@@ -26,7 +26,7 @@ TFPA_OK, TFPA_EINVAL, TFPA_ERANGE, TFPA_ECAPACITY, TFPA_ECUDA, TFPA_EDEVICE = 0,
 
 EXPORTS = ("tfpa_pages_per_split", "tfpa_num_splits", "tfpa_write_kv", "tfpa_decode_partial",
            "tfpa_merge", "tfpa_decode", "tfpa_prefill", "tfpa_set_launch_hook",
-           "tfpa_strerror", "tfpa_version", "tfpa_decode_static")
+           "tfpa_strerror", "tfpa_version", "tfpa_decode_static", "tfpa_decode_tree")
 
 
 class TfpaError(RuntimeError):
@@ -89,6 +89,9 @@ def lib():
         L.tfpa_decode.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, i32,
                                   ctypes.c_float, P(tfpa_scratch), vp, vp, vp]
         L.tfpa_decode.restype = ctypes.c_int
+        L.tfpa_decode_tree.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, vp, i32,
+                                       ctypes.c_float, P(tfpa_scratch), vp, vp, vp]
+        L.tfpa_decode_tree.restype = ctypes.c_int
         L.tfpa_decode_static.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, i32,
                                          ctypes.c_float, vp, vp, vp]
         L.tfpa_decode_static.restype = ctypes.c_int
@@ -241,6 +244,19 @@ def tfpa_decode(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, softmax_
     _check(lib().tfpa_decode(ctypes.byref(cc), cs, n, _ptr(q), _ptr(rs), _ptr(rp), len(rs),
                              float(softmax_scale), ctypes.byref(sc), _ptr(out), _ptr(lse),
                              _stream(stream)), "tfpa_decode")
+
+
+def tfpa_decode_tree(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, row_anc,
+                     softmax_scale, scratch: Scratch, out, lse=None, stream=None) -> None:
+    """Draft-tree verify: ``row_anc`` is a device tensor of 64-bit ancestor
+    masks, one per row (int64 or uint64 storage; only the bits matter)."""
+    cs, n = _segs(segs)
+    rs, rp = _i32(row_seg), _i32(row_pos)
+    cc, sc = cache.c(), scratch.c()
+    _check(lib().tfpa_decode_tree(ctypes.byref(cc), cs, n, _ptr(q), _ptr(rs), _ptr(rp),
+                                  _ptr(row_anc), len(rs), float(softmax_scale),
+                                  ctypes.byref(sc), _ptr(out), _ptr(lse), _stream(stream)),
+           "tfpa_decode_tree")
 
 
 def tfpa_decode_static(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, softmax_scale,

@@ -25,6 +25,8 @@
 // next item's loads and math.
 // Paged and slab streams differ only in the TMA row coordinate, so they
 // produce the same bytes (PR #1373, "What changes").
+#include <climits>
+
 #include "common.cuh"
 #include "params.h"
 #include "tcgen05.cuh"
@@ -168,14 +170,14 @@ __device__ __forceinline__ int out_col(int nt, int n) {
   return nt < 8 ? 8 * n + nt : 64 + 8 * n + (nt - 8);
 }
 
-// Query fragments of rows gq and gq+8 of an m-tile, the rows' causal limits
-// and their score multipliers (f16 operands for e4m3 caches: each row is
-// scaled by a power of two into f16 range, exact for every element within
-// 2^28 of the row's largest).
+// Query fragments of rows gq and gq+8 of an m-tile, the rows' causal limits,
+// their ancestor masks (all ones for causal rows) and their score multipliers
+// (f16 operands for e4m3 caches: each row is scaled by a power of two into
+// f16 range, exact for every element within 2^28 of the row's largest).
 template <bool FP8>
 __device__ __forceinline__ void load_q(const DecodeParams& p, const RunInfo& ru, const Item& x,
                                        int gq, int c, uint32_t (&qr)[2][16], int (&lim)[2],
-                                       float (&sc)[2]) {
+                                       uint64_t (&anc)[2], float (&sc)[2]) {
   const int nq = ru.nrows * p.group;
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
@@ -183,10 +185,12 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, const RunInfo& ru,
     uint4 v[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
                   make_uint4(0, 0, 0, 0)};
     lim[hr] = -1;
+    anc[hr] = ~0ull;
     if (qv < nq) {
       const int r = qv / p.group;
       const int h = x.g * p.group + (qv - r * p.group);
       lim[hr] = ru.pos0 + r;
+      if (p.anc) anc[hr] = __ldg(p.anc + ru.row0 + r);
       const uint4* qp =
           reinterpret_cast<const uint4*>(p.q + ((size_t)(ru.row0 + r) * p.hq + h) * kHeadDim);
       if (FP8) {
@@ -253,9 +257,11 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
   cta_items(p.n_items, ib, ie);
   int q_run = -1, q_g = -1, q_mt = -1;     // the m-tile whose query is loaded
   int lim[2] = {-1, -1};
+  uint64_t anc[2] = {~0ull, ~0ull};
   float sc[2] = {0.f, 0.f};
   uint32_t qr[2][16];
   int maxlim = -1;
+  int tree_low = INT_MAX;     // keys from here on may be hidden by an ancestor mask
 
   for (int it = ib; it < ie; ++it) {
     const Item x = item_of(p, it);
@@ -263,8 +269,12 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
     int klo, khi;
     item_keys(p, x, klo, khi);
     if (x.run != q_run || x.g != q_g || x.mt != q_mt) {
-      load_q<FP8>(p, ru, x, gq, c, qr, lim, sc);
+      load_q<FP8>(p, ru, x, gq, c, qr, lim, anc, sc);
       maxlim = __reduce_max_sync(0xffffffffu, max(lim[0], lim[1]));
+      if (p.anc) {
+        const int mn = min(lim[0] >= 0 ? lim[0] : INT_MAX, lim[1] >= 0 ? lim[1] : INT_MAX);
+        tree_low = (int)__reduce_min_sync(0xffffffffu, (unsigned)mn) - 63;
+      }
       q_run = x.run;
       q_g = x.g;
       q_mt = x.mt;
@@ -323,9 +333,12 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
               mma_bf16(s[nt], a, kb[2 * ks], kb[2 * ks + 1]);
           }
         }
-        // ---- scale, causal mask, online softmax (rows gq, gq+8; a row's
-        // keys are spread over the 4 threads of a quad).  The running max is
-        // only moved when it grows by more than 2^8, so O is rarely rescaled.
+        // ---- scale, causal (or ancestor) mask, online softmax (rows gq,
+        // gq+8; a row's keys are spread over the 4 threads of a quad).  The
+        // running max is only moved when it grows by more than 2^8, so O is
+        // rarely rescaled.  Ancestor masks are only consulted where a key
+        // lies within 63 positions of some row of the warp.
+        const bool tree_zone = key_base + C::kKeysPerWarp > tree_low;
         float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int nt = 0; nt < C::kNT; ++nt) {
@@ -333,7 +346,12 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
           for (int j = 0; j < 4; ++j) {
             const int hr = j >> 1;
             const int key = key_base + nt * 8 + 2 * c + (j & 1);
-            const float v = key <= lim[hr] ? s[nt][j] * sc[hr] : -INFINITY;
+            bool vis = key <= lim[hr];
+            if (tree_zone) {
+              const int dd = lim[hr] - key;
+              vis = vis && (dd > 63 || ((anc[hr] >> dd) & 1ull));
+            }
+            const float v = vis ? s[nt][j] * sc[hr] : -INFINITY;
             s[nt][j] = v;
             mx[hr] = fmaxf(mx[hr], v);
           }

@@ -284,14 +284,16 @@ void fill_run(RunInfo& ri, const tfpa_seg& g, int src, int row0, int nrows, int 
 // before the next launch; otherwise partials land at the call's own row and
 // no merge runs.
 int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const void* q,
-                const int32_t* row_seg, const int32_t* row_pos, int32_t rows, float scale,
-                const tfpa_scratch* sc, void* out, float* lse, cudaStream_t stream, bool sliced) {
+                const int32_t* row_seg, const int32_t* row_pos, const uint64_t* anc,
+                int32_t rows, float scale, const tfpa_scratch* sc, void* out, float* lse,
+                cudaStream_t stream, bool sliced) {
   int e;
   if ((e = check_cache(c)) || (e = check_segs(c, segs, nseg))) return e;
   if (!sc || !sc->part_o || !sc->part_ml || sc->cap_rows < 1 || sc->max_splits < 1)
     return TFPA_EINVAL;
   if (rows > 0 && (!q || !aligned(q, 16))) return TFPA_EINVAL;
   if (sliced && rows > 0 && (!out || !aligned(out, 8))) return TFPA_EINVAL;
+  if (anc && !aligned(anc, 8)) return TFPA_EINVAL;
   if (!std::isfinite(scale)) return TFPA_EINVAL;
   if (!sliced && rows > sc->cap_rows) return TFPA_ECAPACITY;
   std::vector<Run> runs;
@@ -340,6 +342,7 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
     const int32_t srow = sliced ? 0 : base;  // scratch row of this launch's first row
     const size_t srow_elems = (size_t)srow * c->hq * sc->max_splits;
     p.q = static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd;
+    p.anc = anc ? anc + base : nullptr;   // the ancestor table shifts with the rows
     p.part_o = sc->part_o + srow_elems * kHeadDim;
     p.part_ml = sc->part_ml + srow_elems * 2;
     p.k_scale = c->k_scale;
@@ -383,16 +386,26 @@ extern "C" int tfpa_decode_partial(const tfpa_cache* cache, const tfpa_seg* segs
                                    const void* q, const int32_t* row_seg, const int32_t* row_pos,
                                    int32_t rows, float softmax_scale, const tfpa_scratch* scratch,
                                    cudaStream_t stream) {
-  return decode_impl(cache, segs, nseg, q, row_seg, row_pos, rows, softmax_scale, scratch,
-                     nullptr, nullptr, stream, false);
+  return decode_impl(cache, segs, nseg, q, row_seg, row_pos, nullptr, rows, softmax_scale,
+                     scratch, nullptr, nullptr, stream, false);
 }
 
 extern "C" int tfpa_decode(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
                            const void* q, const int32_t* row_seg, const int32_t* row_pos,
                            int32_t rows, float softmax_scale, const tfpa_scratch* scratch,
                            void* out, float* lse, cudaStream_t stream) {
-  return decode_impl(cache, segs, nseg, q, row_seg, row_pos, rows, softmax_scale, scratch, out,
-                     lse, stream, true);
+  return decode_impl(cache, segs, nseg, q, row_seg, row_pos, nullptr, rows, softmax_scale,
+                     scratch, out, lse, stream, true);
+}
+
+extern "C" int tfpa_decode_tree(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                                const void* q, const int32_t* row_seg, const int32_t* row_pos,
+                                const uint64_t* row_anc, int32_t rows, float softmax_scale,
+                                const tfpa_scratch* scratch, void* out, float* lse,
+                                cudaStream_t stream) {
+  if (rows > 0 && !row_anc) return TFPA_EINVAL;
+  return decode_impl(cache, segs, nseg, q, row_seg, row_pos, row_anc, rows, softmax_scale,
+                     scratch, out, lse, stream, true);
 }
 
 extern "C" int tfpa_merge(const tfpa_scratch* sc, int32_t hq, int32_t rows,

@@ -44,6 +44,7 @@ struct DecodeParams {
   KVMaps maps[kMaxSources];
   RunInfo runs[kMaxRuns];
   const __nv_bfloat16* q;     // rows of this launch: [rows][hq][128]
+  const uint64_t* anc;        // rows of this launch: ancestor masks, or nullptr (causal)
   float* part_o;              // [cap_rows][hq][max_splits][128]
   float* part_ml;             // [cap_rows][hq][max_splits][2]
   const float* k_scale;       // fp8: [hkv]

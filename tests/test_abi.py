@@ -146,3 +146,20 @@ def test_merge_rejects_rows_beyond_capacity():
         with pytest.raises(B.TfpaError) as e:
             B.tfpa_merge(B.Scratch(5 * FAKE, 6 * FAKE, 128), 32, np.ones(129), 7 * FAKE)
     assert e.value.code == B.TFPA_ECAPACITY
+
+
+def test_decode_tree_checks_its_ancestor_table():
+    c = _cache()
+    segs = [B.Seg(1000, page_table=3 * FAKE)]
+    sc = B.Scratch(5 * FAKE, 6 * FAKE, 128)
+    for anc in (None, 8 * FAKE + 4):                  # missing, not 8-byte aligned
+        with B.record_launches() as rec:
+            with pytest.raises(B.TfpaError) as e:
+                B.tfpa_decode_tree(c, segs, 4 * FAKE, [0], [999], anc, 0.088, sc, 7 * FAKE)
+        assert e.value.code == B.TFPA_EINVAL
+        assert rec == []
+    with B.record_launches() as rec:
+        B.tfpa_decode_tree(c, segs, 4 * FAKE, [0] * 200, list(range(800, 1000)), 8 * FAKE,
+                           0.088, sc, 7 * FAKE)
+    assert [(r["kind"], r["row0"], r["rows"]) for r in rec] == [
+        ("partial", 0, 128), ("merge", 0, 128), ("partial", 128, 72), ("merge", 128, 72)]
