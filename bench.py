@@ -343,6 +343,26 @@ def time_prefill(w, torch, B, reps):
     return statistics.median(times)
 
 
+def time_tree_calls(w, torch, B, reps):
+    """tfpa_decode_tree one call at a time, CUDA events around each; median ms."""
+    cache, segs, q = device_case(w, torch, B)
+    anc = torch.from_numpy(np.ascontiguousarray(w.row_anc).view(np.int64)).cuda()
+    sc = B.make_scratch(min(128, w.rows), w.hq)
+    out = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream()
+    times = []
+    for i in range(reps + 3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        B.tfpa_decode_tree(cache, segs, q, w.row_seg, w.row_pos, anc, w.softmax_scale, sc, out)
+        e1.record(s)
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1))
+    assert int(cache.err_flag.item()) == 0, "kernel error flag set"
+    return statistics.median(times)
+
+
 def time_decode_calls(w, torch, B, reps, flush):
     """tfpa_decode (partial + merge) one call at a time, CUDA events around
     each, optionally with L2 flushed before each call; median in ms."""
@@ -510,6 +530,14 @@ def main():
             "seated_streams": len(w6.streams), "waiting_streams": len(w6.waiting),
             "us_per_call": ms6 * 1e3, "kv_gbs": (kv6 + qo6) / (ms6 / 1e3) / 1e9,
             "frac_of_measured_hbm": (kv6 + qo6) / (ms6 / 1e3) / 1e9 / pk["hbm_gbs"]}
+        w7 = wl.tree_verify()
+        ms7 = time_tree_calls(w7, torch, B, 20)
+        kv7, qo7 = kv_bytes(w7)
+        extra["tree_verify"] = {
+            "workload": "8 streams x 65,536 positions, fp8 e4m3, a seeded 16-node draft tree "
+                        "per stream (one row per node, ancestor masks); tfpa_decode_tree per call",
+            "ms_per_call": ms7, "kv_gbs": (kv7 + qo7) / (ms7 / 1e3) / 1e9,
+            "frac_of_measured_hbm": (kv7 + qo7) / (ms7 / 1e3) / 1e9 / pk["hbm_gbs"]}
     value = world * (kv + qo) / (step_ms / 1e3) / 1e9
     achieved = (kv + qo) / (partial_ms / 1e3) / 1e9
     extra["fp8_verify"] = {

@@ -89,11 +89,12 @@ __device__ __forceinline__ Item item_of(const DecodeParams& p, int it) {
   return x;
 }
 
-// Items [begin, end) of this CTA: a contiguous share, so consecutive items
-// are mostly consecutive splits of one (stream, kv head, m-tile).
-__device__ __forceinline__ void cta_items(int n, int& begin, int& end) {
-  begin = (int)(((long long)blockIdx.x * n) / gridDim.x);
-  end = (int)(((long long)(blockIdx.x + 1) * n) / gridDim.x);
+// Items [begin, end) of this CTA: a contiguous share balanced by work on the
+// host, so consecutive items are mostly consecutive splits of one (stream,
+// kv head, m-tile).
+__device__ __forceinline__ void cta_items(const DecodeParams& p, int& begin, int& end) {
+  begin = p.cta_item0[blockIdx.x];
+  end = p.cta_item0[blockIdx.x + 1];
 }
 
 // Key range [klo, khi) an item must read: its split's pages, cut at the
@@ -114,7 +115,7 @@ __device__ void producer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
   using C = Cfg<FP8>;
   if ((threadIdx.x & 31) != 0) return;
   int ib, ie;
-  cta_items(p.n_items, ib, ie);
+  cta_items(p, ib, ie);
   uint32_t stage = 0;
   for (int it = ib; it < ie; ++it) {
     const Item x = item_of(p, it);
@@ -174,7 +175,7 @@ __device__ __forceinline__ int out_col(int nt, int n) {
 // their ancestor masks (all ones for causal rows) and their score multipliers
 // (f16 operands for e4m3 caches: each row is scaled by a power of two into
 // f16 range, exact for every element within 2^28 of the row's largest).
-template <bool FP8>
+template <bool FP8, bool TREE>
 __device__ __forceinline__ void load_q(const DecodeParams& p, const RunInfo& ru, const Item& x,
                                        int gq, int c, uint32_t (&qr)[2][16], int (&lim)[2],
                                        uint64_t (&anc)[2], float (&sc)[2]) {
@@ -190,7 +191,7 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, const RunInfo& ru,
       const int r = qv / p.group;
       const int h = x.g * p.group + (qv - r * p.group);
       lim[hr] = ru.pos0 + r;
-      if (p.anc) anc[hr] = __ldg(p.anc + ru.row0 + r);
+      if (TREE) anc[hr] = __ldg(p.anc + ru.row0 + r);
       const uint4* qp =
           reinterpret_cast<const uint4*>(p.q + ((size_t)(ru.row0 + r) * p.hq + h) * kHeadDim);
       if (FP8) {
@@ -244,7 +245,7 @@ struct CombBars {
   uint64_t* done;        // the combiners finished the item (fold buffer free)
 };
 
-template <bool FP8>
+template <bool FP8, bool TREE>
 __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* full,
                          uint64_t* empty, const int* stage_bad, uint32_t tmem, CombBars bars) {
   using C = Cfg<FP8>;
@@ -254,7 +255,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
   const uint32_t sbase = smem_u32(stage_mem);
   uint32_t stage = 0;
   int ib, ie;
-  cta_items(p.n_items, ib, ie);
+  cta_items(p, ib, ie);
   int q_run = -1, q_g = -1, q_mt = -1;     // the m-tile whose query is loaded
   int lim[2] = {-1, -1};
   uint64_t anc[2] = {~0ull, ~0ull};
@@ -269,9 +270,9 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
     int klo, khi;
     item_keys(p, x, klo, khi);
     if (x.run != q_run || x.g != q_g || x.mt != q_mt) {
-      load_q<FP8>(p, ru, x, gq, c, qr, lim, anc, sc);
+      load_q<FP8, TREE>(p, ru, x, gq, c, qr, lim, anc, sc);
       maxlim = __reduce_max_sync(0xffffffffu, max(lim[0], lim[1]));
-      if (p.anc) {
+      if (TREE) {
         const int mn = min(lim[0] >= 0 ? lim[0] : INT_MAX, lim[1] >= 0 ? lim[1] : INT_MAX);
         tree_low = (int)__reduce_min_sync(0xffffffffu, (unsigned)mn) - 63;
       }
@@ -338,7 +339,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
         // running max is only moved when it grows by more than 2^8, so O is
         // rarely rescaled.  Ancestor masks are only consulted where a key
         // lies within 63 positions of some row of the warp.
-        const bool tree_zone = key_base + C::kKeysPerWarp > tree_low;
+        const bool tree_zone = TREE && key_base + C::kKeysPerWarp > tree_low;
         float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int nt = 0; nt < C::kNT; ++nt) {
@@ -511,7 +512,7 @@ __device__ void combiner(const DecodeParams& p, uint32_t tmem, float4* fold, flo
   const int q = warp - kCombineWarp0;
   const int gq = lane >> 2, c = lane & 3;
   int ib, ie;
-  cta_items(p.n_items, ib, ie);
+  cta_items(p, ib, ie);
   const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
   for (int it = ib; it < ie; ++it) {
     const Item x = item_of(p, it);
@@ -633,7 +634,7 @@ __device__ void combiner(const DecodeParams& p, uint32_t tmem, float4* fold, flo
   }
 }
 
-template <bool FP8>
+template <bool FP8, bool TREE>
 __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
     const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -681,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
   wait_prior_grid();
   if (warp < kCombineWarp0) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsConsumer));
-    consumer<FP8>(p, stage_mem, full, empty, stage_bad, tmem, cb);
+    consumer<FP8, TREE>(p, stage_mem, full, empty, stage_bad, tmem, cb);
   } else if (warp < kProducerWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCombine));
     combiner<FP8>(p, tmem, fold, ml_buf, cb);
@@ -759,24 +760,24 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
   if (p.lse && lane == 0) p.lse[(size_t)row * p.hq + h] = (M + log2f(L)) * 0.6931471805599453f;
 }
 
-template <bool FP8>
+template <bool FP8, bool TREE>
 cudaError_t launch_partial(const DecodeParams& p, int grid, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
     // The register split only works if the block launches with at least the
     // registers it hands out; otherwise setmaxnreg.inc would wait forever.
     cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, decode_partial_kernel<FP8>);
+    cudaError_t e = cudaFuncGetAttributes(&attr, decode_partial_kernel<FP8, TREE>);
     if (e != cudaSuccess) return e;
     if (attr.numRegs * kThreads < 128 * (2 * kRegsConsumer + kRegsCombine + kRegsProducer))
       return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(decode_partial_kernel<FP8>,
+    e = cudaFuncSetAttribute(decode_partial_kernel<FP8, TREE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   cudaError_t e =
-      launch_pdl(decode_partial_kernel<FP8>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
+      launch_pdl(decode_partial_kernel<FP8, TREE>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -785,7 +786,11 @@ cudaError_t launch_partial(const DecodeParams& p, int grid, cudaStream_t s) {
 
 cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cudaStream_t s) {
   if (grid <= 0 || p.n_items == 0) return cudaSuccess;
-  return fp8 ? launch_partial<true>(p, grid, s) : launch_partial<false>(p, grid, s);
+  // Rows with ancestor masks take their own instantiation, so causal calls
+  // keep the causal kernel's code.
+  if (p.anc)
+    return fp8 ? launch_partial<true, true>(p, grid, s) : launch_partial<false, true>(p, grid, s);
+  return fp8 ? launch_partial<true, false>(p, grid, s) : launch_partial<false, false>(p, grid, s);
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {

@@ -279,6 +279,47 @@ void fill_run(RunInfo& ri, const tfpa_seg& g, int src, int row0, int nrows, int 
   ri.pad_ = 0;
 }
 
+// Key stages of decode work item (m-tile mt, split sigma) of a run: its
+// split's keys, cut at the stream's end and at the m-tile's last position
+// (the kernel's item key range, in units of the kernel's chunk).
+int item_stages(const RunInfo& ri, int G, int mt, int sigma, int chunk) {
+  const int nq = ri.nrows * G;
+  const int last_qv = std::min(mt * 16 + 15, nq - 1);
+  const int maxpos = ri.pos0 + last_qv / G;
+  const int klo = sigma * ri.pps * kPage;
+  const int khi = std::min(std::min(klo + ri.pps * kPage, ri.seq_len), maxpos + 1);
+  return khi > klo ? (khi - klo + chunk - 1) / chunk : 0;
+}
+
+// Per-CTA item ranges of a decode partial launch, balanced by work: an item
+// weighs its key stages plus a fixed cost (its query load and combine), and
+// CTA b starts at the first item whose prefix weight reaches b / grid of the
+// total.  Items are walked in the kernel's order: kv head, m-tile, split.
+void plan_cta_ranges(DecodeParams& p, int nr, int G, bool fp8, int grid) {
+  const int chunk = fp8 ? 256 : 128;
+  constexpr int64_t kItemCost = 2;
+  auto for_items = [&](auto&& fn) {
+    for (int r = 0; r < nr; ++r) {
+      const RunInfo& ri = p.runs[r];
+      const int mtiles = (ri.nrows * G + 15) / 16;
+      for (int g = 0; g < p.hkv; ++g)
+        for (int mt = 0; mt < mtiles; ++mt)
+          for (int sg = 0; sg < ri.nsplit; ++sg) fn(item_stages(ri, G, mt, sg, chunk) + kItemCost);
+    }
+  };
+  int64_t total = 0;
+  for_items([&](int64_t w) { total += w; });
+  int b = 1, item = 0;
+  int64_t prefix = 0;
+  p.cta_item0[0] = 0;
+  for_items([&](int64_t w) {
+    while (b < grid && prefix * grid >= total * b) p.cta_item0[b++] = item;
+    prefix += w;
+    ++item;
+  });
+  while (b <= grid) p.cta_item0[b++] = item;
+}
+
 // Partial (and optionally merge) launches over the call's rows.  With
 // `sliced`, each launch's partials start at scratch row 0 and are merged
 // before the next launch; otherwise partials land at the call's own row and
@@ -357,7 +398,8 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
     p.num_pages = c->num_pages;
     p.rows = nrows;
     p.scale_log2 = scale * 1.4426950408889634f;
-    const int grid = std::min(items, nsm);
+    const int grid = std::min(std::min(items, nsm), kMaxDecodeGrid);
+    plan_cta_ranges(p, nr, G, fp8, grid);
     record(1, base, nrows, nr, items, grid, (int64_t)base * hd, 0);
     if (!dry_run()) {
       if ((e = to_err(launch_decode_partial(p, fp8, grid, stream)))) return e;

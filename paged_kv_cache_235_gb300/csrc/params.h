@@ -19,6 +19,7 @@ constexpr int kMaxSplits = 32;      // split-K partials per (row, head), at most
 constexpr int kMaxRuns = 64;        // runs per launch
 constexpr int kMaxSlabs = 15;       // slab streams per launch (+1 source for the pool)
 constexpr int kMaxSources = kMaxSlabs + 1;
+constexpr int kMaxDecodeGrid = 256;  // CTAs of one decode partial launch, at most
 
 // TMA descriptors of one K/V source: the page pool (source 0) or a slab.
 struct KVMaps {
@@ -58,6 +59,9 @@ struct DecodeParams {
   int32_t num_pages;
   int32_t rows;
   float scale_log2;           // softmax_scale * log2(e)
+  // CTA b takes the work items [cta_item0[b], cta_item0[b + 1]), ranges the
+  // host balances by the items' key stages.
+  int32_t cta_item0[kMaxDecodeGrid + 1];
 };
 
 struct MergeRun {
