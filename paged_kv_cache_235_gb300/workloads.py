@@ -142,6 +142,23 @@ def tree_masks(parents) -> List[int]:
     return masks
 
 
+def rope_table(theta: float, n_pos: int, d: int = HEAD_DIM):
+    """The caller's rotary table: float32 cos and sin ``[n_pos][d / 2]`` of
+    ``t * theta ** (-2 i / d)``, computed in float64 and rounded once."""
+    i = np.arange(d // 2, dtype=np.float64)
+    inv = theta ** (-2.0 * i / d)
+    ang = np.arange(n_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def tree_depths(parents) -> List[int]:
+    """Depth of each node of a draft tree (the root has depth 0)."""
+    depth = []
+    for i, par in enumerate(parents):
+        depth.append(0 if par < 0 else depth[par] + 1)
+    return depth
+
+
 def random_tree(n: int, seed: int) -> List[int]:
     """Parents of a seeded random recursive tree of ``n`` nodes (node 0 the root)."""
     rng = np.random.default_rng(seed)
