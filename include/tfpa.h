@@ -82,7 +82,8 @@ typedef struct {
   int32_t num_pages;
   const float* k_scale;           /* DEVICE float[hkv], fp8 only: value = e4m3 * scale      */
   const float* v_scale;
-  int32_t* err_flag;              /* optional DEVICE int32, OR-ed with 1 on a bad page id   */
+  int32_t* err_flag;              /* optional DEVICE int32: OR-ed with 1 on a bad page id,
+                                     4 on a rotary position outside the table */
 } tfpa_cache;
 
 /* Split-K scratch for decode partials (float32).
@@ -95,6 +96,42 @@ typedef struct {
   int32_t cap_rows;               /* rows one partial launch can hold                      */
   int32_t max_splits;             /* >= tfpa_num_splits(seq_len) of every segment used     */
 } tfpa_scratch;
+
+/* KV write with rotary position embedding: tfpa_write_kv, with each row's K
+ * rotated before it is stored.  The pages list "rope stores" among the paged
+ * KV store's checks (PR #1373 review) without defining the rotation; this
+ * reading is used: for i < 64, with c = rope_cos[t][i], s = rope_sin[t][i]
+ * and t the row's rotary position,
+ *   k'[i] = k[i] c - k[i+64] s,   k'[i+64] = k[i+64] c + k[i] s,
+ * each product, difference and sum rounded to float32 (no fused multiply-
+ * add), then stored as bf16 (round to nearest even) or as tfpa_write_kv
+ * stores an fp8 value.  V is stored as tfpa_write_kv stores it.
+ *   rope_pos : DEVICE int32[rows], 4-byte aligned, each in [0, rope_n); or
+ *              NULL: the storage positions row_pos (then checked on the host,
+ *              TFPA_ERANGE).  A device position outside the table leaves the
+ *              row unwritten and ORs 4 into cache->err_flag.  The rotary
+ *              position may differ from the storage position (a draft-tree
+ *              node is rotated by its depth and stored at its index).
+ *   rope_cos, rope_sin : DEVICE float32 [rope_n][64], 16-byte aligned.
+ * Sliced like the rows.  TFPA_EINVAL for a NULL or misaligned table. */
+int tfpa_write_kv_rope(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                       const void* k_rows, const void* v_rows, const int32_t* row_seg,
+                       const int32_t* row_pos, const int32_t* rope_pos, const float* rope_cos,
+                       const float* rope_sin, int32_t rope_n, int32_t rows,
+                       cudaStream_t stream);
+
+/* Keep: copy stored K/V rows (every kv head, the stored bytes unchanged)
+ * from position keep_src[i] to keep_dst[i] of segment keep_seg[i] (HOST
+ * int32[n] each), e.g. to move a draft tree's accepted path to the committed
+ * positions.  The pages list "keep" among the paged store's checks (PR #1373
+ * review); reading used: every source row is read before any destination is
+ * written, so chains of moves within one call are exact.  Positions must lie
+ * in [0, seq_len) (TFPA_ERANGE); a destination may appear only once per
+ * segment (TFPA_EINVAL); at most 256 pairs a call (TFPA_ECAPACITY).  A page
+ * id out of range skips that pair and ORs 1 into cache->err_flag. */
+int tfpa_keep_kv(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                 const int32_t* keep_seg, const int32_t* keep_src, const int32_t* keep_dst,
+                 int32_t n, cudaStream_t stream);
 
 /* Split policy, a function of a stream's own length only (so a stream's
  * partials never depend on its batch): pages_per_split = max(2,
@@ -203,7 +240,7 @@ int tfpa_prefill(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
  * launch is reported; with dry_run != 0 nothing is enqueued and no CUDA call
  * is made, so the slicing logic runs on a machine without a GPU. */
 typedef struct {
-  int32_t kind;          /* 0 write_kv, 1 decode partial, 2 merge, 3 prefill */
+  int32_t kind;          /* 0 write_kv, 1 decode partial, 2 merge, 3 prefill, 4 keep */
   int32_t row0;          /* first row of the call this launch covers */
   int32_t rows;          /* rows it covers */
   int32_t runs;          /* row groups (segment, consecutive positions) */

@@ -26,7 +26,8 @@ TFPA_OK, TFPA_EINVAL, TFPA_ERANGE, TFPA_ECAPACITY, TFPA_ECUDA, TFPA_EDEVICE = 0,
 
 EXPORTS = ("tfpa_pages_per_split", "tfpa_num_splits", "tfpa_write_kv", "tfpa_decode_partial",
            "tfpa_merge", "tfpa_decode", "tfpa_prefill", "tfpa_set_launch_hook",
-           "tfpa_strerror", "tfpa_version", "tfpa_decode_static", "tfpa_decode_tree")
+           "tfpa_strerror", "tfpa_version", "tfpa_decode_static", "tfpa_decode_tree",
+           "tfpa_write_kv_rope", "tfpa_keep_kv")
 
 
 class TfpaError(RuntimeError):
@@ -61,7 +62,7 @@ class tfpa_launch_record(ctypes.Structure):
 
 
 HOOK = ctypes.CFUNCTYPE(None, ctypes.POINTER(tfpa_launch_record), ctypes.c_void_p)
-KINDS = {0: "write_kv", 1: "partial", 2: "merge", 3: "prefill"}
+KINDS = {0: "write_kv", 1: "partial", 2: "merge", 3: "prefill", 4: "keep"}
 
 _lib = None
 
@@ -89,6 +90,11 @@ def lib():
         L.tfpa_decode.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, i32,
                                   ctypes.c_float, P(tfpa_scratch), vp, vp, vp]
         L.tfpa_decode.restype = ctypes.c_int
+        L.tfpa_write_kv_rope.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, vp, vp,
+                                         vp, vp, i32, i32, vp]
+        L.tfpa_write_kv_rope.restype = ctypes.c_int
+        L.tfpa_keep_kv.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, i32, vp]
+        L.tfpa_keep_kv.restype = ctypes.c_int
         L.tfpa_decode_tree.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, vp, i32,
                                        ctypes.c_float, P(tfpa_scratch), vp, vp, vp]
         L.tfpa_decode_tree.restype = ctypes.c_int
@@ -244,6 +250,32 @@ def tfpa_decode(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, softmax_
     _check(lib().tfpa_decode(ctypes.byref(cc), cs, n, _ptr(q), _ptr(rs), _ptr(rp), len(rs),
                              float(softmax_scale), ctypes.byref(sc), _ptr(out), _ptr(lse),
                              _stream(stream)), "tfpa_decode")
+
+
+def tfpa_write_kv_rope(cache: Cache, segs: Sequence[Seg], k_rows, v_rows, row_seg, row_pos,
+                       rope_cos, rope_sin, rope_pos=None, stream=None) -> None:
+    """KV write with K rotated by each row's rotary position: ``rope_cos`` /
+    ``rope_sin`` are device float32 ``[n][64]`` tables; ``rope_pos`` a device
+    int32 tensor (one per row) or None for the storage positions."""
+    cs, n = _segs(segs)
+    rs, rp = _i32(row_seg), _i32(row_pos)
+    cc = cache.c()
+    _check(lib().tfpa_write_kv_rope(ctypes.byref(cc), cs, n, _ptr(k_rows), _ptr(v_rows),
+                                    _ptr(rs), _ptr(rp), _ptr(rope_pos), _ptr(rope_cos),
+                                    _ptr(rope_sin), int(rope_cos.shape[0]), len(rs),
+                                    _stream(stream)), "tfpa_write_kv_rope")
+
+
+def tfpa_keep_kv(cache: Cache, segs: Sequence[Seg], keep_seg, keep_src, keep_dst,
+                 stream=None) -> None:
+    """Copy stored K/V rows from keep_src to keep_dst positions (host tables)."""
+    cs, n = _segs(segs)
+    a, b, d = _i32(keep_seg), _i32(keep_src), _i32(keep_dst)
+    if not (len(a) == len(b) == len(d)):
+        raise ValueError("keep tables differ in length")
+    cc = cache.c()
+    _check(lib().tfpa_keep_kv(ctypes.byref(cc), cs, n, _ptr(a), _ptr(b), _ptr(d), len(a),
+                              _stream(stream)), "tfpa_keep_kv")
 
 
 def tfpa_decode_tree(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, row_anc,

@@ -12,6 +12,7 @@ namespace tfpa {
 // Error bits a kernel may OR into the caller's err_flag.
 constexpr int kErrBadPage = 1;     // page id outside [0, num_pages): its keys are masked
 constexpr int kErrTimeout = 2;     // a wait gave up (a bug; the kernel returned early)
+constexpr int kErrRopeRange = 4;   // rotary position outside the caller's table: row not stored
 
 // Longest a wait may spin before the kernel gives up (ns of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

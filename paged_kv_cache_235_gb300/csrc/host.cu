@@ -490,13 +490,30 @@ extern "C" int tfpa_merge(const tfpa_scratch* sc, int32_t hq, int32_t rows,
   return TFPA_OK;
 }
 
-extern "C" int tfpa_write_kv(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg,
-                             const void* k_rows, const void* v_rows, const int32_t* row_seg,
-                             const int32_t* row_pos, int32_t rows, cudaStream_t stream) {
+namespace {
+
+struct RopeArgs {
+  const int32_t* pos;   // DEVICE [rows] or nullptr (the storage positions)
+  const float* cos;     // DEVICE [n][64] or nullptr (plain store)
+  const float* sin;
+  int32_t n;
+};
+
+int write_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const void* k_rows,
+               const void* v_rows, const int32_t* row_seg, const int32_t* row_pos, int32_t rows,
+               const RopeArgs& rope, cudaStream_t stream) {
   int e;
   if ((e = check_cache(c)) || (e = check_segs(c, segs, nseg))) return e;
   if (rows > 0 && (!k_rows || !v_rows || !aligned(k_rows, 16) || !aligned(v_rows, 16)))
     return TFPA_EINVAL;
+  if (rope.cos) {
+    if (!rope.sin || rope.n < 1 || !aligned(rope.cos, 16) || !aligned(rope.sin, 16) ||
+        (rope.pos && !aligned(rope.pos, 4)))
+      return TFPA_EINVAL;
+    if (!rope.pos)
+      for (int32_t r = 0; r < rows; ++r)
+        if (row_pos && row_pos[r] >= rope.n) return TFPA_ERANGE;
+  }
   std::vector<Run> runs;
   if ((e = build_runs(segs, nseg, row_seg, row_pos, rows, runs))) return e;
   if (rows == 0) return TFPA_OK;
@@ -529,6 +546,10 @@ extern "C" int tfpa_write_kv(const tfpa_cache* c, const tfpa_seg* segs, int32_t 
     p.k_scale = c->k_scale;
     p.v_scale = c->v_scale;
     p.err_flag = c->err_flag;
+    p.rope_cos = rope.cos;
+    p.rope_sin = rope.sin;
+    p.rope_pos = rope.pos ? rope.pos + base : nullptr;   // shifts with the rows
+    p.rope_n = rope.n;
     p.nruns = nr;
     p.rows = nrows;
     p.hkv = c->hkv;
@@ -538,6 +559,71 @@ extern "C" int tfpa_write_kv(const tfpa_cache* c, const tfpa_seg* segs, int32_t 
     if (!dry_run())
       if ((e = to_err(launch_write_kv(p, stream)))) return e;
   }
+  return TFPA_OK;
+}
+
+}  // namespace
+
+extern "C" int tfpa_write_kv(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg,
+                             const void* k_rows, const void* v_rows, const int32_t* row_seg,
+                             const int32_t* row_pos, int32_t rows, cudaStream_t stream) {
+  return write_impl(c, segs, nseg, k_rows, v_rows, row_seg, row_pos, rows,
+                    RopeArgs{nullptr, nullptr, nullptr, 0}, stream);
+}
+
+extern "C" int tfpa_write_kv_rope(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg,
+                                  const void* k_rows, const void* v_rows,
+                                  const int32_t* row_seg, const int32_t* row_pos,
+                                  const int32_t* rope_pos, const float* rope_cos,
+                                  const float* rope_sin, int32_t rope_n, int32_t rows,
+                                  cudaStream_t stream) {
+  if (!rope_cos) return TFPA_EINVAL;
+  return write_impl(c, segs, nseg, k_rows, v_rows, row_seg, row_pos, rows,
+                    RopeArgs{rope_pos, rope_cos, rope_sin, rope_n}, stream);
+}
+
+extern "C" int tfpa_keep_kv(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg,
+                            const int32_t* keep_seg, const int32_t* keep_src,
+                            const int32_t* keep_dst, int32_t n, cudaStream_t stream) {
+  int e;
+  if ((e = check_cache(c)) || (e = check_segs(c, segs, nseg))) return e;
+  if (n < 0 || (n > 0 && (!keep_seg || !keep_src || !keep_dst))) return TFPA_EINVAL;
+  if (n > kMaxKeep) return TFPA_ECAPACITY;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t sg = keep_seg[i];
+    if (sg < 0 || sg >= nseg) return TFPA_ERANGE;
+    const tfpa_seg& g = segs[sg];
+    if (keep_src[i] < 0 || keep_src[i] >= g.seq_len || keep_dst[i] < 0 ||
+        keep_dst[i] >= g.seq_len)
+      return TFPA_ERANGE;
+    for (int32_t j = 0; j < i; ++j)          // one writer per destination row
+      if (keep_seg[j] == sg && keep_dst[j] == keep_dst[i]) return TFPA_EINVAL;
+  }
+  if (n == 0) return TFPA_OK;
+  if ((e = check_device())) return e;
+  std::lock_guard<std::mutex> lock(g_mu);
+  static KeepParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int32_t i = 0; i < n; ++i) {
+    const tfpa_seg& g = segs[keep_seg[i]];
+    KeepPair& kp = p.pairs[i];
+    kp.page_table = g.page_table;
+    kp.k_slab = g.page_table ? nullptr : g.k_slab;
+    kp.v_slab = g.page_table ? nullptr : g.v_slab;
+    kp.slab_cap = g.page_table ? 0 : g.slab_cap;
+    kp.src = keep_src[i];
+    kp.dst = keep_dst[i];
+  }
+  p.k_pool = c->k_pool;
+  p.v_pool = c->v_pool;
+  p.err_flag = c->err_flag;
+  p.n = n;
+  p.hkv = c->hkv;
+  p.num_pages = c->num_pages;
+  p.row_bytes = c->dtype == TFPA_FP8_E4M3 ? kHeadDim : 2 * kHeadDim;
+  record(4, 0, n, 0, n * c->hkv, c->hkv, 0, 0);
+  if (!dry_run())
+    if ((e = to_err(launch_keep(p, stream)))) return e;
   return TFPA_OK;
 }
 

@@ -102,11 +102,40 @@ struct WriteParams {
   const float* k_scale;
   const float* v_scale;
   int32_t* err_flag;
+  // Rotary store (nullptr rope_cos: plain store): K is rotated by rope_pos[row]
+  // (nullptr: the storage position) with the caller's cos/sin [rope_n][64].
+  const float* rope_cos;
+  const float* rope_sin;
+  const int32_t* rope_pos;    // rows of this launch
+  int32_t rope_n;
   int32_t nruns;
   int32_t rows;
   int32_t hkv;
   int32_t num_pages;
   int32_t fp8;
+};
+
+// Keep: stored rows copied between positions of a stream (all kv heads).
+constexpr int kMaxKeep = 256;
+struct KeepPair {
+  const int32_t* page_table;  // nullptr => slab
+  void* k_slab;
+  void* v_slab;
+  int32_t slab_cap;
+  int32_t src;
+  int32_t dst;
+  int32_t pad_;
+};
+
+struct KeepParams {
+  KeepPair pairs[kMaxKeep];
+  void* k_pool;
+  void* v_pool;
+  int32_t* err_flag;
+  int32_t n;
+  int32_t hkv;
+  int32_t num_pages;
+  int32_t row_bytes;          // 256 (bf16) or 128 (e4m3)
 };
 
 // Prefill: one work tile = (run, kv head g, query-head pair, 128 rows).
@@ -131,6 +160,7 @@ struct PrefillParams {
 
 // Launchers (defined next to their kernels).
 cudaError_t launch_write_kv(const WriteParams& p, cudaStream_t s);
+cudaError_t launch_keep(const KeepParams& p, cudaStream_t s);
 cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, bool fp8, int grid, cudaStream_t s);

@@ -1,16 +1,61 @@
 // KV write: new rows' K and V into their pages or slab, bf16 copy or e4m3
 // quantisation (TensorFold PR #1373, "What changes": the page-run layout the
-// KV store kernels write).
+// KV store kernels write), optionally with K rotated by its rotary position
+// first; and keep: stored rows copied between positions of a stream (the
+// PR #1373 review lists "rope stores and keep" among the paged store's
+// checks).
 //
-// One 16-thread group per (row, kv head); each thread moves 8 elements
-// (16 bytes of bf16 in; 16 bytes of bf16 or 8 bytes of e4m3 out).  The page
-// is looked up once per (row, head).
+// Write: one 16-thread group per (row, kv head); each thread moves 8
+// elements (16 bytes of bf16 in; 16 bytes of bf16 or 8 bytes of e4m3 out).
+// The page is looked up once per (row, head).  The rotation pairs element i
+// with i + 64 (rotate-half), so a thread also reads its partner's 8
+// elements; every product and sum is rounded on its own (no fused
+// multiply-add), so the stored code is a function of the inputs alone.
 #include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "params.h"
 
 namespace tfpa {
+
+namespace {
+
+// Eight float32 values -> eight e4m3 codes: value / scale rounded to float32
+// (IEEE division), then e4m3 RNE, saturating.
+__device__ __forceinline__ uint2 quant8(const float (&x)[8], float s) {
+  uint32_t out[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = make_float2(__fdiv_rn(x[2 * i], s), __fdiv_rn(x[2 * i + 1], s));
+    const __nv_fp8x2_storage_t b = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+    if (i & 1)
+      out[i >> 1] |= (uint32_t)b << 16;
+    else
+      out[i >> 1] = (uint32_t)b;
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+__device__ __forceinline__ void unpack8(const uint4& in, float (&x)[8]) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float (&x)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+}  // namespace
 
 __global__ void __launch_bounds__(256) write_kv_kernel(const __grid_constant__ WriteParams p) {
   allow_next_grid();
@@ -36,39 +81,93 @@ __global__ void __launch_bounds__(256) write_kv_kernel(const __grid_constant__ W
   } else {
     dst_row = (size_t)g * run.slab_cap + pos;
   }
-  const size_t src = ((size_t)row * p.hkv + g) * kHeadDim + t * 8;
+  const size_t src_row = ((size_t)row * p.hkv + g) * kHeadDim;
+  const size_t src = src_row + t * 8;
   const uint4 kv = *reinterpret_cast<const uint4*>(p.k_rows + src);
   const uint4 vv = *reinterpret_cast<const uint4*>(p.v_rows + src);
+
+  float kf[8];
+  unpack8(kv, kf);
+  if (p.rope_cos) {
+    const int rpos = p.rope_pos ? __ldg(p.rope_pos + row) : pos;
+    if ((unsigned)rpos >= (unsigned)p.rope_n) {
+      if (t == 0) flag_error(p.err_flag, kErrRopeRange);
+      return;
+    }
+    const bool second = t >= 8;                // elements 64.. of the head
+    const int i0 = (t & 7) * 8;                // index within the half
+    float other[8];
+    unpack8(*reinterpret_cast<const uint4*>(p.k_rows + src_row + (second ? i0 : 64 + i0)),
+            other);
+    const float4* cp = reinterpret_cast<const float4*>(p.rope_cos + (size_t)rpos * 64 + i0);
+    const float4* sp = reinterpret_cast<const float4*>(p.rope_sin + (size_t)rpos * 64 + i0);
+    const float4 c0 = __ldg(cp), c1 = __ldg(cp + 1), s0 = __ldg(sp), s1 = __ldg(sp + 1);
+    const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float a = second ? other[e] : kf[e];   // element i
+      const float b = second ? kf[e] : other[e];   // element i + 64
+      kf[e] = second ? __fadd_rn(__fmul_rn(b, c[e]), __fmul_rn(a, s[e]))
+                     : __fsub_rn(__fmul_rn(a, c[e]), __fmul_rn(b, s[e]));
+    }
+  }
   if (!p.fp8) {
     __nv_bfloat16* kd = static_cast<__nv_bfloat16*>(run.k_dst) + dst_row * kHeadDim + t * 8;
     __nv_bfloat16* vd = static_cast<__nv_bfloat16*>(run.v_dst) + dst_row * kHeadDim + t * 8;
-    *reinterpret_cast<uint4*>(kd) = kv;
+    *reinterpret_cast<uint4*>(kd) = p.rope_cos ? pack8_bf16(kf) : kv;
     *reinterpret_cast<uint4*>(vd) = vv;
     return;
   }
-  const float ks = __ldg(p.k_scale + g);
-  const float vs = __ldg(p.v_scale + g);
-  auto quant8 = [](const uint4& in, float s) {
-    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-    uint32_t out[2];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float lo = __uint_as_float(w[i] << 16);
-      const float hi = __uint_as_float(w[i] & 0xFFFF0000u);
-      // value / scale rounded to float32 (IEEE division), then e4m3 RNE, saturating
-      const float2 f = make_float2(__fdiv_rn(lo, s), __fdiv_rn(hi, s));
-      const __nv_fp8x2_storage_t b = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
-      if (i & 1)
-        out[i >> 1] |= (uint32_t)b << 16;
-      else
-        out[i >> 1] = (uint32_t)b;
-    }
-    return make_uint2(out[0], out[1]);
-  };
+  float vf[8];
+  unpack8(vv, vf);
   uint8_t* kd = static_cast<uint8_t*>(run.k_dst) + dst_row * kHeadDim + t * 8;
   uint8_t* vd = static_cast<uint8_t*>(run.v_dst) + dst_row * kHeadDim + t * 8;
-  *reinterpret_cast<uint2*>(kd) = quant8(kv, ks);
-  *reinterpret_cast<uint2*>(vd) = quant8(vv, vs);
+  *reinterpret_cast<uint2*>(kd) = quant8(kf, __ldg(p.k_scale + g));
+  *reinterpret_cast<uint2*>(vd) = quant8(vf, __ldg(p.v_scale + g));
+}
+
+// Keep: CTA g handles kv head g of every pair.  All source rows (K and V) are
+// read into shared memory before any destination is written, so chains of
+// moves within a call (2 -> 1, 5 -> 2) copy the rows as they were.  A pair
+// whose source or destination page id is out of range is skipped and flagged.
+__global__ void __launch_bounds__(256) keep_kernel(const __grid_constant__ KeepParams p) {
+  extern __shared__ uint4 stash[];                 // [n][K, V][row_bytes / 16]
+  allow_next_grid();
+  wait_prior_grid();
+  const int g = blockIdx.x;
+  const int cpr = p.row_bytes / 16;               // 16-byte chunks per row
+  auto row_ptr = [&](const KeepPair& kp, int which, int pos) -> uint4* {
+    uint8_t* base;
+    size_t idx;
+    if (kp.page_table) {
+      const int pid = __ldg(kp.page_table + (pos >> 8));
+      if ((unsigned)pid >= (unsigned)p.num_pages) return nullptr;
+      base = static_cast<uint8_t*>(which ? p.v_pool : p.k_pool);
+      idx = ((size_t)pid * p.hkv + g) * kPage + (pos & (kPage - 1));
+    } else {
+      base = static_cast<uint8_t*>(which ? kp.v_slab : kp.k_slab);
+      idx = (size_t)g * kp.slab_cap + pos;
+    }
+    return reinterpret_cast<uint4*>(base + idx * p.row_bytes);
+  };
+  const int total = p.n * 2 * cpr;
+  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    const int pair = i / (2 * cpr), which = (i / cpr) & 1, ch = i % cpr;
+    const uint4* src = row_ptr(p.pairs[pair], which, p.pairs[pair].src);
+    stash[i] = src ? src[ch] : make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    const int pair = i / (2 * cpr), which = (i / cpr) & 1, ch = i % cpr;
+    const KeepPair& kp = p.pairs[pair];
+    uint4* dst = row_ptr(kp, which, kp.dst);
+    if (!dst || !row_ptr(kp, which, kp.src)) {
+      if (ch == 0) flag_error(p.err_flag, kErrBadPage);
+      continue;
+    }
+    dst[ch] = stash[i];
+  }
 }
 
 cudaError_t launch_write_kv(const WriteParams& p, cudaStream_t s) {
@@ -76,6 +175,19 @@ cudaError_t launch_write_kv(const WriteParams& p, cudaStream_t s) {
   const int grid = (pairs + 15) / 16;
   if (grid == 0) return cudaSuccess;
   return launch_pdl(write_kv_kernel, dim3(grid), dim3(256), 0, s, p);
+}
+
+cudaError_t launch_keep(const KeepParams& p, cudaStream_t s) {
+  if (p.n == 0) return cudaSuccess;
+  const int smem = p.n * 2 * p.row_bytes;
+  static int configured = 0;
+  if (smem > 48 * 1024 && configured < smem) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        keep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxKeep * 2 * 256);
+    if (e != cudaSuccess) return e;
+    configured = kMaxKeep * 2 * 256;
+  }
+  return launch_pdl(keep_kernel, dim3(p.hkv), dim3(256), smem, s, p);
 }
 
 }  // namespace tfpa

@@ -163,3 +163,35 @@ def test_decode_tree_checks_its_ancestor_table():
                            0.088, sc, 7 * FAKE)
     assert [(r["kind"], r["row0"], r["rows"]) for r in rec] == [
         ("partial", 0, 128), ("merge", 0, 128), ("partial", 128, 72), ("merge", 128, 72)]
+
+
+def test_write_kv_rope_and_keep_argument_checks():
+    c = _cache()
+    segs = [B.Seg(1000, page_table=3 * FAKE), B.Seg(500, page_table=4 * FAKE)]
+
+    class T:          # a fake device table: address and shape only
+        def __init__(self, addr, n):
+            self.addr, self.shape = addr, (n, 64)
+
+        def data_ptr(self):
+            return self.addr
+    cos, sin = T(5 * FAKE, 900), T(6 * FAKE, 900)
+    with B.record_launches() as rec:
+        with pytest.raises(B.TfpaError) as e:       # storage position 950 outside a 900-row table
+            B.tfpa_write_kv_rope(c, segs, FAKE, 2 * FAKE, [0], [950], cos, sin)
+    assert e.value.code == B.TFPA_ERANGE and rec == []
+    with B.record_launches() as rec:
+        B.tfpa_write_kv_rope(c, segs, FAKE, 2 * FAKE, [0, 0, 1], [800, 801, 3], cos, sin)
+    assert [(r["kind"], r["rows"]) for r in rec] == [("write_kv", 3)]
+    bad_keep = [([0], [1000], [5], B.TFPA_ERANGE),          # source past the end
+                ([2], [3], [5], B.TFPA_ERANGE),             # no such segment
+                ([0, 0], [3, 4], [5, 5], B.TFPA_EINVAL),    # two writers for one row
+                ([0] * 257, list(range(257)), list(range(300, 557)), B.TFPA_ECAPACITY)]
+    for ks, src, dst, code in bad_keep:
+        with B.record_launches() as rec:
+            with pytest.raises(B.TfpaError) as e:
+                B.tfpa_keep_kv(c, segs, ks, src, dst)
+        assert e.value.code == code and rec == []
+    with B.record_launches() as rec:
+        B.tfpa_keep_kv(c, segs, [0, 0, 1], [3, 2, 7], [2, 1, 8])
+    assert [(r["kind"], r["rows"], r["grid"]) for r in rec] == [("keep", 3, 8)]
