@@ -39,7 +39,7 @@ METRIC = "paged decode KV GB/s (% HBM peak); prompt-chunk attn TFLOP/s (% TC pea
 # from ncu (dram__bytes_read.sum + dram__bytes_write.sum, see
 # profiles/decode_partial_batched_decode.md), valid only while the kernel's
 # sources hash to the value it was taken on.
-DECODE_TRAFFIC = {"bytes": 268_598_784 + 4_458_240, "sources_sha256_16": "383004a4e26b3207"}
+DECODE_TRAFFIC = {"bytes": 268_595_456 + 4_658_688, "sources_sha256_16": "6ff7a4d271fc881d"}
 DECODE_SOURCES = ["paged_kv_cache_235_gb300/csrc/decode.cu",
                   "paged_kv_cache_235_gb300/csrc/common.cuh",
                   "paged_kv_cache_235_gb300/csrc/params.h",
@@ -343,6 +343,45 @@ def time_prefill(w, torch, B, reps):
     return statistics.median(times)
 
 
+def time_store_and_keep(w, torch, B, reps):
+    """tfpa_write_kv_rope of every chunk row and tfpa_keep_kv of 256 rows, one
+    call at a time, L2 flushed before each, CUDA events; medians in ms."""
+    cache, segs, _ = device_case(w, torch, B)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(13)
+    k = torch.randn(w.rows, w.hkv, 128, generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn(w.rows, w.hkv, 128, generator=g, device="cuda").to(torch.bfloat16)
+    n_pos = int(w.row_pos.max()) + 1
+    cos, sin = wl_rope(n_pos)
+    cos, sin = torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda()
+    base = int(w.row_pos.min())
+    ks = np.zeros(256, np.int32)
+    src = (base + 2 * np.arange(256) + 1).astype(np.int32)
+    dst = (base + 1024 + np.arange(256)).astype(np.int32)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    t_store, t_keep = [], []
+    for i in range(reps + 3):
+        for fn, acc in ((lambda: B.tfpa_write_kv_rope(cache, segs, k, v, w.row_seg, w.row_pos,
+                                                      cos, sin), t_store),
+                        (lambda: B.tfpa_keep_kv(cache, segs, ks, src, dst), t_keep)):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            fn()
+            e1.record(s)
+            torch.cuda.synchronize()
+            if i >= 3:
+                acc.append(e0.elapsed_time(e1))
+    assert int(cache.err_flag.item()) == 0, "kernel error flag set"
+    return statistics.median(t_store), statistics.median(t_keep)
+
+
+def wl_rope(n_pos):
+    from paged_kv_cache_235_gb300 import workloads as wl
+    return wl.rope_table(1e6, n_pos)
+
+
 def time_tree_calls(w, torch, B, reps):
     """tfpa_decode_tree one call at a time, CUDA events around each; median ms."""
     cache, segs, q = device_case(w, torch, B)
@@ -530,6 +569,21 @@ def main():
             "seated_streams": len(w6.streams), "waiting_streams": len(w6.waiting),
             "us_per_call": ms6 * 1e3, "kv_gbs": (kv6 + qo6) / (ms6 / 1e3) / 1e9,
             "frac_of_measured_hbm": (kv6 + qo6) / (ms6 / 1e3) / 1e9 / pk["hbm_gbs"]}
+        w8 = wl.prompt_chunk()
+        ms_st, ms_kp = time_store_and_keep(w8, torch, B, 20)
+        st_bytes = w8.rows * w8.hkv * 128 * 2 * (2 + 2) + w8.rows * 64 * 4 * 2
+        kp_bytes = 256 * w8.hkv * 2 * 256 * 2
+        extra["kv_store_rope"] = {
+            "workload": "4,096 prompt-chunk rows into a paged bf16 cache, 8 kv heads, K rotated "
+                        "by its position (float32 cos/sin table); L2 flushed before each call",
+            "us_per_call": ms_st * 1e3, "gbs": st_bytes / (ms_st / 1e3) / 1e9,
+            "frac_of_measured_hbm": st_bytes / (ms_st / 1e3) / 1e9 / pk["hbm_gbs"],
+            "bytes": st_bytes}
+        extra["keep"] = {
+            "workload": "256 stored rows (8 kv heads, K and V, bf16) moved within one paged "
+                        "stream in one call; L2 flushed before each call",
+            "us_per_call": ms_kp * 1e3, "gbs": kp_bytes / (ms_kp / 1e3) / 1e9,
+            "note": "2 MB moved: launch and latency bound"}
         w7 = wl.tree_verify()
         ms7 = time_tree_calls(w7, torch, B, 20)
         kv7, qo7 = kv_bytes(w7)
