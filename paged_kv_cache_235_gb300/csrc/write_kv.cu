@@ -127,12 +127,18 @@ __global__ void __launch_bounds__(256) write_kv_kernel(const __grid_constant__ W
   *reinterpret_cast<uint2*>(vd) = quant8(vf, __ldg(p.v_scale + g));
 }
 
-// Keep: CTA g handles kv head g of every pair.  All source rows (K and V) are
-// read into shared memory before any destination is written, so chains of
-// moves within a call (2 -> 1, 5 -> 2) copy the rows as they were.  A pair
-// whose source or destination page id is out of range is skipped and flagged.
-__global__ void __launch_bounds__(256) keep_kernel(const __grid_constant__ KeepParams p) {
+// Keep: CTA g handles kv head g of every pair.  The pairs' source and
+// destination row addresses (K and V) are looked up once into shared memory;
+// then every source row is read into shared memory before any destination is
+// written, so chains of moves within a call (2 -> 1, 5 -> 2) copy the rows
+// as they were.  A pair whose source or destination page id is out of range
+// is skipped and flagged.
+constexpr int kKeepThreads = 1024;
+__global__ void __launch_bounds__(kKeepThreads)
+    keep_kernel(const __grid_constant__ KeepParams p) {
   extern __shared__ uint4 stash[];                 // [n][K, V][row_bytes / 16]
+  __shared__ uint4* src_row[kMaxKeep][2];
+  __shared__ uint4* dst_row[kMaxKeep][2];
   allow_next_grid();
   wait_prior_grid();
   const int g = blockIdx.x;
@@ -151,22 +157,27 @@ __global__ void __launch_bounds__(256) keep_kernel(const __grid_constant__ KeepP
     }
     return reinterpret_cast<uint4*>(base + idx * p.row_bytes);
   };
+  for (int i = threadIdx.x; i < 2 * p.n; i += blockDim.x) {
+    const KeepPair& kp = p.pairs[i >> 1];
+    uint4* s = row_ptr(kp, i & 1, kp.src);
+    uint4* d = row_ptr(kp, i & 1, kp.dst);
+    if (!s || !d) {
+      flag_error(p.err_flag, kErrBadPage);
+      s = d = nullptr;
+    }
+    src_row[i >> 1][i & 1] = s;
+    dst_row[i >> 1][i & 1] = d;
+  }
+  __syncthreads();
   const int total = p.n * 2 * cpr;
   for (int i = threadIdx.x; i < total; i += blockDim.x) {
-    const int pair = i / (2 * cpr), which = (i / cpr) & 1, ch = i % cpr;
-    const uint4* src = row_ptr(p.pairs[pair], which, p.pairs[pair].src);
-    stash[i] = src ? src[ch] : make_uint4(0, 0, 0, 0);
+    const uint4* s = src_row[i / (2 * cpr)][(i / cpr) & 1];
+    stash[i] = s ? s[i % cpr] : make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
   for (int i = threadIdx.x; i < total; i += blockDim.x) {
-    const int pair = i / (2 * cpr), which = (i / cpr) & 1, ch = i % cpr;
-    const KeepPair& kp = p.pairs[pair];
-    uint4* dst = row_ptr(kp, which, kp.dst);
-    if (!dst || !row_ptr(kp, which, kp.src)) {
-      if (ch == 0) flag_error(p.err_flag, kErrBadPage);
-      continue;
-    }
-    dst[ch] = stash[i];
+    uint4* d = dst_row[i / (2 * cpr)][(i / cpr) & 1];
+    if (d) d[i % cpr] = stash[i];
   }
 }
 
@@ -187,7 +198,7 @@ cudaError_t launch_keep(const KeepParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = kMaxKeep * 2 * 256;
   }
-  return launch_pdl(keep_kernel, dim3(p.hkv), dim3(256), smem, s, p);
+  return launch_pdl(keep_kernel, dim3(p.hkv), dim3(kKeepThreads), smem, s, p);
 }
 
 }  // namespace tfpa
