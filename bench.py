@@ -377,6 +377,36 @@ def time_store_and_keep(w, torch, B, reps):
     return statistics.median(t_store), statistics.median(t_keep)
 
 
+def time_save_restore(w, torch, B, reps):
+    """tfpa_save_kv / tfpa_restore_kv of a whole 32k-position stream to and
+    from pinned host memory, next to plain runtime copies of the same byte
+    count (device -> pinned host, and back) as the link's reference; medians
+    in ms: (save, restore, d2h copy, h2d copy)."""
+    cache, segs, _ = device_case(w, torch, B)
+    seg = segs[0]
+    L = w.streams[0].seq_len
+    nbytes = 2 * w.hkv * L * 128 * 2
+    img = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    out = {k: [] for k in ("save", "restore", "d2h", "h2d")}
+    ops = (("save", lambda: B.tfpa_save_kv(cache, seg, 0, L, img)),
+           ("restore", lambda: B.tfpa_restore_kv(cache, seg, 0, L, img)),
+           ("d2h", lambda: img.copy_(dev, non_blocking=True)),
+           ("h2d", lambda: dev.copy_(img, non_blocking=True)))
+    for i in range(reps + 2):
+        for name, fn in ops:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            fn()
+            e1.record(s)
+            torch.cuda.synchronize()
+            if i >= 2:
+                out[name].append(e0.elapsed_time(e1))
+    assert int(cache.err_flag.item()) == 0, "kernel error flag set"
+    return nbytes, {k: statistics.median(v) for k, v in out.items()}
+
+
 def wl_rope(n_pos):
     from paged_kv_cache_235_gb300 import workloads as wl
     return wl.rope_table(1e6, n_pos)
@@ -584,6 +614,19 @@ def main():
                         "stream in one call; L2 flushed before each call",
             "us_per_call": ms_kp * 1e3, "gbs": kp_bytes / (ms_kp / 1e3) / 1e9,
             "note": "2 MB moved: launch and latency bound"}
+        w9 = wl.prompt_chunk(prefix=28672, chunk=4096)
+        nb9, t9 = time_save_restore(w9, torch, B, 10)
+        gbs = {k: nb9 / (v / 1e3) / 1e9 for k, v in t9.items()}
+        extra["save_restore"] = {
+            "workload": "one 32,768-position bf16 stream, 8 kv heads (134 MB of K and V), saved "
+                        "to and restored from pinned host memory by one kernel each",
+            "bytes": nb9, "save_ms": t9["save"], "restore_ms": t9["restore"],
+            "save_gbs": gbs["save"], "restore_gbs": gbs["restore"],
+            "runtime_copy_gbs": {"d2h": gbs["d2h"], "h2d": gbs["h2d"]},
+            "frac_of_runtime_copy": {"save": gbs["save"] / gbs["d2h"],
+                                     "restore": gbs["restore"] / gbs["h2d"]},
+            "note": "the reference is a plain runtime copy of the same byte count between a "
+                    "contiguous device buffer and the same pinned buffer"}
         w7 = wl.tree_verify()
         ms7 = time_tree_calls(w7, torch, B, 20)
         kv7, qo7 = kv_bytes(w7)

@@ -58,7 +58,8 @@ enum {
   TFPA_ERANGE = -2,      /* a position, segment or (host-mirrored) page id out of range */
   TFPA_ECAPACITY = -3,   /* scratch too small for the requested rows/splits */
   TFPA_ECUDA = -4,       /* a CUDA runtime/driver call or a launch failed    */
-  TFPA_EDEVICE = -5      /* current device is not sm_100-family (tcgen05)    */
+  TFPA_EDEVICE = -5,     /* current device is not sm_100-family (tcgen05)    */
+  TFPA_ELANEMEM = -6     /* the page pool cannot hold the claim now: wait     */
 };
 
 typedef enum { TFPA_BF16 = 0, TFPA_FP8_E4M3 = 1 } tfpa_kv_dtype;
@@ -132,6 +133,53 @@ int tfpa_write_kv_rope(const tfpa_cache* cache, const tfpa_seg* segs, int32_t ns
 int tfpa_keep_kv(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
                  const int32_t* keep_seg, const int32_t* keep_src, const int32_t* keep_dst,
                  int32_t n, cudaStream_t stream);
+
+/* ---- Page pool admission (host) ------------------------------------------
+ * The pages' memory admission (PR #2011 review, "Memory admission"): a
+ * request claims its pages (prompt, max_tokens and one more forward) up front
+ * when it is seated, never grows them, waits with LaneMemory when the pool is
+ * full, and is turned away by fits() when it could never fit.  Reading used:
+ * a claim is all or nothing and takes the lowest free page ids (pages need not
+ * be contiguous, so only the free count decides); a released page may be
+ * claimed again.  Thread-safe.  No CUDA call. */
+typedef struct tfpa_pool tfpa_pool;
+tfpa_pool* tfpa_pool_create(int32_t num_pages);      /* NULL if num_pages < 1       */
+void tfpa_pool_destroy(tfpa_pool* pool);
+int32_t tfpa_pool_free(const tfpa_pool* pool);        /* pages free now              */
+int tfpa_pool_fits(const tfpa_pool* pool, int32_t npages);  /* 1 if npages <= pool size */
+/* Claims npages pages into pages_out (HOST int32[npages], ascending).
+ * TFPA_ELANEMEM when fewer are free now (nothing claimed), TFPA_ECAPACITY
+ * when the pool could never hold them, TFPA_EINVAL for npages < 0 or NULL. */
+int tfpa_pool_claim(tfpa_pool* pool, int32_t npages, int32_t* pages_out);
+/* Returns pages (HOST int32[n]).  TFPA_EINVAL (and nothing released) if one
+ * is out of range, not claimed, or listed twice. */
+int tfpa_pool_release(tfpa_pool* pool, const int32_t* pages, int32_t n);
+
+/* Device-side page-table staging (the pages stage a prompt chunk's page ids
+ * between chunks, PR #2011 review, and measure host gaps from it): writes
+ * pages[0..n) (HOST int32) into page_table (DEVICE int32) at [first, first+n)
+ * on the stream.  The ids travel in kernel parameters (up to 2,048 a launch),
+ * so there is no copy call and no host synchronisation; later work on the
+ * stream sees the entries.  TFPA_EINVAL for NULL, first < 0 or n < 0. */
+int tfpa_stage_pages(int32_t* page_table, int32_t first, const int32_t* pages, int32_t n,
+                     cudaStream_t stream);
+
+/* ---- Save and restore a stream's stored rows ------------------------------
+ * Page-granular save/restore of a stream's K and V (PR #2011 review: save
+ * and restore copies, one copy per page, and a kernel writing mapped host
+ * memory measured faster than copies at 32k).  Positions [p0, p1) of segment
+ * seg, every kv head, the stored bytes unchanged, to or from an image laid out
+ * [K, V][hkv][p1 - p0][128] elements of the cache's dtype (2 or 1 bytes):
+ *   image : a pointer the GPU can access, 16-byte aligned: pinned (page-
+ *           locked) host memory, registered host memory, or device memory.
+ * One kernel launch; the copy runs on the stream (no host synchronisation).
+ * A page id out of range skips its rows and ORs 1 into cache->err_flag.
+ * TFPA_ERANGE unless 0 <= p0 <= p1 <= seq_len; TFPA_EINVAL for a NULL or
+ * misaligned image. */
+int tfpa_save_kv(const tfpa_cache* cache, const tfpa_seg* seg, int32_t p0, int32_t p1,
+                 void* image, cudaStream_t stream);
+int tfpa_restore_kv(const tfpa_cache* cache, const tfpa_seg* seg, int32_t p0, int32_t p1,
+                    const void* image, cudaStream_t stream);
 
 /* Split policy, a function of a stream's own length only (so a stream's
  * partials never depend on its batch): pages_per_split = max(2,

@@ -113,3 +113,27 @@ def gather(cache: Cache, seg: Segment, g: int, n: int):
     ks = np.float64(np.float32(cache.k_scale[g]))
     vs = np.float64(np.float32(cache.v_scale[g]))
     return e4m3.decode(k_raw) * ks, e4m3.decode(v_raw) * vs
+
+
+def save_image(cache: Cache, seg: Segment, p0: int, p1: int) -> np.ndarray:
+    """Stored rows [p0, p1) of a stream, every kv head, K then V, as stored
+    (bf16 bits or e4m3 codes): ``[2][hkv][p1 - p0][d]``.  The layout of a
+    save/restore image (TensorFold PR #2011 review: save and restore copies)."""
+    out = []
+    for which in ("k", "v"):
+        heads = []
+        for g in range(cache.hkv):
+            heads.append(np.stack([_store(cache, seg, which, g, p)[0][
+                _store(cache, seg, which, g, p)[1]] for p in range(p0, p1)]) if p1 > p0 else
+                np.zeros((0, cache.d), dtype=(np.uint16 if cache.dtype == "bf16" else np.uint8)))
+        out.append(np.stack(heads))
+    return np.stack(out)
+
+
+def restore_image(cache: Cache, seg: Segment, p0: int, p1: int, image: np.ndarray) -> None:
+    """The inverse of ``save_image``: writes the image back into rows [p0, p1) (in place)."""
+    for wi, which in enumerate(("k", "v")):
+        for g in range(cache.hkv):
+            for i, p in enumerate(range(p0, p1)):
+                arr, idx = _store(cache, seg, which, g, p)
+                arr[idx] = image[wi, g, i]

@@ -23,11 +23,14 @@ MAX_SPLITS = 32
 BF16, FP8_E4M3 = 0, 1
 
 TFPA_OK, TFPA_EINVAL, TFPA_ERANGE, TFPA_ECAPACITY, TFPA_ECUDA, TFPA_EDEVICE = 0, -1, -2, -3, -4, -5
+TFPA_ELANEMEM = -6
 
 EXPORTS = ("tfpa_pages_per_split", "tfpa_num_splits", "tfpa_write_kv", "tfpa_decode_partial",
            "tfpa_merge", "tfpa_decode", "tfpa_prefill", "tfpa_set_launch_hook",
            "tfpa_strerror", "tfpa_version", "tfpa_decode_static", "tfpa_decode_tree",
-           "tfpa_write_kv_rope", "tfpa_keep_kv")
+           "tfpa_write_kv_rope", "tfpa_keep_kv", "tfpa_pool_create", "tfpa_pool_destroy",
+           "tfpa_pool_free", "tfpa_pool_fits", "tfpa_pool_claim", "tfpa_pool_release",
+           "tfpa_stage_pages", "tfpa_save_kv", "tfpa_restore_kv")
 
 
 class TfpaError(RuntimeError):
@@ -62,7 +65,8 @@ class tfpa_launch_record(ctypes.Structure):
 
 
 HOOK = ctypes.CFUNCTYPE(None, ctypes.POINTER(tfpa_launch_record), ctypes.c_void_p)
-KINDS = {0: "write_kv", 1: "partial", 2: "merge", 3: "prefill", 4: "keep"}
+KINDS = {0: "write_kv", 1: "partial", 2: "merge", 3: "prefill", 4: "keep", 5: "stage",
+         6: "save", 7: "restore"}
 
 _lib = None
 
@@ -95,6 +99,24 @@ def lib():
         L.tfpa_write_kv_rope.restype = ctypes.c_int
         L.tfpa_keep_kv.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, i32, vp]
         L.tfpa_keep_kv.restype = ctypes.c_int
+        L.tfpa_pool_create.argtypes = [i32]
+        L.tfpa_pool_create.restype = vp
+        L.tfpa_pool_destroy.argtypes = [vp]
+        L.tfpa_pool_destroy.restype = None
+        L.tfpa_pool_free.argtypes = [vp]
+        L.tfpa_pool_free.restype = i32
+        L.tfpa_pool_fits.argtypes = [vp, i32]
+        L.tfpa_pool_fits.restype = ctypes.c_int
+        L.tfpa_pool_claim.argtypes = [vp, i32, vp]
+        L.tfpa_pool_claim.restype = ctypes.c_int
+        L.tfpa_pool_release.argtypes = [vp, vp, i32]
+        L.tfpa_pool_release.restype = ctypes.c_int
+        L.tfpa_stage_pages.argtypes = [vp, i32, vp, i32, vp]
+        L.tfpa_stage_pages.restype = ctypes.c_int
+        L.tfpa_save_kv.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, i32, vp, vp]
+        L.tfpa_save_kv.restype = ctypes.c_int
+        L.tfpa_restore_kv.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, i32, vp, vp]
+        L.tfpa_restore_kv.restype = ctypes.c_int
         L.tfpa_decode_tree.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, vp, i32,
                                        ctypes.c_float, P(tfpa_scratch), vp, vp, vp]
         L.tfpa_decode_tree.restype = ctypes.c_int
@@ -276,6 +298,61 @@ def tfpa_keep_kv(cache: Cache, segs: Sequence[Seg], keep_seg, keep_src, keep_dst
     cc = cache.c()
     _check(lib().tfpa_keep_kv(ctypes.byref(cc), cs, n, _ptr(a), _ptr(b), _ptr(d), len(a),
                               _stream(stream)), "tfpa_keep_kv")
+
+
+class Pool:
+    """The page pool's admission ledger (host only): claims are up front and
+    all or nothing; ``claim`` raises TfpaError(TFPA_ELANEMEM) while the pool
+    cannot hold the request and TfpaError(TFPA_ECAPACITY) if it never could."""
+
+    def __init__(self, num_pages: int):
+        self._p = lib().tfpa_pool_create(int(num_pages))
+        if not self._p:
+            raise TfpaError(TFPA_EINVAL, "tfpa_pool_create")
+        self.num_pages = int(num_pages)
+
+    def free(self) -> int:
+        return int(lib().tfpa_pool_free(self._p))
+
+    def fits(self, npages: int) -> bool:
+        return bool(lib().tfpa_pool_fits(self._p, int(npages)))
+
+    def claim(self, npages: int) -> np.ndarray:
+        out = np.zeros(max(1, int(npages)), np.int32)
+        _check(lib().tfpa_pool_claim(self._p, int(npages), out.ctypes.data), "tfpa_pool_claim")
+        return out[: int(npages)]
+
+    def release(self, pages) -> None:
+        a = _i32(pages)
+        _check(lib().tfpa_pool_release(self._p, _ptr(a), len(a)), "tfpa_pool_release")
+
+    def __del__(self):
+        if getattr(self, "_p", None):
+            lib().tfpa_pool_destroy(self._p)
+            self._p = None
+
+
+def tfpa_stage_pages(page_table, first: int, pages, stream=None) -> None:
+    """Write page ids into a device page table at [first, first + len) on the stream."""
+    a = _i32(pages)
+    _check(lib().tfpa_stage_pages(_ptr(page_table), int(first), _ptr(a), len(a),
+                                  _stream(stream)), "tfpa_stage_pages")
+
+
+def tfpa_save_kv(cache: Cache, seg: Seg, p0: int, p1: int, image, stream=None) -> None:
+    """Stored rows [p0, p1) of one stream into ``image`` ([K, V][hkv][p1-p0][128])."""
+    cs, _ = _segs([seg])
+    cc = cache.c()
+    _check(lib().tfpa_save_kv(ctypes.byref(cc), cs, int(p0), int(p1), _ptr(image),
+                              _stream(stream)), "tfpa_save_kv")
+
+
+def tfpa_restore_kv(cache: Cache, seg: Seg, p0: int, p1: int, image, stream=None) -> None:
+    """The reverse of tfpa_save_kv: ``image`` back into rows [p0, p1) of the stream."""
+    cs, _ = _segs([seg])
+    cc = cache.c()
+    _check(lib().tfpa_restore_kv(ctypes.byref(cc), cs, int(p0), int(p1), _ptr(image),
+                                 _stream(stream)), "tfpa_restore_kv")
 
 
 def tfpa_decode_tree(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, row_anc,

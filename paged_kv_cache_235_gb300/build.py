@@ -17,7 +17,8 @@ LIB = os.path.join(PKG, "libtfpa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I" + os.path.join(ROOT, "include"), "-I" + CSRC]
-SOURCES = ["host.cu", "write_kv.cu", "decode.cu", "prefill.cu", "static_scratch.cu"]
+SOURCES = ["host.cu", "write_kv.cu", "decode.cu", "prefill.cu", "static_scratch.cu", "copy.cu",
+           "pool.cu"]
 
 
 def nvcc() -> str:

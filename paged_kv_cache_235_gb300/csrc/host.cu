@@ -627,6 +627,71 @@ extern "C" int tfpa_keep_kv(const tfpa_cache* c, const tfpa_seg* segs, int32_t n
   return TFPA_OK;
 }
 
+extern "C" int tfpa_stage_pages(int32_t* page_table, int32_t first, const int32_t* pages,
+                                int32_t n, cudaStream_t stream) {
+  if (!page_table || first < 0 || n < 0 || (n > 0 && !pages)) return TFPA_EINVAL;
+  if (n == 0) return TFPA_OK;
+  int e;
+  if (!dry_run() && (e = check_device())) return e;
+  std::lock_guard<std::mutex> lock(g_mu);
+  static StageParams p;
+  for (int32_t done = 0; done < n; done += kMaxStage) {
+    const int32_t m = std::min<int32_t>(kMaxStage, n - done);
+    p.table = page_table;
+    p.first = first + done;
+    p.n = m;
+    std::memcpy(p.ids, pages + done, sizeof(int32_t) * m);
+    record(5, done, m, 0, m, 1, 0, 0);
+    if (!dry_run())
+      if ((e = to_err(launch_stage(p, stream)))) return e;
+  }
+  return TFPA_OK;
+}
+
+namespace {
+
+int copy_impl(const tfpa_cache* c, const tfpa_seg* seg, int32_t p0, int32_t p1, const void* image,
+              bool restore, cudaStream_t stream) {
+  int e;
+  if ((e = check_cache(c)) || (e = check_segs(c, seg, 1))) return e;
+  if (!image || !aligned(image, 16)) return TFPA_EINVAL;
+  if (p0 < 0 || p0 > p1 || p1 > seg->seq_len) return TFPA_ERANGE;
+  if (p0 == p1) return TFPA_OK;
+  if (!dry_run() && (e = check_device())) return e;
+  CopyParams p{};
+  p.page_table = seg->page_table;
+  p.k_base = seg->page_table ? c->k_pool : seg->k_slab;
+  p.v_base = seg->page_table ? c->v_pool : seg->v_slab;
+  p.image = static_cast<uint8_t*>(const_cast<void*>(image));
+  p.err_flag = c->err_flag;
+  p.slab_cap = seg->page_table ? 0 : seg->slab_cap;
+  p.p0 = p0;
+  p.p1 = p1;
+  p.page0 = p0 / kPage;
+  p.hkv = c->hkv;
+  p.num_pages = c->num_pages;
+  p.row_bytes = c->dtype == TFPA_FP8_E4M3 ? kHeadDim : 2 * kHeadDim;
+  p.restore = restore ? 1 : 0;
+  const int npages = (p1 - 1) / kPage - p0 / kPage + 1;
+  std::lock_guard<std::mutex> lock(g_mu);
+  record(restore ? 7 : 6, p0, p1 - p0, 0, npages * c->hkv * 2, npages * c->hkv * 2, 0, 0);
+  if (!dry_run())
+    if ((e = to_err(launch_copy(p, npages, stream)))) return e;
+  return TFPA_OK;
+}
+
+}  // namespace
+
+extern "C" int tfpa_save_kv(const tfpa_cache* cache, const tfpa_seg* seg, int32_t p0, int32_t p1,
+                            void* image, cudaStream_t stream) {
+  return copy_impl(cache, seg, p0, p1, image, false, stream);
+}
+
+extern "C" int tfpa_restore_kv(const tfpa_cache* cache, const tfpa_seg* seg, int32_t p0,
+                               int32_t p1, const void* image, cudaStream_t stream) {
+  return copy_impl(cache, seg, p0, p1, image, true, stream);
+}
+
 extern "C" void tfpa_set_launch_hook(tfpa_launch_hook hook, void* user, int dry_run_flag) {
   std::lock_guard<std::mutex> lock(g_mu);
   g_hook.fn = hook;
@@ -642,6 +707,7 @@ extern "C" const char* tfpa_strerror(int code) {
     case TFPA_ECAPACITY: return "scratch capacity exceeded (rows or splits)";
     case TFPA_ECUDA: return "CUDA call or launch failed";
     case TFPA_EDEVICE: return "current device is not sm_100-family";
+    case TFPA_ELANEMEM: return "the page pool cannot hold the claim now (wait for releases)";
     default: return "unknown error";
   }
 }

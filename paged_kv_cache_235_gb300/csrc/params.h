@@ -158,9 +158,37 @@ struct PrefillParams {
   float scale_log2;
 };
 
+// Page-table staging: ids written into a device page table on the stream.
+constexpr int kMaxStage = 2048;
+struct StageParams {
+  int32_t* table;
+  int32_t first;
+  int32_t n;
+  int32_t ids[kMaxStage];
+};
+
+// Save / restore of a stream's stored rows [p0, p1) to / from an image laid
+// out [K, V][hkv][p1 - p0][row].
+struct CopyParams {
+  const int32_t* page_table;  // nullptr => slab
+  void* k_base;               // pool or slab
+  void* v_base;
+  uint8_t* image;
+  int32_t* err_flag;
+  int32_t slab_cap;
+  int32_t p0, p1;
+  int32_t page0;              // first page of the range
+  int32_t hkv;
+  int32_t num_pages;
+  int32_t row_bytes;          // 256 (bf16) or 128 (e4m3)
+  int32_t restore;            // 0: cache -> image, 1: image -> cache
+};
+
 // Launchers (defined next to their kernels).
 cudaError_t launch_write_kv(const WriteParams& p, cudaStream_t s);
 cudaError_t launch_keep(const KeepParams& p, cudaStream_t s);
+cudaError_t launch_stage(const StageParams& p, cudaStream_t s);
+cudaError_t launch_copy(const CopyParams& p, int npages, cudaStream_t s);
 cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, bool fp8, int grid, cudaStream_t s);
