@@ -713,6 +713,16 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
   while (ri + 1 < p.nruns && p.runs[ri + 1].row0 <= row) ++ri;
   const int nsplit = p.runs[ri].nsplit;
   const size_t slot0 = ((size_t)row * p.hq + h) * p.max_splits;
+  // Every slot below nsplit was written by the partial kernel (an empty split
+  // holds o = 0 with weight 0).  Every split's o chunk is loaded together
+  // with the (m, l) pairs, before the reductions that need them, so a merge
+  // waits for one round of loads; the sums run in split order.
+  static_assert(kMaxSplits == 32, "one load per split");
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + slot0 * kHeadDim) + lane;
+  float4 v0[kMaxSplits];
+#pragma unroll
+  for (int u = 0; u < kMaxSplits; ++u)
+    if (u < nsplit) v0[u] = po[u * (kHeadDim / 4)];
   float m = -INFINITY, l = 0.f;
   if (lane < nsplit) {
     const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (slot0 + lane) * 2);
@@ -726,32 +736,17 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
   float L = a * l;
 #pragma unroll
   for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  // Every slot below nsplit was written by the partial kernel (an empty split
-  // holds o = 0 with weight 0), so the loads need no guard and can be batched.
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* po = reinterpret_cast<const float4*>(p.part_o + slot0 * kHeadDim) + lane;
-  int s = 0;
-  for (; s + 8 <= nsplit; s += 8) {
-    float4 v[8];
+  auto add = [&](int sp, const float4& v) {
+    const float as = __shfl_sync(0xffffffffu, a, sp);
+    acc.x = __fmaf_rn(as, v.x, acc.x);
+    acc.y = __fmaf_rn(as, v.y, acc.y);
+    acc.z = __fmaf_rn(as, v.z, acc.z);
+    acc.w = __fmaf_rn(as, v.w, acc.w);
+  };
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = po[(s + u) * (kHeadDim / 4)];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float as = __shfl_sync(0xffffffffu, a, s + u);
-      acc.x += as * v[u].x;
-      acc.y += as * v[u].y;
-      acc.z += as * v[u].z;
-      acc.w += as * v[u].w;
-    }
-  }
-  for (; s < nsplit; ++s) {
-    const float4 v = po[s * (kHeadDim / 4)];
-    const float as = __shfl_sync(0xffffffffu, a, s);
-    acc.x += as * v.x;
-    acc.y += as * v.y;
-    acc.z += as * v.z;
-    acc.w += as * v.w;
-  }
+  for (int u = 0; u < kMaxSplits; ++u)
+    if (u < nsplit) add(u, v0[u]);
   const float inv = 1.f / L;
   uint2 packed;
   packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
