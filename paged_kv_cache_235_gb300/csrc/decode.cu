@@ -70,22 +70,29 @@ struct Cfg {
   static constexpr int kKS = kKeysPerWarp / 16;        // PV k-steps per warp
 };
 
+// A work item: (run, kv head g, m-tile mt, split sigma).  In a wide run an
+// item covers the four m-tiles 4 mt .. 4 mt + 3 (one per consumer warp pair).
 struct Item {
   int run, g, mt, sigma;
 };
+
+__device__ __forceinline__ int mtile_groups(const RunInfo& ru, int group) {
+  const int mtiles = (ru.nrows * group + 15) >> 4;
+  return ru.wide ? (mtiles + 3) >> 2 : mtiles;
+}
 
 __device__ __forceinline__ Item item_of(const DecodeParams& p, int it) {
   int r = 0;
   while (r + 1 < p.nruns && p.runs[r + 1].item0 <= it) ++r;
   const RunInfo& ru = p.runs[r];
   int local = it - ru.item0;
-  const int mtiles = (ru.nrows * p.group + 15) >> 4;
+  const int mgroups = mtile_groups(ru, p.group);
   Item x;
   x.run = r;
   x.sigma = local % ru.nsplit;
   local /= ru.nsplit;
-  x.mt = local % mtiles;
-  x.g = local / mtiles;
+  x.mt = local % mgroups;
+  x.g = local / mgroups;
   return x;
 }
 
@@ -98,12 +105,12 @@ __device__ __forceinline__ void cta_items(const DecodeParams& p, int& begin, int
 }
 
 // Key range [klo, khi) an item must read: its split's pages, cut at the
-// stream length and at the last position among the m-tile's rows.
+// stream length and at the last position among the item's rows.
 __device__ __forceinline__ void item_keys(const DecodeParams& p, const Item& x, int& klo,
                                           int& khi) {
   const RunInfo& ru = p.runs[x.run];
   const int nq = ru.nrows * p.group;
-  const int last_qv = min(x.mt * 16 + 15, nq - 1);
+  const int last_qv = min((ru.wide ? 64 * x.mt + 63 : 16 * x.mt + 15), nq - 1);
   const int maxpos = ru.pos0 + last_qv / p.group;
   klo = x.sigma * ru.pps * kPage;
   khi = min(min(klo + ru.pps * kPage, ru.seq_len), maxpos + 1);
@@ -175,7 +182,7 @@ __device__ __forceinline__ int out_col(int nt, int n) {
 // their ancestor masks (all ones for causal rows) and their score multipliers
 // (f16 operands for e4m3 caches: each row is scaled by a power of two into
 // f16 range, exact for every element within 2^28 of the row's largest).
-template <bool FP8, bool TREE>
+template <bool FP8, bool GEN>
 __device__ __forceinline__ void load_q(const DecodeParams& p, const RunInfo& ru, const Item& x,
                                        int gq, int c, uint32_t (&qr)[2][16], int (&lim)[2],
                                        uint64_t (&anc)[2], float (&sc)[2]) {
@@ -191,7 +198,7 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, const RunInfo& ru,
       const int r = qv / p.group;
       const int h = x.g * p.group + (qv - r * p.group);
       lim[hr] = ru.pos0 + r;
-      if (TREE) anc[hr] = __ldg(p.anc + ru.row0 + r);
+      if (GEN && p.anc) anc[hr] = __ldg(p.anc + ru.row0 + r);
       const uint4* qp =
           reinterpret_cast<const uint4*>(p.q + ((size_t)(ru.row0 + r) * p.hq + h) * kHeadDim);
       if (FP8) {
@@ -245,7 +252,182 @@ struct CombBars {
   uint64_t* done;        // the combiners finished the item (fold buffer free)
 };
 
-template <bool FP8, bool TREE>
+// One block of this warp's keys: NSB sub-blocks of kKeysPerWarp keys from key
+// wk0 of the stage chunk at sb (k0 = the chunk's first key): scores, the
+// causal or ancestor mask, the online softmax, and O += P V.
+template <bool FP8, bool GEN, int NSB>
+__device__ __forceinline__ void attend_block(uint32_t sb, int wk0, int k0, int seq_len,
+                                             const uint32_t (&qr)[2][16], const int (&lim)[2],
+                                             const float (&sc)[2], const uint64_t (&anc)[2],
+                                             int tree_low, int gq, int c, float (&m_run)[2],
+                                             float (&l_run)[2], float (&o)[16][4]) {
+  using C = Cfg<FP8>;
+  constexpr int kNT = C::kNT * NSB;       // score n-tiles
+  constexpr int kKS = C::kKS * NSB;       // PV k-steps
+  constexpr int kKeys = C::kKeysPerWarp * NSB;
+  const int key_base = k0 + wk0;
+  // ---- S = Q K^T over this warp's keys
+  float s[kNT][4];
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) {
+    s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    const int kr = wk0 + nt * 8 + gq;
+    uint32_t kb[16];
+    if (FP8) {
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const uint4 w = lds128(swz128(sb, kr, 2 * c + ch));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          kb[8 * ch + 2 * i] = e4m3x2_to_f16x2((uint16_t)(ws[i] & 0xFFFF));
+          kb[8 * ch + 2 * i + 1] = e4m3x2_to_f16x2((uint16_t)(ws[i] >> 16));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const uint32_t base = sb + (ch >> 1) * 16384u;
+        const uint4 w = lds128(swz128(base, kr, 2 * c + (ch & 1)));
+        kb[4 * ch + 0] = w.x;
+        kb[4 * ch + 1] = w.y;
+        kb[4 * ch + 2] = w.z;
+        kb[4 * ch + 3] = w.w;
+      }
+    }
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t a[4] = {qr[0][2 * ks], qr[1][2 * ks], qr[0][2 * ks + 1],
+                             qr[1][2 * ks + 1]};
+      if (FP8)
+        mma_f16(s[nt], a, kb[2 * ks], kb[2 * ks + 1]);
+      else
+        mma_bf16(s[nt], a, kb[2 * ks], kb[2 * ks + 1]);
+    }
+  }
+  // ---- scale, causal (or ancestor) mask, online softmax (rows gq,
+  // gq+8; a row's keys are spread over the 4 threads of a quad).  The
+  // running max is only moved when it grows by more than 2^8, so O is
+  // rarely rescaled.  Ancestor masks are only consulted where a key
+  // lies within 63 positions of some row of the warp.
+  const bool tree_zone = GEN && key_base + kKeys > tree_low;
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int hr = j >> 1;
+      const int key = key_base + nt * 8 + 2 * c + (j & 1);
+      bool vis = key <= lim[hr];
+      if (tree_zone) {
+        const int dd = lim[hr] - key;
+        vis = vis && (dd > 63 || ((anc[hr] >> dd) & 1ull));
+      }
+      const float v = vis ? s[nt][j] * sc[hr] : -INFINITY;
+      s[nt][j] = v;
+      mx[hr] = fmaxf(mx[hr], v);
+    }
+  }
+  float alpha[2];
+  bool resc = false;
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
+    mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
+    alpha[hr] = 1.f;
+    if (mx[hr] > m_run[hr] + kRescaleThreshold) {
+      alpha[hr] = fast_exp2(m_run[hr] - mx[hr]);
+      l_run[hr] *= alpha[hr];
+      m_run[hr] = mx[hr];
+      resc = true;
+    }
+  }
+  if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      o[nt][0] *= alpha[0];
+      o[nt][1] *= alpha[0];
+      o[nt][2] *= alpha[1];
+      o[nt][3] *= alpha[1];
+    }
+  }
+  const float base0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
+  const float base1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float e = fast_exp2(s[nt][j] - ((j >> 1) ? base1 : base0));
+      s[nt][j] = e;
+      l_run[j >> 1] += e;
+    }
+  }
+  // ---- O += P V
+  const uint32_t vb = sb + 32768u;
+#pragma unroll
+  for (int kk = 0; kk < kKS; ++kk) {
+    uint32_t a[4];
+    if (FP8) {
+      a[0] = pack_f16x2(s[2 * kk][0], s[2 * kk][1]);
+      a[1] = pack_f16x2(s[2 * kk][2], s[2 * kk][3]);
+      a[2] = pack_f16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      a[3] = pack_f16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+    } else {
+      a[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
+      a[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
+      a[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      a[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+    }
+    const int kv0 = wk0 + 16 * kk + 2 * c;   // rows kv0, kv0+1, kv0+8, kv0+9
+    const int krow[4] = {kv0, kv0 + 1, kv0 + 8, kv0 + 9};
+    if (FP8) {
+      uint32_t w[4][4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint4 t = lds128(swz128(vb, krow[q4], gq));
+        if (k0 + krow[q4] >= seq_len) t = make_uint4(0, 0, 0, 0);
+        w[q4][0] = t.x; w[q4][1] = t.y; w[q4][2] = t.z; w[q4][3] = t.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t x01 = prmt(w[0][i], w[1][i], 0x5140);
+        const uint32_t y01 = prmt(w[0][i], w[1][i], 0x7362);
+        const uint32_t x23 = prmt(w[2][i], w[3][i], 0x5140);
+        const uint32_t y23 = prmt(w[2][i], w[3][i], 0x7362);
+        mma_f16(o[4 * i + 0], a, e4m3x2_to_f16x2((uint16_t)(x01 & 0xFFFF)),
+                e4m3x2_to_f16x2((uint16_t)(x23 & 0xFFFF)));
+        mma_f16(o[4 * i + 1], a, e4m3x2_to_f16x2((uint16_t)(x01 >> 16)),
+                e4m3x2_to_f16x2((uint16_t)(x23 >> 16)));
+        mma_f16(o[4 * i + 2], a, e4m3x2_to_f16x2((uint16_t)(y01 & 0xFFFF)),
+                e4m3x2_to_f16x2((uint16_t)(y23 & 0xFFFF)));
+        mma_f16(o[4 * i + 3], a, e4m3x2_to_f16x2((uint16_t)(y01 >> 16)),
+                e4m3x2_to_f16x2((uint16_t)(y23 >> 16)));
+      }
+    } else {
+      uint32_t r[4][8];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint4 t0 = lds128(swz128(vb, krow[q4], gq));
+        uint4 t1 = lds128(swz128(vb + 16384u, krow[q4], gq));
+        if (k0 + krow[q4] >= seq_len) {
+          t0 = make_uint4(0, 0, 0, 0);
+          t1 = t0;
+        }
+        r[q4][0] = t0.x; r[q4][1] = t0.y; r[q4][2] = t0.z; r[q4][3] = t0.w;
+        r[q4][4] = t1.x; r[q4][5] = t1.y; r[q4][6] = t1.z; r[q4][7] = t1.w;
+      }
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const uint32_t sel = (nt & 1) ? 0x7632u : 0x5410u;
+        const uint32_t b0 = prmt(r[0][nt >> 1], r[1][nt >> 1], sel);
+        const uint32_t b1 = prmt(r[2][nt >> 1], r[3][nt >> 1], sel);
+        mma_bf16(o[nt], a, b0, b1);
+      }
+    }
+  }
+}
+
+template <bool FP8, bool GEN>
 __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* full,
                          uint64_t* empty, const int* stage_bad, uint32_t tmem, CombBars bars) {
   using C = Cfg<FP8>;
@@ -269,16 +451,24 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
     const RunInfo& ru = p.runs[x.run];
     int klo, khi;
     item_keys(p, x, klo, khi);
-    if (x.run != q_run || x.g != q_g || x.mt != q_mt) {
-      load_q<FP8, TREE>(p, ru, x, gq, c, qr, lim, anc, sc);
+    // The m-tile this warp works on, and its key sub-blocks in every stage
+    // chunk: a narrow item splits the chunk's 8 sub-blocks of kKeysPerWarp
+    // keys over the 8 warps; a wide item gives warps w and w + 4 m-tile
+    // 4 mt + (w & 3) and 4 sub-blocks each (the two halves of the chunk).
+    const bool wide = GEN && ru.wide;
+    const int sub0 = wide ? (warp >> 2) * 4 : warp;
+    Item xq = x;
+    if (wide) xq.mt = 4 * x.mt + (warp & 3);
+    if (x.run != q_run || x.g != q_g || xq.mt != q_mt) {
+      load_q<FP8, GEN>(p, ru, xq, gq, c, qr, lim, anc, sc);
       maxlim = __reduce_max_sync(0xffffffffu, max(lim[0], lim[1]));
-      if (TREE) {
+      if (GEN && p.anc) {
         const int mn = min(lim[0] >= 0 ? lim[0] : INT_MAX, lim[1] >= 0 ? lim[1] : INT_MAX);
         tree_low = (int)__reduce_min_sync(0xffffffffu, (unsigned)mn) - 63;
       }
       q_run = x.run;
       q_g = x.g;
-      q_mt = x.mt;
+      q_mt = xq.mt;
     }
 
     float m_run[2] = {-INFINITY, -INFINITY};
@@ -292,167 +482,19 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
       const uint32_t ph = (stage / kStages) & 1;
       if (!mbar_wait(&full[buf], ph, p.err_flag)) return;
       const uint32_t sb = sbase + (uint32_t)buf * kStageBytes;
-      const int wk0 = warp * C::kKeysPerWarp;
-      const int key_base = k0 + wk0;
-      if (!stage_bad[buf] && key_base <= maxlim) {
-        // ---- S = Q K^T over this warp's keys
-        float s[C::kNT][4];
-#pragma unroll
-        for (int nt = 0; nt < C::kNT; ++nt) {
-          s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-          const int kr = wk0 + nt * 8 + gq;
-          uint32_t kb[16];
-          if (FP8) {
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-              const uint4 w = lds128(swz128(sb, kr, 2 * c + ch));
-              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                kb[8 * ch + 2 * i] = e4m3x2_to_f16x2((uint16_t)(ws[i] & 0xFFFF));
-                kb[8 * ch + 2 * i + 1] = e4m3x2_to_f16x2((uint16_t)(ws[i] >> 16));
-              }
-            }
-          } else {
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-              const uint32_t base = sb + (ch >> 1) * 16384u;
-              const uint4 w = lds128(swz128(base, kr, 2 * c + (ch & 1)));
-              kb[4 * ch + 0] = w.x;
-              kb[4 * ch + 1] = w.y;
-              kb[4 * ch + 2] = w.z;
-              kb[4 * ch + 3] = w.w;
-            }
-          }
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t a[4] = {qr[0][2 * ks], qr[1][2 * ks], qr[0][2 * ks + 1],
-                                   qr[1][2 * ks + 1]};
-            if (FP8)
-              mma_f16(s[nt], a, kb[2 * ks], kb[2 * ks + 1]);
-            else
-              mma_bf16(s[nt], a, kb[2 * ks], kb[2 * ks + 1]);
-          }
-        }
-        // ---- scale, causal (or ancestor) mask, online softmax (rows gq,
-        // gq+8; a row's keys are spread over the 4 threads of a quad).  The
-        // running max is only moved when it grows by more than 2^8, so O is
-        // rarely rescaled.  Ancestor masks are only consulted where a key
-        // lies within 63 positions of some row of the warp.
-        const bool tree_zone = TREE && key_base + C::kKeysPerWarp > tree_low;
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int nt = 0; nt < C::kNT; ++nt) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int hr = j >> 1;
-            const int key = key_base + nt * 8 + 2 * c + (j & 1);
-            bool vis = key <= lim[hr];
-            if (tree_zone) {
-              const int dd = lim[hr] - key;
-              vis = vis && (dd > 63 || ((anc[hr] >> dd) & 1ull));
-            }
-            const float v = vis ? s[nt][j] * sc[hr] : -INFINITY;
-            s[nt][j] = v;
-            mx[hr] = fmaxf(mx[hr], v);
-          }
-        }
-        float alpha[2];
-        bool resc = false;
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
-          mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
-          alpha[hr] = 1.f;
-          if (mx[hr] > m_run[hr] + kRescaleThreshold) {
-            alpha[hr] = fast_exp2(m_run[hr] - mx[hr]);
-            l_run[hr] *= alpha[hr];
-            m_run[hr] = mx[hr];
-            resc = true;
-          }
-        }
-        if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll
-          for (int nt = 0; nt < 16; ++nt) {
-            o[nt][0] *= alpha[0];
-            o[nt][1] *= alpha[0];
-            o[nt][2] *= alpha[1];
-            o[nt][3] *= alpha[1];
-          }
-        }
-        const float base0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
-        const float base1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
-#pragma unroll
-        for (int nt = 0; nt < C::kNT; ++nt) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float e = fast_exp2(s[nt][j] - ((j >> 1) ? base1 : base0));
-            s[nt][j] = e;
-            l_run[j >> 1] += e;
-          }
-        }
-        // ---- O += P V
-        const uint32_t vb = sb + 32768u;
-#pragma unroll
-        for (int kk = 0; kk < C::kKS; ++kk) {
-          uint32_t a[4];
-          if (FP8) {
-            a[0] = pack_f16x2(s[2 * kk][0], s[2 * kk][1]);
-            a[1] = pack_f16x2(s[2 * kk][2], s[2 * kk][3]);
-            a[2] = pack_f16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-            a[3] = pack_f16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-          } else {
-            a[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-            a[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-            a[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-            a[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-          }
-          const int kv0 = wk0 + 16 * kk + 2 * c;   // rows kv0, kv0+1, kv0+8, kv0+9
-          const int krow[4] = {kv0, kv0 + 1, kv0 + 8, kv0 + 9};
-          if (FP8) {
-            uint32_t w[4][4];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 t = lds128(swz128(vb, krow[q4], gq));
-              if (k0 + krow[q4] >= ru.seq_len) t = make_uint4(0, 0, 0, 0);
-              w[q4][0] = t.x; w[q4][1] = t.y; w[q4][2] = t.z; w[q4][3] = t.w;
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t x01 = prmt(w[0][i], w[1][i], 0x5140);
-              const uint32_t y01 = prmt(w[0][i], w[1][i], 0x7362);
-              const uint32_t x23 = prmt(w[2][i], w[3][i], 0x5140);
-              const uint32_t y23 = prmt(w[2][i], w[3][i], 0x7362);
-              mma_f16(o[4 * i + 0], a, e4m3x2_to_f16x2((uint16_t)(x01 & 0xFFFF)),
-                      e4m3x2_to_f16x2((uint16_t)(x23 & 0xFFFF)));
-              mma_f16(o[4 * i + 1], a, e4m3x2_to_f16x2((uint16_t)(x01 >> 16)),
-                      e4m3x2_to_f16x2((uint16_t)(x23 >> 16)));
-              mma_f16(o[4 * i + 2], a, e4m3x2_to_f16x2((uint16_t)(y01 & 0xFFFF)),
-                      e4m3x2_to_f16x2((uint16_t)(y23 & 0xFFFF)));
-              mma_f16(o[4 * i + 3], a, e4m3x2_to_f16x2((uint16_t)(y01 >> 16)),
-                      e4m3x2_to_f16x2((uint16_t)(y23 >> 16)));
-            }
-          } else {
-            uint32_t r[4][8];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 t0 = lds128(swz128(vb, krow[q4], gq));
-              uint4 t1 = lds128(swz128(vb + 16384u, krow[q4], gq));
-              if (k0 + krow[q4] >= ru.seq_len) {
-                t0 = make_uint4(0, 0, 0, 0);
-                t1 = t0;
-              }
-              r[q4][0] = t0.x; r[q4][1] = t0.y; r[q4][2] = t0.z; r[q4][3] = t0.w;
-              r[q4][4] = t1.x; r[q4][5] = t1.y; r[q4][6] = t1.z; r[q4][7] = t1.w;
-            }
-#pragma unroll
-            for (int nt = 0; nt < 16; ++nt) {
-              const uint32_t sel = (nt & 1) ? 0x7632u : 0x5410u;
-              const uint32_t b0 = prmt(r[0][nt >> 1], r[1][nt >> 1], sel);
-              const uint32_t b1 = prmt(r[2][nt >> 1], r[3][nt >> 1], sel);
-              mma_bf16(o[nt], a, b0, b1);
-            }
-          }
+      if (!wide) {
+        const int wk0 = sub0 * C::kKeysPerWarp;
+        if (!stage_bad[buf] && k0 + wk0 <= maxlim)
+          attend_block<FP8, GEN, 1>(sb, wk0, k0, ru.seq_len, qr, lim, sc, anc, tree_low, gq, c,
+                                    m_run, l_run, o);
+      } else {
+        // a wide item: this warp's four sub-blocks as two blocks of two, for
+        // more independent work per step than four sequential sub-blocks
+        for (int bb = 0; bb < 2; ++bb) {
+          const int wk0 = (sub0 + 2 * bb) * C::kKeysPerWarp;
+          if (!stage_bad[buf] && k0 + wk0 <= maxlim)
+            attend_block<FP8, GEN, 2>(sb, wk0, k0, ru.seq_len, qr, lim, sc, anc, tree_low, gq, c,
+                                      m_run, l_run, o);
         }
       }
       __syncwarp();
@@ -504,7 +546,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
 // Each of pub, folded and done completes once per item (parity = item & 1);
 // a combiner waits for done of the previous item before publishing, so the
 // fold and (m, l) buffers are never overwritten while still being read.
-template <bool FP8>
+template <bool FP8, bool GEN>
 __device__ void combiner(const DecodeParams& p, uint32_t tmem, float4* fold, float* ml_buf,
                          CombBars bars) {
   const int warp = threadIdx.x >> 5;
@@ -530,7 +572,8 @@ __device__ void combiner(const DecodeParams& p, uint32_t tmem, float4* fold, flo
     umma::tmem_ld4(tB + 64, mlB);
     umma::tmem_ld_wait();
     if (rel > 0 && !mbar_wait(bars.done, par ^ 1u, p.err_flag)) return;
-    if (c == 0) {
+    const bool wide = GEN && ru.wide;
+    if (!wide && c == 0) {
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int row = gq + 8 * hr;
@@ -543,6 +586,76 @@ __device__ void combiner(const DecodeParams& p, uint32_t tmem, float4* fold, flo
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.pub);
     if (!mbar_wait(bars.pub, par, p.err_flag)) return;
+    if (wide) {
+      // A wide item: consumer warps q and q + 4 hold the only two states of
+      // m-tile 4 mt + q, so their fold is that m-tile's partial.  Same
+      // barriers as a narrow item (their phases count every item).
+      const int mtq = 4 * x.mt + q;
+      float Mw[2], Aw[2], Bw[2], Lw[2];
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const float mA = __uint_as_float(mlA[2 * hr]), lA = __uint_as_float(mlA[2 * hr + 1]);
+        const float mB = __uint_as_float(mlB[2 * hr]), lB = __uint_as_float(mlB[2 * hr + 1]);
+        Mw[hr] = fmaxf(mA, mB);
+        Aw[hr] = mA == -INFINITY ? 0.f : fast_exp2(mA - Mw[hr]);
+        Bw[hr] = mB == -INFINITY ? 0.f : fast_exp2(mB - Mw[hr]);
+        Lw[hr] = __fmaf_rn(Bw[hr], lB, __fmul_rn(Aw[hr], lA));
+      }
+      const float vs = FP8 ? __ldg(p.v_scale + x.g) : 1.f;
+      float* orow[2] = {nullptr, nullptr};
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int qv = mtq * 16 + gq + 8 * hr;
+        if (qv >= nq) continue;
+        const int r = qv / p.group;
+        const int h = x.g * p.group + (qv - r * p.group);
+        const size_t pslot = ((size_t)(ru.row0 + r) * p.hq + h) * p.max_splits + x.sigma;
+        orow[hr] = p.part_o + pslot * kHeadDim;
+        if (c == 0) {
+          p.part_ml[pslot * 2 + 0] = Mw[hr];
+          p.part_ml[pslot * 2 + 1] = Lw[hr];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t xa[16], xb[16];
+        umma::tmem_ld16(tA + 16 * k, xa);
+        umma::tmem_ld16(tB + 16 * k, xb);
+        umma::tmem_ld_wait();
+        float v[4][4];                       // [n-tile 4k + u][fragment element j]
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int i = 4 * u + j, hr = j >> 1;
+            v[u][j] = __fmaf_rn(Bw[hr], __uint_as_float(xb[i]),
+                                __fmul_rn(Aw[hr], __uint_as_float(xa[i]))) * vs;
+          }
+        }
+        // fragment element j = 2 hr + e of n-tiles 4k..4k+3 lies in four
+        // consecutive columns starting at out_col(4k, 2c + e)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          if (!orow[hr]) continue;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int j = 2 * hr + e;
+            *reinterpret_cast<float4*>(orow[hr] + out_col<FP8>(4 * k, 2 * c + e)) =
+                make_float4(v[0][j], v[1][j], v[2][j], v[3][j]);
+          }
+        }
+      }
+      umma::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars.tmem_free[b]);
+        mbar_arrive(bars.folded);
+      }
+      if (!mbar_wait(bars.folded, par, p.err_flag)) return;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.done);
+      continue;
+    }
     float M[2], aA[2], aB[2];
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
@@ -634,7 +747,7 @@ __device__ void combiner(const DecodeParams& p, uint32_t tmem, float4* fold, flo
   }
 }
 
-template <bool FP8, bool TREE>
+template <bool FP8, bool GEN>
 __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
     const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -682,10 +795,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
   wait_prior_grid();
   if (warp < kCombineWarp0) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsConsumer));
-    consumer<FP8, TREE>(p, stage_mem, full, empty, stage_bad, tmem, cb);
+    consumer<FP8, GEN>(p, stage_mem, full, empty, stage_bad, tmem, cb);
   } else if (warp < kProducerWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCombine));
-    combiner<FP8>(p, tmem, fold, ml_buf, cb);
+    combiner<FP8, GEN>(p, tmem, fold, ml_buf, cb);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
     if (warp == kProducerWarp) producer<FP8>(p, stage_mem, full, empty, stage_bad);
@@ -755,24 +868,24 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
   if (p.lse && lane == 0) p.lse[(size_t)row * p.hq + h] = (M + log2f(L)) * 0.6931471805599453f;
 }
 
-template <bool FP8, bool TREE>
+template <bool FP8, bool GEN>
 cudaError_t launch_partial(const DecodeParams& p, int grid, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
     // The register split only works if the block launches with at least the
     // registers it hands out; otherwise setmaxnreg.inc would wait forever.
     cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, decode_partial_kernel<FP8, TREE>);
+    cudaError_t e = cudaFuncGetAttributes(&attr, decode_partial_kernel<FP8, GEN>);
     if (e != cudaSuccess) return e;
     if (attr.numRegs * kThreads < 128 * (2 * kRegsConsumer + kRegsCombine + kRegsProducer))
       return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(decode_partial_kernel<FP8, TREE>,
+    e = cudaFuncSetAttribute(decode_partial_kernel<FP8, GEN>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   cudaError_t e =
-      launch_pdl(decode_partial_kernel<FP8, TREE>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
+      launch_pdl(decode_partial_kernel<FP8, GEN>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -781,9 +894,11 @@ cudaError_t launch_partial(const DecodeParams& p, int grid, cudaStream_t s) {
 
 cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cudaStream_t s) {
   if (grid <= 0 || p.n_items == 0) return cudaSuccess;
-  // Rows with ancestor masks take their own instantiation, so causal calls
-  // keep the causal kernel's code.
-  if (p.anc)
+  // Rows with ancestor masks, or runs of wide items, take the general
+  // instantiation, so the plain causal calls keep their own kernel's code.
+  bool gen = p.anc != nullptr;
+  for (int r = 0; r < p.nruns; ++r) gen = gen || p.runs[r].wide;
+  if (gen)
     return fp8 ? launch_partial<true, true>(p, grid, s) : launch_partial<false, true>(p, grid, s);
   return fp8 ? launch_partial<true, false>(p, grid, s) : launch_partial<false, false>(p, grid, s);
 }

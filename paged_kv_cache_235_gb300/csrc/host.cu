@@ -276,15 +276,16 @@ void fill_run(RunInfo& ri, const tfpa_seg& g, int src, int row0, int nrows, int 
   ri.pps = tfpa_pages_per_split(g.seq_len);
   ri.item0 = 0;
   ri.slab_cap = g.page_table ? 0 : g.slab_cap;
-  ri.pad_ = 0;
+  ri.wide = 0;
 }
 
-// Key stages of decode work item (m-tile mt, split sigma) of a run: its
-// split's keys, cut at the stream's end and at the m-tile's last position
-// (the kernel's item key range, in units of the kernel's chunk).
+// Key stages of decode work item (m-tile mt, or m-tile group mt of a wide
+// run, split sigma) of a run: its split's keys, cut at the stream's end and
+// at the last position of the item's rows (the kernel's item key range, in
+// units of the kernel's chunk).
 int item_stages(const RunInfo& ri, int G, int mt, int sigma, int chunk) {
   const int nq = ri.nrows * G;
-  const int last_qv = std::min(mt * 16 + 15, nq - 1);
+  const int last_qv = std::min(ri.wide ? 64 * mt + 63 : 16 * mt + 15, nq - 1);
   const int maxpos = ri.pos0 + last_qv / G;
   const int klo = sigma * ri.pps * kPage;
   const int khi = std::min(std::min(klo + ri.pps * kPage, ri.seq_len), maxpos + 1);
@@ -302,9 +303,12 @@ void plan_cta_ranges(DecodeParams& p, int nr, int G, bool fp8, int grid) {
     for (int r = 0; r < nr; ++r) {
       const RunInfo& ri = p.runs[r];
       const int mtiles = (ri.nrows * G + 15) / 16;
+      const int mgroups = ri.wide ? (mtiles + 3) / 4 : mtiles;
+      const int64_t per_stage = ri.wide ? 2 : 1;    // a wide item computes 4 m-tiles a stage
       for (int g = 0; g < p.hkv; ++g)
-        for (int mt = 0; mt < mtiles; ++mt)
-          for (int sg = 0; sg < ri.nsplit; ++sg) fn(item_stages(ri, G, mt, sg, chunk) + kItemCost);
+        for (int mt = 0; mt < mgroups; ++mt)
+          for (int sg = 0; sg < ri.nsplit; ++sg)
+            fn(per_stage * item_stages(ri, G, mt, sg, chunk) + kItemCost);
     }
   };
   int64_t total = 0;
@@ -368,7 +372,14 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
       RunInfo& info = p.runs[nr];
       fill_run(info, segs[r.seg], src, nrows, take, r.pos0 + taken);
       info.item0 = items;
-      items += c->hkv * ((take * G + 15) / 16) * info.nsplit;
+      // Runs of four or more m-tiles (16 query vectors each) take wide items:
+      // four m-tiles share each K/V stage instead of reading it once each.
+      // Decided on the call's whole run, so every slice of it computes its
+      // rows with the same arithmetic (slices give the same bytes as one
+      // launch).
+      const int mtiles = (take * G + 15) / 16;
+      info.wide = (r.nrows * G + 15) / 16 >= 4 ? 1 : 0;
+      items += c->hkv * (info.wide ? (mtiles + 3) / 4 : mtiles) * info.nsplit;
       mp.runs[nr] = MergeRun{nrows, take, info.nsplit, 0};
       ++nr;
       nrows += take;
