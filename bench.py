@@ -39,7 +39,7 @@ METRIC = "paged decode KV GB/s (% HBM peak); prompt-chunk attn TFLOP/s (% TC pea
 # from ncu (dram__bytes_read.sum + dram__bytes_write.sum, see
 # profiles/decode_partial_batched_decode.md), valid only while the kernel's
 # sources hash to the value it was taken on.
-DECODE_TRAFFIC = {"bytes": 268_595_456 + 4_658_688, "sources_sha256_16": "6ff7a4d271fc881d"}
+DECODE_TRAFFIC = {"bytes": 268_613_376 + 4_083_968, "sources_sha256_16": "09fff6a37ef28b0b"}
 DECODE_SOURCES = ["paged_kv_cache_235_gb300/csrc/decode.cu",
                   "paged_kv_cache_235_gb300/csrc/common.cuh",
                   "paged_kv_cache_235_gb300/csrc/params.h",
@@ -627,14 +627,16 @@ def main():
                                      "restore": gbs["restore"] / gbs["h2d"]},
             "note": "the reference is a plain runtime copy of the same byte count between a "
                     "contiguous device buffer and the same pinned buffer"}
-        w7 = wl.tree_verify()
-        ms7 = time_tree_calls(w7, torch, B, 20)
-        kv7, qo7 = kv_bytes(w7)
-        extra["tree_verify"] = {
-            "workload": "8 streams x 65,536 positions, fp8 e4m3, a seeded 16-node draft tree "
-                        "per stream (one row per node, ancestor masks); tfpa_decode_tree per call",
-            "ms_per_call": ms7, "kv_gbs": (kv7 + qo7) / (ms7 / 1e3) / 1e9,
-            "frac_of_measured_hbm": (kv7 + qo7) / (ms7 / 1e3) / 1e9 / pk["hbm_gbs"]}
+        for kvd in ("fp8", "bf16"):
+            w7 = wl.tree_verify(kv_dtype=kvd)
+            ms7 = time_tree_calls(w7, torch, B, 20)
+            kv7, qo7 = kv_bytes(w7)
+            extra["tree_verify" + ("" if kvd == "fp8" else "_bf16")] = {
+                "workload": f"8 streams x 65,536 positions, {kvd} KV, a seeded 16-node draft "
+                            "tree per stream (one row per node, ancestor masks); "
+                            "tfpa_decode_tree per call",
+                "ms_per_call": ms7, "kv_gbs": (kv7 + qo7) / (ms7 / 1e3) / 1e9,
+                "frac_of_measured_hbm": (kv7 + qo7) / (ms7 / 1e3) / 1e9 / pk["hbm_gbs"]}
     value = world * (kv + qo) / (step_ms / 1e3) / 1e9
     achieved = (kv + qo) / (partial_ms / 1e3) / 1e9
     extra["fp8_verify"] = {
