@@ -288,12 +288,13 @@ int tfpa_prefill(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
  * launch is reported; with dry_run != 0 nothing is enqueued and no CUDA call
  * is made, so the slicing logic runs on a machine without a GPU. */
 typedef struct {
-  int32_t kind;          /* 0 write_kv, 1 decode partial, 2 merge, 3 prefill, 4 keep */
+  int32_t kind;          /* 0 write_kv, 1 decode partial, 2 merge, 3 prefill, 4 keep,
+                            5 stage pages, 6 save, 7 restore */
   int32_t row0;          /* first row of the call this launch covers */
   int32_t rows;          /* rows it covers */
   int32_t runs;          /* row groups (segment, consecutive positions) */
   int32_t items;         /* work items (decode: tiles of (kv head, m-tile, split)) */
-  int32_t grid;          /* CTAs */
+  int32_t grid;          /* CTAs (prefill: two per tile, in clusters of two) */
   int64_t q_offset;      /* element offset of the q pointer it got, from the call's q */
   int64_t out_offset;    /* element offset of the out pointer, from the call's out */
 } tfpa_launch_record;

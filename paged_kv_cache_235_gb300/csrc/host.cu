@@ -793,10 +793,11 @@ extern "C" int tfpa_prefill(const tfpa_cache* c, const tfpa_seg* segs, int32_t n
     p.num_pages = c->num_pages;
     p.rows = nrows;
     p.scale_log2 = scale * 1.4426950408889634f;
-    const int grid = tiles;   // one CTA per tile, heaviest tiles first
-    record(3, base, nrows, nr, tiles, grid, (int64_t)base * hd, (int64_t)base * hd);
+    // A cluster of two CTAs per tile (each takes half of the tile's key
+    // tiles), heaviest tiles first.
+    record(3, base, nrows, nr, tiles, 2 * tiles, (int64_t)base * hd, (int64_t)base * hd);
     if (!dry_run())
-      if ((e = to_err(launch_prefill(p, fp8, grid, stream)))) return e;
+      if ((e = to_err(launch_prefill(p, fp8, tiles, stream)))) return e;
   }
   return TFPA_OK;
 }

@@ -3,10 +3,18 @@
 // 256, a key tile's page looked up once; PR #1373, "What changes": the
 // prompt tiles read pages through the page table, else the slab).
 //
-// One CTA per work tile = (run, kv head g, pair of query heads of g, 128
-// rows).  One online-softmax pass over key tiles of 128 keys aligned to
-// absolute positions, so a row's result never depends on how the rows are
-// sliced into launches or tiles.
+// One cluster of two CTAs per work tile = (run, kv head g, pair of query
+// heads of g, 128 rows).  The tile's key tiles (128 keys, aligned to
+// absolute positions) are cut at the midpoint: CTA 0 of the cluster takes
+// the first half, CTA 1 the second (which holds the diagonal).  Each runs
+// one online-softmax pass over its half.  Once CTA 0's MMAs are done with its
+// K and V rings it tells CTA 1, which stores its (m, l, O) there through
+// distributed shared memory; CTA 0 merges it with its own.  The cut depends
+// only on the tile's key
+// count, so a row's result never depends on how the rows are sliced into
+// launches or tiles.  Two CTAs per tile halve the unit of work, so that the
+// tiles of a prompt chunk fill the SMs' last wave (1,024 half tiles make
+// 6.7 waves on 152 SMs where 512 whole tiles made 3.4).
 //   warp 0      TMA producer: Q of both heads once, then K and V tiles into
 //               2-stage rings (128B swizzle).  Each 128-key tile lies inside
 //               one 256-position page: one page lookup per key tile.
@@ -15,19 +23,23 @@
 //               V MN-major from shared memory).  The two heads ping-pong:
 //               S_A(j+1) is issued right after PV_A(j), so head A's softmax
 //               overlaps head B's MMAs and the other way round.
-//   warps 2-3   (e4m3 caches only) converters: TMA lands e4m3 K/V tiles in
-//               a staging buffer; these warps write the exact f16 operand
-//               tiles (and zero V rows past the stream's end).
 //   warps 4-7   softmax of head A, warps 8-11 of head B: one thread per row
 //               (TMEM lane), causal mask on the diagonal tiles, online
 //               max/sum, P written back over S as bf16 (f16 for e4m3
 //               caches), O rescaled in TMEM only when the running max grows
 //               by more than 2^8.
+//   warps 12-15 (e4m3 caches only) converters: TMA lands e4m3 K/V tiles in
+//               a staging buffer; these warps write the exact f16 operand
+//               tiles (and zero V rows past the stream's end).
 // With an e4m3 cache the MMAs run in f16: each softmax thread first turns its
 // Q row into f16 scaled by a power of two (exact for every element within
 // 2^28 of the row's largest), and the K and V scales are applied to the
 // scores and to the output.
 // TMEM (512 columns): S_A [0,128) O_A [128,256) S_B [256,384) O_B [384,512).
+// CTA 1's partial lands in CTA 0's shared memory once CTA 0's MMAs are done:
+// O (float32 [2 heads][128 rows][128], 16-byte chunks permuted by row against
+// bank conflicts) over the K and V rings, (m, l) over the Q tiles.
+#include "cluster.cuh"
 #include "common.cuh"
 #include "params.h"
 #include "tcgen05.cuh"
@@ -61,6 +73,31 @@ constexpr int kRegsHigh = 200;     // warps 4-11: softmax
 constexpr int kRegsConv = 56;      // warps 12-15: converters
 static_assert(128 * (kRegsLow + 2 * kRegsHigh + kRegsConv) <= 512 * 128, "register split");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+// One pair of exponentials in kPolyPeriod is computed on the FMA pipe
+// (exp2_poly) instead of the MUFU unit; 0: none.
+constexpr int kPolyPeriod = 0;
+
+// 2^x for a pair on the FMA pipe (the offload of part of the softmax's
+// exponentials from the MUFU unit described for Blackwell attention in the
+// FlashAttention-4 work): x is rounded to the nearest integer n by adding
+// and subtracting 1.5 * 2^23, 2^(x - n) on [-1/2, 1/2] is a cubic fitted
+// here for least maximum relative error (7.5e-5, below a bf16 or f16
+// rounding of P), and n is added into the exponent field.  x is first
+// clamped to -125, so the exponent stays normal (2^-125 for smaller x, below
+// anything a row sum of at least 1 can see).
+__device__ __forceinline__ f2 exp2_poly(f2 x) {
+  constexpr float kShift = 12582912.f;          // 1.5 * 2^23
+  x.x = fmaxf(x.x, -125.f);
+  x.y = fmaxf(x.y, -125.f);
+  const f2 t = fadd2(x, {kShift, kShift});      // low mantissa bits: round(x)
+  const f2 n = fadd2(t, {-kShift, -kShift});
+  const f2 f = ffma2(n, {-1.f, -1.f}, x);       // x - n, exact
+  f2 p = ffma2({0.0551716685f, 0.0551716685f}, f, {0.2426111251f, 0.2426111251f});
+  p = ffma2(p, f, {0.6932609677f, 0.6932609677f});
+  p = ffma2(p, f, {0.9999280572f, 0.9999280572f});
+  return {__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
+          __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23))};
+}
 
 __device__ __forceinline__ uint32_t col_s(int hh) { return hh ? 256u : 0u; }
 __device__ __forceinline__ uint32_t col_o(int hh) { return hh ? 384u : 128u; }
@@ -80,6 +117,8 @@ struct Bars {
   uint64_t* p_ready;     // [2] per head: P in TMEM, O corrected
   uint64_t* o_final;
   uint64_t* drain;
+  uint64_t* peer_ready;  // CTA 0: CTA 1's softmax threads stored their partial here
+  uint64_t* dst_free;    // CTA 1: CTA 0's MMAs are done with its rings
   uint32_t* tmem_slot;
   volatile int* abort;
 };
@@ -111,17 +150,22 @@ __device__ __forceinline__ Tile tile_of(const PrefillParams& p, int i) {
 struct TileGeom {
   int row_lo;      // first row of the tile, relative to the run
   int nrows;       // valid rows in the tile
-  int kend;        // keys [0, kend) are read
-  int nkt;         // key tiles
+  int kend;        // the tile's rows see keys [0, kend)
+  int kt0, nkt;    // this CTA's key tiles: kt0 .. kt0 + nkt - 1
 };
 
-__device__ __forceinline__ TileGeom geom_of(const RunInfo& ru, const Tile& x) {
+// Key tiles [0, n / 2) go to CTA 0 of the cluster, [n / 2, n) to CTA 1
+// (CTA 0 has none when n = 1).
+__device__ __forceinline__ TileGeom geom_of(const RunInfo& ru, const Tile& x, uint32_t rank) {
   TileGeom gm;
   gm.row_lo = x.t * kTileRows;
   gm.nrows = min(kTileRows, ru.nrows - gm.row_lo);
   const int maxpos = ru.pos0 + gm.row_lo + gm.nrows - 1;
   gm.kend = min(ru.seq_len, maxpos + 1);
-  gm.nkt = (gm.kend + kTileKeys - 1) / kTileKeys;
+  const int n = (gm.kend + kTileKeys - 1) / kTileKeys;
+  const int mid = n >> 1;
+  gm.kt0 = rank ? mid : 0;
+  gm.nkt = rank ? n - mid : mid;
   return gm;
 }
 
@@ -130,16 +174,18 @@ __device__ __forceinline__ TileGeom geom_of(const RunInfo& ru, const Tile& x) {
 struct PageCheck {
   const int32_t* pt;
   int npages, num_pages, next_pid;
-  bool cur_bad;
-  __device__ __forceinline__ PageCheck(const PrefillParams& p, const RunInfo& ru, int kend)
-      : pt(ru.page_table), npages((kend + kPage - 1) / kPage), num_pages(p.num_pages),
-        next_pid(0), cur_bad(false) {
-    if (pt) next_pid = __ldg(pt);
+  bool cur_bad, first;
+  __device__ __forceinline__ PageCheck(const PrefillParams& p, const RunInfo& ru,
+                                       const TileGeom& gm)
+      : pt(ru.page_table), npages((gm.kend + kPage - 1) / kPage), num_pages(p.num_pages),
+        next_pid(0), cur_bad(false), first(true) {
+    if (pt && gm.nkt > 0) next_pid = __ldg(pt + (gm.kt0 >> 1));
   }
-  // Call for j = 0, 1, 2, ... in order; true if tile j's page is bad.
+  // Call for j = kt0, kt0 + 1, ... in order; true if tile j's page is bad.
   __device__ __forceinline__ bool bad(int j) {
     if (!pt) return false;
-    if ((j & 1) == 0) {
+    if ((j & 1) == 0 || first) {
+      first = false;
       const int page = j >> 1;
       cur_bad = (unsigned)next_pid >= (unsigned)num_pages;
       if (page + 1 < npages) next_pid = __ldg(pt + page + 1);
@@ -162,6 +208,7 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
   const CUtensorMap* mk = &p.maps[ru.src].k;
   const CUtensorMap* mv = &p.maps[ru.src].v;
   const int h0 = x.g * p.group + 2 * x.hp;
+  if (gm.nkt == 0) return;
   mbar_arrive_expect_tx(b.q_full, 65536);
   for (int hh = 0; hh < 2; ++hh)
     for (int rg = 0; rg < 2; ++rg)
@@ -169,10 +216,10 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
                   ru.row0 + gm.row_lo, b.q_full);
   int cached_page = -1, cached_pid = 0;
   int issued_k = 0, issued_v = 0;
-  for (int j = 0; j < gm.nkt; ++j) {
-    const int s = j & 1;
-    const uint32_t ph = (j >> 1) & 1;
-    const int kt = j * kTileKeys;
+  for (int jj = 0; jj < gm.nkt; ++jj) {     // jj counts this CTA's tiles
+    const int s = jj & 1;
+    const uint32_t ph = (jj >> 1) & 1;
+    const int kt = (gm.kt0 + jj) * kTileKeys;
     int y;
     if (ru.page_table) {
       const int page = kt >> 8;
@@ -190,25 +237,25 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
     }
     if (FP8) {
       // One staging tile each for K and V; the converters free them.
-      if (!mbar_wait_or_abort(b.k8_empty, (j & 1) ^ 1, p.err_flag, b.abort)) break;
+      if (!mbar_wait_or_abort(b.k8_empty, (jj & 1) ^ 1, p.err_flag, b.abort)) break;
       mbar_arrive_expect_tx(b.k8_full, 16384);
       tma_load_2d(smem + kOffK8, mk, 0, y, b.k8_full);
-      issued_k = j + 1;
-      if (!mbar_wait_or_abort(b.v8_empty, (j & 1) ^ 1, p.err_flag, b.abort)) break;
+      issued_k = jj + 1;
+      if (!mbar_wait_or_abort(b.v8_empty, (jj & 1) ^ 1, p.err_flag, b.abort)) break;
       mbar_arrive_expect_tx(b.v8_full, 16384);
       tma_load_2d(smem + kOffV8, mv, 0, y, b.v8_full);
-      issued_v = j + 1;
+      issued_v = jj + 1;
     } else {
       if (!mbar_wait_or_abort(&b.k_empty[s], ph ^ 1, p.err_flag, b.abort)) break;
       mbar_arrive_expect_tx(&b.k_full[s], 32768);
       tma_load_2d(smem + kOffK + s * 32768, mk, 0, y, &b.k_full[s]);
       tma_load_2d(smem + kOffK + s * 32768 + 16384, mk, 64, y, &b.k_full[s]);
-      issued_k = j + 1;
+      issued_k = jj + 1;
       if (!mbar_wait_or_abort(&b.v_empty[s], ph ^ 1, p.err_flag, b.abort)) break;
       mbar_arrive_expect_tx(&b.v_full[s], 32768);
       tma_load_2d(smem + kOffV + s * 32768, mv, 0, y, &b.v_full[s]);
       tma_load_2d(smem + kOffV + s * 32768 + 16384, mv, 64, y, &b.v_full[s]);
-      issued_v = j + 1;
+      issued_v = jj + 1;
     }
   }
   if (*b.abort) {
@@ -270,12 +317,13 @@ __device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileG
                           uint8_t* smem, const Bars& b) {
   const int t = threadIdx.x - kConvWarp0 * 32;   // 0..127
   const int lane = threadIdx.x & 31;
-  PageCheck pc(p, ru, gm.kend);
-  for (int j = 0; j < gm.nkt; ++j) {
+  PageCheck pc(p, ru, gm);
+  for (int jj = 0; jj < gm.nkt; ++jj) {
+    const int j = gm.kt0 + jj;
     const int z0 = v_zero_from(ru, j, pc.bad(j));
-    const int s = j & 1;
-    const uint32_t ph = (j >> 1) & 1;
-    if (!mbar_wait_or_abort(b.k8_full, j & 1, p.err_flag, b.abort)) return;
+    const int s = jj & 1;
+    const uint32_t ph = (jj >> 1) & 1;
+    if (!mbar_wait_or_abort(b.k8_full, jj & 1, p.err_flag, b.abort)) return;
     if (!mbar_wait_or_abort(&b.k_empty[s], ph ^ 1, p.err_flag, b.abort)) return;
     convert_tile(smem + kOffK8, smem + kOffK + s * 32768, kTileKeys, t);
     fence_proxy_async_smem();
@@ -284,7 +332,7 @@ __device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileG
       mbar_arrive(b.k8_empty);
       mbar_arrive(&b.k_full[s]);
     }
-    if (!mbar_wait_or_abort(b.v8_full, j & 1, p.err_flag, b.abort)) return;
+    if (!mbar_wait_or_abort(b.v8_full, jj & 1, p.err_flag, b.abort)) return;
     if (!mbar_wait_or_abort(&b.v_empty[s], ph ^ 1, p.err_flag, b.abort)) return;
     convert_tile(smem + kOffV8, smem + kOffV + s * 32768, z0, t);
     fence_proxy_async_smem();
@@ -325,6 +373,11 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
     }
   };
 
+  if (gm.nkt == 0) {                  // no keys in this half: nothing to wait for
+    if (leader) mbar_arrive(b.o_final);
+    __syncwarp();
+    return;
+  }
   bool ok = mbar_wait_or_abort(b.q_ready, 0, p.err_flag, b.abort) &&
             mbar_wait_or_abort(&b.k_full[0], 0, p.err_flag, b.abort);
   if (ok) {
@@ -338,23 +391,24 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
     }
     __syncwarp();
   }
-  PageCheck pc(p, ru, gm.kend);
-  for (int j = 0; ok && j < gm.nkt; ++j) {
+  PageCheck pc(p, ru, gm);
+  for (int jj = 0; ok && jj < gm.nkt; ++jj) {
+    const int j = gm.kt0 + jj;
     const bool page_bad = pc.bad(j);
-    const int s = j & 1;
-    const uint32_t ph = (j >> 1) & 1;
-    const int s1 = (j + 1) & 1;
-    const uint32_t ph1 = ((j + 1) >> 1) & 1;
-    const bool more = j + 1 < gm.nkt;
+    const int s = jj & 1;
+    const uint32_t ph = (jj >> 1) & 1;
+    const int s1 = (jj + 1) & 1;
+    const uint32_t ph1 = ((jj + 1) >> 1) & 1;
+    const bool more = jj + 1 < gm.nkt;
     if (!(ok = mbar_wait_or_abort(&b.v_full[s], ph, p.err_flag, b.abort))) break;
     if (!FP8) {   // the e4m3 converters zero these rows themselves
       const int z0 = v_zero_from(ru, j, page_bad);
       if (z0 < kTileKeys) zero_v_rows(smem + kOffV + s * 32768, z0, lane);
     }
     // head A
-    if (!(ok = mbar_wait_or_abort(&b.p_ready[0], j & 1, p.err_flag, b.abort))) break;
+    if (!(ok = mbar_wait_or_abort(&b.p_ready[0], jj & 1, p.err_flag, b.abort))) break;
     umma::fence_after_sync();
-    if (leader) issue_pv(0, s, j > 0);
+    if (leader) issue_pv(0, s, jj > 0);
     if (more) {
       if (!(ok = mbar_wait_or_abort(&b.k_full[s1], ph1, p.err_flag, b.abort))) break;
       umma::fence_after_sync();
@@ -364,10 +418,10 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
       }
     }
     // head B
-    if (!(ok = mbar_wait_or_abort(&b.p_ready[1], j & 1, p.err_flag, b.abort))) break;
+    if (!(ok = mbar_wait_or_abort(&b.p_ready[1], jj & 1, p.err_flag, b.abort))) break;
     umma::fence_after_sync();
     if (leader) {
-      issue_pv(1, s, j > 0);
+      issue_pv(1, s, jj > 0);
       if (more) {
         issue_s(1, s1);
         umma::commit(&b.s_full[1]);
@@ -424,10 +478,22 @@ __device__ __forceinline__ float q_row_to_f16(uint8_t* qtile, int r) {
   return __int_as_float((127 - 14 + ex) << 23);
 }
 
+// Offsets of CTA 1's partial for (head hh, row r) in CTA 0's shared memory:
+// O over the K/V rings, (m, l) over the Q tiles.
+__device__ __forceinline__ uint32_t part_o_row(uint32_t smem_base, int hh, int r) {
+  return smem_base + kOffK + hh * 65536 + r * 512;
+}
+__device__ __forceinline__ uint32_t part_o_chunk(int r, int c) {   // c: 16-byte chunk 0..31
+  return (uint32_t)((c ^ (r & 7)) * 16);
+}
+__device__ __forceinline__ uint32_t part_ml(uint32_t smem_base, int hh, int r) {
+  return smem_base + kOffQ + (hh * kTileRows + r) * 8;
+}
+
 template <bool FP8>
 __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Tile& x,
-                             const TileGeom& gm, int hh, uint8_t* smem, uint32_t tmem,
-                             const Bars& b) {
+                             const TileGeom& gm, uint32_t rank, int hh, uint8_t* smem,
+                             uint32_t tmem, const Bars& b) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = 32 * (warp & 3) + lane;                 // row of the tile = TMEM lane
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
@@ -436,20 +502,24 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
   const bool valid = r < gm.nrows;
   const int pos = ru.pos0 + gm.row_lo + (valid ? r : 0);
   float sl2 = p.scale_log2;
-  if (FP8) {
-    if (!mbar_wait_or_abort(b.q_full, 0, p.err_flag, b.abort)) return;
-    const float down = q_row_to_f16(smem + kOffQ + hh * 32768, r);
-    sl2 = p.scale_log2 * down * __ldg(p.k_scale + x.g);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(b.q_ready);
+  bool ok = true;
+  if (FP8 && gm.nkt > 0) {
+    ok = mbar_wait_or_abort(b.q_full, 0, p.err_flag, b.abort);
+    if (ok) {
+      const float down = q_row_to_f16(smem + kOffQ + hh * 32768, r);
+      sl2 = p.scale_log2 * down * __ldg(p.k_scale + x.g);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b.q_ready);
+    }
   }
   float m_run = -INFINITY, l = 0.f;
-  PageCheck pc(p, ru, gm.kend);
+  PageCheck pc(p, ru, gm);
 
-  for (int j = 0; j < gm.nkt; ++j) {
+  for (int jj = 0; ok && jj < gm.nkt; ++jj) {
+    const int j = gm.kt0 + jj;
     const bool page_bad = pc.bad(j);
-    if (!mbar_wait_or_abort(&b.s_full[hh], j & 1, p.err_flag, b.abort)) return;
+    if (!(ok = mbar_wait_or_abort(&b.s_full[hh], jj & 1, p.err_flag, b.abort))) break;
     umma::fence_after_sync();
     const int kt = j * kTileKeys;
     const int lim = page_bad ? -1 : pos - kt;            // key kt+i visible iff i <= lim
@@ -490,7 +560,11 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
       const int i0 = 2 * k;
       f2 t = ffma2({__uint_as_float(sv[i0 >> 5][i0 & 31]),
                     __uint_as_float(sv[(i0 + 1) >> 5][(i0 + 1) & 31])}, sc2, nb2);
-      f2 e = {fast_exp2(t.x), fast_exp2(t.y)};
+      f2 e;
+      if (kPolyPeriod > 0 && k % kPolyPeriod == kPolyPeriod - 1)
+        e = exp2_poly(t);
+      else
+        e = {fast_exp2(t.x), fast_exp2(t.y)};
       if (!full_tile) {
         e.x = i0 <= lim ? e.x : 0.f;
         e.y = i0 + 1 <= lim ? e.y : 0.f;
@@ -501,7 +575,7 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
     const float rs = acc.x + acc.y;
     umma::tmem_st32(tS, sv[0]);
     umma::tmem_st32(tS + 32, sv[1]);
-    if (j > 0 && __any_sync(0xffffffffu, resc)) {      // O *= alpha in TMEM
+    if (jj > 0 && __any_sync(0xffffffffu, resc)) {     // O *= alpha in TMEM
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
@@ -518,33 +592,86 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
     __syncwarp();
     if (lane == 0) mbar_arrive(&b.p_ready[hh]);
   }
-  if (!mbar_wait_or_abort(b.o_final, 0, p.err_flag, b.abort)) return;
-  umma::fence_after_sync();
+  if (ok) ok = mbar_wait_or_abort(b.o_final, 0, p.err_flag, b.abort);
+  if (ok) umma::fence_after_sync();
+  const uint32_t sbase = smem_u32(smem);
+
+  if (rank == 1) {
+    // Store (m, l, O) into CTA 0 once its rings are free; arrive on its
+    // barrier whatever happened, so that it never waits out the time limit
+    // on this CTA's account.
+    const bool free = mbar_wait_cluster(b.dst_free, 0, p.err_flag);
+    if (ok && free) {
+      const uint32_t orow = mapa_shared(part_o_row(sbase, hh, r), 0);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        umma::tmem_ld32(tO + 32 * c, o);
+        umma::tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          st_cluster128(orow + part_o_chunk(r, 8 * c + q), o[4 * q], o[4 * q + 1], o[4 * q + 2],
+                        o[4 * q + 3]);
+      }
+      st_cluster_f2(mapa_shared(part_ml(sbase, hh, r), 0), m_run, l);
+    }
+    mbar_arrive_remote(mapa_shared(smem_u32(b.peer_ready), 0));
+    return;
+  }
+
+  // CTA 0: its MMAs are done (or it gave up), so CTA 1 may store into the
+  // rings.  Then merge CTA 1's half into this one, normalise, write.
+  if (threadIdx.x == 128) mbar_arrive_remote(mapa_shared(smem_u32(b.dst_free), 1));
+  const bool peer = mbar_wait_cluster(b.peer_ready, 0, p.err_flag);
+  if (!ok || !peer) return;
+  float2 ml1;
+  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(ml1.x), "=f"(ml1.y)
+               : "r"(part_ml(sbase, hh, r)) : "memory");
+  const float m_all = fmaxf(m_run, ml1.x);
+  const float a0 = m_run == -INFINITY ? 0.f : fast_exp2(m_run - m_all);
+  const float a1 = ml1.x == -INFINITY ? 0.f : fast_exp2(ml1.x - m_all);
+  const float l_all = __fmaf_rn(l, a0, __fmul_rn(ml1.y, a1));
+  const float inv = (l_all > 0.f ? 1.f / l_all : 0.f) * (FP8 ? __ldg(p.v_scale + x.g) : 1.f);
+  const float c0 = a0 * inv, c1 = a1 * inv;
   const int h = x.g * p.group + 2 * x.hp + hh;
   const bool write = valid && (2 * x.hp + hh) < p.group;
-  const float inv = (l > 0.f ? 1.f / l : 0.f) * (FP8 ? __ldg(p.v_scale + x.g) : 1.f);
   uint4* dst = reinterpret_cast<uint4*>(
       p.out + ((size_t)(ru.row0 + gm.row_lo + r) * p.hq + h) * kHeadDim);
+  const uint32_t prow = part_o_row(sbase, hh, r);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t o[32];
-    umma::tmem_ld32(tO + 32 * c, o);
-    umma::tmem_ld_wait();
+    if (gm.nkt > 0) {
+      umma::tmem_ld32(tO + 32 * c, o);
+      umma::tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = 0u;
+    }
+    float f[32];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint4 w = lds128(prow + part_o_chunk(r, 8 * c + q));
+      f[4 * q + 0] = __fmaf_rn(__uint_as_float(o[4 * q + 0]), c0, __fmul_rn(__uint_as_float(w.x), c1));
+      f[4 * q + 1] = __fmaf_rn(__uint_as_float(o[4 * q + 1]), c0, __fmul_rn(__uint_as_float(w.y), c1));
+      f[4 * q + 2] = __fmaf_rn(__uint_as_float(o[4 * q + 2]), c0, __fmul_rn(__uint_as_float(w.z), c1));
+      f[4 * q + 3] = __fmaf_rn(__uint_as_float(o[4 * q + 3]), c0, __fmul_rn(__uint_as_float(w.w), c1));
+    }
     if (write) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4 v;
-        v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-        v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-        v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-        v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+        v.x = pack_bf16x2(f[8 * q + 0], f[8 * q + 1]);
+        v.y = pack_bf16x2(f[8 * q + 2], f[8 * q + 3]);
+        v.z = pack_bf16x2(f[8 * q + 4], f[8 * q + 5]);
+        v.w = pack_bf16x2(f[8 * q + 6], f[8 * q + 7]);
         dst[4 * c + q] = v;
       }
     }
   }
   if (write && p.lse)
     p.lse[(size_t)(ru.row0 + gm.row_lo + r) * p.hq + h] =
-        l > 0.f ? (m_run + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        l_all > 0.f ? (m_all + log2f(l_all)) * 0.6931471805599453f : -INFINITY;
 }
 
 template <bool FP8>
@@ -571,6 +698,8 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   b.drain = bars + 19;
   b.tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   b.abort = reinterpret_cast<volatile int*>(bars + 21);
+  b.peer_ready = bars + 22;
+  b.dst_free = bars + 23;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -591,6 +720,8 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
     mbar_init(b.v8_empty, kConvWarps);
     mbar_init(b.o_final, 1);
     mbar_init(b.drain, 1);
+    mbar_init(b.peer_ready, 256);                  // every softmax thread of CTA 1
+    mbar_init(b.dst_free, 1);
     *b.abort = 0;
     fence_mbar_init();
   }
@@ -604,14 +735,16 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   if (warp == 1) umma::tmem_alloc(b.tmem_slot, kTmemCols);
   umma::fence_before_sync();
   __syncthreads();
+  cluster_sync();            // both CTAs' barriers initialised before any remote arrival
   umma::fence_after_sync();
   const uint32_t tmem = *b.tmem_slot;
   allow_next_grid();
   wait_prior_grid();
 
-  const Tile x = tile_of(p, blockIdx.x);
+  const uint32_t rank = cluster_ctarank();
+  const Tile x = tile_of(p, blockIdx.x >> 1);
   const RunInfo& ru = p.runs[x.run];
-  const TileGeom gm = geom_of(ru, x);
+  const TileGeom gm = geom_of(ru, x, rank);
 
   // Registers (e4m3 caches, where the softmax also holds the Q conversion):
   // the block launches with 512 x 128 = 65,536; the TMA/MMA warpgroup and
@@ -625,13 +758,14 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
     }
   } else if (warp < kConvWarp0) {
     if (FP8) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
-    softmax_role<FP8>(p, ru, x, gm, (warp - 4) >> 2, smem, tmem, b);
+    softmax_role<FP8>(p, ru, x, gm, rank, (warp - 4) >> 2, smem, tmem, b);
   } else if (FP8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsConv));
     converter(p, ru, gm, smem, b);
   }
   umma::fence_before_sync();
   __syncthreads();
+  cluster_sync();            // CTA 1's shared memory stays until CTA 0 has read it
   if (warp == 1) {
     umma::fence_after_sync();
     umma::tmem_dealloc(tmem, kTmemCols);
@@ -639,7 +773,7 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
 }
 
 template <bool FP8>
-cudaError_t launch(const PrefillParams& p, int grid, cudaStream_t s) {
+cudaError_t launch(const PrefillParams& p, int tiles, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
     // The register split only works if the block launches with at least the
@@ -654,15 +788,15 @@ cudaError_t launch(const PrefillParams& p, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_pdl(prefill_kernel<FP8>, dim3(grid), dim3(threads_of<FP8>()),
-                    Layout<FP8>::kSmemBytes, s, p);
+  return launch_pdl_cluster(prefill_kernel<FP8>, dim3(2 * tiles), dim3(threads_of<FP8>()),
+                            Layout<FP8>::kSmemBytes, s, p, 2);
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillParams& p, bool fp8, int grid, cudaStream_t s) {
-  if (grid <= 0) return cudaSuccess;
-  return fp8 ? launch<true>(p, grid, s) : launch<false>(p, grid, s);
+cudaError_t launch_prefill(const PrefillParams& p, bool fp8, int tiles, cudaStream_t s) {
+  if (tiles <= 0) return cudaSuccess;
+  return fp8 ? launch<true>(p, tiles, s) : launch<false>(p, tiles, s);
 }
 
 }  // namespace tfpa

@@ -98,8 +98,9 @@ def test_prefill_slices():
                        7 * FAKE, max_rows_per_launch=128)
     assert [(r["kind"], r["row0"], r["rows"]) for r in rec] == [
         ("prefill", 0, 128), ("prefill", 128, 128), ("prefill", 256, 1)]
-    # tiles: kv heads x head pairs x 128-row tiles
+    # tiles: kv heads x head pairs x 128-row tiles; a cluster of two CTAs per tile
     assert [r["items"] for r in rec] == [8 * 2 * 1] * 3
+    assert [r["grid"] for r in rec] == [2 * 8 * 2 * 1] * 3
     with B.record_launches() as rec:
         B.tfpa_prefill(c, segs, 4 * FAKE, np.zeros(257), np.arange(28672, 28929), 0.088,
                        7 * FAKE)
