@@ -67,11 +67,33 @@ struct Layout {
 };
 static_assert(Layout<true>::kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
-// e4m3 register split (the block launches with 512 x 128 = 65,536):
-constexpr int kRegsLow = 56;       // warps 0-3: TMA producer, MMA issuer
-constexpr int kRegsHigh = 200;     // warps 4-11: softmax
-constexpr int kRegsConv = 56;      // warps 12-15: converters
-static_assert(128 * (kRegsLow + 2 * kRegsHigh + kRegsConv) <= 512 * 128, "register split");
+// Register split per warpgroup (setmaxnreg): warps 0-3 (TMA producer, MMA
+// issuer) and the converters need few registers, the softmax warps (a
+// row's 128 scores each) many.  A split hands out no more than the block
+// launches with (e4m3: 512 x 128, bf16: 384 x 168), and no SM sub-partition
+// (one warp of each warpgroup) more than its 16,384.  The bf16 split was
+// picked by measurement: 64 / 216 ran 2.7 % faster than no split, where
+// 56 / 224 and 72 / 216 (the latter without any spill) ran slower.
+template <bool FP8>
+struct Regs;
+template <>
+struct Regs<true> {
+  static constexpr int kLow = 56, kHigh = 200, kConv = 56, kLaunch = 128;
+};
+template <>
+struct Regs<false> {
+  static constexpr int kLow = 64, kHigh = 216, kConv = 0, kLaunch = 168;
+};
+template <bool FP8>
+constexpr int regs_split() {
+  return 128 * (Regs<FP8>::kLow + 2 * Regs<FP8>::kHigh + Regs<FP8>::kConv);
+}
+static_assert(regs_split<true>() <= 512 * Regs<true>::kLaunch, "register split");
+static_assert(regs_split<false>() <= 384 * Regs<false>::kLaunch, "register split");
+static_assert(32 * (Regs<true>::kLow + 2 * Regs<true>::kHigh + Regs<true>::kConv) <= 16384,
+              "sub-partition registers");
+static_assert(32 * (Regs<false>::kLow + 2 * Regs<false>::kHigh) <= 16384,
+              "sub-partition registers");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 // One pair of exponentials in kPolyPeriod is computed on the FMA pipe
 // (exp2_poly) instead of the MUFU unit; 0: none.
@@ -561,7 +583,7 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
       f2 t = ffma2({__uint_as_float(sv[i0 >> 5][i0 & 31]),
                     __uint_as_float(sv[(i0 + 1) >> 5][(i0 + 1) & 31])}, sc2, nb2);
       f2 e;
-      if (kPolyPeriod > 0 && k % kPolyPeriod == kPolyPeriod - 1)
+      if (kPolyPeriod > 0 && k % (kPolyPeriod > 0 ? kPolyPeriod : 1) == kPolyPeriod - 1)
         e = exp2_poly(t);
       else
         e = {fast_exp2(t.x), fast_exp2(t.y)};
@@ -746,21 +768,18 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   const RunInfo& ru = p.runs[x.run];
   const TileGeom gm = geom_of(ru, x, rank);
 
-  // Registers (e4m3 caches, where the softmax also holds the Q conversion):
-  // the block launches with 512 x 128 = 65,536; the TMA/MMA warpgroup and
-  // the converters need few, the two softmax warpgroups more.
   if (warp < 4) {
-    if (FP8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kLow));
     if (warp == 0) {
       if (lane == 0) producer<FP8>(p, ru, x, gm, smem, b);
     } else if (warp == 1) {
       mma_issuer<FP8>(p, ru, gm, smem, tmem, b);
     }
   } else if (warp < kConvWarp0) {
-    if (FP8) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kHigh));
     softmax_role<FP8>(p, ru, x, gm, rank, (warp - 4) >> 2, smem, tmem, b);
   } else if (FP8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsConv));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kConv));
     converter(p, ru, gm, smem, b);
   }
   umma::fence_before_sync();
@@ -781,7 +800,7 @@ cudaError_t launch(const PrefillParams& p, int tiles, cudaStream_t s) {
     cudaFuncAttributes attr;
     cudaError_t e = cudaFuncGetAttributes(&attr, prefill_kernel<FP8>);
     if (e != cudaSuccess) return e;
-    if (FP8 && attr.numRegs * threads_of<FP8>() < 128 * (kRegsLow + 2 * kRegsHigh + kRegsConv))
+    if (attr.numRegs * threads_of<FP8>() < regs_split<FP8>())
       return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(prefill_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Layout<FP8>::kSmemBytes);
