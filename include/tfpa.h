@@ -54,7 +54,8 @@ extern "C" {
 
 enum {
   TFPA_OK = 0,
-  TFPA_EINVAL = -1,      /* bad dims, dtype, NULL pointer or misalignment    */
+  TFPA_EINVAL = -1,      /* bad dims, dtype, NULL pointer, misalignment, or a
+                            softmax_scale that is not finite and positive   */
   TFPA_ERANGE = -2,      /* a position, segment or (host-mirrored) page id out of range */
   TFPA_ECAPACITY = -3,   /* scratch too small for the requested rows/splits */
   TFPA_ECUDA = -4,       /* a CUDA runtime/driver call or a launch failed    */
@@ -289,7 +290,9 @@ int tfpa_prefill(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
  * is made, so the slicing logic runs on a machine without a GPU. */
 typedef struct {
   int32_t kind;          /* 0 write_kv, 1 decode partial, 2 merge, 3 prefill, 4 keep,
-                            5 stage pages, 6 save, 7 restore */
+                            5 stage pages, 6 save, 7 restore, 8 verify (decode or tree
+                            rows of runs with 49 or more query vectors per kv head, on
+                            tensor cores; items = tiles) */
   int32_t row0;          /* first row of the call this launch covers */
   int32_t rows;          /* rows it covers */
   int32_t runs;          /* row groups (segment, consecutive positions) */

@@ -66,7 +66,7 @@ class tfpa_launch_record(ctypes.Structure):
 
 HOOK = ctypes.CFUNCTYPE(None, ctypes.POINTER(tfpa_launch_record), ctypes.c_void_p)
 KINDS = {0: "write_kv", 1: "partial", 2: "merge", 3: "prefill", 4: "keep", 5: "stage",
-         6: "save", 7: "restore"}
+         6: "save", 7: "restore", 8: "verify"}
 
 _lib = None
 

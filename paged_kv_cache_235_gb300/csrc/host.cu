@@ -128,9 +128,10 @@ int get_map(const void* ptr, uint64_t rows, bool fp8, int box_inner, int box_row
   return TFPA_OK;
 }
 
-// q of one launch as a 3D tensor [rows][hq][128] bf16, box 64 x 1 x 128 rows
-// (one head's 128-row tile, half the head dim), 128B swizzle.
-int get_qmap(const void* q, int hq, int rows, CUtensorMap* out) {
+// q of one launch as a 3D tensor [rows][hq][128] bf16, 128B swizzle; box
+// 64 x 1 x 128 (prefill: one head's 128-row tile, half the head dim) or
+// 64 x 2 x 64 (verify: 64 rows of a head pair).
+int get_qmap(const void* q, int hq, int rows, int box_heads, int box_rows, CUtensorMap* out) {
   if (dry_run()) {
     std::memset(out, 0, sizeof(*out));
     return TFPA_OK;
@@ -139,7 +140,7 @@ int get_qmap(const void* q, int hq, int rows, CUtensorMap* out) {
   if (!fn) return TFPA_ECUDA;
   cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hq, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)hq * kHeadDim * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -227,6 +228,21 @@ extern "C" int32_t tfpa_num_splits(int32_t seq_len) {
 }
 
 namespace {
+
+// Splits of a run on the tensor-core verify path: at least 16 pages (4,096
+// keys, so a tile's fixed costs stay small against its key tiles) and at
+// most kMaxSplits per stream; never more splits than the decode path's, so
+// a scratch sized for decode holds them.  A function of the stream's length
+// only, like the decode splits.
+int32_t verify_pages_per_split(int32_t seq_len) {
+  const int32_t np = pages_of(std::max(seq_len, 1));
+  return std::max<int32_t>(16, (np + kMaxSplits - 1) / kMaxSplits);
+}
+int32_t verify_num_splits(int32_t seq_len) {
+  const int32_t np = pages_of(std::max(seq_len, 1));
+  const int32_t pps = verify_pages_per_split(seq_len);
+  return (np + pps - 1) / pps;
+}
 
 // K/V sources of one launch: source 0 is the pool, 1.. are slab streams.
 struct SourceSet {
@@ -339,7 +355,7 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
   if (rows > 0 && (!q || !aligned(q, 16))) return TFPA_EINVAL;
   if (sliced && rows > 0 && (!out || !aligned(out, 8))) return TFPA_EINVAL;
   if (anc && !aligned(anc, 8)) return TFPA_EINVAL;
-  if (!std::isfinite(scale)) return TFPA_EINVAL;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return TFPA_EINVAL;
   if (!sliced && rows > sc->cap_rows) return TFPA_ECAPACITY;
   std::vector<Run> runs;
   if ((e = build_runs(segs, nseg, row_seg, row_pos, rows, runs))) return e;
@@ -355,32 +371,53 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
 
   size_t ri = 0;
   int32_t taken = 0;  // rows of runs[ri] already launched
-  static DecodeParams p;  // large; built under the lock below
+  static DecodeParams p;   // large; built under the lock below
+  static PrefillParams pv;  // the tensor-core verify launch of the same rows
   static MergeParams mp;
   std::lock_guard<std::mutex> lock(g_mu);
+  // Runs of four or more m-tiles (16 query vectors each, so at least 49
+  // vectors per kv head) are dense enough for the tensor cores: they go to
+  // the prefill kernel in verify mode (64 rows x 2 heads per MMA slot),
+  // the rest to the decode partial kernel.  Decided on the call's whole
+  // run, so every slice of it computes its rows with the same arithmetic
+  // (slices give the same bytes as one launch).  Verify slots hold head
+  // pairs, so a cache with one query head per kv head keeps the decode
+  // kernel's wide items instead.
+  const bool verify_ok = G >= 2;
+  auto is_wide = [&](const Run& r) { return (r.nrows * G + 15) / 16 >= 4; };
+  const int npairs = (G + 1) / 2, ngroups = (npairs + 1) / 2;
   while (ri < runs.size()) {
     std::memset(&p, 0, sizeof(p));
+    std::memset(&pv, 0, sizeof(pv));
     SourceSet ss;
     const int32_t base = runs[ri].row0 + taken;  // first call row of this launch
-    int32_t nrows = 0, items = 0;
-    int nr = 0;
+    int32_t nrows = 0, items = 0, tiles = 0;
+    int nr = 0, nd = 0, nv = 0;  // runs of the slice: all, decode, verify
     while (ri < runs.size() && nr < kMaxRuns && nrows < sc->cap_rows) {
       const Run& r = runs[ri];
       const int src = ss.add(segs, r.seg);
       if (src < 0) break;
       const int32_t take = std::min(r.nrows - taken, sc->cap_rows - nrows);
-      RunInfo& info = p.runs[nr];
-      fill_run(info, segs[r.seg], src, nrows, take, r.pos0 + taken);
-      info.item0 = items;
-      // Runs of four or more m-tiles (16 query vectors each) take wide items:
-      // four m-tiles share each K/V stage instead of reading it once each.
-      // Decided on the call's whole run, so every slice of it computes its
-      // rows with the same arithmetic (slices give the same bytes as one
-      // launch).
-      const int mtiles = (take * G + 15) / 16;
-      info.wide = (r.nrows * G + 15) / 16 >= 4 ? 1 : 0;
-      items += c->hkv * (info.wide ? (mtiles + 3) / 4 : mtiles) * info.nsplit;
-      mp.runs[nr] = MergeRun{nrows, take, info.nsplit, 0};
+      const tfpa_seg& g = segs[r.seg];
+      if (verify_ok && is_wide(r)) {
+        RunInfo& info = pv.runs[nv++];
+        fill_run(info, g, src, nrows, take, r.pos0 + taken);
+        info.pps = verify_pages_per_split(g.seq_len);
+        info.nsplit = verify_num_splits(g.seq_len);
+        info.item0 = tiles;
+        tiles += c->hkv * ngroups * ((take + kVerifyRows - 1) / kVerifyRows) * info.nsplit;
+        mp.runs[nr] = MergeRun{nrows, take, info.nsplit, 0};
+      } else {
+        RunInfo& info = p.runs[nd++];
+        fill_run(info, g, src, nrows, take, r.pos0 + taken);
+        info.item0 = items;
+        // Wide items (one cache head per query head only): four m-tiles
+        // share each K/V stage instead of reading it once each.
+        const int mtiles = (take * G + 15) / 16;
+        info.wide = is_wide(r) ? 1 : 0;
+        items += c->hkv * (info.wide ? (mtiles + 3) / 4 : mtiles) * info.nsplit;
+        mp.runs[nr] = MergeRun{nrows, take, info.nsplit, 0};
+      }
       ++nr;
       nrows += take;
       taken += take;
@@ -389,35 +426,65 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
         taken = 0;
       }
     }
-    if ((e = fill_maps(c, segs, ss, fp8, fp8 ? 128 : 64, fp8 ? 256 : 128, p.maps, p.nsrc)))
-      return e;
     const int32_t srow = sliced ? 0 : base;  // scratch row of this launch's first row
     const size_t srow_elems = (size_t)srow * c->hq * sc->max_splits;
-    p.q = static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd;
-    p.anc = anc ? anc + base : nullptr;   // the ancestor table shifts with the rows
-    p.part_o = sc->part_o + srow_elems * kHeadDim;
-    p.part_ml = sc->part_ml + srow_elems * 2;
-    p.k_scale = c->k_scale;
-    p.v_scale = c->v_scale;
-    p.err_flag = c->err_flag;
-    p.nruns = nr;
-    p.n_items = items;
-    p.hq = c->hq;
-    p.hkv = c->hkv;
-    p.group = G;
-    p.max_splits = sc->max_splits;
-    p.num_pages = c->num_pages;
-    p.rows = nrows;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    const int grid = std::min(std::min(items, nsm), kMaxDecodeGrid);
-    plan_cta_ranges(p, nr, G, fp8, grid);
-    record(1, base, nrows, nr, items, grid, (int64_t)base * hd, 0);
-    if (!dry_run()) {
-      if ((e = to_err(launch_decode_partial(p, fp8, grid, stream)))) return e;
+    float* part_o = sc->part_o + srow_elems * kHeadDim;
+    float* part_ml = sc->part_ml + srow_elems * 2;
+    if (nd > 0) {
+      if ((e = fill_maps(c, segs, ss, fp8, fp8 ? 128 : 64, fp8 ? 256 : 128, p.maps, p.nsrc)))
+        return e;
+      p.q = static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd;
+      p.anc = anc ? anc + base : nullptr;   // the ancestor table shifts with the rows
+      p.part_o = part_o;
+      p.part_ml = part_ml;
+      p.k_scale = c->k_scale;
+      p.v_scale = c->v_scale;
+      p.err_flag = c->err_flag;
+      p.nruns = nd;
+      p.n_items = items;
+      p.hq = c->hq;
+      p.hkv = c->hkv;
+      p.group = G;
+      p.max_splits = sc->max_splits;
+      p.num_pages = c->num_pages;
+      p.rows = nrows;
+      p.scale_log2 = scale * 1.4426950408889634f;
+      const int grid = std::min(std::min(items, nsm), kMaxDecodeGrid);
+      plan_cta_ranges(p, nd, G, fp8, grid);
+      record(1, base, nrows, nd, items, grid, (int64_t)base * hd, 0);
+      if (!dry_run()) {
+        if ((e = to_err(launch_decode_partial(p, fp8, grid, stream)))) return e;
+      }
+    }
+    if (nv > 0) {
+      if ((e = fill_maps(c, segs, ss, fp8, fp8 ? 128 : 64, 128, pv.maps, pv.nsrc))) return e;
+      if ((e = get_qmap(static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd, c->hq, nrows,
+                        2, kVerifyRows, &pv.qmap)))
+        return e;
+      pv.q = static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd;
+      pv.anc = anc ? anc + base : nullptr;
+      pv.part_o = part_o;
+      pv.part_ml = part_ml;
+      pv.k_scale = c->k_scale;
+      pv.v_scale = c->v_scale;
+      pv.err_flag = c->err_flag;
+      pv.nruns = nv;
+      pv.n_tiles = tiles;
+      pv.hq = c->hq;
+      pv.hkv = c->hkv;
+      pv.group = G;
+      pv.num_pages = c->num_pages;
+      pv.rows = nrows;
+      pv.max_splits = sc->max_splits;
+      pv.scale_log2 = scale * 1.4426950408889634f;
+      record(8, base, nrows, nv, tiles, tiles, (int64_t)base * hd, 0);
+      if (!dry_run()) {
+        if ((e = to_err(launch_verify(pv, fp8, tiles, stream)))) return e;
+      }
     }
     if (sliced) {
-      mp.part_o = p.part_o;
-      mp.part_ml = p.part_ml;
+      mp.part_o = part_o;
+      mp.part_ml = part_ml;
       mp.out = static_cast<__nv_bfloat16*>(out) + (size_t)base * hd;
       mp.lse = lse ? lse + (size_t)base * c->hq : nullptr;
       mp.nruns = nr;
@@ -737,7 +804,7 @@ extern "C" int tfpa_prefill(const tfpa_cache* c, const tfpa_seg* segs, int32_t n
   int e;
   if ((e = check_cache(c)) || (e = check_segs(c, segs, nseg))) return e;
   if (rows > 0 && (!q || !aligned(q, 16) || !out || !aligned(out, 16))) return TFPA_EINVAL;
-  if (max_rows_per_launch < 0 || !std::isfinite(scale)) return TFPA_EINVAL;
+  if (max_rows_per_launch < 0 || !std::isfinite(scale) || !(scale > 0.f)) return TFPA_EINVAL;
   std::vector<Run> runs;
   if ((e = build_runs(segs, nseg, row_seg, row_pos, rows, runs))) return e;
   if (rows == 0) return TFPA_OK;
@@ -776,7 +843,8 @@ extern "C" int tfpa_prefill(const tfpa_cache* c, const tfpa_seg* segs, int32_t n
       }
     }
     if ((e = fill_maps(c, segs, ss, fp8, fp8 ? 128 : 64, 128, p.maps, p.nsrc))) return e;
-    if ((e = get_qmap(static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd, c->hq, nrows,
+    if ((e = get_qmap(static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd, c->hq, nrows, 1,
+                      kPrefillTileRows,
                       &p.qmap)))
       return e;
     p.q = static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd;

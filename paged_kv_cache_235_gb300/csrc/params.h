@@ -34,8 +34,8 @@ struct RunInfo {
   int32_t row0;               // first row, relative to this launch
   int32_t nrows;
   int32_t pos0;               // position of the first row
-  int32_t nsplit;             // decode: splits of this stream
-  int32_t pps;                // decode: pages per split
+  int32_t nsplit;             // decode and verify: splits of this stream
+  int32_t pps;                // decode and verify: pages per split
   int32_t item0;              // first work item of this run
   int32_t slab_cap;           // slab capacity in positions (slab runs)
   int32_t wide;               // decode: an item covers four m-tiles (runs of >= 4 m-tiles)
@@ -139,13 +139,22 @@ struct KeepParams {
 };
 
 // Prefill: one work tile = (run, kv head g, query-head pair, 128 rows).
+// The same kernel in verify mode (decode runs of many query vectors, on
+// tensor cores): one work tile = (run, kv head g, group of two head pairs,
+// 64 rows, key split); the two slots hold the two pairs' query vectors
+// (64 rows x 2 heads each), and the tile writes split partials.
+constexpr int kVerifyRows = 64;
 struct PrefillParams {
   KVMaps maps[kMaxSources];
-  CUtensorMap qmap;           // q as 3D [rows][hq][128], box 64 x 1 x 128, 128B swizzle
+  CUtensorMap qmap;           // q as 3D [rows][hq][128], 128B swizzle; box 64 x 1 x 128
+                              // (prefill) or 64 x 2 x 64 (verify)
   RunInfo runs[kMaxRuns];     // item0 = first tile of the run
   const __nv_bfloat16* q;     // [rows][hq][128]
-  __nv_bfloat16* out;
-  float* lse;
+  __nv_bfloat16* out;         // prefill
+  float* lse;                 // prefill, or nullptr
+  const uint64_t* anc;        // verify: the rows' ancestor masks, or nullptr (causal)
+  float* part_o;              // verify: [rows][hq][max_splits][128]
+  float* part_ml;             // verify: [rows][hq][max_splits][2]
   const float* k_scale;
   const float* v_scale;
   int32_t* err_flag;
@@ -155,6 +164,7 @@ struct PrefillParams {
   int32_t hq, hkv, group;
   int32_t num_pages;
   int32_t rows;
+  int32_t max_splits;         // verify
   float scale_log2;
 };
 
@@ -191,6 +201,8 @@ cudaError_t launch_stage(const StageParams& p, cudaStream_t s);
 cudaError_t launch_copy(const CopyParams& p, int npages, cudaStream_t s);
 cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
-cudaError_t launch_prefill(const PrefillParams& p, bool fp8, int grid, cudaStream_t s);
+// Prefill launches a cluster of two CTAs per tile; verify one CTA per tile.
+cudaError_t launch_prefill(const PrefillParams& p, bool fp8, int tiles, cudaStream_t s);
+cudaError_t launch_verify(const PrefillParams& p, bool fp8, int tiles, cudaStream_t s);
 
 }  // namespace tfpa

@@ -146,26 +146,40 @@ struct Bars {
 };
 
 struct Tile {
-  int run, g, hp, t;
+  int run, g, hp, t, sigma;   // verify: hp is the group of two head pairs
 };
 
-// Tiles are numbered heaviest first: the row-tile index is the slowest digit
-// and runs from the last (longest causal range) to the first.
+// Prefill tiles are numbered heaviest first: the row-tile index is the
+// slowest digit and runs from the last (longest causal range) to the first.
+// Verify tiles: split, kv head, pair group, row tile (slowest first).
+template <bool VERIFY>
 __device__ __forceinline__ Tile tile_of(const PrefillParams& p, int i) {
   int r = 0;
   while (r + 1 < p.nruns && p.runs[r + 1].item0 <= i) ++r;
   const RunInfo& ru = p.runs[r];
-  const int local = i - ru.item0;
+  int local = i - ru.item0;
   const int npairs = (p.group + 1) >> 1;
+  Tile x;
+  x.run = r;
+  if (VERIFY) {
+    const int ngroups = (npairs + 1) >> 1;
+    const int nrt = (ru.nrows + kVerifyRows - 1) / kVerifyRows;
+    x.t = local % nrt;
+    local /= nrt;
+    x.hp = local % ngroups;
+    local /= ngroups;
+    x.g = local % p.hkv;
+    x.sigma = local / p.hkv;
+    return x;
+  }
   const int pairs_total = p.hkv * npairs;
   const int ntr = (ru.nrows + kTileRows - 1) / kTileRows;
   const int t_rev = local / pairs_total;
   const int gp = local - t_rev * pairs_total;
-  Tile x;
-  x.run = r;
   x.g = gp / npairs;
   x.hp = gp - x.g * npairs;
   x.t = ntr - 1 - t_rev;
+  x.sigma = 0;
   return x;
 }
 
@@ -176,15 +190,25 @@ struct TileGeom {
   int kt0, nkt;    // this CTA's key tiles: kt0 .. kt0 + nkt - 1
 };
 
-// Key tiles [0, n / 2) go to CTA 0 of the cluster, [n / 2, n) to CTA 1
-// (CTA 0 has none when n = 1).
+// Prefill: key tiles [0, n / 2) go to CTA 0 of the cluster, [n / 2, n) to
+// CTA 1 (CTA 0 has none when n = 1).  Verify: the key tiles of split sigma
+// (pps pages of the stream each), cut at the tile's last position; a split
+// past it has none.
+template <bool VERIFY>
 __device__ __forceinline__ TileGeom geom_of(const RunInfo& ru, const Tile& x, uint32_t rank) {
   TileGeom gm;
-  gm.row_lo = x.t * kTileRows;
-  gm.nrows = min(kTileRows, ru.nrows - gm.row_lo);
+  const int rows = VERIFY ? kVerifyRows : kTileRows;
+  gm.row_lo = x.t * rows;
+  gm.nrows = min(rows, ru.nrows - gm.row_lo);
   const int maxpos = ru.pos0 + gm.row_lo + gm.nrows - 1;
   gm.kend = min(ru.seq_len, maxpos + 1);
   const int n = (gm.kend + kTileKeys - 1) / kTileKeys;
+  if (VERIFY) {
+    const int per = ru.pps * (kPage / kTileKeys);
+    gm.kt0 = x.sigma * per;
+    gm.nkt = max(0, min(n, gm.kt0 + per) - gm.kt0);
+    return gm;
+  }
   const int mid = n >> 1;
   gm.kt0 = rank ? mid : 0;
   gm.nkt = rank ? n - mid : mid;
@@ -224,21 +248,64 @@ __device__ __forceinline__ int v_zero_from(const RunInfo& ru, int j, bool page_b
   return kt + kTileKeys > ru.seq_len ? ru.seq_len - kt : kTileKeys;
 }
 
-template <bool FP8>
+// Prefetch of one box of a tensor into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
+               : "memory");
+}
+
+// Verify tiles stream their keys from HBM once (prefill tiles re-read a
+// prefix that mostly sits in L2), and a ring of two stages holds them only
+// about one step ahead of the MMAs: the producer also prefetches the K and
+// V boxes of the tile kAhead steps ahead into L2.
+constexpr int kAhead = 4;
+
+template <bool FP8, bool VERIFY>
 __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& x,
                          const TileGeom& gm, uint8_t* smem, const Bars& b) {
   const CUtensorMap* mk = &p.maps[ru.src].k;
   const CUtensorMap* mv = &p.maps[ru.src].v;
-  const int h0 = x.g * p.group + 2 * x.hp;
   if (gm.nkt == 0) return;
+  // Prefill: slot hh is head h0 + hh, 128 rows (box 64 x 1 x 128).  Verify:
+  // slot hh is head pair 2 hp + hh, 64 rows x its two heads (box 64 x 2 x
+  // 64, landing as M row 2 (row) + head); past the pairs or the rows, the
+  // tile holds other heads' rows or zeros, which no output reads.
   mbar_arrive_expect_tx(b.q_full, 65536);
-  for (int hh = 0; hh < 2; ++hh)
+  for (int hh = 0; hh < 2; ++hh) {
+    const int h = VERIFY ? x.g * p.group + 2 * (2 * x.hp + hh) : x.g * p.group + 2 * x.hp + hh;
     for (int rg = 0; rg < 2; ++rg)
-      tma_load_3d(smem + kOffQ + hh * 32768 + rg * 16384, &p.qmap, rg * 64, h0 + hh,
+      tma_load_3d(smem + kOffQ + hh * 32768 + rg * 16384, &p.qmap, rg * 64, h,
                   ru.row0 + gm.row_lo, b.q_full);
+  }
   int cached_page = -1, cached_pid = 0;
+  int pf_page = -1, pf_pid = 0;
+  auto prefetch = [&](int jj) {             // verify: tile jj of this CTA into L2
+    if (!VERIFY || jj >= gm.nkt) return;
+    const int kt = (gm.kt0 + jj) * kTileKeys;
+    int y;
+    if (ru.page_table) {
+      const int page = kt >> 8;
+      if (page != pf_page) {
+        pf_pid = __ldg(ru.page_table + page);
+        pf_page = page;
+      }
+      if ((unsigned)pf_pid >= (unsigned)p.num_pages) return;   // the load flags it
+      y = (pf_pid * p.hkv + x.g) * kPage + (kt & (kPage - 1));
+    } else {
+      y = x.g * ru.slab_cap + kt;
+    }
+    tma_prefetch_l2(mk, 0, y);
+    tma_prefetch_l2(mv, 0, y);
+    if (!FP8) {
+      tma_prefetch_l2(mk, 64, y);
+      tma_prefetch_l2(mv, 64, y);
+    }
+  };
+  for (int a = 0; a < kAhead; ++a) prefetch(a);
   int issued_k = 0, issued_v = 0;
   for (int jj = 0; jj < gm.nkt; ++jj) {     // jj counts this CTA's tiles
+    prefetch(jj + kAhead);
     const int s = jj & 1;
     const uint32_t ph = (jj >> 1) & 1;
     const int kt = (gm.kt0 + jj) * kTileKeys;
@@ -512,7 +579,7 @@ __device__ __forceinline__ uint32_t part_ml(uint32_t smem_base, int hh, int r) {
   return smem_base + kOffQ + (hh * kTileRows + r) * 8;
 }
 
-template <bool FP8>
+template <bool FP8, bool VERIFY>
 __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Tile& x,
                              const TileGeom& gm, uint32_t rank, int hh, uint8_t* smem,
                              uint32_t tmem, const Bars& b) {
@@ -521,8 +588,17 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
   const uint32_t tS = tmem + lane_off + col_s(hh);
   const uint32_t tO = tmem + lane_off + col_o(hh);
-  const bool valid = r < gm.nrows;
-  const int pos = ru.pos0 + gm.row_lo + (valid ? r : 0);
+  // Verify: TMEM lane r holds query vector (row r / 2, head 2 (pair) + r % 2).
+  const int rho = VERIFY ? r >> 1 : r;                  // row within the tile
+  const int hig = 2 * (2 * x.hp + hh) + (r & 1);        // verify: head within the group
+  const bool valid = rho < gm.nrows && (!VERIFY || hig < p.group);
+  const int pos = ru.pos0 + gm.row_lo + (valid ? rho : 0);
+  // Verify with ancestor masks: key pos - d (d < 64) is visible iff bit d of
+  // the row's mask is set; keys further back always are.  Bit-reversed, the
+  // mask lines up with key order: key lim - d of a tile is bit 63 - d.
+  const bool tree = VERIFY && p.anc != nullptr;
+  const uint64_t anc_rev =
+      __brevll(tree && valid ? __ldg(p.anc + ru.row0 + gm.row_lo + rho) : ~0ull);
   float sl2 = p.scale_log2;
   bool ok = true;
   if (FP8 && gm.nkt > 0) {
@@ -545,22 +621,43 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
     umma::fence_after_sync();
     const int kt = j * kTileKeys;
     const int lim = page_bad ? -1 : pos - kt;            // key kt+i visible iff i <= lim
-    const bool full_tile = lim >= kTileKeys - 1;
+    const bool full_tile = lim >= kTileKeys - 1 + (tree ? 64 : 0);
     uint32_t sv[4][32];
 #pragma unroll
     for (int c = 0; c < 4; ++c) umma::tmem_ld32(tS + 32 * c, sv[c]);
     umma::tmem_ld_wait();
-    float mx = -INFINITY;
-    if (full_tile) {
+    if (!full_tile) {
+      // Masked keys' scores become -inf: they take no part in the max, and
+      // with a positive scale their exponentials are exactly 0.  Bit b of
+      // word w: key kt + 32 w + b is visible (causal bound, then the
+      // ancestor bits over the 64 keys up to the row's position).
+      uint32_t vis[4];
 #pragma unroll
-      for (int k = 0; k < 64; ++k)
-        mx = fmax3(mx, __uint_as_float(sv[(2 * k) >> 5][(2 * k) & 31]),
-                   __uint_as_float(sv[(2 * k + 1) >> 5][(2 * k + 1) & 31]));
-    } else {
+      for (int w = 0; w < 4; ++w) {
+        const int n = lim - 32 * w + 1;                  // causal keys in this word
+        vis[w] = n >= 32 ? ~0u : (n <= 0 ? 0u : (1u << n) - 1u);
+        if (tree) {
+          const int o = 32 * w - lim + 63;               // reversed-mask bit of key 32 w
+          uint32_t win = 0u, bits = 0u;
+          if (o >= 0 && o < 64) {
+            win = (uint32_t)(~0ull >> o);
+            bits = (uint32_t)(anc_rev >> o);
+          } else if (o < 0 && o > -32) {
+            win = (uint32_t)(~0ull << -o);
+            bits = (uint32_t)(anc_rev << -o);
+          }
+          vis[w] = (vis[w] & ~win) | (bits & win);
+        }
+      }
 #pragma unroll
       for (int i = 0; i < 128; ++i)
-        mx = i <= lim ? fmaxf(mx, __uint_as_float(sv[i >> 5][i & 31])) : mx;
+        if (!((vis[i >> 5] >> (i & 31)) & 1u)) sv[i >> 5][i & 31] = 0xff800000u;   // -inf
     }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 64; ++k)
+      mx = fmax3(mx, __uint_as_float(sv[(2 * k) >> 5][(2 * k) & 31]),
+                 __uint_as_float(sv[(2 * k + 1) >> 5][(2 * k + 1) & 31]));
     mx = mx * sl2;
     const float m_new = fmaxf(m_run, mx);
     const bool resc = m_new > m_run + kRescaleThreshold;
@@ -587,10 +684,6 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
         e = exp2_poly(t);
       else
         e = {fast_exp2(t.x), fast_exp2(t.y)};
-      if (!full_tile) {
-        e.x = i0 <= lim ? e.x : 0.f;
-        e.y = i0 + 1 <= lim ? e.y : 0.f;
-      }
       acc = fadd2(acc, e);
       sv[k >> 5][k & 31] = FP8 ? pack_f16x2(e.x, e.y) : pack_bf16x2(e.x, e.y);
     }
@@ -616,6 +709,41 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
   }
   if (ok) ok = mbar_wait_or_abort(b.o_final, 0, p.err_flag, b.abort);
   if (ok) umma::fence_after_sync();
+
+  if (VERIFY) {
+    // Split sigma's partial, as the decode partial kernel leaves it: m in
+    // log2 units, l, and O (unnormalised, V scale applied).  A vector that
+    // saw no key here gets m = -inf, l = 0, O = 0.  Every lane takes part in
+    // the TMEM loads; only the stores depend on the row.
+    if (!__all_sync(0xffffffffu, ok)) return;
+    const size_t slot =
+        ((size_t)(ru.row0 + gm.row_lo + rho) * p.hq + x.g * p.group + hig) * p.max_splits +
+        x.sigma;
+    const float vs = FP8 ? __ldg(p.v_scale + x.g) : 1.f;
+    float4* po = reinterpret_cast<float4*>(p.part_o + slot * kHeadDim);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t o[32];
+      if (gm.nkt > 0) {
+        umma::tmem_ld32(tO + 32 * c, o);
+        umma::tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0u;
+      }
+      if (valid) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          po[8 * c + q] = make_float4(__uint_as_float(o[4 * q]) * vs,
+                                      __uint_as_float(o[4 * q + 1]) * vs,
+                                      __uint_as_float(o[4 * q + 2]) * vs,
+                                      __uint_as_float(o[4 * q + 3]) * vs);
+      }
+    }
+    if (valid) *reinterpret_cast<float2*>(p.part_ml + slot * 2) = make_float2(m_run, l);
+    return;
+  }
+
   const uint32_t sbase = smem_u32(smem);
 
   if (rank == 1) {
@@ -696,7 +824,7 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
         l_all > 0.f ? (m_all + log2f(l_all)) * 0.6931471805599453f : -INFINITY;
 }
 
-template <bool FP8>
+template <bool FP8, bool VERIFY>
 __global__ void __launch_bounds__(threads_of<FP8>(), 1)
     prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -757,65 +885,74 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   if (warp == 1) umma::tmem_alloc(b.tmem_slot, kTmemCols);
   umma::fence_before_sync();
   __syncthreads();
-  cluster_sync();            // both CTAs' barriers initialised before any remote arrival
+  if (!VERIFY) cluster_sync();   // both CTAs' barriers initialised before any remote arrival
   umma::fence_after_sync();
   const uint32_t tmem = *b.tmem_slot;
   allow_next_grid();
   wait_prior_grid();
 
-  const uint32_t rank = cluster_ctarank();
-  const Tile x = tile_of(p, blockIdx.x >> 1);
+  // Prefill: two CTAs (a cluster) per tile; verify: one CTA per tile.
+  const uint32_t rank = VERIFY ? 0 : cluster_ctarank();
+  const Tile x = tile_of<VERIFY>(p, VERIFY ? blockIdx.x : blockIdx.x >> 1);
   const RunInfo& ru = p.runs[x.run];
-  const TileGeom gm = geom_of(ru, x, rank);
+  const TileGeom gm = geom_of<VERIFY>(ru, x, rank);
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kLow));
     if (warp == 0) {
-      if (lane == 0) producer<FP8>(p, ru, x, gm, smem, b);
+      if (lane == 0) producer<FP8, VERIFY>(p, ru, x, gm, smem, b);
     } else if (warp == 1) {
       mma_issuer<FP8>(p, ru, gm, smem, tmem, b);
     }
   } else if (warp < kConvWarp0) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kHigh));
-    softmax_role<FP8>(p, ru, x, gm, rank, (warp - 4) >> 2, smem, tmem, b);
+    softmax_role<FP8, VERIFY>(p, ru, x, gm, rank, (warp - 4) >> 2, smem, tmem, b);
   } else if (FP8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kConv));
     converter(p, ru, gm, smem, b);
   }
   umma::fence_before_sync();
   __syncthreads();
-  cluster_sync();            // CTA 1's shared memory stays until CTA 0 has read it
+  if (!VERIFY) cluster_sync();   // CTA 1's shared memory stays until CTA 0 has read it
   if (warp == 1) {
     umma::fence_after_sync();
     umma::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-template <bool FP8>
+template <bool FP8, bool VERIFY>
 cudaError_t launch(const PrefillParams& p, int tiles, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
     // The register split only works if the block launches with at least the
     // registers it hands out; otherwise setmaxnreg.inc would wait forever.
     cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, prefill_kernel<FP8>);
+    cudaError_t e = cudaFuncGetAttributes(&attr, prefill_kernel<FP8, VERIFY>);
     if (e != cudaSuccess) return e;
     if (attr.numRegs * threads_of<FP8>() < regs_split<FP8>())
       return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(prefill_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Layout<FP8>::kSmemBytes);
+    e = cudaFuncSetAttribute(prefill_kernel<FP8, VERIFY>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<FP8>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_pdl_cluster(prefill_kernel<FP8>, dim3(2 * tiles), dim3(threads_of<FP8>()),
-                            Layout<FP8>::kSmemBytes, s, p, 2);
+  if (VERIFY)
+    return launch_pdl(prefill_kernel<FP8, VERIFY>, dim3(tiles), dim3(threads_of<FP8>()),
+                      Layout<FP8>::kSmemBytes, s, p);
+  return launch_pdl_cluster(prefill_kernel<FP8, VERIFY>, dim3(2 * tiles),
+                            dim3(threads_of<FP8>()), Layout<FP8>::kSmemBytes, s, p, 2);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillParams& p, bool fp8, int tiles, cudaStream_t s) {
   if (tiles <= 0) return cudaSuccess;
-  return fp8 ? launch<true>(p, tiles, s) : launch<false>(p, tiles, s);
+  return fp8 ? launch<true, false>(p, tiles, s) : launch<false, false>(p, tiles, s);
+}
+
+cudaError_t launch_verify(const PrefillParams& p, bool fp8, int tiles, cudaStream_t s) {
+  if (tiles <= 0) return cudaSuccess;
+  return fp8 ? launch<true, true>(p, tiles, s) : launch<false, true>(p, tiles, s);
 }
 
 }  // namespace tfpa

@@ -47,18 +47,25 @@ def _cache(hq=32, hkv=8, dtype="bf16"):
                    FAKE if dtype == "fp8" else None, None, 4096)
 
 
-@pytest.mark.parametrize("rows", [1, 127, 128, 129, 255, 256, 257, 4096])
+# A run of 13 or more rows (49+ query vectors per kv head at 32/8 heads) is
+# computed by the tensor-core verify kernel, a shorter one by the decode
+# partial kernel; both leave split partials for the same merge.
+PARTIALS = ("partial", "verify")
+
+
+@pytest.mark.parametrize("rows", [1, 12, 13, 127, 128, 129, 255, 256, 257, 4096])
 def test_decode_slices_of_at_most_cap_rows(rows):
     c = _cache()
     segs = [B.Seg(rows + 40000, page_table=3 * FAKE)]
     with B.record_launches() as rec:
         B.tfpa_decode(c, segs, 4 * FAKE, np.zeros(rows), np.arange(40000, 40000 + rows), 0.088,
                       B.Scratch(5 * FAKE, 6 * FAKE, 128), 7 * FAKE)
-    parts = [r for r in rec if r["kind"] == "partial"]
+    parts = [r for r in rec if r["kind"] in PARTIALS]
     merges = [r for r in rec if r["kind"] == "merge"]
     n = (rows + 127) // 128
+    kind = "verify" if rows >= 13 else "partial"
     assert len(parts) == len(merges) == n
-    assert [r["kind"] for r in rec] == ["partial", "merge"] * n      # pairs, in order
+    assert [r["kind"] for r in rec] == [kind, "merge"] * n           # pairs, in order
     assert [r["row0"] for r in parts] == [128 * i for i in range(n)]
     assert sum(r["rows"] for r in merges) == rows                    # every row merged once
     hd = 32 * 128
@@ -72,9 +79,11 @@ def test_257_row_chunk_issues_three_pairs():
     with B.record_launches() as rec:
         B.tfpa_decode(c, segs, 4 * FAKE, np.zeros(257), np.arange(28672, 28929), 0.088,
                       B.Scratch(5 * FAKE, 6 * FAKE, 128), 7 * FAKE)
+    # the 1-row tail belongs to a 257-row run: decided on the call's run, it
+    # stays on the verify kernel
     assert [(r["kind"], r["row0"], r["rows"]) for r in rec] == [
-        ("partial", 0, 128), ("merge", 0, 128), ("partial", 128, 128), ("merge", 128, 128),
-        ("partial", 256, 1), ("merge", 256, 1)]
+        ("verify", 0, 128), ("merge", 0, 128), ("verify", 128, 128), ("merge", 128, 128),
+        ("verify", 256, 1), ("merge", 256, 1)]
 
 
 def test_mixed_paged_and_slab_streams_cross_slices():
@@ -86,7 +95,7 @@ def test_mixed_paged_and_slab_streams_cross_slices():
     with B.record_launches() as rec:
         B.tfpa_decode(c, segs, 4 * FAKE, rs, rp, 0.088, B.Scratch(5 * FAKE, 6 * FAKE, 128),
                       7 * FAKE)
-    parts = [r for r in rec if r["kind"] == "partial"]
+    parts = [r for r in rec if r["kind"] in PARTIALS]
     assert [(r["row0"], r["rows"], r["runs"]) for r in parts] == [(0, 128, 2), (128, 72, 1)]
 
 
@@ -105,6 +114,26 @@ def test_prefill_slices():
         B.tfpa_prefill(c, segs, 4 * FAKE, np.zeros(257), np.arange(28672, 28929), 0.088,
                        7 * FAKE)
     assert [(r["kind"], r["rows"], r["items"]) for r in rec] == [("prefill", 257, 8 * 2 * 3)]
+
+
+def test_verify_tiles_and_mixed_launch_order():
+    """Verify tiles: kv head x pair group x 64-row tile x split, splits of at
+    least 16 pages; a call with a short and a long run issues the decode
+    partial, then the verify launch, then one merge over both."""
+    c = _cache()
+    L = 65536
+    segs = [B.Seg(L, page_table=3 * FAKE), B.Seg(L, page_table=3 * FAKE)]
+    rs = np.array([0] + [1] * 16)
+    rp = np.concatenate([[L - 1], np.arange(L - 16, L)])
+    with B.record_launches() as rec:
+        B.tfpa_decode(c, segs, 4 * FAKE, rs, rp, 0.088, B.Scratch(5 * FAKE, 6 * FAKE, 128),
+                      7 * FAKE)
+    assert [(r["kind"], r["row0"], r["rows"], r["runs"]) for r in rec] == [
+        ("partial", 0, 17, 1), ("verify", 0, 17, 1), ("merge", 0, 17, 2)]
+    v = rec[1]
+    splits = 256 // 16                            # 65,536 keys = 256 pages, 16 a split
+    assert v["items"] == v["grid"] == 8 * 1 * 1 * splits
+    assert rec[0]["items"] == 8 * 1 * B.tfpa_num_splits(L)   # 4 vectors: one m-tile
 
 
 def test_write_kv_one_launch_per_64_runs():
@@ -163,7 +192,7 @@ def test_decode_tree_checks_its_ancestor_table():
         B.tfpa_decode_tree(c, segs, 4 * FAKE, [0] * 200, list(range(800, 1000)), 8 * FAKE,
                            0.088, sc, 7 * FAKE)
     assert [(r["kind"], r["row0"], r["rows"]) for r in rec] == [
-        ("partial", 0, 128), ("merge", 0, 128), ("partial", 128, 72), ("merge", 128, 72)]
+        ("verify", 0, 128), ("merge", 0, 128), ("verify", 128, 72), ("merge", 128, 72)]
 
 
 def test_write_kv_rope_and_keep_argument_checks():
