@@ -39,7 +39,7 @@ METRIC = "paged decode KV GB/s (% HBM peak); prompt-chunk attn TFLOP/s (% TC pea
 # from ncu (dram__bytes_read.sum + dram__bytes_write.sum, see
 # profiles/decode_partial_batched_decode.md), valid only while the kernel's
 # sources hash to the value it was taken on.
-DECODE_TRAFFIC = {"bytes": 268_613_376 + 4_083_968, "sources_sha256_16": "09fff6a37ef28b0b"}
+DECODE_TRAFFIC = {"bytes": 268_591_872 + 4_723_968, "sources_sha256_16": "6f51b467fb3bc848"}
 DECODE_SOURCES = ["paged_kv_cache_235_gb300/csrc/decode.cu",
                   "paged_kv_cache_235_gb300/csrc/common.cuh",
                   "paged_kv_cache_235_gb300/csrc/params.h",
@@ -463,13 +463,24 @@ def profile_case(args, torch, B, wl):
         ms = time_prefill(w, torch, B, args.steps)
         print(f"{args.case}: {ms:.4f} ms, {prefill_flops(w) / ms / 1e9:.1f} TFLOP/s")
         return
-    w = wl.batched_decode() if args.case == "decode" else wl.fp8_verify()
+    if args.case in ("tree_verify", "tree_verify_bf16"):
+        w = wl.tree_verify(kv_dtype="bf16" if args.case == "tree_verify_bf16" else "fp8")
+    else:
+        w = wl.batched_decode() if args.case == "decode" else wl.fp8_verify()
     cache, segs, q = device_case(w, torch, B)
     sc = B.make_scratch(min(128, w.rows), w.hq)
     out = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16, device="cuda")
+    anc = None
+    if w.row_anc is not None:
+        anc = torch.from_numpy(np.ascontiguousarray(w.row_anc).view(np.int64)).cuda()
     for _ in range(args.warmup + args.steps):
-        B.tfpa_decode(cache, segs, q, w.row_seg, w.row_pos, w.softmax_scale, sc, out)
+        if anc is None:
+            B.tfpa_decode(cache, segs, q, w.row_seg, w.row_pos, w.softmax_scale, sc, out)
+        else:
+            B.tfpa_decode_tree(cache, segs, q, w.row_seg, w.row_pos, anc, w.softmax_scale, sc,
+                               out)
     torch.cuda.synchronize()
+    assert int(cache.err_flag.item()) == 0, "kernel error flag set"
     print(f"{args.case}: {args.warmup + args.steps} decode calls done")
 
 
@@ -516,7 +527,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--case", default=None,
-                    choices=["decode", "fp8_verify", "prefill", "prefill_fp8"],
+                    choices=["decode", "fp8_verify", "prefill", "prefill_fp8", "tree_verify",
+                             "tree_verify_bf16"],
                     help="profiling mode: run only this workload's kernels --steps times "
                          "after --warmup, print its timing, no JSON line")
     args = ap.parse_args()
