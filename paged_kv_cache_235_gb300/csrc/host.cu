@@ -130,7 +130,7 @@ int get_map(const void* ptr, uint64_t rows, bool fp8, int box_inner, int box_row
 
 // q of one launch as a 3D tensor [rows][hq][128] bf16, 128B swizzle; box
 // 64 x 1 x 128 (prefill: one head's 128-row tile, half the head dim) or
-// 64 x 2 x 64 (verify: 64 rows of a head pair).
+// 64 x G x 128 / G (verify: a kv head's query vectors of 128 / G rows).
 int get_qmap(const void* q, int hq, int rows, int box_heads, int box_rows, CUtensorMap* out) {
   if (dry_run()) {
     std::memset(out, 0, sizeof(*out));
@@ -377,15 +377,14 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
   std::lock_guard<std::mutex> lock(g_mu);
   // Runs of four or more m-tiles (16 query vectors each, so at least 49
   // vectors per kv head) are dense enough for the tensor cores: they go to
-  // the prefill kernel in verify mode (64 rows x 2 heads per MMA slot),
-  // the rest to the decode partial kernel.  Decided on the call's whole
-  // run, so every slice of it computes its rows with the same arithmetic
-  // (slices give the same bytes as one launch).  Verify slots hold head
-  // pairs, so a cache with one query head per kv head keeps the decode
-  // kernel's wide items instead.
-  const bool verify_ok = G >= 2;
+  // the prefill kernel in verify mode (128 / G rows x the group's G heads
+  // per tile), the rest to the decode partial kernel.  Decided on the
+  // call's whole run, so every slice of it computes its rows with the same
+  // arithmetic (slices give the same bytes as one launch).  A group wider
+  // than a tile keeps the decode kernel's wide items.
+  const bool verify_ok = G <= kVerifyVectors;
   auto is_wide = [&](const Run& r) { return (r.nrows * G + 15) / 16 >= 4; };
-  const int npairs = (G + 1) / 2, ngroups = (npairs + 1) / 2;
+  const int vrows = verify_ok ? kVerifyVectors / G : 1;   // rows of a verify tile
   while (ri < runs.size()) {
     std::memset(&p, 0, sizeof(p));
     std::memset(&pv, 0, sizeof(pv));
@@ -405,7 +404,7 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
         info.pps = verify_pages_per_split(g.seq_len);
         info.nsplit = verify_num_splits(g.seq_len);
         info.item0 = tiles;
-        tiles += c->hkv * ngroups * ((take + kVerifyRows - 1) / kVerifyRows) * info.nsplit;
+        tiles += c->hkv * ((take + vrows - 1) / vrows) * info.nsplit;
         mp.runs[nr] = MergeRun{nrows, take, info.nsplit, 0};
       } else {
         RunInfo& info = p.runs[nd++];
@@ -459,7 +458,7 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
     if (nv > 0) {
       if ((e = fill_maps(c, segs, ss, fp8, fp8 ? 128 : 64, 128, pv.maps, pv.nsrc))) return e;
       if ((e = get_qmap(static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd, c->hq, nrows,
-                        2, kVerifyRows, &pv.qmap)))
+                        G, vrows, &pv.qmap)))
         return e;
       pv.q = static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd;
       pv.anc = anc ? anc + base : nullptr;

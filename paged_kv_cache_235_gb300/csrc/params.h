@@ -140,14 +140,15 @@ struct KeepParams {
 
 // Prefill: one work tile = (run, kv head g, query-head pair, 128 rows).
 // The same kernel in verify mode (decode runs of many query vectors, on
-// tensor cores): one work tile = (run, kv head g, group of two head pairs,
-// 64 rows, key split); the two slots hold the two pairs' query vectors
-// (64 rows x 2 heads each), and the tile writes split partials.
-constexpr int kVerifyRows = 64;
+// tensor cores): one work tile = (run, kv head g, 128 / G rows, key split);
+// its query vectors (rows x the group's G heads, at most 128) form one Q
+// tile that both MMA slots read, slot A taking the split's even key tiles
+// and slot B the odd ones, each leaving its own split partial.
+constexpr int kVerifyVectors = 128;
 struct PrefillParams {
   KVMaps maps[kMaxSources];
   CUtensorMap qmap;           // q as 3D [rows][hq][128], 128B swizzle; box 64 x 1 x 128
-                              // (prefill) or 64 x 2 x 64 (verify)
+                              // (prefill) or 64 x G x (128 / G) (verify)
   RunInfo runs[kMaxRuns];     // item0 = first tile of the run
   const __nv_bfloat16* q;     // [rows][hq][128]
   __nv_bfloat16* out;         // prefill

@@ -63,7 +63,11 @@ constexpr int kOffV8 = 212992;           // e4m3 staging: one V tile, 16 KB
 template <bool FP8>
 struct Layout {
   static constexpr int kOffBar = FP8 ? 229376 : 196608;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  // Verify: the Q rows' scale factors (e4m3 caches; 128 floats) and slot
+  // B's (m, l) per row for the merge of the two slots (128 float2).
+  static constexpr int kOffDown = kOffBar + 256;
+  static constexpr int kOffMl = kOffDown + 512;
+  static constexpr int kSmemBytes = kOffMl + 1024 + 1024;
 };
 static_assert(Layout<true>::kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
@@ -146,12 +150,12 @@ struct Bars {
 };
 
 struct Tile {
-  int run, g, hp, t, sigma;   // verify: hp is the group of two head pairs
+  int run, g, hp, t, sigma;
 };
 
 // Prefill tiles are numbered heaviest first: the row-tile index is the
 // slowest digit and runs from the last (longest causal range) to the first.
-// Verify tiles: split, kv head, pair group, row tile (slowest first).
+// Verify tiles: split, kv head, row tile (slowest first).
 template <bool VERIFY>
 __device__ __forceinline__ Tile tile_of(const PrefillParams& p, int i) {
   int r = 0;
@@ -162,14 +166,13 @@ __device__ __forceinline__ Tile tile_of(const PrefillParams& p, int i) {
   Tile x;
   x.run = r;
   if (VERIFY) {
-    const int ngroups = (npairs + 1) >> 1;
-    const int nrt = (ru.nrows + kVerifyRows - 1) / kVerifyRows;
+    const int rt = kVerifyVectors / p.group;           // rows of a tile
+    const int nrt = (ru.nrows + rt - 1) / rt;
     x.t = local % nrt;
     local /= nrt;
-    x.hp = local % ngroups;
-    local /= ngroups;
     x.g = local % p.hkv;
     x.sigma = local / p.hkv;
+    x.hp = 0;
     return x;
   }
   const int pairs_total = p.hkv * npairs;
@@ -190,14 +193,27 @@ struct TileGeom {
   int kt0, nkt;    // this CTA's key tiles: kt0 .. kt0 + nkt - 1
 };
 
+// Key tiles of MMA slot hh and their order.  Prefill: both slots (two query
+// heads) take every tile.  Verify: slot A the tiles kt0, kt0 + 2, ..., slot
+// B kt0 + 1, kt0 + 3, ... (one Q tile, two independent online softmaxes).
+template <bool VERIFY>
+__device__ __forceinline__ int slot_tiles(const TileGeom& gm, int hh) {
+  return VERIFY ? (gm.nkt + 1 - hh) >> 1 : gm.nkt;
+}
+template <bool VERIFY>
+__device__ __forceinline__ int slot_tile(const TileGeom& gm, int jj, int hh) {
+  return VERIFY ? gm.kt0 + 2 * jj + hh : gm.kt0 + jj;
+}
+
 // Prefill: key tiles [0, n / 2) go to CTA 0 of the cluster, [n / 2, n) to
 // CTA 1 (CTA 0 has none when n = 1).  Verify: the key tiles of split sigma
 // (pps pages of the stream each), cut at the tile's last position; a split
 // past it has none.
 template <bool VERIFY>
-__device__ __forceinline__ TileGeom geom_of(const RunInfo& ru, const Tile& x, uint32_t rank) {
+__device__ __forceinline__ TileGeom geom_of(const PrefillParams& p, const RunInfo& ru,
+                                            const Tile& x, uint32_t rank) {
   TileGeom gm;
-  const int rows = VERIFY ? kVerifyRows : kTileRows;
+  const int rows = VERIFY ? kVerifyVectors / p.group : kTileRows;
   gm.row_lo = x.t * rows;
   gm.nrows = min(rows, ru.nrows - gm.row_lo);
   const int maxpos = ru.pos0 + gm.row_lo + gm.nrows - 1;
@@ -219,18 +235,19 @@ __device__ __forceinline__ TileGeom geom_of(const RunInfo& ru, const Tile& x, ui
 // load is off the critical path (two key tiles share a page).
 struct PageCheck {
   const int32_t* pt;
-  int npages, num_pages, next_pid;
+  int npages, num_pages, next_pid, stride;
   bool cur_bad, first;
+  // Tiles j0, j0 + stride, ... (stride 1 or 2), n of them.
   __device__ __forceinline__ PageCheck(const PrefillParams& p, const RunInfo& ru,
-                                       const TileGeom& gm)
+                                       const TileGeom& gm, int j0, int n, int stride_)
       : pt(ru.page_table), npages((gm.kend + kPage - 1) / kPage), num_pages(p.num_pages),
-        next_pid(0), cur_bad(false), first(true) {
-    if (pt && gm.nkt > 0) next_pid = __ldg(pt + (gm.kt0 >> 1));
+        next_pid(0), stride(stride_), cur_bad(false), first(true) {
+    if (pt && n > 0) next_pid = __ldg(pt + (j0 >> 1));
   }
-  // Call for j = kt0, kt0 + 1, ... in order; true if tile j's page is bad.
+  // Call for the tiles in order; true if tile j's page is bad.
   __device__ __forceinline__ bool bad(int j) {
     if (!pt) return false;
-    if ((j & 1) == 0 || first) {
+    if ((j & 1) == 0 || first || stride == 2) {
       first = false;
       const int page = j >> 1;
       cur_bad = (unsigned)next_pid >= (unsigned)num_pages;
@@ -267,22 +284,45 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
   const CUtensorMap* mk = &p.maps[ru.src].k;
   const CUtensorMap* mv = &p.maps[ru.src].v;
   if (gm.nkt == 0) return;
-  // Prefill: slot hh is head h0 + hh, 128 rows (box 64 x 1 x 128).  Verify:
-  // slot hh is head pair 2 hp + hh, 64 rows x its two heads (box 64 x 2 x
-  // 64, landing as M row 2 (row) + head); past the pairs or the rows, the
-  // tile holds other heads' rows or zeros, which no output reads.
-  mbar_arrive_expect_tx(b.q_full, 65536);
-  for (int hh = 0; hh < 2; ++hh) {
-    const int h = VERIFY ? x.g * p.group + 2 * (2 * x.hp + hh) : x.g * p.group + 2 * x.hp + hh;
+  if (VERIFY) {
+    // One Q tile, both slots: 128 / G rows x the group's G heads (box 64 x G
+    // x rows, landing as M row G (row) + head).  Rows past the run hold the
+    // next rows or zeros, which no output reads.
+    const int rt = kVerifyVectors / p.group;
+    mbar_arrive_expect_tx(b.q_full, 2u * 128u * (uint32_t)(p.group * rt));
     for (int rg = 0; rg < 2; ++rg)
-      tma_load_3d(smem + kOffQ + hh * 32768 + rg * 16384, &p.qmap, rg * 64, h,
+      tma_load_3d(smem + kOffQ + rg * 16384, &p.qmap, rg * 64, x.g * p.group,
                   ru.row0 + gm.row_lo, b.q_full);
+  } else {
+    // Slot hh is query head h0 + hh, 128 rows (box 64 x 1 x 128).
+    mbar_arrive_expect_tx(b.q_full, 65536);
+    for (int hh = 0; hh < 2; ++hh)
+      for (int rg = 0; rg < 2; ++rg)
+        tma_load_3d(smem + kOffQ + hh * 32768 + rg * 16384, &p.qmap, rg * 64,
+                    x.g * p.group + 2 * x.hp + hh, ru.row0 + gm.row_lo, b.q_full);
   }
+  // Row coordinate of key tile j in its source; one page lookup per page.  A
+  // bad page id is flagged and a valid page read in its place (its keys are
+  // masked).
   int cached_page = -1, cached_pid = 0;
+  auto row_of = [&](int j) {
+    const int kt = j * kTileKeys;
+    if (!ru.page_table) return x.g * ru.slab_cap + kt;
+    const int page = kt >> 8;
+    if (page != cached_page) {
+      cached_pid = __ldg(ru.page_table + page);
+      cached_page = page;
+      if ((unsigned)cached_pid >= (unsigned)p.num_pages) {
+        flag_error(p.err_flag, kErrBadPage);
+        cached_pid = 0;
+      }
+    }
+    return (cached_pid * p.hkv + x.g) * kPage + (kt & (kPage - 1));
+  };
   int pf_page = -1, pf_pid = 0;
-  auto prefetch = [&](int jj) {             // verify: tile jj of this CTA into L2
-    if (!VERIFY || jj >= gm.nkt) return;
-    const int kt = (gm.kt0 + jj) * kTileKeys;
+  auto prefetch = [&](int j) {              // verify: key tile j into L2
+    if (!VERIFY || j >= gm.kt0 + gm.nkt) return;
+    const int kt = j * kTileKeys;
     int y;
     if (ru.page_table) {
       const int page = kt >> 8;
@@ -302,65 +342,79 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
       tma_prefetch_l2(mv, 64, y);
     }
   };
-  for (int a = 0; a < kAhead; ++a) prefetch(a);
-  int issued_k = 0, issued_v = 0;
-  for (int jj = 0; jj < gm.nkt; ++jj) {     // jj counts this CTA's tiles
-    prefetch(jj + kAhead);
-    const int s = jj & 1;
-    const uint32_t ph = (jj >> 1) & 1;
-    const int kt = (gm.kt0 + jj) * kTileKeys;
-    int y;
-    if (ru.page_table) {
-      const int page = kt >> 8;
-      if (page != cached_page) {          // one lookup per page
-        cached_pid = __ldg(ru.page_table + page);
-        cached_page = page;
-        if ((unsigned)cached_pid >= (unsigned)p.num_pages) {
-          flag_error(p.err_flag, kErrBadPage);
-          cached_pid = 0;                  // read a valid page; its keys are masked
-        }
-      }
-      y = (cached_pid * p.hkv + x.g) * kPage + (kt & (kPage - 1));
-    } else {
-      y = x.g * ru.slab_cap + kt;
-    }
+  // Loads into a 16-bit operand stage (bf16), or into the e4m3 staging
+  // tile (the converters move it on).  The staging tiles see K and V loads
+  // in the order the converters take them.
+  int staged_k = 0, staged_v = 0;       // e4m3: staging loads issued
+  auto load = [&](bool is_v, int stage, uint32_t parity, int y) {
     if (FP8) {
-      // One staging tile each for K and V; the converters free them.
-      if (!mbar_wait_or_abort(b.k8_empty, (jj & 1) ^ 1, p.err_flag, b.abort)) break;
-      mbar_arrive_expect_tx(b.k8_full, 16384);
-      tma_load_2d(smem + kOffK8, mk, 0, y, b.k8_full);
-      issued_k = jj + 1;
-      if (!mbar_wait_or_abort(b.v8_empty, (jj & 1) ^ 1, p.err_flag, b.abort)) break;
-      mbar_arrive_expect_tx(b.v8_full, 16384);
-      tma_load_2d(smem + kOffV8, mv, 0, y, b.v8_full);
-      issued_v = jj + 1;
-    } else {
-      if (!mbar_wait_or_abort(&b.k_empty[s], ph ^ 1, p.err_flag, b.abort)) break;
-      mbar_arrive_expect_tx(&b.k_full[s], 32768);
-      tma_load_2d(smem + kOffK + s * 32768, mk, 0, y, &b.k_full[s]);
-      tma_load_2d(smem + kOffK + s * 32768 + 16384, mk, 64, y, &b.k_full[s]);
-      issued_k = jj + 1;
-      if (!mbar_wait_or_abort(&b.v_empty[s], ph ^ 1, p.err_flag, b.abort)) break;
-      mbar_arrive_expect_tx(&b.v_full[s], 32768);
-      tma_load_2d(smem + kOffV + s * 32768, mv, 0, y, &b.v_full[s]);
-      tma_load_2d(smem + kOffV + s * 32768 + 16384, mv, 64, y, &b.v_full[s]);
-      issued_v = jj + 1;
+      uint64_t* empty = is_v ? b.v8_empty : b.k8_empty;
+      uint64_t* full = is_v ? b.v8_full : b.k8_full;
+      int& n = is_v ? staged_v : staged_k;
+      if (!mbar_wait_or_abort(empty, (n & 1) ^ 1, p.err_flag, b.abort)) return false;
+      mbar_arrive_expect_tx(full, 16384);
+      tma_load_2d(smem + (is_v ? kOffV8 : kOffK8), is_v ? mv : mk, 0, y, full);
+      ++n;
+      return true;
+    }
+    uint64_t* empty = is_v ? &b.v_empty[stage] : &b.k_empty[stage];
+    uint64_t* full = is_v ? &b.v_full[stage] : &b.k_full[stage];
+    if (!mbar_wait_or_abort(empty, parity ^ 1, p.err_flag, b.abort)) return false;
+    uint8_t* dst = smem + (is_v ? kOffV : kOffK) + stage * 32768;
+    mbar_arrive_expect_tx(full, 32768);
+    tma_load_2d(dst, is_v ? mv : mk, 0, y, full);
+    tma_load_2d(dst + 16384, is_v ? mv : mk, 64, y, full);
+    return true;
+  };
+  // Last load issued into each 16-bit stage (phase parity, or -1): an
+  // aborting CTA waits for these before it exits.
+  int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1;
+  auto issued = [&](bool is_v, int stage, uint32_t ph) {
+    int& w = is_v ? (stage ? last_v1 : last_v0) : (stage ? last_k1 : last_k0);
+    w = (int)ph;
+  };
+  if (VERIFY) {
+    // Step jj: slot A's tile kt0 + 2 jj into stage 0, slot B's kt0 + 2 jj + 1
+    // into stage 1; K of both, then V of both.
+    for (int j = gm.kt0; j < gm.kt0 + kAhead; ++j) prefetch(j);
+    bool ok = true;
+    for (int jj = 0; ok && jj < slot_tiles<true>(gm, 0); ++jj) {
+      prefetch(gm.kt0 + 2 * jj + kAhead);
+      prefetch(gm.kt0 + 2 * jj + 1 + kAhead);
+      const uint32_t ph = jj & 1;
+      for (int kv = 0; ok && kv < 2; ++kv)
+        for (int hh = 0; ok && hh < 2; ++hh) {
+          if (jj >= slot_tiles<true>(gm, hh)) continue;
+          ok = load(kv == 1, hh, ph, row_of(slot_tile<true>(gm, jj, hh)));
+          if (ok) issued(kv == 1, hh, ph);
+        }
+    }
+  } else {
+    for (int jj = 0; jj < gm.nkt; ++jj) {   // jj counts this CTA's tiles
+      const int s = jj & 1;
+      const uint32_t ph = (jj >> 1) & 1;
+      const int y = row_of(gm.kt0 + jj);
+      if (!load(false, s, ph, y)) break;
+      issued(false, s, ph);
+      if (!load(true, s, ph, y)) break;
+      issued(true, s, ph);
     }
   }
   if (*b.abort) {
     // Let this CTA's loads in flight land before it exits.
     mbar_wait(b.q_full, 0, p.err_flag);
     if (FP8) {
-      if (issued_k) mbar_wait(b.k8_full, (issued_k - 1) & 1, p.err_flag);
-      if (issued_v) mbar_wait(b.v8_full, (issued_v - 1) & 1, p.err_flag);
+      if (staged_k) mbar_wait(b.k8_full, (staged_k - 1) & 1, p.err_flag);
+      if (staged_v) mbar_wait(b.v8_full, (staged_v - 1) & 1, p.err_flag);
     } else {
-      for (int j = max(0, issued_k - 2); j < issued_k; ++j)
-        mbar_wait(&b.k_full[j & 1], (j >> 1) & 1, p.err_flag);
-      for (int j = max(0, issued_v - 2); j < issued_v; ++j)
-        mbar_wait(&b.v_full[j & 1], (j >> 1) & 1, p.err_flag);
+      if (last_k0 >= 0) mbar_wait(&b.k_full[0], (uint32_t)last_k0, p.err_flag);
+      if (last_k1 >= 0) mbar_wait(&b.k_full[1], (uint32_t)last_k1, p.err_flag);
+      if (last_v0 >= 0) mbar_wait(&b.v_full[0], (uint32_t)last_v0, p.err_flag);
+      if (last_v1 >= 0) mbar_wait(&b.v_full[1], (uint32_t)last_v1, p.err_flag);
     }
   }
 }
+
 
 // Zero rows [z0, 128) of a 16-bit V operand tile (both 64-column halves):
 // keys past the stream's end, or a tile whose page id was bad, must add
@@ -401,39 +455,64 @@ __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, i
   }
 }
 
-// Warps 12-15 for e4m3 caches: staging -> f16 operand stages.
+// Warps 12-15 for e4m3 caches: staging -> f16 operand stages, in the order
+// the producer fills each staging tile.
+template <bool VERIFY>
 __device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileGeom& gm,
                           uint8_t* smem, const Bars& b) {
   const int t = threadIdx.x - kConvWarp0 * 32;   // 0..127
   const int lane = threadIdx.x & 31;
-  PageCheck pc(p, ru, gm);
+  int nk = 0, nv = 0;                            // staging tiles taken
+  // The next staging tile (K, or V with rows from z0 on zeroed: past the
+  // stream's end, or all rows of a bad page) into 16-bit stage s.
+  auto convert = [&](bool is_v, int s, uint32_t ph, int z0) {
+    uint64_t* full8 = is_v ? b.v8_full : b.k8_full;
+    uint64_t* empty8 = is_v ? b.v8_empty : b.k8_empty;
+    uint64_t* empty = is_v ? &b.v_empty[s] : &b.k_empty[s];
+    uint64_t* full = is_v ? &b.v_full[s] : &b.k_full[s];
+    int& n = is_v ? nv : nk;
+    if (!mbar_wait_or_abort(full8, n & 1, p.err_flag, b.abort)) return false;
+    if (!mbar_wait_or_abort(empty, ph ^ 1, p.err_flag, b.abort)) return false;
+    convert_tile(smem + (is_v ? kOffV8 : kOffK8), smem + (is_v ? kOffV : kOffK) + s * 32768,
+                 is_v ? z0 : kTileKeys, t);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(empty8);
+      mbar_arrive(full);
+    }
+    ++n;
+    return true;
+  };
+  if (VERIFY) {
+    PageCheck pc0(p, ru, gm, gm.kt0, slot_tiles<true>(gm, 0), 2);
+    PageCheck pc1(p, ru, gm, gm.kt0 + 1, slot_tiles<true>(gm, 1), 2);
+    bool ok = true;
+    for (int jj = 0; ok && jj < slot_tiles<true>(gm, 0); ++jj) {
+      int z0[2] = {kTileKeys, kTileKeys};
+      for (int hh = 0; hh < 2; ++hh) {
+        if (jj >= slot_tiles<true>(gm, hh)) continue;
+        const int j = slot_tile<true>(gm, jj, hh);
+        z0[hh] = v_zero_from(ru, j, hh ? pc1.bad(j) : pc0.bad(j));
+      }
+      for (int kv = 0; ok && kv < 2; ++kv)
+        for (int hh = 0; ok && hh < 2; ++hh)
+          if (jj < slot_tiles<true>(gm, hh)) ok = convert(kv == 1, hh, jj & 1, z0[hh]);
+    }
+    return;
+  }
+  PageCheck pc(p, ru, gm, gm.kt0, gm.nkt, 1);
   for (int jj = 0; jj < gm.nkt; ++jj) {
     const int j = gm.kt0 + jj;
     const int z0 = v_zero_from(ru, j, pc.bad(j));
     const int s = jj & 1;
     const uint32_t ph = (jj >> 1) & 1;
-    if (!mbar_wait_or_abort(b.k8_full, jj & 1, p.err_flag, b.abort)) return;
-    if (!mbar_wait_or_abort(&b.k_empty[s], ph ^ 1, p.err_flag, b.abort)) return;
-    convert_tile(smem + kOffK8, smem + kOffK + s * 32768, kTileKeys, t);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(b.k8_empty);
-      mbar_arrive(&b.k_full[s]);
-    }
-    if (!mbar_wait_or_abort(b.v8_full, jj & 1, p.err_flag, b.abort)) return;
-    if (!mbar_wait_or_abort(&b.v_empty[s], ph ^ 1, p.err_flag, b.abort)) return;
-    convert_tile(smem + kOffV8, smem + kOffV + s * 32768, z0, t);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(b.v8_empty);
-      mbar_arrive(&b.v_full[s]);
-    }
+    if (!convert(false, s, ph, z0)) return;
+    if (!convert(true, s, ph, z0)) return;
   }
 }
 
-template <bool FP8>
+template <bool FP8, bool VERIFY>
 __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const TileGeom& gm,
                            uint8_t* smem, uint32_t tmem, const Bars& b) {
   const int lane = threadIdx.x & 31;
@@ -444,11 +523,11 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
   const uint32_t kb = smem_u32(smem + kOffK);
   const uint32_t vb = smem_u32(smem + kOffV);
 
-  auto issue_s = [&](int hh, int s) {     // S_hh = Q_hh K_s^T
+  auto issue_s = [&](int hh, int s) {     // S_hh = Q_hh K_s^T (verify: one Q tile)
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-      const uint64_t a = umma::smem_desc_sw128(qb + hh * 32768 + off, 16, 1024);
+      const uint64_t a = umma::smem_desc_sw128(qb + (VERIFY ? 0 : hh * 32768) + off, 16, 1024);
       const uint64_t bd = umma::smem_desc_sw128(kb + s * 32768 + off, 16, 1024);
       umma::mma_ss(tmem + col_s(hh), a, bd, kIdescQK, ks > 0 ? 1u : 0u);
     }
@@ -467,6 +546,65 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
     __syncwarp();
     return;
   }
+  if (VERIFY) {
+    // Slot hh: its tiles' K in stage hh (S_hh), V in stage hh (PV_hh); the
+    // slots alternate, each at its own phase (its step jj).
+    bool ok = mbar_wait_or_abort(b.q_ready, 0, p.err_flag, b.abort);
+    for (int hh = 0; ok && hh < 2; ++hh) {
+      if (slot_tiles<true>(gm, hh) == 0) continue;
+      if (!(ok = mbar_wait_or_abort(&b.k_full[hh], 0, p.err_flag, b.abort))) break;
+      umma::fence_after_sync();
+      if (leader) {
+        issue_s(hh, hh);
+        umma::commit(&b.s_full[hh]);
+        umma::commit(&b.k_empty[hh]);
+      }
+      __syncwarp();
+    }
+    PageCheck pc0(p, ru, gm, gm.kt0, slot_tiles<true>(gm, 0), 2);
+    PageCheck pc1(p, ru, gm, gm.kt0 + 1, slot_tiles<true>(gm, 1), 2);
+    for (int jj = 0; ok && jj < slot_tiles<true>(gm, 0); ++jj) {
+      for (int hh = 0; ok && hh < 2; ++hh) {
+        const int n = slot_tiles<true>(gm, hh);
+        if (jj >= n) continue;
+        const int j = slot_tile<true>(gm, jj, hh);
+        const bool page_bad = hh ? pc1.bad(j) : pc0.bad(j);
+        if (!(ok = mbar_wait_or_abort(&b.v_full[hh], jj & 1, p.err_flag, b.abort))) break;
+        if (!FP8) {
+          const int z0 = v_zero_from(ru, j, page_bad);
+          if (z0 < kTileKeys) zero_v_rows(smem + kOffV + hh * 32768, z0, lane);
+        }
+        if (!(ok = mbar_wait_or_abort(&b.p_ready[hh], jj & 1, p.err_flag, b.abort))) break;
+        umma::fence_after_sync();
+        if (leader) {
+          issue_pv(hh, hh, jj > 0);
+          umma::commit(&b.v_empty[hh]);
+        }
+        __syncwarp();
+        if (jj + 1 < n) {
+          if (!(ok = mbar_wait_or_abort(&b.k_full[hh], (jj + 1) & 1, p.err_flag, b.abort)))
+            break;
+          umma::fence_after_sync();
+          if (leader) {
+            issue_s(hh, hh);
+            umma::commit(&b.s_full[hh]);
+            umma::commit(&b.k_empty[hh]);
+          }
+          __syncwarp();
+        }
+      }
+    }
+    if (leader) {
+      if (ok) {
+        umma::commit(b.o_final);
+      } else {
+        umma::commit(b.drain);        // let issued MMAs finish before TMEM is freed
+        mbar_wait(b.drain, 0, p.err_flag);
+      }
+    }
+    __syncwarp();
+    return;
+  }
   bool ok = mbar_wait_or_abort(b.q_ready, 0, p.err_flag, b.abort) &&
             mbar_wait_or_abort(&b.k_full[0], 0, p.err_flag, b.abort);
   if (ok) {
@@ -480,7 +618,7 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
     }
     __syncwarp();
   }
-  PageCheck pc(p, ru, gm);
+  PageCheck pc(p, ru, gm, gm.kt0, gm.nkt, 1);
   for (int jj = 0; ok && jj < gm.nkt; ++jj) {
     const int j = gm.kt0 + jj;
     const bool page_bad = pc.bad(j);
@@ -588,11 +726,13 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
   const uint32_t tS = tmem + lane_off + col_s(hh);
   const uint32_t tO = tmem + lane_off + col_o(hh);
-  // Verify: TMEM lane r holds query vector (row r / 2, head 2 (pair) + r % 2).
-  const int rho = VERIFY ? r >> 1 : r;                  // row within the tile
-  const int hig = 2 * (2 * x.hp + hh) + (r & 1);        // verify: head within the group
-  const bool valid = rho < gm.nrows && (!VERIFY || hig < p.group);
+  // Verify: TMEM lane r holds query vector (row r / G, head r % G of the
+  // group) in both slots; the slots see alternate key tiles.
+  const int rho = VERIFY ? r / p.group : r;             // row within the tile
+  const int hig = VERIFY ? r - rho * p.group : 0;       // verify: head within the group
+  const bool valid = rho < gm.nrows && (!VERIFY || r < p.group * (kVerifyVectors / p.group));
   const int pos = ru.pos0 + gm.row_lo + (valid ? rho : 0);
+  const int nt = slot_tiles<VERIFY>(gm, hh);             // this slot's key tiles
   // Verify with ancestor masks: key pos - d (d < 64) is visible iff bit d of
   // the row's mask is set; keys further back always are.  Bit-reversed, the
   // mask lines up with key order: key lim - d of a tile is bit 63 - d.
@@ -602,20 +742,30 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
   float sl2 = p.scale_log2;
   bool ok = true;
   if (FP8 && gm.nkt > 0) {
-    ok = mbar_wait_or_abort(b.q_full, 0, p.err_flag, b.abort);
-    if (ok) {
-      const float down = q_row_to_f16(smem + kOffQ + hh * 32768, r);
-      sl2 = p.scale_log2 * down * __ldg(p.k_scale + x.g);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b.q_ready);
+    // Prefill: each slot's warps turn their head's Q rows into f16.  Verify:
+    // slot A's warps turn the one Q tile, publish each row's factor, and
+    // slot B's take it once they see the tile ready.
+    float* down_s = reinterpret_cast<float*>(smem + Layout<FP8>::kOffDown);
+    if (!VERIFY || hh == 0) {
+      ok = mbar_wait_or_abort(b.q_full, 0, p.err_flag, b.abort);
+      if (ok) {
+        const float down = q_row_to_f16(smem + kOffQ + (VERIFY ? 0 : hh * 32768), r);
+        sl2 = p.scale_log2 * down * __ldg(p.k_scale + x.g);
+        if (VERIFY) down_s[r] = down;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b.q_ready);
+      }
+    } else {
+      ok = mbar_wait_or_abort(b.q_ready, 0, p.err_flag, b.abort);
+      if (ok) sl2 = p.scale_log2 * down_s[r] * __ldg(p.k_scale + x.g);
     }
   }
   float m_run = -INFINITY, l = 0.f;
-  PageCheck pc(p, ru, gm);
+  PageCheck pc(p, ru, gm, VERIFY ? gm.kt0 + hh : gm.kt0, nt, VERIFY ? 2 : 1);
 
-  for (int jj = 0; ok && jj < gm.nkt; ++jj) {
-    const int j = gm.kt0 + jj;
+  for (int jj = 0; ok && jj < nt; ++jj) {
+    const int j = slot_tile<VERIFY>(gm, jj, hh);
     const bool page_bad = pc.bad(j);
     if (!(ok = mbar_wait_or_abort(&b.s_full[hh], jj & 1, p.err_flag, b.abort))) break;
     umma::fence_after_sync();
@@ -711,36 +861,61 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
   if (ok) umma::fence_after_sync();
 
   if (VERIFY) {
-    // Split sigma's partial, as the decode partial kernel leaves it: m in
-    // log2 units, l, and O (unnormalised, V scale applied).  A vector that
-    // saw no key here gets m = -inf, l = 0, O = 0.  Every lane takes part in
-    // the TMEM loads; only the stores depend on the row.
-    if (!__all_sync(0xffffffffu, ok)) return;
+    // Merge the two slots (the same query vectors over alternate key tiles)
+    // into split sigma's partial, as the decode partial kernel leaves it: m
+    // in log2 units, l, and O (unnormalised, V scale applied).  Slot B's
+    // threads leave their (m, l) in shared memory; after one barrier of all
+    // eight softmax warps (which every one of them reaches), slot A's read
+    // both slots' O from TMEM (the same lane quarter) and write.  A slot
+    // without tiles counts as m = -inf, l = 0, O = 0.
+    float2* ml_s = reinterpret_cast<float2*>(smem + Layout<FP8>::kOffMl);
+    if (hh == 1) ml_s[r] = make_float2(m_run, l);
+    __syncwarp();
+    named_bar_sync(1, 256);
+    if (hh == 1 || !__all_sync(0xffffffffu, ok)) return;
+    const float2 mlb = ml_s[r];
+    const float mx = fmaxf(m_run, mlb.x);
+    const float a0 = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mx);
+    const float a1 = mlb.x == -INFINITY ? 0.f : fast_exp2(mlb.x - mx);
+    const float vs = FP8 ? __ldg(p.v_scale + x.g) : 1.f;
+    const float c0 = a0 * vs, c1 = a1 * vs;
+    const int nb = slot_tiles<true>(gm, 1);
     const size_t slot =
         ((size_t)(ru.row0 + gm.row_lo + rho) * p.hq + x.g * p.group + hig) * p.max_splits +
         x.sigma;
-    const float vs = FP8 ? __ldg(p.v_scale + x.g) : 1.f;
     float4* po = reinterpret_cast<float4*>(p.part_o + slot * kHeadDim);
+    const uint32_t tOb = tmem + lane_off + col_o(1);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      uint32_t o[32];
-      if (gm.nkt > 0) {
-        umma::tmem_ld32(tO + 32 * c, o);
-        umma::tmem_ld_wait();
+      uint32_t oa[32], ob[32];
+      if (nt > 0) {
+        umma::tmem_ld32(tO + 32 * c, oa);
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0u;
+        for (int i = 0; i < 32; ++i) oa[i] = 0u;
       }
+      if (nb > 0) {
+        umma::tmem_ld32(tOb + 32 * c, ob);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ob[i] = 0u;
+      }
+      umma::tmem_ld_wait();
       if (valid) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          po[8 * c + q] = make_float4(__uint_as_float(o[4 * q]) * vs,
-                                      __uint_as_float(o[4 * q + 1]) * vs,
-                                      __uint_as_float(o[4 * q + 2]) * vs,
-                                      __uint_as_float(o[4 * q + 3]) * vs);
+        for (int q = 0; q < 8; ++q) {
+          float v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            v[e] = __fmaf_rn(__uint_as_float(oa[4 * q + e]), c0,
+                             __fmul_rn(__uint_as_float(ob[4 * q + e]), c1));
+          po[8 * c + q] = make_float4(v[0], v[1], v[2], v[3]);
+        }
       }
     }
-    if (valid) *reinterpret_cast<float2*>(p.part_ml + slot * 2) = make_float2(m_run, l);
+    if (valid)
+      *reinterpret_cast<float2*>(p.part_ml + slot * 2) =
+          make_float2(mx, __fmaf_rn(l, a0, __fmul_rn(mlb.y, a1)));
     return;
   }
 
@@ -855,7 +1030,7 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   if (threadIdx.x == 0) {
     const uint32_t stage_arrivals = FP8 ? kConvWarps : 1;   // the converters, or the producer
     mbar_init(b.q_full, 1);
-    mbar_init(bars + 1, 8);                        // q_ready: the softmax warps
+    mbar_init(bars + 1, VERIFY ? 4 : 8);           // q_ready: the (slot A) softmax warps
     for (int i = 0; i < 2; ++i) {
       mbar_init(&b.k_full[i], stage_arrivals);
       mbar_init(&b.k_empty[i], 1);
@@ -895,21 +1070,21 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   const uint32_t rank = VERIFY ? 0 : cluster_ctarank();
   const Tile x = tile_of<VERIFY>(p, VERIFY ? blockIdx.x : blockIdx.x >> 1);
   const RunInfo& ru = p.runs[x.run];
-  const TileGeom gm = geom_of<VERIFY>(ru, x, rank);
+  const TileGeom gm = geom_of<VERIFY>(p, ru, x, rank);
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kLow));
     if (warp == 0) {
       if (lane == 0) producer<FP8, VERIFY>(p, ru, x, gm, smem, b);
     } else if (warp == 1) {
-      mma_issuer<FP8>(p, ru, gm, smem, tmem, b);
+      mma_issuer<FP8, VERIFY>(p, ru, gm, smem, tmem, b);
     }
   } else if (warp < kConvWarp0) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kHigh));
     softmax_role<FP8, VERIFY>(p, ru, x, gm, rank, (warp - 4) >> 2, smem, tmem, b);
   } else if (FP8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kConv));
-    converter(p, ru, gm, smem, b);
+    converter<VERIFY>(p, ru, gm, smem, b);
   }
   umma::fence_before_sync();
   __syncthreads();

@@ -117,7 +117,7 @@ def test_prefill_slices():
 
 
 def test_verify_tiles_and_mixed_launch_order():
-    """Verify tiles: kv head x pair group x 64-row tile x split, splits of at
+    """Verify tiles: kv head x tile of 128 / G rows x split, splits of at
     least 16 pages; a call with a short and a long run issues the decode
     partial, then the verify launch, then one merge over both."""
     c = _cache()
