@@ -39,7 +39,7 @@ METRIC = "paged decode KV GB/s (% HBM peak); prompt-chunk attn TFLOP/s (% TC pea
 # from ncu (dram__bytes_read.sum + dram__bytes_write.sum, see
 # profiles/decode_partial_batched_decode.md), valid only while the kernel's
 # sources hash to the value it was taken on.
-DECODE_TRAFFIC = {"bytes": 268_591_872 + 4_723_968, "sources_sha256_16": "6f51b467fb3bc848"}
+DECODE_TRAFFIC = {"bytes": 268_614_656 + 4_640_000, "sources_sha256_16": "c1ed5addc80cc3a2"}
 DECODE_SOURCES = ["paged_kv_cache_235_gb300/csrc/decode.cu",
                   "paged_kv_cache_235_gb300/csrc/common.cuh",
                   "paged_kv_cache_235_gb300/csrc/params.h",

@@ -70,15 +70,13 @@ struct Cfg {
   static constexpr int kKS = kKeysPerWarp / 16;        // PV k-steps per warp
 };
 
-// A work item: (run, kv head g, m-tile mt, split sigma).  In a wide run an
-// item covers the four m-tiles 4 mt .. 4 mt + 3 (one per consumer warp pair).
+// A work item: (run, kv head g, m-tile mt of 16 query vectors, split sigma).
 struct Item {
   int run, g, mt, sigma;
 };
 
-__device__ __forceinline__ int mtile_groups(const RunInfo& ru, int group) {
-  const int mtiles = (ru.nrows * group + 15) >> 4;
-  return ru.wide ? (mtiles + 3) >> 2 : mtiles;
+__device__ __forceinline__ int mtiles_of(const RunInfo& ru, int group) {
+  return (ru.nrows * group + 15) >> 4;
 }
 
 __device__ __forceinline__ Item item_of(const DecodeParams& p, int it) {
@@ -86,7 +84,7 @@ __device__ __forceinline__ Item item_of(const DecodeParams& p, int it) {
   while (r + 1 < p.nruns && p.runs[r + 1].item0 <= it) ++r;
   const RunInfo& ru = p.runs[r];
   int local = it - ru.item0;
-  const int mgroups = mtile_groups(ru, p.group);
+  const int mgroups = mtiles_of(ru, p.group);
   Item x;
   x.run = r;
   x.sigma = local % ru.nsplit;
@@ -110,7 +108,7 @@ __device__ __forceinline__ void item_keys(const DecodeParams& p, const Item& x, 
                                           int& khi) {
   const RunInfo& ru = p.runs[x.run];
   const int nq = ru.nrows * p.group;
-  const int last_qv = min((ru.wide ? 64 * x.mt + 63 : 16 * x.mt + 15), nq - 1);
+  const int last_qv = min(16 * x.mt + 15, nq - 1);
   const int maxpos = ru.pos0 + last_qv / p.group;
   klo = x.sigma * ru.pps * kPage;
   khi = min(min(klo + ru.pps * kPage, ru.seq_len), maxpos + 1);
@@ -252,19 +250,19 @@ struct CombBars {
   uint64_t* done;        // the combiners finished the item (fold buffer free)
 };
 
-// One block of this warp's keys: NSB sub-blocks of kKeysPerWarp keys from key
-// wk0 of the stage chunk at sb (k0 = the chunk's first key): scores, the
-// causal or ancestor mask, the online softmax, and O += P V.
-template <bool FP8, bool GEN, int NSB>
+// This warp's kKeysPerWarp keys from key wk0 of the stage chunk at sb (k0 =
+// the chunk's first key): scores, the causal or ancestor mask, the online
+// softmax, and O += P V.
+template <bool FP8, bool GEN>
 __device__ __forceinline__ void attend_block(uint32_t sb, int wk0, int k0, int seq_len,
                                              const uint32_t (&qr)[2][16], const int (&lim)[2],
                                              const float (&sc)[2], const uint64_t (&anc)[2],
                                              int tree_low, int gq, int c, float (&m_run)[2],
                                              float (&l_run)[2], float (&o)[16][4]) {
   using C = Cfg<FP8>;
-  constexpr int kNT = C::kNT * NSB;       // score n-tiles
-  constexpr int kKS = C::kKS * NSB;       // PV k-steps
-  constexpr int kKeys = C::kKeysPerWarp * NSB;
+  constexpr int kNT = C::kNT;             // score n-tiles
+  constexpr int kKS = C::kKS;             // PV k-steps
+  constexpr int kKeys = C::kKeysPerWarp;
   const int key_base = k0 + wk0;
   // ---- S = Q K^T over this warp's keys
   float s[kNT][4];
@@ -451,16 +449,10 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
     const RunInfo& ru = p.runs[x.run];
     int klo, khi;
     item_keys(p, x, klo, khi);
-    // The m-tile this warp works on, and its key sub-blocks in every stage
-    // chunk: a narrow item splits the chunk's 8 sub-blocks of kKeysPerWarp
-    // keys over the 8 warps; a wide item gives warps w and w + 4 m-tile
-    // 4 mt + (w & 3) and 4 sub-blocks each (the two halves of the chunk).
-    const bool wide = GEN && ru.wide;
-    const int sub0 = wide ? (warp >> 2) * 4 : warp;
-    Item xq = x;
-    if (wide) xq.mt = 4 * x.mt + (warp & 3);
-    if (x.run != q_run || x.g != q_g || xq.mt != q_mt) {
-      load_q<FP8, GEN>(p, ru, xq, gq, c, qr, lim, anc, sc);
+    // The chunk's 8 sub-blocks of kKeysPerWarp keys go to the 8 warps.
+    const int sub0 = warp;
+    if (x.run != q_run || x.g != q_g || x.mt != q_mt) {
+      load_q<FP8, GEN>(p, ru, x, gq, c, qr, lim, anc, sc);
       maxlim = __reduce_max_sync(0xffffffffu, max(lim[0], lim[1]));
       if (GEN && p.anc) {
         const int mn = min(lim[0] >= 0 ? lim[0] : INT_MAX, lim[1] >= 0 ? lim[1] : INT_MAX);
@@ -468,7 +460,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
       }
       q_run = x.run;
       q_g = x.g;
-      q_mt = xq.mt;
+      q_mt = x.mt;
     }
 
     float m_run[2] = {-INFINITY, -INFINITY};
@@ -482,21 +474,10 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
       const uint32_t ph = (stage / kStages) & 1;
       if (!mbar_wait(&full[buf], ph, p.err_flag)) return;
       const uint32_t sb = sbase + (uint32_t)buf * kStageBytes;
-      if (!wide) {
-        const int wk0 = sub0 * C::kKeysPerWarp;
-        if (!stage_bad[buf] && k0 + wk0 <= maxlim)
-          attend_block<FP8, GEN, 1>(sb, wk0, k0, ru.seq_len, qr, lim, sc, anc, tree_low, gq, c,
-                                    m_run, l_run, o);
-      } else {
-        // a wide item: this warp's four sub-blocks as two blocks of two, for
-        // more independent work per step than four sequential sub-blocks
-        for (int bb = 0; bb < 2; ++bb) {
-          const int wk0 = (sub0 + 2 * bb) * C::kKeysPerWarp;
-          if (!stage_bad[buf] && k0 + wk0 <= maxlim)
-            attend_block<FP8, GEN, 2>(sb, wk0, k0, ru.seq_len, qr, lim, sc, anc, tree_low, gq, c,
-                                      m_run, l_run, o);
-        }
-      }
+      const int wk0 = sub0 * C::kKeysPerWarp;
+      if (!stage_bad[buf] && k0 + wk0 <= maxlim)
+        attend_block<FP8, GEN>(sb, wk0, k0, ru.seq_len, qr, lim, sc, anc, tree_low, gq, c,
+                               m_run, l_run, o);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[buf]);
     }
@@ -572,8 +553,7 @@ __device__ void combiner(const DecodeParams& p, uint32_t tmem, float4* fold, flo
     umma::tmem_ld4(tB + 64, mlB);
     umma::tmem_ld_wait();
     if (rel > 0 && !mbar_wait(bars.done, par ^ 1u, p.err_flag)) return;
-    const bool wide = GEN && ru.wide;
-    if (!wide && c == 0) {
+    if (c == 0) {
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int row = gq + 8 * hr;
@@ -586,76 +566,6 @@ __device__ void combiner(const DecodeParams& p, uint32_t tmem, float4* fold, flo
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.pub);
     if (!mbar_wait(bars.pub, par, p.err_flag)) return;
-    if (wide) {
-      // A wide item: consumer warps q and q + 4 hold the only two states of
-      // m-tile 4 mt + q, so their fold is that m-tile's partial.  Same
-      // barriers as a narrow item (their phases count every item).
-      const int mtq = 4 * x.mt + q;
-      float Mw[2], Aw[2], Bw[2], Lw[2];
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const float mA = __uint_as_float(mlA[2 * hr]), lA = __uint_as_float(mlA[2 * hr + 1]);
-        const float mB = __uint_as_float(mlB[2 * hr]), lB = __uint_as_float(mlB[2 * hr + 1]);
-        Mw[hr] = fmaxf(mA, mB);
-        Aw[hr] = mA == -INFINITY ? 0.f : fast_exp2(mA - Mw[hr]);
-        Bw[hr] = mB == -INFINITY ? 0.f : fast_exp2(mB - Mw[hr]);
-        Lw[hr] = __fmaf_rn(Bw[hr], lB, __fmul_rn(Aw[hr], lA));
-      }
-      const float vs = FP8 ? __ldg(p.v_scale + x.g) : 1.f;
-      float* orow[2] = {nullptr, nullptr};
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int qv = mtq * 16 + gq + 8 * hr;
-        if (qv >= nq) continue;
-        const int r = qv / p.group;
-        const int h = x.g * p.group + (qv - r * p.group);
-        const size_t pslot = ((size_t)(ru.row0 + r) * p.hq + h) * p.max_splits + x.sigma;
-        orow[hr] = p.part_o + pslot * kHeadDim;
-        if (c == 0) {
-          p.part_ml[pslot * 2 + 0] = Mw[hr];
-          p.part_ml[pslot * 2 + 1] = Lw[hr];
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t xa[16], xb[16];
-        umma::tmem_ld16(tA + 16 * k, xa);
-        umma::tmem_ld16(tB + 16 * k, xb);
-        umma::tmem_ld_wait();
-        float v[4][4];                       // [n-tile 4k + u][fragment element j]
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int i = 4 * u + j, hr = j >> 1;
-            v[u][j] = __fmaf_rn(Bw[hr], __uint_as_float(xb[i]),
-                                __fmul_rn(Aw[hr], __uint_as_float(xa[i]))) * vs;
-          }
-        }
-        // fragment element j = 2 hr + e of n-tiles 4k..4k+3 lies in four
-        // consecutive columns starting at out_col(4k, 2c + e)
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          if (!orow[hr]) continue;
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int j = 2 * hr + e;
-            *reinterpret_cast<float4*>(orow[hr] + out_col<FP8>(4 * k, 2 * c + e)) =
-                make_float4(v[0][j], v[1][j], v[2][j], v[3][j]);
-          }
-        }
-      }
-      umma::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars.tmem_free[b]);
-        mbar_arrive(bars.folded);
-      }
-      if (!mbar_wait(bars.folded, par, p.err_flag)) return;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars.done);
-      continue;
-    }
     float M[2], aA[2], aB[2];
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
@@ -894,11 +804,9 @@ cudaError_t launch_partial(const DecodeParams& p, int grid, cudaStream_t s) {
 
 cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cudaStream_t s) {
   if (grid <= 0 || p.n_items == 0) return cudaSuccess;
-  // Rows with ancestor masks, or runs of wide items, take the general
-  // instantiation, so the plain causal calls keep their own kernel's code.
-  bool gen = p.anc != nullptr;
-  for (int r = 0; r < p.nruns; ++r) gen = gen || p.runs[r].wide;
-  if (gen)
+  // Rows with ancestor masks take the general instantiation, so the plain
+  // causal calls keep their own kernel's code.
+  if (p.anc)
     return fp8 ? launch_partial<true, true>(p, grid, s) : launch_partial<false, true>(p, grid, s);
   return fp8 ? launch_partial<true, false>(p, grid, s) : launch_partial<false, false>(p, grid, s);
 }

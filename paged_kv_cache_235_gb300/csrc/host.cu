@@ -292,16 +292,15 @@ void fill_run(RunInfo& ri, const tfpa_seg& g, int src, int row0, int nrows, int 
   ri.pps = tfpa_pages_per_split(g.seq_len);
   ri.item0 = 0;
   ri.slab_cap = g.page_table ? 0 : g.slab_cap;
-  ri.wide = 0;
+  ri.pad_ = 0;
 }
 
-// Key stages of decode work item (m-tile mt, or m-tile group mt of a wide
-// run, split sigma) of a run: its split's keys, cut at the stream's end and
-// at the last position of the item's rows (the kernel's item key range, in
-// units of the kernel's chunk).
+// Key stages of decode work item (m-tile mt, split sigma) of a run: its
+// split's keys, cut at the stream's end and at the last position of the
+// item's rows (the kernel's item key range, in units of the kernel's chunk).
 int item_stages(const RunInfo& ri, int G, int mt, int sigma, int chunk) {
   const int nq = ri.nrows * G;
-  const int last_qv = std::min(ri.wide ? 64 * mt + 63 : 16 * mt + 15, nq - 1);
+  const int last_qv = std::min(16 * mt + 15, nq - 1);
   const int maxpos = ri.pos0 + last_qv / G;
   const int klo = sigma * ri.pps * kPage;
   const int khi = std::min(std::min(klo + ri.pps * kPage, ri.seq_len), maxpos + 1);
@@ -319,12 +318,10 @@ void plan_cta_ranges(DecodeParams& p, int nr, int G, bool fp8, int grid) {
     for (int r = 0; r < nr; ++r) {
       const RunInfo& ri = p.runs[r];
       const int mtiles = (ri.nrows * G + 15) / 16;
-      const int mgroups = ri.wide ? (mtiles + 3) / 4 : mtiles;
-      const int64_t per_stage = ri.wide ? 2 : 1;    // a wide item computes 4 m-tiles a stage
       for (int g = 0; g < p.hkv; ++g)
-        for (int mt = 0; mt < mgroups; ++mt)
+        for (int mt = 0; mt < mtiles; ++mt)
           for (int sg = 0; sg < ri.nsplit; ++sg)
-            fn(per_stage * item_stages(ri, G, mt, sg, chunk) + kItemCost);
+            fn(item_stages(ri, G, mt, sg, chunk) + kItemCost);
     }
   };
   int64_t total = 0;
@@ -381,7 +378,8 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
   // per tile), the rest to the decode partial kernel.  Decided on the
   // call's whole run, so every slice of it computes its rows with the same
   // arithmetic (slices give the same bytes as one launch).  A group wider
-  // than a tile keeps the decode kernel's wide items.
+  // than a tile (more than 128 query heads per kv head) stays on the decode
+  // kernel.
   const bool verify_ok = G <= kVerifyVectors;
   auto is_wide = [&](const Run& r) { return (r.nrows * G + 15) / 16 >= 4; };
   const int vrows = verify_ok ? kVerifyVectors / G : 1;   // rows of a verify tile
@@ -410,11 +408,7 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
         RunInfo& info = p.runs[nd++];
         fill_run(info, g, src, nrows, take, r.pos0 + taken);
         info.item0 = items;
-        // Wide items (one cache head per query head only): four m-tiles
-        // share each K/V stage instead of reading it once each.
-        const int mtiles = (take * G + 15) / 16;
-        info.wide = is_wide(r) ? 1 : 0;
-        items += c->hkv * (info.wide ? (mtiles + 3) / 4 : mtiles) * info.nsplit;
+        items += c->hkv * ((take * G + 15) / 16) * info.nsplit;
         mp.runs[nr] = MergeRun{nrows, take, info.nsplit, 0};
       }
       ++nr;

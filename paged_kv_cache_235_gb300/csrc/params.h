@@ -38,7 +38,7 @@ struct RunInfo {
   int32_t pps;                // decode and verify: pages per split
   int32_t item0;              // first work item of this run
   int32_t slab_cap;           // slab capacity in positions (slab runs)
-  int32_t wide;               // decode: an item covers four m-tiles (runs of >= 4 m-tiles)
+  int32_t pad_;
 };
 
 struct DecodeParams {
