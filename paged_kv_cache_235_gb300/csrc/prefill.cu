@@ -60,6 +60,16 @@ constexpr int kOffK = 65536;             // 2 stages x 32 KB (16-bit operand til
 constexpr int kOffV = 131072;            // 2 stages x 32 KB
 constexpr int kOffK8 = 196608;           // e4m3 staging: one K tile, 16 KB
 constexpr int kOffV8 = 212992;           // e4m3 staging: one V tile, 16 KB
+// Verify mode uses only the first Q tile (32 KB); the second holds a second
+// e4m3 staging tile each for K and V, so the producer can fetch the next
+// tile while the converters work on the last.
+constexpr int kOffK8b = 32768;
+constexpr int kOffV8b = 49152;
+constexpr int kStage8Bar = 14;
+template <bool VERIFY>
+__device__ __forceinline__ int stage8_off(bool is_v, int i) {
+  return i ? (is_v ? kOffV8b : kOffK8b) : (is_v ? kOffV8 : kOffK8);
+}
 template <bool FP8>
 struct Layout {
   static constexpr int kOffBar = FP8 ? 229376 : 196608;
@@ -135,8 +145,8 @@ struct Bars {
   uint64_t* k_empty;     // [2]
   uint64_t* v_full;      // [2]
   uint64_t* v_empty;     // [2]
-  uint64_t* k8_full;     // e4m3 staging landed / free
-  uint64_t* k8_empty;
+  uint64_t* k8_full;     // e4m3 staging tile 0 landed / free; tile 1's barriers
+  uint64_t* k8_empty;    // (verify only) follow kStage8Bar barriers later
   uint64_t* v8_full;
   uint64_t* v8_empty;
   uint64_t* s_full;      // [2] per head: S in TMEM
@@ -348,12 +358,15 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
   int staged_k = 0, staged_v = 0;       // e4m3: staging loads issued
   auto load = [&](bool is_v, int stage, uint32_t parity, int y) {
     if (FP8) {
-      uint64_t* empty = is_v ? b.v8_empty : b.k8_empty;
-      uint64_t* full = is_v ? b.v8_full : b.k8_full;
+      // staging tile n & 1 (verify) or 0, at the phase of its own count
       int& n = is_v ? staged_v : staged_k;
-      if (!mbar_wait_or_abort(empty, (n & 1) ^ 1, p.err_flag, b.abort)) return false;
+      const int i = VERIFY ? (n & 1) : 0;
+      const uint32_t ph8 = VERIFY ? ((n >> 1) & 1) : (n & 1);
+      uint64_t* empty = (is_v ? b.v8_empty : b.k8_empty) + i * kStage8Bar;
+      uint64_t* full = (is_v ? b.v8_full : b.k8_full) + i * kStage8Bar;
+      if (!mbar_wait_or_abort(empty, ph8 ^ 1, p.err_flag, b.abort)) return false;
       mbar_arrive_expect_tx(full, 16384);
-      tma_load_2d(smem + (is_v ? kOffV8 : kOffK8), is_v ? mv : mk, 0, y, full);
+      tma_load_2d(smem + stage8_off<VERIFY>(is_v, i), is_v ? mv : mk, 0, y, full);
       ++n;
       return true;
     }
@@ -404,8 +417,12 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
     // Let this CTA's loads in flight land before it exits.
     mbar_wait(b.q_full, 0, p.err_flag);
     if (FP8) {
-      if (staged_k) mbar_wait(b.k8_full, (staged_k - 1) & 1, p.err_flag);
-      if (staged_v) mbar_wait(b.v8_full, (staged_v - 1) & 1, p.err_flag);
+      for (int n = max(0, staged_k - (VERIFY ? 2 : 1)); n < staged_k; ++n)
+        mbar_wait(b.k8_full + (VERIFY ? (n & 1) : 0) * kStage8Bar,
+                  VERIFY ? ((n >> 1) & 1) : (n & 1), p.err_flag);
+      for (int n = max(0, staged_v - (VERIFY ? 2 : 1)); n < staged_v; ++n)
+        mbar_wait(b.v8_full + (VERIFY ? (n & 1) : 0) * kStage8Bar,
+                  VERIFY ? ((n >> 1) & 1) : (n & 1), p.err_flag);
     } else {
       if (last_k0 >= 0) mbar_wait(&b.k_full[0], (uint32_t)last_k0, p.err_flag);
       if (last_k1 >= 0) mbar_wait(&b.k_full[1], (uint32_t)last_k1, p.err_flag);
@@ -466,14 +483,16 @@ __device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileG
   // The next staging tile (K, or V with rows from z0 on zeroed: past the
   // stream's end, or all rows of a bad page) into 16-bit stage s.
   auto convert = [&](bool is_v, int s, uint32_t ph, int z0) {
-    uint64_t* full8 = is_v ? b.v8_full : b.k8_full;
-    uint64_t* empty8 = is_v ? b.v8_empty : b.k8_empty;
+    int& n = is_v ? nv : nk;
+    const int i = VERIFY ? (n & 1) : 0;
+    const uint32_t ph8 = VERIFY ? ((n >> 1) & 1) : (n & 1);
+    uint64_t* full8 = (is_v ? b.v8_full : b.k8_full) + i * kStage8Bar;
+    uint64_t* empty8 = (is_v ? b.v8_empty : b.k8_empty) + i * kStage8Bar;
     uint64_t* empty = is_v ? &b.v_empty[s] : &b.k_empty[s];
     uint64_t* full = is_v ? &b.v_full[s] : &b.k_full[s];
-    int& n = is_v ? nv : nk;
-    if (!mbar_wait_or_abort(full8, n & 1, p.err_flag, b.abort)) return false;
+    if (!mbar_wait_or_abort(full8, ph8, p.err_flag, b.abort)) return false;
     if (!mbar_wait_or_abort(empty, ph ^ 1, p.err_flag, b.abort)) return false;
-    convert_tile(smem + (is_v ? kOffV8 : kOffK8), smem + (is_v ? kOffV : kOffK) + s * 32768,
+    convert_tile(smem + stage8_off<VERIFY>(is_v, i), smem + (is_v ? kOffV : kOffK) + s * 32768,
                  is_v ? z0 : kTileKeys, t);
     fence_proxy_async_smem();
     __syncwarp();
@@ -1013,10 +1032,11 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   b.k_empty = bars + 4;
   b.v_full = bars + 6;
   b.v_empty = bars + 8;
-  b.k8_full = bars + 10;
+  b.k8_full = bars + 10;        // tile 1: bars + 24 .. 27
   b.k8_empty = bars + 11;
   b.v8_full = bars + 12;
   b.v8_empty = bars + 13;
+  static_assert(10 + kStage8Bar == 24, "staging tile 1 barriers");
   b.s_full = bars + 14;
   b.p_ready = bars + 16;
   b.o_final = bars + 18;
@@ -1039,10 +1059,12 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
       mbar_init(&b.s_full[i], 1);
       mbar_init(&b.p_ready[i], 4);
     }
-    mbar_init(b.k8_full, 1);
-    mbar_init(b.k8_empty, kConvWarps);
-    mbar_init(b.v8_full, 1);
-    mbar_init(b.v8_empty, kConvWarps);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b.k8_full + i * kStage8Bar, 1);
+      mbar_init(b.k8_empty + i * kStage8Bar, kConvWarps);
+      mbar_init(b.v8_full + i * kStage8Bar, 1);
+      mbar_init(b.v8_empty + i * kStage8Bar, kConvWarps);
+    }
     mbar_init(b.o_final, 1);
     mbar_init(b.drain, 1);
     mbar_init(b.peer_ready, 256);                  // every softmax thread of CTA 1
