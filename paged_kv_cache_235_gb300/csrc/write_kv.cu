@@ -169,10 +169,26 @@ __global__ void __launch_bounds__(kKeepThreads)
     dst_row[i >> 1][i & 1] = d;
   }
   __syncthreads();
+  // Each thread issues its (up to) kUnroll loads before any shared store, so
+  // they are in flight together rather than one round trip each.
+  constexpr int kUnroll = 8;
   const int total = p.n * 2 * cpr;
-  for (int i = threadIdx.x; i < total; i += blockDim.x) {
-    const uint4* s = src_row[i / (2 * cpr)][(i / cpr) & 1];
-    stash[i] = s ? s[i % cpr] : make_uint4(0, 0, 0, 0);
+  for (int i0 = threadIdx.x; i0 < total; i0 += kUnroll * blockDim.x) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 + u * blockDim.x;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (i < total) {
+        const uint4* s = src_row[i / (2 * cpr)][(i / cpr) & 1];
+        if (s) v[u] = s[i % cpr];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < total) stash[i] = v[u];
+    }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < total; i += blockDim.x) {
