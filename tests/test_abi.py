@@ -136,6 +136,28 @@ def test_verify_tiles_and_mixed_launch_order():
     assert rec[0]["items"] == 8 * 1 * B.tfpa_num_splits(L)   # 4 vectors: one m-tile
 
 
+@pytest.mark.parametrize("hq,hkv,rows,kind,count", [
+    (32, 8, 12, "partial", 8 * 3 * 32),    # 48 vectors a kv head: decode items
+    (32, 8, 13, "verify", 8 * 1 * 16),     # 52 vectors: 32-row tiles, 16 splits
+    (8, 8, 49, "verify", 8 * 1 * 16),      # one head a group: 128-row tiles
+    (24, 8, 20, "verify", 8 * 1 * 16),     # three heads: 42-row tiles
+    (64, 8, 20, "verify", 8 * 2 * 16),     # eight heads: 16-row tiles, two of them
+    (129, 1, 1, "partial", 1 * 9 * 32),    # a group wider than a tile: decode items
+])
+def test_kernel_choice_by_query_vectors(hq, hkv, rows, kind, count):
+    """Which kernel a run takes depends on its query vectors per kv head only:
+    49 or more (and at most 128 heads a group) go to the verify kernel, whose
+    tiles hold 128 / G rows; the items or tiles count follows."""
+    c = _cache(hq, hkv)
+    L = 65536
+    segs = [B.Seg(L, page_table=3 * FAKE)]
+    with B.record_launches() as rec:
+        B.tfpa_decode(c, segs, 4 * FAKE, np.zeros(rows), np.arange(L - rows, L), 0.088,
+                      B.Scratch(5 * FAKE, 6 * FAKE, 128), 7 * FAKE)
+    assert [r["kind"] for r in rec] == [kind, "merge"]
+    assert rec[0]["items"] == count
+
+
 def test_write_kv_one_launch_per_64_runs():
     c = _cache()
     segs = [B.Seg(1000, page_table=3 * FAKE) for _ in range(100)]
