@@ -34,11 +34,15 @@
 // With an e4m3 cache the MMAs run in f16: each softmax thread first turns its
 // Q row into f16 scaled by a power of two (exact for every element within
 // 2^28 of the row's largest), and the K and V scales are applied to the
-// scores and to the output.
+// scores and to the output.  Verify tiles on an e4m3 cache instead split Q
+// into two e4m3 tiles (hi + lo) and take S from 8-bit MMAs straight off the
+// e4m3 K tiles, so only V passes through the converters.
 // TMEM (512 columns): S_A [0,128) O_A [128,256) S_B [256,384) O_B [384,512).
 // CTA 1's partial lands in CTA 0's shared memory once CTA 0's MMAs are done:
 // O (float32 [2 heads][128 rows][128], 16-byte chunks permuted by row against
 // bank conflicts) over the K and V rings, (m, l) over the Q tiles.
+#include <cuda_fp8.h>
+
 #include "cluster.cuh"
 #include "common.cuh"
 #include "params.h"
@@ -60,16 +64,22 @@ constexpr int kOffK = 65536;             // 2 stages x 32 KB (16-bit operand til
 constexpr int kOffV = 131072;            // 2 stages x 32 KB
 constexpr int kOffK8 = 196608;           // e4m3 staging: one K tile, 16 KB
 constexpr int kOffV8 = 212992;           // e4m3 staging: one V tile, 16 KB
-// Verify mode uses only the first Q tile (32 KB); the second holds a second
-// e4m3 staging tile each for K and V, so the producer can fetch the next
-// tile while the converters work on the last.
+// Verify mode uses only the first Q tile (32 KB).  With a bf16 cache the
+// second is unused.  With an e4m3 cache the Q tile becomes two e4m3 tiles
+// (hi and lo, 16 KB each) that feed 8-bit MMAs with K straight from its
+// e4m3 stages: four of 16 KB over the 16-bit K region, two per slot.  V
+// still goes through the converters, from four e4m3 staging tiles (two per
+// slot): the prefill staging pair and the second Q tile.
 constexpr int kOffK8b = 32768;
 constexpr int kOffV8b = 49152;
-constexpr int kStage8Bar = 14;
-template <bool VERIFY>
 __device__ __forceinline__ int stage8_off(bool is_v, int i) {
   return i ? (is_v ? kOffV8b : kOffK8b) : (is_v ? kOffV8 : kOffK8);
 }
+// Verify, e4m3: V staging tile i (2 x slot + step parity) and K stage i.
+__device__ __forceinline__ int vstage8_off(int i) {
+  return i < 2 ? kOffK8 + i * 16384 : kOffK8b + (i - 2) * 16384;
+}
+__device__ __forceinline__ int kstage8_off(int i) { return kOffK + i * 16384; }
 template <bool FP8>
 struct Layout {
   static constexpr int kOffBar = FP8 ? 229376 : 196608;
@@ -141,14 +151,14 @@ __device__ __forceinline__ uint32_t col_o(int hh) { return hh ? 384u : 128u; }
 struct Bars {
   uint64_t* q_full;      // Q tiles landed (TMA)
   uint64_t* q_ready;     // Q operand ready for the MMA (e4m3 caches: after conversion)
-  uint64_t* k_full;      // [2] K operand stage ready
-  uint64_t* k_empty;     // [2]
+  uint64_t* k_full;      // [2] K operand stage ready (verify, e4m3: [4])
+  uint64_t* k_empty;     // [2] (verify, e4m3: [4])
   uint64_t* v_full;      // [2]
   uint64_t* v_empty;     // [2]
-  uint64_t* k8_full;     // e4m3 staging tile 0 landed / free; tile 1's barriers
-  uint64_t* k8_empty;    // (verify only) follow kStage8Bar barriers later
-  uint64_t* v8_full;
-  uint64_t* v8_empty;
+  uint64_t* k8_full;     // prefill, e4m3: the staging tile landed / free
+  uint64_t* k8_empty;
+  uint64_t* v8_full;     // (verify, e4m3: [4])
+  uint64_t* v8_empty;    // (verify, e4m3: [4])
   uint64_t* s_full;      // [2] per head: S in TMEM
   uint64_t* p_ready;     // [2] per head: P in TMEM, O corrected
   uint64_t* o_final;
@@ -352,21 +362,17 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
       tma_prefetch_l2(mv, 64, y);
     }
   };
-  // Loads into a 16-bit operand stage (bf16), or into the e4m3 staging
-  // tile (the converters move it on).  The staging tiles see K and V loads
-  // in the order the converters take them.
+  // Loads into a 16-bit operand stage (bf16), or (prefill, e4m3) into the
+  // staging tile that the converters move on, K and V in their order.
   int staged_k = 0, staged_v = 0;       // e4m3: staging loads issued
   auto load = [&](bool is_v, int stage, uint32_t parity, int y) {
     if (FP8) {
-      // staging tile n & 1 (verify) or 0, at the phase of its own count
       int& n = is_v ? staged_v : staged_k;
-      const int i = VERIFY ? (n & 1) : 0;
-      const uint32_t ph8 = VERIFY ? ((n >> 1) & 1) : (n & 1);
-      uint64_t* empty = (is_v ? b.v8_empty : b.k8_empty) + i * kStage8Bar;
-      uint64_t* full = (is_v ? b.v8_full : b.k8_full) + i * kStage8Bar;
-      if (!mbar_wait_or_abort(empty, ph8 ^ 1, p.err_flag, b.abort)) return false;
+      uint64_t* empty = is_v ? b.v8_empty : b.k8_empty;
+      uint64_t* full = is_v ? b.v8_full : b.k8_full;
+      if (!mbar_wait_or_abort(empty, (n & 1) ^ 1, p.err_flag, b.abort)) return false;
       mbar_arrive_expect_tx(full, 16384);
-      tma_load_2d(smem + stage8_off<VERIFY>(is_v, i), is_v ? mv : mk, 0, y, full);
+      tma_load_2d(smem + stage8_off(is_v, 0), is_v ? mv : mk, 0, y, full);
       ++n;
       return true;
     }
@@ -386,7 +392,34 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
     int& w = is_v ? (stage ? last_v1 : last_v0) : (stage ? last_k1 : last_k0);
     w = (int)ph;
   };
-  if (VERIFY) {
+  if (VERIFY && FP8) {
+    // Step jj, slot hh: K into e4m3 stage 2 hh + (jj & 1), V into staging
+    // tile 2 hh + (jj & 1), each at phase (jj >> 1) & 1; K of both slots,
+    // then V of both.  last_k*, last_v*: each slot's last step loaded.
+    for (int j = gm.kt0; j < gm.kt0 + kAhead; ++j) prefetch(j);
+    bool ok = true;
+    for (int jj = 0; ok && jj < slot_tiles<true>(gm, 0); ++jj) {
+      prefetch(gm.kt0 + 2 * jj + kAhead);
+      prefetch(gm.kt0 + 2 * jj + 1 + kAhead);
+      const uint32_t ph = (jj >> 1) & 1;
+      for (int kv = 0; ok && kv < 2; ++kv)
+        for (int hh = 0; ok && hh < 2; ++hh) {
+          if (jj >= slot_tiles<true>(gm, hh)) continue;
+          const int i = 2 * hh + (jj & 1);
+          uint64_t* empty = kv ? b.v8_empty + i : b.k_empty + i;
+          uint64_t* full = kv ? b.v8_full + i : b.k_full + i;
+          const int y = row_of(slot_tile<true>(gm, jj, hh));
+          if (!(ok = mbar_wait_or_abort(empty, ph ^ 1, p.err_flag, b.abort))) break;
+          mbar_arrive_expect_tx(full, 16384);
+          tma_load_2d(smem + (kv ? vstage8_off(i) : kstage8_off(i)), kv ? mv : mk, 0, y, full);
+          if (kv) {
+            (hh ? last_v1 : last_v0) = jj;
+          } else {
+            (hh ? last_k1 : last_k0) = jj;
+          }
+        }
+    }
+  } else if (VERIFY) {
     // Step jj: slot A's tile kt0 + 2 jj into stage 0, slot B's kt0 + 2 jj + 1
     // into stage 1; K of both, then V of both.
     for (int j = gm.kt0; j < gm.kt0 + kAhead; ++j) prefetch(j);
@@ -416,13 +449,22 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
   if (*b.abort) {
     // Let this CTA's loads in flight land before it exits.
     mbar_wait(b.q_full, 0, p.err_flag);
-    if (FP8) {
-      for (int n = max(0, staged_k - (VERIFY ? 2 : 1)); n < staged_k; ++n)
-        mbar_wait(b.k8_full + (VERIFY ? (n & 1) : 0) * kStage8Bar,
-                  VERIFY ? ((n >> 1) & 1) : (n & 1), p.err_flag);
-      for (int n = max(0, staged_v - (VERIFY ? 2 : 1)); n < staged_v; ++n)
-        mbar_wait(b.v8_full + (VERIFY ? (n & 1) : 0) * kStage8Bar,
-                  VERIFY ? ((n >> 1) & 1) : (n & 1), p.err_flag);
+    if (VERIFY && FP8) {
+      // each slot's last two steps loaded (buffers alternate by step)
+      const int lasts[4] = {last_k0, last_k1, last_v0, last_v1};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int hh = u & 1;
+        uint64_t* full = u < 2 ? b.k_full : b.v8_full;
+#pragma unroll
+        for (int d = 0; d < 2; ++d) {
+          const int jj = lasts[u] - d;
+          if (jj >= 0) mbar_wait(full + 2 * hh + (jj & 1), (uint32_t)((jj >> 1) & 1), p.err_flag);
+        }
+      }
+    } else if (FP8) {
+      if (staged_k > 0) mbar_wait(b.k8_full, (uint32_t)((staged_k - 1) & 1), p.err_flag);
+      if (staged_v > 0) mbar_wait(b.v8_full, (uint32_t)((staged_v - 1) & 1), p.err_flag);
     } else {
       if (last_k0 >= 0) mbar_wait(&b.k_full[0], (uint32_t)last_k0, p.err_flag);
       if (last_k1 >= 0) mbar_wait(&b.k_full[1], (uint32_t)last_k1, p.err_flag);
@@ -473,34 +515,29 @@ __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, i
 }
 
 // Warps 12-15 for e4m3 caches: staging -> f16 operand stages, in the order
-// the producer fills each staging tile.
+// the producer fills the staging tiles.  Prefill: K and V of each key tile
+// through one staging tile each.  Verify: V only (K feeds 8-bit MMAs), slot
+// hh's step jj from staging tile 2 hh + (jj & 1).
 template <bool VERIFY>
 __device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileGeom& gm,
                           uint8_t* smem, const Bars& b) {
   const int t = threadIdx.x - kConvWarp0 * 32;   // 0..127
   const int lane = threadIdx.x & 31;
-  int nk = 0, nv = 0;                            // staging tiles taken
-  // The next staging tile (K, or V with rows from z0 on zeroed: past the
+  // Staging tile `src` (K, or V with rows from z0 on zeroed: past the
   // stream's end, or all rows of a bad page) into 16-bit stage s.
-  auto convert = [&](bool is_v, int s, uint32_t ph, int z0) {
-    int& n = is_v ? nv : nk;
-    const int i = VERIFY ? (n & 1) : 0;
-    const uint32_t ph8 = VERIFY ? ((n >> 1) & 1) : (n & 1);
-    uint64_t* full8 = (is_v ? b.v8_full : b.k8_full) + i * kStage8Bar;
-    uint64_t* empty8 = (is_v ? b.v8_empty : b.k8_empty) + i * kStage8Bar;
+  auto convert = [&](bool is_v, int s, uint32_t ph, int z0, int src, uint32_t ph8,
+                     uint64_t* full8, uint64_t* empty8) {
     uint64_t* empty = is_v ? &b.v_empty[s] : &b.k_empty[s];
     uint64_t* full = is_v ? &b.v_full[s] : &b.k_full[s];
     if (!mbar_wait_or_abort(full8, ph8, p.err_flag, b.abort)) return false;
     if (!mbar_wait_or_abort(empty, ph ^ 1, p.err_flag, b.abort)) return false;
-    convert_tile(smem + stage8_off<VERIFY>(is_v, i), smem + (is_v ? kOffV : kOffK) + s * 32768,
-                 is_v ? z0 : kTileKeys, t);
+    convert_tile(smem + src, smem + (is_v ? kOffV : kOffK) + s * 32768, is_v ? z0 : kTileKeys, t);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(empty8);
       mbar_arrive(full);
     }
-    ++n;
     return true;
   };
   if (VERIFY) {
@@ -508,15 +545,14 @@ __device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileG
     PageCheck pc1(p, ru, gm, gm.kt0 + 1, slot_tiles<true>(gm, 1), 2);
     bool ok = true;
     for (int jj = 0; ok && jj < slot_tiles<true>(gm, 0); ++jj) {
-      int z0[2] = {kTileKeys, kTileKeys};
-      for (int hh = 0; hh < 2; ++hh) {
+      for (int hh = 0; ok && hh < 2; ++hh) {
         if (jj >= slot_tiles<true>(gm, hh)) continue;
         const int j = slot_tile<true>(gm, jj, hh);
-        z0[hh] = v_zero_from(ru, j, hh ? pc1.bad(j) : pc0.bad(j));
+        const int z0 = v_zero_from(ru, j, hh ? pc1.bad(j) : pc0.bad(j));
+        const int i = 2 * hh + (jj & 1);
+        ok = convert(true, hh, jj & 1, z0, vstage8_off(i), (uint32_t)((jj >> 1) & 1),
+                     b.v8_full + i, b.v8_empty + i);
       }
-      for (int kv = 0; ok && kv < 2; ++kv)
-        for (int hh = 0; ok && hh < 2; ++hh)
-          if (jj < slot_tiles<true>(gm, hh)) ok = convert(kv == 1, hh, jj & 1, z0[hh]);
     }
     return;
   }
@@ -526,8 +562,10 @@ __device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileG
     const int z0 = v_zero_from(ru, j, pc.bad(j));
     const int s = jj & 1;
     const uint32_t ph = (jj >> 1) & 1;
-    if (!convert(false, s, ph, z0)) return;
-    if (!convert(true, s, ph, z0)) return;
+    // one staging tile each for K and V: its jj-th fill is phase jj & 1
+    const uint32_t ph8 = (uint32_t)(jj & 1);
+    if (!convert(false, s, ph, z0, stage8_off(false, 0), ph8, b.k8_full, b.k8_empty)) return;
+    if (!convert(true, s, ph, z0, stage8_off(true, 0), ph8, b.v8_full, b.v8_empty)) return;
   }
 }
 
@@ -542,13 +580,27 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
   const uint32_t kb = smem_u32(smem + kOffK);
   const uint32_t vb = smem_u32(smem + kOffV);
 
+  constexpr uint32_t kIdescQK8 = umma::idesc_e4m3(128, 128);
   auto issue_s = [&](int hh, int s) {     // S_hh = Q_hh K_s^T (verify: one Q tile)
+    if constexpr (VERIFY && FP8) {
+      // S_hh = Q_hi K^T + Q_lo K^T over e4m3 K stage s (K = 32 per MMA)
+      const uint32_t k8 = smem_u32(smem + kstage8_off(s));
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-      const uint64_t a = umma::smem_desc_sw128(qb + (VERIFY ? 0 : hh * 32768) + off, 16, 1024);
-      const uint64_t bd = umma::smem_desc_sw128(kb + s * 32768 + off, 16, 1024);
-      umma::mma_ss(tmem + col_s(hh), a, bd, kIdescQK, ks > 0 ? 1u : 0u);
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = umma::smem_desc_sw128(qb + q * 16384 + ks * 32, 16, 1024);
+          const uint64_t bd = umma::smem_desc_sw128(k8 + ks * 32, 16, 1024);
+          umma::mma_ss_f8(tmem + col_s(hh), a, bd, kIdescQK8, (q | ks) ? 1u : 0u);
+        }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+        const uint64_t a = umma::smem_desc_sw128(qb + (VERIFY ? 0 : hh * 32768) + off, 16, 1024);
+        const uint64_t bd = umma::smem_desc_sw128(kb + s * 32768 + off, 16, 1024);
+        umma::mma_ss(tmem + col_s(hh), a, bd, kIdescQK, ks > 0 ? 1u : 0u);
+      }
     }
   };
   auto issue_pv = [&](int hh, int s, bool acc) {   // O_hh (+)= P_hh V_s
@@ -566,17 +618,20 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
     return;
   }
   if (VERIFY) {
-    // Slot hh: its tiles' K in stage hh (S_hh), V in stage hh (PV_hh); the
-    // slots alternate, each at its own phase (its step jj).
+    // Slot hh: V in stage hh (PV_hh); K in stage hh (bf16), or in e4m3 stage
+    // 2 hh + (jj & 1) at phase (jj >> 1) & 1.  The slots alternate, each at
+    // its own phase (its step jj).
+    auto kst = [&](int hh, int jj) { return FP8 ? 2 * hh + (jj & 1) : hh; };
+    auto kph = [&](int jj) { return (uint32_t)(FP8 ? (jj >> 1) & 1 : jj & 1); };
     bool ok = mbar_wait_or_abort(b.q_ready, 0, p.err_flag, b.abort);
     for (int hh = 0; ok && hh < 2; ++hh) {
       if (slot_tiles<true>(gm, hh) == 0) continue;
-      if (!(ok = mbar_wait_or_abort(&b.k_full[hh], 0, p.err_flag, b.abort))) break;
+      if (!(ok = mbar_wait_or_abort(&b.k_full[kst(hh, 0)], 0, p.err_flag, b.abort))) break;
       umma::fence_after_sync();
       if (leader) {
-        issue_s(hh, hh);
+        issue_s(hh, kst(hh, 0));
         umma::commit(&b.s_full[hh]);
-        umma::commit(&b.k_empty[hh]);
+        umma::commit(&b.k_empty[kst(hh, 0)]);
       }
       __syncwarp();
     }
@@ -601,13 +656,14 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
         }
         __syncwarp();
         if (jj + 1 < n) {
-          if (!(ok = mbar_wait_or_abort(&b.k_full[hh], (jj + 1) & 1, p.err_flag, b.abort)))
+          const int ks = kst(hh, jj + 1);
+          if (!(ok = mbar_wait_or_abort(&b.k_full[ks], kph(jj + 1), p.err_flag, b.abort)))
             break;
           umma::fence_after_sync();
           if (leader) {
-            issue_s(hh, hh);
+            issue_s(hh, ks);
             umma::commit(&b.s_full[hh]);
-            umma::commit(&b.k_empty[hh]);
+            umma::commit(&b.k_empty[ks]);
           }
           __syncwarp();
         }
@@ -724,6 +780,72 @@ __device__ __forceinline__ float q_row_to_f16(uint8_t* qtile, int r) {
   return __int_as_float((127 - 14 + ex) << 23);
 }
 
+// Verify with an e4m3 cache: this thread's Q row (bf16, in the operand
+// tile) becomes two e4m3 rows for the 8-bit MMAs, hi = e4m3(q 2^e) and
+// lo = e4m3(q 2^e - hi), both rounded to nearest, with e putting the row's
+// largest magnitude in [2^7, 2^8).  q 2^e - hi is exact in float32 and has
+// at most four significant bits, so hi + lo = q 2^e exactly for every
+// element of magnitude 2^-2 or more after scaling (within 2^9 of the row's
+// largest), and to within one e4m3 rounding of the remainder below that.
+// hi lands over the first 64-column half (a [128 rows][128 B] tile, 128B
+// swizzle, as TMA lays out an e4m3 K tile), lo over the second; each thread
+// reads its whole row before it writes.  Returns 2^-e.
+__device__ __forceinline__ float q_row_to_e4m3_pair(uint8_t* qtile, int r) {
+  const uint32_t base = smem_u32(qtile);
+  uint32_t v[64];
+#pragma unroll
+  for (int ch = 0; ch < 16; ++ch) {
+    const uint4 w = lds128(swz128(base + (ch >> 3) * 16384u, r, ch & 7));
+    v[4 * ch + 0] = w.x;
+    v[4 * ch + 1] = w.y;
+    v[4 * ch + 2] = w.z;
+    v[4 * ch + 3] = w.w;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    amax = fmaxf(amax, fabsf(__uint_as_float(v[i] << 16)));
+    amax = fmaxf(amax, fabsf(__uint_as_float(v[i] & 0xFFFF0000u)));
+  }
+  int ex;
+  frexpf(amax, &ex);
+  ex = max(min(ex, 120), -100);
+  const float up = __int_as_float((127 + 8 - ex) << 23);
+  // Word i of a row: dims 4i .. 4i + 3, dim 4i in the low byte.
+  auto e4m3x2 = [](float a, float b) -> uint32_t {   // a in the low byte
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  };
+  auto rest2 = [](float a, float b, uint32_t h2) -> float2 {   // (a, b) - their e4m3 pair
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+    return make_float2(a - f.x, b - f.y);
+  };
+  uint32_t hi[32], lo[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float x0 = __uint_as_float(v[2 * i] << 16) * up;
+    const float x1 = __uint_as_float(v[2 * i] & 0xFFFF0000u) * up;
+    const float x2 = __uint_as_float(v[2 * i + 1] << 16) * up;
+    const float x3 = __uint_as_float(v[2 * i + 1] & 0xFFFF0000u) * up;
+    const uint32_t h01 = e4m3x2(x0, x1), h23 = e4m3x2(x2, x3);
+    const float2 r01 = rest2(x0, x1, e4m3x2_to_f16x2((uint16_t)h01));
+    const float2 r23 = rest2(x2, x3, e4m3x2_to_f16x2((uint16_t)h23));
+    hi[i] = h01 | (h23 << 16);
+    lo[i] = e4m3x2(r01.x, r01.y) | (e4m3x2(r23.x, r23.y) << 16);
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};"
+                 ::"r"(swz128(base, r, c)), "r"(hi[4 * c]), "r"(hi[4 * c + 1]),
+                   "r"(hi[4 * c + 2]), "r"(hi[4 * c + 3])
+                 : "memory");
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};"
+                 ::"r"(swz128(base + 16384u, r, c)), "r"(lo[4 * c]), "r"(lo[4 * c + 1]),
+                   "r"(lo[4 * c + 2]), "r"(lo[4 * c + 3])
+                 : "memory");
+  }
+  return __int_as_float((127 - 8 + ex) << 23);
+}
+
 // Offsets of CTA 1's partial for (head hh, row r) in CTA 0's shared memory:
 // O over the K/V rings, (m, l) over the Q tiles.
 __device__ __forceinline__ uint32_t part_o_row(uint32_t smem_base, int hh, int r) {
@@ -768,7 +890,8 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
     if (!VERIFY || hh == 0) {
       ok = mbar_wait_or_abort(b.q_full, 0, p.err_flag, b.abort);
       if (ok) {
-        const float down = q_row_to_f16(smem + kOffQ + (VERIFY ? 0 : hh * 32768), r);
+        const float down = VERIFY ? q_row_to_e4m3_pair(smem + kOffQ, r)
+                                  : q_row_to_f16(smem + kOffQ + hh * 32768, r);
         sl2 = p.scale_log2 * down * __ldg(p.k_scale + x.g);
         if (VERIFY) down_s[r] = down;
         fence_proxy_async_smem();
@@ -1028,15 +1151,17 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   Bars b;
   b.q_full = bars + 0;
   b.q_ready = FP8 ? bars + 1 : bars + 0;
+  // Verify with an e4m3 cache: four K stages (bars 2-5 full, 10-13 empty)
+  // and four V staging tiles (24-27 full, 28-31 empty); no K staging.
+  constexpr bool kDirectK = VERIFY && FP8;
   b.k_full = bars + 2;
-  b.k_empty = bars + 4;
+  b.k_empty = kDirectK ? bars + 10 : bars + 4;
   b.v_full = bars + 6;
   b.v_empty = bars + 8;
-  b.k8_full = bars + 10;        // tile 1: bars + 24 .. 27
+  b.k8_full = bars + 10;
   b.k8_empty = bars + 11;
-  b.v8_full = bars + 12;
-  b.v8_empty = bars + 13;
-  static_assert(10 + kStage8Bar == 24, "staging tile 1 barriers");
+  b.v8_full = kDirectK ? bars + 24 : bars + 12;
+  b.v8_empty = kDirectK ? bars + 28 : bars + 13;
   b.s_full = bars + 14;
   b.p_ready = bars + 16;
   b.o_final = bars + 18;
@@ -1052,18 +1177,29 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
     mbar_init(b.q_full, 1);
     mbar_init(bars + 1, VERIFY ? 4 : 8);           // q_ready: the (slot A) softmax warps
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&b.k_full[i], stage_arrivals);
-      mbar_init(&b.k_empty[i], 1);
       mbar_init(&b.v_full[i], stage_arrivals);
       mbar_init(&b.v_empty[i], 1);
       mbar_init(&b.s_full[i], 1);
       mbar_init(&b.p_ready[i], 4);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(b.k8_full + i * kStage8Bar, 1);
-      mbar_init(b.k8_empty + i * kStage8Bar, kConvWarps);
-      mbar_init(b.v8_full + i * kStage8Bar, 1);
-      mbar_init(b.v8_empty + i * kStage8Bar, kConvWarps);
+    if (kDirectK) {
+      for (int i = 0; i < 4; ++i) {
+        mbar_init(&b.k_full[i], 1);                // the producer's TMA
+        mbar_init(&b.k_empty[i], 1);
+        mbar_init(&b.v8_full[i], 1);
+        mbar_init(&b.v8_empty[i], kConvWarps);
+      }
+    } else {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&b.k_full[i], stage_arrivals);
+        mbar_init(&b.k_empty[i], 1);
+      }
+      if (FP8) {
+        mbar_init(b.k8_full, 1);
+        mbar_init(b.k8_empty, kConvWarps);
+        mbar_init(b.v8_full, 1);
+        mbar_init(b.v8_empty, kConvWarps);
+      }
     }
     mbar_init(b.o_final, 1);
     mbar_init(b.drain, 1);
