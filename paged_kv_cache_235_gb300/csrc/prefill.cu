@@ -80,9 +80,14 @@ __device__ __forceinline__ int vstage8_off(int i) {
   return i < 2 ? kOffK8 + i * 16384 : kOffK8b + (i - 2) * 16384;
 }
 __device__ __forceinline__ int kstage8_off(int i) { return kOffK + i * 16384; }
+// Verify, bf16: a ring of three 16-bit stages each for K and V over the
+// CTA's key tiles in the slots' common order (tile n = 2 step + slot in
+// stage n mod 3): K stage 2 is the unused second Q tile, V stage 2 follows
+// the prefill V ring.
+__device__ __forceinline__ int kstage16_off(int t) { return t < 2 ? kOffK + t * 32768 : 32768; }
 template <bool FP8>
 struct Layout {
-  static constexpr int kOffBar = FP8 ? 229376 : 196608;
+  static constexpr int kOffBar = 229376;
   // Verify: the Q rows' scale factors (e4m3 caches; 128 floats) and slot
   // B's (m, l) per row for the merge of the two slots (128 float2).
   static constexpr int kOffDown = kOffBar + 256;
@@ -379,7 +384,8 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
     uint64_t* empty = is_v ? &b.v_empty[stage] : &b.k_empty[stage];
     uint64_t* full = is_v ? &b.v_full[stage] : &b.k_full[stage];
     if (!mbar_wait_or_abort(empty, parity ^ 1, p.err_flag, b.abort)) return false;
-    uint8_t* dst = smem + (is_v ? kOffV : kOffK) + stage * 32768;
+    uint8_t* dst = smem + (is_v ? kOffV + stage * 32768
+                                : (VERIFY ? kstage16_off(stage) : kOffK + stage * 32768));
     mbar_arrive_expect_tx(full, 32768);
     tma_load_2d(dst, is_v ? mv : mk, 0, y, full);
     tma_load_2d(dst + 16384, is_v ? mv : mk, 64, y, full);
@@ -387,9 +393,10 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
   };
   // Last load issued into each 16-bit stage (phase parity, or -1): an
   // aborting CTA waits for these before it exits.
-  int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1;
+  int last_k0 = -1, last_k1 = -1, last_k2 = -1, last_v0 = -1, last_v1 = -1, last_v2 = -1;
   auto issued = [&](bool is_v, int stage, uint32_t ph) {
-    int& w = is_v ? (stage ? last_v1 : last_v0) : (stage ? last_k1 : last_k0);
+    int& w = is_v ? (stage == 2 ? last_v2 : stage ? last_v1 : last_v0)
+                  : (stage == 2 ? last_k2 : stage ? last_k1 : last_k0);
     w = (int)ph;
   };
   if (VERIFY && FP8) {
@@ -420,19 +427,20 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
         }
     }
   } else if (VERIFY) {
-    // Step jj: slot A's tile kt0 + 2 jj into stage 0, slot B's kt0 + 2 jj + 1
-    // into stage 1; K of both, then V of both.
+    // Step jj, slot hh: tile n = 2 jj + hh (kt0 + n) into stage n mod 3 at
+    // phase (n / 3) & 1; K of both slots, then V of both.
     for (int j = gm.kt0; j < gm.kt0 + kAhead; ++j) prefetch(j);
     bool ok = true;
     for (int jj = 0; ok && jj < slot_tiles<true>(gm, 0); ++jj) {
       prefetch(gm.kt0 + 2 * jj + kAhead);
       prefetch(gm.kt0 + 2 * jj + 1 + kAhead);
-      const uint32_t ph = jj & 1;
       for (int kv = 0; ok && kv < 2; ++kv)
         for (int hh = 0; ok && hh < 2; ++hh) {
           if (jj >= slot_tiles<true>(gm, hh)) continue;
-          ok = load(kv == 1, hh, ph, row_of(slot_tile<true>(gm, jj, hh)));
-          if (ok) issued(kv == 1, hh, ph);
+          const int n = 2 * jj + hh;
+          const uint32_t ph = (uint32_t)((n / 3) & 1);
+          ok = load(kv == 1, n % 3, ph, row_of(slot_tile<true>(gm, jj, hh)));
+          if (ok) issued(kv == 1, n % 3, ph);
         }
     }
   } else {
@@ -468,8 +476,10 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
     } else {
       if (last_k0 >= 0) mbar_wait(&b.k_full[0], (uint32_t)last_k0, p.err_flag);
       if (last_k1 >= 0) mbar_wait(&b.k_full[1], (uint32_t)last_k1, p.err_flag);
+      if (last_k2 >= 0) mbar_wait(&b.k_full[2], (uint32_t)last_k2, p.err_flag);
       if (last_v0 >= 0) mbar_wait(&b.v_full[0], (uint32_t)last_v0, p.err_flag);
       if (last_v1 >= 0) mbar_wait(&b.v_full[1], (uint32_t)last_v1, p.err_flag);
+      if (last_v2 >= 0) mbar_wait(&b.v_full[2], (uint32_t)last_v2, p.err_flag);
     }
   }
 }
@@ -598,7 +608,8 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
         const uint64_t a = umma::smem_desc_sw128(qb + (VERIFY ? 0 : hh * 32768) + off, 16, 1024);
-        const uint64_t bd = umma::smem_desc_sw128(kb + s * 32768 + off, 16, 1024);
+        const uint32_t k16 = VERIFY ? smem_u32(smem + kstage16_off(s)) : kb + s * 32768;
+        const uint64_t bd = umma::smem_desc_sw128(k16 + off, 16, 1024);
         umma::mma_ss(tmem + col_s(hh), a, bd, kIdescQK, ks > 0 ? 1u : 0u);
       }
     }
@@ -618,11 +629,15 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
     return;
   }
   if (VERIFY) {
-    // Slot hh: V in stage hh (PV_hh); K in stage hh (bf16), or in e4m3 stage
-    // 2 hh + (jj & 1) at phase (jj >> 1) & 1.  The slots alternate, each at
-    // its own phase (its step jj).
-    auto kst = [&](int hh, int jj) { return FP8 ? 2 * hh + (jj & 1) : hh; };
-    auto kph = [&](int jj) { return (uint32_t)(FP8 ? (jj >> 1) & 1 : jj & 1); };
+    // Slot hh, step jj.  bf16: K and V of tile n = 2 jj + hh in stage n mod
+    // 3 at phase (n / 3) & 1.  e4m3: K in e4m3 stage 2 hh + (jj & 1) at phase
+    // (jj >> 1) & 1, V in 16-bit stage hh at phase jj & 1.
+    auto kst = [&](int hh, int jj) { return FP8 ? 2 * hh + (jj & 1) : (2 * jj + hh) % 3; };
+    auto kph = [&](int hh, int jj) {
+      return (uint32_t)(FP8 ? (jj >> 1) & 1 : ((2 * jj + hh) / 3) & 1);
+    };
+    auto vst = [&](int hh, int jj) { return FP8 ? hh : (2 * jj + hh) % 3; };
+    auto vph = [&](int hh, int jj) { return (uint32_t)(FP8 ? jj & 1 : ((2 * jj + hh) / 3) & 1); };
     bool ok = mbar_wait_or_abort(b.q_ready, 0, p.err_flag, b.abort);
     for (int hh = 0; ok && hh < 2; ++hh) {
       if (slot_tiles<true>(gm, hh) == 0) continue;
@@ -643,21 +658,22 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
         if (jj >= n) continue;
         const int j = slot_tile<true>(gm, jj, hh);
         const bool page_bad = hh ? pc1.bad(j) : pc0.bad(j);
-        if (!(ok = mbar_wait_or_abort(&b.v_full[hh], jj & 1, p.err_flag, b.abort))) break;
+        const int vs = vst(hh, jj);
+        if (!(ok = mbar_wait_or_abort(&b.v_full[vs], vph(hh, jj), p.err_flag, b.abort))) break;
         if (!FP8) {
           const int z0 = v_zero_from(ru, j, page_bad);
-          if (z0 < kTileKeys) zero_v_rows(smem + kOffV + hh * 32768, z0, lane);
+          if (z0 < kTileKeys) zero_v_rows(smem + kOffV + vs * 32768, z0, lane);
         }
         if (!(ok = mbar_wait_or_abort(&b.p_ready[hh], jj & 1, p.err_flag, b.abort))) break;
         umma::fence_after_sync();
         if (leader) {
-          issue_pv(hh, hh, jj > 0);
-          umma::commit(&b.v_empty[hh]);
+          issue_pv(hh, vs, jj > 0);
+          umma::commit(&b.v_empty[vs]);
         }
         __syncwarp();
         if (jj + 1 < n) {
           const int ks = kst(hh, jj + 1);
-          if (!(ok = mbar_wait_or_abort(&b.k_full[ks], kph(jj + 1), p.err_flag, b.abort)))
+          if (!(ok = mbar_wait_or_abort(&b.k_full[ks], kph(hh, jj + 1), p.err_flag, b.abort)))
             break;
           umma::fence_after_sync();
           if (leader) {
@@ -1153,11 +1169,14 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   b.q_ready = FP8 ? bars + 1 : bars + 0;
   // Verify with an e4m3 cache: four K stages (bars 2-5 full, 10-13 empty)
   // and four V staging tiles (24-27 full, 28-31 empty); no K staging.
+  // Verify with a bf16 cache: rings of three, K full 24-26 and empty 27-29,
+  // V full 2-4 and empty 5-7.
   constexpr bool kDirectK = VERIFY && FP8;
-  b.k_full = bars + 2;
-  b.k_empty = kDirectK ? bars + 10 : bars + 4;
-  b.v_full = bars + 6;
-  b.v_empty = bars + 8;
+  constexpr bool kRing3 = VERIFY && !FP8;
+  b.k_full = kRing3 ? bars + 24 : bars + 2;
+  b.k_empty = kDirectK ? bars + 10 : kRing3 ? bars + 27 : bars + 4;
+  b.v_full = kRing3 ? bars + 2 : bars + 6;
+  b.v_empty = kRing3 ? bars + 5 : bars + 8;
   b.k8_full = bars + 10;
   b.k8_empty = bars + 11;
   b.v8_full = kDirectK ? bars + 24 : bars + 12;
@@ -1177,10 +1196,12 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
     mbar_init(b.q_full, 1);
     mbar_init(bars + 1, VERIFY ? 4 : 8);           // q_ready: the (slot A) softmax warps
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&b.v_full[i], stage_arrivals);
-      mbar_init(&b.v_empty[i], 1);
       mbar_init(&b.s_full[i], 1);
       mbar_init(&b.p_ready[i], 4);
+    }
+    for (int i = 0; i < (kRing3 ? 3 : 2); ++i) {
+      mbar_init(&b.v_full[i], stage_arrivals);
+      mbar_init(&b.v_empty[i], 1);
     }
     if (kDirectK) {
       for (int i = 0; i < 4; ++i) {
@@ -1190,7 +1211,7 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
         mbar_init(&b.v8_empty[i], kConvWarps);
       }
     } else {
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < (kRing3 ? 3 : 2); ++i) {
         mbar_init(&b.k_full[i], stage_arrivals);
         mbar_init(&b.k_empty[i], 1);
       }
