@@ -37,6 +37,13 @@
 // scores and to the output.  Verify tiles on an e4m3 cache instead split Q
 // into two e4m3 tiles (hi + lo) and take S from 8-bit MMAs straight off the
 // e4m3 K tiles, so only V passes through the converters.
+// Verify mode (launch_verify): one CTA per tile (run, kv head, 128 / G rows,
+// key split), no cluster.  One Q tile holds the group's query vectors (row x
+// head) and both slots read it: slot A takes the split's even key tiles,
+// slot B the odd ones, and the CTA merges the two into the split's partial.
+// bf16: rings of three K and V stages over the slots' common tile order.
+// e4m3: two e4m3 K stages per slot (8-bit S MMAs), two V staging tiles per
+// slot, one f16 V stage per slot.
 // TMEM (512 columns): S_A [0,128) O_A [128,256) S_B [256,384) O_B [384,512).
 // CTA 1's partial lands in CTA 0's shared memory once CTA 0's MMAs are done:
 // O (float32 [2 heads][128 rows][128], 16-byte chunks permuted by row against
@@ -298,9 +305,9 @@ __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, i
 }
 
 // Verify tiles stream their keys from HBM once (prefill tiles re-read a
-// prefix that mostly sits in L2), and a ring of two stages holds them only
-// about one step ahead of the MMAs: the producer also prefetches the K and
-// V boxes of the tile kAhead steps ahead into L2.
+// prefix that mostly sits in L2), and their stages hold them only one to two
+// steps ahead of the MMAs: the producer also prefetches the K and V boxes of
+// the tile kAhead steps ahead into L2.
 constexpr int kAhead = 4;
 
 template <bool FP8, bool VERIFY>
