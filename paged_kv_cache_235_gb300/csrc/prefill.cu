@@ -163,10 +163,10 @@ __device__ __forceinline__ uint32_t col_o(int hh) { return hh ? 384u : 128u; }
 struct Bars {
   uint64_t* q_full;      // Q tiles landed (TMA)
   uint64_t* q_ready;     // Q operand ready for the MMA (e4m3 caches: after conversion)
-  uint64_t* k_full;      // [2] K operand stage ready (verify, e4m3: [4])
-  uint64_t* k_empty;     // [2] (verify, e4m3: [4])
-  uint64_t* v_full;      // [2]
-  uint64_t* v_empty;     // [2]
+  uint64_t* k_full;      // [2] K operand stage ready (verify: bf16 [3], e4m3 [4])
+  uint64_t* k_empty;     // [2] (verify: bf16 [3], e4m3 [4])
+  uint64_t* v_full;      // [2] (verify, bf16: [3])
+  uint64_t* v_empty;     // [2] (verify, bf16: [3])
   uint64_t* k8_full;     // prefill, e4m3: the staging tile landed / free
   uint64_t* k8_empty;
   uint64_t* v8_full;     // (verify, e4m3: [4])
