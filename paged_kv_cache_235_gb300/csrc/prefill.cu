@@ -69,29 +69,26 @@ constexpr int kConvWarps = 4;
 constexpr int kOffQ = 0;                 // 2 heads x [128 rows][128] 16-bit = 64 KB
 constexpr int kOffK = 65536;             // 2 stages x 32 KB (16-bit operand tiles)
 constexpr int kOffV = 131072;            // 2 stages x 32 KB
-constexpr int kOffK8 = 196608;           // e4m3 staging: one K tile, 16 KB
-constexpr int kOffV8 = 212992;           // e4m3 staging: one V tile, 16 KB
-// Verify mode uses only the first Q tile (32 KB).  With a bf16 cache the
-// second is unused.  With an e4m3 cache the Q tile becomes two e4m3 tiles
-// (hi and lo, 16 KB each) that feed 8-bit MMAs with K straight from its
-// e4m3 stages: four of 16 KB over the 16-bit K region, two per slot.  V
+constexpr int kOffK8 = 196608;           // prefill, e4m3: the K staging tile, 16 KB
+constexpr int kOffV8 = 212992;           // prefill, e4m3: the V staging tile, 16 KB
+// Verify mode holds Q in the first Q tile (32 KB) only.  bf16: the second
+// is K stage 2 of the rings of three.  e4m3: the Q tile becomes two e4m3
+// tiles (hi and lo, 16 KB each) that feed 8-bit MMAs with K straight from
+// its e4m3 stages, four of 16 KB over the 16-bit K region, two per slot; V
 // still goes through the converters, from four e4m3 staging tiles (two per
 // slot): the prefill staging pair and the second Q tile.
-constexpr int kOffK8b = 32768;
-constexpr int kOffV8b = 49152;
-__device__ __forceinline__ int stage8_off(bool is_v, int i) {
-  return i ? (is_v ? kOffV8b : kOffK8b) : (is_v ? kOffV8 : kOffK8);
-}
+constexpr int kOffQ2 = 32768;
+__device__ __forceinline__ int stage8_off(bool is_v) { return is_v ? kOffV8 : kOffK8; }
 // Verify, e4m3: V staging tile i (2 x slot + step parity) and K stage i.
 __device__ __forceinline__ int vstage8_off(int i) {
-  return i < 2 ? kOffK8 + i * 16384 : kOffK8b + (i - 2) * 16384;
+  return i < 2 ? kOffK8 + i * 16384 : kOffQ2 + (i - 2) * 16384;
 }
 __device__ __forceinline__ int kstage8_off(int i) { return kOffK + i * 16384; }
 // Verify, bf16: a ring of three 16-bit stages each for K and V over the
 // CTA's key tiles in the slots' common order (tile n = 2 step + slot in
 // stage n mod 3): K stage 2 is the unused second Q tile, V stage 2 follows
 // the prefill V ring.
-__device__ __forceinline__ int kstage16_off(int t) { return t < 2 ? kOffK + t * 32768 : 32768; }
+__device__ __forceinline__ int kstage16_off(int t) { return t < 2 ? kOffK + t * 32768 : kOffQ2; }
 template <bool FP8>
 struct Layout {
   static constexpr int kOffBar = 229376;
@@ -384,7 +381,7 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
       uint64_t* full = is_v ? b.v8_full : b.k8_full;
       if (!mbar_wait_or_abort(empty, (n & 1) ^ 1, p.err_flag, b.abort)) return false;
       mbar_arrive_expect_tx(full, 16384);
-      tma_load_2d(smem + stage8_off(is_v, 0), is_v ? mv : mk, 0, y, full);
+      tma_load_2d(smem + stage8_off(is_v), is_v ? mv : mk, 0, y, full);
       ++n;
       return true;
     }
@@ -581,8 +578,8 @@ __device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileG
     const uint32_t ph = (jj >> 1) & 1;
     // one staging tile each for K and V: its jj-th fill is phase jj & 1
     const uint32_t ph8 = (uint32_t)(jj & 1);
-    if (!convert(false, s, ph, z0, stage8_off(false, 0), ph8, b.k8_full, b.k8_empty)) return;
-    if (!convert(true, s, ph, z0, stage8_off(true, 0), ph8, b.v8_full, b.v8_empty)) return;
+    if (!convert(false, s, ph, z0, stage8_off(false), ph8, b.k8_full, b.k8_empty)) return;
+    if (!convert(true, s, ph, z0, stage8_off(true), ph8, b.v8_full, b.v8_empty)) return;
   }
 }
 
