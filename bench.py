@@ -35,13 +35,11 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode KV GB/s (% HBM peak); prompt-chunk attn TFLOP/s (% TC peak)"
 
 
-# DRAM traffic of one decode partial launch on the batched-decode workload,
-# from ncu (dram__bytes_read.sum + dram__bytes_write.sum, see
-# profiles/decode_partial_batched_decode.md), valid only while the kernel's
-# sources hash to the value below.  The counters were taken on sources that
-# hashed to c1ed5addc80cc3a2; since then tcgen05.cuh only gained two functions
-# the decode kernel does not call, and decode.cu compiles to the same cubin
-# bytes with either header.
+# DRAM traffic of one decode partial launch on the batched-decode workload
+# (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture of this
+# bench's partial launch), valid only while the kernel's sources hash to the
+# value below: after any change to them the line reports null until the
+# counters are taken again.
 DECODE_TRAFFIC = {"bytes": 268_614_656 + 4_640_000, "sources_sha256_16": "b149c2ad83c776c9"}
 DECODE_SOURCES = ["paged_kv_cache_235_gb300/csrc/decode.cu",
                   "paged_kv_cache_235_gb300/csrc/common.cuh",
@@ -261,9 +259,21 @@ def time_decode(w, torch, B, steps, warmup, dist):
     barrier(dist, torch)
     step_ms = e0.elapsed_time(e1) / steps
 
-    # the dominant kernel alone: decode partial launches, back to back
+    # A/A: the same replays timed again right after
+    e0.record(s)
+    for _ in range(steps):
+        graph.replay()
+    e1.record(s)
+    barrier(dist, torch)
+    step_ms_again = e0.elapsed_time(e1) / steps
+
+    # the dominant kernel alone: decode partial launches, back to back, for at
+    # least about 0.2 s, enqueued while the GPU sleeps (the host runs ahead)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    n = max(steps, 10)
+    n = max(steps, 4000)
+    for _ in range(3):
+        B.tfpa_decode_partial(cache, segs, q, w.row_seg, w.row_pos, w.softmax_scale, sc)
+    host_cover(torch)
     ev[0].record(s)
     for _ in range(n):
         B.tfpa_decode_partial(cache, segs, q, w.row_seg, w.row_pos, w.softmax_scale, sc)
@@ -271,29 +281,22 @@ def time_decode(w, torch, B, steps, warmup, dist):
     torch.cuda.synchronize()
     partial_ms = ev[0].elapsed_time(ev[1]) / n
     assert int(cache.err_flag.item()) == 0, "kernel error flag set"
-    return step_ms, partial_ms, (cache, segs, q, sc, out)
+    return step_ms, partial_ms, (cache, segs, q, sc, out), step_ms_again
 
 
-def time_e2e(w, torch, B, ctx, steps, warmup):
-    """Through the public API with host buffers: per step, copy the step's
-    inputs (q and the new K/V rows) from pinned host memory, run the step and
-    read the output back to the host (host clock, one sync per step)."""
+def time_e2e_graph(w, torch, B, ctx, steps, warmup):
+    """Upper bound: the whole step (copies in, kernels, copy out) captured once
+    as a CUDA graph and replayed, the host waiting for each step's output.
+    The replay repeats one step's kernel parameters (lengths frozen at
+    capture), so a decode loop whose lengths advance cannot run this way."""
     cache, segs, _, sc, out = ctx
     nst = len(w.streams)
-    hq = torch.randn(w.rows, w.hq, 128).to(torch.bfloat16).pin_memory()
-    hk = torch.randn(nst, w.hkv, 128).to(torch.bfloat16).pin_memory()
-    hv = torch.randn(nst, w.hkv, 128).to(torch.bfloat16).pin_memory()
-    hout = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16).pin_memory()
-    dq = torch.empty_like(hq, device="cuda")
-    dk = torch.empty_like(hk, device="cuda")
-    dv = torch.empty_like(hv, device="cuda")
+    h_in, d_in, dq, dk, dv, hout = e2e_buffers(w, torch, nst)
     last = np.array([st.seq_len - 1 for st in w.streams], np.int32)
     sidx = np.arange(nst, dtype=np.int32)
 
     def enqueue():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         B.tfpa_write_kv(cache, segs, dk, dv, sidx, last)
         B.tfpa_decode(cache, segs, dq, w.row_seg, w.row_pos, w.softmax_scale, sc, out)
         hout.copy_(out, non_blocking=True)
@@ -301,8 +304,6 @@ def time_e2e(w, torch, B, ctx, steps, warmup):
     for _ in range(warmup):
         enqueue()
     torch.cuda.synchronize()
-    # The whole step (copies in, kernels, copy out) as one CUDA graph; the
-    # host waits for each step's output before starting the next.
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
     cap.wait_stream(torch.cuda.current_stream())
@@ -319,9 +320,93 @@ def time_e2e(w, torch, B, ctx, steps, warmup):
     for _ in range(steps):
         graph.replay()
         s.synchronize()
+    return (time.perf_counter() - t0) / steps
+
+
+def e2e_buffers(w, torch, nst):
+    """One pinned host buffer per step's inputs (q rows, then the new K and V
+    rows), its device copy with views, and a pinned buffer for the output."""
+    nq, nk = w.rows * w.hq * 128, nst * w.hkv * 128
+    h_in = torch.randn(nq + 2 * nk).to(torch.bfloat16).pin_memory()
+    d_in = torch.empty_like(h_in, device="cuda")
+    dq = d_in[:nq].view(w.rows, w.hq, 128)
+    dk = d_in[nq:nq + nk].view(nst, w.hkv, 128)
+    dv = d_in[nq + nk:].view(nst, w.hkv, 128)
+    hout = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16).pin_memory()
+    return h_in, d_in, dq, dk, dv, hout
+
+
+def time_e2e_calls(w, torch, B, ctx, steps, warmup, in_flight=1):
+    """A decode loop through the public API with host buffers, one real call
+    of each entry point per step.  Every stream's length grows by one each
+    step, so every call is planned anew (lengths, splits, CTA ranges): step i
+    of n has length L - n + 1 + i (L = the workload's 8,192), writes each
+    stream's new K/V row at its last position and decodes that row.  Per step:
+    one copy of the step's inputs (q and the new K/V rows, one pinned buffer)
+    to the device, tfpa_write_kv, tfpa_decode, the output copied back to
+    pinned host memory, and the host waits for it.  With in_flight = 2 the
+    host enqueues step i + 1 before it waits for step i's output (double-
+    buffered inputs and outputs).  Returns (s per step, KV + Q + O bytes per
+    step on average, host us per tfpa_write_kv call, per tfpa_decode call,
+    h2d bytes, d2h bytes)."""
+    cache, segs, _, sc, out0 = ctx
+    nst = len(w.streams)
+    assert list(w.row_seg) == list(range(nst)), "one decode row per stream"
+    tab = B.SegTable(segs)
+    bufs = [e2e_buffers(w, torch, nst) for _ in range(in_flight)]
+    outs = [out0] + [torch.empty_like(out0) for _ in range(in_flight - 1)]
+    evs = [torch.cuda.Event() for _ in range(in_flight)]
+    sidx = np.arange(nst, dtype=np.int32)
+    pos = [np.zeros(nst, np.int32) for _ in range(in_flight)]
+    s = torch.cuda.current_stream()
+    sh = s.cuda_stream
+    L = w.streams[0].seq_len
+    assert all(st.seq_len == L for st in w.streams)
+    total = warmup + steps
+    t_w, t_d = [], []
+    b, kvb = (2 if w.kv_dtype == "bf16" else 1), 0
+
+    def enqueue(i, k):
+        h_in, d_in, dq, dk, dv, hout = bufs[k]
+        n = L - total + 1 + i
+        for j in range(nst):
+            tab.set_seq_len(j, n)
+        rp = pos[k]
+        rp.fill(n - 1)
+        d_in.copy_(h_in, non_blocking=True)
+        t0 = time.perf_counter_ns()
+        B.tfpa_write_kv(cache, tab, dk, dv, sidx, rp, stream=sh)
+        t1 = time.perf_counter_ns()
+        B.tfpa_decode(cache, tab, dq, sidx, rp, w.softmax_scale, sc, outs[k], stream=sh)
+        t2 = time.perf_counter_ns()
+        hout.copy_(outs[k], non_blocking=True)
+        evs[k].record(s)
+        return n, (t1 - t0) / 1e3, (t2 - t1) / 1e3
+
+    def run(first, count, keep):
+        nonlocal kvb
+        for i in range(first, first + count):
+            k = i % in_flight
+            if i - first >= in_flight:
+                evs[k].synchronize()            # the output of step i - in_flight is home
+            n, a, d = enqueue(i, k)
+            if keep:
+                t_w.append(a)
+                t_d.append(d)
+                kvb += n * nst * w.hkv * 128 * 2 * b
+        for k in range(in_flight):
+            evs[k].synchronize()
+
+    run(0, warmup, False)
+    t0 = time.perf_counter()
+    run(warmup, steps, True)
     dt = (time.perf_counter() - t0) / steps
-    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
-    return dt, h2d, hout.numel() * 2
+    for j, st in enumerate(w.streams):          # back to the workload's lengths
+        tab.set_seq_len(j, st.seq_len)
+    qo = w.rows * w.hq * 128 * 2 * 2
+    h2d = bufs[0][0].numel() * 2
+    return (dt, kvb / steps + qo, statistics.median(t_w), statistics.median(t_d), h2d,
+            bufs[0][5].numel() * 2)
 
 
 def host_cover(torch):
@@ -596,12 +681,17 @@ def main():
     w3 = wl.fp8_verify()
     kv3, qo3 = kv_bytes(w3)
     with ClockSampler(local) as clk:
-        step_ms, partial_ms, ctx = time_decode(w, torch, B, args.steps, args.warmup, dist)
+        step_ms, partial_ms, ctx, step_ms_aa = time_decode(w, torch, B, args.steps, args.warmup,
+                                                          dist)
         step_ms = max_over_ranks(dist, torch, step_ms)
-        e2e_s, h2d, d2h = time_e2e(w, torch, B, ctx, max(10, min(args.steps, 500)), args.warmup)
-        e2e_s = max_over_ranks(dist, torch, e2e_s)
+        n_e2e = max(10, min(args.steps, 500))
+        e2e = time_e2e_calls(w, torch, B, ctx, n_e2e, args.warmup)
+        e2e_s = max_over_ranks(dist, torch, e2e[0])
+        e2e_aa = time_e2e_calls(w, torch, B, ctx, n_e2e, args.warmup)
+        e2e_pipe = time_e2e_calls(w, torch, B, ctx, n_e2e, args.warmup, in_flight=2)
+        e2e_graph_s = time_e2e_graph(w, torch, B, ctx, n_e2e, args.warmup)
         del ctx
-        s3, p3, ctx3 = time_decode(w3, torch, B, max(10, args.steps // 4), args.warmup, None)
+        s3, p3, ctx3, _ = time_decode(w3, torch, B, max(10, args.steps // 4), args.warmup, None)
         del ctx3
         if not args.skip_prefill:
             w4 = wl.prompt_chunk()
@@ -705,14 +795,39 @@ def main():
                      "kernel": "decode_partial_kernel<bf16>", "peak_source": pk["source"],
                      "partial_ms": partial_ms},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * (kv + qo) / e2e_s / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": world * e2e[1] / e2e_s / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": e2e[4], "d2h_bytes_per_step": e2e[5],
+                "ms_per_step": e2e_s * 1e3, "vs_device_step": e2e_s * 1e3 / step_ms,
+                "host_us_per_call": {"tfpa_write_kv": e2e[2], "tfpa_decode": e2e[3]},
+                "steps": n_e2e,
+                "how": "real tfpa_write_kv + tfpa_decode calls every step (no graph), each "
+                       "stream one position longer every step (%d..%d), one pinned input "
+                       "copy (q + new K/V rows) and one output copy per step, the host "
+                       "waits for each step's output before the next; host_us_per_call = "
+                       "host clock around each call (binding + C planning + launches), "
+                       "median" % (w.streams[0].seq_len - n_e2e + 1, w.streams[0].seq_len)},
+        "e2e_aa_repeat": {"ms_per_step": [e2e_s * 1e3, e2e_aa[0] * 1e3],
+                          "spread_pct": 100 * abs(e2e_aa[0] - e2e_s) / e2e_s},
+        "e2e_two_in_flight": {
+            "value": world * e2e_pipe[1] / e2e_pipe[0] / 1e9, "unit": "GB/s",
+            "ms_per_step": e2e_pipe[0] * 1e3,
+            "host_us_per_call": {"tfpa_write_kv": e2e_pipe[2], "tfpa_decode": e2e_pipe[3]},
+            "how": "the same loop with step i + 1 enqueued before the host waits for step "
+                   "i's output (two input and output buffers)"},
+        "e2e_graph_replay": {
+            "value": world * (kv + qo) / e2e_graph_s / 1e9, "unit": "GB/s",
+            "ms_per_step": e2e_graph_s * 1e3,
+            "how": "upper bound: one step (copies, 3 kernels) captured once as a CUDA graph "
+                   "and replayed with its lengths frozen; no host planning per step"},
+        "aa_repeat": {"ms_per_step": [step_ms, step_ms_aa],
+                      "spread_pct": 100 * abs(step_ms_aa - step_ms) / step_ms},
         "gpu_launches": 3 * args.steps,
         "timing": "decode step = one CUDA-graph replay of tfpa_write_kv + tfpa_decode "
-                  "(3 kernels), CUDA events over --steps replays; the per-call lines "
-                  "(prefill, tiny_decode, overcommitted_pool, tree_verify, kv_store_rope, "
-                  "keep, save_restore) are device time: CUDA events around one call, "
-                  "enqueued by the host during a preceding GPU sleep",
+                  "(3 kernels), CUDA events over --steps replays (device time); e2e = real "
+                  "calls per step, host clock (see e2e.how); the per-call lines (prefill, "
+                  "tiny_decode, overcommitted_pool, tree_verify, kv_store_rope, keep, "
+                  "save_restore) are device time: CUDA events around one call, enqueued by "
+                  "the host during a preceding GPU sleep",
         "clocks": clk.summary(),
         **extra,
     }

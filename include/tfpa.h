@@ -28,9 +28,18 @@
  *
  * Memory and ownership.  Every buffer is allocated by the caller.  Pointers
  * marked DEVICE are device memory of the current device; HOST arrays are read
- * during the call only and not retained.  The library allocates nothing, keeps
- * no state between calls except a host-side cache of TMA tensor maps, and never
- * synchronises the stream: all work is enqueued on `stream`.
+ * during the call only and not retained.  The library allocates no device
+ * memory, keeps no state between calls except host-side caches (TMA tensor
+ * maps, per host thread; each device's SM count), and never synchronises the
+ * stream: all work is enqueued on `stream`.
+ *
+ * Threads.  Calls may be made from several host threads at once, on any
+ * streams and devices: each thread builds its launch parameters in its own
+ * buffers and no call takes a lock on that path (the pool ledger and the
+ * static-scratch address lookup lock their own state).  Work enqueued on
+ * different streams runs concurrently on the GPU, so two calls must not
+ * write the same output, scratch or cache rows at once.
+ * tfpa_set_launch_hook must not run while another call is in progress.
  *
  * Errors.  Every call returns TFPA_OK (0) or a negative code below and
  * enqueues nothing on error.  Kernels never trap: a page id outside
@@ -263,7 +272,9 @@ int tfpa_decode_tree(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg
  *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress, with that device current); make that first
- * call before any stream capture.  Every call shares the one array and it
+ * call before any stream capture.  The address is kept per device context:
+ * if the context is replaced (cudaDeviceReset, then new work), the next call
+ * looks it up again, so it is also a set-up call.  Every call shares the one array and it
  * keeps the last call's contents; nothing in it needs to start at zero, as
  * every slot the merge reads is written by the partial kernel of the same
  * call.  Calls that overlap on the GPU (other streams, other host threads)

@@ -149,16 +149,21 @@ def _ptr(x) -> Optional[int]:
     """Device (or host) address of a tensor/array, or an int passed through."""
     if x is None:
         return None
-    if isinstance(x, int):
+    t = type(x)
+    if t is int:
         return x
-    if isinstance(x, np.ndarray):
+    if t is np.ndarray:
         return x.ctypes.data
+    if isinstance(x, int):
+        return int(x)
     return x.data_ptr()
 
 
 def _stream(stream) -> Optional[int]:
+    """A ``cudaStream_t`` handle: an int passes through (the cheapest form in a
+    loop), a torch stream gives its handle, None the current torch stream."""
     if stream is not None:
-        return stream if isinstance(stream, int) else stream.cuda_stream
+        return stream if type(stream) is int else stream.cuda_stream
     import torch
     if torch.cuda.is_available():
         return torch.cuda.current_stream().cuda_stream
@@ -166,11 +171,29 @@ def _stream(stream) -> Optional[int]:
 
 
 def _i32(a) -> np.ndarray:
+    if type(a) is np.ndarray and a.dtype == np.int32 and a.flags.c_contiguous:
+        return a
     return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
 
 
-@dataclass
-class Cache:
+class _Cached:
+    """Keeps the C struct of a dataclass until one of its fields is assigned."""
+
+    def __setattr__(self, k, v):
+        object.__setattr__(self, k, v)
+        if k != "_cs":
+            object.__setattr__(self, "_cs", None)
+
+    def c(self):
+        cs = self.__dict__.get("_cs")
+        if cs is None:
+            cs = self._make_c()
+            object.__setattr__(self, "_cs", cs)
+        return cs
+
+
+@dataclass(eq=False)
+class Cache(_Cached):
     """One layer's KV cache; holds the tensors so their memory stays alive."""
     dtype: str                    # "bf16" or "fp8"
     hq: int
@@ -182,14 +205,14 @@ class Cache:
     err_flag: object = None       # int32 [1]
     num_pages: int = 0
 
-    def c(self) -> tfpa_cache:
+    def _make_c(self) -> tfpa_cache:
         return tfpa_cache(BF16 if self.dtype == "bf16" else FP8_E4M3, self.hq, self.hkv,
                           HEAD_DIM, _ptr(self.k_pool), _ptr(self.v_pool), self.num_pages,
                           _ptr(self.k_scale), _ptr(self.v_scale), _ptr(self.err_flag))
 
 
-@dataclass
-class Seg:
+@dataclass(eq=False)
+class Seg(_Cached):
     """One stream: a device page table or a pair of slabs."""
     seq_len: int
     page_table: object = None         # device int32 [>= ceil(seq_len/256)]
@@ -198,23 +221,23 @@ class Seg:
     v_slab: object = None
     slab_cap: int = 0
 
-    def c(self) -> tfpa_seg:
+    def _make_c(self) -> tfpa_seg:
         host = None
         if self.page_table_host is not None:
-            self.page_table_host = _i32(self.page_table_host)
+            object.__setattr__(self, "page_table_host", _i32(self.page_table_host))
             host = _ptr(self.page_table_host)
         return tfpa_seg(int(self.seq_len), _ptr(self.page_table), host, _ptr(self.k_slab),
                         _ptr(self.v_slab), int(self.slab_cap))
 
 
-@dataclass
-class Scratch:
+@dataclass(eq=False)
+class Scratch(_Cached):
     part_o: object
     part_ml: object
     cap_rows: int
     max_splits: int = MAX_SPLITS
 
-    def c(self) -> tfpa_scratch:
+    def _make_c(self) -> tfpa_scratch:
         return tfpa_scratch(_ptr(self.part_o), _ptr(self.part_ml), self.cap_rows, self.max_splits)
 
 
@@ -225,7 +248,38 @@ def make_scratch(cap_rows: int, hq: int, max_splits: int = MAX_SPLITS, device="c
     return Scratch(o, ml, cap_rows, max_splits)
 
 
-def _segs(segs: Sequence[Seg]):
+class SegTable:
+    """The call's segments as one C array, built once.  A decode loop moves
+    each stream's length forward in place (``set_seq_len``) instead of
+    rebuilding the table for every call; every entry point that takes
+    ``segs`` accepts a SegTable.  The Seg objects (and their tensors) stay
+    referenced for as long as the table lives."""
+
+    def __init__(self, segs: Sequence[Seg]):
+        self.segs = list(segs)
+        self.n = len(self.segs)
+        self.arr = (tfpa_seg * max(1, self.n))(*[s.c() for s in self.segs])
+
+    def __len__(self):
+        return self.n
+
+    def __getitem__(self, i):
+        return self.segs[i]
+
+    def set_seq_len(self, i: int, seq_len: int) -> None:
+        """Stream i now holds seq_len keys (its page table, and the host mirror
+        if one was given, must cover ceil(seq_len / 256) pages)."""
+        self.arr[i].seq_len = seq_len
+        seg = self.segs[i]
+        object.__setattr__(seg, "seq_len", seq_len)
+        cs = seg.__dict__.get("_cs")
+        if cs is not None:
+            cs.seq_len = seq_len
+
+
+def _segs(segs):
+    if type(segs) is SegTable:
+        return segs.arr, segs.n
     arr = (tfpa_seg * max(1, len(segs)))(*[s.c() for s in segs])
     return arr, len(segs)
 

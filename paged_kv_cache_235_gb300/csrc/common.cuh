@@ -7,6 +7,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace tfpa {
 
 // Error bits a kernel may OR into the caller's err_flag.
@@ -59,6 +61,25 @@ cudaError_t launch_pdl(void (*kernel)(P), dim3 grid, dim3 block, size_t smem, cu
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
+
+// One-time set-up of a kernel's attributes on each device (attributes
+// belong to a device's context).  `setup` runs on the current device until
+// it has succeeded there; two threads that reach a device's first launch
+// together may both run it, so it must be idempotent.
+struct PerDeviceOnce {
+  std::atomic<uint64_t> done{0};
+  template <typename F>
+  cudaError_t run(F&& setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = setup();
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+};
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -780,21 +780,20 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
 
 template <bool FP8, bool GEN>
 cudaError_t launch_partial(const DecodeParams& p, int grid, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
+  static PerDeviceOnce configured;
+  cudaError_t e = configured.run([] {
     // The register split only works if the block launches with at least the
     // registers it hands out; otherwise setmaxnreg.inc would wait forever.
     cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, decode_partial_kernel<FP8, GEN>);
-    if (e != cudaSuccess) return e;
+    cudaError_t r = cudaFuncGetAttributes(&attr, decode_partial_kernel<FP8, GEN>);
+    if (r != cudaSuccess) return r;
     if (attr.numRegs * kThreads < 128 * (2 * kRegsConsumer + kRegsCombine + kRegsProducer))
       return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(decode_partial_kernel<FP8, GEN>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  cudaError_t e =
+    return cudaFuncSetAttribute(decode_partial_kernel<FP8, GEN>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (e != cudaSuccess) return e;
+  e =
       launch_pdl(decode_partial_kernel<FP8, GEN>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -3,9 +3,9 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
-#include <mutex>
 #include <unordered_map>
 #include <vector>
 
@@ -17,19 +17,21 @@ using namespace tfpa;
 namespace {
 
 // ------------------------------------------------------------ launch hook
-struct Hook {
-  tfpa_launch_hook fn = nullptr;
-  void* user = nullptr;
-  int dry = 0;
-};
-Hook g_hook;
-std::mutex g_mu;
+// Set from one thread while no other call runs (a test facility); read by
+// every call without a lock.
+std::atomic<tfpa_launch_hook> g_hook_fn{nullptr};
+std::atomic<void*> g_hook_user{nullptr};
+std::atomic<int> g_hook_dry{0};
 
-bool dry_run() { return g_hook.fn != nullptr && g_hook.dry != 0; }
+bool dry_run() {
+  return g_hook_dry.load(std::memory_order_relaxed) != 0 &&
+         g_hook_fn.load(std::memory_order_relaxed) != nullptr;
+}
 
 void record(int kind, int row0, int rows, int runs, int items, int grid, int64_t qoff,
             int64_t ooff) {
-  if (!g_hook.fn) return;
+  const tfpa_launch_hook fn = g_hook_fn.load(std::memory_order_acquire);
+  if (!fn) return;
   tfpa_launch_record r;
   r.kind = kind;
   r.row0 = row0;
@@ -39,40 +41,60 @@ void record(int kind, int row0, int rows, int runs, int items, int grid, int64_t
   r.grid = grid;
   r.q_offset = qoff;
   r.out_offset = ooff;
-  g_hook.fn(&r, g_hook.user);
+  fn(&r, g_hook_user.load(std::memory_order_relaxed));
 }
 
 // ------------------------------------------------------------ device info
+// SM count and compute capability of each device, read once per device.
+struct DeviceInfo {
+  std::atomic<int> ready{0};
+  int sm_count = 0;
+  int major = 0;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+
+// The current device's info, or nullptr if a CUDA call fails.
+const DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready.load(std::memory_order_acquire)) {
+    int n = 0, major = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+      return nullptr;
+    d.sm_count = n;     // two threads may both get here: they store the same values
+    d.major = major;
+    d.ready.store(1, std::memory_order_release);
+  }
+  return &d;
+}
+
 int sm_count() {
   if (dry_run()) return 152;
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n;
+  const DeviceInfo* d = device_info();
+  return d ? d->sm_count : 0;
 }
 
 int check_device() {
   if (dry_run()) return TFPA_OK;
-  int dev = 0, major = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TFPA_ECUDA;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
-    return TFPA_ECUDA;
-  return major == 10 ? TFPA_OK : TFPA_EDEVICE;
+  const DeviceInfo* d = device_info();
+  if (!d) return TFPA_ECUDA;
+  return d->major == 10 ? TFPA_OK : TFPA_EDEVICE;
 }
 
 // ------------------------------------------------------------ tensor maps
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -93,7 +115,11 @@ struct MapKeyHash {
     return h;
   }
 };
-std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+// Each host thread keeps its own cache of encoded maps, so calls from
+// several threads share no lock.  A map only describes an address range and
+// a box, so it stays valid for any buffer later placed at the same address
+// with the same extent.
+thread_local std::unordered_map<MapKey, CUtensorMap, MapKeyHash> t_maps;
 
 // A 2D view [rows][128] of a K or V buffer, 128B swizzle, box
 // [box_inner elements][box_rows rows].
@@ -104,8 +130,8 @@ int get_map(const void* ptr, uint64_t rows, bool fp8, int box_inner, int box_row
     return TFPA_OK;
   }
   MapKey key{ptr, rows, fp8 ? 1 : 0, box_inner, box_rows};
-  auto it = g_maps.find(key);
-  if (it != g_maps.end()) {
+  auto it = t_maps.find(key);
+  if (it != t_maps.end()) {
     *out = it->second;
     return TFPA_OK;
   }
@@ -122,8 +148,8 @@ int get_map(const void* ptr, uint64_t rows, bool fp8, int box_inner, int box_row
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return TFPA_ECUDA;
-  if (g_maps.size() > 4096) g_maps.clear();
-  g_maps.emplace(key, m);
+  if (t_maps.size() > 4096) t_maps.clear();
+  t_maps.emplace(key, m);
   *out = m;
   return TFPA_OK;
 }
@@ -310,31 +336,54 @@ int item_stages(const RunInfo& ri, int G, int mt, int sigma, int chunk) {
 // Per-CTA item ranges of a decode partial launch, balanced by work: an item
 // weighs its key stages plus a fixed cost (its query load and combine), and
 // CTA b starts at the first item whose prefix weight reaches b / grid of the
-// total.  Items are walked in the kernel's order: kv head, m-tile, split.
+// total.  Items are walked in the kernel's order: run, kv head, m-tile,
+// split.  An item's weight does not depend on its kv head, so each run's
+// (m-tile, split) prefix weights are computed once, and each CTA boundary is
+// found by a binary search in the block of the kv head that holds it.
 void plan_cta_ranges(DecodeParams& p, int nr, int G, bool fp8, int grid) {
   const int chunk = fp8 ? 256 : 128;
   constexpr int64_t kItemCost = 2;
-  auto for_items = [&](auto&& fn) {
-    for (int r = 0; r < nr; ++r) {
-      const RunInfo& ri = p.runs[r];
-      const int mtiles = (ri.nrows * G + 15) / 16;
-      for (int g = 0; g < p.hkv; ++g)
-        for (int mt = 0; mt < mtiles; ++mt)
-          for (int sg = 0; sg < ri.nsplit; ++sg)
-            fn(item_stages(ri, G, mt, sg, chunk) + kItemCost);
-    }
-  };
+  thread_local std::vector<int64_t> cum;     // per run: 0, w0, w0 + w1, ...
+  int32_t blk[kMaxRuns + 1];                 // run r's prefix weights: cum[blk[r] .. blk[r + 1]]
+  cum.clear();
   int64_t total = 0;
-  for_items([&](int64_t w) { total += w; });
+  for (int r = 0; r < nr; ++r) {
+    const RunInfo& ri = p.runs[r];
+    const int mtiles = (ri.nrows * G + 15) / 16;
+    blk[r] = (int32_t)cum.size();
+    int64_t sum = 0;
+    cum.push_back(0);
+    for (int mt = 0; mt < mtiles; ++mt)
+      for (int sg = 0; sg < ri.nsplit; ++sg) {
+        sum += item_stages(ri, G, mt, sg, chunk) + kItemCost;
+        cum.push_back(sum);
+      }
+    total += sum * p.hkv;
+  }
+  blk[nr] = (int32_t)cum.size();
   int b = 1, item = 0;
-  int64_t prefix = 0;
+  int64_t prefix = 0;   // weight of the items before the current block
   p.cta_item0[0] = 0;
-  for_items([&](int64_t w) {
-    while (b < grid && prefix * grid >= total * b) p.cta_item0[b++] = item;
-    prefix += w;
-    ++item;
-  });
-  while (b <= grid) p.cta_item0[b++] = item;
+  for (int r = 0; r < nr && b < grid; ++r) {
+    const int64_t* c = cum.data() + blk[r];
+    const int32_t n = blk[r + 1] - blk[r] - 1;   // items of one kv head's block
+    for (int g = 0; g < p.hkv && b < grid; ++g) {
+      // CTA b starts at the first item whose prefix weight P satisfies
+      // P * grid >= total * b, i.e. P >= ceil(total * b / grid)
+      while (b < grid) {
+        const int64_t need = (total * b + grid - 1) / grid - prefix;
+        const int32_t i = (int32_t)(std::lower_bound(c, c + n, need) - c);
+        if (i >= n) break;
+        p.cta_item0[b++] = item + i;
+      }
+      prefix += c[n];
+      item += n;
+    }
+  }
+  // CTAs past the last boundary get empty ranges at the end
+  int n_items = 0;
+  for (int r = 0; r < nr; ++r) n_items += (blk[r + 1] - blk[r] - 1) * p.hkv;
+  while (b <= grid) p.cta_item0[b++] = n_items;
 }
 
 // Partial (and optionally merge) launches over the call's rows.  With
@@ -354,7 +403,7 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
   if (anc && !aligned(anc, 8)) return TFPA_EINVAL;
   if (!std::isfinite(scale) || !(scale > 0.f)) return TFPA_EINVAL;
   if (!sliced && rows > sc->cap_rows) return TFPA_ECAPACITY;
-  std::vector<Run> runs;
+  thread_local std::vector<Run> runs;   // reused by every call of this thread
   if ((e = build_runs(segs, nseg, row_seg, row_pos, rows, runs))) return e;
   for (const Run& r : runs)
     if (tfpa_num_splits(segs[r.seg].seq_len) > sc->max_splits) return TFPA_ECAPACITY;
@@ -368,10 +417,11 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
 
   size_t ri = 0;
   int32_t taken = 0;  // rows of runs[ri] already launched
-  static DecodeParams p;   // large; built under the lock below
-  static PrefillParams pv;  // the tensor-core verify launch of the same rows
-  static MergeParams mp;
-  std::lock_guard<std::mutex> lock(g_mu);
+  // Launch parameters are large (kernel arguments by value): each host
+  // thread builds them in its own buffers.
+  thread_local DecodeParams p;
+  thread_local PrefillParams pv;   // the tensor-core verify launch of the same rows
+  thread_local MergeParams mp;
   // Runs of four or more m-tiles (16 query vectors each, so at least 49
   // vectors per kv head) are dense enough for the tensor cores: they go to
   // the prefill kernel in verify mode (128 / G rows x the group's G heads
@@ -384,8 +434,6 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
   auto is_wide = [&](const Run& r) { return (r.nrows * G + 15) / 16 >= 4; };
   const int vrows = verify_ok ? kVerifyVectors / G : 1;   // rows of a verify tile
   while (ri < runs.size()) {
-    std::memset(&p, 0, sizeof(p));
-    std::memset(&pv, 0, sizeof(pv));
     SourceSet ss;
     const int32_t base = runs[ri].row0 + taken;  // first call row of this launch
     int32_t nrows = 0, items = 0, tiles = 0;
@@ -397,6 +445,7 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
       const int32_t take = std::min(r.nrows - taken, sc->cap_rows - nrows);
       const tfpa_seg& g = segs[r.seg];
       if (verify_ok && is_wide(r)) {
+        if (nv == 0) std::memset(&pv, 0, sizeof(pv));   // only launches that run are built
         RunInfo& info = pv.runs[nv++];
         fill_run(info, g, src, nrows, take, r.pos0 + taken);
         info.pps = verify_pages_per_split(g.seq_len);
@@ -405,6 +454,7 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
         tiles += c->hkv * ((take + vrows - 1) / vrows) * info.nsplit;
         mp.runs[nr] = MergeRun{nrows, take, info.nsplit, 0};
       } else {
+        if (nd == 0) std::memset(&p, 0, sizeof(p));
         RunInfo& info = p.runs[nd++];
         fill_run(info, g, src, nrows, take, r.pos0 + taken);
         info.item0 = items;
@@ -531,8 +581,7 @@ extern "C" int tfpa_merge(const tfpa_scratch* sc, int32_t hq, int32_t rows,
     if (nsplit[r] < 1 || nsplit[r] > std::min(sc->max_splits, kMaxSplits)) return TFPA_ECAPACITY;
   int e;
   if ((e = check_device())) return e;
-  std::lock_guard<std::mutex> lock(g_mu);
-  static MergeParams mp;
+  thread_local MergeParams mp;
   int32_t r = 0;
   while (r < rows) {
     std::memset(&mp, 0, sizeof(mp));
@@ -585,13 +634,12 @@ int write_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const vo
       for (int32_t r = 0; r < rows; ++r)
         if (row_pos && row_pos[r] >= rope.n) return TFPA_ERANGE;
   }
-  std::vector<Run> runs;
+  thread_local std::vector<Run> runs;   // reused by every call of this thread
   if ((e = build_runs(segs, nseg, row_seg, row_pos, rows, runs))) return e;
   if (rows == 0) return TFPA_OK;
   if ((e = check_device())) return e;
   const size_t rd = (size_t)c->hkv * kHeadDim;
-  std::lock_guard<std::mutex> lock(g_mu);
-  static WriteParams p;
+  thread_local WriteParams p;
   size_t ri = 0;
   while (ri < runs.size()) {
     std::memset(&p, 0, sizeof(p));
@@ -672,8 +720,7 @@ extern "C" int tfpa_keep_kv(const tfpa_cache* c, const tfpa_seg* segs, int32_t n
   }
   if (n == 0) return TFPA_OK;
   if ((e = check_device())) return e;
-  std::lock_guard<std::mutex> lock(g_mu);
-  static KeepParams p;
+  thread_local KeepParams p;
   std::memset(&p, 0, sizeof(p));
   for (int32_t i = 0; i < n; ++i) {
     const tfpa_seg& g = segs[keep_seg[i]];
@@ -704,8 +751,7 @@ extern "C" int tfpa_stage_pages(int32_t* page_table, int32_t first, const int32_
   if (n == 0) return TFPA_OK;
   int e;
   if (!dry_run() && (e = check_device())) return e;
-  std::lock_guard<std::mutex> lock(g_mu);
-  static StageParams p;
+  thread_local StageParams p;
   for (int32_t done = 0; done < n; done += kMaxStage) {
     const int32_t m = std::min<int32_t>(kMaxStage, n - done);
     p.table = page_table;
@@ -744,7 +790,6 @@ int copy_impl(const tfpa_cache* c, const tfpa_seg* seg, int32_t p0, int32_t p1, 
   p.row_bytes = c->dtype == TFPA_FP8_E4M3 ? kHeadDim : 2 * kHeadDim;
   p.restore = restore ? 1 : 0;
   const int npages = (p1 - 1) / kPage - p0 / kPage + 1;
-  std::lock_guard<std::mutex> lock(g_mu);
   record(restore ? 7 : 6, p0, p1 - p0, 0, npages * c->hkv * 2, npages * c->hkv * 2, 0, 0);
   if (!dry_run())
     if ((e = to_err(launch_copy(p, npages, stream)))) return e;
@@ -764,10 +809,9 @@ extern "C" int tfpa_restore_kv(const tfpa_cache* cache, const tfpa_seg* seg, int
 }
 
 extern "C" void tfpa_set_launch_hook(tfpa_launch_hook hook, void* user, int dry_run_flag) {
-  std::lock_guard<std::mutex> lock(g_mu);
-  g_hook.fn = hook;
-  g_hook.user = user;
-  g_hook.dry = hook ? dry_run_flag : 0;
+  g_hook_user.store(user, std::memory_order_relaxed);
+  g_hook_dry.store(hook ? dry_run_flag : 0, std::memory_order_relaxed);
+  g_hook_fn.store(hook, std::memory_order_release);
 }
 
 extern "C" const char* tfpa_strerror(int code) {
@@ -798,7 +842,7 @@ extern "C" int tfpa_prefill(const tfpa_cache* c, const tfpa_seg* segs, int32_t n
   if ((e = check_cache(c)) || (e = check_segs(c, segs, nseg))) return e;
   if (rows > 0 && (!q || !aligned(q, 16) || !out || !aligned(out, 16))) return TFPA_EINVAL;
   if (max_rows_per_launch < 0 || !std::isfinite(scale) || !(scale > 0.f)) return TFPA_EINVAL;
-  std::vector<Run> runs;
+  thread_local std::vector<Run> runs;   // reused by every call of this thread
   if ((e = build_runs(segs, nseg, row_seg, row_pos, rows, runs))) return e;
   if (rows == 0) return TFPA_OK;
   if ((e = check_device())) return e;
@@ -809,8 +853,7 @@ extern "C" int tfpa_prefill(const tfpa_cache* c, const tfpa_seg* segs, int32_t n
   const int nsm = sm_count();
   if (nsm < 1) return TFPA_ECUDA;
   const size_t hd = (size_t)c->hq * kHeadDim;
-  std::lock_guard<std::mutex> lock(g_mu);
-  static PrefillParams p;
+  thread_local PrefillParams p;
   size_t ri = 0;
   int32_t taken = 0;
   while (ri < runs.size()) {

@@ -1280,20 +1280,19 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
 
 template <bool FP8, bool VERIFY>
 cudaError_t launch(const PrefillParams& p, int tiles, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
+  static PerDeviceOnce configured;
+  const cudaError_t e = configured.run([] {
     // The register split only works if the block launches with at least the
     // registers it hands out; otherwise setmaxnreg.inc would wait forever.
     cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, prefill_kernel<FP8, VERIFY>);
-    if (e != cudaSuccess) return e;
-    if (attr.numRegs * threads_of<FP8>() < regs_split<FP8>())
-      return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(prefill_kernel<FP8, VERIFY>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<FP8>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+    cudaError_t r = cudaFuncGetAttributes(&attr, prefill_kernel<FP8, VERIFY>);
+    if (r != cudaSuccess) return r;
+    if (attr.numRegs * threads_of<FP8>() < regs_split<FP8>()) return cudaErrorInvalidValue;
+    return cudaFuncSetAttribute(prefill_kernel<FP8, VERIFY>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Layout<FP8>::kSmemBytes);
+  });
+  if (e != cudaSuccess) return e;
   if (VERIFY)
     return launch_pdl(prefill_kernel<FP8, VERIFY>, dim3(tiles), dim3(threads_of<FP8>()),
                       Layout<FP8>::kSmemBytes, s, p);

@@ -207,12 +207,13 @@ cudaError_t launch_write_kv(const WriteParams& p, cudaStream_t s) {
 cudaError_t launch_keep(const KeepParams& p, cudaStream_t s) {
   if (p.n == 0) return cudaSuccess;
   const int smem = p.n * 2 * p.row_bytes;
-  static int configured = 0;
-  if (smem > 48 * 1024 && configured < smem) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        keep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxKeep * 2 * 256);
+  static PerDeviceOnce configured;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = configured.run([] {
+      return cudaFuncSetAttribute(keep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kMaxKeep * 2 * 256);
+    });
     if (e != cudaSuccess) return e;
-    configured = kMaxKeep * 2 * 256;
   }
   return launch_pdl(keep_kernel, dim3(p.hkv), dim3(kKeepThreads), smem, s, p);
 }

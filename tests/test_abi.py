@@ -247,3 +247,43 @@ def test_write_kv_rope_and_keep_argument_checks():
     with B.record_launches() as rec:
         B.tfpa_keep_kv(c, segs, [0, 0, 1], [3, 2, 7], [2, 1, 8])
     assert [(r["kind"], r["rows"], r["grid"]) for r in rec] == [("keep", 3, 8)]
+
+
+def test_planning_from_two_host_threads_at_once():
+    """Dry-run calls from two threads at once plan the same launches as one
+    thread alone (each thread builds its parameters in its own buffers)."""
+    import threading
+    c = _cache()
+    segs_a = [B.Seg(40000 + 37 * i, page_table=3 * FAKE) for i in range(6)]
+    segs_b = [B.Seg(9000, page_table=3 * FAKE), B.Seg(700, k_slab=8 * FAKE, v_slab=9 * FAKE,
+                                                    slab_cap=768)]
+    args_a = (np.repeat(np.arange(6), 3), np.concatenate([np.arange(L - 3, L) for L in
+                                                          (40000 + 37 * i for i in range(6))]))
+    args_b = (np.array([0] * 20 + [1]), np.array(list(range(8980, 9000)) + [699]))
+
+    def call(segs, rs, rp):
+        B.tfpa_decode(c, segs, 4 * FAKE, rs, rp, 0.088, B.Scratch(5 * FAKE, 6 * FAKE, 16),
+                      7 * FAKE, stream=0)
+
+    with B.record_launches() as rec:
+        call(segs_a, *args_a)
+    alone_a = list(rec)
+    with B.record_launches() as rec:
+        call(segs_b, *args_b)
+    alone_b = list(rec)
+
+    def worker(segs, args, n):
+        for _ in range(n):
+            call(segs, *args)
+
+    with B.record_launches() as rec:
+        ts = [threading.Thread(target=worker, args=(segs_a, args_a, 200)),
+              threading.Thread(target=worker, args=(segs_b, args_b, 200))]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+    # every launch of both threads was recorded; the multiset equals 200 of each alone
+    key = lambda r: tuple(sorted(r.items()))
+    want = sorted([key(r) for r in alone_a] * 200 + [key(r) for r in alone_b] * 200)
+    assert sorted(key(r) for r in rec) == want

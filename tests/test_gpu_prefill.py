@@ -115,3 +115,30 @@ def test_prompt_chunk_full_size_sampled(kv):
     assert_close(to_f64(out[rows]), ref, TOL[kv], "full prefill")
     assert_close(to_f64(lse[rows]), ref_lse, 1e-3, "full prefill lse")
     assert int(g.err.item()) == 0
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_257_row_chunk_on_the_full_prefix_slices_bitwise(kv):
+    """A 257-row chunk on the 28,672-position paged prefix (PR #1355, "Follow-up
+    checks": the 257-row chunk run as 128-row partial slices): 128 + 128 + 1
+    slices equal one launch, and both equal the contiguous path, bit for bit;
+    at this length every tile splits its key range over the cluster's two
+    CTAs and crosses many page edges.  Sampled rows against the oracle."""
+    from tests.test_gpu_full import oracle_stream
+    w = wl.prompt_chunk(prefix=28672, chunk=257, kv_dtype=kv)
+    g, scales = _case(w)
+    q = g.q()
+    one, l1 = g.prefill(q, w.row_seg, w.row_pos)
+    sl, l2 = g.prefill(q, w.row_seg, w.row_pos, max_rows=128)
+    assert np.array_equal(bits(one), bits(sl))
+    assert torch.equal(l1, l2)
+    gc = GpuCase(w, scales, all_paged=False)
+    cont, l3 = gc.prefill(gc.q(), w.row_seg, w.row_pos)
+    assert np.array_equal(bits(one), bits(cont))
+    assert torch.equal(l1, l3)
+    rows = np.array([0, 1, 127, 128, 200, 255, 256])
+    ref, ref_lse = oracle_stream(w, 0, rows, scales)
+    assert_close(to_f64(one[rows]), ref, TOL[kv], "257-row chunk, full prefix")
+    assert_close(to_f64(l1[rows]), ref_lse, 1e-3, "257-row chunk, full prefix, lse")
+    assert int(g.err.item()) == 0 and int(gc.err.item()) == 0

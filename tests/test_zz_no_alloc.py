@@ -37,6 +37,26 @@ def test_static_scratch_decode_matches_decode(name):
         assert np.array_equal(bits(out), bits(ref))
 
 
+def test_static_scratch_wide_run_matches_decode_bitwise():
+    """A 64-row run of one stream (256 query vectors per kv head at 32 / 8
+    heads) takes the tensor-core verify kernel; through the library's array it
+    runs in slices of 8 rows, and still gives tfpa_decode's bytes."""
+    import torch
+    from tests.test_gpu_edges import _make
+    L = 5000
+    w = _make([L], [True], [0] * 64, list(range(L - 64, L)), 32, 8, "bf16", seed=615)
+    g = GpuCase(w)
+    q = g.q()
+    ref, ref_lse = g.decode(q, w.row_seg, w.row_pos)
+    for call in range(2):
+        out = torch.empty_like(ref)
+        lse = torch.empty_like(ref_lse)
+        B.tfpa_decode_static(g.cache, g.segs, q, w.row_seg, w.row_pos, w.softmax_scale, out, lse)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(out), bits(ref)), f"call {call}"
+        assert torch.equal(lse, ref_lse)
+
+
 def test_static_scratch_refuses_head_counts_beyond_its_size():
     import torch
     w = wl.small("batched_decode")
