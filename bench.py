@@ -521,6 +521,67 @@ def time_save_restore(w, torch, B, reps):
     return nbytes, {k: statistics.median(v) for k, v in out.items()}
 
 
+def time_page_staging(w, torch, B, reps):
+    """Two consecutive prompt chunks of the prompt-chunk workload (rows
+    28,672..30,719, then 30,720..32,767; 8 new pages each).  Before each chunk
+    its 8 page ids are written into the stream's device page table, then its
+    K/V rows are stored (tfpa_write_kv) and its attention runs (tfpa_prefill).
+    The ids are written three ways: tfpa_stage_pages (ids in the launch
+    parameters), a copy from pinned host memory (cudaMemcpyAsync), and a copy
+    from pageable host memory, which the runtime performs only after the
+    stream's earlier work has finished, so the host stops between chunks.
+    CUDA events around both chunks, host enqueue included (no GPU sleep
+    first), L2 flushed before each pair; median ms per pair of chunks."""
+    cache, segs, _ = device_case(w, torch, B)
+    table = segs[0].page_table
+    ids = np.ascontiguousarray(w.streams[0].page_table, np.int32)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(17)
+    q = torch.randn(w.rows, w.hq, 128, generator=g, device="cuda").to(torch.bfloat16)
+    k = torch.randn(w.rows, w.hkv, 128, generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn(w.rows, w.hkv, 128, generator=g, device="cuda").to(torch.bfloat16)
+    out = torch.empty_like(q)
+    half = w.rows // 2
+    chunks = []
+    for c in range(2):
+        rp = np.ascontiguousarray(w.row_pos[c * half:(c + 1) * half])
+        first = int(rp[0]) // 256
+        n = half // 256
+        host = ids[first:first + n].copy()
+        chunks.append((c, rp, first, n, host, torch.from_numpy(host).pin_memory(),
+                       torch.from_numpy(host.copy())))
+    rs = np.zeros(half, np.int32)
+    flush = L2Flush(torch)
+    s = torch.cuda.current_stream()
+
+    def pair(mode):
+        for c, rp, first, n, host, pinned, pageable in chunks:
+            if mode == "stage":
+                B.tfpa_stage_pages(table, first, host)
+            elif mode == "pinned_copy":
+                table[first:first + n].copy_(pinned, non_blocking=True)
+            else:
+                table[first:first + n].copy_(pageable)
+            sl = slice(c * half, (c + 1) * half)
+            B.tfpa_write_kv(cache, segs, k[sl], v[sl], rs, rp)
+            B.tfpa_prefill(cache, segs, q[sl], rs, rp, w.softmax_scale, out[sl])
+
+    times = {m: [] for m in ("stage", "pinned_copy", "pageable_copy")}
+    for i in range(reps + 2):
+        for m in times:
+            flush(i)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            pair(m)
+            e1.record(s)
+            torch.cuda.synchronize()
+            if i >= 2:
+                times[m].append(e0.elapsed_time(e1))
+    assert int(cache.err_flag.item()) == 0, "kernel error flag set"
+    return {m: statistics.median(t) for m, t in times.items()}
+
+
 def wl_rope(n_pos):
     from paged_kv_cache_235_gb300 import workloads as wl
     return wl.rope_table(1e6, n_pos)
@@ -760,6 +821,20 @@ def main():
                                      "restore": gbs["restore"] / gbs["h2d"]},
             "note": "the reference is a plain runtime copy of the same byte count between a "
                     "contiguous device buffer and the same pinned buffer"}
+        w10 = wl.prompt_chunk()
+        t10 = time_page_staging(w10, torch, B, 10)
+        extra["page_staging"] = {
+            "workload": "two consecutive 2,048-row prompt chunks (positions 28,672..32,767, bf16, "
+                        "32/8 heads), each preceded by writing its 8 page ids into the device "
+                        "page table, then tfpa_write_kv and tfpa_prefill; host enqueue included, "
+                        "L2 flushed before each pair",
+            "ms_per_two_chunks": t10,
+            "gap_us_per_chunk_vs_stage": {m: (t - t10["stage"]) * 1e3 / 2
+                                          for m, t in t10.items() if m != "stage"},
+            "note": "stage = tfpa_stage_pages (ids in kernel parameters); pinned_copy = "
+                    "cudaMemcpyAsync from pinned memory; pageable_copy = a copy from pageable "
+                    "memory, which waits for the stream's earlier work (the host stops between "
+                    "chunks)"}
         for kvd in ("fp8", "bf16"):
             w7 = wl.tree_verify(kv_dtype=kvd)
             ms7 = time_tree_calls(w7, torch, B, 20)
