@@ -98,25 +98,14 @@ typedef struct {
 } tfpa_cache;
 
 /* Split-K scratch for decode partials (float32).
- *   part_o   : DEVICE [cap_rows][hq][max_splits][128]  unnormalised outputs o
- *   part_ml  : DEVICE [cap_rows][hq][max_splits][2]    (m, l): running max of the
- *              scores in log2 units (score * log2(e)) and the sum of 2^(s2 - m)
- *   counters : optional DEVICE int32 [cap_rows][hq], 4-byte aligned, all zero
- *              before the first call.  With counters, tfpa_decode and
- *              tfpa_decode_tree merge the rows of the decode partial kernel
- *              inside that kernel (the last split of a group of query vectors
- *              to finish merges the group, with the merge's arithmetic, so the
- *              bytes are those of the separate merge) and launch the merge
- *              kernel only for rows computed on tensor-core verify tiles.
- *              Every call leaves the counters zero again, except one whose
- *              kernel gave up a wait (err_flag bit 2): zero them after that.
- *              NULL: a separate merge kernel merges every row. */
+ *   part_o  : DEVICE [cap_rows][hq][max_splits][128]  unnormalised outputs o
+ *   part_ml : DEVICE [cap_rows][hq][max_splits][2]    (m, l): running max of the
+ *             scores in log2 units (score * log2(e)) and the sum of 2^(s2 - m)  */
 typedef struct {
   float* part_o;
   float* part_ml;
   int32_t cap_rows;               /* rows one partial launch can hold                      */
   int32_t max_splits;             /* >= tfpa_num_splits(seq_len) of every segment used     */
-  int32_t* counters;
 } tfpa_scratch;
 
 /* KV write with rotary position embedding: tfpa_write_kv, with each row's K

@@ -55,8 +55,7 @@ class tfpa_cache(ctypes.Structure):
 
 class tfpa_scratch(ctypes.Structure):
     _fields_ = [("part_o", ctypes.c_void_p), ("part_ml", ctypes.c_void_p),
-                ("cap_rows", ctypes.c_int32), ("max_splits", ctypes.c_int32),
-                ("counters", ctypes.c_void_p)]
+                ("cap_rows", ctypes.c_int32), ("max_splits", ctypes.c_int32)]
 
 
 class tfpa_launch_record(ctypes.Structure):
@@ -237,22 +236,16 @@ class Scratch(_Cached):
     part_ml: object
     cap_rows: int
     max_splits: int = MAX_SPLITS
-    counters: object = None       # int32 [cap_rows * hq], zero: merge inside the partial kernel
 
     def _make_c(self) -> tfpa_scratch:
-        return tfpa_scratch(_ptr(self.part_o), _ptr(self.part_ml), self.cap_rows, self.max_splits,
-                            _ptr(self.counters))
+        return tfpa_scratch(_ptr(self.part_o), _ptr(self.part_ml), self.cap_rows, self.max_splits)
 
 
-def make_scratch(cap_rows: int, hq: int, max_splits: int = MAX_SPLITS, device="cuda",
-                 fused_merge: bool = True) -> Scratch:
-    """Split-K scratch for cap_rows rows; with fused_merge, also the zeroed
-    group counters that let decode rows merge inside the partial kernel."""
+def make_scratch(cap_rows: int, hq: int, max_splits: int = MAX_SPLITS, device="cuda") -> Scratch:
     import torch
     o = torch.empty(cap_rows * hq * max_splits * HEAD_DIM, dtype=torch.float32, device=device)
     ml = torch.empty(cap_rows * hq * max_splits * 2, dtype=torch.float32, device=device)
-    cnt = torch.zeros(cap_rows * hq, dtype=torch.int32, device=device) if fused_merge else None
-    return Scratch(o, ml, cap_rows, max_splits, cnt)
+    return Scratch(o, ml, cap_rows, max_splits)
 
 
 class SegTable:

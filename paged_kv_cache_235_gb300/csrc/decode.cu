@@ -43,10 +43,8 @@ constexpr int kProducerWarp = 12;     // warps 13..15 only take part in the regi
 constexpr int kThreads = 16 * 32;
 // Registers after the split: the block launches with 512 x 128 = 65,536 and
 // 128 x (2 x kRegsConsumer + kRegsCombine + kRegsProducer) must not exceed it.
-// (176 / 128 / 32: the combiners also run the fused merge; 184 / 112 left
-// them spilling.)
-constexpr int kRegsConsumer = 176;
-constexpr int kRegsCombine = 128;
+constexpr int kRegsConsumer = 184;
+constexpr int kRegsCombine = 112;
 constexpr int kRegsProducer = 32;
 static_assert(128 * (2 * kRegsConsumer + kRegsCombine + kRegsProducer) <= 65536, "register split");
 // TMEM: two buffers (item parity) x two halves (consumer warps q, q+4) of
@@ -60,7 +58,7 @@ constexpr int kCombBytes = kCombineWarps * 16 * 32 * 16;
 constexpr int kMlBytes = kConsumerWarps * 16 * 2 * 4;
 constexpr int kNumBars = 2 * kStages + 7;
 constexpr int kSmemBytes =
-    kStages * kStageBytes + kCombBytes + kMlBytes + kStages * 4 + 8 + kNumBars * 8 + 1024;
+    kStages * kStageBytes + kCombBytes + kMlBytes + kStages * 4 + 4 + kNumBars * 8 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
@@ -242,63 +240,6 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, const RunInfo& ru,
       sc[hr] = p.scale_log2 * down * __ldg(p.k_scale + x.g);
     }
   }
-}
-
-// ---------------------------------------------------------------- merge
-// Log-sum-exp merge of one (row, head) by one warp: lane s holds split s's
-// (m, l); each lane owns 4 consecutive head-dim elements of the output.
-// Every slot below nsplit was written by a partial kernel (an empty split
-// holds o = 0 with weight 0).  The splits' o chunks are loaded kBatch at a
-// time, ahead of the sums that need them; the sums run in split order, so
-// the result does not depend on kBatch.  kL2: the partials were written by
-// other CTAs of the running kernel, so they are read from L2 (ld.global.cg).
-template <int kBatch, bool kL2>
-__device__ __forceinline__ void merge_one(const float* part_o, const float* part_ml,
-                                          size_t slot0, int nsplit, int lane,
-                                          __nv_bfloat16* out_row, float* lse_out) {
-  static_assert(kMaxSplits == 32 && kMaxSplits % kBatch == 0, "split batches");
-  const float4* po = reinterpret_cast<const float4*>(part_o + slot0 * kHeadDim) + lane;
-  float m = -INFINITY, l = 0.f;
-  if (lane < nsplit) {
-    const float2* pml = reinterpret_cast<const float2*>(part_ml + (slot0 + lane) * 2);
-    const float2 ml = kL2 ? __ldcg(pml) : *pml;
-    m = ml.x;
-    l = ml.y;
-  }
-  float M = m;
-#pragma unroll
-  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  const float a = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
-  float L = a * l;
-#pragma unroll
-  for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int u0 = 0; u0 < kMaxSplits; u0 += kBatch) {
-    if (u0 >= nsplit) break;
-    float4 v[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u)
-      if (u0 + u < nsplit) {
-        const float4* src = po + (u0 + u) * (kHeadDim / 4);
-        v[u] = kL2 ? __ldcg(src) : *src;
-      }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u)
-      if (u0 + u < nsplit) {
-        const float as = __shfl_sync(0xffffffffu, a, u0 + u);
-        acc.x = __fmaf_rn(as, v[u].x, acc.x);
-        acc.y = __fmaf_rn(as, v[u].y, acc.y);
-        acc.z = __fmaf_rn(as, v[u].z, acc.z);
-        acc.w = __fmaf_rn(as, v[u].w, acc.w);
-      }
-  }
-  const float inv = 1.f / L;
-  uint2 packed;
-  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2*>(out_row + lane * 4) = packed;
-  if (lse_out && lane == 0) *lse_out = (M + log2f(L)) * 0.6931471805599453f;
 }
 
 struct CombBars {
@@ -588,7 +529,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
 // fold and (m, l) buffers are never overwritten while still being read.
 template <bool FP8, bool GEN>
 __device__ void combiner(const DecodeParams& p, uint32_t tmem, float4* fold, float* ml_buf,
-                         volatile int* merge_flag, CombBars bars) {
+                         CombBars bars) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int q = warp - kCombineWarp0;
@@ -713,34 +654,6 @@ __device__ void combiner(const DecodeParams& p, uint32_t tmem, float4* fold, flo
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.done);
-    if (p.counters) {
-      // Merge inside the kernel: the item's partial stores (all four
-      // combiners, fenced) come before one arrival on its group's count;
-      // the arrival of the group's last split merges the group's query
-      // vectors, one warp per (row, head), as merge_kernel does.
-      __threadfence();
-      named_bar_sync(1, kCombineWarps * 32);
-      if (q == 0 && lane == 0) {
-        const int qv0 = x.mt * 16;
-        const int r0 = qv0 / p.group;
-        int* cnt = p.counters + (size_t)(ru.row0 + r0) * p.hq + x.g * p.group + (qv0 - r0 * p.group);
-        const int last = atomicAdd(cnt, 1) == ru.nsplit - 1;
-        if (last) *cnt = 0;                       // every split has arrived: reset for the next call
-        *merge_flag = last;
-      }
-      named_bar_sync(1, kCombineWarps * 32);
-      if (*merge_flag) {
-        __threadfence();
-        for (int i = q; i < 16; i += kCombineWarps) {
-          const int qv = x.mt * 16 + i;
-          if (qv >= nq) break;
-          const int r = qv / p.group;
-          const size_t rh = (size_t)(ru.row0 + r) * p.hq + x.g * p.group + (qv - r * p.group);
-          merge_one<8, true>(p.part_o, p.part_ml, rh * p.max_splits, ru.nsplit, lane,
-                             p.out + rh * kHeadDim, p.lse ? p.lse + rh : nullptr);
-        }
-      }
-    }
   }
 }
 
@@ -755,9 +668,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
   float* ml_buf = reinterpret_cast<float*>(smem + kStages * kStageBytes + kCombBytes);
   int* stage_bad = reinterpret_cast<int*>(ml_buf + kConsumerWarps * 16 * 2);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stage_bad + kStages);
-  volatile int* merge_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint64_t* bars = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(tmem_slot + 2) + 7) & ~uintptr_t(7));
+      (reinterpret_cast<uintptr_t>(tmem_slot + 1) + 7) & ~uintptr_t(7));
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* cbar = bars + 2 * kStages;
@@ -796,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
     consumer<FP8, GEN>(p, stage_mem, full, empty, stage_bad, tmem, cb);
   } else if (warp < kProducerWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCombine));
-    combiner<FP8, GEN>(p, tmem, fold, ml_buf, merge_flag, cb);
+    combiner<FP8, GEN>(p, tmem, fold, ml_buf, cb);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
     if (warp == kProducerWarp) producer<FP8>(p, stage_mem, full, empty, stage_bad);
@@ -809,23 +721,61 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
   }
 }
 
-// One warp per (row, head) of the listed runs (run ri covers warps
-// [w0, w0 + nrows * hq)).
+// ---------------------------------------------------------------- merge
+// One warp per (row, head): lane s holds split s's (m, l); lanes own 4
+// consecutive head-dim elements of the output.  Fixed summation order.
 __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ MergeParams p) {
   allow_next_grid();
   wait_prior_grid();
   const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (wid >= p.warps) return;
+  if (wid >= p.rows * p.hq) return;
+  const int row = wid / p.hq;
+  const int h = wid - row * p.hq;
   int ri = 0;
-  while (ri + 1 < p.nruns && p.runs[ri + 1].w0 <= wid) ++ri;
-  const MergeRun& mr = p.runs[ri];
-  const int local = wid - mr.w0;
-  const int row = mr.row0 + local / p.hq;
-  const int h = local - (row - mr.row0) * p.hq;
-  const size_t rh = (size_t)row * p.hq + h;
-  merge_one<kMaxSplits, false>(p.part_o, p.part_ml, rh * p.max_splits, mr.nsplit, lane,
-                               p.out + rh * kHeadDim, p.lse ? p.lse + rh : nullptr);
+  while (ri + 1 < p.nruns && p.runs[ri + 1].row0 <= row) ++ri;
+  const int nsplit = p.runs[ri].nsplit;
+  const size_t slot0 = ((size_t)row * p.hq + h) * p.max_splits;
+  // Every slot below nsplit was written by the partial kernel (an empty split
+  // holds o = 0 with weight 0).  Every split's o chunk is loaded together
+  // with the (m, l) pairs, before the reductions that need them, so a merge
+  // waits for one round of loads; the sums run in split order.
+  static_assert(kMaxSplits == 32, "one load per split");
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + slot0 * kHeadDim) + lane;
+  float4 v0[kMaxSplits];
+#pragma unroll
+  for (int u = 0; u < kMaxSplits; ++u)
+    if (u < nsplit) v0[u] = po[u * (kHeadDim / 4)];
+  float m = -INFINITY, l = 0.f;
+  if (lane < nsplit) {
+    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (slot0 + lane) * 2);
+    m = ml.x;
+    l = ml.y;
+  }
+  float M = m;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float a = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
+  float L = a * l;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto add = [&](int sp, const float4& v) {
+    const float as = __shfl_sync(0xffffffffu, a, sp);
+    acc.x = __fmaf_rn(as, v.x, acc.x);
+    acc.y = __fmaf_rn(as, v.y, acc.y);
+    acc.z = __fmaf_rn(as, v.z, acc.z);
+    acc.w = __fmaf_rn(as, v.w, acc.w);
+  };
+#pragma unroll
+  for (int u = 0; u < kMaxSplits; ++u)
+    if (u < nsplit) add(u, v0[u]);
+  const float inv = 1.f / L;
+  uint2 packed;
+  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(p.out + ((size_t)row * p.hq + h) * kHeadDim + lane * 4) = packed;
+  if (p.lse && lane == 0) p.lse[(size_t)row * p.hq + h] = (M + log2f(L)) * 0.6931471805599453f;
 }
 
 template <bool FP8, bool GEN>
@@ -861,8 +811,9 @@ cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cud
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
-  if (p.warps == 0) return cudaSuccess;
-  return launch_pdl(merge_kernel, dim3((p.warps + 7) / 8), dim3(256), 0, s, p);
+  const int warps = p.rows * p.hq;
+  if (warps == 0) return cudaSuccess;
+  return launch_pdl(merge_kernel, dim3((warps + 7) / 8), dim3(256), 0, s, p);
 }
 
 }  // namespace tfpa

@@ -398,7 +398,6 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
   if ((e = check_cache(c)) || (e = check_segs(c, segs, nseg))) return e;
   if (!sc || !sc->part_o || !sc->part_ml || sc->cap_rows < 1 || sc->max_splits < 1)
     return TFPA_EINVAL;
-  if (sc->counters && !aligned(sc->counters, 4)) return TFPA_EINVAL;
   if (rows > 0 && (!q || !aligned(q, 16))) return TFPA_EINVAL;
   if (sliced && rows > 0 && (!out || !aligned(out, 8))) return TFPA_EINVAL;
   if (anc && !aligned(anc, 8)) return TFPA_EINVAL;
@@ -415,9 +414,6 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
   const int nsm = sm_count();
   if (nsm < 1) return TFPA_ECUDA;
   const size_t hd = (size_t)c->hq * kHeadDim;
-  // With counters, decode runs merge inside the partial kernel; only verify
-  // runs (tensor-core tiles) need the merge kernel.
-  const bool fused = sliced && sc->counters != nullptr;
 
   size_t ri = 0;
   int32_t taken = 0;  // rows of runs[ri] already launched
@@ -440,8 +436,8 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
   while (ri < runs.size()) {
     SourceSet ss;
     const int32_t base = runs[ri].row0 + taken;  // first call row of this launch
-    int32_t nrows = 0, items = 0, tiles = 0, mwarps = 0;
-    int nr = 0, nd = 0, nv = 0, nm = 0;  // runs of the slice: all, decode, verify, merged
+    int32_t nrows = 0, items = 0, tiles = 0;
+    int nr = 0, nd = 0, nv = 0;  // runs of the slice: all, decode, verify
     while (ri < runs.size() && nr < kMaxRuns && nrows < sc->cap_rows) {
       const Run& r = runs[ri];
       const int src = ss.add(segs, r.seg);
@@ -456,18 +452,14 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
         info.nsplit = verify_num_splits(g.seq_len);
         info.item0 = tiles;
         tiles += c->hkv * ((take + vrows - 1) / vrows) * info.nsplit;
-        mp.runs[nm++] = MergeRun{nrows, take, info.nsplit, mwarps};
-        mwarps += take * c->hq;
+        mp.runs[nr] = MergeRun{nrows, take, info.nsplit, 0};
       } else {
         if (nd == 0) std::memset(&p, 0, sizeof(p));
         RunInfo& info = p.runs[nd++];
         fill_run(info, g, src, nrows, take, r.pos0 + taken);
         info.item0 = items;
         items += c->hkv * ((take * G + 15) / 16) * info.nsplit;
-        if (!fused) {
-          mp.runs[nm++] = MergeRun{nrows, take, info.nsplit, mwarps};
-          mwarps += take * c->hq;
-        }
+        mp.runs[nr] = MergeRun{nrows, take, info.nsplit, 0};
       }
       ++nr;
       nrows += take;
@@ -488,11 +480,6 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
       p.anc = anc ? anc + base : nullptr;   // the ancestor table shifts with the rows
       p.part_o = part_o;
       p.part_ml = part_ml;
-      if (fused) {
-        p.counters = sc->counters;    // [cap_rows][hq]: sliced launches start at scratch row 0
-        p.out = static_cast<__nv_bfloat16*>(out) + (size_t)base * hd;
-        p.lse = lse ? lse + (size_t)base * c->hq : nullptr;
-      }
       p.k_scale = c->k_scale;
       p.v_scale = c->v_scale;
       p.err_flag = c->err_flag;
@@ -538,16 +525,16 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
         if ((e = to_err(launch_verify(pv, fp8, tiles, stream)))) return e;
       }
     }
-    if (sliced && nm > 0) {
+    if (sliced) {
       mp.part_o = part_o;
       mp.part_ml = part_ml;
       mp.out = static_cast<__nv_bfloat16*>(out) + (size_t)base * hd;
       mp.lse = lse ? lse + (size_t)base * c->hq : nullptr;
-      mp.nruns = nm;
-      mp.warps = mwarps;
+      mp.nruns = nr;
+      mp.rows = nrows;
       mp.hq = c->hq;
       mp.max_splits = sc->max_splits;
-      record(2, base, mwarps / c->hq, nm, mwarps, (mwarps + 7) / 8, 0, (int64_t)base * hd);
+      record(2, base, nrows, nr, nrows * c->hq, (nrows * c->hq + 7) / 8, 0, (int64_t)base * hd);
       if (!dry_run()) {
         if ((e = to_err(launch_merge(mp, stream)))) return e;
       }
@@ -603,7 +590,7 @@ extern "C" int tfpa_merge(const tfpa_scratch* sc, int32_t hq, int32_t rows,
     while (r < rows && nr < (int)(sizeof(mp.runs) / sizeof(mp.runs[0]))) {
       int32_t n = 1;
       while (r + n < rows && nsplit[r + n] == nsplit[r]) ++n;
-      mp.runs[nr++] = MergeRun{r - base, n, nsplit[r], (r - base) * hq};
+      mp.runs[nr++] = MergeRun{r - base, n, nsplit[r], 0};
       r += n;
     }
     const size_t srow = (size_t)base * hq * sc->max_splits;
@@ -612,7 +599,7 @@ extern "C" int tfpa_merge(const tfpa_scratch* sc, int32_t hq, int32_t rows,
     mp.out = static_cast<__nv_bfloat16*>(out) + (size_t)base * hq * kHeadDim;
     mp.lse = lse ? lse + (size_t)base * hq : nullptr;
     mp.nruns = nr;
-    mp.warps = (r - base) * hq;
+    mp.rows = r - base;
     mp.hq = hq;
     mp.max_splits = sc->max_splits;
     record(2, base, r - base, nr, (r - base) * hq, ((r - base) * hq + 7) / 8, 0,

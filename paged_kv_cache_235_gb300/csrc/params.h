@@ -48,13 +48,6 @@ struct DecodeParams {
   const uint64_t* anc;        // rows of this launch: ancestor masks, or nullptr (causal)
   float* part_o;              // [cap_rows][hq][max_splits][128]
   float* part_ml;             // [cap_rows][hq][max_splits][2]
-  // Merge inside the partial kernel (counters != nullptr): the last of a
-  // (run, kv head, m-tile) group's splits to finish merges the group's
-  // partials into out / lse.  counters: [cap_rows][hq], the group's count at
-  // the slot of its first query vector; zero before the launch, left zero.
-  int32_t* counters;
-  __nv_bfloat16* out;         // rows of this launch: [rows][hq][128]
-  float* lse;                 // [rows][hq] or nullptr
   const float* k_scale;       // fp8: [hkv]
   const float* v_scale;
   int32_t* err_flag;
@@ -72,10 +65,10 @@ struct DecodeParams {
 };
 
 struct MergeRun {
-  int32_t row0;               // first row, relative to the launch
+  int32_t row0;
   int32_t nrows;
   int32_t nsplit;
-  int32_t w0;                 // its first (row, head) among the launch's warps
+  int32_t pad_;
 };
 
 struct MergeParams {
@@ -85,7 +78,7 @@ struct MergeParams {
   __nv_bfloat16* out;         // rows of this launch: [rows][hq][128]
   float* lse;                 // [rows][hq] or nullptr
   int32_t nruns;
-  int32_t warps;              // (row, head) pairs merged: the listed runs' rows x hq
+  int32_t rows;
   int32_t hq;
   int32_t max_splits;
 };

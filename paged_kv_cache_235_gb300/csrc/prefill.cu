@@ -42,8 +42,8 @@
 // head) and both slots read it: slot A takes the split's even key tiles,
 // slot B the odd ones, and the CTA merges the two into the split's partial.
 // bf16: rings of three K and V stages over the slots' common tile order.
-// e4m3: two e4m3 K stages per slot (8-bit S MMAs), one V staging tile per
-// slot, and a ring of three f16 V stages over the slots' common tile order.
+// e4m3: two e4m3 K stages per slot (8-bit S MMAs), two V staging tiles per
+// slot, one f16 V stage per slot.
 // TMEM (512 columns): S_A [0,128) O_A [128,256) S_B [256,384) O_B [384,512).
 // CTA 1's partial lands in CTA 0's shared memory once CTA 0's MMAs are done:
 // O (float32 [2 heads][128 rows][128], 16-byte chunks permuted by row against
@@ -75,14 +75,14 @@ constexpr int kOffV8 = 212992;           // prefill, e4m3: the V staging tile, 1
 // is K stage 2 of the rings of three.  e4m3: the Q tile becomes two e4m3
 // tiles (hi and lo, 16 KB each) that feed 8-bit MMAs with K straight from
 // its e4m3 stages, four of 16 KB over the 16-bit K region, two per slot; V
-// still goes through the converters, from two e4m3 staging tiles (one per
-// slot) in the second Q tile into a ring of three 16-bit V stages (V stage
-// 2 over the prefill staging pair), as the bf16 V ring.
+// still goes through the converters, from four e4m3 staging tiles (two per
+// slot): the prefill staging pair and the second Q tile.
 constexpr int kOffQ2 = 32768;
 __device__ __forceinline__ int stage8_off(bool is_v) { return is_v ? kOffV8 : kOffK8; }
-// Verify, e4m3: the V staging tile of slot hh, and K stage i (2 x slot +
-// step parity).
-__device__ __forceinline__ int vstage8_off(int hh) { return kOffQ2 + hh * 16384; }
+// Verify, e4m3: V staging tile i (2 x slot + step parity) and K stage i.
+__device__ __forceinline__ int vstage8_off(int i) {
+  return i < 2 ? kOffK8 + i * 16384 : kOffQ2 + (i - 2) * 16384;
+}
 __device__ __forceinline__ int kstage8_off(int i) { return kOffK + i * 16384; }
 // Verify, bf16: a ring of three 16-bit stages each for K and V over the
 // CTA's key tiles in the slots' common order (tile n = 2 step + slot in
@@ -106,35 +106,27 @@ constexpr uint32_t kTmemCols = 512;
 // launches with (e4m3: 512 x 128, bf16: 384 x 168), and no SM sub-partition
 // (one warp of each warpgroup) more than its 16,384.  The bf16 split was
 // picked by measurement: 64 / 216 ran 2.7 % faster than no split, where
-// 56 / 224 and 72 / 216 (the latter without any spill) ran slower.  e4m3
-// prompt tiles: 56 / 200 / 56.  e4m3 verify tiles: 64 / 200 / 48, which
-// leaves their producer without spills (at 56 for warps 0-3 it spilled).
-template <bool FP8, bool VERIFY>
-struct Regs {
-  static constexpr int kLow = 64, kHigh = 216, kConv = 0, kLaunch = 168;
-};
+// 56 / 224 and 72 / 216 (the latter without any spill) ran slower.
+template <bool FP8>
+struct Regs;
 template <>
-struct Regs<true, false> {
+struct Regs<true> {
   static constexpr int kLow = 56, kHigh = 200, kConv = 56, kLaunch = 128;
 };
 template <>
-struct Regs<true, true> {
-  static constexpr int kLow = 64, kHigh = 200, kConv = 48, kLaunch = 128;
+struct Regs<false> {
+  static constexpr int kLow = 64, kHigh = 216, kConv = 0, kLaunch = 168;
 };
-template <bool FP8, bool VERIFY>
+template <bool FP8>
 constexpr int regs_split() {
-  using R = Regs<FP8, VERIFY>;
-  return 128 * (R::kLow + 2 * R::kHigh + R::kConv);
+  return 128 * (Regs<FP8>::kLow + 2 * Regs<FP8>::kHigh + Regs<FP8>::kConv);
 }
-template <bool FP8, bool VERIFY>
-constexpr bool regs_fit() {
-  using R = Regs<FP8, VERIFY>;
-  return regs_split<FP8, VERIFY>() <= threads_of<FP8>() * R::kLaunch &&
-         32 * (R::kLow + 2 * R::kHigh + R::kConv) <= 16384;   // per SM sub-partition
-}
-static_assert(regs_fit<true, false>() && regs_fit<true, true>() && regs_fit<false, false>() &&
-                  regs_fit<false, true>(),
-              "register split");
+static_assert(regs_split<true>() <= 512 * Regs<true>::kLaunch, "register split");
+static_assert(regs_split<false>() <= 384 * Regs<false>::kLaunch, "register split");
+static_assert(32 * (Regs<true>::kLow + 2 * Regs<true>::kHigh + Regs<true>::kConv) <= 16384,
+              "sub-partition registers");
+static_assert(32 * (Regs<false>::kLow + 2 * Regs<false>::kHigh) <= 16384,
+              "sub-partition registers");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 __device__ __forceinline__ uint32_t col_s(int hh) { return hh ? 256u : 0u; }
 __device__ __forceinline__ uint32_t col_o(int hh) { return hh ? 384u : 128u; }
@@ -144,12 +136,12 @@ struct Bars {
   uint64_t* q_ready;     // Q operand ready for the MMA (e4m3 caches: after conversion)
   uint64_t* k_full;      // [2] K operand stage ready (verify: bf16 [3], e4m3 [4])
   uint64_t* k_empty;     // [2] (verify: bf16 [3], e4m3 [4])
-  uint64_t* v_full;      // [2] 16-bit V operand stage ready (verify: [3])
-  uint64_t* v_empty;     // [2] (verify: [3])
+  uint64_t* v_full;      // [2] (verify, bf16: [3])
+  uint64_t* v_empty;     // [2] (verify, bf16: [3])
   uint64_t* k8_full;     // prefill, e4m3: the staging tile landed / free
   uint64_t* k8_empty;
-  uint64_t* v8_full;     // (verify, e4m3: [2], one per slot)
-  uint64_t* v8_empty;    // (verify, e4m3: [2])
+  uint64_t* v8_full;     // (verify, e4m3: [4])
+  uint64_t* v8_empty;    // (verify, e4m3: [4])
   uint64_t* s_full;      // [2] per head: S in TMEM
   uint64_t* p_ready;     // [2] per head: P in TMEM, O corrected
   uint64_t* o_final;
@@ -386,20 +378,19 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
     w = (int)ph;
   };
   if (VERIFY && FP8) {
-    // Step jj, slot hh: K into e4m3 stage 2 hh + (jj & 1) at phase
-    // (jj >> 1) & 1, V into slot hh's staging tile at phase jj & 1; K of both
-    // slots, then V of both.  last_k*, last_v*: each slot's last step loaded.
+    // Step jj, slot hh: K into e4m3 stage 2 hh + (jj & 1), V into staging
+    // tile 2 hh + (jj & 1), each at phase (jj >> 1) & 1; K of both slots,
+    // then V of both.  last_k*, last_v*: each slot's last step loaded.
     for (int j = gm.kt0; j < gm.kt0 + kAhead; ++j) prefetch(j);
     bool ok = true;
     for (int jj = 0; ok && jj < slot_tiles<true>(gm, 0); ++jj) {
       prefetch(gm.kt0 + 2 * jj + kAhead);
       prefetch(gm.kt0 + 2 * jj + 1 + kAhead);
-      const uint32_t ph_k = (jj >> 1) & 1, ph_v = jj & 1;
+      const uint32_t ph = (jj >> 1) & 1;
       for (int kv = 0; ok && kv < 2; ++kv)
         for (int hh = 0; ok && hh < 2; ++hh) {
           if (jj >= slot_tiles<true>(gm, hh)) continue;
-          const int i = kv ? hh : 2 * hh + (jj & 1);
-          const uint32_t ph = kv ? ph_v : ph_k;
+          const int i = 2 * hh + (jj & 1);
           uint64_t* empty = kv ? b.v8_empty + i : b.k_empty + i;
           uint64_t* full = kv ? b.v8_full + i : b.k_full + i;
           const int y = row_of(slot_tile<true>(gm, jj, hh));
@@ -445,21 +436,16 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
     // Let this CTA's loads in flight land before it exits.
     mbar_wait(b.q_full, 0, p.err_flag);
     if (VERIFY && FP8) {
-      // K: each slot's last two steps loaded (its two stages alternate by
-      // step); V: each slot's last step (one staging tile per slot, loaded
-      // only once the previous load was converted)
+      // each slot's last two steps loaded (buffers alternate by step)
       const int lasts[4] = {last_k0, last_k1, last_v0, last_v1};
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int hh = u & 1;
+        uint64_t* full = u < 2 ? b.k_full : b.v8_full;
 #pragma unroll
         for (int d = 0; d < 2; ++d) {
           const int jj = lasts[u] - d;
-          if (jj < 0) continue;
-          if (u < 2)
-            mbar_wait(b.k_full + 2 * hh + (jj & 1), (uint32_t)((jj >> 1) & 1), p.err_flag);
-          else if (d == 0)
-            mbar_wait(b.v8_full + hh, (uint32_t)(jj & 1), p.err_flag);
+          if (jj >= 0) mbar_wait(full + 2 * hh + (jj & 1), (uint32_t)((jj >> 1) & 1), p.err_flag);
         }
       }
     } else if (FP8) {
@@ -509,19 +495,10 @@ __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, i
     }
     const uint32_t half = db + (uint32_t)(c8 >> 2) * 16384u;
     const int c16 = 2 * (c8 & 3);
-    // The eight threads of a row (one 128-bit store phase) write chunks
-    // c16 and c16 + 1 of two halves that share banks: threads of the second
-    // half store their odd chunk first, so each phase hits eight distinct
-    // 16-byte bank groups.
-    const int odd_first = c8 >> 2;
-    const uint32_t a0 = swz128(half, row, c16 + odd_first);
-    const uint32_t a1 = swz128(half, row, c16 + 1 - odd_first);
-    const uint4 lo = make_uint4(h[0], h[1], h[2], h[3]), hi = make_uint4(h[4], h[5], h[6], h[7]);
-    const uint4 f = odd_first ? hi : lo, g = odd_first ? lo : hi;
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a0), "r"(f.x), "r"(f.y), "r"(f.z),
-                 "r"(f.w) : "memory");
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a1), "r"(g.x), "r"(g.y), "r"(g.z),
-                 "r"(g.w) : "memory");
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(swz128(half, row, c16)),
+                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(swz128(half, row, c16 + 1)),
+                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]) : "memory");
   }
 }
 
@@ -535,8 +512,7 @@ __device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileG
   const int t = threadIdx.x - kConvWarp0 * 32;   // 0..127
   const int lane = threadIdx.x & 31;
   // Staging tile `src` (K, or V with rows from z0 on zeroed: past the
-  // stream's end, or all rows of a bad page) into 16-bit stage s (the V
-  // stages, three in verify mode, lie back to back from kOffV).
+  // stream's end, or all rows of a bad page) into 16-bit stage s.
   auto convert = [&](bool is_v, int s, uint32_t ph, int z0, int src, uint32_t ph8,
                      uint64_t* full8, uint64_t* empty8) {
     uint64_t* empty = is_v ? &b.v_empty[s] : &b.k_empty[s];
@@ -561,11 +537,9 @@ __device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileG
         if (jj >= slot_tiles<true>(gm, hh)) continue;
         const int j = slot_tile<true>(gm, jj, hh);
         const int z0 = v_zero_from(ru, j, hh ? pc1.bad(j) : pc0.bad(j));
-        // tile n = 2 jj + hh of the slots' common order: 16-bit stage n mod 3
-        // at phase (n / 3) & 1, from slot hh's staging tile at phase jj & 1
-        const int n = 2 * jj + hh;
-        ok = convert(true, n % 3, (uint32_t)((n / 3) & 1), z0, vstage8_off(hh),
-                     (uint32_t)(jj & 1), b.v8_full + hh, b.v8_empty + hh);
+        const int i = 2 * hh + (jj & 1);
+        ok = convert(true, hh, jj & 1, z0, vstage8_off(i), (uint32_t)((jj >> 1) & 1),
+                     b.v8_full + i, b.v8_empty + i);
       }
     }
     return;
@@ -633,15 +607,15 @@ __device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const Tile
     return;
   }
   if (VERIFY) {
-    // Slot hh, step jj, tile n = 2 jj + hh: V in 16-bit stage n mod 3 at
-    // phase (n / 3) & 1; K likewise with a bf16 cache, in e4m3 stage
-    // 2 hh + (jj & 1) at phase (jj >> 1) & 1 with an e4m3 cache.
+    // Slot hh, step jj.  bf16: K and V of tile n = 2 jj + hh in stage n mod
+    // 3 at phase (n / 3) & 1.  e4m3: K in e4m3 stage 2 hh + (jj & 1) at phase
+    // (jj >> 1) & 1, V in 16-bit stage hh at phase jj & 1.
     auto kst = [&](int hh, int jj) { return FP8 ? 2 * hh + (jj & 1) : (2 * jj + hh) % 3; };
     auto kph = [&](int hh, int jj) {
       return (uint32_t)(FP8 ? (jj >> 1) & 1 : ((2 * jj + hh) / 3) & 1);
     };
-    auto vst = [&](int hh, int jj) { return (2 * jj + hh) % 3; };
-    auto vph = [&](int hh, int jj) { return (uint32_t)(((2 * jj + hh) / 3) & 1); };
+    auto vst = [&](int hh, int jj) { return FP8 ? hh : (2 * jj + hh) % 3; };
+    auto vph = [&](int hh, int jj) { return (uint32_t)(FP8 ? jj & 1 : ((2 * jj + hh) / 3) & 1); };
     bool ok = mbar_wait_or_abort(b.q_ready, 0, p.err_flag, b.abort);
     for (int hh = 0; ok && hh < 2; ++hh) {
       if (slot_tiles<true>(gm, hh) == 0) continue;
@@ -1177,21 +1151,20 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   Bars b;
   b.q_full = bars + 0;
   b.q_ready = FP8 ? bars + 1 : bars + 0;
-  // Verify with an e4m3 cache: four K stages (bars 2-5 full, 10-13 empty),
-  // two V staging tiles (6-7 full, 8-9 empty) and a ring of three 16-bit V
-  // stages (24-26 full, 27-29 empty); no K staging.
+  // Verify with an e4m3 cache: four K stages (bars 2-5 full, 10-13 empty)
+  // and four V staging tiles (24-27 full, 28-31 empty); no K staging.
   // Verify with a bf16 cache: rings of three, K full 24-26 and empty 27-29,
   // V full 2-4 and empty 5-7.
   constexpr bool kDirectK = VERIFY && FP8;
   constexpr bool kRing3 = VERIFY && !FP8;
   b.k_full = kRing3 ? bars + 24 : bars + 2;
   b.k_empty = kDirectK ? bars + 10 : kRing3 ? bars + 27 : bars + 4;
-  b.v_full = kRing3 ? bars + 2 : kDirectK ? bars + 24 : bars + 6;
-  b.v_empty = kRing3 ? bars + 5 : kDirectK ? bars + 27 : bars + 8;
+  b.v_full = kRing3 ? bars + 2 : bars + 6;
+  b.v_empty = kRing3 ? bars + 5 : bars + 8;
   b.k8_full = bars + 10;
   b.k8_empty = bars + 11;
-  b.v8_full = kDirectK ? bars + 6 : bars + 12;
-  b.v8_empty = kDirectK ? bars + 8 : bars + 13;
+  b.v8_full = kDirectK ? bars + 24 : bars + 12;
+  b.v8_empty = kDirectK ? bars + 28 : bars + 13;
   b.s_full = bars + 14;
   b.p_ready = bars + 16;
   b.o_final = bars + 18;
@@ -1210,7 +1183,7 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
       mbar_init(&b.s_full[i], 1);
       mbar_init(&b.p_ready[i], 4);
     }
-    for (int i = 0; i < (VERIFY ? 3 : 2); ++i) {
+    for (int i = 0; i < (kRing3 ? 3 : 2); ++i) {
       mbar_init(&b.v_full[i], stage_arrivals);
       mbar_init(&b.v_empty[i], 1);
     }
@@ -1218,8 +1191,6 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
       for (int i = 0; i < 4; ++i) {
         mbar_init(&b.k_full[i], 1);                // the producer's TMA
         mbar_init(&b.k_empty[i], 1);
-      }
-      for (int i = 0; i < 2; ++i) {
         mbar_init(&b.v8_full[i], 1);
         mbar_init(&b.v8_empty[i], kConvWarps);
       }
@@ -1265,17 +1236,17 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   const TileGeom gm = geom_of<VERIFY>(p, ru, x, rank);
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8, VERIFY>::kLow));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kLow));
     if (warp == 0) {
       if (lane == 0) producer<FP8, VERIFY>(p, ru, x, gm, smem, b);
     } else if (warp == 1) {
       mma_issuer<FP8, VERIFY>(p, ru, gm, smem, tmem, b);
     }
   } else if (warp < kConvWarp0) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<FP8, VERIFY>::kHigh));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kHigh));
     softmax_role<FP8, VERIFY>(p, ru, x, gm, rank, (warp - 4) >> 2, smem, tmem, b);
   } else if (FP8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8, VERIFY>::kConv));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kConv));
     converter<VERIFY>(p, ru, gm, smem, b);
   }
   umma::fence_before_sync();
@@ -1296,7 +1267,7 @@ cudaError_t launch(const PrefillParams& p, int tiles, cudaStream_t s) {
     cudaFuncAttributes attr;
     cudaError_t r = cudaFuncGetAttributes(&attr, prefill_kernel<FP8, VERIFY>);
     if (r != cudaSuccess) return r;
-    if (attr.numRegs * threads_of<FP8>() < regs_split<FP8, VERIFY>()) return cudaErrorInvalidValue;
+    if (attr.numRegs * threads_of<FP8>() < regs_split<FP8>()) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(prefill_kernel<FP8, VERIFY>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Layout<FP8>::kSmemBytes);

@@ -287,32 +287,3 @@ def test_planning_from_two_host_threads_at_once():
     key = lambda r: tuple(sorted(r.items()))
     want = sorted([key(r) for r in alone_a] * 200 + [key(r) for r in alone_b] * 200)
     assert sorted(key(r) for r in rec) == want
-
-
-def test_fused_merge_launches_the_merge_kernel_only_for_verify_rows():
-    """With scratch counters, decode-kernel rows merge inside the partial
-    kernel: a slice of narrow runs launches no merge kernel, and a slice with
-    a wide (tensor-core verify) run launches one merge over that run's rows."""
-    c = _cache()
-    sc = B.Scratch(5 * FAKE, 6 * FAKE, 128, 32, 8 * FAKE)
-    segs = [B.Seg(9000, page_table=3 * FAKE), B.Seg(700, k_slab=8 * FAKE, v_slab=9 * FAKE,
-                                                    slab_cap=768)]
-    with B.record_launches() as rec:
-        B.tfpa_decode(c, segs, 4 * FAKE, [0, 1], [8999, 699], 0.088, sc, 7 * FAKE)
-    assert [r["kind"] for r in rec] == ["partial"]
-    rs = [0] * 20 + [1]
-    rp = list(range(8980, 9000)) + [699]
-    with B.record_launches() as rec:
-        B.tfpa_decode(c, segs, 4 * FAKE, rs, rp, 0.088, sc, 7 * FAKE)
-    assert [r["kind"] for r in rec] == ["partial", "verify", "merge"]
-    merge = rec[-1]
-    assert (merge["rows"], merge["runs"], merge["items"]) == (20, 1, 20 * 32)
-    # the plain partial entry point never merges
-    with B.record_launches() as rec:
-        B.tfpa_decode_partial(c, segs, 4 * FAKE, [0, 1], [8999, 699], 0.088, sc)
-    assert [r["kind"] for r in rec] == ["partial"]
-    with B.record_launches() as rec:
-        with pytest.raises(B.TfpaError) as e:
-            B.tfpa_decode(c, segs, 4 * FAKE, [0], [8999], 0.088,
-                          B.Scratch(5 * FAKE, 6 * FAKE, 128, 32, 8 * FAKE + 2), 7 * FAKE)
-    assert e.value.code == B.TFPA_EINVAL and rec == []
