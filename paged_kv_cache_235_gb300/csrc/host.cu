@@ -520,10 +520,9 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
       pv.rows = nrows;
       pv.max_splits = sc->max_splits;
       pv.scale_log2 = scale * 1.4426950408889634f;
-      const int vgrid = std::min(tiles, nsm);   // persistent CTAs, one per SM at most
-      record(8, base, nrows, nv, tiles, vgrid, (int64_t)base * hd, 0);
+      record(8, base, nrows, nv, tiles, tiles, (int64_t)base * hd, 0);
       if (!dry_run()) {
-        if ((e = to_err(launch_verify(pv, fp8, vgrid, stream)))) return e;
+        if ((e = to_err(launch_verify(pv, fp8, tiles, stream)))) return e;
       }
     }
     if (sliced) {

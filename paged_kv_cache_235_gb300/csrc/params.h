@@ -202,9 +202,8 @@ cudaError_t launch_stage(const StageParams& p, cudaStream_t s);
 cudaError_t launch_copy(const CopyParams& p, int npages, cudaStream_t s);
 cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
-// Prefill launches a cluster of two CTAs per tile; verify `grid` persistent
-// CTAs over p.n_tiles tiles.
+// Prefill launches a cluster of two CTAs per tile; verify one CTA per tile.
 cudaError_t launch_prefill(const PrefillParams& p, bool fp8, int tiles, cudaStream_t s);
-cudaError_t launch_verify(const PrefillParams& p, bool fp8, int grid, cudaStream_t s);
+cudaError_t launch_verify(const PrefillParams& p, bool fp8, int tiles, cudaStream_t s);
 
 }  // namespace tfpa

@@ -37,10 +37,8 @@
 // scores and to the output.  Verify tiles on an e4m3 cache instead split Q
 // into two e4m3 tiles (hi + lo) and take S from 8-bit MMAs straight off the
 // e4m3 K tiles, so only V passes through the converters.
-// Verify mode (launch_verify): tiles (run, kv head, 128 / G rows, key
-// split), no cluster; persistent CTAs, one per SM, each walking tiles
-// blockIdx.x, + gridDim.x, ... with its rings and barriers carried from one
-// tile to the next, so a tile's loads start while the previous one ends.  One Q tile holds the group's query vectors (row x
+// Verify mode (launch_verify): one CTA per tile (run, kv head, 128 / G rows,
+// key split), no cluster.  One Q tile holds the group's query vectors (row x
 // head) and both slots read it: slot A takes the split's even key tiles,
 // slot B the odd ones, and the CTA merges the two into the split's partial.
 // bf16: rings of three K and V stages over the slots' common tile order.
@@ -93,10 +91,10 @@ __device__ __forceinline__ int kstage8_off(int i) { return kOffK + i * 16384; }
 __device__ __forceinline__ int kstage16_off(int t) { return t < 2 ? kOffK + t * 32768 : kOffQ2; }
 template <bool FP8>
 struct Layout {
-  static constexpr int kOffBar = 229376;     // 34 barriers
+  static constexpr int kOffBar = 229376;
   // Verify: the Q rows' scale factors (e4m3 caches; 128 floats) and slot
   // B's (m, l) per row for the merge of the two slots (128 float2).
-  static constexpr int kOffDown = kOffBar + 34 * 8;
+  static constexpr int kOffDown = kOffBar + 256;
   static constexpr int kOffMl = kOffDown + 512;
   static constexpr int kSmemBytes = kOffMl + 1024 + 1024;
 };
@@ -109,38 +107,26 @@ constexpr uint32_t kTmemCols = 512;
 // (one warp of each warpgroup) more than its 16,384.  The bf16 split was
 // picked by measurement: 64 / 216 ran 2.7 % faster than no split, where
 // 56 / 224 and 72 / 216 (the latter without any spill) ran slower.
-// Persistent verify CTAs carry their tile loop's counts in every role: 80 /
-// 208 (bf16) and 72 / 200 / 40 (e4m3) spill least (8 and 4 bytes).
-template <bool FP8, bool VERIFY>
-struct Regs {
-  static constexpr int kLow = 64, kHigh = 216, kConv = 0, kLaunch = 168;
-};
+template <bool FP8>
+struct Regs;
 template <>
-struct Regs<false, true> {
-  static constexpr int kLow = 80, kHigh = 208, kConv = 0, kLaunch = 168;
-};
-template <>
-struct Regs<true, false> {
+struct Regs<true> {
   static constexpr int kLow = 56, kHigh = 200, kConv = 56, kLaunch = 128;
 };
 template <>
-struct Regs<true, true> {
-  static constexpr int kLow = 72, kHigh = 200, kConv = 40, kLaunch = 128;
+struct Regs<false> {
+  static constexpr int kLow = 64, kHigh = 216, kConv = 0, kLaunch = 168;
 };
-template <bool FP8, bool VERIFY>
+template <bool FP8>
 constexpr int regs_split() {
-  using R = Regs<FP8, VERIFY>;
-  return 128 * (R::kLow + 2 * R::kHigh + R::kConv);
+  return 128 * (Regs<FP8>::kLow + 2 * Regs<FP8>::kHigh + Regs<FP8>::kConv);
 }
-template <bool FP8, bool VERIFY>
-constexpr bool regs_fit() {
-  using R = Regs<FP8, VERIFY>;
-  return regs_split<FP8, VERIFY>() <= threads_of<FP8>() * R::kLaunch &&
-         32 * (R::kLow + 2 * R::kHigh + R::kConv) <= 16384;   // per SM sub-partition
-}
-static_assert(regs_fit<true, false>() && regs_fit<true, true>() && regs_fit<false, false>() &&
-                  regs_fit<false, true>(),
-              "register split");
+static_assert(regs_split<true>() <= 512 * Regs<true>::kLaunch, "register split");
+static_assert(regs_split<false>() <= 384 * Regs<false>::kLaunch, "register split");
+static_assert(32 * (Regs<true>::kLow + 2 * Regs<true>::kHigh + Regs<true>::kConv) <= 16384,
+              "sub-partition registers");
+static_assert(32 * (Regs<false>::kLow + 2 * Regs<false>::kHigh) <= 16384,
+              "sub-partition registers");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 __device__ __forceinline__ uint32_t col_s(int hh) { return hh ? 256u : 0u; }
 __device__ __forceinline__ uint32_t col_o(int hh) { return hh ? 384u : 128u; }
@@ -162,8 +148,6 @@ struct Bars {
   uint64_t* drain;
   uint64_t* peer_ready;  // CTA 0: CTA 1's softmax threads stored their partial here
   uint64_t* dst_free;    // CTA 1: CTA 0's MMAs are done with its rings
-  uint64_t* q_empty;     // verify: the tile's S MMAs are done with the Q tile
-  uint64_t* o_free;      // verify: slot A read both slots' O (the next tile's PV may start)
   uint32_t* tmem_slot;
   volatile int* abort;
 };
@@ -297,61 +281,21 @@ __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, i
 // the tile kAhead steps ahead into L2.
 constexpr int kAhead = 4;
 
-// Verify mode runs persistent CTAs (tiles blockIdx.x, + gridDim.x, ...),
-// and its rings and barriers carry on from one tile to the next: each role
-// counts what it has passed, and every stage index and phase parity derives
-// from these counts.  A prompt-chunk CTA runs one tile with all counts 0.
-struct Pipe {
-  int q;          // tiles with keys so far (Q loads and splits)
-  int tile;       // tiles so far (o_final and o_free completions)
-  int step_a;     // steps of slot A so far
-  int step_b;     // steps of slot B so far
-  int common;     // key tiles so far in the slots' common order (bf16 verify rings)
-  // Slot hh's steps so far (a select, not an indexed array, so the counts
-  // stay in registers).
-  __device__ __forceinline__ int step(int hh) const { return hh ? step_b : step_a; }
-  __device__ __forceinline__ void advance(const TileGeom& gm, bool verify) {
-    q += gm.nkt > 0;
-    ++tile;
-    step_a += verify ? (gm.nkt + 1) >> 1 : gm.nkt;
-    step_b += verify ? gm.nkt >> 1 : gm.nkt;
-    common += gm.nkt;
-  }
-};
-
-// The producer's loads in flight, one bit per stage barrier: bit set = a
-// load was issued, with its phase parity in `phase`.  An aborting CTA waits
-// for each before it exits.
-struct Drain {
-  uint32_t issued = 0, phase = 0;
-  __device__ void note(int bit, uint32_t ph) {
-    issued |= 1u << bit;
-    phase = (phase & ~(1u << bit)) | (ph << bit);
-  }
-};
-constexpr int kBitK = 0, kBitV = 4, kBitK8 = 8, kBitV8 = 9, kBitQ = 10;
-
-// One tile's loads.  Returns false if the CTA is aborting.
 template <bool FP8, bool VERIFY>
-__device__ bool producer_tile(const PrefillParams& p, const RunInfo& ru, const Tile& x,
-                              const TileGeom& gm, uint8_t* smem, const Bars& b, const Pipe& ps,
-                              Drain& dr, int& staged_k, int& staged_v) {
+__device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& x,
+                         const TileGeom& gm, uint8_t* smem, const Bars& b) {
   const CUtensorMap* mk = &p.maps[ru.src].k;
   const CUtensorMap* mv = &p.maps[ru.src].v;
-  if (gm.nkt == 0) return true;
+  if (gm.nkt == 0) return;
   if (VERIFY) {
     // One Q tile, both slots: 128 / G rows x the group's G heads (box 64 x G
     // x rows, landing as M row G (row) + head).  Rows past the run hold the
-    // next rows or zeros, which no output reads.  The previous tile's S
-    // MMAs must be done with the Q tile first.
-    const uint32_t qph = (uint32_t)(ps.q & 1);
-    if (!mbar_wait_or_abort(b.q_empty, qph ^ 1, p.err_flag, b.abort)) return false;
+    // next rows or zeros, which no output reads.
     const int rt = kVerifyVectors / p.group;
     mbar_arrive_expect_tx(b.q_full, 2u * 128u * (uint32_t)(p.group * rt));
     for (int rg = 0; rg < 2; ++rg)
       tma_load_3d(smem + kOffQ + rg * 16384, &p.qmap, rg * 64, x.g * p.group,
                   ru.row0 + gm.row_lo, b.q_full);
-    dr.note(kBitQ, qph);
   } else {
     // Slot hh is query head h0 + hh, 128 rows (box 64 x 1 x 128).
     mbar_arrive_expect_tx(b.q_full, 65536);
@@ -359,7 +303,6 @@ __device__ bool producer_tile(const PrefillParams& p, const RunInfo& ru, const T
       for (int rg = 0; rg < 2; ++rg)
         tma_load_3d(smem + kOffQ + hh * 32768 + rg * 16384, &p.qmap, rg * 64,
                     x.g * p.group + 2 * x.hp + hh, ru.row0 + gm.row_lo, b.q_full);
-    dr.note(kBitQ, 0);
   }
   // Row coordinate of key tile j in its source; one page lookup per page.  A
   // bad page id is flagged and a valid page read in its place (its keys are
@@ -404,6 +347,7 @@ __device__ bool producer_tile(const PrefillParams& p, const RunInfo& ru, const T
   };
   // Loads into a 16-bit operand stage (bf16), or (prefill, e4m3) into the
   // staging tile that the converters move on, K and V in their order.
+  int staged_k = 0, staged_v = 0;       // e4m3: staging loads issued
   auto load = [&](bool is_v, int stage, uint32_t parity, int y) {
     if (FP8) {
       int& n = is_v ? staged_v : staged_k;
@@ -412,7 +356,6 @@ __device__ bool producer_tile(const PrefillParams& p, const RunInfo& ru, const T
       if (!mbar_wait_or_abort(empty, (n & 1) ^ 1, p.err_flag, b.abort)) return false;
       mbar_arrive_expect_tx(full, 16384);
       tma_load_2d(smem + stage8_off(is_v), is_v ? mv : mk, 0, y, full);
-      dr.note(is_v ? kBitV8 : kBitK8, (uint32_t)(n & 1));
       ++n;
       return true;
     }
@@ -424,46 +367,58 @@ __device__ bool producer_tile(const PrefillParams& p, const RunInfo& ru, const T
     mbar_arrive_expect_tx(full, 32768);
     tma_load_2d(dst, is_v ? mv : mk, 0, y, full);
     tma_load_2d(dst + 16384, is_v ? mv : mk, 64, y, full);
-    dr.note((is_v ? kBitV : kBitK) + stage, parity);
     return true;
   };
+  // Last load issued into each 16-bit stage (phase parity, or -1): an
+  // aborting CTA waits for these before it exits.
+  int last_k0 = -1, last_k1 = -1, last_k2 = -1, last_v0 = -1, last_v1 = -1, last_v2 = -1;
+  auto issued = [&](bool is_v, int stage, uint32_t ph) {
+    int& w = is_v ? (stage == 2 ? last_v2 : stage ? last_v1 : last_v0)
+                  : (stage == 2 ? last_k2 : stage ? last_k1 : last_k0);
+    w = (int)ph;
+  };
   if (VERIFY && FP8) {
-    // Step jj of slot hh (its idx-th step, idx = ps.step(hh) + jj): K into
-    // e4m3 stage 2 hh + (idx & 1), V into staging tile 2 hh + (idx & 1), each
-    // at phase (idx >> 1) & 1; K of both slots, then V of both.
+    // Step jj, slot hh: K into e4m3 stage 2 hh + (jj & 1), V into staging
+    // tile 2 hh + (jj & 1), each at phase (jj >> 1) & 1; K of both slots,
+    // then V of both.  last_k*, last_v*: each slot's last step loaded.
     for (int j = gm.kt0; j < gm.kt0 + kAhead; ++j) prefetch(j);
-    for (int jj = 0; jj < slot_tiles<true>(gm, 0); ++jj) {
+    bool ok = true;
+    for (int jj = 0; ok && jj < slot_tiles<true>(gm, 0); ++jj) {
       prefetch(gm.kt0 + 2 * jj + kAhead);
       prefetch(gm.kt0 + 2 * jj + 1 + kAhead);
-      for (int kv = 0; kv < 2; ++kv)
-        for (int hh = 0; hh < 2; ++hh) {
+      const uint32_t ph = (jj >> 1) & 1;
+      for (int kv = 0; ok && kv < 2; ++kv)
+        for (int hh = 0; ok && hh < 2; ++hh) {
           if (jj >= slot_tiles<true>(gm, hh)) continue;
-          const int idx = ps.step(hh) + jj;
-          const int i = 2 * hh + (idx & 1);
-          const uint32_t ph = (uint32_t)((idx >> 1) & 1);
+          const int i = 2 * hh + (jj & 1);
           uint64_t* empty = kv ? b.v8_empty + i : b.k_empty + i;
           uint64_t* full = kv ? b.v8_full + i : b.k_full + i;
           const int y = row_of(slot_tile<true>(gm, jj, hh));
-          if (!mbar_wait_or_abort(empty, ph ^ 1, p.err_flag, b.abort)) return false;
+          if (!(ok = mbar_wait_or_abort(empty, ph ^ 1, p.err_flag, b.abort))) break;
           mbar_arrive_expect_tx(full, 16384);
           tma_load_2d(smem + (kv ? vstage8_off(i) : kstage8_off(i)), kv ? mv : mk, 0, y, full);
-          dr.note((kv ? kBitV : kBitK) + i, ph);
+          if (kv) {
+            (hh ? last_v1 : last_v0) = jj;
+          } else {
+            (hh ? last_k1 : last_k0) = jj;
+          }
         }
     }
   } else if (VERIFY) {
-    // Step jj, slot hh: the key tile n = ps.common + 2 jj + hh of the CTA's
-    // common order into stage n mod 3 at phase (n / 3) & 1; K of both
-    // slots, then V of both.
+    // Step jj, slot hh: tile n = 2 jj + hh (kt0 + n) into stage n mod 3 at
+    // phase (n / 3) & 1; K of both slots, then V of both.
     for (int j = gm.kt0; j < gm.kt0 + kAhead; ++j) prefetch(j);
-    for (int jj = 0; jj < slot_tiles<true>(gm, 0); ++jj) {
+    bool ok = true;
+    for (int jj = 0; ok && jj < slot_tiles<true>(gm, 0); ++jj) {
       prefetch(gm.kt0 + 2 * jj + kAhead);
       prefetch(gm.kt0 + 2 * jj + 1 + kAhead);
-      for (int kv = 0; kv < 2; ++kv)
-        for (int hh = 0; hh < 2; ++hh) {
+      for (int kv = 0; ok && kv < 2; ++kv)
+        for (int hh = 0; ok && hh < 2; ++hh) {
           if (jj >= slot_tiles<true>(gm, hh)) continue;
-          const int n = ps.common + 2 * jj + hh;
-          if (!load(kv == 1, n % 3, (uint32_t)((n / 3) & 1), row_of(slot_tile<true>(gm, jj, hh))))
-            return false;
+          const int n = 2 * jj + hh;
+          const uint32_t ph = (uint32_t)((n / 3) & 1);
+          ok = load(kv == 1, n % 3, ph, row_of(slot_tile<true>(gm, jj, hh)));
+          if (ok) issued(kv == 1, n % 3, ph);
         }
     }
   } else {
@@ -471,25 +426,42 @@ __device__ bool producer_tile(const PrefillParams& p, const RunInfo& ru, const T
       const int s = jj & 1;
       const uint32_t ph = (jj >> 1) & 1;
       const int y = row_of(gm.kt0 + jj);
-      if (!load(false, s, ph, y) || !load(true, s, ph, y)) return false;
+      if (!load(false, s, ph, y)) break;
+      issued(false, s, ph);
+      if (!load(true, s, ph, y)) break;
+      issued(true, s, ph);
     }
   }
-  return true;
-}
-
-template <bool FP8, bool VERIFY>
-__device__ void drain_loads(const PrefillParams& p, const Bars& b, const Drain& dr) {
-  for (int bit = 0; bit <= kBitQ; ++bit) {
-    if (!((dr.issued >> bit) & 1u)) continue;
-    uint64_t* full;
-    if (bit == kBitQ) full = b.q_full;
-    else if (bit == kBitK8) full = b.k8_full;
-    else if (bit == kBitV8) full = b.v8_full;
-    else if (bit >= kBitV) full = (VERIFY && FP8 ? b.v8_full : b.v_full) + (bit - kBitV);
-    else full = b.k_full + (bit - kBitK);
-    mbar_wait(full, (dr.phase >> bit) & 1u, p.err_flag);
+  if (*b.abort) {
+    // Let this CTA's loads in flight land before it exits.
+    mbar_wait(b.q_full, 0, p.err_flag);
+    if (VERIFY && FP8) {
+      // each slot's last two steps loaded (buffers alternate by step)
+      const int lasts[4] = {last_k0, last_k1, last_v0, last_v1};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int hh = u & 1;
+        uint64_t* full = u < 2 ? b.k_full : b.v8_full;
+#pragma unroll
+        for (int d = 0; d < 2; ++d) {
+          const int jj = lasts[u] - d;
+          if (jj >= 0) mbar_wait(full + 2 * hh + (jj & 1), (uint32_t)((jj >> 1) & 1), p.err_flag);
+        }
+      }
+    } else if (FP8) {
+      if (staged_k > 0) mbar_wait(b.k8_full, (uint32_t)((staged_k - 1) & 1), p.err_flag);
+      if (staged_v > 0) mbar_wait(b.v8_full, (uint32_t)((staged_v - 1) & 1), p.err_flag);
+    } else {
+      if (last_k0 >= 0) mbar_wait(&b.k_full[0], (uint32_t)last_k0, p.err_flag);
+      if (last_k1 >= 0) mbar_wait(&b.k_full[1], (uint32_t)last_k1, p.err_flag);
+      if (last_k2 >= 0) mbar_wait(&b.k_full[2], (uint32_t)last_k2, p.err_flag);
+      if (last_v0 >= 0) mbar_wait(&b.v_full[0], (uint32_t)last_v0, p.err_flag);
+      if (last_v1 >= 0) mbar_wait(&b.v_full[1], (uint32_t)last_v1, p.err_flag);
+      if (last_v2 >= 0) mbar_wait(&b.v_full[2], (uint32_t)last_v2, p.err_flag);
+    }
   }
 }
+
 
 // Zero rows [z0, 128) of a 16-bit V operand tile (both 64-column halves):
 // keys past the stream's end, or a tile whose page id was bad, must add
@@ -535,8 +507,8 @@ __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, i
 // through one staging tile each.  Verify: V only (K feeds 8-bit MMAs), slot
 // hh's step jj from staging tile 2 hh + (jj & 1).
 template <bool VERIFY>
-__device__ bool converter_tile(const PrefillParams& p, const RunInfo& ru, const TileGeom& gm,
-                               uint8_t* smem, const Bars& b, const Pipe& ps) {
+__device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileGeom& gm,
+                          uint8_t* smem, const Bars& b) {
   const int t = threadIdx.x - kConvWarp0 * 32;   // 0..127
   const int lane = threadIdx.x & 31;
   // Staging tile `src` (K, or V with rows from z0 on zeroed: past the
@@ -559,19 +531,18 @@ __device__ bool converter_tile(const PrefillParams& p, const RunInfo& ru, const 
   if (VERIFY) {
     PageCheck pc0(p, ru, gm, gm.kt0, slot_tiles<true>(gm, 0), 2);
     PageCheck pc1(p, ru, gm, gm.kt0 + 1, slot_tiles<true>(gm, 1), 2);
-    for (int jj = 0; jj < slot_tiles<true>(gm, 0); ++jj) {
-      for (int hh = 0; hh < 2; ++hh) {
+    bool ok = true;
+    for (int jj = 0; ok && jj < slot_tiles<true>(gm, 0); ++jj) {
+      for (int hh = 0; ok && hh < 2; ++hh) {
         if (jj >= slot_tiles<true>(gm, hh)) continue;
         const int j = slot_tile<true>(gm, jj, hh);
         const int z0 = v_zero_from(ru, j, hh ? pc1.bad(j) : pc0.bad(j));
-        const int idx = ps.step(hh) + jj;        // this slot's idx-th step
-        const int i = 2 * hh + (idx & 1);
-        if (!convert(true, hh, idx & 1, z0, vstage8_off(i), (uint32_t)((idx >> 1) & 1),
-                     b.v8_full + i, b.v8_empty + i))
-          return false;
+        const int i = 2 * hh + (jj & 1);
+        ok = convert(true, hh, jj & 1, z0, vstage8_off(i), (uint32_t)((jj >> 1) & 1),
+                     b.v8_full + i, b.v8_empty + i);
       }
     }
-    return true;
+    return;
   }
   PageCheck pc(p, ru, gm, gm.kt0, gm.nkt, 1);
   for (int jj = 0; jj < gm.nkt; ++jj) {
@@ -581,17 +552,14 @@ __device__ bool converter_tile(const PrefillParams& p, const RunInfo& ru, const 
     const uint32_t ph = (jj >> 1) & 1;
     // one staging tile each for K and V: its jj-th fill is phase jj & 1
     const uint32_t ph8 = (uint32_t)(jj & 1);
-    if (!convert(false, s, ph, z0, stage8_off(false), ph8, b.k8_full, b.k8_empty)) return false;
-    if (!convert(true, s, ph, z0, stage8_off(true), ph8, b.v8_full, b.v8_empty)) return false;
+    if (!convert(false, s, ph, z0, stage8_off(false), ph8, b.k8_full, b.k8_empty)) return;
+    if (!convert(true, s, ph, z0, stage8_off(true), ph8, b.v8_full, b.v8_empty)) return;
   }
-  return true;
 }
 
-// One tile's MMAs.  Returns false if the CTA is aborting (its MMAs issued
-// so far have then completed).
 template <bool FP8, bool VERIFY>
-__device__ bool mma_tile(const PrefillParams& p, const RunInfo& ru, const TileGeom& gm,
-                         uint8_t* smem, uint32_t tmem, const Bars& b, const Pipe& ps) {
+__device__ void mma_issuer(const PrefillParams& p, const RunInfo& ru, const TileGeom& gm,
+                           uint8_t* smem, uint32_t tmem, const Bars& b) {
   const int lane = threadIdx.x & 31;
   const bool leader = lane == 0;
   constexpr uint32_t kIdescQK = umma::idesc_f16(128, 128, !FP8, false);
@@ -633,56 +601,33 @@ __device__ bool mma_tile(const PrefillParams& p, const RunInfo& ru, const TileGe
     }
   };
 
-  if (gm.nkt == 0) {
-    // No keys in this tile (or half): nothing to wait for.  A commit, not a
-    // plain arrival: in a persistent CTA it completes only after the
-    // previous tile's MMAs, so o_final's phases stay in tile order.
-    if (leader) umma::commit(b.o_final);
+  if (gm.nkt == 0) {                  // no keys in this half: nothing to wait for
+    if (leader) mbar_arrive(b.o_final);
     __syncwarp();
-    return true;
+    return;
   }
   if (VERIFY) {
-    // Slot hh, step jj, the slot's idx-th step (idx = ps.step(hh) + jj).
-    // bf16: K and V of key tile n = ps.common + 2 jj + hh of the common order
-    // in stage n mod 3 at phase (n / 3) & 1.  e4m3: K in e4m3 stage
-    // 2 hh + (idx & 1) at phase (idx >> 1) & 1, V in 16-bit stage hh at
-    // phase idx & 1.
-    auto kst = [&](int hh, int jj) {
-      const int idx = ps.step(hh) + jj, n = ps.common + 2 * jj + hh;
-      return FP8 ? 2 * hh + (idx & 1) : n % 3;
-    };
+    // Slot hh, step jj.  bf16: K and V of tile n = 2 jj + hh in stage n mod
+    // 3 at phase (n / 3) & 1.  e4m3: K in e4m3 stage 2 hh + (jj & 1) at phase
+    // (jj >> 1) & 1, V in 16-bit stage hh at phase jj & 1.
+    auto kst = [&](int hh, int jj) { return FP8 ? 2 * hh + (jj & 1) : (2 * jj + hh) % 3; };
     auto kph = [&](int hh, int jj) {
-      const int idx = ps.step(hh) + jj, n = ps.common + 2 * jj + hh;
-      return (uint32_t)(FP8 ? (idx >> 1) & 1 : (n / 3) & 1);
+      return (uint32_t)(FP8 ? (jj >> 1) & 1 : ((2 * jj + hh) / 3) & 1);
     };
-    auto vst = [&](int hh, int jj) { return FP8 ? hh : (ps.common + 2 * jj + hh) % 3; };
-    auto vph = [&](int hh, int jj) {
-      return (uint32_t)(FP8 ? (ps.step(hh) + jj) & 1 : ((ps.common + 2 * jj + hh) / 3) & 1);
-    };
-    // The last S MMA of the tile frees the Q tile for the next one.
-    const int s_total = slot_tiles<true>(gm, 0) + slot_tiles<true>(gm, 1);
-    int s_issued = 0;
-    auto s_issued_one = [&]() {
-      if (++s_issued == s_total && leader) umma::commit(b.q_empty);
-    };
-    bool ok = mbar_wait_or_abort(b.q_ready, (uint32_t)(ps.q & 1), p.err_flag, b.abort);
+    auto vst = [&](int hh, int jj) { return FP8 ? hh : (2 * jj + hh) % 3; };
+    auto vph = [&](int hh, int jj) { return (uint32_t)(FP8 ? jj & 1 : ((2 * jj + hh) / 3) & 1); };
+    bool ok = mbar_wait_or_abort(b.q_ready, 0, p.err_flag, b.abort);
     for (int hh = 0; ok && hh < 2; ++hh) {
       if (slot_tiles<true>(gm, hh) == 0) continue;
-      if (!(ok = mbar_wait_or_abort(&b.k_full[kst(hh, 0)], kph(hh, 0), p.err_flag, b.abort)))
-        break;
+      if (!(ok = mbar_wait_or_abort(&b.k_full[kst(hh, 0)], 0, p.err_flag, b.abort))) break;
       umma::fence_after_sync();
       if (leader) {
         issue_s(hh, kst(hh, 0));
         umma::commit(&b.s_full[hh]);
         umma::commit(&b.k_empty[kst(hh, 0)]);
       }
-      s_issued_one();
       __syncwarp();
     }
-    // The first PV of the tile overwrites O: the previous tile's epilogue
-    // must have read it.
-    if (ok && ps.tile > 0)
-      ok = mbar_wait_or_abort(b.o_free, (uint32_t)((ps.tile - 1) & 1), p.err_flag, b.abort);
     PageCheck pc0(p, ru, gm, gm.kt0, slot_tiles<true>(gm, 0), 2);
     PageCheck pc1(p, ru, gm, gm.kt0 + 1, slot_tiles<true>(gm, 1), 2);
     for (int jj = 0; ok && jj < slot_tiles<true>(gm, 0); ++jj) {
@@ -697,9 +642,7 @@ __device__ bool mma_tile(const PrefillParams& p, const RunInfo& ru, const TileGe
           const int z0 = v_zero_from(ru, j, page_bad);
           if (z0 < kTileKeys) zero_v_rows(smem + kOffV + vs * 32768, z0, lane);
         }
-        if (!(ok = mbar_wait_or_abort(&b.p_ready[hh], (uint32_t)((ps.step(hh) + jj) & 1),
-                                      p.err_flag, b.abort)))
-          break;
+        if (!(ok = mbar_wait_or_abort(&b.p_ready[hh], jj & 1, p.err_flag, b.abort))) break;
         umma::fence_after_sync();
         if (leader) {
           issue_pv(hh, vs, jj > 0);
@@ -716,7 +659,6 @@ __device__ bool mma_tile(const PrefillParams& p, const RunInfo& ru, const TileGe
             umma::commit(&b.s_full[hh]);
             umma::commit(&b.k_empty[ks]);
           }
-          s_issued_one();
           __syncwarp();
         }
       }
@@ -730,7 +672,7 @@ __device__ bool mma_tile(const PrefillParams& p, const RunInfo& ru, const TileGe
       }
     }
     __syncwarp();
-    return ok;
+    return;
   }
   bool ok = mbar_wait_or_abort(b.q_ready, 0, p.err_flag, b.abort) &&
             mbar_wait_or_abort(&b.k_full[0], 0, p.err_flag, b.abort);
@@ -794,7 +736,6 @@ __device__ bool mma_tile(const PrefillParams& p, const RunInfo& ru, const TileGe
     }
   }
   __syncwarp();
-  return ok;
 }
 
 // e4m3 caches: turn this thread's Q row (bf16, in the operand tile) into f16
@@ -912,9 +853,9 @@ __device__ __forceinline__ uint32_t part_ml(uint32_t smem_base, int hh, int r) {
 }
 
 template <bool FP8, bool VERIFY>
-__device__ bool softmax_role(const PrefillParams& p, const RunInfo& ru, const Tile& x,
+__device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Tile& x,
                              const TileGeom& gm, uint32_t rank, int hh, uint8_t* smem,
-                             uint32_t tmem, const Bars& b, const Pipe& ps) {
+                             uint32_t tmem, const Bars& b) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = 32 * (warp & 3) + lane;                 // row of the tile = TMEM lane
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
@@ -941,7 +882,7 @@ __device__ bool softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
     // slot B's take it once they see the tile ready.
     float* down_s = reinterpret_cast<float*>(smem + Layout<FP8>::kOffDown);
     if (!VERIFY || hh == 0) {
-      ok = mbar_wait_or_abort(b.q_full, (uint32_t)(ps.q & 1), p.err_flag, b.abort);
+      ok = mbar_wait_or_abort(b.q_full, 0, p.err_flag, b.abort);
       if (ok) {
         const float down = VERIFY ? q_row_to_e4m3_pair(smem + kOffQ, r)
                                   : q_row_to_f16(smem + kOffQ + hh * 32768, r);
@@ -952,7 +893,7 @@ __device__ bool softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
         if (lane == 0) mbar_arrive(b.q_ready);
       }
     } else {
-      ok = mbar_wait_or_abort(b.q_ready, (uint32_t)(ps.q & 1), p.err_flag, b.abort);
+      ok = mbar_wait_or_abort(b.q_ready, 0, p.err_flag, b.abort);
       if (ok) sl2 = p.scale_log2 * down_s[r] * __ldg(p.k_scale + x.g);
     }
   }
@@ -967,9 +908,7 @@ __device__ bool softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
   for (int jj = 0; ok && jj < nt; ++jj) {
     const int j = slot_tile<VERIFY>(gm, jj, hh);
     const bool page_bad = pc.bad(j);
-    if (!(ok = mbar_wait_or_abort(&b.s_full[hh], (uint32_t)((ps.step(hh) + jj) & 1), p.err_flag,
-                                  b.abort)))
-      break;
+    if (!(ok = mbar_wait_or_abort(&b.s_full[hh], jj & 1, p.err_flag, b.abort))) break;
     if (idle) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&b.p_ready[hh]);
@@ -1060,7 +999,7 @@ __device__ bool softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
     __syncwarp();
     if (lane == 0) mbar_arrive(&b.p_ready[hh]);
   }
-  if (ok) ok = mbar_wait_or_abort(b.o_final, (uint32_t)(ps.tile & 1), p.err_flag, b.abort);
+  if (ok) ok = mbar_wait_or_abort(b.o_final, 0, p.err_flag, b.abort);
   if (ok) umma::fence_after_sync();
 
   if (VERIFY) {
@@ -1071,18 +1010,12 @@ __device__ bool softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
     // eight softmax warps (which every one of them reaches), slot A's read
     // both slots' O from TMEM (the same lane quarter) and write.  A slot
     // without tiles counts as m = -inf, l = 0, O = 0.
-    // A second barrier once slot A has read (m, l) lets slot B go on to the
-    // next tile; slot A tells the MMA issuer (o_free) once it has read both
-    // slots' O, which the next tile's first PV MMAs overwrite.
     float2* ml_s = reinterpret_cast<float2*>(smem + Layout<FP8>::kOffMl);
     if (hh == 1) ml_s[r] = make_float2(m_run, l);
     __syncwarp();
     named_bar_sync(1, 256);
-    float2 mlb = make_float2(-INFINITY, 0.f);
-    if (hh == 0) mlb = ml_s[r];
-    named_bar_sync(2, 256);
-    if (hh == 1) return ok;
-    if (!__all_sync(0xffffffffu, ok)) return false;
+    if (hh == 1 || !__all_sync(0xffffffffu, ok)) return;
+    const float2 mlb = ml_s[r];
     const float mx = fmaxf(m_run, mlb.x);
     const float a0 = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mx);
     const float a1 = mlb.x == -INFINITY ? 0.f : fast_exp2(mlb.x - mx);
@@ -1122,13 +1055,10 @@ __device__ bool softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
         }
       }
     }
-    umma::fence_before_sync();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(b.o_free);
     if (valid)
       *reinterpret_cast<float2*>(p.part_ml + slot * 2) =
           make_float2(mx, __fmaf_rn(l, a0, __fmul_rn(mlb.y, a1)));
-    return true;
+    return;
   }
 
   const uint32_t sbase = smem_u32(smem);
@@ -1153,14 +1083,14 @@ __device__ bool softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
       st_cluster_f2(mapa_shared(part_ml(sbase, hh, r), 0), m_run, l);
     }
     mbar_arrive_remote(mapa_shared(smem_u32(b.peer_ready), 0));
-    return ok;
+    return;
   }
 
   // CTA 0: its MMAs are done (or it gave up), so CTA 1 may store into the
   // rings.  Then merge CTA 1's half into this one, normalise, write.
   if (threadIdx.x == 128) mbar_arrive_remote(mapa_shared(smem_u32(b.dst_free), 1));
   const bool peer = mbar_wait_cluster(b.peer_ready, 0, p.err_flag);
-  if (!ok || !peer) return false;
+  if (!ok || !peer) return;
   float2 ml1;
   asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(ml1.x), "=f"(ml1.y)
                : "r"(part_ml(sbase, hh, r)) : "memory");
@@ -1209,7 +1139,6 @@ __device__ bool softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
   if (write && p.lse)
     p.lse[(size_t)(ru.row0 + gm.row_lo + r) * p.hq + h] =
         l_all > 0.f ? (m_all + log2f(l_all)) * 0.6931471805599453f : -INFINITY;
-  return true;
 }
 
 template <bool FP8, bool VERIFY>
@@ -1244,8 +1173,6 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   b.abort = reinterpret_cast<volatile int*>(bars + 21);
   b.peer_ready = bars + 22;
   b.dst_free = bars + 23;
-  b.q_empty = bars + 32;
-  b.o_free = bars + 33;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -1283,8 +1210,6 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
     mbar_init(b.drain, 1);
     mbar_init(b.peer_ready, 256);                  // every softmax thread of CTA 1
     mbar_init(b.dst_free, 1);
-    mbar_init(b.q_empty, 1);                       // verify: the tile's last S MMA
-    mbar_init(b.o_free, 4);                        // verify: slot A's softmax warps
     *b.abort = 0;
     fence_mbar_init();
   }
@@ -1304,75 +1229,25 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   allow_next_grid();
   wait_prior_grid();
 
-  // Prefill: two CTAs (a cluster) per tile, one tile.  Verify: one CTA per
-  // SM, taking tiles blockIdx.x, + gridDim.x, ...; each role walks the same
-  // tiles in the same order and keeps its own running counts (Pipe).
+  // Prefill: two CTAs (a cluster) per tile; verify: one CTA per tile.
   const uint32_t rank = VERIFY ? 0 : cluster_ctarank();
-  // Calls fn(x, ru, gm, ps) for each of this CTA's tiles until it returns
-  // false (verify); a prompt-chunk CTA pair has one tile.
-  auto for_tiles = [&](auto&& fn) {
-    Pipe ps{};
-    for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
-      const Tile x = tile_of<true>(p, t);
-      const RunInfo& ru = p.runs[x.run];
-      const TileGeom gm = geom_of<true>(p, ru, x, 0);
-      if (!fn(x, ru, gm, ps)) return;
-      ps.advance(gm, true);
-    }
-  };
+  const Tile x = tile_of<VERIFY>(p, VERIFY ? blockIdx.x : blockIdx.x >> 1);
+  const RunInfo& ru = p.runs[x.run];
+  const TileGeom gm = geom_of<VERIFY>(p, ru, x, rank);
 
-  if constexpr (!VERIFY) {
-    const Pipe ps{};
-    const Tile x = tile_of<false>(p, blockIdx.x >> 1);
-    const RunInfo& ru = p.runs[x.run];
-    const TileGeom gm = geom_of<false>(p, ru, x, rank);
-    if (warp < 4) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8, VERIFY>::kLow));
-      if (warp == 0) {
-        if (lane == 0) {
-          Drain dr;
-          int staged_k = 0, staged_v = 0;
-          producer_tile<FP8, false>(p, ru, x, gm, smem, b, ps, dr, staged_k, staged_v);
-          if (*b.abort) drain_loads<FP8, false>(p, b, dr);   // its loads land before it exits
-        }
-      } else if (warp == 1) {
-        mma_tile<FP8, false>(p, ru, gm, smem, tmem, b, ps);
-      }
-    } else if (warp < kConvWarp0) {
-      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<FP8, VERIFY>::kHigh));
-      softmax_role<FP8, false>(p, ru, x, gm, rank, (warp - 4) >> 2, smem, tmem, b, ps);
-    } else if (FP8) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8, VERIFY>::kConv));
-      converter_tile<false>(p, ru, gm, smem, b, ps);
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kLow));
+    if (warp == 0) {
+      if (lane == 0) producer<FP8, VERIFY>(p, ru, x, gm, smem, b);
+    } else if (warp == 1) {
+      mma_issuer<FP8, VERIFY>(p, ru, gm, smem, tmem, b);
     }
-  } else {
-    if (warp < 4) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8, VERIFY>::kLow));
-      if (warp == 0) {
-        if (lane == 0) {
-          Drain dr;
-          int staged_k = 0, staged_v = 0;
-          for_tiles([&](const Tile& x, const RunInfo& ru, const TileGeom& gm, const Pipe& ps) {
-            return producer_tile<FP8, VERIFY>(p, ru, x, gm, smem, b, ps, dr, staged_k, staged_v);
-          });
-          if (*b.abort) drain_loads<FP8, VERIFY>(p, b, dr);   // its loads land before it exits
-        }
-      } else if (warp == 1) {
-        for_tiles([&](const Tile&, const RunInfo& ru, const TileGeom& gm, const Pipe& ps) {
-          return mma_tile<FP8, VERIFY>(p, ru, gm, smem, tmem, b, ps);
-        });
-      }
-    } else if (warp < kConvWarp0) {
-      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<FP8, VERIFY>::kHigh));
-      for_tiles([&](const Tile& x, const RunInfo& ru, const TileGeom& gm, const Pipe& ps) {
-        return softmax_role<FP8, VERIFY>(p, ru, x, gm, rank, (warp - 4) >> 2, smem, tmem, b, ps);
-      });
-    } else if (FP8) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8, VERIFY>::kConv));
-      for_tiles([&](const Tile&, const RunInfo& ru, const TileGeom& gm, const Pipe& ps) {
-        return converter_tile<VERIFY>(p, ru, gm, smem, b, ps);
-      });
-    }
+  } else if (warp < kConvWarp0) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kHigh));
+    softmax_role<FP8, VERIFY>(p, ru, x, gm, rank, (warp - 4) >> 2, smem, tmem, b);
+  } else if (FP8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kConv));
+    converter<VERIFY>(p, ru, gm, smem, b);
   }
   umma::fence_before_sync();
   __syncthreads();
@@ -1383,10 +1258,8 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   }
 }
 
-// Prefill: `grid` is the tile count (a cluster of two CTAs each).  Verify:
-// `grid` persistent CTAs share p.n_tiles tiles.
 template <bool FP8, bool VERIFY>
-cudaError_t launch(const PrefillParams& p, int grid, cudaStream_t s) {
+cudaError_t launch(const PrefillParams& p, int tiles, cudaStream_t s) {
   static PerDeviceOnce configured;
   const cudaError_t e = configured.run([] {
     // The register split only works if the block launches with at least the
@@ -1394,16 +1267,16 @@ cudaError_t launch(const PrefillParams& p, int grid, cudaStream_t s) {
     cudaFuncAttributes attr;
     cudaError_t r = cudaFuncGetAttributes(&attr, prefill_kernel<FP8, VERIFY>);
     if (r != cudaSuccess) return r;
-    if (attr.numRegs * threads_of<FP8>() < regs_split<FP8, VERIFY>()) return cudaErrorInvalidValue;
+    if (attr.numRegs * threads_of<FP8>() < regs_split<FP8>()) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(prefill_kernel<FP8, VERIFY>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Layout<FP8>::kSmemBytes);
   });
   if (e != cudaSuccess) return e;
   if (VERIFY)
-    return launch_pdl(prefill_kernel<FP8, VERIFY>, dim3(grid), dim3(threads_of<FP8>()),
+    return launch_pdl(prefill_kernel<FP8, VERIFY>, dim3(tiles), dim3(threads_of<FP8>()),
                       Layout<FP8>::kSmemBytes, s, p);
-  return launch_pdl_cluster(prefill_kernel<FP8, VERIFY>, dim3(2 * grid),
+  return launch_pdl_cluster(prefill_kernel<FP8, VERIFY>, dim3(2 * tiles),
                             dim3(threads_of<FP8>()), Layout<FP8>::kSmemBytes, s, p, 2);
 }
 
@@ -1414,9 +1287,9 @@ cudaError_t launch_prefill(const PrefillParams& p, bool fp8, int tiles, cudaStre
   return fp8 ? launch<true, false>(p, tiles, s) : launch<false, false>(p, tiles, s);
 }
 
-cudaError_t launch_verify(const PrefillParams& p, bool fp8, int grid, cudaStream_t s) {
-  if (grid <= 0 || p.n_tiles <= 0) return cudaSuccess;
-  return fp8 ? launch<true, true>(p, grid, s) : launch<false, true>(p, grid, s);
+cudaError_t launch_verify(const PrefillParams& p, bool fp8, int tiles, cudaStream_t s) {
+  if (tiles <= 0) return cudaSuccess;
+  return fp8 ? launch<true, true>(p, tiles, s) : launch<false, true>(p, tiles, s);
 }
 
 }  // namespace tfpa

@@ -132,8 +132,7 @@ def test_verify_tiles_and_mixed_launch_order():
         ("partial", 0, 17, 1), ("verify", 0, 17, 1), ("merge", 0, 17, 2)]
     v = rec[1]
     splits = 256 // 16                            # 65,536 keys = 256 pages, 16 a split
-    assert v["items"] == 8 * 1 * 1 * splits
-    assert v["grid"] == min(v["items"], 152)           # persistent CTAs, one per SM at most
+    assert v["items"] == v["grid"] == 8 * 1 * 1 * splits
     assert rec[0]["items"] == 8 * 1 * B.tfpa_num_splits(L)   # 4 vectors: one m-tile
 
 
