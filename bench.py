@@ -40,7 +40,7 @@ METRIC = "paged decode KV GB/s (% HBM peak); prompt-chunk attn TFLOP/s (% TC pea
 # bench's partial launch), valid only while the kernel's sources hash to the
 # value below: after any change to them the line reports null until the
 # counters are taken again.
-DECODE_TRAFFIC = {"bytes": 268_614_656 + 4_640_000, "sources_sha256_16": "b149c2ad83c776c9"}
+DECODE_TRAFFIC = {"bytes": 268_617_472 + 3_739_648, "sources_sha256_16": "5689a524af816ddd"}
 DECODE_SOURCES = ["paged_kv_cache_235_gb300/csrc/decode.cu",
                   "paged_kv_cache_235_gb300/csrc/common.cuh",
                   "paged_kv_cache_235_gb300/csrc/params.h",
