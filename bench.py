@@ -336,6 +336,65 @@ def e2e_buffers(w, torch, nst):
     return h_in, d_in, dq, dk, dv, hout
 
 
+def time_e2e_planned(w, torch, B, ctx, steps, warmup):
+    """The decode loop of time_e2e_calls, one step at a time, with each step
+    planned while the previous one runs: after enqueueing step i the host
+    plans step i + 1 (B.Plan: tfpa_plan_write_kv + tfpa_plan_decode, lengths
+    one position longer), then waits for step i's output, then enqueues the
+    next input copy, launches the plan and enqueues the output copy.
+    Returns (s per step, KV + Q + O bytes per step, host us per plan launch,
+    host us planning a step)."""
+    cache, segs, _, sc, out = ctx
+    nst = len(w.streams)
+    tab = B.SegTable(segs)
+    h_in, d_in, dq, dk, dv, hout = e2e_buffers(w, torch, nst)
+    sidx = np.arange(nst, dtype=np.int32)
+    s = torch.cuda.current_stream()
+    sh = s.cuda_stream
+    L = w.streams[0].seq_len
+    total = warmup + steps
+    plan = B.Plan()
+    ev = torch.cuda.Event()
+    b = 2 if w.kv_dtype == "bf16" else 1
+    t_launch, t_plan = [], []
+    kvb = 0
+
+    def plan_step(i):
+        n = L - total + 1 + i
+        for j in range(nst):
+            tab.set_seq_len(j, n)
+        rp = np.full(nst, n - 1, np.int32)
+        plan.clear()
+        plan.write_kv(cache, tab, dk, dv, sidx, rp)
+        plan.decode(cache, tab, dq, sidx, rp, w.softmax_scale, sc, out)
+        return n
+
+    n = plan_step(0)
+    t0 = None
+    for i in range(total):
+        if i == warmup:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        d_in.copy_(h_in, non_blocking=True)
+        a = time.perf_counter_ns()
+        plan.launch(sh)
+        t_launch.append((time.perf_counter_ns() - a) / 1e3)
+        hout.copy_(out, non_blocking=True)
+        ev.record(s)
+        if i >= warmup:
+            kvb += n * nst * w.hkv * 128 * 2 * b
+        if i + 1 < total:
+            a = time.perf_counter_ns()
+            n = plan_step(i + 1)                 # while the GPU runs step i
+            t_plan.append((time.perf_counter_ns() - a) / 1e3)
+        ev.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    for j, st in enumerate(w.streams):
+        tab.set_seq_len(j, st.seq_len)
+    qo = w.rows * w.hq * 128 * 2 * 2
+    return dt, kvb / steps + qo, statistics.median(t_launch[warmup:]), statistics.median(t_plan)
+
+
 def time_e2e_calls(w, torch, B, ctx, steps, warmup, in_flight=1):
     """A decode loop through the public API with host buffers, one real call
     of each entry point per step.  Every stream's length grows by one each
@@ -750,6 +809,7 @@ def main():
         e2e_s = max_over_ranks(dist, torch, e2e[0])
         e2e_aa = time_e2e_calls(w, torch, B, ctx, n_e2e, args.warmup)
         e2e_pipe = time_e2e_calls(w, torch, B, ctx, n_e2e, args.warmup, in_flight=2)
+        e2e_plan = time_e2e_planned(w, torch, B, ctx, n_e2e, args.warmup)
         e2e_graph_s = time_e2e_graph(w, torch, B, ctx, n_e2e, args.warmup)
         del ctx
         s3, p3, ctx3, _ = time_decode(w3, torch, B, max(10, args.steps // 4), args.warmup, None)
@@ -889,6 +949,13 @@ def main():
             "host_us_per_call": {"tfpa_write_kv": e2e_pipe[2], "tfpa_decode": e2e_pipe[3]},
             "how": "the same loop with step i + 1 enqueued before the host waits for step "
                    "i's output (two input and output buffers)"},
+        "e2e_planned": {
+            "value": world * e2e_plan[1] / e2e_plan[0] / 1e9, "unit": "GB/s",
+            "ms_per_step": e2e_plan[0] * 1e3, "vs_device_step": e2e_plan[0] * 1e3 / step_ms,
+            "host_us_per_plan_launch": e2e_plan[2], "host_us_planning_a_step": e2e_plan[3],
+            "how": "the same serial loop (one step at a time, host waits for each output), "
+                   "each step planned with tfpa_plan_write_kv + tfpa_plan_decode while the "
+                   "previous step runs, then launched with tfpa_plan_launch"},
         "e2e_graph_replay": {
             "value": world * (kv + qo) / e2e_graph_s / 1e9, "unit": "GB/s",
             "ms_per_step": e2e_graph_s * 1e3,

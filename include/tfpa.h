@@ -285,6 +285,41 @@ int tfpa_decode_static(const tfpa_cache* cache, const tfpa_seg* segs, int32_t ns
                        int32_t rows, float softmax_scale, void* out, float* lse,
                        cudaStream_t stream);
 
+/* ---- Plans: planning a call apart from enqueueing it -----------------------
+ * A decode loop's host work (checks, grouping rows into runs, split counts,
+ * per-CTA item ranges, tensor maps) does not need the GPU.  A plan does that
+ * work for a tfpa_write_kv or tfpa_decode call (same arguments, without the
+ * stream) and keeps the resulting launches by value; tfpa_plan_launch then
+ * only enqueues them.  A loop can plan step i + 1 while the GPU runs step i,
+ * so that between the host's wait for step i's output and step i + 1's
+ * kernels there are only the launches.  None of the TensorFold sources has a
+ * counterpart to this.
+ *
+ * A plan keeps the pointers it was given (device buffers, the cache's pools,
+ * scales and page tables, the scratch) and reads them when its launches
+ * run: they must stay valid and hold that step's data then.  Host arrays
+ * (segs, row tables, host page-table mirrors) are read during the planning
+ * call only.  Planning calls append to the plan in order; tfpa_plan_launch
+ * enqueues every launch on `stream` in that order and may be called any
+ * number of times.  A planning call that fails returns its error code (as
+ * the direct call would) and leaves the plan as it was.  A plan is used by
+ * one host thread at a time.  tfpa_plan_create returns NULL if host memory
+ * runs out; tfpa_plan_launch returns TFPA_ECUDA if a launch fails (launches
+ * before it stay enqueued). */
+typedef struct tfpa_plan tfpa_plan;
+tfpa_plan* tfpa_plan_create(void);
+void tfpa_plan_destroy(tfpa_plan* plan);
+void tfpa_plan_clear(tfpa_plan* plan);                 /* drops every planned launch */
+int32_t tfpa_plan_launches(const tfpa_plan* plan);     /* launches planned so far    */
+int tfpa_plan_write_kv(tfpa_plan* plan, const tfpa_cache* cache, const tfpa_seg* segs,
+                       int32_t nseg, const void* k_rows, const void* v_rows,
+                       const int32_t* row_seg, const int32_t* row_pos, int32_t rows);
+int tfpa_plan_decode(tfpa_plan* plan, const tfpa_cache* cache, const tfpa_seg* segs,
+                     int32_t nseg, const void* q, const int32_t* row_seg,
+                     const int32_t* row_pos, int32_t rows, float softmax_scale,
+                     const tfpa_scratch* scratch, void* out, float* lse);
+int tfpa_plan_launch(const tfpa_plan* plan, cudaStream_t stream);
+
 /* Causal prompt-chunk attention over the paged prefix, one pass with online
  * softmax on tcgen05/TMEM tiles (PR #2011, "hpattn_p256_kernel": page size a
  * constant 256, one page lookup per key tile).  max_rows_per_launch > 0 runs

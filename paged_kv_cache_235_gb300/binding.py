@@ -30,7 +30,9 @@ EXPORTS = ("tfpa_pages_per_split", "tfpa_num_splits", "tfpa_write_kv", "tfpa_dec
            "tfpa_strerror", "tfpa_version", "tfpa_decode_static", "tfpa_decode_tree",
            "tfpa_write_kv_rope", "tfpa_keep_kv", "tfpa_pool_create", "tfpa_pool_destroy",
            "tfpa_pool_free", "tfpa_pool_fits", "tfpa_pool_claim", "tfpa_pool_release",
-           "tfpa_stage_pages", "tfpa_save_kv", "tfpa_restore_kv")
+           "tfpa_stage_pages", "tfpa_save_kv", "tfpa_restore_kv", "tfpa_plan_create",
+           "tfpa_plan_destroy", "tfpa_plan_clear", "tfpa_plan_launches", "tfpa_plan_write_kv",
+           "tfpa_plan_decode", "tfpa_plan_launch")
 
 
 class TfpaError(RuntimeError):
@@ -126,6 +128,21 @@ def lib():
         L.tfpa_prefill.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, i32,
                                    ctypes.c_float, i32, vp, vp, vp]
         L.tfpa_prefill.restype = ctypes.c_int
+        L.tfpa_plan_create.argtypes = []
+        L.tfpa_plan_create.restype = vp
+        L.tfpa_plan_destroy.argtypes = [vp]
+        L.tfpa_plan_destroy.restype = None
+        L.tfpa_plan_clear.argtypes = [vp]
+        L.tfpa_plan_clear.restype = None
+        L.tfpa_plan_launches.argtypes = [vp]
+        L.tfpa_plan_launches.restype = i32
+        L.tfpa_plan_write_kv.argtypes = [vp, P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, vp, i32]
+        L.tfpa_plan_write_kv.restype = ctypes.c_int
+        L.tfpa_plan_decode.argtypes = [vp, P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, i32,
+                                       ctypes.c_float, P(tfpa_scratch), vp, vp]
+        L.tfpa_plan_decode.restype = ctypes.c_int
+        L.tfpa_plan_launch.argtypes = [vp, vp]
+        L.tfpa_plan_launch.restype = ctypes.c_int
         L.tfpa_set_launch_hook.argtypes = [HOOK, vp, ctypes.c_int]
         L.tfpa_set_launch_hook.restype = None
         L.tfpa_strerror.argtypes = [ctypes.c_int]
@@ -442,6 +459,47 @@ def tfpa_prefill(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, softmax
     _check(lib().tfpa_prefill(ctypes.byref(cc), cs, n, _ptr(q), _ptr(rs), _ptr(rp), len(rs),
                               float(softmax_scale), int(max_rows_per_launch), _ptr(out),
                               _ptr(lse), _stream(stream)), "tfpa_prefill")
+
+
+class Plan:
+    """Launches planned ahead (tfpa_plan_*): ``write_kv`` and ``decode`` take
+    the arguments of tfpa_write_kv / tfpa_decode without a stream and do all
+    of the call's host work; ``launch`` enqueues the planned launches."""
+
+    def __init__(self):
+        self._p = lib().tfpa_plan_create()
+        if not self._p:
+            raise MemoryError("tfpa_plan_create")
+
+    def clear(self) -> None:
+        lib().tfpa_plan_clear(self._p)
+
+    def __len__(self) -> int:
+        return int(lib().tfpa_plan_launches(self._p))
+
+    def write_kv(self, cache: Cache, segs, k_rows, v_rows, row_seg, row_pos) -> None:
+        cs, n = _segs(segs)
+        rs, rp = _i32(row_seg), _i32(row_pos)
+        _check(lib().tfpa_plan_write_kv(self._p, ctypes.byref(cache.c()), cs, n, _ptr(k_rows),
+                                        _ptr(v_rows), _ptr(rs), _ptr(rp), len(rs)),
+               "tfpa_plan_write_kv")
+
+    def decode(self, cache: Cache, segs, q, row_seg, row_pos, softmax_scale, scratch: Scratch,
+               out, lse=None) -> None:
+        cs, n = _segs(segs)
+        rs, rp = _i32(row_seg), _i32(row_pos)
+        _check(lib().tfpa_plan_decode(self._p, ctypes.byref(cache.c()), cs, n, _ptr(q), _ptr(rs),
+                                      _ptr(rp), len(rs), float(softmax_scale),
+                                      ctypes.byref(scratch.c()), _ptr(out), _ptr(lse)),
+               "tfpa_plan_decode")
+
+    def launch(self, stream=None) -> None:
+        _check(lib().tfpa_plan_launch(self._p, _stream(stream)), "tfpa_plan_launch")
+
+    def __del__(self):
+        if getattr(self, "_p", None):
+            lib().tfpa_plan_destroy(self._p)
+            self._p = None
 
 
 @contextlib.contextmanager

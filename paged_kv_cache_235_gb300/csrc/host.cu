@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <new>
 #include <cmath>
 #include <cstring>
 #include <unordered_map>
@@ -242,6 +243,71 @@ int to_err(cudaError_t e) { return e == cudaSuccess ? TFPA_OK : TFPA_ECUDA; }
 
 }  // namespace
 
+// A call's launches, planned and kept by value for a later tfpa_plan_launch.
+struct tfpa_plan {
+  enum Kind : int { kDecode, kVerify, kMerge, kWrite };
+  struct Entry {
+    Kind kind;
+    bool fp8;
+    int grid;
+    size_t index;   // into the vector of its kind
+  };
+  std::vector<Entry> entries;
+  std::vector<DecodeParams> decode;
+  std::vector<PrefillParams> verify;
+  std::vector<MergeParams> merge;
+  std::vector<WriteParams> write;
+};
+
+namespace {
+
+// Where a call's launches go: enqueued on a stream now, or appended to a
+// plan.  A planning call that fails takes back what it appended (Mark).
+struct Sink {
+  cudaStream_t stream = nullptr;
+  tfpa_plan* plan = nullptr;
+  struct Mark {
+    size_t e, d, v, m, w;
+  };
+  Mark mark() const {
+    return plan ? Mark{plan->entries.size(), plan->decode.size(), plan->verify.size(),
+                       plan->merge.size(), plan->write.size()}
+                : Mark{0, 0, 0, 0, 0};
+  }
+  void rollback(const Mark& k) const {
+    if (!plan) return;
+    plan->entries.resize(k.e);
+    plan->decode.resize(k.d);
+    plan->verify.resize(k.v);
+    plan->merge.resize(k.m);
+    plan->write.resize(k.w);
+  }
+  template <typename P>
+  int keep(tfpa_plan::Kind kind, std::vector<P>& v, const P& p, bool fp8, int grid) const {
+    v.push_back(p);
+    plan->entries.push_back(tfpa_plan::Entry{kind, fp8, grid, v.size() - 1});
+    return TFPA_OK;
+  }
+  int decode(const DecodeParams& p, bool fp8, int grid) const {
+    if (plan) return keep(tfpa_plan::kDecode, plan->decode, p, fp8, grid);
+    return dry_run() ? TFPA_OK : to_err(launch_decode_partial(p, fp8, grid, stream));
+  }
+  int verify(const PrefillParams& p, bool fp8, int tiles) const {
+    if (plan) return keep(tfpa_plan::kVerify, plan->verify, p, fp8, tiles);
+    return dry_run() ? TFPA_OK : to_err(launch_verify(p, fp8, tiles, stream));
+  }
+  int merge(const MergeParams& p) const {
+    if (plan) return keep(tfpa_plan::kMerge, plan->merge, p, false, 0);
+    return dry_run() ? TFPA_OK : to_err(launch_merge(p, stream));
+  }
+  int write(const WriteParams& p) const {
+    if (plan) return keep(tfpa_plan::kWrite, plan->write, p, false, 0);
+    return dry_run() ? TFPA_OK : to_err(launch_write_kv(p, stream));
+  }
+};
+
+}  // namespace
+
 extern "C" int32_t tfpa_pages_per_split(int32_t seq_len) {
   const int32_t np = pages_of(std::max(seq_len, 1));
   return std::max<int32_t>(2, (np + kMaxSplits - 1) / kMaxSplits);
@@ -393,7 +459,7 @@ void plan_cta_ranges(DecodeParams& p, int nr, int G, bool fp8, int grid) {
 int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const void* q,
                 const int32_t* row_seg, const int32_t* row_pos, const uint64_t* anc,
                 int32_t rows, float scale, const tfpa_scratch* sc, void* out, float* lse,
-                cudaStream_t stream, bool sliced) {
+                const Sink& sink, bool sliced) {
   int e;
   if ((e = check_cache(c)) || (e = check_segs(c, segs, nseg))) return e;
   if (!sc || !sc->part_o || !sc->part_ml || sc->cap_rows < 1 || sc->max_splits < 1)
@@ -495,9 +561,7 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
       const int grid = std::min(std::min(items, nsm), kMaxDecodeGrid);
       plan_cta_ranges(p, nd, G, fp8, grid);
       record(1, base, nrows, nd, items, grid, (int64_t)base * hd, 0);
-      if (!dry_run()) {
-        if ((e = to_err(launch_decode_partial(p, fp8, grid, stream)))) return e;
-      }
+      if ((e = sink.decode(p, fp8, grid))) return e;
     }
     if (nv > 0) {
       if ((e = fill_maps(c, segs, ss, fp8, fp8 ? 128 : 64, 128, pv.maps, pv.nsrc))) return e;
@@ -521,9 +585,7 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
       pv.max_splits = sc->max_splits;
       pv.scale_log2 = scale * 1.4426950408889634f;
       record(8, base, nrows, nv, tiles, tiles, (int64_t)base * hd, 0);
-      if (!dry_run()) {
-        if ((e = to_err(launch_verify(pv, fp8, tiles, stream)))) return e;
-      }
+      if ((e = sink.verify(pv, fp8, tiles))) return e;
     }
     if (sliced) {
       mp.part_o = part_o;
@@ -535,9 +597,7 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
       mp.hq = c->hq;
       mp.max_splits = sc->max_splits;
       record(2, base, nrows, nr, nrows * c->hq, (nrows * c->hq + 7) / 8, 0, (int64_t)base * hd);
-      if (!dry_run()) {
-        if ((e = to_err(launch_merge(mp, stream)))) return e;
-      }
+      if ((e = sink.merge(mp))) return e;
     }
   }
   return TFPA_OK;
@@ -550,7 +610,7 @@ extern "C" int tfpa_decode_partial(const tfpa_cache* cache, const tfpa_seg* segs
                                    int32_t rows, float softmax_scale, const tfpa_scratch* scratch,
                                    cudaStream_t stream) {
   return decode_impl(cache, segs, nseg, q, row_seg, row_pos, nullptr, rows, softmax_scale,
-                     scratch, nullptr, nullptr, stream, false);
+                     scratch, nullptr, nullptr, Sink{stream, nullptr}, false);
 }
 
 extern "C" int tfpa_decode(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
@@ -558,7 +618,7 @@ extern "C" int tfpa_decode(const tfpa_cache* cache, const tfpa_seg* segs, int32_
                            int32_t rows, float softmax_scale, const tfpa_scratch* scratch,
                            void* out, float* lse, cudaStream_t stream) {
   return decode_impl(cache, segs, nseg, q, row_seg, row_pos, nullptr, rows, softmax_scale,
-                     scratch, out, lse, stream, true);
+                     scratch, out, lse, Sink{stream, nullptr}, true);
 }
 
 extern "C" int tfpa_decode_tree(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
@@ -568,7 +628,7 @@ extern "C" int tfpa_decode_tree(const tfpa_cache* cache, const tfpa_seg* segs, i
                                 cudaStream_t stream) {
   if (rows > 0 && !row_anc) return TFPA_EINVAL;
   return decode_impl(cache, segs, nseg, q, row_seg, row_pos, row_anc, rows, softmax_scale,
-                     scratch, out, lse, stream, true);
+                     scratch, out, lse, Sink{stream, nullptr}, true);
 }
 
 extern "C" int tfpa_merge(const tfpa_scratch* sc, int32_t hq, int32_t rows,
@@ -621,7 +681,7 @@ struct RopeArgs {
 
 int write_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const void* k_rows,
                const void* v_rows, const int32_t* row_seg, const int32_t* row_pos, int32_t rows,
-               const RopeArgs& rope, cudaStream_t stream) {
+               const RopeArgs& rope, const Sink& sink) {
   int e;
   if ((e = check_cache(c)) || (e = check_segs(c, segs, nseg))) return e;
   if (rows > 0 && (!k_rows || !v_rows || !aligned(k_rows, 16) || !aligned(v_rows, 16)))
@@ -675,8 +735,7 @@ int write_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const vo
     p.num_pages = c->num_pages;
     p.fp8 = c->dtype == TFPA_FP8_E4M3;
     record(0, base, nrows, nr, nrows * c->hkv, (nrows * c->hkv + 15) / 16, 0, 0);
-    if (!dry_run())
-      if ((e = to_err(launch_write_kv(p, stream)))) return e;
+    if ((e = sink.write(p))) return e;
   }
   return TFPA_OK;
 }
@@ -687,7 +746,7 @@ extern "C" int tfpa_write_kv(const tfpa_cache* c, const tfpa_seg* segs, int32_t 
                              const void* k_rows, const void* v_rows, const int32_t* row_seg,
                              const int32_t* row_pos, int32_t rows, cudaStream_t stream) {
   return write_impl(c, segs, nseg, k_rows, v_rows, row_seg, row_pos, rows,
-                    RopeArgs{nullptr, nullptr, nullptr, 0}, stream);
+                    RopeArgs{nullptr, nullptr, nullptr, 0}, Sink{stream, nullptr});
 }
 
 extern "C" int tfpa_write_kv_rope(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg,
@@ -698,7 +757,87 @@ extern "C" int tfpa_write_kv_rope(const tfpa_cache* c, const tfpa_seg* segs, int
                                   cudaStream_t stream) {
   if (!rope_cos) return TFPA_EINVAL;
   return write_impl(c, segs, nseg, k_rows, v_rows, row_seg, row_pos, rows,
-                    RopeArgs{rope_pos, rope_cos, rope_sin, rope_n}, stream);
+                    RopeArgs{rope_pos, rope_cos, rope_sin, rope_n}, Sink{stream, nullptr});
+}
+
+// ------------------------------------------------------------ plans
+extern "C" tfpa_plan* tfpa_plan_create(void) { return new (std::nothrow) tfpa_plan(); }
+
+extern "C" void tfpa_plan_destroy(tfpa_plan* plan) { delete plan; }
+
+extern "C" void tfpa_plan_clear(tfpa_plan* plan) {
+  if (!plan) return;
+  plan->entries.clear();
+  plan->decode.clear();
+  plan->verify.clear();
+  plan->merge.clear();
+  plan->write.clear();
+}
+
+extern "C" int32_t tfpa_plan_launches(const tfpa_plan* plan) {
+  return plan ? (int32_t)plan->entries.size() : 0;
+}
+
+namespace {
+// Runs a planning call into `plan`; on failure the plan is left as it was.
+template <typename F>
+int plan_call(tfpa_plan* plan, F&& fn) {
+  if (!plan) return TFPA_EINVAL;
+  const Sink sink{nullptr, plan};
+  const Sink::Mark m = sink.mark();
+  int e;
+  try {
+    e = fn(sink);
+  } catch (const std::bad_alloc&) {
+    e = TFPA_EINVAL;
+  }
+  if (e != TFPA_OK) sink.rollback(m);
+  return e;
+}
+}  // namespace
+
+extern "C" int tfpa_plan_write_kv(tfpa_plan* plan, const tfpa_cache* c, const tfpa_seg* segs,
+                                  int32_t nseg, const void* k_rows, const void* v_rows,
+                                  const int32_t* row_seg, const int32_t* row_pos,
+                                  int32_t rows) {
+  return plan_call(plan, [&](const Sink& sink) {
+    return write_impl(c, segs, nseg, k_rows, v_rows, row_seg, row_pos, rows,
+                      RopeArgs{nullptr, nullptr, nullptr, 0}, sink);
+  });
+}
+
+extern "C" int tfpa_plan_decode(tfpa_plan* plan, const tfpa_cache* cache, const tfpa_seg* segs,
+                                int32_t nseg, const void* q, const int32_t* row_seg,
+                                const int32_t* row_pos, int32_t rows, float softmax_scale,
+                                const tfpa_scratch* scratch, void* out, float* lse) {
+  return plan_call(plan, [&](const Sink& sink) {
+    return decode_impl(cache, segs, nseg, q, row_seg, row_pos, nullptr, rows, softmax_scale,
+                       scratch, out, lse, sink, true);
+  });
+}
+
+extern "C" int tfpa_plan_launch(const tfpa_plan* plan, cudaStream_t stream) {
+  if (!plan) return TFPA_EINVAL;
+  if (dry_run()) return TFPA_OK;
+  for (const tfpa_plan::Entry& en : plan->entries) {
+    cudaError_t r = cudaSuccess;
+    switch (en.kind) {
+      case tfpa_plan::kDecode:
+        r = launch_decode_partial(plan->decode[en.index], en.fp8, en.grid, stream);
+        break;
+      case tfpa_plan::kVerify:
+        r = launch_verify(plan->verify[en.index], en.fp8, en.grid, stream);
+        break;
+      case tfpa_plan::kMerge:
+        r = launch_merge(plan->merge[en.index], stream);
+        break;
+      case tfpa_plan::kWrite:
+        r = launch_write_kv(plan->write[en.index], stream);
+        break;
+    }
+    if (r != cudaSuccess) return TFPA_ECUDA;
+  }
+  return TFPA_OK;
 }
 
 extern "C" int tfpa_keep_kv(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg,

@@ -287,3 +287,32 @@ def test_planning_from_two_host_threads_at_once():
     key = lambda r: tuple(sorted(r.items()))
     want = sorted([key(r) for r in alone_a] * 200 + [key(r) for r in alone_b] * 200)
     assert sorted(key(r) for r in rec) == want
+
+
+def test_plans_hold_the_direct_calls_launches():
+    """A plan records the same launches as the direct calls (at planning
+    time), holds them until cleared, and a failing planning call leaves it
+    as it was."""
+    c = _cache()
+    segs = [B.Seg(40000, page_table=3 * FAKE), B.Seg(700, k_slab=8 * FAKE, v_slab=9 * FAKE,
+                                                     slab_cap=768)]
+    rs = np.array([0] * 20 + [1])
+    rp = np.array(list(range(39980, 40000)) + [699])
+    sc = B.Scratch(5 * FAKE, 6 * FAKE, 16)
+    with B.record_launches() as direct:
+        B.tfpa_write_kv(c, segs, 4 * FAKE, 5 * FAKE, rs, rp, stream=0)
+        B.tfpa_decode(c, segs, 4 * FAKE, rs, rp, 0.088, sc, 7 * FAKE, stream=0)
+    plan = B.Plan()
+    with B.record_launches() as planned:
+        plan.write_kv(c, segs, 4 * FAKE, 5 * FAKE, rs, rp)
+        plan.decode(c, segs, 4 * FAKE, rs, rp, 0.088, sc, 7 * FAKE)
+        plan.launch(stream=0)                       # dry run: nothing is enqueued or recorded
+    assert planned == direct
+    assert len(plan) == len(direct)
+    with B.record_launches():
+        with pytest.raises(B.TfpaError) as e:
+            plan.decode(c, segs, 4 * FAKE, rs, np.full(21, 40000), 0.088, sc, 7 * FAKE)
+    assert e.value.code == B.TFPA_ERANGE
+    assert len(plan) == len(direct)                 # the failed call appended nothing
+    plan.clear()
+    assert len(plan) == 0
