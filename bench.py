@@ -807,9 +807,10 @@ def main():
         n_e2e = max(10, min(args.steps, 500))
         e2e = time_e2e_calls(w, torch, B, ctx, n_e2e, args.warmup)
         e2e_s = max_over_ranks(dist, torch, e2e[0])
-        e2e_aa = time_e2e_calls(w, torch, B, ctx, n_e2e, args.warmup)
         e2e_pipe = time_e2e_calls(w, torch, B, ctx, n_e2e, args.warmup, in_flight=2)
         e2e_plan = time_e2e_planned(w, torch, B, ctx, n_e2e, args.warmup)
+        e2e_plan = (max_over_ranks(dist, torch, e2e_plan[0]),) + tuple(e2e_plan[1:])
+        e2e_plan_aa = time_e2e_planned(w, torch, B, ctx, n_e2e, args.warmup)
         e2e_graph_s = time_e2e_graph(w, torch, B, ctx, n_e2e, args.warmup)
         del ctx
         s3, p3, ctx3, _ = time_decode(w3, torch, B, max(10, args.steps // 4), args.warmup, None)
@@ -930,32 +931,34 @@ def main():
                      "kernel": "decode_partial_kernel<bf16>", "peak_source": pk["source"],
                      "partial_ms": partial_ms},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * e2e[1] / e2e_s / 1e9, "unit": "GB/s",
+        "e2e": {"value": world * e2e_plan[1] / e2e_plan[0] / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": e2e[4], "d2h_bytes_per_step": e2e[5],
-                "ms_per_step": e2e_s * 1e3, "vs_device_step": e2e_s * 1e3 / step_ms,
-                "host_us_per_call": {"tfpa_write_kv": e2e[2], "tfpa_decode": e2e[3]},
+                "ms_per_step": e2e_plan[0] * 1e3, "vs_device_step": e2e_plan[0] * 1e3 / step_ms,
+                "host_us_per_call": {"tfpa_plan_launch": e2e_plan[2],
+                                     "planning_a_step_overlapped": e2e_plan[3]},
                 "steps": n_e2e,
-                "how": "real tfpa_write_kv + tfpa_decode calls every step (no graph), each "
-                       "stream one position longer every step (%d..%d), one pinned input "
-                       "copy (q + new K/V rows) and one output copy per step, the host "
-                       "waits for each step's output before the next; host_us_per_call = "
-                       "host clock around each call (binding + C planning + launches), "
-                       "median" % (w.streams[0].seq_len - n_e2e + 1, w.streams[0].seq_len)},
-        "e2e_aa_repeat": {"ms_per_step": [e2e_s * 1e3, e2e_aa[0] * 1e3],
-                          "spread_pct": 100 * abs(e2e_aa[0] - e2e_s) / e2e_s},
+                "how": "a decode loop through the public API with host buffers, one step at a "
+                       "time: each stream one position longer every step (%d..%d); per step one "
+                       "pinned input copy (q + new K/V rows), tfpa_plan_launch of the step's "
+                       "tfpa_write_kv + tfpa_decode launches (planned with tfpa_plan_write_kv "
+                       "+ tfpa_plan_decode while the previous step ran), one output copy, and "
+                       "the host waits for the output before the next step; host times are "
+                       "host clock, median" % (w.streams[0].seq_len - n_e2e + 1,
+                                               w.streams[0].seq_len),
+                "direct_calls": {
+                    "value": world * e2e[1] / e2e_s / 1e9, "unit": "GB/s",
+                    "ms_per_step": e2e_s * 1e3, "vs_device_step": e2e_s * 1e3 / step_ms,
+                    "host_us_per_call": {"tfpa_write_kv": e2e[2], "tfpa_decode": e2e[3]},
+                    "how": "the same loop calling tfpa_write_kv and tfpa_decode directly "
+                           "(planning and launching inside each call)"}},
+        "e2e_aa_repeat": {"ms_per_step": [e2e_plan[0] * 1e3, e2e_plan_aa[0] * 1e3],
+                          "spread_pct": 100 * abs(e2e_plan_aa[0] - e2e_plan[0]) / e2e_plan[0]},
         "e2e_two_in_flight": {
             "value": world * e2e_pipe[1] / e2e_pipe[0] / 1e9, "unit": "GB/s",
             "ms_per_step": e2e_pipe[0] * 1e3,
             "host_us_per_call": {"tfpa_write_kv": e2e_pipe[2], "tfpa_decode": e2e_pipe[3]},
             "how": "the same loop with step i + 1 enqueued before the host waits for step "
                    "i's output (two input and output buffers)"},
-        "e2e_planned": {
-            "value": world * e2e_plan[1] / e2e_plan[0] / 1e9, "unit": "GB/s",
-            "ms_per_step": e2e_plan[0] * 1e3, "vs_device_step": e2e_plan[0] * 1e3 / step_ms,
-            "host_us_per_plan_launch": e2e_plan[2], "host_us_planning_a_step": e2e_plan[3],
-            "how": "the same serial loop (one step at a time, host waits for each output), "
-                   "each step planned with tfpa_plan_write_kv + tfpa_plan_decode while the "
-                   "previous step runs, then launched with tfpa_plan_launch"},
         "e2e_graph_replay": {
             "value": world * (kv + qo) / e2e_graph_s / 1e9, "unit": "GB/s",
             "ms_per_step": e2e_graph_s * 1e3,
@@ -966,7 +969,7 @@ def main():
         "gpu_launches": 3 * args.steps,
         "timing": "decode step = one CUDA-graph replay of tfpa_write_kv + tfpa_decode "
                   "(3 kernels), CUDA events over --steps replays (device time); e2e = real "
-                  "calls per step, host clock (see e2e.how); the per-call lines (prefill, "
+                  "planned calls per step, host clock (see e2e.how); the per-call lines (prefill, "
                   "tiny_decode, overcommitted_pool, tree_verify, kv_store_rope, keep, "
                   "save_restore) are device time: CUDA events around one call, enqueued by "
                   "the host during a preceding GPU sleep",
