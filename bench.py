@@ -12,6 +12,13 @@ unmasked (row, key) pairs.
 Inputs are 268 MB of KV per step, above the 129 MB L2, so no flush is needed
 between decode steps; the prompt-chunk timing flushes L2 between launches.
 
+e2e is a decode loop through the public API with host buffers, one step at a
+time and every stream one position longer each step: a pinned input copy,
+the step's planned launches (tfpa_plan_launch; the next step is planned with
+tfpa_plan_write_kv / tfpa_plan_decode while this one runs), an output copy,
+and a host wait.  The same loop with direct tfpa_write_kv / tfpa_decode calls
+is reported beside it, with the host time of each call.
+
 Launch: ``python bench.py [--gpus N --steps K --warmup W] [--impl reference]``;
 for N > 1 under torchrun every rank runs its own replica (no collective on the
 data path) and rank 0 prints one JSON line with the max time over ranks.
