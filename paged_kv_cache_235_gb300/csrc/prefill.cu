@@ -477,13 +477,12 @@ __device__ __forceinline__ void zero_v_rows(uint8_t* vtile, int z0, int lane) {
 }
 
 // e4m3 staging tile [128 rows][128 B] (128B swizzle) -> f16 operand tile
-// [128 rows][2 halves of 64] (128B swizzle) by nthr threads (thread t of
-// them; nthr 128, 192, 256 or 320); rows >= z0 become 0.
-__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int z0, int t,
-                                             int nthr) {
+// [128 rows][2 halves of 64] (128B swizzle), 64 threads; rows >= z0 become 0.
+__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int z0, int t) {
   const uint32_t sb = smem_u32(src), db = smem_u32(dst);
-#pragma unroll 2
-  for (int i = t; i < kTileKeys * 8; i += nthr) {   // (row, 16-byte source chunk)
+#pragma unroll 4
+  for (int k = 0; k < 8; ++k) {
+    const int i = t + 128 * k;             // (row, 16-byte source chunk)
     const int row = i >> 3, c8 = i & 7;    // source chunk c8 = head dims 16*c8 .. +15
     uint4 w = lds128(swz128(sb, row, c8));
     if (row >= z0) w = make_uint4(0, 0, 0, 0);
@@ -508,11 +507,9 @@ __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, i
 // through one staging tile each.  Verify: V only (K feeds 8-bit MMAs), slot
 // hh's step jj from staging tile 2 hh + (jj & 1).
 template <bool VERIFY>
-// t: this thread among the nthr converting threads (the converter warps,
-// and in verify mode also the softmax warps whose rows are all past the
-// tile's last row).
-__device__ bool converter(const PrefillParams& p, const RunInfo& ru, const TileGeom& gm,
-                          uint8_t* smem, const Bars& b, int t, int nthr) {
+__device__ void converter(const PrefillParams& p, const RunInfo& ru, const TileGeom& gm,
+                          uint8_t* smem, const Bars& b) {
+  const int t = threadIdx.x - kConvWarp0 * 32;   // 0..127
   const int lane = threadIdx.x & 31;
   // Staging tile `src` (K, or V with rows from z0 on zeroed: past the
   // stream's end, or all rows of a bad page) into 16-bit stage s.
@@ -522,8 +519,7 @@ __device__ bool converter(const PrefillParams& p, const RunInfo& ru, const TileG
     uint64_t* full = is_v ? &b.v_full[s] : &b.k_full[s];
     if (!mbar_wait_or_abort(full8, ph8, p.err_flag, b.abort)) return false;
     if (!mbar_wait_or_abort(empty, ph ^ 1, p.err_flag, b.abort)) return false;
-    convert_tile(smem + src, smem + (is_v ? kOffV : kOffK) + s * 32768, is_v ? z0 : kTileKeys, t,
-                 nthr);
+    convert_tile(smem + src, smem + (is_v ? kOffV : kOffK) + s * 32768, is_v ? z0 : kTileKeys, t);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
@@ -546,7 +542,7 @@ __device__ bool converter(const PrefillParams& p, const RunInfo& ru, const TileG
                      b.v8_full + i, b.v8_empty + i);
       }
     }
-    return ok;
+    return;
   }
   PageCheck pc(p, ru, gm, gm.kt0, gm.nkt, 1);
   for (int jj = 0; jj < gm.nkt; ++jj) {
@@ -556,10 +552,9 @@ __device__ bool converter(const PrefillParams& p, const RunInfo& ru, const TileG
     const uint32_t ph = (jj >> 1) & 1;
     // one staging tile each for K and V: its jj-th fill is phase jj & 1
     const uint32_t ph8 = (uint32_t)(jj & 1);
-    if (!convert(false, s, ph, z0, stage8_off(false), ph8, b.k8_full, b.k8_empty)) return false;
-    if (!convert(true, s, ph, z0, stage8_off(true), ph8, b.v8_full, b.v8_empty)) return false;
+    if (!convert(false, s, ph, z0, stage8_off(false), ph8, b.k8_full, b.k8_empty)) return;
+    if (!convert(true, s, ph, z0, stage8_off(true), ph8, b.v8_full, b.v8_empty)) return;
   }
-  return true;
 }
 
 template <bool FP8, bool VERIFY>
@@ -858,11 +853,9 @@ __device__ __forceinline__ uint32_t part_ml(uint32_t smem_base, int hh, int r) {
 }
 
 template <bool FP8, bool VERIFY>
-// conv_t >= 0 (verify tiles on e4m3 caches): this warp has no rows of the
-// tile and converts V as thread conv_t of the conv_n converting threads.
 __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Tile& x,
                              const TileGeom& gm, uint32_t rank, int hh, uint8_t* smem,
-                             uint32_t tmem, const Bars& b, int conv_t, int conv_n) {
+                             uint32_t tmem, const Bars& b) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = 32 * (warp & 3) + lane;                 // row of the tile = TMEM lane
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
@@ -911,9 +904,7 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
   // read into any output.  It still waits for each S and arrives on p_ready,
   // which keeps it in step with the MMA issuer.
   const bool idle = !__any_sync(0xffffffffu, valid);
-  if (VERIFY && FP8 && conv_t >= 0) {
-    if (ok) ok = converter<VERIFY>(p, ru, gm, smem, b, conv_t, conv_n);
-  } else
+
   for (int jj = 0; ok && jj < nt; ++jj) {
     const int j = slot_tile<VERIFY>(gm, jj, hh);
     const bool page_bad = pc.bad(j);
@@ -1184,26 +1175,13 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
   b.dst_free = bars + 23;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // Verify tiles on e4m3 caches: the softmax warps whose 32 rows all lie
-  // past the tile's query vectors (warps `active`..3 of each slot) convert V
-  // with the converter warps, and p_ready counts the others only.
-  int active = 4;
-  if (VERIFY && FP8) {
-    const Tile x0 = tile_of<VERIFY>(p, blockIdx.x);
-    const int nrows = geom_of<VERIFY>(p, p.runs[x0.run], x0, 0).nrows;
-    const int vq = min(nrows * p.group, p.group * (kVerifyVectors / p.group));
-    active = min(4, (vq + 31) >> 5);
-  }
-  const int conv_n = kConvWarps * 32 + 64 * (4 - active);   // converting threads
-
   if (threadIdx.x == 0) {
-    // the converter warps (and their helpers), or the producer
-    const uint32_t stage_arrivals = FP8 ? (uint32_t)(conv_n >> 5) : 1;
+    const uint32_t stage_arrivals = FP8 ? kConvWarps : 1;   // the converters, or the producer
     mbar_init(b.q_full, 1);
     mbar_init(bars + 1, VERIFY ? 4 : 8);           // q_ready: the (slot A) softmax warps
     for (int i = 0; i < 2; ++i) {
       mbar_init(&b.s_full[i], 1);
-      mbar_init(&b.p_ready[i], (uint32_t)active);
+      mbar_init(&b.p_ready[i], 4);
     }
     for (int i = 0; i < (kRing3 ? 3 : 2); ++i) {
       mbar_init(&b.v_full[i], stage_arrivals);
@@ -1214,7 +1192,7 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
         mbar_init(&b.k_full[i], 1);                // the producer's TMA
         mbar_init(&b.k_empty[i], 1);
         mbar_init(&b.v8_full[i], 1);
-        mbar_init(&b.v8_empty[i], (uint32_t)(conv_n >> 5));
+        mbar_init(&b.v8_empty[i], kConvWarps);
       }
     } else {
       for (int i = 0; i < (kRing3 ? 3 : 2); ++i) {
@@ -1266,14 +1244,10 @@ __global__ void __launch_bounds__(threads_of<FP8>(), 1)
     }
   } else if (warp < kConvWarp0) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kHigh));
-    const int hh = (warp - 4) >> 2, wq = (warp - 4) & 3;
-    const int conv_t = (VERIFY && FP8 && wq >= active)
-                           ? kConvWarps * 32 + 32 * (hh * (4 - active) + wq - active) + lane
-                           : -1;
-    softmax_role<FP8, VERIFY>(p, ru, x, gm, rank, hh, smem, tmem, b, conv_t, conv_n);
+    softmax_role<FP8, VERIFY>(p, ru, x, gm, rank, (warp - 4) >> 2, smem, tmem, b);
   } else if (FP8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kConv));
-    converter<VERIFY>(p, ru, gm, smem, b, threadIdx.x - kConvWarp0 * 32, conv_n);
+    converter<VERIFY>(p, ru, gm, smem, b);
   }
   umma::fence_before_sync();
   __syncthreads();
