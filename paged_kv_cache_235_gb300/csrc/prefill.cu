@@ -156,8 +156,8 @@ struct Tile {
   int run, g, hp, t, sigma;
 };
 
-// Prefill tiles: kv head slowest, then row tiles heaviest first (from the
-// last, longest causal range, to the first), then query-head pairs.
+// Prefill tiles are numbered heaviest first: the row-tile index is the
+// slowest digit and runs from the last (longest causal range) to the first.
 // Verify tiles: split, kv head, row tile (slowest first).
 template <bool VERIFY>
 __device__ __forceinline__ Tile tile_of(const PrefillParams& p, int i) {
@@ -178,14 +178,12 @@ __device__ __forceinline__ Tile tile_of(const PrefillParams& p, int i) {
     x.hp = 0;
     return x;
   }
-  // kv head slowest, so the tiles running at once share one or two kv
-  // heads' K and V in L2; then row tiles heaviest first, then head pairs
+  const int pairs_total = p.hkv * npairs;
   const int ntr = (ru.nrows + kTileRows - 1) / kTileRows;
-  const int per_g = ntr * npairs;
-  x.g = local / per_g;
-  const int rest = local - x.g * per_g;
-  const int t_rev = rest / npairs;
-  x.hp = rest - t_rev * npairs;
+  const int t_rev = local / pairs_total;
+  const int gp = local - t_rev * pairs_total;
+  x.g = gp / npairs;
+  x.hp = gp - x.g * npairs;
   x.t = ntr - 1 - t_rev;
   x.sigma = 0;
   return x;
