@@ -62,12 +62,8 @@ constexpr int kTileRows = 128;
 constexpr int kTileKeys = 128;
 // bf16: warps 0-11.  e4m3: warps 0-15, warps 12-15 converting the staged
 // e4m3 tiles (one warp per SM sub-partition, beside the softmax warps).
-// bf16 prompt tiles: warps 0-19, the softmax of each head and row quarter
-// shared by two warps (key columns 0-63 and 64-127 of each tile).
-template <bool FP8, bool VERIFY>
-__host__ __device__ constexpr bool split_softmax() { return !FP8 && !VERIFY; }
-template <bool FP8, bool VERIFY>
-__host__ __device__ constexpr int threads_of() { return FP8 ? 512 : (VERIFY ? 384 : 640); }
+template <bool FP8>
+constexpr int threads_of() { return FP8 ? 512 : 384; }
 constexpr int kConvWarp0 = 12;
 constexpr int kConvWarps = 4;
 constexpr int kOffQ = 0;                 // 2 heads x [128 rows][128] 16-bit = 64 KB
@@ -75,11 +71,6 @@ constexpr int kOffK = 65536;             // 2 stages x 32 KB (16-bit operand til
 constexpr int kOffV = 131072;            // 2 stages x 32 KB
 constexpr int kOffK8 = 196608;           // prefill, e4m3: the K staging tile, 16 KB
 constexpr int kOffV8 = 212992;           // prefill, e4m3: the V staging tile, 16 KB
-// bf16 prompt tiles: the two halves' row maxima and sums, [2 step parities]
-// [2 heads][4 row quarters][2 halves][32 rows] floats, then one mbarrier per
-// (head, row quarter) that both halves arrive on once a step
-constexpr int kOffXch = kOffK8;
-constexpr int kOffXchBar = kOffXch + 2 * 2 * 4 * 2 * 32 * 4;
 // Verify mode holds Q in the first Q tile (32 KB) only.  bf16: the second
 // is K stage 2 of the rings of three.  e4m3: the Q tile becomes two e4m3
 // tiles (hi and lo, 16 KB each) that feed 8-bit MMAs with K straight from
@@ -111,40 +102,31 @@ static_assert(Layout<true>::kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
 // Register split per warpgroup (setmaxnreg): warps 0-3 (TMA producer, MMA
 // issuer) and the converters need few registers, the softmax warps (a
-// row's 128 scores each, or 64 with split softmax) many.  A split hands out
-// no more than the block launches with (e4m3: 512 x 128, bf16 verify: 384 x
-// 168, bf16 prompt tiles: 640 x 96), and no SM sub-partition (one warp of
-// each warpgroup) more than its 16,384.  The bf16 verify split was picked by
-// measurement: 64 / 216 ran 2.7 % faster than no split, where 56 / 224 and
-// 72 / 216 (the latter without any spill) ran slower.
-template <bool FP8, bool VERIFY>
+// row's 128 scores each) many.  A split hands out no more than the block
+// launches with (e4m3: 512 x 128, bf16: 384 x 168), and no SM sub-partition
+// (one warp of each warpgroup) more than its 16,384.  The bf16 split was
+// picked by measurement: 64 / 216 ran 2.7 % faster than no split, where
+// 56 / 224 and 72 / 216 (the latter without any spill) ran slower.
+template <bool FP8>
 struct Regs;
-template <bool VERIFY>
-struct Regs<true, VERIFY> {
-  static constexpr int kLow = 56, kHigh = 200, kConv = 56, kLaunch = 128, kHighGroups = 2;
+template <>
+struct Regs<true> {
+  static constexpr int kLow = 56, kHigh = 200, kConv = 56, kLaunch = 128;
 };
 template <>
-struct Regs<false, true> {
-  static constexpr int kLow = 64, kHigh = 216, kConv = 0, kLaunch = 168, kHighGroups = 2;
+struct Regs<false> {
+  static constexpr int kLow = 64, kHigh = 216, kConv = 0, kLaunch = 168;
 };
-template <>
-struct Regs<false, false> {
-  static constexpr int kLow = 64, kHigh = 104, kConv = 0, kLaunch = 96, kHighGroups = 4;
-};
-template <bool FP8, bool VERIFY>
+template <bool FP8>
 constexpr int regs_split() {
-  using R = Regs<FP8, VERIFY>;
-  return 128 * (R::kLow + R::kHighGroups * R::kHigh + R::kConv);
+  return 128 * (Regs<FP8>::kLow + 2 * Regs<FP8>::kHigh + Regs<FP8>::kConv);
 }
-template <bool FP8, bool VERIFY>
-constexpr bool regs_fit() {
-  using R = Regs<FP8, VERIFY>;
-  return regs_split<FP8, VERIFY>() <= threads_of<FP8, VERIFY>() * R::kLaunch &&
-         32 * (R::kLow + R::kHighGroups * R::kHigh + R::kConv) <= 16384;
-}
-static_assert(regs_fit<true, false>() && regs_fit<true, true>() && regs_fit<false, true>() &&
-                  regs_fit<false, false>(),
-              "register split");
+static_assert(regs_split<true>() <= 512 * Regs<true>::kLaunch, "register split");
+static_assert(regs_split<false>() <= 384 * Regs<false>::kLaunch, "register split");
+static_assert(32 * (Regs<true>::kLow + 2 * Regs<true>::kHigh + Regs<true>::kConv) <= 16384,
+              "sub-partition registers");
+static_assert(32 * (Regs<false>::kLow + 2 * Regs<false>::kHigh) <= 16384,
+              "sub-partition registers");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 __device__ __forceinline__ uint32_t col_s(int hh) { return hh ? 256u : 0u; }
 __device__ __forceinline__ uint32_t col_o(int hh) { return hh ? 384u : 128u; }
@@ -166,7 +148,6 @@ struct Bars {
   uint64_t* drain;
   uint64_t* peer_ready;  // CTA 0: CTA 1's softmax threads stored their partial here
   uint64_t* dst_free;    // CTA 1: CTA 0's MMAs are done with its rings
-  uint64_t* xch;         // bf16 prompt tiles: [2 heads][4 row quarters], the halves' exchange
   uint32_t* tmem_slot;
   volatile int* abort;
 };
@@ -1160,200 +1141,8 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
         l_all > 0.f ? (m_all + log2f(l_all)) * 0.6931471805599453f : -INFINITY;
 }
 
-// bf16 prompt tiles with split softmax: two warps per (head hh, row
-// quarter), half 0 over key columns 0-63 of each key tile and half 1 over
-// columns 64-127.  Each step both halves load their scores, take their rows'
-// partial maxima and exchange them in shared memory (an mbarrier of the
-// pair, both halves arriving once a step; slots alternate by step parity),
-// so both compute the same running max; each writes its 32 P pairs (P pair k
-// of the tile = keys 2k, 2k + 1, so half h's pairs are TMEM columns 32h ..),
-// rescales its 64 O columns and keeps its own row sum.  After the last step
-// the halves exchange their sums and add them in a fixed order.  In the
-// epilogue each half merges and writes its 64 output columns.  Half 1's P
-// store overwrites scores of half 0 (columns 32-63): both halves have read
-// their scores before the exchange, which comes first.
-__device__ void softmax_split_role(const PrefillParams& p, const RunInfo& ru, const Tile& x,
-                                   const TileGeom& gm, uint32_t rank, int hh, int half,
-                                   uint8_t* smem, uint32_t tmem, const Bars& b) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, qtr = warp & 3;
-  const int r = 32 * qtr + lane;                        // row of the tile = TMEM lane
-  const uint32_t lane_off = (uint32_t)(32 * qtr) << 16;
-  const uint32_t tS = tmem + lane_off + col_s(hh) + 64u * half;   // this half's scores
-  const uint32_t tP = tmem + lane_off + col_s(hh) + 32u * half;   // its P pairs
-  const uint32_t tO = tmem + lane_off + col_o(hh) + 64u * half;   // its O columns
-  const bool valid = r < gm.nrows;
-  const int pos = ru.pos0 + gm.row_lo + (valid ? r : 0);
-  const float sl2 = p.scale_log2;
-  float* xch = reinterpret_cast<float*>(smem + kOffXch);
-  uint64_t* xbar = b.xch + hh * 4 + qtr;
-  auto slot = [&](int par, int hf) -> float* {
-    return xch + ((((par * 2 + hh) * 4 + qtr) * 2 + hf) << 5) + lane;
-  };
-  // Both halves' values of this round (parity par): write own, arrive, wait.
-  auto exchange = [&](float mine, int round, float& other) {
-    const int par = round & 1;
-    *slot(par, half) = mine;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(xbar);
-    if (!mbar_wait_or_abort(xbar, (uint32_t)par, p.err_flag, b.abort)) return false;
-    other = *slot(par, half ^ 1);
-    return true;
-  };
-  float m_run = -INFINITY, l = 0.f;
-  bool ok = true;
-  PageCheck pc(p, ru, gm, gm.kt0, gm.nkt, 1);
-  int jj = 0;
-  for (; ok && jj < gm.nkt; ++jj) {
-    const int j = gm.kt0 + jj;
-    const bool page_bad = pc.bad(j);
-    if (!(ok = mbar_wait_or_abort(&b.s_full[hh], jj & 1, p.err_flag, b.abort))) break;
-    umma::fence_after_sync();
-    const int kt = j * kTileKeys + 64 * half;
-    const int lim = page_bad ? -1 : pos - kt;            // key kt+i visible iff i <= lim
-    uint32_t sv[2][32];
-    umma::tmem_ld32(tS, sv[0]);
-    umma::tmem_ld32(tS + 32, sv[1]);
-    umma::tmem_ld_wait();
-    if (lim < 63) {
-      // hidden keys' scores become -inf (exactly 0 after the exponential)
-#pragma unroll
-      for (int i = 0; i < 64; ++i)
-        if (i > lim) sv[i >> 5][i & 31] = 0xff800000u;
-    }
-    float mx = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < 32; ++k)
-      mx = fmax3(mx, __uint_as_float(sv[(2 * k) >> 5][(2 * k) & 31]),
-                 __uint_as_float(sv[(2 * k + 1) >> 5][(2 * k + 1) & 31]));
-    float mo;
-    if (!(ok = exchange(mx, jj, mo))) break;
-    mx = fmaxf(mx, mo) * sl2;                            // the same in both halves
-    const float m_new = fmaxf(m_run, mx);
-    const bool resc = m_new > m_run + kRescaleThreshold;
-    float alpha = 1.f;
-    if (resc) {
-      alpha = fast_exp2(m_run - m_new);
-      l *= alpha;
-      m_run = m_new;
-    }
-    const float nbase = m_run == -INFINITY ? 0.f : -m_run;
-    f2 acc = {0.f, 0.f};
-    const f2 sc2 = {sl2, sl2}, nb2 = {nbase, nbase};
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const int i0 = 2 * k;
-      const f2 t = ffma2({__uint_as_float(sv[i0 >> 5][i0 & 31]),
-                          __uint_as_float(sv[(i0 + 1) >> 5][(i0 + 1) & 31])}, sc2, nb2);
-      const f2 e = {fast_exp2(t.x), fast_exp2(t.y)};
-      acc = fadd2(acc, e);
-      sv[0][k] = pack_bf16x2(e.x, e.y);
-    }
-    umma::tmem_st32(tP, sv[0]);
-    if (jj > 0 && __any_sync(0xffffffffu, resc)) {     // this half's O *= alpha in TMEM
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t o[32];
-        umma::tmem_ld32(tO + 32 * c, o);
-        umma::tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        umma::tmem_st32(tO + 32 * c, o);
-      }
-    }
-    l += acc.x + acc.y;
-    umma::tmem_st_wait();
-    umma::fence_before_sync();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&b.p_ready[hh]);
-  }
-  if (ok) ok = mbar_wait_or_abort(b.o_final, 0, p.err_flag, b.abort);
-  if (ok) umma::fence_after_sync();
-  // the row sum: both halves' parts, added in a fixed order
-  float lo = 0.f;
-  if (ok) ok = exchange(l, gm.nkt, lo);
-  l = ok ? (half ? lo + l : l + lo) : l;
-
-  const uint32_t sbase = smem_u32(smem);
-  if (rank == 1) {
-    // Store (m, l, O) into CTA 0 once its rings are free; arrive on its
-    // barrier whatever happened, so that it never waits out the time limit
-    // on this CTA's account.
-    const bool free = mbar_wait_cluster(b.dst_free, 0, p.err_flag);
-    if (ok && free) {
-      const uint32_t orow = mapa_shared(part_o_row(sbase, hh, r), 0);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t o[32];
-        umma::tmem_ld32(tO + 32 * c, o);
-        umma::tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st_cluster128(orow + part_o_chunk(r, 16 * half + 8 * c + q), o[4 * q], o[4 * q + 1],
-                        o[4 * q + 2], o[4 * q + 3]);
-      }
-      if (half == 0) st_cluster_f2(mapa_shared(part_ml(sbase, hh, r), 0), m_run, l);
-    }
-    mbar_arrive_remote(mapa_shared(smem_u32(b.peer_ready), 0));
-    return;
-  }
-
-  // CTA 0: its MMAs are done (or it gave up), so CTA 1 may store into the
-  // rings.  Then merge CTA 1's half into this one, normalise, write.
-  if (threadIdx.x == 128) mbar_arrive_remote(mapa_shared(smem_u32(b.dst_free), 1));
-  const bool peer = mbar_wait_cluster(b.peer_ready, 0, p.err_flag);
-  if (!ok || !peer) return;
-  float2 ml1;
-  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(ml1.x), "=f"(ml1.y)
-               : "r"(part_ml(sbase, hh, r)) : "memory");
-  const float m_all = fmaxf(m_run, ml1.x);
-  const float a0 = m_run == -INFINITY ? 0.f : fast_exp2(m_run - m_all);
-  const float a1 = ml1.x == -INFINITY ? 0.f : fast_exp2(ml1.x - m_all);
-  const float l_all = __fmaf_rn(l, a0, __fmul_rn(ml1.y, a1));
-  const float inv = l_all > 0.f ? 1.f / l_all : 0.f;
-  const float c0 = a0 * inv, c1 = a1 * inv;
-  const int h = x.g * p.group + 2 * x.hp + hh;
-  const bool write = valid && (2 * x.hp + hh) < p.group;
-  uint4* dst = reinterpret_cast<uint4*>(
-      p.out + ((size_t)(ru.row0 + gm.row_lo + r) * p.hq + h) * kHeadDim);
-  const uint32_t prow = part_o_row(sbase, hh, r);
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    uint32_t o[32];
-    if (gm.nkt > 0) {
-      umma::tmem_ld32(tO + 32 * c, o);
-      umma::tmem_ld_wait();
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] = 0u;
-    }
-    float f[32];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const uint4 w = lds128(prow + part_o_chunk(r, 16 * half + 8 * c + q));
-      f[4 * q + 0] = __fmaf_rn(__uint_as_float(o[4 * q + 0]), c0, __fmul_rn(__uint_as_float(w.x), c1));
-      f[4 * q + 1] = __fmaf_rn(__uint_as_float(o[4 * q + 1]), c0, __fmul_rn(__uint_as_float(w.y), c1));
-      f[4 * q + 2] = __fmaf_rn(__uint_as_float(o[4 * q + 2]), c0, __fmul_rn(__uint_as_float(w.z), c1));
-      f[4 * q + 3] = __fmaf_rn(__uint_as_float(o[4 * q + 3]), c0, __fmul_rn(__uint_as_float(w.w), c1));
-    }
-    if (write) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 v;
-        v.x = pack_bf16x2(f[8 * q + 0], f[8 * q + 1]);
-        v.y = pack_bf16x2(f[8 * q + 2], f[8 * q + 3]);
-        v.z = pack_bf16x2(f[8 * q + 4], f[8 * q + 5]);
-        v.w = pack_bf16x2(f[8 * q + 6], f[8 * q + 7]);
-        dst[8 * half + 4 * c + q] = v;
-      }
-    }
-  }
-  if (write && half == 0 && p.lse)
-    p.lse[(size_t)(ru.row0 + gm.row_lo + r) * p.hq + h] =
-        l_all > 0.f ? (m_all + log2f(l_all)) * 0.6931471805599453f : -INFINITY;
-}
-
 template <bool FP8, bool VERIFY>
-__global__ void __launch_bounds__(threads_of<FP8, VERIFY>(), 1)
+__global__ void __launch_bounds__(threads_of<FP8>(), 1)
     prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1384,8 +1173,6 @@ __global__ void __launch_bounds__(threads_of<FP8, VERIFY>(), 1)
   b.abort = reinterpret_cast<volatile int*>(bars + 21);
   b.peer_ready = bars + 22;
   b.dst_free = bars + 23;
-  b.xch = reinterpret_cast<uint64_t*>(smem + kOffXchBar);
-  constexpr bool kSplit = split_softmax<FP8, VERIFY>();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -1394,10 +1181,8 @@ __global__ void __launch_bounds__(threads_of<FP8, VERIFY>(), 1)
     mbar_init(bars + 1, VERIFY ? 4 : 8);           // q_ready: the (slot A) softmax warps
     for (int i = 0; i < 2; ++i) {
       mbar_init(&b.s_full[i], 1);
-      mbar_init(&b.p_ready[i], kSplit ? 8 : 4);    // the head's softmax warps
+      mbar_init(&b.p_ready[i], 4);
     }
-    if (kSplit)
-      for (int i = 0; i < 8; ++i) mbar_init(&b.xch[i], 2);   // the two halves
     for (int i = 0; i < (kRing3 ? 3 : 2); ++i) {
       mbar_init(&b.v_full[i], stage_arrivals);
       mbar_init(&b.v_empty[i], 1);
@@ -1423,7 +1208,7 @@ __global__ void __launch_bounds__(threads_of<FP8, VERIFY>(), 1)
     }
     mbar_init(b.o_final, 1);
     mbar_init(b.drain, 1);
-    mbar_init(b.peer_ready, kSplit ? 512 : 256);   // every softmax thread of CTA 1
+    mbar_init(b.peer_ready, 256);                  // every softmax thread of CTA 1
     mbar_init(b.dst_free, 1);
     *b.abort = 0;
     fence_mbar_init();
@@ -1451,21 +1236,17 @@ __global__ void __launch_bounds__(threads_of<FP8, VERIFY>(), 1)
   const TileGeom gm = geom_of<VERIFY>(p, ru, x, rank);
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8, VERIFY>::kLow));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kLow));
     if (warp == 0) {
       if (lane == 0) producer<FP8, VERIFY>(p, ru, x, gm, smem, b);
     } else if (warp == 1) {
       mma_issuer<FP8, VERIFY>(p, ru, gm, smem, tmem, b);
     }
-  } else if (kSplit) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<FP8, VERIFY>::kHigh));
-    // warps 4-11: half 0, 12-19: half 1; head (warp - 4) / 4 mod 2
-    softmax_split_role(p, ru, x, gm, rank, ((warp - 4) >> 2) & 1, (warp - 4) >> 3, smem, tmem, b);
   } else if (warp < kConvWarp0) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<FP8, VERIFY>::kHigh));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kHigh));
     softmax_role<FP8, VERIFY>(p, ru, x, gm, rank, (warp - 4) >> 2, smem, tmem, b);
   } else if (FP8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8, VERIFY>::kConv));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<FP8>::kConv));
     converter<VERIFY>(p, ru, gm, smem, b);
   }
   umma::fence_before_sync();
@@ -1486,18 +1267,17 @@ cudaError_t launch(const PrefillParams& p, int tiles, cudaStream_t s) {
     cudaFuncAttributes attr;
     cudaError_t r = cudaFuncGetAttributes(&attr, prefill_kernel<FP8, VERIFY>);
     if (r != cudaSuccess) return r;
-    if (attr.numRegs * threads_of<FP8, VERIFY>() < regs_split<FP8, VERIFY>())
-      return cudaErrorInvalidValue;
+    if (attr.numRegs * threads_of<FP8>() < regs_split<FP8>()) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(prefill_kernel<FP8, VERIFY>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Layout<FP8>::kSmemBytes);
   });
   if (e != cudaSuccess) return e;
   if (VERIFY)
-    return launch_pdl(prefill_kernel<FP8, VERIFY>, dim3(tiles), dim3(threads_of<FP8, VERIFY>()),
+    return launch_pdl(prefill_kernel<FP8, VERIFY>, dim3(tiles), dim3(threads_of<FP8>()),
                       Layout<FP8>::kSmemBytes, s, p);
   return launch_pdl_cluster(prefill_kernel<FP8, VERIFY>, dim3(2 * tiles),
-                            dim3(threads_of<FP8, VERIFY>()), Layout<FP8>::kSmemBytes, s, p, 2);
+                            dim3(threads_of<FP8>()), Layout<FP8>::kSmemBytes, s, p, 2);
 }
 
 }  // namespace
