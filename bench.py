@@ -13,11 +13,13 @@ Inputs are 268 MB of KV per step, above the 129 MB L2, so no flush is needed
 between decode steps; the prompt-chunk timing flushes L2 between launches.
 
 e2e is a decode loop through the public API with host buffers, one step at a
-time and every stream one position longer each step: a pinned input copy,
-the step's planned launches (tfpa_plan_launch; the next step is planned with
-tfpa_plan_write_kv / tfpa_plan_decode while this one runs), an output copy,
-and a host wait.  The same loop with direct tfpa_write_kv / tfpa_decode calls
-is reported beside it, with the host time of each call.
+time and every stream one position longer each step: every step is planned
+anew (tfpa_plan_write_kv / tfpa_plan_decode, plan in device mode) while the
+previous one runs, its lengths packed for the device (tfpa_plan_dyn_pack),
+then one CUDA-graph replay runs a pinned input copy, the packed-data copy,
+the planned launches and an output copy, and the host waits.  The same loop
+with the plan in parameter mode (tfpa_plan_launch each step) and with direct
+tfpa_write_kv / tfpa_decode calls is reported beside it, with host times.
 
 Launch: ``python bench.py [--gpus N --steps K --warmup W] [--impl reference]``;
 for N > 1 under torchrun every rank runs its own replica (no collective on the
@@ -400,6 +402,89 @@ def time_e2e_planned(w, torch, B, ctx, steps, warmup):
         tab.set_seq_len(j, st.seq_len)
     qo = w.rows * w.hq * 128 * 2 * 2
     return dt, kvb / steps + qo, statistics.median(t_launch[warmup:]), statistics.median(t_plan)
+
+
+def time_e2e_device(w, torch, B, ctx, steps, warmup):
+    """The decode loop of time_e2e_planned with the plan in device mode
+    (tfpa_plan_set_device): each step is still planned anew with lengths one
+    position longer, but its launches read their lengths, splits and CTA
+    ranges from a device buffer, so one captured CUDA graph per packed-data
+    buffer (input copy, copy of the packed data, the planned launches, output
+    copy) is replayed every step.  Two pinned packed-data buffers alternate:
+    while the GPU runs step i the host plans step i + 1 and packs it into the
+    other buffer, then waits for step i's output and replays.
+    Returns (s per step, KV + Q + O bytes per step, host us per replay,
+    host us planning and packing a step, packed bytes copied per step)."""
+    cache, segs, _, sc, out = ctx
+    nst = len(w.streams)
+    tab = B.SegTable(segs)
+    h_in, d_in, dq, dk, dv, hout = e2e_buffers(w, torch, nst)
+    sidx = np.arange(nst, dtype=np.int32)
+    s = torch.cuda.current_stream()
+    L = w.streams[0].seq_len
+    total = warmup + steps
+    dyn = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    hdyn = [torch.zeros(1 << 16, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    plan = B.Plan()
+    plan.set_device(dyn)
+    ev = torch.cuda.Event()
+    b = 2 if w.kv_dtype == "bf16" else 1
+    t_launch, t_plan = [], []
+    kvb = 0
+
+    def plan_step(i):
+        n = L - total + 1 + i
+        for j in range(nst):
+            tab.set_seq_len(j, n)
+        rp = np.full(nst, n - 1, np.int32)
+        plan.clear()
+        plan.write_kv(cache, tab, dk, dv, sidx, rp)
+        plan.decode(cache, tab, dq, sidx, rp, w.softmax_scale, sc, out)
+        plan.pack(hdyn[i % 2])
+        return n
+
+    n = plan_step(0)
+    nb, shape = plan.dyn_bytes(), plan.shape()
+    dyn[:nb].copy_(hdyn[0][:nb], non_blocking=True)
+    plan.launch()                                  # sets the kernels up before capture
+    torch.cuda.synchronize()
+    graphs = []
+    cap = torch.cuda.Stream()
+    for k in range(2):
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(s)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                d_in.copy_(h_in, non_blocking=True)
+                dyn[:nb].copy_(hdyn[k][:nb], non_blocking=True)
+                plan.launch(cap)
+                hout.copy_(out, non_blocking=True)
+        s.wait_stream(cap)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    t0 = None
+    for i in range(total):
+        if i == warmup:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        a = time.perf_counter_ns()
+        graphs[i % 2].replay()
+        t_launch.append((time.perf_counter_ns() - a) / 1e3)
+        ev.record(s)
+        if i >= warmup:
+            kvb += n * nst * w.hkv * 128 * 2 * b
+        if i + 1 < total:
+            a = time.perf_counter_ns()
+            n = plan_step(i + 1)                 # while the GPU runs step i
+            t_plan.append((time.perf_counter_ns() - a) / 1e3)
+            assert plan.shape() == shape and plan.dyn_bytes() == nb
+        ev.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    for j, st in enumerate(w.streams):
+        tab.set_seq_len(j, st.seq_len)
+    qo = w.rows * w.hq * 128 * 2 * 2
+    return (dt, kvb / steps + qo, statistics.median(t_launch[warmup:]), statistics.median(t_plan),
+            nb)
 
 
 def time_e2e_calls(w, torch, B, ctx, steps, warmup, in_flight=1):
@@ -819,6 +904,9 @@ def main():
         e2e_plan = (max_over_ranks(dist, torch, e2e_plan[0]),) + tuple(e2e_plan[1:])
         e2e_plan_aa = time_e2e_planned(w, torch, B, ctx, n_e2e, args.warmup)
         e2e_graph_s = time_e2e_graph(w, torch, B, ctx, n_e2e, args.warmup)
+        e2e_dev = time_e2e_device(w, torch, B, ctx, n_e2e, args.warmup)
+        e2e_dev = (max_over_ranks(dist, torch, e2e_dev[0]),) + tuple(e2e_dev[1:])
+        e2e_dev_aa = time_e2e_device(w, torch, B, ctx, n_e2e, args.warmup)
         del ctx
         s3, p3, ctx3, _ = time_decode(w3, torch, B, max(10, args.steps // 4), args.warmup, None)
         del ctx3
@@ -938,28 +1026,39 @@ def main():
                      "kernel": "decode_partial_kernel<bf16>", "peak_source": pk["source"],
                      "partial_ms": partial_ms},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * e2e_plan[1] / e2e_plan[0] / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": e2e[4], "d2h_bytes_per_step": e2e[5],
-                "ms_per_step": e2e_plan[0] * 1e3, "vs_device_step": e2e_plan[0] * 1e3 / step_ms,
-                "host_us_per_call": {"tfpa_plan_launch": e2e_plan[2],
-                                     "planning_a_step_overlapped": e2e_plan[3]},
+        "e2e": {"value": world * e2e_dev[1] / e2e_dev[0] / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": e2e[4] + e2e_dev[4], "d2h_bytes_per_step": e2e[5],
+                "ms_per_step": e2e_dev[0] * 1e3, "vs_device_step": e2e_dev[0] * 1e3 / step_ms,
+                "host_us_per_call": {"graph_replay": e2e_dev[2],
+                                     "planning_and_packing_a_step_overlapped": e2e_dev[3]},
                 "steps": n_e2e,
                 "how": "a decode loop through the public API with host buffers, one step at a "
-                       "time: each stream one position longer every step (%d..%d); per step one "
-                       "pinned input copy (q + new K/V rows), tfpa_plan_launch of the step's "
-                       "tfpa_write_kv + tfpa_decode launches (planned with tfpa_plan_write_kv "
-                       "+ tfpa_plan_decode while the previous step ran), one output copy, and "
-                       "the host waits for the output before the next step; host times are "
-                       "host clock, median" % (w.streams[0].seq_len - n_e2e + 1,
-                                               w.streams[0].seq_len),
+                       "time: each stream one position longer every step (%d..%d), every step "
+                       "planned anew (tfpa_plan_write_kv + tfpa_plan_decode, plan in device "
+                       "mode) and packed (tfpa_plan_dyn_pack) while the previous step runs; per "
+                       "step one replay of a CUDA graph captured once per packed-data buffer: "
+                       "pinned input copy (q + new K/V rows), copy of the packed lengths/splits/"
+                       "CTA ranges, the planned launches (tfpa_plan_launch), output copy; the "
+                       "host waits for the output before the next step; host times are host "
+                       "clock, median" % (w.streams[0].seq_len - n_e2e + 1, w.streams[0].seq_len),
+                "packed_bytes_per_step": e2e_dev[4],
+                "planned_calls": {
+                    "value": world * e2e_plan[1] / e2e_plan[0] / 1e9, "unit": "GB/s",
+                    "ms_per_step": e2e_plan[0] * 1e3,
+                    "vs_device_step": e2e_plan[0] * 1e3 / step_ms,
+                    "host_us_per_call": {"tfpa_plan_launch": e2e_plan[2],
+                                         "planning_a_step_overlapped": e2e_plan[3]},
+                    "how": "the same loop with the plan in parameter mode: tfpa_plan_launch "
+                           "enqueues the planned launches each step (no graph)"},
                 "direct_calls": {
                     "value": world * e2e[1] / e2e_s / 1e9, "unit": "GB/s",
                     "ms_per_step": e2e_s * 1e3, "vs_device_step": e2e_s * 1e3 / step_ms,
                     "host_us_per_call": {"tfpa_write_kv": e2e[2], "tfpa_decode": e2e[3]},
                     "how": "the same loop calling tfpa_write_kv and tfpa_decode directly "
                            "(planning and launching inside each call)"}},
-        "e2e_aa_repeat": {"ms_per_step": [e2e_plan[0] * 1e3, e2e_plan_aa[0] * 1e3],
-                          "spread_pct": 100 * abs(e2e_plan_aa[0] - e2e_plan[0]) / e2e_plan[0]},
+        "e2e_aa_repeat": {"ms_per_step": [e2e_dev[0] * 1e3, e2e_dev_aa[0] * 1e3],
+                          "spread_pct": 100 * abs(e2e_dev_aa[0] - e2e_dev[0]) / e2e_dev[0],
+                          "planned_calls_ms_per_step": [e2e_plan[0] * 1e3, e2e_plan_aa[0] * 1e3]},
         "e2e_two_in_flight": {
             "value": world * e2e_pipe[1] / e2e_pipe[0] / 1e9, "unit": "GB/s",
             "ms_per_step": e2e_pipe[0] * 1e3,

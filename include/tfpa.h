@@ -320,6 +320,43 @@ int tfpa_plan_decode(tfpa_plan* plan, const tfpa_cache* cache, const tfpa_seg* s
                      const tfpa_scratch* scratch, void* out, float* lse);
 int tfpa_plan_launch(const tfpa_plan* plan, cudaStream_t stream);
 
+/* Device mode: replaying a captured plan as the streams grow.
+ * A plan's launches normally carry everything by value, so a CUDA graph
+ * captured from tfpa_plan_launch repeats the lengths it was captured with.
+ * In device mode each write, decode and merge launch instead reads the data
+ * that changes as streams grow (run lengths and positions, split counts,
+ * work-item and per-CTA ranges) from its own slot of a DEVICE buffer that
+ * the caller owns, and the launch shapes stop depending on the lengths: a
+ * decode partial launch takes one CTA per SM (at most 256) whatever its
+ * work.  A decode loop then captures once [copy of the packed data into the
+ * buffer, tfpa_plan_launch] and, each step, re-plans with the new lengths,
+ * packs and replays.
+ *
+ * tfpa_plan_set_device(plan, dyn, bytes): dyn = DEVICE buffer, 16-byte
+ *   aligned, `bytes` long, or NULL to go back to parameter mode.  Only on an
+ *   empty plan (after create or clear), else TFPA_EINVAL.  The plan keeps the
+ *   pointer; tfpa_plan_clear keeps the mode.  A planning call whose slots do
+ *   not fit returns TFPA_ECAPACITY; rows that would take the tensor-core
+ *   verify path (a stream with 4 or more 16-vector m-tiles, whose grid
+ *   follows the lengths) return TFPA_EINVAL.
+ * tfpa_plan_dyn_bytes: bytes of the buffer the planned launches use (about
+ *   4 KB per decode launch, 2.6 KB per write, 2 KB per merge).
+ * tfpa_plan_dyn_pack(plan, host, bytes): writes those bytes, the data of
+ *   the launches as planned now, to HOST memory `host` (the caller copies
+ *   them to `dyn` before the launches run, e.g. with a copy captured in the
+ *   same graph from pinned memory; the host buffer must not change while
+ *   such a copy is pending).  TFPA_EINVAL outside device mode,
+ *   TFPA_ECAPACITY if bytes < tfpa_plan_dyn_bytes.
+ * tfpa_plan_shape: a 64-bit hash of everything the launches take by value
+ *   except that data (kinds, grids, pointers, tensor maps, head counts).
+ *   Two plans with the same shape may replay one captured graph; a
+ *   different shape (new rows, a stream moved between pool and slab, a
+ *   slice boundary moved) needs a new capture. */
+int tfpa_plan_set_device(tfpa_plan* plan, void* dyn, size_t bytes);
+size_t tfpa_plan_dyn_bytes(const tfpa_plan* plan);
+int tfpa_plan_dyn_pack(const tfpa_plan* plan, void* host, size_t bytes);
+uint64_t tfpa_plan_shape(const tfpa_plan* plan);
+
 /* Causal prompt-chunk attention over the paged prefix, one pass with online
  * softmax on tcgen05/TMEM tiles (PR #2011, "hpattn_p256_kernel": page size a
  * constant 256, one page lookup per key tile).  max_rows_per_launch > 0 runs

@@ -32,7 +32,8 @@ EXPORTS = ("tfpa_pages_per_split", "tfpa_num_splits", "tfpa_write_kv", "tfpa_dec
            "tfpa_pool_free", "tfpa_pool_fits", "tfpa_pool_claim", "tfpa_pool_release",
            "tfpa_stage_pages", "tfpa_save_kv", "tfpa_restore_kv", "tfpa_plan_create",
            "tfpa_plan_destroy", "tfpa_plan_clear", "tfpa_plan_launches", "tfpa_plan_write_kv",
-           "tfpa_plan_decode", "tfpa_plan_launch")
+           "tfpa_plan_decode", "tfpa_plan_launch", "tfpa_plan_set_device", "tfpa_plan_dyn_bytes",
+           "tfpa_plan_dyn_pack", "tfpa_plan_shape")
 
 
 class TfpaError(RuntimeError):
@@ -143,6 +144,14 @@ def lib():
         L.tfpa_plan_decode.restype = ctypes.c_int
         L.tfpa_plan_launch.argtypes = [vp, vp]
         L.tfpa_plan_launch.restype = ctypes.c_int
+        L.tfpa_plan_set_device.argtypes = [vp, vp, ctypes.c_size_t]
+        L.tfpa_plan_set_device.restype = ctypes.c_int
+        L.tfpa_plan_dyn_bytes.argtypes = [vp]
+        L.tfpa_plan_dyn_bytes.restype = ctypes.c_size_t
+        L.tfpa_plan_dyn_pack.argtypes = [vp, vp, ctypes.c_size_t]
+        L.tfpa_plan_dyn_pack.restype = ctypes.c_int
+        L.tfpa_plan_shape.argtypes = [vp]
+        L.tfpa_plan_shape.restype = ctypes.c_uint64
         L.tfpa_set_launch_hook.argtypes = [HOOK, vp, ctypes.c_int]
         L.tfpa_set_launch_hook.restype = None
         L.tfpa_strerror.argtypes = [ctypes.c_int]
@@ -495,6 +504,27 @@ class Plan:
 
     def launch(self, stream=None) -> None:
         _check(lib().tfpa_plan_launch(self._p, _stream(stream)), "tfpa_plan_launch")
+
+    def set_device(self, dyn) -> None:
+        """Device mode (tfpa_plan_set_device): ``dyn`` is a device tensor
+        (kept alive by the plan) whose bytes hold the launches' dynamic
+        data, or None for parameter mode."""
+        nbytes = 0 if dyn is None else dyn.numel() * dyn.element_size()
+        _check(lib().tfpa_plan_set_device(self._p, _ptr(dyn), nbytes), "tfpa_plan_set_device")
+        self._dyn = dyn
+
+    def dyn_bytes(self) -> int:
+        return int(lib().tfpa_plan_dyn_bytes(self._p))
+
+    def pack(self, host) -> None:
+        """Writes the planned launches' dynamic data into the host tensor
+        ``host`` (tfpa_plan_dyn_pack), for a copy to the device buffer."""
+        _check(lib().tfpa_plan_dyn_pack(self._p, ctypes.c_void_p(host.data_ptr()),
+                                        host.numel() * host.element_size()),
+               "tfpa_plan_dyn_pack")
+
+    def shape(self) -> int:
+        return int(lib().tfpa_plan_shape(self._p))
 
     def __del__(self):
         if getattr(self, "_p", None):

@@ -79,10 +79,10 @@ __device__ __forceinline__ int mtiles_of(const RunInfo& ru, int group) {
   return (ru.nrows * group + 15) >> 4;
 }
 
-__device__ __forceinline__ Item item_of(const DecodeParams& p, int it) {
+__device__ __forceinline__ Item item_of(const DecodeParams& p, const DecodeDyn& D, int it) {
   int r = 0;
-  while (r + 1 < p.nruns && p.runs[r + 1].item0 <= it) ++r;
-  const RunInfo& ru = p.runs[r];
+  while (r + 1 < D.nruns && D.runs[r + 1].item0 <= it) ++r;
+  const RunInfo& ru = D.runs[r];
   int local = it - ru.item0;
   const int mgroups = mtiles_of(ru, p.group);
   Item x;
@@ -97,16 +97,16 @@ __device__ __forceinline__ Item item_of(const DecodeParams& p, int it) {
 // Items [begin, end) of this CTA: a contiguous share balanced by work on the
 // host, so consecutive items are mostly consecutive splits of one (stream,
 // kv head, m-tile).
-__device__ __forceinline__ void cta_items(const DecodeParams& p, int& begin, int& end) {
-  begin = p.cta_item0[blockIdx.x];
-  end = p.cta_item0[blockIdx.x + 1];
+__device__ __forceinline__ void cta_items(const DecodeDyn& D, int& begin, int& end) {
+  begin = D.cta_item0[blockIdx.x];
+  end = D.cta_item0[blockIdx.x + 1];
 }
 
 // Key range [klo, khi) an item must read: its split's pages, cut at the
 // stream length and at the last position among the item's rows.
-__device__ __forceinline__ void item_keys(const DecodeParams& p, const Item& x, int& klo,
-                                          int& khi) {
-  const RunInfo& ru = p.runs[x.run];
+__device__ __forceinline__ void item_keys(const DecodeParams& p, const DecodeDyn& D, const Item& x,
+                                          int& klo, int& khi) {
+  const RunInfo& ru = D.runs[x.run];
   const int nq = ru.nrows * p.group;
   const int last_qv = min(16 * x.mt + 15, nq - 1);
   const int maxpos = ru.pos0 + last_qv / p.group;
@@ -115,18 +115,18 @@ __device__ __forceinline__ void item_keys(const DecodeParams& p, const Item& x, 
 }
 
 template <bool FP8>
-__device__ void producer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* full,
-                         uint64_t* empty, int* stage_bad) {
+__device__ void producer(const DecodeParams& p, const DecodeDyn& D, uint8_t* stage_mem,
+                         uint64_t* full, uint64_t* empty, int* stage_bad) {
   using C = Cfg<FP8>;
   if ((threadIdx.x & 31) != 0) return;
   int ib, ie;
-  cta_items(p, ib, ie);
+  cta_items(D, ib, ie);
   uint32_t stage = 0;
   for (int it = ib; it < ie; ++it) {
-    const Item x = item_of(p, it);
-    const RunInfo& ru = p.runs[x.run];
+    const Item x = item_of(p, D, it);
+    const RunInfo& ru = D.runs[x.run];
     int klo, khi;
-    item_keys(p, x, klo, khi);
+    item_keys(p, D, x, klo, khi);
     const CUtensorMap* mk = &p.maps[ru.src].k;
     const CUtensorMap* mv = &p.maps[ru.src].v;
     int cached_page = -1, cached_pid = 0;
@@ -426,8 +426,9 @@ __device__ __forceinline__ void attend_block(uint32_t sb, int wk0, int k0, int s
 }
 
 template <bool FP8, bool GEN>
-__device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* full,
-                         uint64_t* empty, const int* stage_bad, uint32_t tmem, CombBars bars) {
+__device__ void consumer(const DecodeParams& p, const DecodeDyn& D, uint8_t* stage_mem,
+                         uint64_t* full, uint64_t* empty, const int* stage_bad, uint32_t tmem,
+                         CombBars bars) {
   using C = Cfg<FP8>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -435,7 +436,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
   const uint32_t sbase = smem_u32(stage_mem);
   uint32_t stage = 0;
   int ib, ie;
-  cta_items(p, ib, ie);
+  cta_items(D, ib, ie);
   int q_run = -1, q_g = -1, q_mt = -1;     // the m-tile whose query is loaded
   int lim[2] = {-1, -1};
   uint64_t anc[2] = {~0ull, ~0ull};
@@ -445,10 +446,10 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
   int tree_low = INT_MAX;     // keys from here on may be hidden by an ancestor mask
 
   for (int it = ib; it < ie; ++it) {
-    const Item x = item_of(p, it);
-    const RunInfo& ru = p.runs[x.run];
+    const Item x = item_of(p, D, it);
+    const RunInfo& ru = D.runs[x.run];
     int klo, khi;
-    item_keys(p, x, klo, khi);
+    item_keys(p, D, x, klo, khi);
     // The chunk's 8 sub-blocks of kKeysPerWarp keys go to the 8 warps.
     const int sub0 = warp;
     if (x.run != q_run || x.g != q_g || x.mt != q_mt) {
@@ -528,18 +529,18 @@ __device__ void consumer(const DecodeParams& p, uint8_t* stage_mem, uint64_t* fu
 // a combiner waits for done of the previous item before publishing, so the
 // fold and (m, l) buffers are never overwritten while still being read.
 template <bool FP8, bool GEN>
-__device__ void combiner(const DecodeParams& p, uint32_t tmem, float4* fold, float* ml_buf,
-                         CombBars bars) {
+__device__ void combiner(const DecodeParams& p, const DecodeDyn& D, uint32_t tmem, float4* fold,
+                         float* ml_buf, CombBars bars) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int q = warp - kCombineWarp0;
   const int gq = lane >> 2, c = lane & 3;
   int ib, ie;
-  cta_items(p, ib, ie);
+  cta_items(D, ib, ie);
   const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
   for (int it = ib; it < ie; ++it) {
-    const Item x = item_of(p, it);
-    const RunInfo& ru = p.runs[x.run];
+    const Item x = item_of(p, D, it);
+    const RunInfo& ru = D.runs[x.run];
     const int nq = ru.nrows * p.group;
     const int rel = it - ib;
     const int b = rel & 1;
@@ -657,9 +658,11 @@ __device__ void combiner(const DecodeParams& p, uint32_t tmem, float4* fold, flo
   }
 }
 
-template <bool FP8, bool GEN>
+// DEV: the runs and CTA ranges are read from p.dyn (a plan in device mode).
+template <bool FP8, bool GEN, bool DEV>
 __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
     const __grid_constant__ DecodeParams p) {
+  const DecodeDyn& D = DEV ? *p.dyn : p.d;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -705,13 +708,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
   wait_prior_grid();
   if (warp < kCombineWarp0) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsConsumer));
-    consumer<FP8, GEN>(p, stage_mem, full, empty, stage_bad, tmem, cb);
+    consumer<FP8, GEN>(p, D, stage_mem, full, empty, stage_bad, tmem, cb);
   } else if (warp < kProducerWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCombine));
-    combiner<FP8, GEN>(p, tmem, fold, ml_buf, cb);
+    combiner<FP8, GEN>(p, D, tmem, fold, ml_buf, cb);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
-    if (warp == kProducerWarp) producer<FP8>(p, stage_mem, full, empty, stage_bad);
+    if (warp == kProducerWarp) producer<FP8>(p, D, stage_mem, full, empty, stage_bad);
   }
   umma::fence_before_sync();
   __syncthreads();
@@ -724,17 +727,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
 // ---------------------------------------------------------------- merge
 // One warp per (row, head): lane s holds split s's (m, l); lanes own 4
 // consecutive head-dim elements of the output.  Fixed summation order.
+// DEV: the runs are read from p.dyn (a plan in device mode).
+template <bool DEV>
 __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ MergeParams p) {
   allow_next_grid();
   wait_prior_grid();
+  const MergeDyn& D = DEV ? *p.dyn : p.d;
   const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (wid >= p.rows * p.hq) return;
+  if (wid >= D.rows * p.hq) return;
   const int row = wid / p.hq;
   const int h = wid - row * p.hq;
   int ri = 0;
-  while (ri + 1 < p.nruns && p.runs[ri + 1].row0 <= row) ++ri;
-  const int nsplit = p.runs[ri].nsplit;
+  while (ri + 1 < D.nruns && D.runs[ri + 1].row0 <= row) ++ri;
+  const int nsplit = D.runs[ri].nsplit;
   const size_t slot0 = ((size_t)row * p.hq + h) * p.max_splits;
   // Every slot below nsplit was written by the partial kernel (an empty split
   // holds o = 0 with weight 0).  Every split's o chunk is loaded together
@@ -778,42 +784,53 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
   if (p.lse && lane == 0) p.lse[(size_t)row * p.hq + h] = (M + log2f(L)) * 0.6931471805599453f;
 }
 
-template <bool FP8, bool GEN>
+template <bool FP8, bool GEN, bool DEV>
 cudaError_t launch_partial(const DecodeParams& p, int grid, cudaStream_t s) {
   static PerDeviceOnce configured;
   cudaError_t e = configured.run([] {
     // The register split only works if the block launches with at least the
     // registers it hands out; otherwise setmaxnreg.inc would wait forever.
     cudaFuncAttributes attr;
-    cudaError_t r = cudaFuncGetAttributes(&attr, decode_partial_kernel<FP8, GEN>);
+    cudaError_t r = cudaFuncGetAttributes(&attr, decode_partial_kernel<FP8, GEN, DEV>);
     if (r != cudaSuccess) return r;
     if (attr.numRegs * kThreads < 128 * (2 * kRegsConsumer + kRegsCombine + kRegsProducer))
       return cudaErrorInvalidValue;
-    return cudaFuncSetAttribute(decode_partial_kernel<FP8, GEN>,
+    return cudaFuncSetAttribute(decode_partial_kernel<FP8, GEN, DEV>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (e != cudaSuccess) return e;
   e =
-      launch_pdl(decode_partial_kernel<FP8, GEN>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
+      launch_pdl(decode_partial_kernel<FP8, GEN, DEV>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-}  // namespace
-
-cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cudaStream_t s) {
-  if (grid <= 0 || p.n_items == 0) return cudaSuccess;
+template <bool DEV>
+cudaError_t launch_partial_dev(const DecodeParams& p, bool fp8, int grid, cudaStream_t s) {
   // Rows with ancestor masks take the general instantiation, so the plain
   // causal calls keep their own kernel's code.
   if (p.anc)
-    return fp8 ? launch_partial<true, true>(p, grid, s) : launch_partial<false, true>(p, grid, s);
-  return fp8 ? launch_partial<true, false>(p, grid, s) : launch_partial<false, false>(p, grid, s);
+    return fp8 ? launch_partial<true, true, DEV>(p, grid, s)
+               : launch_partial<false, true, DEV>(p, grid, s);
+  return fp8 ? launch_partial<true, false, DEV>(p, grid, s)
+             : launch_partial<false, false, DEV>(p, grid, s);
+}
+
+}  // namespace
+
+// The launch shape comes from the parameters' own copy of the dynamic data
+// (p.d), which a device-mode plan keeps fixed from step to step.
+cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cudaStream_t s) {
+  if (grid <= 0 || p.d.n_items == 0) return cudaSuccess;
+  return p.dyn ? launch_partial_dev<true>(p, fp8, grid, s)
+               : launch_partial_dev<false>(p, fp8, grid, s);
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
-  const int warps = p.rows * p.hq;
+  const int warps = p.d.rows * p.hq;
   if (warps == 0) return cudaSuccess;
-  return launch_pdl(merge_kernel, dim3((warps + 7) / 8), dim3(256), 0, s, p);
+  return p.dyn ? launch_pdl(merge_kernel<true>, dim3((warps + 7) / 8), dim3(256), 0, s, p)
+               : launch_pdl(merge_kernel<false>, dim3((warps + 7) / 8), dim3(256), 0, s, p);
 }
 
 }  // namespace tfpa

@@ -244,6 +244,10 @@ int to_err(cudaError_t e) { return e == cudaSuccess ? TFPA_OK : TFPA_ECUDA; }
 }  // namespace
 
 // A call's launches, planned and kept by value for a later tfpa_plan_launch.
+// In device mode (dyn_base set) each decode, merge and write launch owns a
+// 16-byte aligned slot of the caller's device buffer at dyn_base, from which
+// it reads its dynamic data; the plan keeps the host image in the launch's
+// parameters (`d`) for tfpa_plan_dyn_pack.
 struct tfpa_plan {
   enum Kind : int { kDecode, kVerify, kMerge, kWrite };
   struct Entry {
@@ -257,6 +261,9 @@ struct tfpa_plan {
   std::vector<PrefillParams> verify;
   std::vector<MergeParams> merge;
   std::vector<WriteParams> write;
+  uint8_t* dyn_base = nullptr;   // DEVICE, or nullptr: parameter mode
+  size_t dyn_cap = 0;
+  size_t dyn_used = 0;           // bytes of dyn_base handed out
 };
 
 namespace {
@@ -267,12 +274,14 @@ struct Sink {
   cudaStream_t stream = nullptr;
   tfpa_plan* plan = nullptr;
   struct Mark {
-    size_t e, d, v, m, w;
+    size_t e, d, v, m, w, dyn;
   };
+  // Device mode: launch shapes must not depend on the streams' lengths.
+  bool device() const { return plan && plan->dyn_base; }
   Mark mark() const {
     return plan ? Mark{plan->entries.size(), plan->decode.size(), plan->verify.size(),
-                       plan->merge.size(), plan->write.size()}
-                : Mark{0, 0, 0, 0, 0};
+                       plan->merge.size(), plan->write.size(), plan->dyn_used}
+                : Mark{0, 0, 0, 0, 0, 0};
   }
   void rollback(const Mark& k) const {
     if (!plan) return;
@@ -281,6 +290,7 @@ struct Sink {
     plan->verify.resize(k.v);
     plan->merge.resize(k.m);
     plan->write.resize(k.w);
+    plan->dyn_used = k.dyn;
   }
   template <typename P>
   int keep(tfpa_plan::Kind kind, std::vector<P>& v, const P& p, bool fp8, int grid) const {
@@ -288,20 +298,38 @@ struct Sink {
     plan->entries.push_back(tfpa_plan::Entry{kind, fp8, grid, v.size() - 1});
     return TFPA_OK;
   }
+  // keep() for a launch with dynamic data: in device mode the launch takes
+  // the next slot of the plan's device buffer.
+  template <typename P>
+  int keep_dyn(tfpa_plan::Kind kind, std::vector<P>& v, const P& p, bool fp8, int grid) const {
+    const size_t off = plan->dyn_used;
+    if (plan->dyn_base) {
+      const size_t end = (off + sizeof(p.d) + 15) & ~size_t(15);
+      if (end > plan->dyn_cap) return TFPA_ECAPACITY;
+      plan->dyn_used = end;
+    }
+    keep(kind, v, p, fp8, grid);
+    v.back().dyn = plan->dyn_base
+                       ? reinterpret_cast<decltype(p.dyn)>(plan->dyn_base + off)
+                       : nullptr;
+    return TFPA_OK;
+  }
   int decode(const DecodeParams& p, bool fp8, int grid) const {
-    if (plan) return keep(tfpa_plan::kDecode, plan->decode, p, fp8, grid);
+    if (plan) return keep_dyn(tfpa_plan::kDecode, plan->decode, p, fp8, grid);
     return dry_run() ? TFPA_OK : to_err(launch_decode_partial(p, fp8, grid, stream));
   }
   int verify(const PrefillParams& p, bool fp8, int tiles) const {
+    // the tensor-core verify launch's grid follows the streams' lengths
+    if (device()) return TFPA_EINVAL;
     if (plan) return keep(tfpa_plan::kVerify, plan->verify, p, fp8, tiles);
     return dry_run() ? TFPA_OK : to_err(launch_verify(p, fp8, tiles, stream));
   }
   int merge(const MergeParams& p) const {
-    if (plan) return keep(tfpa_plan::kMerge, plan->merge, p, false, 0);
+    if (plan) return keep_dyn(tfpa_plan::kMerge, plan->merge, p, false, 0);
     return dry_run() ? TFPA_OK : to_err(launch_merge(p, stream));
   }
   int write(const WriteParams& p) const {
-    if (plan) return keep(tfpa_plan::kWrite, plan->write, p, false, 0);
+    if (plan) return keep_dyn(tfpa_plan::kWrite, plan->write, p, false, 0);
     return dry_run() ? TFPA_OK : to_err(launch_write_kv(p, stream));
   }
 };
@@ -414,7 +442,7 @@ void plan_cta_ranges(DecodeParams& p, int nr, int G, bool fp8, int grid) {
   cum.clear();
   int64_t total = 0;
   for (int r = 0; r < nr; ++r) {
-    const RunInfo& ri = p.runs[r];
+    const RunInfo& ri = p.d.runs[r];
     const int mtiles = (ri.nrows * G + 15) / 16;
     blk[r] = (int32_t)cum.size();
     int64_t sum = 0;
@@ -429,7 +457,7 @@ void plan_cta_ranges(DecodeParams& p, int nr, int G, bool fp8, int grid) {
   blk[nr] = (int32_t)cum.size();
   int b = 1, item = 0;
   int64_t prefix = 0;   // weight of the items before the current block
-  p.cta_item0[0] = 0;
+  p.d.cta_item0[0] = 0;
   for (int r = 0; r < nr && b < grid; ++r) {
     const int64_t* c = cum.data() + blk[r];
     const int32_t n = blk[r + 1] - blk[r] - 1;   // items of one kv head's block
@@ -440,7 +468,7 @@ void plan_cta_ranges(DecodeParams& p, int nr, int G, bool fp8, int grid) {
         const int64_t need = (total * b + grid - 1) / grid - prefix;
         const int32_t i = (int32_t)(std::lower_bound(c, c + n, need) - c);
         if (i >= n) break;
-        p.cta_item0[b++] = item + i;
+        p.d.cta_item0[b++] = item + i;
       }
       prefix += c[n];
       item += n;
@@ -449,7 +477,7 @@ void plan_cta_ranges(DecodeParams& p, int nr, int G, bool fp8, int grid) {
   // CTAs past the last boundary get empty ranges at the end
   int n_items = 0;
   for (int r = 0; r < nr; ++r) n_items += (blk[r + 1] - blk[r] - 1) * p.hkv;
-  while (b <= grid) p.cta_item0[b++] = n_items;
+  while (b <= grid) p.d.cta_item0[b++] = n_items;
 }
 
 // Partial (and optionally merge) launches over the call's rows.  With
@@ -518,14 +546,14 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
         info.nsplit = verify_num_splits(g.seq_len);
         info.item0 = tiles;
         tiles += c->hkv * ((take + vrows - 1) / vrows) * info.nsplit;
-        mp.runs[nr] = MergeRun{nrows, take, info.nsplit, 0};
+        mp.d.runs[nr] = MergeRun{nrows, take, info.nsplit, 0};
       } else {
         if (nd == 0) std::memset(&p, 0, sizeof(p));
-        RunInfo& info = p.runs[nd++];
+        RunInfo& info = p.d.runs[nd++];
         fill_run(info, g, src, nrows, take, r.pos0 + taken);
         info.item0 = items;
         items += c->hkv * ((take * G + 15) / 16) * info.nsplit;
-        mp.runs[nr] = MergeRun{nrows, take, info.nsplit, 0};
+        mp.d.runs[nr] = MergeRun{nrows, take, info.nsplit, 0};
       }
       ++nr;
       nrows += take;
@@ -549,8 +577,8 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
       p.k_scale = c->k_scale;
       p.v_scale = c->v_scale;
       p.err_flag = c->err_flag;
-      p.nruns = nd;
-      p.n_items = items;
+      p.d.nruns = nd;
+      p.d.n_items = items;
       p.hq = c->hq;
       p.hkv = c->hkv;
       p.group = G;
@@ -558,7 +586,9 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
       p.num_pages = c->num_pages;
       p.rows = nrows;
       p.scale_log2 = scale * 1.4426950408889634f;
-      const int grid = std::min(std::min(items, nsm), kMaxDecodeGrid);
+      // In device mode the grid is one CTA per SM whatever the work, so
+      // that the launch can be replayed as the streams grow.
+      const int grid = std::min(sink.device() ? nsm : std::min(items, nsm), kMaxDecodeGrid);
       plan_cta_ranges(p, nd, G, fp8, grid);
       record(1, base, nrows, nd, items, grid, (int64_t)base * hd, 0);
       if ((e = sink.decode(p, fp8, grid))) return e;
@@ -592,8 +622,8 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
       mp.part_ml = part_ml;
       mp.out = static_cast<__nv_bfloat16*>(out) + (size_t)base * hd;
       mp.lse = lse ? lse + (size_t)base * c->hq : nullptr;
-      mp.nruns = nr;
-      mp.rows = nrows;
+      mp.d.nruns = nr;
+      mp.d.rows = nrows;
       mp.hq = c->hq;
       mp.max_splits = sc->max_splits;
       record(2, base, nrows, nr, nrows * c->hq, (nrows * c->hq + 7) / 8, 0, (int64_t)base * hd);
@@ -647,10 +677,10 @@ extern "C" int tfpa_merge(const tfpa_scratch* sc, int32_t hq, int32_t rows,
     std::memset(&mp, 0, sizeof(mp));
     const int32_t base = r;
     int nr = 0;
-    while (r < rows && nr < (int)(sizeof(mp.runs) / sizeof(mp.runs[0]))) {
+    while (r < rows && nr < (int)(sizeof(mp.d.runs) / sizeof(mp.d.runs[0]))) {
       int32_t n = 1;
       while (r + n < rows && nsplit[r + n] == nsplit[r]) ++n;
-      mp.runs[nr++] = MergeRun{r - base, n, nsplit[r], 0};
+      mp.d.runs[nr++] = MergeRun{r - base, n, nsplit[r], 0};
       r += n;
     }
     const size_t srow = (size_t)base * hq * sc->max_splits;
@@ -658,8 +688,8 @@ extern "C" int tfpa_merge(const tfpa_scratch* sc, int32_t hq, int32_t rows,
     mp.part_ml = sc->part_ml + srow * 2;
     mp.out = static_cast<__nv_bfloat16*>(out) + (size_t)base * hq * kHeadDim;
     mp.lse = lse ? lse + (size_t)base * hq : nullptr;
-    mp.nruns = nr;
-    mp.rows = r - base;
+    mp.d.nruns = nr;
+    mp.d.rows = r - base;
     mp.hq = hq;
     mp.max_splits = sc->max_splits;
     record(2, base, r - base, nr, (r - base) * hq, ((r - base) * hq + 7) / 8, 0,
@@ -709,7 +739,7 @@ int write_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const vo
     while (ri < runs.size() && nr < kMaxRuns) {
       const Run& r = runs[ri++];
       const tfpa_seg& g = segs[r.seg];
-      WriteRun& w = p.runs[nr++];
+      WriteRun& w = p.d.runs[nr++];
       w.page_table = g.page_table;
       w.k_dst = g.page_table ? c->k_pool : g.k_slab;
       w.v_dst = g.page_table ? c->v_pool : g.v_slab;
@@ -729,8 +759,8 @@ int write_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const vo
     p.rope_sin = rope.sin;
     p.rope_pos = rope.pos ? rope.pos + base : nullptr;   // shifts with the rows
     p.rope_n = rope.n;
-    p.nruns = nr;
-    p.rows = nrows;
+    p.d.nruns = nr;
+    p.d.rows = nrows;
     p.hkv = c->hkv;
     p.num_pages = c->num_pages;
     p.fp8 = c->dtype == TFPA_FP8_E4M3;
@@ -772,10 +802,72 @@ extern "C" void tfpa_plan_clear(tfpa_plan* plan) {
   plan->verify.clear();
   plan->merge.clear();
   plan->write.clear();
+  plan->dyn_used = 0;
 }
 
 extern "C" int32_t tfpa_plan_launches(const tfpa_plan* plan) {
   return plan ? (int32_t)plan->entries.size() : 0;
+}
+
+extern "C" int tfpa_plan_set_device(tfpa_plan* plan, void* dyn, size_t bytes) {
+  if (!plan || !plan->entries.empty()) return TFPA_EINVAL;
+  if (dyn && (!aligned(dyn, 16) || bytes < 16)) return TFPA_EINVAL;
+  plan->dyn_base = static_cast<uint8_t*>(dyn);
+  plan->dyn_cap = dyn ? bytes : 0;
+  plan->dyn_used = 0;
+  return TFPA_OK;
+}
+
+extern "C" size_t tfpa_plan_dyn_bytes(const tfpa_plan* plan) {
+  return plan ? plan->dyn_used : 0;
+}
+
+extern "C" int tfpa_plan_dyn_pack(const tfpa_plan* plan, void* host, size_t bytes) {
+  if (!plan || !plan->dyn_base) return TFPA_EINVAL;
+  if (plan->dyn_used == 0) return TFPA_OK;
+  if (!host) return TFPA_EINVAL;
+  if (bytes < plan->dyn_used) return TFPA_ECAPACITY;
+  uint8_t* dst = static_cast<uint8_t*>(host);
+  auto put = [&](const void* slot, const void* d, size_t n) {
+    std::memcpy(dst + (static_cast<const uint8_t*>(slot) - plan->dyn_base), d, n);
+  };
+  for (const DecodeParams& p : plan->decode) put(p.dyn, &p.d, sizeof(p.d));
+  for (const MergeParams& p : plan->merge) put(p.dyn, &p.d, sizeof(p.d));
+  for (const WriteParams& p : plan->write) put(p.dyn, &p.d, sizeof(p.d));
+  return TFPA_OK;
+}
+
+namespace {
+// FNV-1a over a byte range.
+uint64_t fnv1a(uint64_t h, const void* data, size_t n) {
+  const uint8_t* b = static_cast<const uint8_t*>(data);
+  for (size_t i = 0; i < n; ++i) h = (h ^ b[i]) * 1099511628211ull;
+  return h;
+}
+// A launch's parameters without its dynamic data.
+template <typename P>
+uint64_t hash_static(uint64_t h, const P& p) {
+  const uint8_t* b = reinterpret_cast<const uint8_t*>(&p);
+  const size_t d0 = reinterpret_cast<const uint8_t*>(&p.d) - b;
+  h = fnv1a(h, b, d0);
+  return fnv1a(h, b + d0 + sizeof(p.d), sizeof(P) - d0 - sizeof(p.d));
+}
+}  // namespace
+
+extern "C" uint64_t tfpa_plan_shape(const tfpa_plan* plan) {
+  if (!plan) return 0;
+  uint64_t h = 14695981039346656037ull;
+  for (const tfpa_plan::Entry& en : plan->entries) {
+    const int32_t head[3] = {(int32_t)en.kind, (int32_t)en.fp8, en.grid};
+    h = fnv1a(h, head, sizeof(head));
+    switch (en.kind) {
+      case tfpa_plan::kDecode: h = hash_static(h, plan->decode[en.index]); break;
+      case tfpa_plan::kVerify: h = fnv1a(h, &plan->verify[en.index], sizeof(PrefillParams)); break;
+      case tfpa_plan::kMerge: h = hash_static(h, plan->merge[en.index]); break;
+      case tfpa_plan::kWrite: h = hash_static(h, plan->write[en.index]); break;
+    }
+  }
+  return h;
 }
 
 namespace {

@@ -41,9 +41,24 @@ struct RunInfo {
   int32_t pad_;
 };
 
+// The parts of a launch that change as streams grow (lengths, positions,
+// split counts, item and CTA ranges).  A launch reads them from its own
+// parameters, or, for a plan in device mode, from a device copy (`dyn`),
+// which lets a captured launch be replayed step after step with new data.
+struct DecodeDyn {
+  RunInfo runs[kMaxRuns];
+  int32_t nruns;
+  int32_t n_items;
+  int32_t pad_[2];
+  // CTA b takes the work items [cta_item0[b], cta_item0[b + 1]), ranges the
+  // host balances by the items' key stages.
+  int32_t cta_item0[kMaxDecodeGrid + 1];
+};
+
 struct DecodeParams {
   KVMaps maps[kMaxSources];
-  RunInfo runs[kMaxRuns];
+  DecodeDyn d;
+  const DecodeDyn* dyn;       // device copy of d to read instead, or nullptr
   const __nv_bfloat16* q;     // rows of this launch: [rows][hq][128]
   const uint64_t* anc;        // rows of this launch: ancestor masks, or nullptr (causal)
   float* part_o;              // [cap_rows][hq][max_splits][128]
@@ -51,17 +66,12 @@ struct DecodeParams {
   const float* k_scale;       // fp8: [hkv]
   const float* v_scale;
   int32_t* err_flag;
-  int32_t nruns;
   int32_t nsrc;
-  int32_t n_items;
   int32_t hq, hkv, group;     // group = hq / hkv
   int32_t max_splits;
   int32_t num_pages;
   int32_t rows;
   float scale_log2;           // softmax_scale * log2(e)
-  // CTA b takes the work items [cta_item0[b], cta_item0[b + 1]), ranges the
-  // host balances by the items' key stages.
-  int32_t cta_item0[kMaxDecodeGrid + 1];
 };
 
 struct MergeRun {
@@ -71,14 +81,20 @@ struct MergeRun {
   int32_t pad_;
 };
 
-struct MergeParams {
+struct MergeDyn {
   MergeRun runs[kMaxRuns * 2];
+  int32_t nruns;
+  int32_t rows;
+  int32_t pad_[2];
+};
+
+struct MergeParams {
+  MergeDyn d;
+  const MergeDyn* dyn;        // device copy of d to read instead, or nullptr
   const float* part_o;
   const float* part_ml;
   __nv_bfloat16* out;         // rows of this launch: [rows][hq][128]
   float* lse;                 // [rows][hq] or nullptr
-  int32_t nruns;
-  int32_t rows;
   int32_t hq;
   int32_t max_splits;
 };
@@ -95,8 +111,16 @@ struct WriteRun {
   int32_t pad_;
 };
 
-struct WriteParams {
+struct WriteDyn {
   WriteRun runs[kMaxRuns];
+  int32_t nruns;
+  int32_t rows;
+  int32_t pad_[2];
+};
+
+struct WriteParams {
+  WriteDyn d;
+  const WriteDyn* dyn;        // device copy of d to read instead, or nullptr
   const __nv_bfloat16* k_rows;  // [rows][hkv][128], rows of this launch
   const __nv_bfloat16* v_rows;
   const float* k_scale;
@@ -108,8 +132,6 @@ struct WriteParams {
   const float* rope_sin;
   const int32_t* rope_pos;    // rows of this launch
   int32_t rope_n;
-  int32_t nruns;
-  int32_t rows;
   int32_t hkv;
   int32_t num_pages;
   int32_t fp8;

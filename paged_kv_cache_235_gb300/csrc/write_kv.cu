@@ -57,17 +57,20 @@ __device__ __forceinline__ uint4 pack8_bf16(const float (&x)[8]) {
 
 }  // namespace
 
+// DEV: the runs are read from p.dyn (a plan in device mode).
+template <bool DEV>
 __global__ void __launch_bounds__(256) write_kv_kernel(const __grid_constant__ WriteParams p) {
   allow_next_grid();
   wait_prior_grid();
+  const WriteDyn& D = DEV ? *p.dyn : p.d;
   const int gid = blockIdx.x * 16 + (threadIdx.x >> 4);  // (row, head) pair
   const int t = threadIdx.x & 15;                          // 8-element slice
-  if (gid >= p.rows * p.hkv) return;
+  if (gid >= D.rows * p.hkv) return;
   const int row = gid / p.hkv;
   const int g = gid - row * p.hkv;
   int ri = 0;
-  while (ri + 1 < p.nruns && p.runs[ri + 1].row0 <= row) ++ri;
-  const WriteRun& run = p.runs[ri];
+  while (ri + 1 < D.nruns && D.runs[ri + 1].row0 <= row) ++ri;
+  const WriteRun& run = D.runs[ri];
   const int pos = run.pos0 + (row - run.row0);
 
   size_t dst_row;  // element index of the destination row
@@ -198,10 +201,11 @@ __global__ void __launch_bounds__(kKeepThreads)
 }
 
 cudaError_t launch_write_kv(const WriteParams& p, cudaStream_t s) {
-  const int pairs = p.rows * p.hkv;
+  const int pairs = p.d.rows * p.hkv;
   const int grid = (pairs + 15) / 16;
   if (grid == 0) return cudaSuccess;
-  return launch_pdl(write_kv_kernel, dim3(grid), dim3(256), 0, s, p);
+  return p.dyn ? launch_pdl(write_kv_kernel<true>, dim3(grid), dim3(256), 0, s, p)
+               : launch_pdl(write_kv_kernel<false>, dim3(grid), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_keep(const KeepParams& p, cudaStream_t s) {

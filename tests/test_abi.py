@@ -316,3 +316,78 @@ def test_plans_hold_the_direct_calls_launches():
     assert len(plan) == len(direct)                 # the failed call appended nothing
     plan.clear()
     assert len(plan) == 0
+
+
+def test_device_mode_plans_keep_their_shape_as_lengths_grow():
+    """Device mode: the launches' lengths, splits and CTA ranges go to the
+    packed data, not to the launch shape, so plans of a growing decode loop
+    hash alike while their packed data differ; the decode grid is one CTA per
+    SM whatever the work; rows for the tensor-core verify path, a buffer too
+    small and a mode switch on a non-empty plan are refused."""
+    torch = pytest.importorskip("torch")
+    c = _cache()
+    sc = B.Scratch(5 * FAKE, 6 * FAKE, 16)
+    dyn = torch.zeros(1 << 16, dtype=torch.uint8)     # never dereferenced while planning
+
+    def plan_at(plan, n):
+        segs = [B.Seg(n, page_table=3 * FAKE), B.Seg(n, k_slab=8 * FAKE, v_slab=9 * FAKE,
+                                                     slab_cap=2048)]
+        rs, rp = np.array([0, 1]), np.array([n - 1, n - 1])
+        plan.clear()
+        with B.record_launches() as rec:
+            plan.write_kv(c, segs, 4 * FAKE, 5 * FAKE, rs, rp)
+            plan.decode(c, segs, 4 * FAKE, rs, rp, 0.088, sc, 7 * FAKE)
+        return rec
+
+    plan = B.Plan()
+    plan.set_device(dyn)
+    shapes, packs = [], []
+    for n in (1020, 1024, 1025, 1300):           # 1025 crosses a split boundary
+        rec = plan_at(plan, n)
+        assert [r["kind"] for r in rec] == ["write_kv", "partial", "merge"]
+        assert rec[1]["grid"] == 152             # one CTA per SM, not min(items, SMs)
+        shapes.append(plan.shape())
+        h = torch.zeros(plan.dyn_bytes(), dtype=torch.uint8)
+        plan.pack(h)
+        packs.append(h.numpy().copy())
+        # the write launch's slot comes first: its first run's pos0 (after
+        # three pointers, row0 and nrows) is the row's position
+        assert int(packs[-1][32:36].view(np.int32)[0]) == n - 1
+    assert len(set(shapes)) == 1
+    assert len({p.tobytes() for p in packs}) == 4
+    assert plan.dyn_bytes() % 16 == 0 and plan.dyn_bytes() > 0
+
+    # parameter mode: the same calls size the decode grid by their work
+    p2 = B.Plan()
+    assert plan_at(p2, 1020)[1]["grid"] < 152
+    with pytest.raises(B.TfpaError) as e:
+        p2.pack(torch.zeros(64, dtype=torch.uint8))
+    assert e.value.code == B.TFPA_EINVAL
+    with pytest.raises(B.TfpaError) as e:         # not on a plan that holds launches
+        p2.set_device(dyn)
+    assert e.value.code == B.TFPA_EINVAL
+
+    # a buffer too small: the call fails and the plan stays as it was
+    p3 = B.Plan()
+    p3.set_device(dyn[:4096])
+    segs = [B.Seg(1000, page_table=3 * FAKE)]
+    with B.record_launches():
+        p3.write_kv(c, segs, 4 * FAKE, 5 * FAKE, np.array([0]), np.array([999]))
+        used = p3.dyn_bytes()
+        with pytest.raises(B.TfpaError) as e:
+            p3.decode(c, segs, 4 * FAKE, np.array([0]), np.array([999]), 0.088, sc, 7 * FAKE)
+    assert e.value.code == B.TFPA_ECAPACITY
+    assert len(p3) == 1 and p3.dyn_bytes() == used
+    with pytest.raises(B.TfpaError) as e:
+        p3.pack(torch.zeros(used - 16, dtype=torch.uint8))
+    assert e.value.code == B.TFPA_ECAPACITY
+
+    # sixteen rows of one stream (four m-tiles with four heads per kv head)
+    # take the tensor-core verify path, whose grid follows the lengths
+    p4 = B.Plan()
+    p4.set_device(dyn)
+    with B.record_launches():
+        with pytest.raises(B.TfpaError) as e:
+            p4.decode(c, segs, 4 * FAKE, np.zeros(16), np.arange(984, 1000), 0.088, sc,
+                      7 * FAKE)
+    assert e.value.code == B.TFPA_EINVAL and len(p4) == 0 and p4.dyn_bytes() == 0
