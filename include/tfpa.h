@@ -100,12 +100,28 @@ typedef struct {
 /* Split-K scratch for decode partials (float32).
  *   part_o  : DEVICE [cap_rows][hq][max_splits][128]  unnormalised outputs o
  *   part_ml : DEVICE [cap_rows][hq][max_splits][2]    (m, l): running max of the
- *             scores in log2 units (score * log2(e)) and the sum of 2^(s2 - m)  */
+ *             scores in log2 units (score * log2(e)) and the sum of 2^(s2 - m)
+ *   arrive  : optional DEVICE uint32[cap_rows][hq], all zero before the first
+ *             call.  With it, tfpa_decode merges a slice inside the partial
+ *             kernel when each of its streams has at most 4 splits
+ *             (seq_len <= 2,048): the last CTA to finish a split of a group
+ *             of query vectors (counted here) merges that group's splits in
+ *             split order, with the merge kernel's arithmetic, so the output
+ *             bytes are those of the separate merge; a launch leaves every
+ *             counter at zero again.  Longer streams, tfpa_decode_tree,
+ *             plans in device mode and slices with rows for the tensor-core
+ *             verify path keep the separate merge (a group's in-kernel merge
+ *             runs on one SM at the kernel's tail: for 32 splits it was
+ *             measured slower than the separate launch).  After a call that
+ *             set the cache's err_flag the counters may be left non-zero:
+ *             zero them before the next call.  NULL: always the separate
+ *             merge. */
 typedef struct {
   float* part_o;
   float* part_ml;
   int32_t cap_rows;               /* rows one partial launch can hold                      */
   int32_t max_splits;             /* >= tfpa_num_splits(seq_len) of every segment used     */
+  uint32_t* arrive;
 } tfpa_scratch;
 
 /* KV write with rotary position embedding: tfpa_write_kv, with each row's K

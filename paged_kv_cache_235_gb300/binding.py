@@ -58,7 +58,8 @@ class tfpa_cache(ctypes.Structure):
 
 class tfpa_scratch(ctypes.Structure):
     _fields_ = [("part_o", ctypes.c_void_p), ("part_ml", ctypes.c_void_p),
-                ("cap_rows", ctypes.c_int32), ("max_splits", ctypes.c_int32)]
+                ("cap_rows", ctypes.c_int32), ("max_splits", ctypes.c_int32),
+                ("arrive", ctypes.c_void_p)]
 
 
 class tfpa_launch_record(ctypes.Structure):
@@ -262,16 +263,23 @@ class Scratch(_Cached):
     part_ml: object
     cap_rows: int
     max_splits: int = MAX_SPLITS
+    arrive: object = None             # uint32 [cap_rows][hq] zeros: merge in the partial kernel
 
     def _make_c(self) -> tfpa_scratch:
-        return tfpa_scratch(_ptr(self.part_o), _ptr(self.part_ml), self.cap_rows, self.max_splits)
+        return tfpa_scratch(_ptr(self.part_o), _ptr(self.part_ml), self.cap_rows, self.max_splits,
+                            _ptr(self.arrive))
 
 
-def make_scratch(cap_rows: int, hq: int, max_splits: int = MAX_SPLITS, device="cuda") -> Scratch:
+def make_scratch(cap_rows: int, hq: int, max_splits: int = MAX_SPLITS, device="cuda",
+                 fused_merge: bool = True) -> Scratch:
+    """Scratch for cap_rows rows; with fused_merge (the default) it carries
+    the zeroed arrival counters that let tfpa_decode merge inside the
+    partial kernel."""
     import torch
     o = torch.empty(cap_rows * hq * max_splits * HEAD_DIM, dtype=torch.float32, device=device)
     ml = torch.empty(cap_rows * hq * max_splits * 2, dtype=torch.float32, device=device)
-    return Scratch(o, ml, cap_rows, max_splits)
+    arrive = torch.zeros(cap_rows * hq, dtype=torch.int32, device=device) if fused_merge else None
+    return Scratch(o, ml, cap_rows, max_splits, arrive)
 
 
 class SegTable:

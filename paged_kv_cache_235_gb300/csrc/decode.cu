@@ -58,7 +58,7 @@ constexpr int kCombBytes = kCombineWarps * 16 * 32 * 16;
 constexpr int kMlBytes = kConsumerWarps * 16 * 2 * 4;
 constexpr int kNumBars = 2 * kStages + 7;
 constexpr int kSmemBytes =
-    kStages * kStageBytes + kCombBytes + kMlBytes + kStages * 4 + 4 + kNumBars * 8 + 1024;
+    kStages * kStageBytes + kCombBytes + kMlBytes + kStages * 4 + 8 + kNumBars * 8 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
@@ -518,6 +518,99 @@ __device__ void consumer(const DecodeParams& p, const DecodeDyn& D, uint8_t* sta
   }
 }
 
+// The log-sum-exp merge of one (row, head) by one warp: lane s holds split
+// s's (m, l), lane t owns head-dim elements 4t..4t+3.  M is the lanes' max,
+// L the butterfly sum of l_s 2^(m_s - M), o = sum_s 2^(m_s - M) o_s taken in
+// split order, out = o / L in bf16 and lse = ln2 (M + log2 L).  The o_s are
+// loaded B splits at a time (every split at once in the merge kernel, fewer
+// where registers are short); the arithmetic and its order do not depend on
+// B, so every caller writes the same bytes.  CG: load through L2 only (the
+// partials of other CTAs of a running grid).
+template <int B, bool CG>
+__device__ __forceinline__ void merge_vector(const float* part_o, const float* part_ml, int nsplit,
+                                             __nv_bfloat16* out, float* lse) {
+  const int lane = threadIdx.x & 31;
+  const float4* po = reinterpret_cast<const float4*>(part_o) + lane;
+  auto ld4 = [](const float4* a) { return CG ? __ldcg(a) : *a; };
+  float4 v0[B];
+#pragma unroll
+  for (int u = 0; u < B; ++u)
+    if (u < nsplit) v0[u] = ld4(po + u * (kHeadDim / 4));
+  float m = -INFINITY, l = 0.f;
+  if (lane < nsplit) {
+    const float2* a = reinterpret_cast<const float2*>(part_ml) + lane;
+    const float2 ml = CG ? __ldcg(a) : *a;
+    m = ml.x;
+    l = ml.y;
+  }
+  float M = m;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float a = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
+  float L = a * l;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto add = [&](int sp, const float4& v) {
+    const float as = __shfl_sync(0xffffffffu, a, sp);
+    acc.x = __fmaf_rn(as, v.x, acc.x);
+    acc.y = __fmaf_rn(as, v.y, acc.y);
+    acc.z = __fmaf_rn(as, v.z, acc.z);
+    acc.w = __fmaf_rn(as, v.w, acc.w);
+  };
+  for (int u0 = 0; u0 < nsplit; u0 += B) {
+    if (u0 > 0) {
+#pragma unroll
+      for (int u = 0; u < B; ++u)
+        if (u0 + u < nsplit) v0[u] = ld4(po + (u0 + u) * (kHeadDim / 4));
+    }
+#pragma unroll
+    for (int u = 0; u < B; ++u)
+      if (u0 + u < nsplit) add(u0 + u, v0[u]);
+  }
+  const float inv = 1.f / L;
+  uint2 packed;
+  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(out + lane * 4) = packed;
+  if (lse && lane == 0) *lse = (M + log2f(L)) * 0.6931471805599453f;
+}
+
+// Merge in the partial kernel, run by the four combiner warps after they
+// wrote an item's partial: the item's group (run, kv head, m-tile) counts
+// its finished splits in p.arrive, at the (row, head) of its first query
+// vector; the CTA that finishes the last split resets the counter and
+// merges the group's query vectors, warp 8+q taking vectors q, q+4, ...
+// Every thread fences its partial stores before the count, and the merging
+// threads fence after it and load the partials through L2.
+__device__ __forceinline__ void merge_if_last(const DecodeParams& p, const RunInfo& ru,
+                                              const Item& x, int nq, int* merge_flag) {
+  const int q = (threadIdx.x >> 5) - kCombineWarp0;
+  __threadfence();
+  named_bar_sync(1, 32 * kCombineWarps);
+  if (threadIdx.x == 32 * kCombineWarp0) {
+    const int qv0 = x.mt * 16;
+    const int r0 = qv0 / p.group;
+    uint32_t* ctr = p.arrive + (size_t)(ru.row0 + r0) * p.hq + x.g * p.group + (qv0 - r0 * p.group);
+    const uint32_t old = atomicAdd(ctr, 1u);
+    const int last = old + 1u == (uint32_t)ru.nsplit;
+    if (last) atomicExch(ctr, 0u);
+    *merge_flag = last;
+  }
+  named_bar_sync(1, 32 * kCombineWarps);
+  if (!*merge_flag) return;
+  __threadfence();
+  for (int j = q; j < 16; j += kCombineWarps) {
+    const int qv = x.mt * 16 + j;
+    if (qv >= nq) break;
+    const int r = qv / p.group;
+    const size_t rh = (size_t)(ru.row0 + r) * p.hq + x.g * p.group + (qv - r * p.group);
+    const size_t slot0 = rh * p.max_splits;
+    merge_vector<4, true>(p.part_o + slot0 * kHeadDim, p.part_ml + slot0 * 2, ru.nsplit,
+                          p.out + rh * kHeadDim, p.lse ? p.lse + rh : nullptr);
+  }
+}
+
 // Combiner warp 8+q: for every item of the CTA, reads the states of consumer
 // warps q and q+4 from TMEM, and
 // (1) publishes their (m, l) so that each combiner knows the eight-warp max;
@@ -528,9 +621,9 @@ __device__ void consumer(const DecodeParams& p, const DecodeDyn& D, uint8_t* sta
 // Each of pub, folded and done completes once per item (parity = item & 1);
 // a combiner waits for done of the previous item before publishing, so the
 // fold and (m, l) buffers are never overwritten while still being read.
-template <bool FP8, bool GEN>
+template <bool FP8, bool GEN, bool MERGE>
 __device__ void combiner(const DecodeParams& p, const DecodeDyn& D, uint32_t tmem, float4* fold,
-                         float* ml_buf, CombBars bars) {
+                         float* ml_buf, int* merge_flag, CombBars bars) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int q = warp - kCombineWarp0;
@@ -655,11 +748,13 @@ __device__ void combiner(const DecodeParams& p, const DecodeDyn& D, uint32_t tme
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.done);
+    if constexpr (MERGE) merge_if_last(p, ru, x, nq, merge_flag);
   }
 }
 
 // DEV: the runs and CTA ranges are read from p.dyn (a plan in device mode).
-template <bool FP8, bool GEN, bool DEV>
+// MERGE: the combiners merge each finished group (p.arrive).
+template <bool FP8, bool GEN, bool DEV, bool MERGE>
 __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
     const __grid_constant__ DecodeParams p) {
   const DecodeDyn& D = DEV ? *p.dyn : p.d;
@@ -671,8 +766,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
   float* ml_buf = reinterpret_cast<float*>(smem + kStages * kStageBytes + kCombBytes);
   int* stage_bad = reinterpret_cast<int*>(ml_buf + kConsumerWarps * 16 * 2);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stage_bad + kStages);
+  int* merge_flag = reinterpret_cast<int*>(tmem_slot + 1);
   uint64_t* bars = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(tmem_slot + 1) + 7) & ~uintptr_t(7));
+      (reinterpret_cast<uintptr_t>(merge_flag + 1) + 7) & ~uintptr_t(7));
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* cbar = bars + 2 * kStages;
@@ -711,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
     consumer<FP8, GEN>(p, D, stage_mem, full, empty, stage_bad, tmem, cb);
   } else if (warp < kProducerWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCombine));
-    combiner<FP8, GEN>(p, D, tmem, fold, ml_buf, cb);
+    combiner<FP8, GEN, MERGE>(p, D, tmem, fold, ml_buf, merge_flag, cb);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
     if (warp == kProducerWarp) producer<FP8>(p, D, stage_mem, full, empty, stage_bad);
@@ -745,62 +841,30 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
   // Every slot below nsplit was written by the partial kernel (an empty split
   // holds o = 0 with weight 0).  Every split's o chunk is loaded together
   // with the (m, l) pairs, before the reductions that need them, so a merge
-  // waits for one round of loads; the sums run in split order.
+  // waits for one round of loads.
   static_assert(kMaxSplits == 32, "one load per split");
-  const float4* po = reinterpret_cast<const float4*>(p.part_o + slot0 * kHeadDim) + lane;
-  float4 v0[kMaxSplits];
-#pragma unroll
-  for (int u = 0; u < kMaxSplits; ++u)
-    if (u < nsplit) v0[u] = po[u * (kHeadDim / 4)];
-  float m = -INFINITY, l = 0.f;
-  if (lane < nsplit) {
-    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (slot0 + lane) * 2);
-    m = ml.x;
-    l = ml.y;
-  }
-  float M = m;
-#pragma unroll
-  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  const float a = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
-  float L = a * l;
-#pragma unroll
-  for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  auto add = [&](int sp, const float4& v) {
-    const float as = __shfl_sync(0xffffffffu, a, sp);
-    acc.x = __fmaf_rn(as, v.x, acc.x);
-    acc.y = __fmaf_rn(as, v.y, acc.y);
-    acc.z = __fmaf_rn(as, v.z, acc.z);
-    acc.w = __fmaf_rn(as, v.w, acc.w);
-  };
-#pragma unroll
-  for (int u = 0; u < kMaxSplits; ++u)
-    if (u < nsplit) add(u, v0[u]);
-  const float inv = 1.f / L;
-  uint2 packed;
-  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2*>(p.out + ((size_t)row * p.hq + h) * kHeadDim + lane * 4) = packed;
-  if (p.lse && lane == 0) p.lse[(size_t)row * p.hq + h] = (M + log2f(L)) * 0.6931471805599453f;
+  merge_vector<kMaxSplits, false>(p.part_o + slot0 * kHeadDim, p.part_ml + slot0 * 2, nsplit,
+                                  p.out + ((size_t)row * p.hq + h) * kHeadDim,
+                                  p.lse ? p.lse + (size_t)row * p.hq + h : nullptr);
 }
 
-template <bool FP8, bool GEN, bool DEV>
+template <bool FP8, bool GEN, bool DEV, bool MERGE>
 cudaError_t launch_partial(const DecodeParams& p, int grid, cudaStream_t s) {
   static PerDeviceOnce configured;
   cudaError_t e = configured.run([] {
     // The register split only works if the block launches with at least the
     // registers it hands out; otherwise setmaxnreg.inc would wait forever.
     cudaFuncAttributes attr;
-    cudaError_t r = cudaFuncGetAttributes(&attr, decode_partial_kernel<FP8, GEN, DEV>);
+    cudaError_t r = cudaFuncGetAttributes(&attr, decode_partial_kernel<FP8, GEN, DEV, MERGE>);
     if (r != cudaSuccess) return r;
     if (attr.numRegs * kThreads < 128 * (2 * kRegsConsumer + kRegsCombine + kRegsProducer))
       return cudaErrorInvalidValue;
-    return cudaFuncSetAttribute(decode_partial_kernel<FP8, GEN, DEV>,
+    return cudaFuncSetAttribute(decode_partial_kernel<FP8, GEN, DEV, MERGE>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (e != cudaSuccess) return e;
   e =
-      launch_pdl(decode_partial_kernel<FP8, GEN, DEV>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
+      launch_pdl(decode_partial_kernel<FP8, GEN, DEV, MERGE>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -810,10 +874,10 @@ cudaError_t launch_partial_dev(const DecodeParams& p, bool fp8, int grid, cudaSt
   // Rows with ancestor masks take the general instantiation, so the plain
   // causal calls keep their own kernel's code.
   if (p.anc)
-    return fp8 ? launch_partial<true, true, DEV>(p, grid, s)
-               : launch_partial<false, true, DEV>(p, grid, s);
-  return fp8 ? launch_partial<true, false, DEV>(p, grid, s)
-             : launch_partial<false, false, DEV>(p, grid, s);
+    return fp8 ? launch_partial<true, true, DEV, false>(p, grid, s)
+               : launch_partial<false, true, DEV, false>(p, grid, s);
+  return fp8 ? launch_partial<true, false, DEV, false>(p, grid, s)
+             : launch_partial<false, false, DEV, false>(p, grid, s);
 }
 
 }  // namespace
@@ -822,6 +886,12 @@ cudaError_t launch_partial_dev(const DecodeParams& p, bool fp8, int grid, cudaSt
 // (p.d), which a device-mode plan keeps fixed from step to step.
 cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cudaStream_t s) {
   if (grid <= 0 || p.d.n_items == 0) return cudaSuccess;
+  // The merge in the kernel is built for plain causal rows in parameter mode.
+  if (p.arrive) {
+    if (p.anc || p.dyn || !p.out) return cudaErrorInvalidValue;
+    return fp8 ? launch_partial<true, false, false, true>(p, grid, s)
+               : launch_partial<false, false, false, true>(p, grid, s);
+  }
   return p.dyn ? launch_partial_dev<true>(p, fp8, grid, s)
                : launch_partial_dev<false>(p, fp8, grid, s);
 }

@@ -480,6 +480,10 @@ void plan_cta_ranges(DecodeParams& p, int nr, int G, bool fp8, int grid) {
   while (b <= grid) p.d.cta_item0[b++] = n_items;
 }
 
+// Streams of at most this many splits (2,048 positions) are merged inside
+// the partial kernel when the scratch has arrival counters.
+constexpr int kFusedMergeMaxSplits = 4;
+
 // Partial (and optionally merge) launches over the call's rows.  With
 // `sliced`, each launch's partials start at scratch row 0 and are merged
 // before the next launch; otherwise partials land at the call's own row and
@@ -567,6 +571,13 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
     const size_t srow_elems = (size_t)srow * c->hq * sc->max_splits;
     float* part_o = sc->part_o + srow_elems * kHeadDim;
     float* part_ml = sc->part_ml + srow_elems * 2;
+    // With arrival counters, plain causal rows in parameter mode, no rows on
+    // the verify path and few splits per stream, the partial kernel merges
+    // the slice itself.  A group's merge runs on the one SM that finished
+    // its last split, reading every split's partial: cheap for a few splits,
+    // slower than a separate grid-wide merge for many.
+    bool fused = sliced && nv == 0 && sc->arrive && !anc && !sink.device();
+    for (int r = 0; fused && r < nd; ++r) fused = p.d.runs[r].nsplit <= kFusedMergeMaxSplits;
     if (nd > 0) {
       if ((e = fill_maps(c, segs, ss, fp8, fp8 ? 128 : 64, fp8 ? 256 : 128, p.maps, p.nsrc)))
         return e;
@@ -577,6 +588,9 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
       p.k_scale = c->k_scale;
       p.v_scale = c->v_scale;
       p.err_flag = c->err_flag;
+      p.arrive = fused ? sc->arrive + (size_t)srow * c->hq : nullptr;
+      p.out = fused ? static_cast<__nv_bfloat16*>(out) + (size_t)base * hd : nullptr;
+      p.lse = fused && lse ? lse + (size_t)base * c->hq : nullptr;
       p.d.nruns = nd;
       p.d.n_items = items;
       p.hq = c->hq;
@@ -617,7 +631,7 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
       record(8, base, nrows, nv, tiles, tiles, (int64_t)base * hd, 0);
       if ((e = sink.verify(pv, fp8, tiles))) return e;
     }
-    if (sliced) {
+    if (sliced && !fused) {
       mp.part_o = part_o;
       mp.part_ml = part_ml;
       mp.out = static_cast<__nv_bfloat16*>(out) + (size_t)base * hd;

@@ -66,6 +66,12 @@ struct DecodeParams {
   const float* k_scale;       // fp8: [hkv]
   const float* v_scale;
   int32_t* err_flag;
+  // Merge in the partial kernel (arrive != nullptr): per (row, head) of a
+  // group's first query vector, the splits finished so far; the last CTA
+  // to finish one merges the group into out / lse (rows of this launch).
+  uint32_t* arrive;           // [cap_rows][hq], scratch rows of this launch
+  __nv_bfloat16* out;         // [rows][hq][128]
+  float* lse;                 // [rows][hq] or nullptr
   int32_t nsrc;
   int32_t hq, hkv, group;     // group = hq / hkv
   int32_t max_splits;

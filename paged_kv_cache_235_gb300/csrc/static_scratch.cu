@@ -106,6 +106,7 @@ extern "C" int tfpa_decode_static(const tfpa_cache* cache, const tfpa_seg* segs,
   sc.part_ml = base + (size_t)kStaticSlots * tfpa::kHeadDim;
   sc.cap_rows = kStaticSlots / per_row;
   sc.max_splits = TFPA_MAX_SPLITS;
+  sc.arrive = nullptr;   // the separate merge launch
   return tfpa_decode(cache, segs, nseg, q, row_seg, row_pos, rows, softmax_scale, &sc, out, lse,
                      stream);
 }

@@ -113,23 +113,23 @@ class GpuCase:
             qb = qb[rows]
         return _dev(qb.view(np.int16), torch.bfloat16)
 
-    def decode(self, q, row_seg, row_pos, cap_rows=128, segs=None, lse=True):
+    def decode(self, q, row_seg, row_pos, cap_rows=128, segs=None, lse=True, fused=True):
         rows = len(row_seg)
         out = torch.empty(rows, self.w.hq, self.w.d, dtype=torch.bfloat16, device="cuda")
         l = torch.empty(rows, self.w.hq, dtype=torch.float32, device="cuda") if lse else None
-        sc = B.make_scratch(cap_rows, self.w.hq)
+        sc = B.make_scratch(cap_rows, self.w.hq, fused_merge=fused)
         B.tfpa_decode(self.cache, segs or self.segs, q, row_seg, row_pos, self.w.softmax_scale,
                       sc, out, l)
         torch.cuda.synchronize()
         return out, l
 
-    def decode_tree(self, q, row_seg, row_pos, row_anc, cap_rows=128, lse=True):
+    def decode_tree(self, q, row_seg, row_pos, row_anc, cap_rows=128, lse=True, fused=True):
         rows = len(row_seg)
         anc = torch.from_numpy(np.ascontiguousarray(np.asarray(row_anc, np.uint64))
                                .view(np.int64)).cuda()
         out = torch.empty(rows, self.w.hq, self.w.d, dtype=torch.bfloat16, device="cuda")
         l = torch.empty(rows, self.w.hq, dtype=torch.float32, device="cuda") if lse else None
-        sc = B.make_scratch(cap_rows, self.w.hq)
+        sc = B.make_scratch(cap_rows, self.w.hq, fused_merge=fused)
         B.tfpa_decode_tree(self.cache, self.segs, q, row_seg, row_pos, anc,
                            self.w.softmax_scale, sc, out, l)
         torch.cuda.synchronize()

@@ -391,3 +391,44 @@ def test_device_mode_plans_keep_their_shape_as_lengths_grow():
             p4.decode(c, segs, 4 * FAKE, np.zeros(16), np.arange(984, 1000), 0.088, sc,
                       7 * FAKE)
     assert e.value.code == B.TFPA_EINVAL and len(p4) == 0 and p4.dyn_bytes() == 0
+
+
+def test_arrival_counters_fold_the_merge_into_the_partial_launch():
+    """With arrival counters a slice of plain decode-path rows over streams
+    of at most 4 splits runs one partial launch and no merge; longer
+    streams, tree rows, device-mode plans and slices with tensor-core verify
+    rows keep the separate merge."""
+    c = _cache()
+    short = [B.Seg(2048, page_table=3 * FAKE), B.Seg(700, k_slab=8 * FAKE, v_slab=9 * FAKE,
+                                                     slab_cap=768)]
+    long = [B.Seg(2049, page_table=3 * FAKE)] + short[1:]
+    plain = B.Scratch(5 * FAKE, 6 * FAKE, 16)
+    counted = B.Scratch(5 * FAKE, 6 * FAKE, 16, 32, 10 * FAKE)
+
+    def kinds(sc, segs, rs, rp, anc=None):
+        with B.record_launches() as rec:
+            if anc is None:
+                B.tfpa_decode(c, segs, 4 * FAKE, rs, rp, 0.088, sc, 7 * FAKE, stream=0)
+            else:
+                B.tfpa_decode_tree(c, segs, 4 * FAKE, rs, rp, anc, 0.088, sc, 7 * FAKE, stream=0)
+        return [r["kind"] for r in rec]
+
+    rs = np.array([0, 1])
+    assert kinds(plain, short, rs, np.array([2047, 699])) == ["partial", "merge"]
+    assert kinds(counted, short, rs, np.array([2047, 699])) == ["partial"]
+    assert kinds(counted, long, rs, np.array([2048, 699])) == ["partial", "merge"]
+    assert kinds(counted, short, rs, np.array([2047, 699]), anc=11 * FAKE) == ["partial", "merge"]
+    # 20 rows of stream 0 (verify path) + 1 of stream 1, 16-row slices
+    rs = np.array([0] * 20 + [1])
+    rp = np.array(list(range(2028, 2048)) + [699])
+    assert kinds(counted, short, rs, rp) == ["verify", "merge", "partial", "verify", "merge"]
+    rs, rp = np.array([0] * 3 + [1]), np.array([2045, 2046, 2047, 699])
+    assert kinds(counted, short, rs, rp) == ["partial"]
+    # a plan in device mode keeps the merge launch
+    torch = pytest.importorskip("torch")
+    plan = B.Plan()
+    plan.set_device(torch.zeros(1 << 16, dtype=torch.uint8))
+    with B.record_launches() as rec:
+        plan.decode(c, short, 4 * FAKE, np.array([0, 1]), np.array([2047, 699]), 0.088, counted,
+                    7 * FAKE)
+    assert [r["kind"] for r in rec] == ["partial", "merge"]
