@@ -609,8 +609,12 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
     }
     if (nv > 0) {
       if ((e = fill_maps(c, segs, ss, fp8, fp8 ? 128 : 64, 128, pv.maps, pv.nsrc))) return e;
+      // The kernel loads a verify tile's Q as two boxes of 64 query vectors
+      // when G divides 64 (so that a tile of at most 64 vectors can hold
+      // them twice, one copy per MMA slot), else as one box.
+      const int qbox = 64 % G == 0 ? 64 / G : vrows;
       if ((e = get_qmap(static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd, c->hq, nrows,
-                        G, vrows, &pv.qmap)))
+                        G, qbox, &pv.qmap)))
         return e;
       pv.q = static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd;
       pv.anc = anc ? anc + base : nullptr;

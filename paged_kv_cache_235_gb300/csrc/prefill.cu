@@ -41,6 +41,9 @@
 // key split), no cluster.  One Q tile holds the group's query vectors (row x
 // head) and both slots read it: slot A takes the split's even key tiles,
 // slot B the odd ones, and the CTA merges the two into the split's partial.
+// A verify tile of at most 64 query vectors holds them twice (M rows 0-63
+// and 64-127) and each slot's softmax takes one copy, so the two slots run
+// on different SM sub-partitions ("half mode").
 // bf16: rings of three K and V stages over the slots' common tile order.
 // e4m3: two e4m3 K stages per slot (8-bit S MMAs), two V staging tiles per
 // slot, one f16 V stage per slot.
@@ -189,6 +192,13 @@ __device__ __forceinline__ Tile tile_of(const PrefillParams& p, int i) {
   return x;
 }
 
+// Verify tiles load Q as two boxes of 64 query vectors (M rows 0-63 and
+// 64-127) when G divides 64.  A tile of at most 64 vectors then loads them
+// into both halves ("half mode"): slot A's softmax takes TMEM lanes 0-63 and
+// slot B's lanes 64-127, so the two slots' softmax threads sit on different
+// SM sub-partitions (a warp reaches only its own quarter of the lanes).
+__device__ __forceinline__ bool q_two_boxes(int group) { return 64 % group == 0; }
+
 struct TileGeom {
   int row_lo;      // first row of the tile, relative to the run
   int nrows;       // valid rows in the tile
@@ -293,9 +303,17 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
     // next rows or zeros, which no output reads.
     const int rt = kVerifyVectors / p.group;
     mbar_arrive_expect_tx(b.q_full, 2u * 128u * (uint32_t)(p.group * rt));
-    for (int rg = 0; rg < 2; ++rg)
-      tma_load_3d(smem + kOffQ + rg * 16384, &p.qmap, rg * 64, x.g * p.group,
-                  ru.row0 + gm.row_lo, b.q_full);
+    if (q_two_boxes(p.group)) {
+      const bool half = gm.nrows * p.group <= 64;
+      for (int rg = 0; rg < 2; ++rg)
+        for (int hb = 0; hb < 2; ++hb)
+          tma_load_3d(smem + kOffQ + rg * 16384 + hb * 8192, &p.qmap, rg * 64, x.g * p.group,
+                      ru.row0 + gm.row_lo + (half ? 0 : hb * (64 / p.group)), b.q_full);
+    } else {
+      for (int rg = 0; rg < 2; ++rg)
+        tma_load_3d(smem + kOffQ + rg * 16384, &p.qmap, rg * 64, x.g * p.group,
+                    ru.row0 + gm.row_lo, b.q_full);
+    }
   } else {
     // Slot hh is query head h0 + hh, 128 rows (box 64 x 1 x 128).
     mbar_arrive_expect_tx(b.q_full, 65536);
@@ -861,11 +879,16 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
   const uint32_t tS = tmem + lane_off + col_s(hh);
   const uint32_t tO = tmem + lane_off + col_o(hh);
-  // Verify: TMEM lane r holds query vector (row r / G, head r % G of the
-  // group) in both slots; the slots see alternate key tiles.
-  const int rho = VERIFY ? r / p.group : r;             // row within the tile
-  const int hig = VERIFY ? r - rho * p.group : 0;       // verify: head within the group
-  const bool valid = rho < gm.nrows && (!VERIFY || r < p.group * (kVerifyVectors / p.group));
+  // Verify: TMEM lane r holds query vector v = r (row v / G, head v % G of
+  // the group) in both slots, or in half mode v = r - 64 hh for the lanes of
+  // slot hh's half; the slots see alternate key tiles.
+  const bool half = VERIFY && q_two_boxes(p.group) && gm.nrows * p.group <= 64;
+  const bool mine = !half || (r >> 6) == hh;            // half mode: this slot's lanes
+  const int v = half ? (r & 63) : r;                    // query vector of this lane
+  const int rho = VERIFY ? v / p.group : r;             // row within the tile
+  const int hig = VERIFY ? v - rho * p.group : 0;       // verify: head within the group
+  const bool valid =
+      mine && rho < gm.nrows && (!VERIFY || v < p.group * (kVerifyVectors / p.group));
   const int pos = ru.pos0 + gm.row_lo + (valid ? rho : 0);
   const int nt = slot_tiles<VERIFY>(gm, hh);             // this slot's key tiles
   // Verify with ancestor masks: key pos - d (d < 64) is visible iff bit d of
@@ -1010,12 +1033,38 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
     // eight softmax warps (which every one of them reaches), slot A's read
     // both slots' O from TMEM (the same lane quarter) and write.  A slot
     // without tiles counts as m = -inf, l = 0, O = 0.
+    // In half mode slot B's lanes are not slot A's: slot B's threads also
+    // leave their O rows in shared memory (over the V stages, free once the
+    // MMAs are done; 16-byte chunks permuted by vector against conflicts).
     float2* ml_s = reinterpret_cast<float2*>(smem + Layout<FP8>::kOffMl);
-    if (hh == 1) ml_s[r] = make_float2(m_run, l);
+    const uint32_t obuf = smem_u32(smem + kOffV) + (uint32_t)v * 512u;
+    if (hh == 1) {
+      if (mine) ml_s[v] = make_float2(m_run, l);
+      // tcgen05.ld is warp-wide: the condition is the same for every lane
+      // (mine and nt are per warp), and only the stores follow `valid`
+      const bool wok = __all_sync(0xffffffffu, ok);
+      if (half && mine && nt > 0 && wok) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          umma::tmem_ld32(tO + 32 * c, o);
+          umma::tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                               obuf + part_o_chunk(v, 8 * c + q)),
+                           "r"(o[4 * q]), "r"(o[4 * q + 1]), "r"(o[4 * q + 2]),
+                           "r"(o[4 * q + 3])
+                           : "memory");
+          }
+        }
+      }
+    }
     __syncwarp();
     named_bar_sync(1, 256);
     if (hh == 1 || !__all_sync(0xffffffffu, ok)) return;
-    const float2 mlb = ml_s[r];
+    const float2 mlb = ml_s[v];
     const float mx = fmaxf(m_run, mlb.x);
     const float a0 = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mx);
     const float a1 = mlb.x == -INFINITY ? 0.f : fast_exp2(mlb.x - mx);
@@ -1036,7 +1085,16 @@ __device__ void softmax_role(const PrefillParams& p, const RunInfo& ru, const Ti
 #pragma unroll
         for (int i = 0; i < 32; ++i) oa[i] = 0u;
       }
-      if (nb > 0) {
+      if (nb > 0 && half) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 w = lds128(obuf + part_o_chunk(v, 8 * c + q));
+          ob[4 * q] = w.x;
+          ob[4 * q + 1] = w.y;
+          ob[4 * q + 2] = w.z;
+          ob[4 * q + 3] = w.w;
+        }
+      } else if (nb > 0) {
         umma::tmem_ld32(tOb + 32 * c, ob);
       } else {
 #pragma unroll
