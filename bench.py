@@ -759,11 +759,11 @@ def time_tree_calls(w, torch, B, reps):
     return statistics.median(times)
 
 
-def time_decode_calls(w, torch, B, reps, flush):
+def time_decode_calls(w, torch, B, reps, flush, fused_merge=False):
     """tfpa_decode (partial + merge) one call at a time, CUDA events around
     each, optionally with L2 flushed before each call; median in ms."""
     cache, segs, q = device_case(w, torch, B)
-    sc = B.make_scratch(min(128, w.rows), w.hq)
+    sc = B.make_scratch(min(128, w.rows), w.hq, fused_merge=fused_merge)
     out = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16, device="cuda")
     buf = L2Flush(torch) if flush else None
     s = torch.cuda.current_stream()
@@ -781,6 +781,30 @@ def time_decode_calls(w, torch, B, reps, flush):
             times.append(e0.elapsed_time(e1))
     assert int(cache.err_flag.item()) == 0, "kernel error flag set"
     return statistics.median(times)
+
+
+def time_launch_floor(torch, reps=40):
+    """The event-timing floor of a call: an empty event pair, and one and two
+    one-element torch kernels between the events (same method as the
+    per-call lines: a GPU sleep first, medians in us)."""
+    s = torch.cuda.current_stream()
+    x = torch.zeros(1, device="cuda")
+
+    def med(fn):
+        t = []
+        for i in range(reps + 3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            host_cover(torch)
+            e0.record(s)
+            fn()
+            e1.record(s)
+            torch.cuda.synchronize()
+            if i >= 3:
+                t.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(t)
+
+    return {"event_pair_us": med(lambda: None), "one_kernel_us": med(lambda: x.add_(1)),
+            "two_kernels_us": med(lambda: (x.add_(1), x.add_(1)))}
 
 
 def profile_case(args, torch, B, wl):
@@ -932,13 +956,18 @@ def main():
                 "frac_of_measured_bf16": fl5 / (ms5 / 1e3) / 1e12 / pk["bf16_tflops"]}
         w1 = wl.tiny_paged_decode()
         ms1 = time_decode_calls(w1, torch, B, 50, flush=True)
+        ms1f = time_decode_calls(w1, torch, B, 50, flush=True, fused_merge=True)
         kv1, qo1 = kv_bytes(w1)
         extra["tiny_decode"] = {
             "workload": "1 stream, 1 row at position 999, 8/2 heads, bf16, 4 of 16 pool pages; "
                         "tfpa_decode per call, L2 flushed before each",
             "us_per_call": ms1 * 1e3, "kv_gbs": (kv1 + qo1) / (ms1 / 1e3) / 1e9,
             "frac_of_measured_hbm": (kv1 + qo1) / (ms1 / 1e3) / 1e9 / pk["hbm_gbs"],
-            "note": "1 MB of KV: launch and latency bound, the HBM roofline is out of reach"}
+            "us_per_call_merge_in_partial": ms1f * 1e3,
+            "timing_floor": time_launch_floor(torch),
+            "note": "1 MB of KV: launch and latency bound, the HBM roofline is out of reach; "
+                    "timing_floor is the same event method around nothing and around one "
+                    "and two one-element kernels"}
         w6 = wl.overcommitted_pool()
         ms6 = time_decode_calls(w6, torch, B, 20, flush=False)
         kv6, qo6 = kv_bytes(w6)

@@ -104,7 +104,7 @@ typedef struct {
  *   arrive  : optional DEVICE uint32[cap_rows][hq], all zero before the first
  *             call.  With it, tfpa_decode merges a slice inside the partial
  *             kernel when each of its streams has at most 4 splits
- *             (seq_len <= 2,048): the last CTA to finish a split of a group
+ *             (seq_len <= 1,024): the last CTA to finish a split of a group
  *             of query vectors (counted here) merges that group's splits in
  *             split order, with the merge kernel's arithmetic, so the output
  *             bytes are those of the separate merge; a launch leaves every
@@ -208,8 +208,8 @@ int tfpa_restore_kv(const tfpa_cache* cache, const tfpa_seg* seg, int32_t p0, in
                     const void* image, cudaStream_t stream);
 
 /* Split policy, a function of a stream's own length only (so a stream's
- * partials never depend on its batch): pages_per_split = max(2,
- * ceil(npages / 32)), nsplit = ceil(npages / pages_per_split). */
+ * partials never depend on its batch): pages_per_split = 1 for npages <= 16,
+ * else max(2, ceil(npages / 32)); nsplit = ceil(npages / pages_per_split). */
 int32_t tfpa_pages_per_split(int32_t seq_len);
 int32_t tfpa_num_splits(int32_t seq_len);
 

@@ -271,10 +271,11 @@ class Scratch(_Cached):
 
 
 def make_scratch(cap_rows: int, hq: int, max_splits: int = MAX_SPLITS, device="cuda",
-                 fused_merge: bool = True) -> Scratch:
-    """Scratch for cap_rows rows; with fused_merge (the default) it carries
-    the zeroed arrival counters that let tfpa_decode merge inside the
-    partial kernel."""
+                 fused_merge: bool = False) -> Scratch:
+    """Scratch for cap_rows rows; with fused_merge it carries the zeroed
+    arrival counters that let tfpa_decode merge short streams inside the
+    partial kernel (measured slower than the separate merge launch, so off
+    by default)."""
     import torch
     o = torch.empty(cap_rows * hq * max_splits * HEAD_DIM, dtype=torch.float32, device=device)
     ml = torch.empty(cap_rows * hq * max_splits * 2, dtype=torch.float32, device=device)

@@ -336,8 +336,11 @@ struct Sink {
 
 }  // namespace
 
+// One page per split up to 16 pages (a short stream's keys spread over as
+// many CTAs as it has pages), then at least two.
 extern "C" int32_t tfpa_pages_per_split(int32_t seq_len) {
   const int32_t np = pages_of(std::max(seq_len, 1));
+  if (np <= 16) return 1;
   return std::max<int32_t>(2, (np + kMaxSplits - 1) / kMaxSplits);
 }
 
@@ -480,7 +483,7 @@ void plan_cta_ranges(DecodeParams& p, int nr, int G, bool fp8, int grid) {
   while (b <= grid) p.d.cta_item0[b++] = n_items;
 }
 
-// Streams of at most this many splits (2,048 positions) are merged inside
+// Streams of at most this many splits (1,024 positions) are merged inside
 // the partial kernel when the scratch has arrival counters.
 constexpr int kFusedMergeMaxSplits = 4;
 

@@ -113,7 +113,7 @@ class GpuCase:
             qb = qb[rows]
         return _dev(qb.view(np.int16), torch.bfloat16)
 
-    def decode(self, q, row_seg, row_pos, cap_rows=128, segs=None, lse=True, fused=True):
+    def decode(self, q, row_seg, row_pos, cap_rows=128, segs=None, lse=True, fused=False):
         rows = len(row_seg)
         out = torch.empty(rows, self.w.hq, self.w.d, dtype=torch.bfloat16, device="cuda")
         l = torch.empty(rows, self.w.hq, dtype=torch.float32, device="cuda") if lse else None
@@ -123,7 +123,7 @@ class GpuCase:
         torch.cuda.synchronize()
         return out, l
 
-    def decode_tree(self, q, row_seg, row_pos, row_anc, cap_rows=128, lse=True, fused=True):
+    def decode_tree(self, q, row_seg, row_pos, row_anc, cap_rows=128, lse=True, fused=False):
         rows = len(row_seg)
         anc = torch.from_numpy(np.ascontiguousarray(np.asarray(row_anc, np.uint64))
                                .view(np.int64)).cuda()

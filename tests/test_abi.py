@@ -31,9 +31,10 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_split_policy_depends_on_length_only():
-    for L, pps, ns in [(1, 2, 1), (256, 2, 1), (257, 2, 1), (513, 2, 2), (1000, 2, 2),
-                       (8192, 2, 16), (8193, 2, 17), (16384, 2, 32), (16385, 3, 22),
-                       (65536, 8, 32), (262144, 32, 32), (109000, 14, 31)]:
+    for L, pps, ns in [(1, 1, 1), (256, 1, 1), (257, 1, 2), (513, 1, 3), (1000, 1, 4),
+                       (4096, 1, 16), (4097, 2, 9), (8192, 2, 16), (8193, 2, 17),
+                       (16384, 2, 32), (16385, 3, 22), (65536, 8, 32), (262144, 32, 32),
+                       (109000, 14, 31)]:
         assert B.tfpa_pages_per_split(L) == pps, L
         assert B.tfpa_num_splits(L) == ns, L
     for L in range(1, 300000, 997):
@@ -399,9 +400,9 @@ def test_arrival_counters_fold_the_merge_into_the_partial_launch():
     streams, tree rows, device-mode plans and slices with tensor-core verify
     rows keep the separate merge."""
     c = _cache()
-    short = [B.Seg(2048, page_table=3 * FAKE), B.Seg(700, k_slab=8 * FAKE, v_slab=9 * FAKE,
+    short = [B.Seg(1024, page_table=3 * FAKE), B.Seg(700, k_slab=8 * FAKE, v_slab=9 * FAKE,
                                                      slab_cap=768)]
-    long = [B.Seg(2049, page_table=3 * FAKE)] + short[1:]
+    long = [B.Seg(1025, page_table=3 * FAKE)] + short[1:]
     plain = B.Scratch(5 * FAKE, 6 * FAKE, 16)
     counted = B.Scratch(5 * FAKE, 6 * FAKE, 16, 32, 10 * FAKE)
 
@@ -414,21 +415,21 @@ def test_arrival_counters_fold_the_merge_into_the_partial_launch():
         return [r["kind"] for r in rec]
 
     rs = np.array([0, 1])
-    assert kinds(plain, short, rs, np.array([2047, 699])) == ["partial", "merge"]
-    assert kinds(counted, short, rs, np.array([2047, 699])) == ["partial"]
-    assert kinds(counted, long, rs, np.array([2048, 699])) == ["partial", "merge"]
-    assert kinds(counted, short, rs, np.array([2047, 699]), anc=11 * FAKE) == ["partial", "merge"]
+    assert kinds(plain, short, rs, np.array([1023, 699])) == ["partial", "merge"]
+    assert kinds(counted, short, rs, np.array([1023, 699])) == ["partial"]
+    assert kinds(counted, long, rs, np.array([1024, 699])) == ["partial", "merge"]
+    assert kinds(counted, short, rs, np.array([1023, 699]), anc=11 * FAKE) == ["partial", "merge"]
     # 20 rows of stream 0 (verify path) + 1 of stream 1, 16-row slices
     rs = np.array([0] * 20 + [1])
-    rp = np.array(list(range(2028, 2048)) + [699])
+    rp = np.array(list(range(1004, 1024)) + [699])
     assert kinds(counted, short, rs, rp) == ["verify", "merge", "partial", "verify", "merge"]
-    rs, rp = np.array([0] * 3 + [1]), np.array([2045, 2046, 2047, 699])
+    rs, rp = np.array([0] * 3 + [1]), np.array([1021, 1022, 1023, 699])
     assert kinds(counted, short, rs, rp) == ["partial"]
     # a plan in device mode keeps the merge launch
     torch = pytest.importorskip("torch")
     plan = B.Plan()
     plan.set_device(torch.zeros(1 << 16, dtype=torch.uint8))
     with B.record_launches() as rec:
-        plan.decode(c, short, 4 * FAKE, np.array([0, 1]), np.array([2047, 699]), 0.088, counted,
+        plan.decode(c, short, 4 * FAKE, np.array([0, 1]), np.array([1023, 699]), 0.088, counted,
                     7 * FAKE)
     assert [r["kind"] for r in rec] == ["partial", "merge"]

@@ -60,7 +60,7 @@ def test_mixed_slices_keep_the_separate_merge_where_verify_rows_run():
 def test_counters_return_to_zero_and_repeat_calls_agree():
     w = wl.small("batched_decode")
     g = GpuCase(w)
-    sc = B.make_scratch(8, w.hq)
+    sc = B.make_scratch(8, w.hq, fused_merge=True)
     out = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16, device="cuda")
     first = None
     for _ in range(5):
