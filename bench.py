@@ -329,7 +329,8 @@ def time_e2e_graph(w, torch, B, ctx, steps, warmup):
     for _ in range(steps):
         graph.replay()
         s.synchronize()
-    return (time.perf_counter() - t0) / steps
+    dt = (time.perf_counter() - t0) / steps
+    return dt, graph_device_us(torch, graph, steps)
 
 
 def e2e_buffers(w, torch, nst):
@@ -408,25 +409,40 @@ def time_e2e_device(w, torch, B, ctx, steps, warmup):
     """The decode loop of time_e2e_planned with the plan in device mode
     (tfpa_plan_set_device): each step is still planned anew with lengths one
     position longer, but its launches read their lengths, splits and CTA
-    ranges from a device buffer, so one captured CUDA graph per packed-data
-    buffer (input copy, copy of the packed data, the planned launches, output
-    copy) is replayed every step.  Two pinned packed-data buffers alternate:
+    ranges from a device buffer, so one captured CUDA graph per pinned input
+    buffer (one copy of the step's inputs and packed data, the planned
+    launches, the output copy) is replayed every step.  The packed data
+    (tfpa_plan_dyn_pack) sits right after the q / K / V rows in the same
+    pinned buffer, so one copy carries both.  Two pinned buffers alternate:
     while the GPU runs step i the host plans step i + 1 and packs it into the
     other buffer, then waits for step i's output and replays.
     Returns (s per step, KV + Q + O bytes per step, host us per replay,
-    host us planning and packing a step, packed bytes copied per step)."""
+    host us planning and packing a step, packed bytes copied per step,
+    device us per replay)."""
     cache, segs, _, sc, out = ctx
     nst = len(w.streams)
     tab = B.SegTable(segs)
-    h_in, d_in, dq, dk, dv, hout = e2e_buffers(w, torch, nst)
+    nq, nk = w.rows * w.hq * 128, nst * w.hkv * 128
+    in_bytes = (nq + 2 * nk) * 2                   # q, new K, new V (bf16)
+    dyn_cap = 1 << 15
+    rows = torch.randn(nq + 2 * nk).to(torch.bfloat16)
+    h = []
+    for _ in range(2):
+        hb = torch.zeros(in_bytes + dyn_cap, dtype=torch.uint8).pin_memory()
+        hb[:in_bytes].view(torch.bfloat16).copy_(rows)
+        h.append(hb)
+    d = torch.empty_like(h[0], device="cuda")
+    d_rows = d[:in_bytes].view(torch.bfloat16)
+    dq = d_rows[:nq].view(w.rows, w.hq, 128)
+    dk = d_rows[nq:nq + nk].view(nst, w.hkv, 128)
+    dv = d_rows[nq + nk:].view(nst, w.hkv, 128)
+    hout = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16).pin_memory()
     sidx = np.arange(nst, dtype=np.int32)
     s = torch.cuda.current_stream()
     L = w.streams[0].seq_len
     total = warmup + steps
-    dyn = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
-    hdyn = [torch.zeros(1 << 16, dtype=torch.uint8).pin_memory() for _ in range(2)]
     plan = B.Plan()
-    plan.set_device(dyn)
+    plan.set_device(d[in_bytes:])                  # in_bytes is a multiple of 16
     ev = torch.cuda.Event()
     b = 2 if w.kv_dtype == "bf16" else 1
     t_launch, t_plan = [], []
@@ -440,12 +456,12 @@ def time_e2e_device(w, torch, B, ctx, steps, warmup):
         plan.clear()
         plan.write_kv(cache, tab, dk, dv, sidx, rp)
         plan.decode(cache, tab, dq, sidx, rp, w.softmax_scale, sc, out)
-        plan.pack(hdyn[i % 2])
+        plan.pack(h[i % 2][in_bytes:])
         return n
 
     n = plan_step(0)
     nb, shape = plan.dyn_bytes(), plan.shape()
-    dyn[:nb].copy_(hdyn[0][:nb], non_blocking=True)
+    d[:in_bytes + nb].copy_(h[0][:in_bytes + nb], non_blocking=True)
     plan.launch()                                  # sets the kernels up before capture
     torch.cuda.synchronize()
     graphs = []
@@ -455,8 +471,7 @@ def time_e2e_device(w, torch, B, ctx, steps, warmup):
         cap.wait_stream(s)
         with torch.cuda.stream(cap):
             with torch.cuda.graph(g, stream=cap):
-                d_in.copy_(h_in, non_blocking=True)
-                dyn[:nb].copy_(hdyn[k][:nb], non_blocking=True)
+                d[:in_bytes + nb].copy_(h[k][:in_bytes + nb], non_blocking=True)
                 plan.launch(cap)
                 hout.copy_(out, non_blocking=True)
         s.wait_stream(cap)
@@ -480,11 +495,28 @@ def time_e2e_device(w, torch, B, ctx, steps, warmup):
             assert plan.shape() == shape and plan.dyn_bytes() == nb
         ev.synchronize()
     dt = (time.perf_counter() - t0) / steps
+    dev_us = graph_device_us(torch, graphs[(total - 1) % 2], steps)
     for j, st in enumerate(w.streams):
         tab.set_seq_len(j, st.seq_len)
     qo = w.rows * w.hq * 128 * 2 * 2
     return (dt, kvb / steps + qo, statistics.median(t_launch[warmup:]), statistics.median(t_plan),
-            nb)
+            nb, dev_us)
+
+
+def graph_device_us(torch, graph, n):
+    """Device time of one replay of `graph` (its copies included): n replays
+    back to back between CUDA events, enqueued during a GPU sleep."""
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    graph.replay()
+    torch.cuda.synchronize()
+    host_cover(torch)
+    e0.record(s)
+    for _ in range(n):
+        graph.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / n
 
 
 def time_e2e_calls(w, torch, B, ctx, steps, warmup, in_flight=1):
@@ -927,7 +959,7 @@ def main():
         e2e_plan = time_e2e_planned(w, torch, B, ctx, n_e2e, args.warmup)
         e2e_plan = (max_over_ranks(dist, torch, e2e_plan[0]),) + tuple(e2e_plan[1:])
         e2e_plan_aa = time_e2e_planned(w, torch, B, ctx, n_e2e, args.warmup)
-        e2e_graph_s = time_e2e_graph(w, torch, B, ctx, n_e2e, args.warmup)
+        e2e_graph_s, e2e_graph_dev_us = time_e2e_graph(w, torch, B, ctx, n_e2e, args.warmup)
         e2e_dev = time_e2e_device(w, torch, B, ctx, n_e2e, args.warmup)
         e2e_dev = (max_over_ranks(dist, torch, e2e_dev[0]),) + tuple(e2e_dev[1:])
         e2e_dev_aa = time_e2e_device(w, torch, B, ctx, n_e2e, args.warmup)
@@ -1057,6 +1089,7 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": world * e2e_dev[1] / e2e_dev[0] / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": e2e[4] + e2e_dev[4], "d2h_bytes_per_step": e2e[5],
+                "h2d_copies_per_step": 1,
                 "ms_per_step": e2e_dev[0] * 1e3, "vs_device_step": e2e_dev[0] * 1e3 / step_ms,
                 "host_us_per_call": {"graph_replay": e2e_dev[2],
                                      "planning_and_packing_a_step_overlapped": e2e_dev[3]},
@@ -1065,12 +1098,13 @@ def main():
                        "time: each stream one position longer every step (%d..%d), every step "
                        "planned anew (tfpa_plan_write_kv + tfpa_plan_decode, plan in device "
                        "mode) and packed (tfpa_plan_dyn_pack) while the previous step runs; per "
-                       "step one replay of a CUDA graph captured once per packed-data buffer: "
-                       "pinned input copy (q + new K/V rows), copy of the packed lengths/splits/"
-                       "CTA ranges, the planned launches (tfpa_plan_launch), output copy; the "
+                       "step one replay of a CUDA graph captured once per pinned input buffer: "
+                       "one copy of q, the new K/V rows and the packed lengths/splits/CTA "
+                       "ranges, the planned launches (tfpa_plan_launch), output copy; the "
                        "host waits for the output before the next step; host times are host "
                        "clock, median" % (w.streams[0].seq_len - n_e2e + 1, w.streams[0].seq_len),
                 "packed_bytes_per_step": e2e_dev[4],
+                "graph_device_us_per_step": e2e_dev[5],
                 "planned_calls": {
                     "value": world * e2e_plan[1] / e2e_plan[0] / 1e9, "unit": "GB/s",
                     "ms_per_step": e2e_plan[0] * 1e3,
@@ -1097,6 +1131,7 @@ def main():
         "e2e_graph_replay": {
             "value": world * (kv + qo) / e2e_graph_s / 1e9, "unit": "GB/s",
             "ms_per_step": e2e_graph_s * 1e3,
+            "graph_device_us_per_step": e2e_graph_dev_us,
             "how": "upper bound: one step (copies, 3 kernels) captured once as a CUDA graph "
                    "and replayed with its lengths frozen; no host planning per step"},
         "aa_repeat": {"ms_per_step": [step_ms, step_ms_aa],

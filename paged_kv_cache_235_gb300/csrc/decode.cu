@@ -79,8 +79,22 @@ __device__ __forceinline__ int mtiles_of(const RunInfo& ru, int group) {
   return (ru.nrows * group + 15) >> 4;
 }
 
-__device__ __forceinline__ Item item_of(const DecodeParams& p, const DecodeDyn& D, int it) {
-  int r = 0;
+// The run holding item `it`, by binary search over the runs' first items
+// (a few dependent loads when the runs sit in device memory).
+__device__ __forceinline__ int run_of(const DecodeDyn& D, int it) {
+  int lo = 0, hi = D.nruns - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (D.runs[mid].item0 <= it) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Work item `it`; r is the run of an earlier item of this CTA (or of `it`)
+// and becomes `it`'s: a CTA walks its items in order, so the run only moves
+// forward.
+__device__ __forceinline__ Item item_of(const DecodeParams& p, const DecodeDyn& D, int it,
+                                        int& r) {
   while (r + 1 < D.nruns && D.runs[r + 1].item0 <= it) ++r;
   const RunInfo& ru = D.runs[r];
   int local = it - ru.item0;
@@ -121,9 +135,10 @@ __device__ void producer(const DecodeParams& p, const DecodeDyn& D, uint8_t* sta
   if ((threadIdx.x & 31) != 0) return;
   int ib, ie;
   cta_items(D, ib, ie);
+  int rh = ib < ie ? run_of(D, ib) : 0;   // run of the current item
   uint32_t stage = 0;
   for (int it = ib; it < ie; ++it) {
-    const Item x = item_of(p, D, it);
+    const Item x = item_of(p, D, it, rh);
     const RunInfo& ru = D.runs[x.run];
     int klo, khi;
     item_keys(p, D, x, klo, khi);
@@ -437,6 +452,7 @@ __device__ void consumer(const DecodeParams& p, const DecodeDyn& D, uint8_t* sta
   uint32_t stage = 0;
   int ib, ie;
   cta_items(D, ib, ie);
+  int rh = ib < ie ? run_of(D, ib) : 0;   // run of the current item
   int q_run = -1, q_g = -1, q_mt = -1;     // the m-tile whose query is loaded
   int lim[2] = {-1, -1};
   uint64_t anc[2] = {~0ull, ~0ull};
@@ -446,7 +462,7 @@ __device__ void consumer(const DecodeParams& p, const DecodeDyn& D, uint8_t* sta
   int tree_low = INT_MAX;     // keys from here on may be hidden by an ancestor mask
 
   for (int it = ib; it < ie; ++it) {
-    const Item x = item_of(p, D, it);
+    const Item x = item_of(p, D, it, rh);
     const RunInfo& ru = D.runs[x.run];
     int klo, khi;
     item_keys(p, D, x, klo, khi);
@@ -630,9 +646,10 @@ __device__ void combiner(const DecodeParams& p, const DecodeDyn& D, uint32_t tme
   const int gq = lane >> 2, c = lane & 3;
   int ib, ie;
   cta_items(D, ib, ie);
+  int rh = ib < ie ? run_of(D, ib) : 0;   // run of the current item
   const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
   for (int it = ib; it < ie; ++it) {
-    const Item x = item_of(p, D, it);
+    const Item x = item_of(p, D, it, rh);
     const RunInfo& ru = D.runs[x.run];
     const int nq = ru.nrows * p.group;
     const int rel = it - ib;
@@ -835,7 +852,18 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
   const int row = wid / p.hq;
   const int h = wid - row * p.hq;
   int ri = 0;
-  while (ri + 1 < D.nruns && D.runs[ri + 1].row0 <= row) ++ri;
+  if (DEV) {
+    // runs in device memory: 32 runs' first rows per round of loads; the
+    // row's run is the last whose first row is at or before it
+    for (int base = 0; base < D.nruns; base += 32) {
+      const int i = base + lane;
+      const unsigned m = __ballot_sync(0xffffffffu, i < D.nruns && D.runs[i].row0 <= row);
+      if (m) ri = base + 31 - __clz(m);
+      if (m != 0xffffffffu) break;
+    }
+  } else {
+    while (ri + 1 < D.nruns && D.runs[ri + 1].row0 <= row) ++ri;
+  }
   const int nsplit = D.runs[ri].nsplit;
   const size_t slot0 = ((size_t)row * p.hq + h) * p.max_splits;
   // Every slot below nsplit was written by the partial kernel (an empty split

@@ -65,11 +65,25 @@ __global__ void __launch_bounds__(256) write_kv_kernel(const __grid_constant__ W
   const WriteDyn& D = DEV ? *p.dyn : p.d;
   const int gid = blockIdx.x * 16 + (threadIdx.x >> 4);  // (row, head) pair
   const int t = threadIdx.x & 15;                          // 8-element slice
-  if (gid >= D.rows * p.hkv) return;
+  const bool live = gid < D.rows * p.hkv;
   const int row = gid / p.hkv;
   const int g = gid - row * p.hkv;
   int ri = 0;
-  while (ri + 1 < D.nruns && D.runs[ri + 1].row0 <= row) ++ri;
+  if (DEV) {
+    // runs in device memory: each 16-thread group reads 16 runs' first
+    // rows per round (every lane of the warp takes part in the ballots);
+    // the row's run is the last whose first row is at or before it
+    const int sh = threadIdx.x & 16;
+    for (int base = 0; base < D.nruns; base += 16) {
+      const int i = base + t;
+      const unsigned m =
+          (__ballot_sync(0xffffffffu, i < D.nruns && D.runs[i].row0 <= row) >> sh) & 0xFFFFu;
+      if (m) ri = base + 31 - __clz(m);
+    }
+  } else if (live) {
+    while (ri + 1 < D.nruns && D.runs[ri + 1].row0 <= row) ++ri;
+  }
+  if (!live) return;
   const WriteRun& run = D.runs[ri];
   const int pos = run.pos0 + (row - run.row0);
 
