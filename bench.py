@@ -330,7 +330,7 @@ def time_e2e_graph(w, torch, B, ctx, steps, warmup):
         graph.replay()
         s.synchronize()
     dt = (time.perf_counter() - t0) / steps
-    return dt, graph_device_us(torch, graph, steps)
+    return dt, graph_device_us(torch, graph.replay, steps)
 
 
 def e2e_buffers(w, torch, nst):
@@ -406,19 +406,20 @@ def time_e2e_planned(w, torch, B, ctx, steps, warmup):
 
 
 def time_e2e_device(w, torch, B, ctx, steps, warmup):
-    """The decode loop of time_e2e_planned with the plan in device mode
+    """The decode loop of time_e2e_planned with plans in device mode
     (tfpa_plan_set_device): each step is still planned anew with lengths one
     position longer, but its launches read their lengths, splits and CTA
-    ranges from a device buffer, so one captured CUDA graph per pinned input
-    buffer (one copy of the step's inputs and packed data, the planned
-    launches, the output copy) is replayed every step.  The packed data
-    (tfpa_plan_dyn_pack) sits right after the q / K / V rows in the same
-    pinned buffer, so one copy carries both.  Two pinned buffers alternate:
-    while the GPU runs step i the host plans step i + 1 and packs it into the
-    other buffer, then waits for step i's output and replays.
-    Returns (s per step, KV + Q + O bytes per step, host us per replay,
-    host us planning and packing a step, packed bytes copied per step,
-    device us per replay)."""
+    ranges from a device buffer, so each plan is captured once as a CUDA
+    graph (tfpa_plan_capture: one copy of the step's inputs and packed data
+    from pinned memory, the planned launches, the output copy) and replayed
+    (tfpa_plan_replay) step after step.  The packed data (tfpa_plan_dyn_pack)
+    sits right after the q / K / V rows in the same pinned buffer, so one
+    copy carries both.  Two plans with their own pinned buffers alternate:
+    while the GPU runs step i the host plans step i + 1 on the other plan
+    and packs it into that plan's buffer, then waits for step i's output and
+    replays.  Returns (s per step, KV + Q + O bytes per step, host us per
+    replay, host us planning and packing a step, packed bytes copied per
+    step, device us per replay)."""
     cache, segs, _, sc, out = ctx
     nst = len(w.streams)
     tab = B.SegTable(segs)
@@ -439,43 +440,39 @@ def time_e2e_device(w, torch, B, ctx, steps, warmup):
     hout = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16).pin_memory()
     sidx = np.arange(nst, dtype=np.int32)
     s = torch.cuda.current_stream()
+    sh = s.cuda_stream
     L = w.streams[0].seq_len
     total = warmup + steps
-    plan = B.Plan()
-    plan.set_device(d[in_bytes:])                  # in_bytes is a multiple of 16
+    plans = [B.Plan(), B.Plan()]
+    for pl in plans:
+        pl.set_device(d[in_bytes:])                # in_bytes is a multiple of 16
     ev = torch.cuda.Event()
     b = 2 if w.kv_dtype == "bf16" else 1
     t_launch, t_plan = [], []
     kvb = 0
 
     def plan_step(i):
+        pl = plans[i % 2]
         n = L - total + 1 + i
         for j in range(nst):
             tab.set_seq_len(j, n)
         rp = np.full(nst, n - 1, np.int32)
-        plan.clear()
-        plan.write_kv(cache, tab, dk, dv, sidx, rp)
-        plan.decode(cache, tab, dq, sidx, rp, w.softmax_scale, sc, out)
-        plan.pack(h[i % 2][in_bytes:])
+        pl.clear()
+        pl.write_kv(cache, tab, dk, dv, sidx, rp)
+        pl.decode(cache, tab, dq, sidx, rp, w.softmax_scale, sc, out)
+        pl.pack(h[i % 2][in_bytes:])
         return n
 
+    plan_step(1)
     n = plan_step(0)
-    nb, shape = plan.dyn_bytes(), plan.shape()
+    nb = plans[0].dyn_bytes()
     d[:in_bytes + nb].copy_(h[0][:in_bytes + nb], non_blocking=True)
-    plan.launch()                                  # sets the kernels up before capture
+    plans[0].launch()                              # sets the kernels up before capture
     torch.cuda.synchronize()
-    graphs = []
     cap = torch.cuda.Stream()
     for k in range(2):
-        g = torch.cuda.CUDAGraph()
-        cap.wait_stream(s)
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(g, stream=cap):
-                d[:in_bytes + nb].copy_(h[k][:in_bytes + nb], non_blocking=True)
-                plan.launch(cap)
-                hout.copy_(out, non_blocking=True)
-        s.wait_stream(cap)
-        graphs.append(g)
+        plans[k].capture(before=[(d, h[k], in_bytes + nb)], after=[(hout, out, hout.numel() * 2)],
+                         stream=cap)
     torch.cuda.synchronize()
     t0 = None
     for i in range(total):
@@ -483,7 +480,7 @@ def time_e2e_device(w, torch, B, ctx, steps, warmup):
             torch.cuda.synchronize()
             t0 = time.perf_counter()
         a = time.perf_counter_ns()
-        graphs[i % 2].replay()
+        plans[i % 2].replay(sh)
         t_launch.append((time.perf_counter_ns() - a) / 1e3)
         ev.record(s)
         if i >= warmup:
@@ -492,10 +489,10 @@ def time_e2e_device(w, torch, B, ctx, steps, warmup):
             a = time.perf_counter_ns()
             n = plan_step(i + 1)                 # while the GPU runs step i
             t_plan.append((time.perf_counter_ns() - a) / 1e3)
-            assert plan.shape() == shape and plan.dyn_bytes() == nb
         ev.synchronize()
     dt = (time.perf_counter() - t0) / steps
-    dev_us = graph_device_us(torch, graphs[(total - 1) % 2], steps)
+    last = plans[(total - 1) % 2]
+    dev_us = graph_device_us(torch, lambda: last.replay(sh), steps)
     for j, st in enumerate(w.streams):
         tab.set_seq_len(j, st.seq_len)
     qo = w.rows * w.hq * 128 * 2 * 2
@@ -503,17 +500,18 @@ def time_e2e_device(w, torch, B, ctx, steps, warmup):
             nb, dev_us)
 
 
-def graph_device_us(torch, graph, n):
-    """Device time of one replay of `graph` (its copies included): n replays
-    back to back between CUDA events, enqueued during a GPU sleep."""
+def graph_device_us(torch, replay, n):
+    """Device time of one call of `replay` (a graph replay, its copies
+    included): n calls back to back between CUDA events, enqueued during a
+    GPU sleep."""
     s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    graph.replay()
+    replay()
     torch.cuda.synchronize()
     host_cover(torch)
     e0.record(s)
     for _ in range(n):
-        graph.replay()
+        replay()
     e1.record(s)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) * 1e3 / n
@@ -1091,14 +1089,15 @@ def main():
                 "h2d_bytes_per_step": e2e[4] + e2e_dev[4], "d2h_bytes_per_step": e2e[5],
                 "h2d_copies_per_step": 1,
                 "ms_per_step": e2e_dev[0] * 1e3, "vs_device_step": e2e_dev[0] * 1e3 / step_ms,
-                "host_us_per_call": {"graph_replay": e2e_dev[2],
+                "host_us_per_call": {"tfpa_plan_replay": e2e_dev[2],
                                      "planning_and_packing_a_step_overlapped": e2e_dev[3]},
                 "steps": n_e2e,
                 "how": "a decode loop through the public API with host buffers, one step at a "
                        "time: each stream one position longer every step (%d..%d), every step "
-                       "planned anew (tfpa_plan_write_kv + tfpa_plan_decode, plan in device "
-                       "mode) and packed (tfpa_plan_dyn_pack) while the previous step runs; per "
-                       "step one replay of a CUDA graph captured once per pinned input buffer: "
+                       "planned anew (tfpa_plan_write_kv + tfpa_plan_decode, two plans in device "
+                       "mode, alternating) and packed (tfpa_plan_dyn_pack) while the previous "
+                       "step runs; per step one tfpa_plan_replay of the plan's CUDA graph "
+                       "(tfpa_plan_capture, once per plan): "
                        "one copy of q, the new K/V rows and the packed lengths/splits/CTA "
                        "ranges, the planned launches (tfpa_plan_launch), output copy; the "
                        "host waits for the output before the next step; host times are host "

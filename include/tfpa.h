@@ -373,6 +373,34 @@ size_t tfpa_plan_dyn_bytes(const tfpa_plan* plan);
 int tfpa_plan_dyn_pack(const tfpa_plan* plan, void* host, size_t bytes);
 uint64_t tfpa_plan_shape(const tfpa_plan* plan);
 
+/* A plan as one CUDA graph, owned by the plan.
+ * tfpa_plan_capture(plan, before, nbefore, after, nafter, stream) captures,
+ *   on `stream` (a created stream: not NULL, not cudaStreamLegacy; nothing
+ *   else may be enqueued on it meanwhile), the copies `before` (each a
+ *   cudaMemcpyAsync of `bytes` from src to dst, kind inferred: e.g. a step's
+ *   inputs and, in device mode, its packed data from pinned host memory),
+ *   the plan's launches and the copies `after` (e.g. the output to pinned
+ *   host memory), instantiates the graph and keeps it with the plan's shape
+ *   (tfpa_plan_shape), replacing an earlier one.  The copies read and write
+ *   their buffers when the graph runs.  TFPA_EINVAL for an empty plan, bad
+ *   copies or stream; TFPA_ECUDA if capture or instantiation fails (the
+ *   plan keeps its earlier graph).  Launch the plan once before its first
+ *   capture on a device, so that kernel attributes are set outside capture.
+ * tfpa_plan_replay(plan, stream): launches the graph on `stream`.
+ *   TFPA_EINVAL if nothing was captured or the plan's shape has changed
+ *   since (re-planned with other rows, streams or pointers: capture again).
+ *   In device mode a loop re-plans each step (tfpa_plan_clear + planning
+ *   calls), packs into the host buffer the graph's first copy reads, and
+ *   replays.  The graph is destroyed with the plan; tfpa_plan_clear keeps it. */
+typedef struct {
+  void* dst;
+  const void* src;
+  size_t bytes;
+} tfpa_copy;
+int tfpa_plan_capture(tfpa_plan* plan, const tfpa_copy* before, int32_t nbefore,
+                      const tfpa_copy* after, int32_t nafter, cudaStream_t stream);
+int tfpa_plan_replay(const tfpa_plan* plan, cudaStream_t stream);
+
 /* Causal prompt-chunk attention over the paged prefix, one pass with online
  * softmax on tcgen05/TMEM tiles (PR #2011, "hpattn_p256_kernel": page size a
  * constant 256, one page lookup per key tile).  max_rows_per_launch > 0 runs

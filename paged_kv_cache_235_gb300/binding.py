@@ -33,7 +33,7 @@ EXPORTS = ("tfpa_pages_per_split", "tfpa_num_splits", "tfpa_write_kv", "tfpa_dec
            "tfpa_stage_pages", "tfpa_save_kv", "tfpa_restore_kv", "tfpa_plan_create",
            "tfpa_plan_destroy", "tfpa_plan_clear", "tfpa_plan_launches", "tfpa_plan_write_kv",
            "tfpa_plan_decode", "tfpa_plan_launch", "tfpa_plan_set_device", "tfpa_plan_dyn_bytes",
-           "tfpa_plan_dyn_pack", "tfpa_plan_shape")
+           "tfpa_plan_dyn_pack", "tfpa_plan_shape", "tfpa_plan_capture", "tfpa_plan_replay")
 
 
 class TfpaError(RuntimeError):
@@ -60,6 +60,10 @@ class tfpa_scratch(ctypes.Structure):
     _fields_ = [("part_o", ctypes.c_void_p), ("part_ml", ctypes.c_void_p),
                 ("cap_rows", ctypes.c_int32), ("max_splits", ctypes.c_int32),
                 ("arrive", ctypes.c_void_p)]
+
+
+class tfpa_copy(ctypes.Structure):
+    _fields_ = [("dst", ctypes.c_void_p), ("src", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
 
 
 class tfpa_launch_record(ctypes.Structure):
@@ -153,6 +157,10 @@ def lib():
         L.tfpa_plan_dyn_pack.restype = ctypes.c_int
         L.tfpa_plan_shape.argtypes = [vp]
         L.tfpa_plan_shape.restype = ctypes.c_uint64
+        L.tfpa_plan_capture.argtypes = [vp, P(tfpa_copy), i32, P(tfpa_copy), i32, vp]
+        L.tfpa_plan_capture.restype = ctypes.c_int
+        L.tfpa_plan_replay.argtypes = [vp, vp]
+        L.tfpa_plan_replay.restype = ctypes.c_int
         L.tfpa_set_launch_hook.argtypes = [HOOK, vp, ctypes.c_int]
         L.tfpa_set_launch_hook.restype = None
         L.tfpa_strerror.argtypes = [ctypes.c_int]
@@ -534,6 +542,22 @@ class Plan:
 
     def shape(self) -> int:
         return int(lib().tfpa_plan_shape(self._p))
+
+    def capture(self, before=(), after=(), stream=None) -> None:
+        """tfpa_plan_capture: `before` / `after` are (dst, src, nbytes)
+        copies (tensors or addresses) around the plan's launches, captured
+        with them as one CUDA graph on `stream` (a created stream)."""
+        def arr(copies):
+            a = (tfpa_copy * max(1, len(copies)))()
+            for i, (dst, src, n) in enumerate(copies):
+                a[i] = tfpa_copy(_ptr(dst), _ptr(src), int(n))
+            return a
+        b, a = arr(before), arr(after)
+        _check(lib().tfpa_plan_capture(self._p, b, len(before), a, len(after), _stream(stream)),
+               "tfpa_plan_capture")
+
+    def replay(self, stream=None) -> None:
+        _check(lib().tfpa_plan_replay(self._p, _stream(stream)), "tfpa_plan_replay")
 
     def __del__(self):
         if getattr(self, "_p", None):

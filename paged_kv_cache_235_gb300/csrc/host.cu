@@ -264,6 +264,12 @@ struct tfpa_plan {
   uint8_t* dyn_base = nullptr;   // DEVICE, or nullptr: parameter mode
   size_t dyn_cap = 0;
   size_t dyn_used = 0;           // bytes of dyn_base handed out
+  cudaGraphExec_t exec = nullptr;   // tfpa_plan_capture's graph
+  uint64_t exec_shape = 0;          // the plan's shape when it was captured
+  bool captured = false;
+  ~tfpa_plan() {
+    if (exec) cudaGraphExecDestroy(exec);
+  }
 };
 
 namespace {
@@ -859,10 +865,18 @@ extern "C" int tfpa_plan_dyn_pack(const tfpa_plan* plan, void* host, size_t byte
 }
 
 namespace {
-// FNV-1a over a byte range.
+// A 64-bit hash of a byte range, eight bytes a step (multiply and
+// xor-shift; FNV-1a for the tail).
 uint64_t fnv1a(uint64_t h, const void* data, size_t n) {
   const uint8_t* b = static_cast<const uint8_t*>(data);
-  for (size_t i = 0; i < n; ++i) h = (h ^ b[i]) * 1099511628211ull;
+  size_t i = 0;
+  for (; i + 8 <= n; i += 8) {
+    uint64_t w;
+    std::memcpy(&w, b + i, 8);
+    h = (h ^ w) * 0x9E3779B97F4A7C15ull;
+    h ^= h >> 29;
+  }
+  for (; i < n; ++i) h = (h ^ b[i]) * 1099511628211ull;
   return h;
 }
 // A launch's parameters without its dynamic data.
@@ -889,6 +903,59 @@ extern "C" uint64_t tfpa_plan_shape(const tfpa_plan* plan) {
     }
   }
   return h;
+}
+
+extern "C" int tfpa_plan_capture(tfpa_plan* plan, const tfpa_copy* before, int32_t nbefore,
+                                 const tfpa_copy* after, int32_t nafter, cudaStream_t stream) {
+  if (!plan || plan->entries.empty() || nbefore < 0 || nafter < 0 ||
+      (nbefore > 0 && !before) || (nafter > 0 && !after))
+    return TFPA_EINVAL;
+  for (int32_t i = 0; i < nbefore; ++i)
+    if (before[i].bytes && (!before[i].dst || !before[i].src)) return TFPA_EINVAL;
+  for (int32_t i = 0; i < nafter; ++i)
+    if (after[i].bytes && (!after[i].dst || !after[i].src)) return TFPA_EINVAL;
+  const uint64_t shape = tfpa_plan_shape(plan);
+  if (dry_run()) {
+    plan->exec_shape = shape;
+    plan->captured = true;
+    return TFPA_OK;
+  }
+  int e;
+  if ((e = check_device())) return e;
+  if (stream == nullptr || stream == cudaStreamLegacy) return TFPA_EINVAL;   // not capturable
+  if (cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+    return TFPA_ECUDA;
+  bool ok = true;
+  for (int32_t i = 0; ok && i < nbefore; ++i)
+    if (before[i].bytes)
+      ok = cudaMemcpyAsync(before[i].dst, before[i].src, before[i].bytes, cudaMemcpyDefault,
+                           stream) == cudaSuccess;
+  if (ok) ok = tfpa_plan_launch(plan, stream) == TFPA_OK;
+  for (int32_t i = 0; ok && i < nafter; ++i)
+    if (after[i].bytes)
+      ok = cudaMemcpyAsync(after[i].dst, after[i].src, after[i].bytes, cudaMemcpyDefault,
+                           stream) == cudaSuccess;
+  cudaGraph_t graph = nullptr;
+  const bool ended = cudaStreamEndCapture(stream, &graph) == cudaSuccess;
+  cudaGraphExec_t exec = nullptr;
+  ok = ok && ended && graph && cudaGraphInstantiate(&exec, graph, 0ull) == cudaSuccess;
+  if (graph) cudaGraphDestroy(graph);
+  if (!ok) {
+    cudaGetLastError();   // the failed call's error stays with this call
+    return TFPA_ECUDA;
+  }
+  if (plan->exec) cudaGraphExecDestroy(plan->exec);
+  plan->exec = exec;
+  plan->exec_shape = shape;
+  plan->captured = true;
+  return TFPA_OK;
+}
+
+extern "C" int tfpa_plan_replay(const tfpa_plan* plan, cudaStream_t stream) {
+  if (!plan || !plan->captured) return TFPA_EINVAL;
+  if (tfpa_plan_shape(plan) != plan->exec_shape) return TFPA_EINVAL;
+  if (dry_run()) return TFPA_OK;
+  return to_err(cudaGraphLaunch(plan->exec, stream));
 }
 
 namespace {

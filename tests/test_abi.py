@@ -433,3 +433,41 @@ def test_arrival_counters_fold_the_merge_into_the_partial_launch():
         plan.decode(c, short, 4 * FAKE, np.array([0, 1]), np.array([1023, 699]), 0.088, counted,
                     7 * FAKE)
     assert [r["kind"] for r in rec] == ["partial", "merge"]
+
+
+def test_plan_capture_and_replay_follow_the_shape():
+    """tfpa_plan_capture keeps the plan's shape; tfpa_plan_replay refuses a
+    plan that was never captured or whose shape has changed since, and
+    accepts a re-planned step of the same shape (dry run: no CUDA calls)."""
+    torch = pytest.importorskip("torch")
+    c = _cache()
+    sc = B.Scratch(5 * FAKE, 6 * FAKE, 16)
+    dyn = torch.zeros(1 << 16, dtype=torch.uint8)
+
+    def plan_at(plan, n, rows=1):
+        segs = [B.Seg(n, page_table=3 * FAKE)]
+        rs, rp = np.zeros(rows), np.arange(n - rows, n)
+        plan.clear()
+        plan.write_kv(c, segs, 4 * FAKE, 5 * FAKE, rs, rp)
+        plan.decode(c, segs, 4 * FAKE, rs, rp, 0.088, sc, 7 * FAKE)
+
+    plan = B.Plan()
+    plan.set_device(dyn)
+    with B.record_launches():
+        plan_at(plan, 3000)
+        with pytest.raises(B.TfpaError) as e:
+            plan.replay(stream=0)
+        assert e.value.code == B.TFPA_EINVAL
+        plan.capture(before=[(8 * FAKE, 9 * FAKE, 4096)], after=[(10 * FAKE, 7 * FAKE, 8192)],
+                     stream=0)
+        plan.replay(stream=0)
+        plan_at(plan, 3001)                       # one position longer: same shape
+        plan.replay(stream=0)
+        plan_at(plan, 3001, rows=2)               # another row: the graph no longer fits
+        with pytest.raises(B.TfpaError) as e:
+            plan.replay(stream=0)
+        assert e.value.code == B.TFPA_EINVAL
+        plan.clear()
+        with pytest.raises(B.TfpaError) as e:     # nothing to capture
+            plan.capture(stream=0)
+        assert e.value.code == B.TFPA_EINVAL

@@ -54,12 +54,14 @@ def test_planned_decode_loop_equals_direct_calls():
     assert int(ga.err.item()) == 0 and int(gb.err.item()) == 0
 
 
+@pytest.mark.parametrize("via", ["torch_graph", "plan_capture"])
 @pytest.mark.parametrize("name", ["batched_decode", "fp8_verify"])
-def test_device_mode_graph_replays_a_growing_decode_loop(name):
+def test_device_mode_graph_replays_a_growing_decode_loop(name, via):
     """A plan in device mode captured once as a CUDA graph (the copy of its
-    packed data, then its launches) and replayed step after step with the
-    lengths growing by one, across a split boundary, gives the bytes of the
-    direct calls at every step."""
+    packed data, then its launches; by torch's graph capture, or by
+    tfpa_plan_capture) and replayed step after step with the lengths growing
+    by one, across a split boundary, gives the bytes of the direct calls at
+    every step."""
     w = wl.small(name)
     nst = len(w.streams)
     L = min(st.seq_len for st in w.streams)
@@ -113,14 +115,18 @@ def test_device_mode_graph_replays_a_growing_decode_loop(name):
             dyn[:nb].copy_(hdyn[:nb], non_blocking=True)
             plan.launch()
             torch.cuda.synchronize()
-            graph = torch.cuda.CUDAGraph()
             cap = torch.cuda.Stream()
-            cap.wait_stream(s)
-            with torch.cuda.stream(cap):
-                with torch.cuda.graph(graph, stream=cap):
-                    dyn[:nb].copy_(hdyn[:nb], non_blocking=True)
-                    plan.launch(cap)
-            s.wait_stream(cap)
+            if via == "plan_capture":
+                plan.capture(before=[(dyn, hdyn, nb)], stream=cap)
+                graph = plan
+            else:
+                graph = torch.cuda.CUDAGraph()
+                cap.wait_stream(s)
+                with torch.cuda.stream(cap):
+                    with torch.cuda.graph(graph, stream=cap):
+                        dyn[:nb].copy_(hdyn[:nb], non_blocking=True)
+                        plan.launch(cap)
+                s.wait_stream(cap)
         else:
             assert plan.shape() == shape and plan.dyn_bytes() == nb, f"step {i}"
             graph.replay()
