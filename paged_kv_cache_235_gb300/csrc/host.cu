@@ -358,14 +358,15 @@ extern "C" int32_t tfpa_num_splits(int32_t seq_len) {
 
 namespace {
 
-// Splits of a run on the tensor-core verify path: at least 16 pages (4,096
-// keys, so a tile's fixed costs stay small against its key tiles) and at
-// most kMaxSplits per stream; never more splits than the decode path's, so
-// a scratch sized for decode holds them.  A function of the stream's length
-// only, like the decode splits.
+// Splits of a run on the tensor-core verify path: at least 24 pages (6,144
+// keys, so a tile's fixed costs stay small against its key tiles; 16 and 32
+// measured slower on 65,536-key trees) and at most kMaxSplits per stream;
+// never more splits than the decode path's, so a scratch sized for decode
+// holds them.  A function of the stream's length only, like the decode
+// splits.
 int32_t verify_pages_per_split(int32_t seq_len) {
   const int32_t np = pages_of(std::max(seq_len, 1));
-  return std::max<int32_t>(16, (np + kMaxSplits - 1) / kMaxSplits);
+  return std::max<int32_t>(24, (np + kMaxSplits - 1) / kMaxSplits);
 }
 int32_t verify_num_splits(int32_t seq_len) {
   const int32_t np = pages_of(std::max(seq_len, 1));

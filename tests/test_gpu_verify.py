@@ -22,11 +22,11 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 @pytest.mark.parametrize("paged", [(True, False), (False, True)])
 def test_several_splits_next_to_a_narrow_run(kv, paged):
-    # 9,000 keys: 36 pages, three verify splits of 16 pages; the 1-row run
-    # of stream 1 stays on the decode kernel in the same call
-    lengths = [9000, 5000]
+    # 15,000 keys: 59 pages, three verify splits (24, 24, 11 pages); the
+    # 1-row run of stream 1 stays on the decode kernel in the same call
+    lengths = [15000, 5000]
     rs = [0] * 20 + [1]
-    rp = list(range(8980, 9000)) + [4999]
+    rp = list(range(14980, 15000)) + [4999]
     _check(_make(lengths, list(paged), rs, rp, kv=kv, seed=611), f"{kv} splits {paged}")
 
 
