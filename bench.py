@@ -49,7 +49,7 @@ METRIC = "paged decode KV GB/s (% HBM peak); prompt-chunk attn TFLOP/s (% TC pea
 # bench's partial launch), valid only while the kernel's sources hash to the
 # value below: after any change to them the line reports null until the
 # counters are taken again.
-DECODE_TRAFFIC = {"bytes": 268_595_200 + 4_013_824, "sources_sha256_16": "f88a0eb591d6c3e7"}
+DECODE_TRAFFIC = {"bytes": 268_597_760 + 4_002_048, "sources_sha256_16": "9a688074e6fb67d4"}
 DECODE_SOURCES = ["paged_kv_cache_235_gb300/csrc/decode.cu",
                   "paged_kv_cache_235_gb300/csrc/common.cuh",
                   "paged_kv_cache_235_gb300/csrc/params.h",
