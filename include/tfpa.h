@@ -30,8 +30,9 @@
  * marked DEVICE are device memory of the current device; HOST arrays are read
  * during the call only and not retained.  The library allocates no device
  * memory, keeps no state between calls except host-side caches (TMA tensor
- * maps, per host thread; each device's SM count), and never synchronises the
- * stream: all work is enqueued on `stream`.
+ * maps, per host thread; each device's SM count) and the plans a caller
+ * creates (a plan may own a CUDA graph, see tfpa_plan_capture), and never
+ * synchronises the stream: all work is enqueued on `stream`.
  *
  * Threads.  Calls may be made from several host threads at once, on any
  * streams and devices: each thread builds its launch parameters in its own
