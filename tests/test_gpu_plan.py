@@ -139,3 +139,40 @@ def test_device_mode_graph_replays_a_growing_decode_loop(name, via):
             assert torch.equal(sa.k_slab, sb.k_slab) and torch.equal(sa.v_slab, sb.v_slab)
     assert torch.equal(ga.k_pool, gb.k_pool)
     assert torch.equal(ga.v_pool, gb.v_pool)
+
+
+def test_plan_capture_refuses_the_legacy_stream_and_a_changed_shape():
+    """tfpa_plan_capture needs a created stream; a replay after the plan was
+    re-planned with another row count is refused (the captured launches no
+    longer fit), and the plan still launches directly."""
+    w = wl.small("batched_decode")
+    g = GpuCase(w)
+    nst = len(w.streams)
+    q = g.q()[:nst].contiguous()
+    sidx = np.arange(nst, dtype=np.int32)
+    rp = np.array([st.seq_len - 1 for st in w.streams], np.int32)
+    sc = B.make_scratch(16, w.hq)
+    out = torch.empty(nst, w.hq, 128, dtype=torch.bfloat16, device="cuda")
+    plan = B.Plan()
+    plan.decode(g.cache, g.segs, q, sidx, rp, w.softmax_scale, sc, out)
+    plan.launch()
+    torch.cuda.synchronize()
+    for bad in (0, 1):                               # NULL and cudaStreamLegacy
+        with pytest.raises(B.TfpaError) as e:
+            plan.capture(stream=bad)
+        assert e.value.code == B.TFPA_EINVAL
+    plan.capture(stream=torch.cuda.Stream())
+    plan.replay()
+    torch.cuda.synchronize()
+    ref = bits(out)
+    plan.clear()
+    plan.decode(g.cache, g.segs, q[:2], sidx[:2], rp[:2], w.softmax_scale, sc, out[:2])
+    with pytest.raises(B.TfpaError) as e:
+        plan.replay()
+    assert e.value.code == B.TFPA_EINVAL
+    plan.clear()
+    plan.decode(g.cache, g.segs, q, sidx, rp, w.softmax_scale, sc, out)
+    plan.replay()                                    # the captured shape again
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(out), ref)
+    assert int(g.err.item()) == 0
