@@ -278,18 +278,6 @@ __device__ __forceinline__ int v_zero_from(const RunInfo& ru, int j, bool page_b
   return kt + kTileKeys > ru.seq_len ? ru.seq_len - kt : kTileKeys;
 }
 
-// Prefetch of one box of a tensor into L2 (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
-               : "memory");
-}
-
-// Verify tiles stream their keys from HBM once (prefill tiles re-read a
-// prefix that mostly sits in L2), and their stages hold them only one to two
-// steps ahead of the MMAs: the producer also prefetches the K and V boxes of
-// the tile kAhead steps ahead into L2.
-constexpr int kAhead = 4;
 
 template <bool FP8, bool VERIFY>
 __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& x,
@@ -340,29 +328,6 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
     }
     return (cached_pid * p.hkv + x.g) * kPage + (kt & (kPage - 1));
   };
-  int pf_page = -1, pf_pid = 0;
-  auto prefetch = [&](int j) {              // verify: key tile j into L2
-    if (!VERIFY || j >= gm.kt0 + gm.nkt) return;
-    const int kt = j * kTileKeys;
-    int y;
-    if (ru.page_table) {
-      const int page = kt >> 8;
-      if (page != pf_page) {
-        pf_pid = __ldg(ru.page_table + page);
-        pf_page = page;
-      }
-      if ((unsigned)pf_pid >= (unsigned)p.num_pages) return;   // the load flags it
-      y = (pf_pid * p.hkv + x.g) * kPage + (kt & (kPage - 1));
-    } else {
-      y = x.g * ru.slab_cap + kt;
-    }
-    tma_prefetch_l2(mk, 0, y);
-    tma_prefetch_l2(mv, 0, y);
-    if (!FP8) {
-      tma_prefetch_l2(mk, 64, y);
-      tma_prefetch_l2(mv, 64, y);
-    }
-  };
   // Loads into a 16-bit operand stage (bf16), or (prefill, e4m3) into the
   // staging tile that the converters move on, K and V in their order.
   int staged_k = 0, staged_v = 0;       // e4m3: staging loads issued
@@ -399,11 +364,8 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
     // Step jj, slot hh: K into e4m3 stage 2 hh + (jj & 1), V into staging
     // tile 2 hh + (jj & 1), each at phase (jj >> 1) & 1; K of both slots,
     // then V of both.  last_k*, last_v*: each slot's last step loaded.
-    for (int j = gm.kt0; j < gm.kt0 + kAhead; ++j) prefetch(j);
     bool ok = true;
     for (int jj = 0; ok && jj < slot_tiles<true>(gm, 0); ++jj) {
-      prefetch(gm.kt0 + 2 * jj + kAhead);
-      prefetch(gm.kt0 + 2 * jj + 1 + kAhead);
       const uint32_t ph = (jj >> 1) & 1;
       for (int kv = 0; ok && kv < 2; ++kv)
         for (int hh = 0; ok && hh < 2; ++hh) {
@@ -425,11 +387,8 @@ __device__ void producer(const PrefillParams& p, const RunInfo& ru, const Tile& 
   } else if (VERIFY) {
     // Step jj, slot hh: tile n = 2 jj + hh (kt0 + n) into stage n mod 3 at
     // phase (n / 3) & 1; K of both slots, then V of both.
-    for (int j = gm.kt0; j < gm.kt0 + kAhead; ++j) prefetch(j);
     bool ok = true;
     for (int jj = 0; ok && jj < slot_tiles<true>(gm, 0); ++jj) {
-      prefetch(gm.kt0 + 2 * jj + kAhead);
-      prefetch(gm.kt0 + 2 * jj + 1 + kAhead);
       for (int kv = 0; ok && kv < 2; ++kv)
         for (int hh = 0; ok && hh < 2; ++hh) {
           if (jj >= slot_tiles<true>(gm, hh)) continue;
