@@ -266,6 +266,7 @@ struct tfpa_plan {
   size_t dyn_used = 0;           // bytes of dyn_base handed out
   cudaGraphExec_t exec = nullptr;   // tfpa_plan_capture's graph
   uint64_t exec_shape = 0;          // the plan's shape when it was captured
+  uint64_t shape = 0;               // the shape of the launches held now
   bool captured = false;
   ~tfpa_plan() {
     if (exec) cudaGraphExecDestroy(exec);
@@ -819,7 +820,15 @@ extern "C" int tfpa_write_kv_rope(const tfpa_cache* c, const tfpa_seg* segs, int
 }
 
 // ------------------------------------------------------------ plans
-extern "C" tfpa_plan* tfpa_plan_create(void) { return new (std::nothrow) tfpa_plan(); }
+namespace {
+uint64_t compute_shape(const tfpa_plan* plan);
+}  // namespace
+
+extern "C" tfpa_plan* tfpa_plan_create(void) {
+  tfpa_plan* plan = new (std::nothrow) tfpa_plan();
+  if (plan) plan->shape = compute_shape(plan);
+  return plan;
+}
 
 extern "C" void tfpa_plan_destroy(tfpa_plan* plan) { delete plan; }
 
@@ -831,6 +840,7 @@ extern "C" void tfpa_plan_clear(tfpa_plan* plan) {
   plan->merge.clear();
   plan->write.clear();
   plan->dyn_used = 0;
+  plan->shape = compute_shape(plan);
 }
 
 extern "C" int32_t tfpa_plan_launches(const tfpa_plan* plan) {
@@ -843,6 +853,7 @@ extern "C" int tfpa_plan_set_device(tfpa_plan* plan, void* dyn, size_t bytes) {
   plan->dyn_base = static_cast<uint8_t*>(dyn);
   plan->dyn_cap = dyn ? bytes : 0;
   plan->dyn_used = 0;
+  plan->shape = compute_shape(plan);
   return TFPA_OK;
 }
 
@@ -890,8 +901,8 @@ uint64_t hash_static(uint64_t h, const P& p) {
 }
 }  // namespace
 
-extern "C" uint64_t tfpa_plan_shape(const tfpa_plan* plan) {
-  if (!plan) return 0;
+namespace {
+uint64_t compute_shape(const tfpa_plan* plan) {
   uint64_t h = 14695981039346656037ull;
   for (const tfpa_plan::Entry& en : plan->entries) {
     const int32_t head[3] = {(int32_t)en.kind, (int32_t)en.fp8, en.grid};
@@ -905,6 +916,11 @@ extern "C" uint64_t tfpa_plan_shape(const tfpa_plan* plan) {
   }
   return h;
 }
+}  // namespace
+
+// The shape is recomputed after each planning call (while the GPU is busy
+// with the previous step), so that a replay only compares two numbers.
+extern "C" uint64_t tfpa_plan_shape(const tfpa_plan* plan) { return plan ? plan->shape : 0; }
 
 extern "C" int tfpa_plan_capture(tfpa_plan* plan, const tfpa_copy* before, int32_t nbefore,
                                  const tfpa_copy* after, int32_t nafter, cudaStream_t stream) {
@@ -972,7 +988,10 @@ int plan_call(tfpa_plan* plan, F&& fn) {
   } catch (const std::bad_alloc&) {
     e = TFPA_EINVAL;
   }
-  if (e != TFPA_OK) sink.rollback(m);
+  if (e != TFPA_OK)
+    sink.rollback(m);   // the plan, and so its shape, as before the call
+  else
+    plan->shape = compute_shape(plan);
   return e;
 }
 }  // namespace
