@@ -958,9 +958,11 @@ def main():
         e2e_plan = (max_over_ranks(dist, torch, e2e_plan[0]),) + tuple(e2e_plan[1:])
         e2e_plan_aa = time_e2e_planned(w, torch, B, ctx, n_e2e, args.warmup)
         e2e_graph_s, e2e_graph_dev_us = time_e2e_graph(w, torch, B, ctx, n_e2e, args.warmup)
-        e2e_dev = time_e2e_device(w, torch, B, ctx, n_e2e, args.warmup)
-        e2e_dev = (max_over_ranks(dist, torch, e2e_dev[0]),) + tuple(e2e_dev[1:])
-        e2e_dev_aa = time_e2e_device(w, torch, B, ctx, n_e2e, args.warmup)
+        # three runs of the loop; the line reports the median run and lists
+        # all three (a transient on the shared host can slow one run)
+        e2e_runs = [time_e2e_device(w, torch, B, ctx, n_e2e, args.warmup) for _ in range(3)]
+        e2e_runs = [(max_over_ranks(dist, torch, r[0]),) + tuple(r[1:]) for r in e2e_runs]
+        e2e_dev = sorted(e2e_runs, key=lambda r: r[0])[1]
         del ctx
         s3, p3, ctx3, _ = time_decode(w3, torch, B, max(10, args.steps // 4), args.warmup, None)
         del ctx3
@@ -1118,8 +1120,10 @@ def main():
                     "host_us_per_call": {"tfpa_write_kv": e2e[2], "tfpa_decode": e2e[3]},
                     "how": "the same loop calling tfpa_write_kv and tfpa_decode directly "
                            "(planning and launching inside each call)"}},
-        "e2e_aa_repeat": {"ms_per_step": [e2e_dev[0] * 1e3, e2e_dev_aa[0] * 1e3],
-                          "spread_pct": 100 * abs(e2e_dev_aa[0] - e2e_dev[0]) / e2e_dev[0],
+        "e2e_aa_repeat": {"ms_per_step": [r[0] * 1e3 for r in e2e_runs],
+                          "spread_pct": 100 * (max(r[0] for r in e2e_runs) -
+                                               min(r[0] for r in e2e_runs)) / e2e_dev[0],
+                          "reported": "median of the three runs",
                           "planned_calls_ms_per_step": [e2e_plan[0] * 1e3, e2e_plan_aa[0] * 1e3]},
         "e2e_two_in_flight": {
             "value": world * e2e_pipe[1] / e2e_pipe[0] / 1e9, "unit": "GB/s",
