@@ -789,7 +789,7 @@ def time_tree_calls(w, torch, B, reps):
     return statistics.median(times)
 
 
-def time_decode_calls(w, torch, B, reps, flush, fused_merge=False):
+def time_decode_calls(w, torch, B, reps, flush, fused_merge=True):
     """tfpa_decode (partial + merge) one call at a time, CUDA events around
     each, optionally with L2 flushed before each call; median in ms."""
     cache, segs, q = device_case(w, torch, B)
@@ -988,14 +988,15 @@ def main():
                 "frac_of_measured_bf16": fl5 / (ms5 / 1e3) / 1e12 / pk["bf16_tflops"]}
         w1 = wl.tiny_paged_decode()
         ms1 = time_decode_calls(w1, torch, B, 50, flush=True)
-        ms1f = time_decode_calls(w1, torch, B, 50, flush=True, fused_merge=True)
+        ms1s = time_decode_calls(w1, torch, B, 50, flush=True, fused_merge=False)
         kv1, qo1 = kv_bytes(w1)
         extra["tiny_decode"] = {
             "workload": "1 stream, 1 row at position 999, 8/2 heads, bf16, 4 of 16 pool pages; "
                         "tfpa_decode per call, L2 flushed before each",
             "us_per_call": ms1 * 1e3, "kv_gbs": (kv1 + qo1) / (ms1 / 1e3) / 1e9,
             "frac_of_measured_hbm": (kv1 + qo1) / (ms1 / 1e3) / 1e9 / pk["hbm_gbs"],
-            "us_per_call_merge_in_partial": ms1f * 1e3,
+            "merge": "inside the partial kernel (scratch with arrival counters)",
+            "us_per_call_separate_merge": ms1s * 1e3,
             "timing_floor": time_launch_floor(torch),
             "note": "1 MB of KV: launch and latency bound, the HBM roofline is out of reach; "
                     "timing_floor is the same event method around nothing and around one "

@@ -279,11 +279,10 @@ class Scratch(_Cached):
 
 
 def make_scratch(cap_rows: int, hq: int, max_splits: int = MAX_SPLITS, device="cuda",
-                 fused_merge: bool = False) -> Scratch:
-    """Scratch for cap_rows rows; with fused_merge it carries the zeroed
-    arrival counters that let tfpa_decode merge short streams inside the
-    partial kernel (measured slower than the separate merge launch, so off
-    by default)."""
+                 fused_merge: bool = True) -> Scratch:
+    """Scratch for cap_rows rows; with fused_merge (the default) it carries
+    the zeroed arrival counters that let tfpa_decode merge streams of up to
+    four splits inside the partial kernel (one launch instead of two)."""
     import torch
     o = torch.empty(cap_rows * hq * max_splits * HEAD_DIM, dtype=torch.float32, device=device)
     ml = torch.empty(cap_rows * hq * max_splits * 2, dtype=torch.float32, device=device)
