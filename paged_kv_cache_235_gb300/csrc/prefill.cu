@@ -109,12 +109,16 @@ constexpr uint32_t kTmemCols = 512;
 // launches with (e4m3: 512 x 128, bf16: 384 x 168), and no SM sub-partition
 // (one warp of each warpgroup) more than its 16,384.  The bf16 split was
 // picked by measurement: 64 / 216 ran 2.7 % faster than no split, where
-// 56 / 224 and 72 / 216 (the latter without any spill) ran slower.
+// 56 / 224 and 72 / 216 (the latter without any spill) ran slower.  The
+// e4m3 split 56 / 184 / 184 / 88 lets the converters issue all eight of a
+// thread's staging loads at once (1.7 % on prompt chunks, 1 % on verify
+// tiles, against 56 / 200 / 200 / 56 with four at a time); it uses each
+// sub-partition's 16,384 registers exactly.
 template <bool FP8>
 struct Regs;
 template <>
 struct Regs<true> {
-  static constexpr int kLow = 56, kHigh = 200, kConv = 56, kLaunch = 128;
+  static constexpr int kLow = 56, kHigh = 184, kConv = 88, kLaunch = 128;
 };
 template <>
 struct Regs<false> {
@@ -457,7 +461,7 @@ __device__ __forceinline__ void zero_v_rows(uint8_t* vtile, int z0, int lane) {
 // [128 rows][2 halves of 64] (128B swizzle), 64 threads; rows >= z0 become 0.
 __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int z0, int t) {
   const uint32_t sb = smem_u32(src), db = smem_u32(dst);
-#pragma unroll 4
+#pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int i = t + 128 * k;             // (row, 16-byte source chunk)
     const int row = i >> 3, c8 = i & 7;    // source chunk c8 = head dims 16*c8 .. +15
