@@ -2,9 +2,10 @@
 
 A step is one decode round of the batched-decode workload (8 streams x 8,192
 positions, 32 query / 8 KV heads, head_dim 128, bf16 KV; streams 0-3 on slabs,
-4-7 on 256-position pages of a permuted 512-page pool): write each stream's
-new K/V row (tfpa_write_kv), then split-K partials and their merge
-(tfpa_decode).  value = algorithmic KV bytes (+ Q and O) per step / step time,
+4-7 on 256-position pages of a permuted 512-page pool): each stream's new
+K/V row stored and decoded by one tfpa_decode_append call (split-K partials,
+whose CTAs store the new rows they read, then the merge).  value =
+algorithmic KV bytes (+ Q and O) per step / step time,
 in GB/s.  The prompt-chunk workload (28,672-position paged prefix plus a
 4,096-row causal chunk) is timed beside it and reported in TFLOP/s of its
 unmasked (row, key) pairs.
@@ -14,12 +15,12 @@ between decode steps; the prompt-chunk timing flushes L2 between launches.
 
 e2e is a decode loop through the public API with host buffers, one step at a
 time and every stream one position longer each step: every step is planned
-anew (tfpa_plan_write_kv / tfpa_plan_decode, plan in device mode) while the
+anew (tfpa_plan_decode_append, plan in device mode) while the
 previous one runs, its lengths packed for the device (tfpa_plan_dyn_pack),
-then one CUDA-graph replay runs a pinned input copy, the packed-data copy,
-the planned launches and an output copy, and the host waits.  The same loop
-with the plan in parameter mode (tfpa_plan_launch each step) and with direct
-tfpa_write_kv / tfpa_decode calls is reported beside it, with host times.
+then one CUDA-graph replay runs one pinned copy of the inputs and the packed
+data, the planned launches and an output copy, and the host waits.  The same
+loop with the plan in parameter mode (tfpa_plan_launch each step) and with
+direct tfpa_decode_append calls is reported beside it, with host times.
 
 Launch: ``python bench.py [--gpus N --steps K --warmup W] [--impl reference]``;
 for N > 1 under torchrun every rank runs its own replica (no collective on the
@@ -241,8 +242,7 @@ def time_decode(w, torch, B, steps, warmup, dist):
     sidx = np.arange(len(w.streams), dtype=np.int32)
 
     def step():
-        B.tfpa_write_kv(cache, segs, newk, newv, sidx, last)
-        B.tfpa_decode(cache, segs, q, w.row_seg, w.row_pos, w.softmax_scale, sc, out, lse)
+        B.tfpa_decode_append(cache, segs, newk, newv, q, sidx, last, w.softmax_scale, sc, out, lse)
 
     for _ in range(warmup):
         step()
@@ -306,8 +306,7 @@ def time_e2e_graph(w, torch, B, ctx, steps, warmup):
 
     def enqueue():
         d_in.copy_(h_in, non_blocking=True)
-        B.tfpa_write_kv(cache, segs, dk, dv, sidx, last)
-        B.tfpa_decode(cache, segs, dq, w.row_seg, w.row_pos, w.softmax_scale, sc, out)
+        B.tfpa_decode_append(cache, segs, dk, dv, dq, sidx, last, w.softmax_scale, sc, out)
         hout.copy_(out, non_blocking=True)
 
     for _ in range(warmup):
@@ -349,7 +348,7 @@ def e2e_buffers(w, torch, nst):
 def time_e2e_planned(w, torch, B, ctx, steps, warmup):
     """The decode loop of time_e2e_calls, one step at a time, with each step
     planned while the previous one runs: after enqueueing step i the host
-    plans step i + 1 (B.Plan: tfpa_plan_write_kv + tfpa_plan_decode, lengths
+    plans step i + 1 (B.Plan: tfpa_plan_decode_append, lengths
     one position longer), then waits for step i's output, then enqueues the
     next input copy, launches the plan and enqueues the output copy.
     Returns (s per step, KV + Q + O bytes per step, host us per plan launch,
@@ -375,8 +374,7 @@ def time_e2e_planned(w, torch, B, ctx, steps, warmup):
             tab.set_seq_len(j, n)
         rp = np.full(nst, n - 1, np.int32)
         plan.clear()
-        plan.write_kv(cache, tab, dk, dv, sidx, rp)
-        plan.decode(cache, tab, dq, sidx, rp, w.softmax_scale, sc, out)
+        plan.decode_append(cache, tab, dk, dv, dq, sidx, rp, w.softmax_scale, sc, out)
         return n
 
     n = plan_step(0)
@@ -458,8 +456,7 @@ def time_e2e_device(w, torch, B, ctx, steps, warmup):
             tab.set_seq_len(j, n)
         rp = np.full(nst, n - 1, np.int32)
         pl.clear()
-        pl.write_kv(cache, tab, dk, dv, sidx, rp)
-        pl.decode(cache, tab, dq, sidx, rp, w.softmax_scale, sc, out)
+        pl.decode_append(cache, tab, dk, dv, dq, sidx, rp, w.softmax_scale, sc, out)
         pl.pack(h[i % 2][in_bytes:])
         return n
 
@@ -524,11 +521,12 @@ def time_e2e_calls(w, torch, B, ctx, steps, warmup, in_flight=1):
     of n has length L - n + 1 + i (L = the workload's 8,192), writes each
     stream's new K/V row at its last position and decodes that row.  Per step:
     one copy of the step's inputs (q and the new K/V rows, one pinned buffer)
-    to the device, tfpa_write_kv, tfpa_decode, the output copied back to
+    to the device, tfpa_decode_append (the new rows stored and decoded), the
+    output copied back to
     pinned host memory, and the host waits for it.  With in_flight = 2 the
     host enqueues step i + 1 before it waits for step i's output (double-
     buffered inputs and outputs).  Returns (s per step, KV + Q + O bytes per
-    step on average, host us per tfpa_write_kv call, per tfpa_decode call,
+    step on average, host us per tfpa_decode_append call, 0.0,
     h2d bytes, d2h bytes)."""
     cache, segs, _, sc, out0 = ctx
     nst = len(w.streams)
@@ -556,13 +554,12 @@ def time_e2e_calls(w, torch, B, ctx, steps, warmup, in_flight=1):
         rp.fill(n - 1)
         d_in.copy_(h_in, non_blocking=True)
         t0 = time.perf_counter_ns()
-        B.tfpa_write_kv(cache, tab, dk, dv, sidx, rp, stream=sh)
+        B.tfpa_decode_append(cache, tab, dk, dv, dq, sidx, rp, w.softmax_scale, sc, outs[k],
+                             stream=sh)
         t1 = time.perf_counter_ns()
-        B.tfpa_decode(cache, tab, dq, sidx, rp, w.softmax_scale, sc, outs[k], stream=sh)
-        t2 = time.perf_counter_ns()
         hout.copy_(outs[k], non_blocking=True)
         evs[k].record(s)
-        return n, (t1 - t0) / 1e3, (t2 - t1) / 1e3
+        return n, (t1 - t0) / 1e3, 0.0
 
     def run(first, count, keep):
         nonlocal kvb
@@ -1080,7 +1077,8 @@ def main():
         "data": "synthetic (seeded N(0,1) rounded to bf16; pages from a seeded permutation)",
         "config": {"workload": "batched_decode: 8 streams x 8,192 positions, 1 row each, "
                                "32/8 heads, head_dim 128, bf16 KV, streams 0-3 slabs, 4-7 "
-                               "paged in a 512-page pool; step = tfpa_write_kv + tfpa_decode",
+                               "paged in a 512-page pool; step = tfpa_decode_append (the new rows' K/V "
+                               "stored, then decoded)",
                    "l2": "no flush: 268 MB of KV per step exceeds the 129 MB L2",
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
@@ -1097,7 +1095,7 @@ def main():
                 "steps": n_e2e,
                 "how": "a decode loop through the public API with host buffers, one step at a "
                        "time: each stream one position longer every step (%d..%d), every step "
-                       "planned anew (tfpa_plan_write_kv + tfpa_plan_decode, two plans in device "
+                       "planned anew (tfpa_plan_decode_append, two plans in device "
                        "mode, alternating) and packed (tfpa_plan_dyn_pack) while the previous "
                        "step runs; per step one tfpa_plan_replay of the plan's CUDA graph "
                        "(tfpa_plan_capture, once per plan): "
@@ -1118,8 +1116,8 @@ def main():
                 "direct_calls": {
                     "value": world * e2e[1] / e2e_s / 1e9, "unit": "GB/s",
                     "ms_per_step": e2e_s * 1e3, "vs_device_step": e2e_s * 1e3 / step_ms,
-                    "host_us_per_call": {"tfpa_write_kv": e2e[2], "tfpa_decode": e2e[3]},
-                    "how": "the same loop calling tfpa_write_kv and tfpa_decode directly "
+                    "host_us_per_call": {"tfpa_decode_append": e2e[2]},
+                    "how": "the same loop calling tfpa_decode_append directly "
                            "(planning and launching inside each call)"}},
         "e2e_aa_repeat": {"ms_per_step": [r[0] * 1e3 for r in e2e_runs],
                           "spread_pct": 100 * (max(r[0] for r in e2e_runs) -
@@ -1129,20 +1127,20 @@ def main():
         "e2e_two_in_flight": {
             "value": world * e2e_pipe[1] / e2e_pipe[0] / 1e9, "unit": "GB/s",
             "ms_per_step": e2e_pipe[0] * 1e3,
-            "host_us_per_call": {"tfpa_write_kv": e2e_pipe[2], "tfpa_decode": e2e_pipe[3]},
+            "host_us_per_call": {"tfpa_decode_append": e2e_pipe[2]},
             "how": "the same loop with step i + 1 enqueued before the host waits for step "
                    "i's output (two input and output buffers)"},
         "e2e_graph_replay": {
             "value": world * (kv + qo) / e2e_graph_s / 1e9, "unit": "GB/s",
             "ms_per_step": e2e_graph_s * 1e3,
             "graph_device_us_per_step": e2e_graph_dev_us,
-            "how": "upper bound: one step (copies, 3 kernels) captured once as a CUDA graph "
+            "how": "upper bound: one step (copies, 2 kernels) captured once as a CUDA graph "
                    "and replayed with its lengths frozen; no host planning per step"},
         "aa_repeat": {"ms_per_step": [step_ms, step_ms_aa],
                       "spread_pct": 100 * abs(step_ms_aa - step_ms) / step_ms},
-        "gpu_launches": 3 * args.steps,
-        "timing": "decode step = one CUDA-graph replay of tfpa_write_kv + tfpa_decode "
-                  "(3 kernels), CUDA events over --steps replays (device time); e2e = real "
+        "gpu_launches": 2 * args.steps,
+        "timing": "decode step = one CUDA-graph replay of tfpa_decode_append "
+                  "(2 kernels: partial with the rows' store, merge), CUDA events over --steps replays (device time); e2e = real "
                   "planned calls per step, host clock (see e2e.how); the per-call lines (prefill, "
                   "tiny_decode, overcommitted_pool, tree_verify, kv_store_rope, keep, "
                   "save_restore) are device time: CUDA events around one call, enqueued by "

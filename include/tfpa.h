@@ -247,6 +247,21 @@ int tfpa_decode(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
                 int32_t rows, float softmax_scale, const tfpa_scratch* scratch,
                 void* out, float* lse, cudaStream_t stream);
 
+/* A decode step in one call: the rows' K and V are stored (as tfpa_write_kv
+ * stores them; k_rows, v_rows: DEVICE bf16 [rows][hkv][128], 16-byte
+ * aligned) and the rows are decoded (as tfpa_decode decodes them), so the
+ * cache and the output hold the bytes of tfpa_write_kv followed by
+ * tfpa_decode.  When every run goes to the decode partial kernel and no
+ * segment has two runs in the call, that kernel stores the rows itself:
+ * the CTAs whose keys include a new row store it before they read it, and
+ * no write launch runs.  Otherwise one KV write launch precedes the decode
+ * launches.  TFPA_EINVAL for NULL or misaligned rows. */
+int tfpa_decode_append(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                       const void* k_rows, const void* v_rows, const void* q,
+                       const int32_t* row_seg, const int32_t* row_pos, int32_t rows,
+                       float softmax_scale, const tfpa_scratch* scratch, void* out, float* lse,
+                       cudaStream_t stream);
+
 /* Draft-tree verify: tfpa_decode whose rows see the keys their ancestor
  * masks allow instead of every earlier key.  The pages' partial and merge
  * kernels index the queries, the row tables, the ancestor table (rowanc),
@@ -305,8 +320,8 @@ int tfpa_decode_static(const tfpa_cache* cache, const tfpa_seg* segs, int32_t ns
 /* ---- Plans: planning a call apart from enqueueing it -----------------------
  * A decode loop's host work (checks, grouping rows into runs, split counts,
  * per-CTA item ranges, tensor maps) does not need the GPU.  A plan does that
- * work for a tfpa_write_kv or tfpa_decode call (same arguments, without the
- * stream) and keeps the resulting launches by value; tfpa_plan_launch then
+ * work for a tfpa_write_kv, tfpa_decode or tfpa_decode_append call (same
+ * arguments, without the stream) and keeps the resulting launches by value; tfpa_plan_launch then
  * only enqueues them.  A loop can plan step i + 1 while the GPU runs step i,
  * so that between the host's wait for step i's output and step i + 1's
  * kernels there are only the launches.  None of the TensorFold sources has a
@@ -335,6 +350,11 @@ int tfpa_plan_decode(tfpa_plan* plan, const tfpa_cache* cache, const tfpa_seg* s
                      int32_t nseg, const void* q, const int32_t* row_seg,
                      const int32_t* row_pos, int32_t rows, float softmax_scale,
                      const tfpa_scratch* scratch, void* out, float* lse);
+int tfpa_plan_decode_append(tfpa_plan* plan, const tfpa_cache* cache, const tfpa_seg* segs,
+                            int32_t nseg, const void* k_rows, const void* v_rows, const void* q,
+                            const int32_t* row_seg, const int32_t* row_pos, int32_t rows,
+                            float softmax_scale, const tfpa_scratch* scratch, void* out,
+                            float* lse);
 int tfpa_plan_launch(const tfpa_plan* plan, cudaStream_t stream);
 
 /* Device mode: replaying a captured plan as the streams grow.

@@ -33,7 +33,8 @@ EXPORTS = ("tfpa_pages_per_split", "tfpa_num_splits", "tfpa_write_kv", "tfpa_dec
            "tfpa_stage_pages", "tfpa_save_kv", "tfpa_restore_kv", "tfpa_plan_create",
            "tfpa_plan_destroy", "tfpa_plan_clear", "tfpa_plan_launches", "tfpa_plan_write_kv",
            "tfpa_plan_decode", "tfpa_plan_launch", "tfpa_plan_set_device", "tfpa_plan_dyn_bytes",
-           "tfpa_plan_dyn_pack", "tfpa_plan_shape", "tfpa_plan_capture", "tfpa_plan_replay")
+           "tfpa_plan_dyn_pack", "tfpa_plan_shape", "tfpa_plan_capture", "tfpa_plan_replay",
+           "tfpa_decode_append", "tfpa_plan_decode_append")
 
 
 class TfpaError(RuntimeError):
@@ -157,6 +158,12 @@ def lib():
         L.tfpa_plan_dyn_pack.restype = ctypes.c_int
         L.tfpa_plan_shape.argtypes = [vp]
         L.tfpa_plan_shape.restype = ctypes.c_uint64
+        L.tfpa_decode_append.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, vp, vp, i32,
+                                         ctypes.c_float, P(tfpa_scratch), vp, vp, vp]
+        L.tfpa_decode_append.restype = ctypes.c_int
+        L.tfpa_plan_decode_append.argtypes = [vp, P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, vp,
+                                              vp, i32, ctypes.c_float, P(tfpa_scratch), vp, vp]
+        L.tfpa_plan_decode_append.restype = ctypes.c_int
         L.tfpa_plan_capture.argtypes = [vp, P(tfpa_copy), i32, P(tfpa_copy), i32, vp]
         L.tfpa_plan_capture.restype = ctypes.c_int
         L.tfpa_plan_replay.argtypes = [vp, vp]
@@ -370,6 +377,18 @@ def tfpa_decode(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, softmax_
                              _stream(stream)), "tfpa_decode")
 
 
+def tfpa_decode_append(cache: Cache, segs: Sequence[Seg], k_rows, v_rows, q, row_seg, row_pos,
+                       softmax_scale, scratch: Scratch, out, lse=None, stream=None) -> None:
+    """Store the rows' K / V and decode the rows in one call (a decode step)."""
+    cs, n = _segs(segs)
+    rs, rp = _i32(row_seg), _i32(row_pos)
+    cc, sc = cache.c(), scratch.c()
+    _check(lib().tfpa_decode_append(ctypes.byref(cc), cs, n, _ptr(k_rows), _ptr(v_rows), _ptr(q),
+                                    _ptr(rs), _ptr(rp), len(rs), float(softmax_scale),
+                                    ctypes.byref(sc), _ptr(out), _ptr(lse), _stream(stream)),
+           "tfpa_decode_append")
+
+
 def tfpa_write_kv_rope(cache: Cache, segs: Sequence[Seg], k_rows, v_rows, row_seg, row_pos,
                        rope_cos, rope_sin, rope_pos=None, stream=None) -> None:
     """KV write with K rotated by each row's rotary position: ``rope_cos`` /
@@ -517,6 +536,16 @@ class Plan:
                                       _ptr(rp), len(rs), float(softmax_scale),
                                       ctypes.byref(scratch.c()), _ptr(out), _ptr(lse)),
                "tfpa_plan_decode")
+
+    def decode_append(self, cache: Cache, segs, k_rows, v_rows, q, row_seg, row_pos,
+                      softmax_scale, scratch: Scratch, out, lse=None) -> None:
+        cs, n = _segs(segs)
+        rs, rp = _i32(row_seg), _i32(row_pos)
+        _check(lib().tfpa_plan_decode_append(self._p, ctypes.byref(cache.c()), cs, n,
+                                             _ptr(k_rows), _ptr(v_rows), _ptr(q), _ptr(rs),
+                                             _ptr(rp), len(rs), float(softmax_scale),
+                                             ctypes.byref(scratch.c()), _ptr(out), _ptr(lse)),
+               "tfpa_plan_decode_append")
 
     def launch(self, stream=None) -> None:
         _check(lib().tfpa_plan_launch(self._p, _stream(stream)), "tfpa_plan_launch")

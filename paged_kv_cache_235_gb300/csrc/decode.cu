@@ -28,6 +28,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "kvstore.cuh"
 #include "params.h"
 #include "tcgen05.cuh"
 
@@ -128,20 +129,90 @@ __device__ __forceinline__ void item_keys(const DecodeParams& p, const DecodeDyn
   khi = min(min(klo + ru.pps * kPage, ru.seq_len), maxpos + 1);
 }
 
+// Append: the producer warp stores the new K and V of kv head g at
+// positions [k0, k1) of run ru (rows of this launch from ru.row0), as the
+// KV write kernel stores them: lanes 0-15 a K row's 8-element slices, lanes
+// 16-31 a V row's.  Each lane then fences its stores against the TMA
+// loads that follow (async proxy), and the warp meets.
 template <bool FP8>
+__device__ void store_new_rows(const DecodeParams& p, const RunInfo& ru, int g, int k0, int k1,
+                               int lane) {
+  const bool is_v = lane >= 16;
+  const int t = lane & 15;
+  const __nv_bfloat16* src_rows = is_v ? p.v_rows : p.k_rows;
+  void* base = is_v ? p.v_base[ru.src] : p.k_base[ru.src];
+  for (int key = k0; key < k1; ++key) {
+    size_t dst_row;
+    if (ru.page_table) {
+      const int pid = __ldg(ru.page_table + (key >> 8));
+      if ((unsigned)pid >= (unsigned)p.num_pages) {   // flagged by the loads of that page
+        continue;
+      }
+      dst_row = ((size_t)pid * p.hkv + g) * kPage + (key & (kPage - 1));
+    } else {
+      dst_row = (size_t)g * ru.slab_cap + key;
+    }
+    const int row = ru.row0 + (key - ru.pos0);
+    const uint4 in =
+        *reinterpret_cast<const uint4*>(src_rows + ((size_t)row * p.hkv + g) * kHeadDim + t * 8);
+    if (FP8) {
+      float f[8];
+      unpack8(in, f);
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(base) + dst_row * kHeadDim + t * 8) =
+          quant8(f, __ldg((is_v ? p.v_scale : p.k_scale) + g));
+    } else {
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + dst_row * kHeadDim + t * 8) =
+          in;
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncwarp();
+}
+
+template <bool FP8>
+__device__ __forceinline__ bool load_item(const DecodeParams& p, const RunInfo& ru, const Item& x,
+                                          int klo, int khi, uint8_t* stage_mem, uint64_t* full,
+                                          uint64_t* empty, int* stage_bad, uint32_t& stage);
+
+// Producer warp: lane 0 looks pages up and issues the TMA loads; with
+// append (APPEND), the whole warp first stores the new rows an item reads.
+template <bool FP8, bool APPEND>
 __device__ void producer(const DecodeParams& p, const DecodeDyn& D, uint8_t* stage_mem,
                          uint64_t* full, uint64_t* empty, int* stage_bad) {
-  using C = Cfg<FP8>;
-  if ((threadIdx.x & 31) != 0) return;
+  const int lane = threadIdx.x & 31;
+  if (!APPEND && lane != 0) return;
   int ib, ie;
   cta_items(D, ib, ie);
   int rh = ib < ie ? run_of(D, ib) : 0;   // run of the current item
   uint32_t stage = 0;
-  for (int it = ib; it < ie; ++it) {
+  bool ok = true;
+  for (int it = ib; ok && it < ie; ++it) {
     const Item x = item_of(p, D, it, rh);
     const RunInfo& ru = D.runs[x.run];
     int klo, khi;
     item_keys(p, D, x, klo, khi);
+    if constexpr (APPEND) {
+      const int k0 = max(klo, ru.pos0), k1 = min(khi, ru.pos0 + ru.nrows);
+      if (k0 < k1) store_new_rows<FP8>(p, ru, x.g, k0, k1, lane);
+      // the warp moves on item by item with lane 0, and leaves with it
+      ok = __shfl_sync(0xffffffffu, lane == 0 ? load_item<FP8>(p, ru, x, klo, khi, stage_mem,
+                                                                full, empty, stage_bad, stage)
+                                              : true,
+                       0);
+    } else {
+      ok = load_item<FP8>(p, ru, x, klo, khi, stage_mem, full, empty, stage_bad, stage);
+    }
+  }
+}
+
+// Lane 0 of the producer warp: the TMA loads of one item's key chunks into
+// the ring, one page lookup per page.  False if a wait gave up.
+template <bool FP8>
+__device__ __forceinline__ bool load_item(const DecodeParams& p, const RunInfo& ru, const Item& x,
+                                          int klo, int khi, uint8_t* stage_mem, uint64_t* full,
+                                          uint64_t* empty, int* stage_bad, uint32_t& stage) {
+  using C = Cfg<FP8>;
+  {
     const CUtensorMap* mk = &p.maps[ru.src].k;
     const CUtensorMap* mv = &p.maps[ru.src].v;
     int cached_page = -1, cached_pid = 0;
@@ -165,7 +236,7 @@ __device__ void producer(const DecodeParams& p, const DecodeDyn& D, uint8_t* sta
       } else {
         y = x.g * ru.slab_cap + k0;
       }
-      if (!mbar_wait(&empty[buf], ph ^ 1, p.err_flag)) return;
+      if (!mbar_wait(&empty[buf], ph ^ 1, p.err_flag)) return false;
       stage_bad[buf] = bad;
       uint64_t* fb = &full[buf];
       uint8_t* sb = stage_mem + (size_t)buf * kStageBytes;
@@ -181,6 +252,7 @@ __device__ void producer(const DecodeParams& p, const DecodeDyn& D, uint8_t* sta
       }
     }
   }
+  return true;
 }
 
 // Real head-dim index of C-fragment column n of PV n-tile nt (the V fragments
@@ -771,7 +843,8 @@ __device__ void combiner(const DecodeParams& p, const DecodeDyn& D, uint32_t tme
 
 // DEV: the runs and CTA ranges are read from p.dyn (a plan in device mode).
 // MERGE: the combiners merge each finished group (p.arrive).
-template <bool FP8, bool GEN, bool DEV, bool MERGE>
+// APPEND: the producer warp stores the rows' new K and V (p.k_rows).
+template <bool FP8, bool GEN, bool DEV, bool MERGE, bool APPEND>
 __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
     const __grid_constant__ DecodeParams p) {
   const DecodeDyn& D = DEV ? *p.dyn : p.d;
@@ -827,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
     combiner<FP8, GEN, MERGE>(p, D, tmem, fold, ml_buf, merge_flag, cb);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
-    if (warp == kProducerWarp) producer<FP8>(p, D, stage_mem, full, empty, stage_bad);
+    if (warp == kProducerWarp) producer<FP8, APPEND>(p, D, stage_mem, full, empty, stage_bad);
   }
   umma::fence_before_sync();
   __syncthreads();
@@ -876,23 +949,23 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
                                   p.lse ? p.lse + (size_t)row * p.hq + h : nullptr);
 }
 
-template <bool FP8, bool GEN, bool DEV, bool MERGE>
+template <bool FP8, bool GEN, bool DEV, bool MERGE, bool APPEND>
 cudaError_t launch_partial(const DecodeParams& p, int grid, cudaStream_t s) {
   static PerDeviceOnce configured;
   cudaError_t e = configured.run([] {
     // The register split only works if the block launches with at least the
     // registers it hands out; otherwise setmaxnreg.inc would wait forever.
     cudaFuncAttributes attr;
-    cudaError_t r = cudaFuncGetAttributes(&attr, decode_partial_kernel<FP8, GEN, DEV, MERGE>);
+    cudaError_t r = cudaFuncGetAttributes(&attr, decode_partial_kernel<FP8, GEN, DEV, MERGE, APPEND>);
     if (r != cudaSuccess) return r;
     if (attr.numRegs * kThreads < 128 * (2 * kRegsConsumer + kRegsCombine + kRegsProducer))
       return cudaErrorInvalidValue;
-    return cudaFuncSetAttribute(decode_partial_kernel<FP8, GEN, DEV, MERGE>,
+    return cudaFuncSetAttribute(decode_partial_kernel<FP8, GEN, DEV, MERGE, APPEND>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (e != cudaSuccess) return e;
   e =
-      launch_pdl(decode_partial_kernel<FP8, GEN, DEV, MERGE>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
+      launch_pdl(decode_partial_kernel<FP8, GEN, DEV, MERGE, APPEND>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -902,10 +975,13 @@ cudaError_t launch_partial_dev(const DecodeParams& p, bool fp8, int grid, cudaSt
   // Rows with ancestor masks take the general instantiation, so the plain
   // causal calls keep their own kernel's code.
   if (p.anc)
-    return fp8 ? launch_partial<true, true, DEV, false>(p, grid, s)
-               : launch_partial<false, true, DEV, false>(p, grid, s);
-  return fp8 ? launch_partial<true, false, DEV, false>(p, grid, s)
-             : launch_partial<false, false, DEV, false>(p, grid, s);
+    return fp8 ? launch_partial<true, true, DEV, false, false>(p, grid, s)
+               : launch_partial<false, true, DEV, false, false>(p, grid, s);
+  if (p.k_rows)
+    return fp8 ? launch_partial<true, false, DEV, false, true>(p, grid, s)
+               : launch_partial<false, false, DEV, false, true>(p, grid, s);
+  return fp8 ? launch_partial<true, false, DEV, false, false>(p, grid, s)
+             : launch_partial<false, false, DEV, false, false>(p, grid, s);
 }
 
 }  // namespace
@@ -915,10 +991,14 @@ cudaError_t launch_partial_dev(const DecodeParams& p, bool fp8, int grid, cudaSt
 cudaError_t launch_decode_partial(const DecodeParams& p, bool fp8, int grid, cudaStream_t s) {
   if (grid <= 0 || p.d.n_items == 0) return cudaSuccess;
   // The merge in the kernel is built for plain causal rows in parameter mode.
+  if (p.k_rows && p.anc) return cudaErrorInvalidValue;   // append has no tree rows
   if (p.arrive) {
     if (p.anc || p.dyn || !p.out) return cudaErrorInvalidValue;
-    return fp8 ? launch_partial<true, false, false, true>(p, grid, s)
-               : launch_partial<false, false, false, true>(p, grid, s);
+    if (p.k_rows)
+      return fp8 ? launch_partial<true, false, false, true, true>(p, grid, s)
+                 : launch_partial<false, false, false, true, true>(p, grid, s);
+    return fp8 ? launch_partial<true, false, false, true, false>(p, grid, s)
+               : launch_partial<false, false, false, true, false>(p, grid, s);
   }
   return p.dyn ? launch_partial_dev<true>(p, fp8, grid, s)
                : launch_partial_dev<false>(p, fp8, grid, s);

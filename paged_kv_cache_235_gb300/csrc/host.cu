@@ -495,14 +495,29 @@ void plan_cta_ranges(DecodeParams& p, int nr, int G, bool fp8, int grid) {
 // the partial kernel when the scratch has arrival counters.
 constexpr int kFusedMergeMaxSplits = 4;
 
+struct RopeArgs {
+  const int32_t* pos;   // DEVICE [rows] or nullptr (the storage positions)
+  const float* cos;     // DEVICE [n][64] or nullptr (plain store)
+  const float* sin;
+  int32_t n;
+};
+int write_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const void* k_rows,
+               const void* v_rows, const int32_t* row_seg, const int32_t* row_pos, int32_t rows,
+               const RopeArgs& rope, const Sink& sink);
+
 // Partial (and optionally merge) launches over the call's rows.  With
 // `sliced`, each launch's partials start at scratch row 0 and are merged
 // before the next launch; otherwise partials land at the call's own row and
 // no merge runs.
+// With k_rows / v_rows (append), the rows' K and V are stored as well: by
+// the decode partial kernel itself when every run takes it and no segment
+// has two runs (a run's CTAs store the new rows they read before reading
+// them), else by a KV write launch ahead of the decode launches.
 int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const void* q,
                 const int32_t* row_seg, const int32_t* row_pos, const uint64_t* anc,
                 int32_t rows, float scale, const tfpa_scratch* sc, void* out, float* lse,
-                const Sink& sink, bool sliced) {
+                const Sink& sink, bool sliced, const void* k_rows = nullptr,
+                const void* v_rows = nullptr) {
   int e;
   if ((e = check_cache(c)) || (e = check_segs(c, segs, nseg))) return e;
   if (!sc || !sc->part_o || !sc->part_ml || sc->cap_rows < 1 || sc->max_splits < 1)
@@ -520,6 +535,20 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
   if ((e = check_device())) return e;
   const bool fp8 = c->dtype == TFPA_FP8_E4M3;
   const int G = c->hq / c->hkv;
+  if (k_rows || v_rows) {
+    if (!k_rows || !v_rows || !aligned(k_rows, 16) || !aligned(v_rows, 16)) return TFPA_EINVAL;
+    bool fuse = true;
+    for (size_t i = 0; fuse && i < runs.size(); ++i) {
+      fuse = G > kVerifyVectors || (runs[i].nrows * G + 15) / 16 < 4;   // decode partial path
+      for (size_t j = 0; fuse && j < i; ++j) fuse = runs[j].seg != runs[i].seg;
+    }
+    if (!fuse) {
+      if ((e = write_impl(c, segs, nseg, k_rows, v_rows, row_seg, row_pos, rows,
+                          RopeArgs{nullptr, nullptr, nullptr, 0}, sink)))
+        return e;
+      k_rows = v_rows = nullptr;
+    }
+  }
   const int nsm = sm_count();
   if (nsm < 1) return TFPA_ECUDA;
   const size_t hd = (size_t)c->hq * kHeadDim;
@@ -599,6 +628,18 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
       p.k_scale = c->k_scale;
       p.v_scale = c->v_scale;
       p.err_flag = c->err_flag;
+      const size_t rd = (size_t)c->hkv * kHeadDim;
+      p.k_rows = k_rows ? static_cast<const __nv_bfloat16*>(k_rows) + (size_t)base * rd : nullptr;
+      p.v_rows = v_rows ? static_cast<const __nv_bfloat16*>(v_rows) + (size_t)base * rd : nullptr;
+      if (k_rows) {
+        // where each source's rows go: the pool, then the slabs in source order
+        p.k_base[0] = c->k_pool;
+        p.v_base[0] = c->v_pool;
+        for (int i = 0; i < ss.nslab; ++i) {
+          p.k_base[i + 1] = segs[ss.slab_seg[i]].k_slab;
+          p.v_base[i + 1] = segs[ss.slab_seg[i]].v_slab;
+        }
+      }
       p.arrive = fused ? sc->arrive + (size_t)srow * c->hq : nullptr;
       p.out = fused ? static_cast<__nv_bfloat16*>(out) + (size_t)base * hd : nullptr;
       p.lse = fused && lse ? lse + (size_t)base * c->hq : nullptr;
@@ -690,6 +731,16 @@ extern "C" int tfpa_decode_tree(const tfpa_cache* cache, const tfpa_seg* segs, i
                      scratch, out, lse, Sink{stream, nullptr}, true);
 }
 
+extern "C" int tfpa_decode_append(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                                  const void* k_rows, const void* v_rows, const void* q,
+                                  const int32_t* row_seg, const int32_t* row_pos, int32_t rows,
+                                  float softmax_scale, const tfpa_scratch* scratch, void* out,
+                                  float* lse, cudaStream_t stream) {
+  if (rows > 0 && (!k_rows || !v_rows)) return TFPA_EINVAL;
+  return decode_impl(cache, segs, nseg, q, row_seg, row_pos, nullptr, rows, softmax_scale,
+                     scratch, out, lse, Sink{stream, nullptr}, true, k_rows, v_rows);
+}
+
 extern "C" int tfpa_merge(const tfpa_scratch* sc, int32_t hq, int32_t rows,
                           const int32_t* nsplit, void* out, float* lse, cudaStream_t stream) {
   if (!sc || !sc->part_o || !sc->part_ml || hq < 1 || rows < 0) return TFPA_EINVAL;
@@ -730,13 +781,6 @@ extern "C" int tfpa_merge(const tfpa_scratch* sc, int32_t hq, int32_t rows,
 }
 
 namespace {
-
-struct RopeArgs {
-  const int32_t* pos;   // DEVICE [rows] or nullptr (the storage positions)
-  const float* cos;     // DEVICE [n][64] or nullptr (plain store)
-  const float* sin;
-  int32_t n;
-};
 
 int write_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const void* k_rows,
                const void* v_rows, const int32_t* row_seg, const int32_t* row_pos, int32_t rows,
@@ -1013,6 +1057,18 @@ extern "C" int tfpa_plan_decode(tfpa_plan* plan, const tfpa_cache* cache, const 
   return plan_call(plan, [&](const Sink& sink) {
     return decode_impl(cache, segs, nseg, q, row_seg, row_pos, nullptr, rows, softmax_scale,
                        scratch, out, lse, sink, true);
+  });
+}
+
+extern "C" int tfpa_plan_decode_append(tfpa_plan* plan, const tfpa_cache* cache,
+                                       const tfpa_seg* segs, int32_t nseg, const void* k_rows,
+                                       const void* v_rows, const void* q, const int32_t* row_seg,
+                                       const int32_t* row_pos, int32_t rows, float softmax_scale,
+                                       const tfpa_scratch* scratch, void* out, float* lse) {
+  if (rows > 0 && (!k_rows || !v_rows)) return TFPA_EINVAL;
+  return plan_call(plan, [&](const Sink& sink) {
+    return decode_impl(cache, segs, nseg, q, row_seg, row_pos, nullptr, rows, softmax_scale,
+                       scratch, out, lse, sink, true, k_rows, v_rows);
   });
 }
 

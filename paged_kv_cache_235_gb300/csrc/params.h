@@ -66,6 +66,14 @@ struct DecodeParams {
   const float* k_scale;       // fp8: [hkv]
   const float* v_scale;
   int32_t* err_flag;
+  // Append (k_rows != nullptr): the rows' new K and V ([rows][hkv][128]
+  // bf16, rows of this launch) are stored by the CTAs whose keys include
+  // them, before they read them; a source's K / V base is where its rows
+  // go (pool: [num_pages][hkv][256][128], slab: [hkv][slab_cap][128]).
+  const __nv_bfloat16* k_rows;
+  const __nv_bfloat16* v_rows;
+  void* k_base[kMaxSources];
+  void* v_base[kMaxSources];
   // Merge in the partial kernel (arrive != nullptr): per (row, head) of a
   // group's first query vector, the splits finished so far; the last CTA
   // to finish one merges the group into out / lse (rows of this launch).

@@ -471,3 +471,39 @@ def test_plan_capture_and_replay_follow_the_shape():
         with pytest.raises(B.TfpaError) as e:     # nothing to capture
             plan.capture(stream=0)
         assert e.value.code == B.TFPA_EINVAL
+
+
+def test_append_stores_in_the_partial_kernel_where_it_can():
+    """tfpa_decode_append: narrow runs, one per segment, run the partial and
+    merge launches only (the partial kernel stores the rows); a wide run or
+    a segment with two runs adds one KV write launch ahead of the decode."""
+    c = _cache()
+    segs = [B.Seg(4000, page_table=3 * FAKE), B.Seg(700, k_slab=8 * FAKE, v_slab=9 * FAKE,
+                                                    slab_cap=768)]
+    sc = B.Scratch(5 * FAKE, 6 * FAKE, 64, 32)
+
+    def kinds(rs, rp):
+        with B.record_launches() as rec:
+            B.tfpa_decode_append(c, segs, 10 * FAKE, 11 * FAKE, 4 * FAKE, rs, rp, 0.088, sc,
+                                 7 * FAKE, stream=0)
+        return [r["kind"] for r in rec]
+
+    assert kinds(np.array([0, 1]), np.array([3999, 699])) == ["partial", "merge"]
+    assert kinds(np.array([0] * 4 + [1]), np.array([3996, 3997, 3998, 3999, 699])) == [
+        "partial", "merge"]
+    # 20 rows of stream 0: the tensor-core verify path
+    assert kinds(np.array([0] * 20 + [1]), np.array(list(range(3980, 4000)) + [699])) == [
+        "write_kv", "partial", "verify", "merge"]
+    # stream 0 in two runs (positions not consecutive)
+    assert kinds(np.array([0, 0, 1]), np.array([3990, 3999, 699])) == [
+        "write_kv", "partial", "merge"]
+    plan = B.Plan()
+    with B.record_launches() as rec:
+        plan.decode_append(c, segs, 10 * FAKE, 11 * FAKE, 4 * FAKE, np.array([0, 1]),
+                           np.array([3999, 699]), 0.088, sc, 7 * FAKE)
+    assert [r["kind"] for r in rec] == ["partial", "merge"]
+    with B.record_launches() as rec:
+        with pytest.raises(B.TfpaError) as e:
+            B.tfpa_decode_append(c, segs, 10 * FAKE + 8, 11 * FAKE, 4 * FAKE, np.array([0]),
+                                 np.array([3999]), 0.088, sc, 7 * FAKE, stream=0)
+    assert e.value.code == B.TFPA_EINVAL and rec == []
