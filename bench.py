@@ -14,13 +14,16 @@ Inputs are 268 MB of KV per step, above the 129 MB L2, so no flush is needed
 between decode steps; the prompt-chunk timing flushes L2 between launches.
 
 e2e is a decode loop through the public API with host buffers, one step at a
-time and every stream one position longer each step: every step is planned
-anew (tfpa_plan_decode_append, plan in device mode) while the
-previous one runs, its lengths packed for the device (tfpa_plan_dyn_pack),
-then one CUDA-graph replay runs one pinned copy of the inputs and the packed
-data, the planned launches and an output copy, and the host waits.  The same
-loop with the plan in parameter mode (tfpa_plan_launch each step) and with
-direct tfpa_decode_append calls is reported beside it, with host times.
+time and every stream one position longer each step: while the previous step
+runs, the host writes the step's inputs into pinned memory and plans the
+step anew (tfpa_plan_decode_append, plan in device mode), packing its
+lengths into the same pinned buffer (tfpa_plan_dyn_pack); then one
+CUDA-graph replay runs the planned launches, which read the inputs and
+lengths from host memory and write the output there over NVLink-C2C, and
+the host waits.  The same loop with copy-engine copies to and from device
+buffers, with the plan in parameter mode (tfpa_plan_launch each step) and
+with direct tfpa_decode_append calls is reported beside it, with host
+times.
 
 Launch: ``python bench.py [--gpus N --steps K --warmup W] [--impl reference]``;
 for N > 1 under torchrun every rank runs its own replica (no collective on the
@@ -297,10 +300,16 @@ def time_e2e_graph(w, torch, B, ctx, steps, warmup):
     """Upper bound: the whole step (copies in, kernels, copy out) captured once
     as a CUDA graph and replayed, the host waiting for each step's output.
     The replay repeats one step's kernel parameters (lengths frozen at
-    capture), so a decode loop whose lengths advance cannot run this way."""
+    capture), so a decode loop whose lengths advance cannot run this way; the
+    inputs are written once, not every step."""
     cache, segs, _, sc, out = ctx
     nst = len(w.streams)
-    h_in, d_in, dq, dk, dv, hout = e2e_buffers(w, torch, nst)
+    feed = FreshInputs(w, torch, 1)
+    feed.write(0)
+    h_in = feed.rows(0)
+    d_in = torch.empty(feed.nbytes, dtype=torch.uint8, device="cuda")
+    dq, dk, dv = feed.split(d_in)
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     last = np.array([st.seq_len - 1 for st in w.streams], np.int32)
     sidx = np.arange(nst, dtype=np.int32)
 
@@ -332,31 +341,60 @@ def time_e2e_graph(w, torch, B, ctx, steps, warmup):
     return dt, graph_device_us(torch, graph.replay, steps)
 
 
-def e2e_buffers(w, torch, nst):
-    """One pinned host buffer per step's inputs (q rows, then the new K and V
-    rows), its device copy with views, and a pinned buffer for the output."""
-    nq, nk = w.rows * w.hq * 128, nst * w.hkv * 128
-    h_in = torch.randn(nq + 2 * nk).to(torch.bfloat16).pin_memory()
-    d_in = torch.empty_like(h_in, device="cuda")
-    dq = d_in[:nq].view(w.rows, w.hq, 128)
-    dk = d_in[nq:nq + nk].view(nst, w.hkv, 128)
-    dv = d_in[nq + nk:].view(nst, w.hkv, 128)
-    hout = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16).pin_memory()
-    return h_in, d_in, dq, dk, dv, hout
+class FreshInputs:
+    """The host's inputs of a decode loop: each step's q rows and new K / V
+    rows, written by the host into a pinned buffer while the GPU runs an
+    earlier step.  `nbuf` pinned buffers rotate (step i uses buffer
+    i % nbuf) and each step copies in one of four seeded sets, so that
+    consecutive steps carry new values (a kernel that reads host memory
+    cannot find a step's inputs in the GPU's L2).  `extra` bytes follow the
+    rows in each buffer (a device-mode plan's packed data)."""
+
+    def __init__(self, w, torch, nbuf, extra=0):
+        self.torch, self.w, self.nbuf = torch, w, nbuf
+        nst = len(w.streams)
+        self.nq, self.nk = w.rows * w.hq * 128, nst * w.hkv * 128
+        n = self.nq + 2 * self.nk
+        self.nbytes = 2 * n
+        g = torch.Generator()
+        g.manual_seed(17)
+        self.src = [torch.randn(n, generator=g).to(torch.bfloat16).view(torch.int16).numpy()
+                    for _ in range(4)]
+        self.buf = [torch.zeros(self.nbytes + extra, dtype=torch.uint8).pin_memory()
+                    for _ in range(nbuf)]
+        self._dst = [b[:self.nbytes].numpy().view(np.int16) for b in self.buf]
+
+    def write(self, i):
+        """Step i's inputs into its buffer (the host's part of the step)."""
+        np.copyto(self._dst[i % self.nbuf], self.src[i % 4])
+
+    def rows(self, i):
+        return self.buf[i % self.nbuf][:self.nbytes]
+
+    def split(self, t):
+        """q, K, V views of a row buffer (host or device, uint8)."""
+        w, nq, nk = self.w, self.nq, self.nk
+        nst = len(w.streams)
+        r = t[:self.nbytes].view(self.torch.bfloat16)
+        return (r[:nq].view(w.rows, w.hq, 128), r[nq:nq + nk].view(nst, w.hkv, 128),
+                r[nq + nk:].view(nst, w.hkv, 128))
 
 
 def time_e2e_planned(w, torch, B, ctx, steps, warmup):
     """The decode loop of time_e2e_calls, one step at a time, with each step
     planned while the previous one runs: after enqueueing step i the host
-    plans step i + 1 (B.Plan: tfpa_plan_decode_append, lengths
-    one position longer), then waits for step i's output, then enqueues the
-    next input copy, launches the plan and enqueues the output copy.
-    Returns (s per step, KV + Q + O bytes per step, host us per plan launch,
-    host us planning a step)."""
+    writes step i + 1's inputs and plans it (B.Plan:
+    tfpa_plan_decode_append, lengths one position longer), then waits for
+    step i's output, then enqueues the next input copy, launches the plan
+    and enqueues the output copy.  Returns (s per step, KV + Q + O bytes per
+    step, host us per plan launch, host us planning a step)."""
     cache, segs, _, sc, out = ctx
     nst = len(w.streams)
     tab = B.SegTable(segs)
-    h_in, d_in, dq, dk, dv, hout = e2e_buffers(w, torch, nst)
+    feed = FreshInputs(w, torch, 2)
+    d_in = torch.empty(feed.nbytes, dtype=torch.uint8, device="cuda")
+    dq, dk, dv = feed.split(d_in)
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     sidx = np.arange(nst, dtype=np.int32)
     s = torch.cuda.current_stream()
     sh = s.cuda_stream
@@ -375,6 +413,7 @@ def time_e2e_planned(w, torch, B, ctx, steps, warmup):
         rp = np.full(nst, n - 1, np.int32)
         plan.clear()
         plan.decode_append(cache, tab, dk, dv, dq, sidx, rp, w.softmax_scale, sc, out)
+        feed.write(i)
         return n
 
     n = plan_step(0)
@@ -383,7 +422,7 @@ def time_e2e_planned(w, torch, B, ctx, steps, warmup):
         if i == warmup:
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-        d_in.copy_(h_in, non_blocking=True)
+        d_in.copy_(feed.rows(i), non_blocking=True)
         a = time.perf_counter_ns()
         plan.launch(sh)
         t_launch.append((time.perf_counter_ns() - a) / 1e3)
@@ -403,73 +442,82 @@ def time_e2e_planned(w, torch, B, ctx, steps, warmup):
     return dt, kvb / steps + qo, statistics.median(t_launch[warmup:]), statistics.median(t_plan)
 
 
-def time_e2e_device(w, torch, B, ctx, steps, warmup):
+def time_e2e_device(w, torch, B, ctx, steps, warmup, zero_copy):
     """The decode loop of time_e2e_planned with plans in device mode
     (tfpa_plan_set_device): each step is still planned anew with lengths one
     position longer, but its launches read their lengths, splits and CTA
-    ranges from a device buffer, so each plan is captured once as a CUDA
-    graph (tfpa_plan_capture: one copy of the step's inputs and packed data
-    from pinned memory, the planned launches, the output copy) and replayed
-    (tfpa_plan_replay) step after step.  The packed data (tfpa_plan_dyn_pack)
-    sits right after the q / K / V rows in the same pinned buffer, so one
-    copy carries both.  Two plans with their own pinned buffers alternate:
-    while the GPU runs step i the host plans step i + 1 on the other plan
-    and packs it into that plan's buffer, then waits for step i's output and
-    replays.  Returns (s per step, KV + Q + O bytes per step, host us per
-    replay, host us planning and packing a step, packed bytes copied per
-    step, device us per replay)."""
+    ranges from the plan's buffer, so each plan is captured once as a CUDA
+    graph (tfpa_plan_capture) and replayed (tfpa_plan_replay) step after
+    step.  Two plans, each with its own pinned buffer (the step's q / K / V
+    rows, then the plan's packed data), alternate: while the GPU runs step i
+    the host plans step i + 1 on the other plan, packs it
+    (tfpa_plan_dyn_pack) and writes that step's inputs into that plan's
+    buffer, then waits for step i's output and replays.
+    zero_copy: the plans read the rows and the packed data straight from the
+    pinned buffer and write the output to pinned memory (the kernels load
+    and store over the host link), so a graph holds only the launches.
+    Else a graph is one copy of the pinned buffer (rows and packed data) to
+    the device, the launches, and the output copy back.
+    Returns (s per step, KV + Q + O bytes per step, host us per replay, host
+    us planning, packing and writing a step, bytes brought from the host per
+    step, bytes sent back, device us per replay)."""
     cache, segs, _, sc, out = ctx
     nst = len(w.streams)
     tab = B.SegTable(segs)
-    nq, nk = w.rows * w.hq * 128, nst * w.hkv * 128
-    in_bytes = (nq + 2 * nk) * 2                   # q, new K, new V (bf16)
     dyn_cap = 1 << 15
-    rows = torch.randn(nq + 2 * nk).to(torch.bfloat16)
-    h = []
-    for _ in range(2):
-        hb = torch.zeros(in_bytes + dyn_cap, dtype=torch.uint8).pin_memory()
-        hb[:in_bytes].view(torch.bfloat16).copy_(rows)
-        h.append(hb)
-    d = torch.empty_like(h[0], device="cuda")
-    d_rows = d[:in_bytes].view(torch.bfloat16)
-    dq = d_rows[:nq].view(w.rows, w.hq, 128)
-    dk = d_rows[nq:nq + nk].view(nst, w.hkv, 128)
-    dv = d_rows[nq + nk:].view(nst, w.hkv, 128)
-    hout = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16).pin_memory()
+    feed = FreshInputs(w, torch, 2, extra=dyn_cap)
+    nin = feed.nbytes                              # a multiple of 16
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    if zero_copy:
+        views = [feed.split(hb) for hb in feed.buf]
+        dyn = [hb[nin:] for hb in feed.buf]
+        dst = hout
+    else:
+        d = torch.empty(nin + dyn_cap, dtype=torch.uint8, device="cuda")
+        views = [feed.split(d)] * 2
+        dyn = [d[nin:]] * 2
+        dst = out
     sidx = np.arange(nst, dtype=np.int32)
     s = torch.cuda.current_stream()
     sh = s.cuda_stream
     L = w.streams[0].seq_len
     total = warmup + steps
     plans = [B.Plan(), B.Plan()]
-    for pl in plans:
-        pl.set_device(d[in_bytes:])                # in_bytes is a multiple of 16
+    for k in range(2):
+        plans[k].set_device(dyn[k])
     ev = torch.cuda.Event()
     b = 2 if w.kv_dtype == "bf16" else 1
     t_launch, t_plan = [], []
     kvb = 0
 
     def plan_step(i):
-        pl = plans[i % 2]
+        k = i % 2
         n = L - total + 1 + i
         for j in range(nst):
             tab.set_seq_len(j, n)
         rp = np.full(nst, n - 1, np.int32)
+        pl = plans[k]
         pl.clear()
-        pl.decode_append(cache, tab, dk, dv, dq, sidx, rp, w.softmax_scale, sc, out)
-        pl.pack(h[i % 2][in_bytes:])
+        q, kk, vv = views[k]
+        pl.decode_append(cache, tab, kk, vv, q, sidx, rp, w.softmax_scale, sc, dst)
+        pl.pack(feed.buf[k][nin:])
+        feed.write(i)
         return n
 
     plan_step(1)
     n = plan_step(0)
     nb = plans[0].dyn_bytes()
-    d[:in_bytes + nb].copy_(h[0][:in_bytes + nb], non_blocking=True)
+    if not zero_copy:
+        d[:nin + nb].copy_(feed.buf[0][:nin + nb], non_blocking=True)
     plans[0].launch()                              # sets the kernels up before capture
     torch.cuda.synchronize()
     cap = torch.cuda.Stream()
     for k in range(2):
-        plans[k].capture(before=[(d, h[k], in_bytes + nb)], after=[(hout, out, hout.numel() * 2)],
-                         stream=cap)
+        if zero_copy:
+            plans[k].capture(stream=cap)
+        else:
+            plans[k].capture(before=[(d, feed.buf[k], nin + nb)],
+                             after=[(hout, out, hout.numel() * 2)], stream=cap)
     torch.cuda.synchronize()
     t0 = None
     for i in range(total):
@@ -494,7 +542,7 @@ def time_e2e_device(w, torch, B, ctx, steps, warmup):
         tab.set_seq_len(j, st.seq_len)
     qo = w.rows * w.hq * 128 * 2 * 2
     return (dt, kvb / steps + qo, statistics.median(t_launch[warmup:]), statistics.median(t_plan),
-            nb, dev_us)
+            nin + nb, hout.numel() * 2, dev_us)
 
 
 def graph_device_us(torch, replay, n):
@@ -520,19 +568,22 @@ def time_e2e_calls(w, torch, B, ctx, steps, warmup, in_flight=1):
     step, so every call is planned anew (lengths, splits, CTA ranges): step i
     of n has length L - n + 1 + i (L = the workload's 8,192), writes each
     stream's new K/V row at its last position and decodes that row.  Per step:
-    one copy of the step's inputs (q and the new K/V rows, one pinned buffer)
-    to the device, tfpa_decode_append (the new rows stored and decoded), the
-    output copied back to
-    pinned host memory, and the host waits for it.  With in_flight = 2 the
-    host enqueues step i + 1 before it waits for step i's output (double-
-    buffered inputs and outputs).  Returns (s per step, KV + Q + O bytes per
-    step on average, host us per tfpa_decode_append call, 0.0,
-    h2d bytes, d2h bytes)."""
+    one copy of the step's inputs (q and the new K/V rows, one pinned buffer,
+    written by the host while the step before ran) to the device,
+    tfpa_decode_append (the new rows stored and decoded), the output copied
+    back to pinned host memory, and the host waits for it.  With in_flight =
+    2 the host enqueues step i + 1 before it waits for step i's output
+    (double-buffered outputs).  Returns (s per step, KV + Q + O bytes per
+    step on average, host us per tfpa_decode_append call, 0.0, h2d bytes,
+    d2h bytes)."""
     cache, segs, _, sc, out0 = ctx
     nst = len(w.streams)
     assert list(w.row_seg) == list(range(nst)), "one decode row per stream"
     tab = B.SegTable(segs)
-    bufs = [e2e_buffers(w, torch, nst) for _ in range(in_flight)]
+    feed = FreshInputs(w, torch, in_flight + 1)
+    d_in = [torch.empty(feed.nbytes, dtype=torch.uint8, device="cuda") for _ in range(in_flight)]
+    dviews = [feed.split(d) for d in d_in]
+    houts = [torch.empty(out0.shape, dtype=out0.dtype).pin_memory() for _ in range(in_flight)]
     outs = [out0] + [torch.empty_like(out0) for _ in range(in_flight - 1)]
     evs = [torch.cuda.Event() for _ in range(in_flight)]
     sidx = np.arange(nst, dtype=np.int32)
@@ -546,18 +597,18 @@ def time_e2e_calls(w, torch, B, ctx, steps, warmup, in_flight=1):
     b, kvb = (2 if w.kv_dtype == "bf16" else 1), 0
 
     def enqueue(i, k):
-        h_in, d_in, dq, dk, dv, hout = bufs[k]
+        dq, dk, dv = dviews[k]
         n = L - total + 1 + i
         for j in range(nst):
             tab.set_seq_len(j, n)
         rp = pos[k]
         rp.fill(n - 1)
-        d_in.copy_(h_in, non_blocking=True)
+        d_in[k].copy_(feed.rows(i), non_blocking=True)
         t0 = time.perf_counter_ns()
         B.tfpa_decode_append(cache, tab, dk, dv, dq, sidx, rp, w.softmax_scale, sc, outs[k],
                              stream=sh)
         t1 = time.perf_counter_ns()
-        hout.copy_(outs[k], non_blocking=True)
+        houts[k].copy_(outs[k], non_blocking=True)
         evs[k].record(s)
         return n, (t1 - t0) / 1e3, 0.0
 
@@ -568,6 +619,7 @@ def time_e2e_calls(w, torch, B, ctx, steps, warmup, in_flight=1):
             if i - first >= in_flight:
                 evs[k].synchronize()            # the output of step i - in_flight is home
             n, a, d = enqueue(i, k)
+            feed.write(i + 1)     # its buffer's last step, i - in_flight, is done
             if keep:
                 t_w.append(a)
                 t_d.append(d)
@@ -575,6 +627,7 @@ def time_e2e_calls(w, torch, B, ctx, steps, warmup, in_flight=1):
         for k in range(in_flight):
             evs[k].synchronize()
 
+    feed.write(0)
     run(0, warmup, False)
     t0 = time.perf_counter()
     run(warmup, steps, True)
@@ -582,9 +635,8 @@ def time_e2e_calls(w, torch, B, ctx, steps, warmup, in_flight=1):
     for j, st in enumerate(w.streams):          # back to the workload's lengths
         tab.set_seq_len(j, st.seq_len)
     qo = w.rows * w.hq * 128 * 2 * 2
-    h2d = bufs[0][0].numel() * 2
-    return (dt, kvb / steps + qo, statistics.median(t_w), statistics.median(t_d), h2d,
-            bufs[0][5].numel() * 2)
+    return (dt, kvb / steps + qo, statistics.median(t_w), statistics.median(t_d), feed.nbytes,
+            houts[0].numel() * 2)
 
 
 def host_cover(torch):
@@ -957,9 +1009,14 @@ def main():
         e2e_graph_s, e2e_graph_dev_us = time_e2e_graph(w, torch, B, ctx, n_e2e, args.warmup)
         # three runs of the loop; the line reports the median run and lists
         # all three (a transient on the shared host can slow one run)
-        e2e_runs = [time_e2e_device(w, torch, B, ctx, n_e2e, args.warmup) for _ in range(3)]
+        e2e_runs = [time_e2e_device(w, torch, B, ctx, n_e2e, args.warmup, zero_copy=True)
+                    for _ in range(3)]
         e2e_runs = [(max_over_ranks(dist, torch, r[0]),) + tuple(r[1:]) for r in e2e_runs]
         e2e_dev = sorted(e2e_runs, key=lambda r: r[0])[1]
+        ce_runs = [time_e2e_device(w, torch, B, ctx, n_e2e, args.warmup, zero_copy=False)
+                   for _ in range(3)]
+        ce_runs = [(max_over_ranks(dist, torch, r[0]),) + tuple(r[1:]) for r in ce_runs]
+        e2e_ce = sorted(ce_runs, key=lambda r: r[0])[1]
         del ctx
         s3, p3, ctx3, _ = time_decode(w3, torch, B, max(10, args.steps // 4), args.warmup, None)
         del ctx3
@@ -1087,24 +1144,38 @@ def main():
                      "partial_ms": partial_ms},
         "cpu_baseline": cpu,
         "e2e": {"value": world * e2e_dev[1] / e2e_dev[0] / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": e2e[4] + e2e_dev[4], "d2h_bytes_per_step": e2e[5],
-                "h2d_copies_per_step": 1,
+                "h2d_bytes_per_step": e2e_dev[4], "d2h_bytes_per_step": e2e_dev[5],
+                "h2d_copies_per_step": 0,
+                "transfer": "zero-copy: the kernels read the step's q, new K/V rows and packed "
+                            "plan data from pinned host memory and the merge writes the output "
+                            "to pinned host memory, over the host link (NVLink-C2C), inside "
+                            "the timed step; the host writes each step's inputs anew",
                 "ms_per_step": e2e_dev[0] * 1e3, "vs_device_step": e2e_dev[0] * 1e3 / step_ms,
                 "host_us_per_call": {"tfpa_plan_replay": e2e_dev[2],
-                                     "planning_and_packing_a_step_overlapped": e2e_dev[3]},
+                                     "planning_packing_and_writing_a_step_overlapped":
+                                         e2e_dev[3]},
                 "steps": n_e2e,
                 "how": "a decode loop through the public API with host buffers, one step at a "
                        "time: each stream one position longer every step (%d..%d), every step "
                        "planned anew (tfpa_plan_decode_append, two plans in device "
-                       "mode, alternating) and packed (tfpa_plan_dyn_pack) while the previous "
-                       "step runs; per step one tfpa_plan_replay of the plan's CUDA graph "
-                       "(tfpa_plan_capture, once per plan): "
-                       "one copy of q, the new K/V rows and the packed lengths/splits/CTA "
-                       "ranges, the planned launches (tfpa_plan_launch), output copy; the "
+                       "mode, alternating) and packed (tfpa_plan_dyn_pack) into its plan's "
+                       "pinned buffer, and its inputs written there by the host, while the "
+                       "previous step runs; per step one tfpa_plan_replay of the plan's CUDA "
+                       "graph (tfpa_plan_capture, once per plan: the planned launches); the "
                        "host waits for the output before the next step; host times are host "
                        "clock, median" % (w.streams[0].seq_len - n_e2e + 1, w.streams[0].seq_len),
-                "packed_bytes_per_step": e2e_dev[4],
-                "graph_device_us_per_step": e2e_dev[5],
+                "packed_bytes_per_step": e2e_dev[4] - e2e[4],
+                "graph_device_us_per_step": e2e_dev[6],
+                "copy_engine": {
+                    "value": world * e2e_ce[1] / e2e_ce[0] / 1e9, "unit": "GB/s",
+                    "ms_per_step": e2e_ce[0] * 1e3, "vs_device_step": e2e_ce[0] * 1e3 / step_ms,
+                    "h2d_bytes_per_step": e2e_ce[4], "d2h_bytes_per_step": e2e_ce[5],
+                    "h2d_copies_per_step": 1,
+                    "host_us_per_call": {"tfpa_plan_replay": e2e_ce[2]},
+                    "graph_device_us_per_step": e2e_ce[6],
+                    "how": "the same loop with the inputs, packed data and output in device "
+                           "memory: each graph is one copy of the pinned buffer (rows and "
+                           "packed data) to the device, the launches and the output copy"},
                 "planned_calls": {
                     "value": world * e2e_plan[1] / e2e_plan[0] / 1e9, "unit": "GB/s",
                     "ms_per_step": e2e_plan[0] * 1e3,
@@ -1123,6 +1194,7 @@ def main():
                           "spread_pct": 100 * (max(r[0] for r in e2e_runs) -
                                                min(r[0] for r in e2e_runs)) / e2e_dev[0],
                           "reported": "median of the three runs",
+                          "copy_engine_ms_per_step": [r[0] * 1e3 for r in ce_runs],
                           "planned_calls_ms_per_step": [e2e_plan[0] * 1e3, e2e_plan_aa[0] * 1e3]},
         "e2e_two_in_flight": {
             "value": world * e2e_pipe[1] / e2e_pipe[0] / 1e9, "unit": "GB/s",

@@ -34,6 +34,20 @@
  * creates (a plan may own a CUDA graph, see tfpa_plan_capture), and never
  * synchronises the stream: all work is enqueued on `stream`.
  *
+ * Pinned host memory on the decode path.  Where DEVICE is marked below for
+ * q, k_rows, v_rows, out or lse of tfpa_decode, tfpa_decode_tree,
+ * tfpa_decode_append, tfpa_merge, tfpa_write_kv and tfpa_write_kv_rope (and
+ * their plans), and for a device-mode plan's buffer, page-locked host memory
+ * mapped at its own address (cudaHostAlloc / cudaMallocHost under unified
+ * addressing, or cudaHostRegister with cudaHostRegisterMapped) may stand in:
+ * the kernels read and write it with plain loads and stores over the host
+ * link (NVLink-C2C on a Grace-Blackwell node), with no copy-engine copy.
+ * Data the host writes there before it enqueues a call is what the call
+ * reads; results are the host's once the stream has passed the call.  A
+ * slice with rows for the tensor-core verify path and tfpa_prefill load q
+ * by TMA from device memory only: host memory there returns TFPA_EINVAL.
+ * Memory that is not page-locked is not supported (and not checked).
+ *
  * Threads.  Calls may be made from several host threads at once, on any
  * streams and devices: each thread builds its launch parameters in its own
  * buffers and no call takes a lock on that path (the pool ledger and the
@@ -370,7 +384,10 @@ int tfpa_plan_launch(const tfpa_plan* plan, cudaStream_t stream);
  * packs and replays.
  *
  * tfpa_plan_set_device(plan, dyn, bytes): dyn = DEVICE buffer, 16-byte
- *   aligned, `bytes` long, or NULL to go back to parameter mode.  Only on an
+ *   aligned, `bytes` long, or NULL to go back to parameter mode.  dyn may
+ *   be mapped pinned host memory (see "Pinned host memory" above): then
+ *   tfpa_plan_dyn_pack may write the packed data into dyn itself, with no
+ *   copy, while no launch that reads it is pending.  Only on an
  *   empty plan (after create or clear), else TFPA_EINVAL.  The plan keeps the
  *   pointer; tfpa_plan_clear keeps the mode.  A planning call whose slots do
  *   not fit returns TFPA_ECAPACITY; rows that would take the tensor-core

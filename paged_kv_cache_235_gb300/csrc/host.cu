@@ -176,6 +176,20 @@ int get_qmap(const void* q, int hq, int rows, int box_heads, int box_rows, CUten
 }
 
 // ------------------------------------------------------------ validation
+// Q tiles of the prompt and verify paths are loaded by TMA, from device (or
+// managed) memory only: pinned host memory, which the decode path takes for
+// q, is refused for them before anything is enqueued.
+int check_tma_source(const void* q) {
+  if (dry_run()) return TFPA_OK;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+    cudaGetLastError();   // the failed query's error stays with this call
+    return TFPA_EINVAL;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged ? TFPA_OK
+                                                                              : TFPA_EINVAL;
+}
+
 int32_t pages_of(int32_t L) { return (L + kPage - 1) / kPage; }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -535,6 +549,12 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
   if ((e = check_device())) return e;
   const bool fp8 = c->dtype == TFPA_FP8_E4M3;
   const int G = c->hq / c->hkv;
+  if (G <= kVerifyVectors)
+    for (const Run& r : runs)
+      if ((r.nrows * G + 15) / 16 >= 4) {   // a run for the tensor-core verify path
+        if ((e = check_tma_source(q))) return e;
+        break;
+      }
   if (k_rows || v_rows) {
     if (!k_rows || !v_rows || !aligned(k_rows, 16) || !aligned(v_rows, 16)) return TFPA_EINVAL;
     bool fuse = true;
@@ -1240,7 +1260,7 @@ extern "C" int tfpa_prefill(const tfpa_cache* c, const tfpa_seg* segs, int32_t n
   thread_local std::vector<Run> runs;   // reused by every call of this thread
   if ((e = build_runs(segs, nseg, row_seg, row_pos, rows, runs))) return e;
   if (rows == 0) return TFPA_OK;
-  if ((e = check_device())) return e;
+  if ((e = check_device()) || (e = check_tma_source(q))) return e;
   const bool fp8 = c->dtype == TFPA_FP8_E4M3;
   const int G = c->hq / c->hkv;
   const int npairs = (G + 1) / 2;

@@ -162,3 +162,28 @@ def assert_close(got: np.ndarray, ref: np.ndarray, tol: float, what: str = ""):
         i = np.unravel_index(np.argmax(err - bound), err.shape)
         raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside {tol}; worst at {i}: "
                              f"got {got[i]} ref {ref[i]} (max abs err {err.max():.3e})")
+
+
+def append_rows(w, rows_per_stream, seed):
+    """The last rows_per_stream positions of every stream, with new K / V
+    and q (device bf16): row_seg, row_pos, k, v, q."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    rs, rp = [], []
+    for s, st in enumerate(w.streams):
+        for i in range(rows_per_stream):
+            rs.append(s)
+            rp.append(st.seq_len - rows_per_stream + i)
+    n = len(rs)
+    k = torch.randn(n, w.hkv, 128, generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn(n, w.hkv, 128, generator=g, device="cuda").to(torch.bfloat16)
+    q = torch.randn(n, w.hq, 128, generator=g, device="cuda").to(torch.bfloat16)
+    return np.array(rs, np.int32), np.array(rp, np.int32), k, v, q
+
+
+def same_cache(ga, gb):
+    """Two GpuCases' pools and slabs hold the same bytes."""
+    assert torch.equal(ga.k_pool, gb.k_pool) and torch.equal(ga.v_pool, gb.v_pool)
+    for sa, sb in zip(ga.segs, gb.segs):
+        if sa.page_table is None:
+            assert torch.equal(sa.k_slab, sb.k_slab) and torch.equal(sa.v_slab, sb.v_slab)

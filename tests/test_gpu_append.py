@@ -12,31 +12,10 @@ import torch
 from paged_kv_cache_235_gb300 import binding as B
 from paged_kv_cache_235_gb300 import workloads as wl
 from tests.gpu_cases import GpuCase, bits, fp8_scales
+from tests.gpu_cases import append_rows as _rows
+from tests.gpu_cases import same_cache as _same_cache
 
 pytestmark = pytest.mark.gpu
-
-
-def _rows(w, rows_per_stream, seed):
-    """The last rows_per_stream positions of every stream, with new K / V."""
-    g = torch.Generator(device="cuda")
-    g.manual_seed(seed)
-    rs, rp = [], []
-    for s, st in enumerate(w.streams):
-        for i in range(rows_per_stream):
-            rs.append(s)
-            rp.append(st.seq_len - rows_per_stream + i)
-    n = len(rs)
-    k = torch.randn(n, w.hkv, 128, generator=g, device="cuda").to(torch.bfloat16)
-    v = torch.randn(n, w.hkv, 128, generator=g, device="cuda").to(torch.bfloat16)
-    q = torch.randn(n, w.hq, 128, generator=g, device="cuda").to(torch.bfloat16)
-    return np.array(rs, np.int32), np.array(rp, np.int32), k, v, q
-
-
-def _same_cache(ga, gb):
-    assert torch.equal(ga.k_pool, gb.k_pool) and torch.equal(ga.v_pool, gb.v_pool)
-    for sa, sb in zip(ga.segs, gb.segs):
-        if sa.page_table is None:
-            assert torch.equal(sa.k_slab, sb.k_slab) and torch.equal(sa.v_slab, sb.v_slab)
 
 
 def _pair(w, rows_per_stream, cap_rows=128, seed=21):
