@@ -129,3 +129,24 @@ def test_host_q_refused_where_tma_loads_it():
     with pytest.raises(B.TfpaError) as e:
         B.tfpa_prefill(gp.cache, gp.segs, qp, wp.row_seg, wp.row_pos, wp.softmax_scale, op)
     assert e.value.code == B.TFPA_EINVAL
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_kv_write_from_host_rows_equals_device_rows(kv):
+    """tfpa_write_kv and tfpa_write_kv_rope reading the new rows from pinned
+    host memory store the bytes they store from device rows."""
+    w = wl.small("fp8_verify" if kv == "fp8" else "batched_decode")
+    scales = fp8_scales(w) if kv == "fp8" else None
+    ga, gb = GpuCase(w, scales), GpuCase(w, scales)
+    rs, rp, k, v, _ = append_rows(w, 3, 47)
+    hk, hv = _pinned(k), _pinned(v)
+    B.tfpa_write_kv(ga.cache, ga.segs, k, v, rs, rp)
+    B.tfpa_write_kv(gb.cache, gb.segs, hk, hv, rs, rp)
+    cos, sin = wl.rope_table(1e6, 4096)
+    cos_d, sin_d = torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda()
+    rp2 = rp - 3                                    # the three positions before
+    B.tfpa_write_kv_rope(ga.cache, ga.segs, k, v, rs, rp2, cos_d, sin_d)
+    B.tfpa_write_kv_rope(gb.cache, gb.segs, hk, hv, rs, rp2, cos_d, sin_d)
+    torch.cuda.synchronize()
+    same_cache(ga, gb)
+    assert int(ga.err.item()) == 0 and int(gb.err.item()) == 0
