@@ -9,8 +9,9 @@
 // Per CTA (four warpgroups):
 //   warp 12     producer: looks each page up once (PR #2011, "the decode
 //               tiles ... look a page up once"), stages K and V chunks into
-//               shared memory with TMA tiled loads (128B swizzle), 3 stages
-//               of 64 KB;
+//               shared memory with TMA tiled loads (128B swizzle), a ring
+//               of three 64 KB key chunks (bf16: a chunk is one stage;
+//               e4m3: two stages, read by consumer warps 0-3 and 4-7);
 //   warps 0..7  consumers: each takes an eighth of every chunk's keys, runs
 //               QK^T and PV on mma.sync m16n8k16 (bf16, or f16 for e4m3
 //               caches, whose bytes convert to f16 exactly) and an online
@@ -35,8 +36,10 @@
 namespace tfpa {
 namespace {
 
-constexpr int kStages = 3;
-constexpr int kStageBytes = 65536;    // K 32 KB + V 32 KB
+// The ring holds three key chunks (64 KB of K and V each); a chunk arrives
+// as Cfg::kSub stages (see Cfg), at most kMaxStages in the ring.
+constexpr int kRingBytes = 3 * 65536;
+constexpr int kMaxStages = 6;
 constexpr int kConsumerWarps = 8;
 constexpr int kCombineWarp0 = 8;      // warps 8..11
 constexpr int kCombineWarps = 4;
@@ -57,15 +60,24 @@ constexpr int kHalfCols = 128;
 // consumer warps (conflict-free float4 stores and loads).
 constexpr int kCombBytes = kCombineWarps * 16 * 32 * 16;
 constexpr int kMlBytes = kConsumerWarps * 16 * 2 * 4;
-constexpr int kNumBars = 2 * kStages + 7;
+constexpr int kNumBars = 2 * kMaxStages + 7;
 constexpr int kSmemBytes =
-    kStages * kStageBytes + kCombBytes + kMlBytes + kStages * 4 + 8 + kNumBars * 8 + 1024;
+    kRingBytes + kCombBytes + kMlBytes + kMaxStages * 4 + 8 + kNumBars * 8 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 template <bool FP8>
 struct Cfg {
-  static constexpr int kChunk = FP8 ? 256 : 128;      // keys per stage
+  static constexpr int kChunk = FP8 ? 256 : 128;      // keys per chunk
+  // e4m3: a chunk in two stages of 128 keys (K 16 KB + V 16 KB), the first
+  // read by consumer warps 0-3, the second by 4-7, so a stage is released
+  // after half the warps' work (fp8 verify partial 174.2 -> 172.5 us);
+  // bf16: one stage of 128 keys (two stages measured 0.7 % slower).
+  static constexpr int kSub = FP8 ? 2 : 1;
+  static constexpr int kStages = 3 * kSub;
+  static constexpr int kStageBytes = 65536 / kSub;
+  static constexpr int kStageKeys = kChunk / kSub;     // 128 either way
+  static constexpr int kSubWarps = kConsumerWarps / kSub;   // warps reading a stage
   static constexpr int kKeysPerWarp = kChunk / kConsumerWarps;
   static constexpr int kNT = kKeysPerWarp / 8;         // score n-tiles per warp
   static constexpr int kKS = kKeysPerWarp / 16;        // PV k-steps per warp
@@ -216,9 +228,8 @@ __device__ __forceinline__ bool load_item(const DecodeParams& p, const RunInfo& 
     const CUtensorMap* mk = &p.maps[ru.src].k;
     const CUtensorMap* mv = &p.maps[ru.src].v;
     int cached_page = -1, cached_pid = 0;
-    for (int k0 = klo; k0 < khi; k0 += C::kChunk, ++stage) {
-      const int buf = stage % kStages;
-      const uint32_t ph = (stage / kStages) & 1;
+    // a chunk (and so each of its stages) lies within one page
+    for (int k0 = klo; k0 < khi; k0 += C::kChunk) {
       const int page = k0 >> 8;
       int y, bad = 0;
       if (ru.page_table) {
@@ -236,19 +247,23 @@ __device__ __forceinline__ bool load_item(const DecodeParams& p, const RunInfo& 
       } else {
         y = x.g * ru.slab_cap + k0;
       }
-      if (!mbar_wait(&empty[buf], ph ^ 1, p.err_flag)) return false;
-      stage_bad[buf] = bad;
-      uint64_t* fb = &full[buf];
-      uint8_t* sb = stage_mem + (size_t)buf * kStageBytes;
-      mbar_arrive_expect_tx(fb, kStageBytes);
-      if (FP8) {
-        tma_load_2d(sb, mk, 0, y, fb);
-        tma_load_2d(sb + 32768, mv, 0, y, fb);
-      } else {
-        tma_load_2d(sb, mk, 0, y, fb);
-        tma_load_2d(sb + 16384, mk, 64, y, fb);
-        tma_load_2d(sb + 32768, mv, 0, y, fb);
-        tma_load_2d(sb + 49152, mv, 64, y, fb);
+      for (int h = 0; h < C::kSub; ++h, ++stage, y += C::kStageKeys) {
+        const int buf = stage % C::kStages;
+        const uint32_t ph = (stage / C::kStages) & 1;
+        if (!mbar_wait(&empty[buf], ph ^ 1, p.err_flag)) return false;
+        stage_bad[buf] = bad;
+        uint64_t* fb = &full[buf];
+        uint8_t* sb = stage_mem + (size_t)buf * C::kStageBytes;
+        mbar_arrive_expect_tx(fb, C::kStageBytes);
+        if (FP8) {
+          tma_load_2d(sb, mk, 0, y, fb);
+          tma_load_2d(sb + C::kStageBytes / 2, mv, 0, y, fb);
+        } else {
+          tma_load_2d(sb, mk, 0, y, fb);
+          tma_load_2d(sb + C::kStageBytes / 4, mk, 64, y, fb);
+          tma_load_2d(sb + C::kStageBytes / 2, mv, 0, y, fb);
+          tma_load_2d(sb + 3 * C::kStageBytes / 4, mv, 64, y, fb);
+        }
       }
     }
   }
@@ -337,11 +352,11 @@ struct CombBars {
   uint64_t* done;        // the combiners finished the item (fold buffer free)
 };
 
-// This warp's kKeysPerWarp keys from key wk0 of the stage chunk at sb (k0 =
-// the chunk's first key): scores, the causal or ancestor mask, the online
-// softmax, and O += P V.
+// This warp's kKeysPerWarp keys, keys key_base.. at rows r0.. of the stage
+// at sb: scores, the causal or ancestor mask, the online softmax, and
+// O += P V.
 template <bool FP8, bool GEN>
-__device__ __forceinline__ void attend_block(uint32_t sb, int wk0, int k0, int seq_len,
+__device__ __forceinline__ void attend_block(uint32_t sb, int r0, int key_base, int seq_len,
                                              const uint32_t (&qr)[2][16], const int (&lim)[2],
                                              const float (&sc)[2], const uint64_t (&anc)[2],
                                              int tree_low, int gq, int c, float (&m_run)[2],
@@ -350,13 +365,12 @@ __device__ __forceinline__ void attend_block(uint32_t sb, int wk0, int k0, int s
   constexpr int kNT = C::kNT;             // score n-tiles
   constexpr int kKS = C::kKS;             // PV k-steps
   constexpr int kKeys = C::kKeysPerWarp;
-  const int key_base = k0 + wk0;
   // ---- S = Q K^T over this warp's keys
   float s[kNT][4];
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt) {
     s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-    const int kr = wk0 + nt * 8 + gq;
+    const int kr = r0 + nt * 8 + gq;
     uint32_t kb[16];
     if (FP8) {
 #pragma unroll
@@ -372,7 +386,7 @@ __device__ __forceinline__ void attend_block(uint32_t sb, int wk0, int k0, int s
     } else {
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        const uint32_t base = sb + (ch >> 1) * 16384u;
+        const uint32_t base = sb + (ch >> 1) * (uint32_t)(C::kStageBytes / 4);
         const uint4 w = lds128(swz128(base, kr, 2 * c + (ch & 1)));
         kb[4 * ch + 0] = w.x;
         kb[4 * ch + 1] = w.y;
@@ -448,7 +462,7 @@ __device__ __forceinline__ void attend_block(uint32_t sb, int wk0, int k0, int s
     }
   }
   // ---- O += P V
-  const uint32_t vb = sb + 32768u;
+  const uint32_t vb = sb + (uint32_t)(C::kStageBytes / 2);
 #pragma unroll
   for (int kk = 0; kk < kKS; ++kk) {
     uint32_t a[4];
@@ -463,14 +477,14 @@ __device__ __forceinline__ void attend_block(uint32_t sb, int wk0, int k0, int s
       a[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
       a[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
     }
-    const int kv0 = wk0 + 16 * kk + 2 * c;   // rows kv0, kv0+1, kv0+8, kv0+9
+    const int kv0 = r0 + 16 * kk + 2 * c;    // rows kv0, kv0+1, kv0+8, kv0+9
     const int krow[4] = {kv0, kv0 + 1, kv0 + 8, kv0 + 9};
     if (FP8) {
       uint32_t w[4][4];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint4 t = lds128(swz128(vb, krow[q4], gq));
-        if (k0 + krow[q4] >= seq_len) t = make_uint4(0, 0, 0, 0);
+        if (key_base - r0 + krow[q4] >= seq_len) t = make_uint4(0, 0, 0, 0);
         w[q4][0] = t.x; w[q4][1] = t.y; w[q4][2] = t.z; w[q4][3] = t.w;
       }
 #pragma unroll
@@ -493,8 +507,8 @@ __device__ __forceinline__ void attend_block(uint32_t sb, int wk0, int k0, int s
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint4 t0 = lds128(swz128(vb, krow[q4], gq));
-        uint4 t1 = lds128(swz128(vb + 16384u, krow[q4], gq));
-        if (k0 + krow[q4] >= seq_len) {
+        uint4 t1 = lds128(swz128(vb + (uint32_t)(C::kStageBytes / 4), krow[q4], gq));
+        if (key_base - r0 + krow[q4] >= seq_len) {
           t0 = make_uint4(0, 0, 0, 0);
           t1 = t0;
         }
@@ -521,7 +535,7 @@ __device__ void consumer(const DecodeParams& p, const DecodeDyn& D, uint8_t* sta
   const int lane = threadIdx.x & 31;
   const int gq = lane >> 2, c = lane & 3;
   const uint32_t sbase = smem_u32(stage_mem);
-  uint32_t stage = 0;
+  uint32_t chunk = 0;                       // key chunks read so far
   int ib, ie;
   cta_items(D, ib, ie);
   int rh = ib < ie ? run_of(D, ib) : 0;   // run of the current item
@@ -558,14 +572,18 @@ __device__ void consumer(const DecodeParams& p, const DecodeDyn& D, uint8_t* sta
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
-    for (int k0 = klo; k0 < khi; k0 += C::kChunk, ++stage) {
-      const int buf = stage % kStages;
-      const uint32_t ph = (stage / kStages) & 1;
+    // Chunk n's stage n * kSub + h holds the keys of warps h * kSubWarps ..
+    // (h + 1) * kSubWarps - 1; this warp reads its stage only.
+    for (int k0 = klo; k0 < khi; k0 += C::kChunk, ++chunk) {
+      const uint32_t st = chunk * C::kSub + sub0 / C::kSubWarps;
+      const int buf = st % C::kStages;
+      const uint32_t ph = (st / C::kStages) & 1;
       if (!mbar_wait(&full[buf], ph, p.err_flag)) return;
-      const uint32_t sb = sbase + (uint32_t)buf * kStageBytes;
+      const uint32_t sb = sbase + (uint32_t)buf * C::kStageBytes;
       const int wk0 = sub0 * C::kKeysPerWarp;
+      const int r0 = wk0 - (sub0 / C::kSubWarps) * C::kStageKeys;
       if (!stage_bad[buf] && k0 + wk0 <= maxlim)
-        attend_block<FP8, GEN>(sb, wk0, k0, ru.seq_len, qr, lim, sc, anc, tree_low, gq, c,
+        attend_block<FP8, GEN>(sb, r0, k0 + wk0, ru.seq_len, qr, lim, sc, anc, tree_low, gq, c,
                                m_run, l_run, o);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[buf]);
@@ -852,23 +870,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* stage_mem = smem;
-  float4* fold = reinterpret_cast<float4*>(smem + kStages * kStageBytes);
-  float* ml_buf = reinterpret_cast<float*>(smem + kStages * kStageBytes + kCombBytes);
+  float4* fold = reinterpret_cast<float4*>(smem + kRingBytes);
+  float* ml_buf = reinterpret_cast<float*>(smem + kRingBytes + kCombBytes);
   int* stage_bad = reinterpret_cast<int*>(ml_buf + kConsumerWarps * 16 * 2);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stage_bad + kStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stage_bad + kMaxStages);
   int* merge_flag = reinterpret_cast<int*>(tmem_slot + 1);
   uint64_t* bars = reinterpret_cast<uint64_t*>(
       (reinterpret_cast<uintptr_t>(merge_flag + 1) + 7) & ~uintptr_t(7));
   uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* cbar = bars + 2 * kStages;
+  uint64_t* empty = bars + kMaxStages;
+  uint64_t* cbar = bars + 2 * kMaxStages;
   CombBars cb{cbar, cbar + 2, cbar + 4, cbar + 5, cbar + 6};
 
   const int warp = threadIdx.x >> 5;
+  // With the launch data in the parameters, the producer's first page id is
+  // brought into L2 while the block sets up: a prefetch reads no value, so
+  // it may come before the wait for the previous grid (which can write the
+  // table).  Batched decode partial 46.6 -> 45.9 us; not with append, whose
+  // producer stores the new rows first (the step measured 0.4 us slower).
+  if (!DEV && !APPEND && warp == kProducerWarp && (threadIdx.x & 31) == 0) {
+    int ib, ie;
+    cta_items(D, ib, ie);
+    if (ib < ie) {
+      int r = run_of(D, ib);
+      const Item x = item_of(p, D, ib, r);
+      if (D.runs[x.run].page_table) {
+        int klo, khi;
+        item_keys(p, D, x, klo, khi);
+        prefetch_l2(D.runs[x.run].page_table + (klo >> 8));
+      }
+    }
+  }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < Cfg<FP8>::kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kConsumerWarps);
+      mbar_init(&empty[i], Cfg<FP8>::kSubWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&cb.posted[i], kConsumerWarps);

@@ -639,7 +639,7 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
     bool fused = sliced && nv == 0 && sc->arrive && !anc && !sink.device();
     for (int r = 0; fused && r < nd; ++r) fused = p.d.runs[r].nsplit <= kFusedMergeMaxSplits;
     if (nd > 0) {
-      if ((e = fill_maps(c, segs, ss, fp8, fp8 ? 128 : 64, fp8 ? 256 : 128, p.maps, p.nsrc)))
+      if ((e = fill_maps(c, segs, ss, fp8, fp8 ? 128 : 64, 128, p.maps, p.nsrc)))
         return e;
       p.q = static_cast<const __nv_bfloat16*>(q) + (size_t)base * hd;
       p.anc = anc ? anc + base : nullptr;   // the ancestor table shifts with the rows
