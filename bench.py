@@ -53,7 +53,7 @@ METRIC = "paged decode KV GB/s (% HBM peak); prompt-chunk attn TFLOP/s (% TC pea
 # bench's partial launch), valid only while the kernel's sources hash to the
 # value below: after any change to them the line reports null until the
 # counters are taken again.
-DECODE_TRAFFIC = {"bytes": 268_594_944 + 4_043_008, "sources_sha256_16": "b4575dcee5686bbd"}
+DECODE_TRAFFIC = {"bytes": 268_608_000 + 3_727_104, "sources_sha256_16": "97252c9c62ebf467"}
 DECODE_SOURCES = ["paged_kv_cache_235_gb300/csrc/decode.cu",
                   "paged_kv_cache_235_gb300/csrc/common.cuh",
                   "paged_kv_cache_235_gb300/csrc/params.h",

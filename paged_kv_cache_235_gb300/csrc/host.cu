@@ -373,15 +373,20 @@ extern "C" int32_t tfpa_num_splits(int32_t seq_len) {
 
 namespace {
 
-// Splits of a run on the tensor-core verify path: at least 24 pages (6,144
-// keys, so a tile's fixed costs stay small against its key tiles; 16 and 32
-// measured slower on 65,536-key trees) and at most kMaxSplits per stream;
-// never more splits than the decode path's, so a scratch sized for decode
-// holds them.  A function of the stream's length only, like the decode
-// splits.
+// Splits of a run on the tensor-core verify path: at least 24 pages and at
+// most 7 a stream.  A verify tile carries a fixed cost (set-up, its first
+// loads, a cold first softmax step and the epilogue: about a quarter of a
+// 24-page tile), so a long stream takes a few long tiles.  A function of the
+// stream's length only, like the decode splits, so a stream's bytes do not
+// depend on its batch.  On 65,536-key streams (7 splits of 37 pages), 8
+// streams x 8 kv heads make 448 tiles, 2.95 waves of 152 SMs; 16-node trees
+// took 294 / 345 us (e4m3 / bf16 cache) with 11 splits of 24 pages, 279 /
+// 331 with 9 of 29, 263 / 325 with 7 of 37 and 295 / 348 with 6 of 43.
+// Other batches fill the waves differently.  Never more splits than the
+// decode path's, so a scratch sized for decode holds them.
 int32_t verify_pages_per_split(int32_t seq_len) {
   const int32_t np = pages_of(std::max(seq_len, 1));
-  return std::max<int32_t>(24, (np + kMaxSplits - 1) / kMaxSplits);
+  return std::max<int32_t>(24, (np + 6) / 7);
 }
 int32_t verify_num_splits(int32_t seq_len) {
   const int32_t np = pages_of(std::max(seq_len, 1));

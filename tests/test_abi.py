@@ -119,8 +119,9 @@ def test_prefill_slices():
 
 def test_verify_tiles_and_mixed_launch_order():
     """Verify tiles: kv head x tile of 128 / G rows x split, splits of at
-    least 24 pages; a call with a short and a long run issues the decode
-    partial, then the verify launch, then one merge over both."""
+    least 24 pages and at most 7 a stream; a call with a short and a long
+    run issues the decode partial, then the verify launch, then one merge
+    over both."""
     c = _cache()
     L = 65536
     segs = [B.Seg(L, page_table=3 * FAKE), B.Seg(L, page_table=3 * FAKE)]
@@ -132,17 +133,17 @@ def test_verify_tiles_and_mixed_launch_order():
     assert [(r["kind"], r["row0"], r["rows"], r["runs"]) for r in rec] == [
         ("partial", 0, 17, 1), ("verify", 0, 17, 1), ("merge", 0, 17, 2)]
     v = rec[1]
-    splits = (256 + 23) // 24                     # 65,536 keys = 256 pages, 24 a split
+    splits = 7                                    # 65,536 keys = 256 pages, 37 a split
     assert v["items"] == v["grid"] == 8 * 1 * 1 * splits
     assert rec[0]["items"] == 8 * 1 * B.tfpa_num_splits(L)   # 4 vectors: one m-tile
 
 
 @pytest.mark.parametrize("hq,hkv,rows,kind,count", [
     (32, 8, 12, "partial", 8 * 3 * 32),    # 48 vectors a kv head: decode items
-    (32, 8, 13, "verify", 8 * 1 * 11),     # 52 vectors: 32-row tiles, 11 splits of 24 pages
-    (8, 8, 49, "verify", 8 * 1 * 11),      # one head a group: 128-row tiles
-    (24, 8, 20, "verify", 8 * 1 * 11),     # three heads: 42-row tiles
-    (64, 8, 20, "verify", 8 * 2 * 11),     # eight heads: 16-row tiles, two of them
+    (32, 8, 13, "verify", 8 * 1 * 7),      # 52 vectors: 32-row tiles, 7 splits of 37 pages
+    (8, 8, 49, "verify", 8 * 1 * 7),       # one head a group: 128-row tiles
+    (24, 8, 20, "verify", 8 * 1 * 7),      # three heads: 42-row tiles
+    (64, 8, 20, "verify", 8 * 2 * 7),      # eight heads: 16-row tiles, two of them
     (129, 1, 1, "partial", 1 * 9 * 32),    # a group wider than a tile: decode items
 ])
 def test_kernel_choice_by_query_vectors(hq, hkv, rows, kind, count):
