@@ -862,6 +862,60 @@ def time_decode_calls(w, torch, B, reps, flush, fused_merge=True):
     return statistics.median(times)
 
 
+def time_tiny_layer_calls(torch, B, wl, layers=32, reps=20):
+    """The tiny decode as one layer of a model's decode step: `layers` calls,
+    each with its own pool, page table, queries and scratch (1 MB of KV
+    each), captured after an L2 flush as one CUDA graph; per call = (graph -
+    the same flush alone) / layers, medians over `reps` replays.  The first
+    call meets a cold instruction cache, the others a warm one (no other
+    kernels run between them), and every call's KV is cold."""
+    cases = []
+    for i in range(layers):
+        w = wl.tiny_paged_decode(seed=500 + i)
+        cache, segs, q = device_case(w, torch, B)
+        sc = B.make_scratch(1, w.hq)
+        out = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16, device="cuda")
+        cases.append((w, cache, segs, q, sc, out))
+    flush = L2Flush(torch)
+
+    def calls():
+        for w, cache, segs, q, sc, out in cases:
+            B.tfpa_decode(cache, segs, q, w.row_seg, w.row_pos, w.softmax_scale, sc, out)
+
+    calls()                                    # per-device set-up before capture
+    flush(0)
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g_all, g_flush = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g_all, stream=cap):
+            flush(1)
+            calls()
+        with torch.cuda.graph(g_flush, stream=cap):
+            flush(1)
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+
+    def med(g):
+        t = []
+        for i in range(reps + 3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+            torch.cuda.synchronize()
+            if i >= 3:
+                t.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(t)
+
+    t_all, t_flush = med(g_all), med(g_flush)
+    for _, cache, _, _, _, _ in cases:
+        assert int(cache.err_flag.item()) == 0, "kernel error flag set"
+    return (t_all - t_flush) / layers, t_all, t_flush
+
+
 def time_launch_floor(torch, reps=40):
     """The event-timing floor of a call: an empty event pair, and one and two
     one-element torch kernels between the events (same method as the
@@ -1055,6 +1109,14 @@ def main():
             "note": "1 MB of KV: launch and latency bound, the HBM roofline is out of reach; "
                     "timing_floor is the same event method around nothing and around one "
                     "and two one-element kernels"}
+        lc, lc_all, lc_flush = time_tiny_layer_calls(torch, B, wl)
+        extra["tiny_decode"]["layer_calls"] = {
+            "workload": "32 calls of the same shape, each on its own 1 MB of KV (own pool, "
+                        "page table, queries, scratch), one CUDA graph after an L2 flush, as "
+                        "one attention call per layer of a decode step",
+            "us_per_call": lc, "graph_us": lc_all, "flush_us": lc_flush,
+            "note": "(graph - flush alone) / 32; every call's KV is cold, the instruction "
+                    "cache is warm after the first call"}
         w6 = wl.overcommitted_pool()
         ms6 = time_decode_calls(w6, torch, B, 20, flush=False)
         kv6, qo6 = kv_bytes(w6)
