@@ -70,3 +70,41 @@ def test_counters_return_to_zero_and_repeat_calls_agree():
         if first is None:
             first = bits(out)
         assert np.array_equal(bits(out), first)
+
+
+def test_graph_of_layer_calls_replays_the_direct_bytes():
+    """Tiny calls on caches of their own (one per layer of a decode step, as
+    the bench's layer-call line runs them) captured as one CUDA graph: every
+    replay gives the direct calls' bytes, and each call leaves its arrival
+    counters at zero, so the next replay merges again."""
+    layers = []
+    for i in range(4):
+        w = wl.tiny_paged_decode(seed=500 + i)
+        g = GpuCase(w)
+        sc = B.make_scratch(1, w.hq)
+        out = torch.empty(w.rows, w.hq, 128, dtype=torch.bfloat16, device="cuda")
+        layers.append((w, g, sc, out, g.q()))
+
+    def calls():
+        for w, g, sc, out, q in layers:
+            B.tfpa_decode(g.cache, g.segs, q, w.row_seg, w.row_pos, w.softmax_scale, sc, out)
+
+    calls()
+    torch.cuda.synchronize()
+    ref = [bits(out).copy() for _, _, _, out, _ in layers]
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            calls()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        for _, _, _, out, _ in layers:
+            out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for (w, g, sc, out, q), r in zip(layers, ref):
+            assert np.array_equal(bits(out), r)
+            assert int(sc.arrive.abs().sum().item()) == 0
+            assert int(g.err.item()) == 0
