@@ -227,7 +227,8 @@ def cpu_oracle_sample(seconds: float = 12.0):
     return {"value": bytes_ / dt / 1e9, "unit": "GB/s", "cores": os.cpu_count(),
             "kind": "oracle", "calls": n, "s_per_call": dt,
             "sample": "stream 0 of the batched-decode workload: 1 row x 32 heads over 8,192 "
-                      "bf16 keys (1/8 of a step), float64 NumPy, repeated for ~%ds" % seconds}
+                      "bf16 keys (1/8 of a step), float64 NumPy, "
+                      + ("repeated for ~%ds" % seconds if seconds > 0 else "one call")}
 
 
 # --------------------------------------------------------------------- timing
