@@ -508,3 +508,23 @@ def test_append_stores_in_the_partial_kernel_where_it_can():
             B.tfpa_decode_append(c, segs, 10 * FAKE + 8, 11 * FAKE, 4 * FAKE, np.array([0]),
                                  np.array([3999]), 0.088, sc, 7 * FAKE, stream=0)
     assert e.value.code == B.TFPA_EINVAL and rec == []
+
+
+@pytest.mark.parametrize("pages,splits", [(1, 1), (24, 1), (25, 2), (59, 3), (168, 7),
+                                          (169, 7), (200, 7), (256, 7), (1024, 7)])
+def test_verify_splits_follow_the_stream_length(pages, splits):
+    """Verify tiles split a stream into pieces of at least 24 pages and at
+    most 7 pieces; the count (kv heads x row tiles x splits in the launch
+    record) depends on the stream's length only."""
+    c = _cache()
+    L = pages * 256
+    rows = 16                                       # 64 vectors a kv head: one row tile
+    segs = [B.Seg(L, page_table=3 * FAKE)]
+    with B.record_launches() as rec:
+        B.tfpa_decode(c, segs, 4 * FAKE, np.zeros(rows), np.arange(L - rows, L), 0.088,
+                      B.Scratch(5 * FAKE, 6 * FAKE, 128), 7 * FAKE)
+    v = [r for r in rec if r["kind"] == "verify"]
+    assert len(v) == 1
+    assert v[0]["items"] == 8 * splits
+    pps = max(24, -(-pages // 7))
+    assert splits == -(-pages // pps)
