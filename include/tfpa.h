@@ -228,6 +228,18 @@ int tfpa_restore_kv(const tfpa_cache* cache, const tfpa_seg* seg, int32_t p0, in
 int32_t tfpa_pages_per_split(int32_t seq_len);
 int32_t tfpa_num_splits(int32_t seq_len);
 
+/* The split count of each row as tfpa_decode_partial leaves its partials
+ * (the nsplit to pass to tfpa_merge for the same rows).  Rows are grouped
+ * into runs (consecutive rows of one segment at consecutive positions); a
+ * run of at least 49 query vectors per kv head (ceil(nrows * G / 16) >= 4,
+ * G = hq / hkv <= 128) takes the tensor-core verify path, whose splits are
+ * at least 24 pages and at most 7 a stream; every other row has
+ * tfpa_num_splits(seq_len).  Host only (no GPU work): nsplit is HOST
+ * int32[rows].  TFPA_EINVAL / TFPA_ERANGE as tfpa_decode. */
+int tfpa_row_splits(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                    const int32_t* row_seg, const int32_t* row_pos, int32_t rows,
+                    int32_t* nsplit);
+
 /* KV write (the KV store kernels that write a stream's page run, PR #1373,
  * "What changes"): row r's K and V for every kv head go to position
  * row_pos[r] of segment row_seg[r], through its page table or slab.  bf16
@@ -240,7 +252,9 @@ int tfpa_write_kv(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
 
 /* Decode/verify split-K partials (Issue #1344, "Mechanism": the partial
  * kernels write pm/pl/po, then attn_merge).  For each row r < rows, head h
- * and split s < tfpa_num_splits(seq_len): (m, l, o) at scratch row r.
+ * and split s < nsplit[r]: (m, l, o) at scratch row r, where nsplit[r] is
+ * what tfpa_row_splits gives for the same rows (tfpa_num_splits(seq_len),
+ * or fewer for rows of a run on the tensor-core verify path).
  * Requires rows <= scratch->cap_rows (TFPA_ECAPACITY otherwise). */
 int tfpa_decode_partial(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
                         const void* q, const int32_t* row_seg, const int32_t* row_pos,

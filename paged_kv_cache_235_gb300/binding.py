@@ -34,7 +34,7 @@ EXPORTS = ("tfpa_pages_per_split", "tfpa_num_splits", "tfpa_write_kv", "tfpa_dec
            "tfpa_plan_destroy", "tfpa_plan_clear", "tfpa_plan_launches", "tfpa_plan_write_kv",
            "tfpa_plan_decode", "tfpa_plan_launch", "tfpa_plan_set_device", "tfpa_plan_dyn_bytes",
            "tfpa_plan_dyn_pack", "tfpa_plan_shape", "tfpa_plan_capture", "tfpa_plan_replay",
-           "tfpa_decode_append", "tfpa_plan_decode_append")
+           "tfpa_decode_append", "tfpa_plan_decode_append", "tfpa_row_splits")
 
 
 class TfpaError(RuntimeError):
@@ -100,6 +100,8 @@ def lib():
         L.tfpa_decode_partial.restype = ctypes.c_int
         L.tfpa_merge.argtypes = [P(tfpa_scratch), i32, i32, vp, vp, vp, vp]
         L.tfpa_merge.restype = ctypes.c_int
+        L.tfpa_row_splits.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, i32, vp]
+        L.tfpa_row_splits.restype = ctypes.c_int
         L.tfpa_decode.argtypes = [P(tfpa_cache), P(tfpa_seg), i32, vp, vp, vp, i32,
                                   ctypes.c_float, P(tfpa_scratch), vp, vp, vp]
         L.tfpa_decode.restype = ctypes.c_int
@@ -358,6 +360,17 @@ def tfpa_decode_partial(cache: Cache, segs: Sequence[Seg], q, row_seg, row_pos, 
     _check(lib().tfpa_decode_partial(ctypes.byref(cc), cs, n, _ptr(q), _ptr(rs), _ptr(rp),
                                      len(rs), float(softmax_scale), ctypes.byref(sc),
                                      _stream(stream)), "tfpa_decode_partial")
+
+
+def tfpa_row_splits(cache: Cache, segs: Sequence[Seg], row_seg, row_pos) -> np.ndarray:
+    """Each row's split count as tfpa_decode_partial leaves it (for tfpa_merge)."""
+    cs, n = _segs(segs)
+    rs, rp = _i32(row_seg), _i32(row_pos)
+    cc = cache.c()
+    ns = np.zeros(len(rs), np.int32)
+    _check(lib().tfpa_row_splits(ctypes.byref(cc), cs, n, _ptr(rs), _ptr(rp), len(rs), _ptr(ns)),
+           "tfpa_row_splits")
+    return ns
 
 
 def tfpa_merge(scratch: Scratch, hq: int, nsplit, out, lse=None, stream=None) -> None:

@@ -746,6 +746,26 @@ extern "C" int tfpa_decode(const tfpa_cache* cache, const tfpa_seg* segs, int32_
                      scratch, out, lse, Sink{stream, nullptr}, true);
 }
 
+extern "C" int tfpa_row_splits(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
+                               const int32_t* row_seg, const int32_t* row_pos, int32_t rows,
+                               int32_t* nsplit) {
+  int e;
+  if ((e = check_cache(cache)) || (e = check_segs(cache, segs, nseg))) return e;
+  if (rows > 0 && !nsplit) return TFPA_EINVAL;
+  thread_local std::vector<Run> runs;
+  if ((e = build_runs(segs, nseg, row_seg, row_pos, rows, runs))) return e;
+  // the same choice of kernel as decode_impl: runs of four or more m-tiles
+  // take the tensor-core verify path and its splits
+  const int G = cache->hq / cache->hkv;
+  for (const Run& r : runs) {
+    const int32_t L = segs[r.seg].seq_len;
+    const bool wide = G <= kVerifyVectors && (r.nrows * G + 15) / 16 >= 4;
+    const int32_t n = wide ? verify_num_splits(L) : tfpa_num_splits(L);
+    for (int32_t i = 0; i < r.nrows; ++i) nsplit[r.row0 + i] = n;
+  }
+  return TFPA_OK;
+}
+
 extern "C" int tfpa_decode_tree(const tfpa_cache* cache, const tfpa_seg* segs, int32_t nseg,
                                 const void* q, const int32_t* row_seg, const int32_t* row_pos,
                                 const uint64_t* row_anc, int32_t rows, float softmax_scale,

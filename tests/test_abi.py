@@ -528,3 +528,22 @@ def test_verify_splits_follow_the_stream_length(pages, splits):
     assert v[0]["items"] == 8 * splits
     pps = max(24, -(-pages // 7))
     assert splits == -(-pages // pps)
+    ns = B.tfpa_row_splits(c, segs, np.zeros(rows), np.arange(L - rows, L))
+    assert ns.tolist() == [splits] * rows
+
+
+def test_row_splits_give_each_row_its_kernels_split_count():
+    """tfpa_row_splits: a narrow run keeps tfpa_num_splits, a run of 49 or
+    more query vectors per kv head the verify path's count, whatever the
+    order of the rows in the call."""
+    c = _cache()
+    segs = [B.Seg(65536, page_table=3 * FAKE), B.Seg(8192, page_table=3 * FAKE)]
+    rs = np.array([1] + [0] * 13 + [1], np.int32)             # 13 rows: 52 vectors
+    rp = np.concatenate([[100], np.arange(65536 - 13, 65536), [8191]]).astype(np.int32)
+    ns = B.tfpa_row_splits(c, segs, rs, rp)
+    assert ns.tolist() == [B.tfpa_num_splits(8192)] + [7] * 13 + [B.tfpa_num_splits(8192)]
+    # twelve rows (48 vectors) stay on the decode kernel
+    ns = B.tfpa_row_splits(c, segs, np.zeros(12), np.arange(65536 - 12, 65536))
+    assert ns.tolist() == [B.tfpa_num_splits(65536)] * 12
+    with pytest.raises(B.TfpaError):
+        B.tfpa_row_splits(c, segs, [2], [0])

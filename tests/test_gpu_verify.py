@@ -6,12 +6,14 @@ Against the oracle: several key splits per stream next to a narrow run in the
 same call, and group sizes that leave a slot empty (three heads per kv head),
 need two pair groups (eight) or fall back to the decode kernel (one).
 Bitwise: a wide run batched with others equals it alone, paged equals slab,
-and slices of any size equal one launch."""
+slices of any size equal one launch, and the partials plus a separate merge
+(with tfpa_row_splits' counts) equal tfpa_decode."""
 
 import numpy as np
 import pytest
 import torch
 
+from paged_kv_cache_235_gb300 import binding as B
 from paged_kv_cache_235_gb300 import workloads as wl
 from tests.gpu_cases import GpuCase, bits, fp8_scales
 from tests.test_gpu_edges import _check, _make
@@ -80,3 +82,28 @@ def test_wide_paged_equals_slab_and_slices_bitwise(kv):
         c, lc = slab.decode(slab.q(), w.row_seg, w.row_pos, cap_rows=cap)
         assert np.array_equal(bits(b), bits(c)), f"slices of {cap}"
         assert torch.equal(lb, lc)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_partial_and_merge_with_row_splits_equal_decode(kv):
+    """tfpa_decode_partial then tfpa_merge, given each row's split count from
+    tfpa_row_splits, give tfpa_decode's bytes for a call whose wide run (20
+    rows, three verify splits) sits beside a narrow one (decode splits)."""
+    lengths = [15000, 5000]
+    rs = [0] * 20 + [1]
+    rp = list(range(14980, 15000)) + [4999]
+    w = _make(lengths, [True, False], rs, rp, kv=kv, seed=612)
+    g = GpuCase(w, fp8_scales(w) if kv == "fp8" else None)
+    q = g.q()
+    ref, ref_lse = g.decode(q, w.row_seg, w.row_pos)
+    ns = B.tfpa_row_splits(g.cache, g.segs, w.row_seg, w.row_pos)
+    assert ns.tolist() == [3] * 20 + [B.tfpa_num_splits(5000)]
+    sc = B.make_scratch(w.rows, w.hq, fused_merge=False)
+    out = torch.empty_like(ref)
+    lse = torch.empty_like(ref_lse)
+    B.tfpa_decode_partial(g.cache, g.segs, q, w.row_seg, w.row_pos, w.softmax_scale, sc)
+    B.tfpa_merge(sc, w.hq, ns, out, lse)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(out), bits(ref))
+    assert torch.equal(lse, ref_lse)
+    assert int(g.err.item()) == 0
