@@ -253,6 +253,13 @@ int build_runs(const tfpa_seg* segs, int32_t nseg, const int32_t* row_seg,
   return TFPA_OK;
 }
 
+// Runs of four or more m-tiles (16 query vectors each, so at least 49
+// vectors per kv head) are dense enough for the tensor cores: they take the
+// prefill kernel in verify mode, when a tile holds the group's heads.
+bool on_verify_path(const Run& r, int G) {
+  return G <= kVerifyVectors && (r.nrows * G + 15) / 16 >= 4;
+}
+
 int to_err(cudaError_t e) { return e == cudaSuccess ? TFPA_OK : TFPA_ECUDA; }
 
 }  // namespace
@@ -557,17 +564,16 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
   if ((e = check_device())) return e;
   const bool fp8 = c->dtype == TFPA_FP8_E4M3;
   const int G = c->hq / c->hkv;
-  if (G <= kVerifyVectors)
-    for (const Run& r : runs)
-      if ((r.nrows * G + 15) / 16 >= 4) {   // a run for the tensor-core verify path
-        if ((e = check_tma_source(q))) return e;
-        break;
-      }
+  for (const Run& r : runs)
+    if (on_verify_path(r, G)) {
+      if ((e = check_tma_source(q))) return e;
+      break;
+    }
   if (k_rows || v_rows) {
     if (!k_rows || !v_rows || !aligned(k_rows, 16) || !aligned(v_rows, 16)) return TFPA_EINVAL;
     bool fuse = true;
     for (size_t i = 0; fuse && i < runs.size(); ++i) {
-      fuse = G > kVerifyVectors || (runs[i].nrows * G + 15) / 16 < 4;   // decode partial path
+      fuse = !on_verify_path(runs[i], G);   // the decode partial path
       for (size_t j = 0; fuse && j < i; ++j) fuse = runs[j].seg != runs[i].seg;
     }
     if (!fuse) {
@@ -595,10 +601,8 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
   // call's whole run, so every slice of it computes its rows with the same
   // arithmetic (slices give the same bytes as one launch).  A group wider
   // than a tile (more than 128 query heads per kv head) stays on the decode
-  // kernel.
-  const bool verify_ok = G <= kVerifyVectors;
-  auto is_wide = [&](const Run& r) { return (r.nrows * G + 15) / 16 >= 4; };
-  const int vrows = verify_ok ? kVerifyVectors / G : 1;   // rows of a verify tile
+  // kernel (on_verify_path).
+  const int vrows = G <= kVerifyVectors ? kVerifyVectors / G : 1;   // rows of a verify tile
   while (ri < runs.size()) {
     SourceSet ss;
     const int32_t base = runs[ri].row0 + taken;  // first call row of this launch
@@ -610,7 +614,7 @@ int decode_impl(const tfpa_cache* c, const tfpa_seg* segs, int32_t nseg, const v
       if (src < 0) break;
       const int32_t take = std::min(r.nrows - taken, sc->cap_rows - nrows);
       const tfpa_seg& g = segs[r.seg];
-      if (verify_ok && is_wide(r)) {
+      if (on_verify_path(r, G)) {
         if (nv == 0) std::memset(&pv, 0, sizeof(pv));   // only launches that run are built
         RunInfo& info = pv.runs[nv++];
         fill_run(info, g, src, nrows, take, r.pos0 + taken);
@@ -762,8 +766,7 @@ extern "C" int tfpa_row_splits(const tfpa_cache* cache, const tfpa_seg* segs, in
   const int G = cache->hq / cache->hkv;
   for (const Run& r : runs) {
     const int32_t L = segs[r.seg].seq_len;
-    const bool wide = G <= kVerifyVectors && (r.nrows * G + 15) / 16 >= 4;
-    const int32_t n = wide ? verify_num_splits(L) : tfpa_num_splits(L);
+    const int32_t n = on_verify_path(r, G) ? verify_num_splits(L) : tfpa_num_splits(L);
     for (int32_t i = 0; i < r.nrows; ++i) nsplit[r.row0 + i] = n;
   }
   return TFPA_OK;
